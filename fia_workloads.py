@@ -1,0 +1,281 @@
+"""Seeded synthetic inputs for the fused inference attention path.
+
+This module only *makes inputs*: shapes, lengths, block tables and random
+values, rounded to their storage formats.  It holds none of the attention
+arithmetic, so both the oracle's tests and the CUDA path's tests, benchmark and
+smoke check can draw from it without sharing any of the method.
+
+Conventions taken from the operator pages:
+
+* Paged KV cache layout (blocknum, KV_N, blocksize, D); a block table of int32
+  rows, one per batch, wide enough for the longest sequence; the pool holds at
+  least sum_b ceil(L_b / blockSize) blocks (aclnnIncreFlashAttentionV3,
+  "Constraints / page attention"; the worked example in aclnnMlaPrologV3WeightNz,
+  BlockNum row: lengths [47, 104, 110, 161], blockSize 128 -> 5 blocks).
+* TND cumulative sequence lengths start at 0 and end at T, one entry per
+  sequence plus the leading 0 (aclnnRingAttentionUpdate, actualSeqQlenOptional);
+  zero-length sequences are allowed (aclnnFlashAttentionScoreV4, "约束说明":
+  lengths [2, 2, 0, 2, 2] give cumulative [2, 4, 4, 6, 8]).
+
+Value recipes (the pages name no dataset; these follow the workload table of
+the design notes): Q/K/V ~ N(0, 1) drawn in fp32 and rounded to nearest-even in
+the storage type; int8 K/V uniform integers in [-127, 127]; per-(kv-head,
+channel) fp32 antiquant scale ~ U(0.005, 0.02) and offset ~ U(-2, 2); per-head
+fp32 sink ~ N(0, 1).  Generators are numpy PCG64 with the seed given.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+# storage dtype names
+FP16, BF16, INT8 = "fp16", "bf16", "int8"
+
+
+# ---------------------------------------------------------------- storage formats
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bfloat16 bit patterns, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 -> binary16 bit patterns (numpy's round-to-nearest-even cast)."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def bits_to_f32(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Widen stored fp16/bf16 bit patterns to fp32 (exact)."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    if dtype == BF16:
+        return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    if dtype == FP16:
+        return bits.view(np.float16).astype(np.float32)
+    raise ValueError(dtype)
+
+
+def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    return to_bf16_bits(x) if dtype == BF16 else to_f16_bits(x)
+
+
+NAN_BITS = {BF16: np.uint16(0x7FC0), FP16: np.uint16(0x7E00)}
+
+
+# ---------------------------------------------------------------- index helpers
+def pool_blocks(lengths: Sequence[int], block_size: int) -> int:
+    """Blocks needed to hold every sequence: sum_b ceil(L_b / block_size)."""
+    return int(sum((int(L) + block_size - 1) // block_size for L in lengths))
+
+
+def cumulative(lengths: Sequence[int]) -> np.ndarray:
+    """B + 1 cumulative lengths starting at 0."""
+    return np.concatenate([[0], np.cumsum(np.asarray(lengths, dtype=np.int64))]).astype(np.int64)
+
+
+def lengths_from_cumulative_ends(ends: Sequence[int]) -> np.ndarray:
+    """Per-sequence lengths from cumulative end offsets (no leading 0)."""
+    e = np.asarray(ends, dtype=np.int64)
+    return np.diff(np.concatenate([[0], e]))
+
+
+def _normal(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:
+    n = int(np.prod(shape))
+    out = np.empty(n, np.float32)
+    for s in range(0, n, chunk):
+        out[s:s + chunk] = rng.standard_normal(min(chunk, n - s), dtype=np.float32)
+    return out.reshape(shape)
+
+
+def _normal_bits(rng: np.random.Generator, shape, dtype: str, chunk: int = 1 << 24) -> np.ndarray:
+    n = int(np.prod(shape))
+    out = np.empty(n, np.uint16)
+    for s in range(0, n, chunk):
+        out[s:s + chunk] = to_bits(rng.standard_normal(min(chunk, n - s), dtype=np.float32), dtype)
+    return out.reshape(shape)
+
+
+# ---------------------------------------------------------------- decode cases
+@dataclasses.dataclass
+class DecodeCase:
+    B: int
+    Nq: int
+    Nkv: int
+    D: int
+    block_size: int
+    dtype: str                 # query / output storage type (fp16 | bf16)
+    kv_dtype: str              # fp16 | bf16 | int8
+    scale: float
+    lengths: np.ndarray        # int64 (B,)
+    block_table: np.ndarray    # int32 (B, width); -1 past each sequence's blocks
+    num_blocks: int
+    q: np.ndarray              # uint16 bits (B, Nq, D)
+    k_cache: np.ndarray        # (num_blocks, Nkv, block_size, D) uint16 bits or int8
+    v_cache: np.ndarray
+    aq_scale: Optional[np.ndarray] = None   # float32 (2, Nkv, D)
+    aq_offset: Optional[np.ndarray] = None  # float32 (2, Nkv, D)
+    sink: Optional[np.ndarray] = None       # float32 (Nq,)
+    seed: int = 0
+
+    @property
+    def max_len(self) -> int:
+        return int(self.lengths.max()) if self.B else 0
+
+    @property
+    def kv_elem_bytes(self) -> int:
+        return 1 if self.kv_dtype == INT8 else 2
+
+    def kv_bytes(self) -> int:
+        """Visible K and V bytes: sum_b L_b * 2 * Nkv * D * element size."""
+        return int(self.lengths.sum()) * 2 * self.Nkv * self.D * self.kv_elem_bytes
+
+
+def make_decode_case(*, B: int, Nq: int, Nkv: int, D: int, block_size: int, dtype: str = BF16,
+                     kv_dtype: Optional[str] = None, lengths=None, len_range=None,
+                     scale: Optional[float] = None, sink: bool = False, seed: int = 0,
+                     spare_blocks: int = 0, table_pad: int = 0, poison: bool = False,
+                     shuffle: bool = True) -> DecodeCase:
+    """Build one seeded paged-decode input.
+
+    lengths: explicit per-batch KV lengths, or len_range=(lo, hi) for U[lo, hi].
+    spare_blocks: extra pool blocks no sequence uses.  table_pad: extra table
+    columns (filled with -1).  poison: fill every cache slot that no sequence
+    uses with NaN (int8 caches cannot hold NaN and get -128 there), to show
+    that unused slots are never read.
+    """
+    rng = np.random.default_rng(seed)
+    kv_dtype = kv_dtype or dtype
+    if lengths is None:
+        lo, hi = len_range
+        lengths = rng.integers(lo, hi, size=B, endpoint=True)
+    lengths = np.asarray(lengths, dtype=np.int64)
+    assert lengths.shape == (B,)
+    need = pool_blocks(lengths, block_size)
+    num_blocks = need + spare_blocks
+    nblk = [(int(L) + block_size - 1) // block_size for L in lengths]
+    width = max(max(nblk) if B else 0, 1) + table_pad
+    perm = rng.permutation(num_blocks) if shuffle else np.arange(num_blocks)
+    table = np.full((B, width), -1, np.int32)
+    nxt = 0
+    for b in range(B):
+        table[b, :nblk[b]] = perm[nxt:nxt + nblk[b]]
+        nxt += nblk[b]
+    q = _normal_bits(rng, (B, Nq, D), dtype)
+    shape = (num_blocks, Nkv, block_size, D)
+    aq_scale = aq_offset = None
+    if kv_dtype == INT8:
+        k_cache = rng.integers(-127, 127, size=shape, endpoint=True, dtype=np.int8)
+        v_cache = rng.integers(-127, 127, size=shape, endpoint=True, dtype=np.int8)
+        aq_scale = rng.uniform(0.005, 0.02, size=(2, Nkv, D)).astype(np.float32)
+        aq_offset = rng.uniform(-2.0, 2.0, size=(2, Nkv, D)).astype(np.float32)
+    else:
+        k_cache = _normal_bits(rng, shape, kv_dtype)
+        v_cache = _normal_bits(rng, shape, kv_dtype)
+    sink_v = rng.standard_normal(Nq, dtype=np.float32) if sink else None
+    if poison:
+        used = np.zeros((num_blocks, block_size), bool)
+        for b in range(B):
+            for t in range(int(lengths[b])):
+                used[table[b, t // block_size], t % block_size] = True
+        bad = np.int8(-128) if kv_dtype == INT8 else NAN_BITS[kv_dtype]
+        mask = ~used[:, None, :, None]
+        k_cache = np.where(mask, bad, k_cache)
+        v_cache = np.where(mask, bad, v_cache)
+    return DecodeCase(B=B, Nq=Nq, Nkv=Nkv, D=D, block_size=block_size, dtype=dtype, kv_dtype=kv_dtype,
+                      scale=scale if scale is not None else 1.0 / math.sqrt(D), lengths=lengths,
+                      block_table=table, num_blocks=num_blocks, q=q, k_cache=k_cache, v_cache=v_cache,
+                      aq_scale=aq_scale, aq_offset=aq_offset, sink=sink_v, seed=seed)
+
+
+# ---------------------------------------------------------------- prefill cases
+@dataclasses.dataclass
+class PrefillCase:
+    B: int
+    Nq: int
+    Nkv: int
+    D: int
+    dtype: str
+    scale: float
+    lengths_q: np.ndarray
+    lengths_kv: np.ndarray
+    cu_q: np.ndarray           # int64 (B + 1,)
+    cu_kv: np.ndarray
+    q: np.ndarray              # uint16 bits (T, Nq, D)
+    k: np.ndarray              # uint16 bits (Tkv, Nkv, D)
+    v: np.ndarray
+    sink: Optional[np.ndarray] = None
+    seed: int = 0
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_q[-1])
+
+    @property
+    def Tkv(self) -> int:
+        return int(self.cu_kv[-1])
+
+
+def make_prefill_case(*, Nq: int, Nkv: int, D: int, dtype: str = BF16, lengths=None, B: int = 0,
+                      len_range=None, lengths_kv=None, scale: Optional[float] = None,
+                      sink: bool = False, seed: int = 0) -> PrefillCase:
+    rng = np.random.default_rng(seed)
+    if lengths is None:
+        lo, hi = len_range
+        lengths = rng.integers(lo, hi, size=B, endpoint=True)
+    lengths = np.asarray(lengths, dtype=np.int64)
+    lengths_kv = lengths.copy() if lengths_kv is None else np.asarray(lengths_kv, dtype=np.int64)
+    B = int(lengths.shape[0])
+    cu_q, cu_kv = cumulative(lengths), cumulative(lengths_kv)
+    q = _normal_bits(rng, (int(cu_q[-1]), Nq, D), dtype)
+    k = _normal_bits(rng, (int(cu_kv[-1]), Nkv, D), dtype)
+    v = _normal_bits(rng, (int(cu_kv[-1]), Nkv, D), dtype)
+    sink_v = rng.standard_normal(Nq, dtype=np.float32) if sink else None
+    return PrefillCase(B=B, Nq=Nq, Nkv=Nkv, D=D, dtype=dtype,
+                       scale=scale if scale is not None else 1.0 / math.sqrt(D),
+                       lengths_q=lengths, lengths_kv=lengths_kv, cu_q=cu_q, cu_kv=cu_kv,
+                       q=q, k=k, v=v, sink=sink_v, seed=seed)
+
+
+# ---------------------------------------------------------------- the five workloads
+def tiny_decode(seed: int = 1000) -> DecodeCase:
+    """B 2, Nq 4, Nkv 2, D 64, fp16, lengths [37, 100], blockSize 16, shuffled pool."""
+    return make_decode_case(B=2, Nq=4, Nkv=2, D=64, block_size=16, dtype=FP16, lengths=[37, 100],
+                            scale=1.0 / 8.0, seed=seed)
+
+
+def bf16_gqa_decode(seed: int = 1001) -> DecodeCase:
+    """B 32, Nq 32, Nkv 8, D 128, bf16, lengths U[1, 4096], blockSize 128."""
+    return make_decode_case(B=32, Nq=32, Nkv=8, D=128, block_size=128, dtype=BF16,
+                            len_range=(1, 4096), seed=seed)
+
+
+def int8_antiquant_decode(seed: int = 1002) -> DecodeCase:
+    """B 64, Nq 64, Nkv 8, D 128, bf16 query, int8 K/V with per-channel antiquant,
+    lengths U[512, 8192], blockSize 128."""
+    return make_decode_case(B=64, Nq=64, Nkv=8, D=128, block_size=128, dtype=BF16, kv_dtype=INT8,
+                            len_range=(512, 8192), seed=seed)
+
+
+def long_ctx_sink_decode(seed: int = 1003) -> DecodeCase:
+    """B 4, Nq 64, Nkv 8, D 64, bf16, length 131072 each, blockSize 128, per-head sink;
+    the KV is split into 32 chunks whose partials are merged."""
+    return make_decode_case(B=4, Nq=64, Nkv=8, D=64, block_size=128, dtype=BF16,
+                            lengths=[131072] * 4, sink=True, seed=seed)
+
+
+def causal_prefill_tnd(seed: int = 1004) -> PrefillCase:
+    """8 sequences, lengths U[1, 2048], Nq 32, Nkv 8, D 128, bf16, causal, TND."""
+    return make_prefill_case(Nq=32, Nkv=8, D=128, dtype=BF16, B=8, len_range=(1, 2048), seed=seed)
+
+
+WORKLOADS = {
+    "tiny_decode": tiny_decode,
+    "bf16_gqa_decode": bf16_gqa_decode,
+    "int8_antiquant_decode": int8_antiquant_decode,
+    "long_ctx_sink_decode": long_ctx_sink_decode,
+    "causal_prefill_tnd": causal_prefill_tnd,
+}
+LONG_CTX_CHUNKS = 32

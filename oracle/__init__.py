@@ -1,0 +1,196 @@
+"""The oracle: a plain fp64 CPU statement of the fused inference attention path.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this package; the product library never uses it.
+The arithmetic lives in ``fia_oracle.c`` (plain C, fp64, built with
+``-ffp-contract=off``); this module compiles it with gcc and marshals numpy
+arrays into it.  It shares no code with the CUDA path.
+
+Functions and the passages they follow:
+
+* ``decode``   -- aclnnIncreFlashAttentionV3, "Function" (softmax attention with
+  scaleValue) and "Constraints / page attention" (block table addressing);
+  aclnnFlashAttentionScoreV4 "计算公式" (learnable sink).
+* ``prefill``  -- FusedInferAttentionScore 全解析 (prefill mode, rightDownCausal);
+  aclnnFlashAttentionScoreV4 "约束说明" (TND, cumulative sequence lengths).
+* ``rau``      -- aclnnRingAttentionUpdate "计算公式", read with each partial
+  weighted by its own softmax sum (the printed formula drops those factors).
+* ``dequant_i8`` -- per-channel antiquant (x - offset) * scale in fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "fia_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+# this interface's dtype codes (match the enum in fia_oracle.c)
+F32, F16, BF16, I8, F64 = 0, 1, 2, 3, 4
+
+GCC_FLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-shared", "-fPIC"]
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile one oracle C source into a shared library (gcc, OpenMP, no FMA contraction)."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *GCC_FLAGS, "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile fia_oracle.c into liboracle.so next to it, if missing or stale."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(SOURCE):
+        return _LIB_PATH
+    return compile_source(SOURCE, _LIB_PATH)
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    lib.oracle_decode.argtypes = [P, i32, P, P, i32, P, i64, P, i32, i32, i32, i32, i32, i64,
+                                  dbl, P, P, P, P, i64, i32, P, P, P]
+    lib.oracle_decode.restype = i32
+    lib.oracle_prefill.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, dbl, i32, P,
+                                   P, i64, i32, P, P, P]
+    lib.oracle_prefill.restype = i32
+    lib.oracle_rau.argtypes = [P, P, P, P, P, P, i64, i32, i32, P, P, P]
+    lib.oracle_rau.restype = i32
+    lib.oracle_dequant_i8.argtypes = [ctypes.c_int8, ctypes.c_float, ctypes.c_float]
+    lib.oracle_dequant_i8.restype = ctypes.c_float
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = i32
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _dtype_code(a: np.ndarray, declared: int | None) -> int:
+    if declared is not None:
+        return declared
+    return {np.dtype(np.float32): F32, np.dtype(np.float64): F64, np.dtype(np.int8): I8}[a.dtype]
+
+
+class Oracle:
+    """numpy front end over one compiled copy of the oracle's C source."""
+
+    def __init__(self, path: str):
+        self.path = path
+        self._lib = _bind(path)
+
+    def max_threads(self) -> int:
+        return self._lib.oracle_max_threads()
+
+    def dequant_i8(self, x: int, offset: float, scale: float) -> float:
+        """One fp32 antiquant step, exactly as the oracle's decode uses it."""
+        return self._lib.oracle_dequant_i8(int(x), float(offset), float(scale))
+
+    def decode(self, q, k_cache, v_cache, seq_lens, *, Nq, Nkv, D, scale, q_dtype=None, kv_dtype=None,
+               block_table=None, block_size=0, kv_rows=0, aq_scale=None, aq_offset=None, sink=None,
+               rows=None, nthreads=0):
+        """Decode attention (query S = 1).
+
+        q: (B, Nq, D) array (uint16 bits with q_dtype=F16/BF16, or float32/float64).
+        k_cache, v_cache: paged (num_blocks, Nkv, block_size, D) when block_table is
+        given, else contiguous (B, Nkv, kv_rows, D).  int8 caches need aq_scale
+        (2, Nkv, D) float32 and optionally aq_offset.  Returns (out, max, sum) as
+        float64 arrays of shape (R, D), (R,), (R,) where R = len(rows) or B * Nq.
+        """
+        q = np.ascontiguousarray(q)
+        k_cache = np.ascontiguousarray(k_cache)
+        v_cache = np.ascontiguousarray(v_cache)
+        seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int64)
+        B = int(seq_lens.shape[0])
+        bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
+        bt_stride = 0 if bt is None else int(bt.shape[1])
+        rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        R = B * Nq if rows_a is None else int(rows_a.shape[0])
+        f32 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+        aq_scale, aq_offset, sink = f32(aq_scale), f32(aq_offset), f32(sink)
+        out = np.zeros((R, D), np.float64)
+        mx = np.zeros(R, np.float64)
+        sm = np.zeros(R, np.float64)
+        rc = self._lib.oracle_decode(
+            _ptr(q), _dtype_code(q, q_dtype), _ptr(k_cache), _ptr(v_cache),
+            _dtype_code(k_cache, kv_dtype), _ptr(bt), bt_stride, _ptr(seq_lens),
+            B, Nq, Nkv, D, block_size, kv_rows, float(scale), _ptr(aq_scale),
+            _ptr(aq_offset), _ptr(sink), _ptr(rows_a), 0 if rows_a is None else R,
+            nthreads, _ptr(out), _ptr(mx), _ptr(sm))
+        if rc != 0:
+            raise ValueError("oracle_decode rejected its arguments")
+        return out, mx, sm
+
+    def prefill(self, q, k, v, cu_q, cu_kv, *, Nq, Nkv, D, scale, causal=True, dtype=None, sink=None,
+                rows=None, nthreads=0):
+        """Prefill attention in TND layout.  q: (T, Nq, D); k, v: (Tkv, Nkv, D);
+        cu_q / cu_kv: B + 1 cumulative lengths from 0.  Returns (out, max, sum) in
+        float64 for the rows (t * Nq + h) asked for, or for all T * Nq rows."""
+        q, k, v = (np.ascontiguousarray(a) for a in (q, k, v))
+        cu_q = np.ascontiguousarray(cu_q, dtype=np.int64)
+        cu_kv = np.ascontiguousarray(cu_kv, dtype=np.int64)
+        B = int(cu_q.shape[0]) - 1
+        T = int(cu_q[-1])
+        rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        R = T * Nq if rows_a is None else int(rows_a.shape[0])
+        sink = None if sink is None else np.ascontiguousarray(sink, dtype=np.float32)
+        out = np.zeros((R, D), np.float64)
+        mx = np.zeros(R, np.float64)
+        sm = np.zeros(R, np.float64)
+        rc = self._lib.oracle_prefill(
+            _ptr(q), _ptr(k), _ptr(v), _dtype_code(q, dtype), _ptr(cu_q), _ptr(cu_kv),
+            B, Nq, Nkv, D, float(scale), int(bool(causal)), _ptr(sink), _ptr(rows_a),
+            0 if rows_a is None else R, nthreads, _ptr(out), _ptr(mx), _ptr(sm))
+        if rc != 0:
+            raise ValueError("oracle_prefill rejected its arguments")
+        return out, mx, sm
+
+    def rau(self, prev_out, prev_max, prev_sum, cur_out, cur_max, cur_sum):
+        """RingAttentionUpdate on fp64 arrays: out (rows, N, D), max/sum (rows, N)."""
+        a = [np.ascontiguousarray(x, dtype=np.float64) for x in
+             (prev_out, prev_max, prev_sum, cur_out, cur_max, cur_sum)]
+        rows, N, D = a[0].shape
+        out = np.zeros((rows, N, D), np.float64)
+        mx = np.zeros((rows, N), np.float64)
+        sm = np.zeros((rows, N), np.float64)
+        self._lib.oracle_rau(*[_ptr(x) for x in a], rows, N, D, _ptr(out), _ptr(mx), _ptr(sm))
+        return out, mx, sm
+
+
+def default() -> Oracle:
+    """The oracle built from fia_oracle.c (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def max_threads() -> int:
+    return default().max_threads()
+
+
+def dequant_i8(x, offset, scale):
+    return default().dequant_i8(x, offset, scale)
+
+
+def decode(*args, **kw):
+    return default().decode(*args, **kw)
+
+
+def prefill(*args, **kw):
+    return default().prefill(*args, **kw)
+
+
+def rau(*args, **kw):
+    return default().rau(*args, **kw)
