@@ -1,0 +1,13 @@
+"""attention_ifa_fia_gb300: fused inference attention for one GB300 (sm_103a).
+
+The compute lives in libfia_gb300.so (hand-written CUDA; C interface in
+include/fia.h).  This package is its Python binding: the functions below carry
+the C entry points' names and only marshal torch tensors into them.
+"""
+from ._binding import (BF16, F16, F32, I8, FiaError, fia_debug_dequant, fia_debug_gather, fia_decode,
+                       fia_decode_workspace_size, fia_device_status, fia_prefill, fia_prefill_workspace_size,
+                       header_functions, library, ring_attention_update)
+
+__all__ = ["FiaError", "fia_decode", "fia_decode_workspace_size", "fia_prefill", "fia_prefill_workspace_size",
+           "ring_attention_update", "fia_device_status", "fia_debug_dequant", "fia_debug_gather",
+           "header_functions", "library", "F32", "F16", "BF16", "I8"]

@@ -1,0 +1,211 @@
+"""ctypes binding of libfia_gb300.so: argument marshalling only.
+
+Each function here has the name of the C entry point it calls and passes torch
+tensors' device addresses, shapes and the current CUDA stream through to it.
+All computation happens in the library's CUDA kernels; if the library has not
+been built, importing this module raises an error instead of falling back to
+anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfia_gb300.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "fia.h")
+
+F32, F16, BF16, I8 = 0, 1, 2, 3
+SUCCESS, ERR_PARAM_NULLPTR, ERR_PARAM_INVALID, ERR_RUNTIME, ERR_INNER_TILING = 0, 161001, 161002, 361001, 561002
+STATUS_WAIT_TIMEOUT, STATUS_BAD_BLOCK_INDEX, STATUS_LENGTH_CLAMPED, STATUS_BAD_SEQLENS = 1, 2, 4, 8
+
+_TORCH_TO_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16, torch.int8: I8}
+
+
+class FiaError(RuntimeError):
+    """A non-zero status from the library, with the library's own message."""
+
+    def __init__(self, code: int, func: str, message: str):
+        super().__init__(f"{func} returned {code}: {message}")
+        self.code = code
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with attention_ifa_fia_gb300.build.build() "
+                          "(nvcc for sm_103a); there is no other implementation to fall back to")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, u32, dbl, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint,
+                                 ctypes.c_double, ctypes.c_size_t)
+    sig = {
+        "fia_last_error": ([], ctypes.c_char_p),
+        "fia_device_status": ([P, ctypes.POINTER(u32)], i32),
+        "fia_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
+        "fia_decode": ([P, i32, P, P, i32, P, i64, P, i32, i32, i32, i32, i32, i32, i64, dbl, P, P, P, P, P, P,
+                        i32, P, sz, P], i32),
+        "fia_prefill_workspace_size": ([i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
+        "fia_prefill": ([P, P, P, i32, P, P, i32, i64, i64, i32, i32, i32, i32, i32, dbl, i32, P, P, P, P, P, sz,
+                         P], i32),
+        "ring_attention_update": ([P, P, P, P, P, P, i32, i64, i32, i32, P, P, P, P], i32),
+        "fia_debug_dequant": ([P, P, P, i64, P, P], i32),
+        "fia_debug_gather": ([P, i32, P, i64, P, i32, i32, i32, i32, i32, i64, i32, i32, P, P], i32),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def header_functions() -> list:
+    """Names of the functions include/fia.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(\w+)\s*\(", text, flags=re.M)))
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(rc: int, func: str):
+    if rc != SUCCESS:
+        raise FiaError(rc, func, _lib.fia_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    return _TORCH_TO_CODE[t.dtype]
+
+
+def fia_device_status(stream=None) -> int:
+    flags = ctypes.c_uint(0)
+    _check(_lib.fia_device_status(_stream(stream), ctypes.byref(flags)), "fia_device_status")
+    return flags.value
+
+
+# ----------------------------------------------------------------------------- decode
+def fia_decode_workspace_size(B: int, Nq: int, Nkv: int, D: int, max_kv_len: int, block_size: int,
+                              num_splits: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.fia_decode_workspace_size(B, Nq, Nkv, D, max_kv_len, block_size, num_splits, ctypes.byref(n)),
+           "fia_decode_workspace_size")
+    return n.value
+
+
+def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+               actual_seq_lengths: torch.Tensor, *, max_kv_len: int, num_heads: int, num_kv_heads: int = 0,
+               scale: Optional[float] = None, antiquant_scale=None, antiquant_offset=None, sink=None,
+               out: Optional[torch.Tensor] = None, softmax_max: Optional[torch.Tensor] = None,
+               softmax_sum: Optional[torch.Tensor] = None, num_splits: int = 0,
+               workspace: Optional[torch.Tensor] = None, stream=None
+               ) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
+    """Paged decode attention.  q: (B, Nq, D) (any layout of that memory); k/v_cache:
+    (num_blocks, Nkv, block_size, D); block_table int32 (B, width); actual_seq_lengths
+    int64 (B,) on the device.  Returns (out, softmax_max, softmax_sum)."""
+    B, D = int(q.shape[0]), int(q.shape[-1])
+    num_blocks, block_size = int(k_cache.shape[0]), int(k_cache.shape[2])
+    nkv = num_kv_heads if num_kv_heads else num_heads
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, num_heads, D), dtype=q.dtype, device=q.device)
+    if workspace is None:
+        nbytes = fia_decode_workspace_size(B, num_heads, nkv, D, max_kv_len, block_size, num_splits)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    rc = _lib.fia_decode(_ptr(q), dtype_code(q), _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache),
+                         _ptr(block_table), int(block_table.shape[1]), _ptr(actual_seq_lengths), int(max_kv_len),
+                         B, num_heads, nkv, D, block_size, num_blocks, float(scale), _ptr(antiquant_scale),
+                         _ptr(antiquant_offset), _ptr(sink), _ptr(out), _ptr(softmax_max), _ptr(softmax_sum),
+                         int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                         _stream(stream))
+    _check(rc, "fia_decode")
+    return out, softmax_max, softmax_sum
+
+
+# ----------------------------------------------------------------------------- prefill
+def fia_prefill_workspace_size(B: int, Nq: int, Nkv: int, D: int, max_seqlen_q: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.fia_prefill_workspace_size(B, Nq, Nkv, D, max_seqlen_q, ctypes.byref(n)),
+           "fia_prefill_workspace_size")
+    return n.value
+
+
+def fia_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                cu_seqlens_kv: torch.Tensor, *, max_seqlen_q: int, max_seqlen_kv: int, num_heads: int,
+                num_kv_heads: int = 0, scale: Optional[float] = None, mask: int = 3, sink=None,
+                out: Optional[torch.Tensor] = None, softmax_max=None, softmax_sum=None,
+                workspace: Optional[torch.Tensor] = None, stream=None):
+    """Prefill attention, TND.  q: (T, Nq, D); k, v: (Tkv, Nkv, D); cu_seqlens int64 (B + 1,)
+    on the device.  mask 3 = rightDownCausal, 0 = none.  Returns (out, softmax_max, softmax_sum)."""
+    T, D = int(q.shape[0]), int(q.shape[-1])
+    Tkv = int(k.shape[0])
+    B = int(cu_seqlens_q.shape[0]) - 1
+    nkv = num_kv_heads if num_kv_heads else num_heads
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((T, num_heads, D), dtype=q.dtype, device=q.device)
+    if workspace is None:
+        nbytes = fia_prefill_workspace_size(B, num_heads, nkv, D, max_seqlen_q)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    rc = _lib.fia_prefill(_ptr(q), _ptr(k), _ptr(v), dtype_code(q), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B,
+                          T, Tkv, int(max_seqlen_q), int(max_seqlen_kv), num_heads, nkv, D, float(scale), int(mask),
+                          _ptr(sink), _ptr(out), _ptr(softmax_max), _ptr(softmax_sum), _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "fia_prefill")
+    return out, softmax_max, softmax_sum
+
+
+# ----------------------------------------------------------------------------- RAU
+def ring_attention_update(prev_out, prev_max, prev_sum, cur_out, cur_max, cur_sum, *, out=None, max_out=None,
+                          sum_out=None, stream=None):
+    """Merge two partials.  *_out: (rows, N, D) f32/f16/bf16; *_max/*_sum: (rows, N) fp32.
+    Outputs default to new tensors; passing the prev_* tensors merges in place."""
+    rows, N, D = (int(x) for x in prev_out.shape)
+    out = torch.empty_like(prev_out) if out is None else out
+    max_out = torch.empty_like(prev_max) if max_out is None else max_out
+    sum_out = torch.empty_like(prev_sum) if sum_out is None else sum_out
+    rc = _lib.ring_attention_update(_ptr(prev_out), _ptr(prev_max), _ptr(prev_sum), _ptr(cur_out), _ptr(cur_max),
+                                    _ptr(cur_sum), dtype_code(prev_out), rows, N, D, _ptr(out), _ptr(max_out),
+                                    _ptr(sum_out), _stream(stream))
+    _check(rc, "ring_attention_update")
+    return out, max_out, sum_out
+
+
+# ----------------------------------------------------------------------------- probes
+def fia_debug_dequant(codes: torch.Tensor, scale: torch.Tensor, offset: torch.Tensor, stream=None) -> torch.Tensor:
+    out = torch.empty(codes.shape, dtype=torch.float32, device=codes.device)
+    _check(_lib.fia_debug_dequant(_ptr(codes), _ptr(scale), _ptr(offset), codes.numel(), _ptr(out),
+                                  _stream(stream)), "fia_debug_dequant")
+    return out
+
+
+def fia_debug_gather(k_cache: torch.Tensor, block_table: torch.Tensor, actual_seq_lengths: torch.Tensor, *,
+                     max_kv_len: int, b: int, hkv: int, length: int, stream=None) -> torch.Tensor:
+    num_blocks, nkv, block_size, D = (int(x) for x in k_cache.shape)
+    B = int(block_table.shape[0])
+    dst = torch.zeros((length, D), dtype=k_cache.dtype, device=k_cache.device)
+    _check(_lib.fia_debug_gather(_ptr(k_cache), dtype_code(k_cache), _ptr(block_table), int(block_table.shape[1]),
+                                 _ptr(actual_seq_lengths), int(max_kv_len), B, nkv, D, block_size, num_blocks, b,
+                                 hkv, _ptr(dst), _stream(stream)), "fia_debug_gather")
+    return dst

@@ -1,0 +1,359 @@
+// api.cu -- the extern "C" entry points declared in include/fia.h.
+//
+// Host side only: argument validation (before any launch), the split planner,
+// TMA tensor-map encoding, the device status word, and dispatch to the kernels.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "fia.h"
+#include "fia_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_err[0] = '\0';
+  return FIA_SUCCESS;
+}
+
+// One status word per device.  Kernels OR bits into it (see fia_device_status).
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool init = false;
+  int num_sms = 0;
+  unsigned int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Per-device set-up with that device current: SM count and the status word's address.
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(FIA_ERR_RUNTIME, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
+    if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    d.init = true;
+  }
+  *out = &d;
+  return FIA_SUCCESS;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D tensor map over a row-major matrix of `rows` rows of `cols` elements;
+// box = box_cols x box_rows; swizzle span = box_cols * element bytes (128 or 64).
+int make_tmap(CUtensorMap* m, const void* base, int dtype, uint64_t cols, uint64_t rows, uint32_t box_cols,
+              uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FIA_ERR_RUNTIME, "cuTensorMapEncodeTiled is not available from the driver");
+  const uint32_t elem = dtype == fia::kI8 ? 1 : 2;
+  CUtensorMapDataType t = dtype == fia::kI8    ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                          : dtype == fia::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint32_t span = box_cols * elem;
+  CUtensorMapSwizzle sw = span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                          : span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                       : CU_TENSOR_MAP_SWIZZLE_32B;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * elem};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, t, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FIA_ERR_RUNTIME, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return FIA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
+
+// ---------------------------------------------------------------- decode planner
+struct DecodePlan {
+  int chunk_tokens = 0;
+  int max_items = 0;
+};
+
+// Work items are (b, kv head, chunk) triples of `chunk_tokens` tokens.  With
+// num_splits = n > 0 each sequence splits into at most n chunks; with 0 the
+// chunk is sized so that the upper bound of the work (every sequence at
+// max_kv_len) gives about 12 items per SM, between one tile and 8192 tokens.
+int plan_decode(int B, int Nkv, int max_kv_len, int num_splits, int num_sms, DecodePlan* plan) {
+  const int64_t T = fia::kDecodeTile;
+  int64_t c;
+  if (num_splits > 0) {
+    c = ((int64_t)max_kv_len + num_splits - 1) / num_splits;
+  } else {
+    const int64_t upper = (int64_t)B * Nkv * max_kv_len;
+    c = upper / (12LL * std::max(num_sms, 1));
+    c = std::min<int64_t>(std::max<int64_t>(c, T), 8192);
+  }
+  c = (c + T - 1) / T * T;
+  if (c < T) c = T;
+  const int64_t chunks = max_kv_len > 0 ? ((int64_t)max_kv_len + c - 1) / c : 1;
+  const int64_t items = (int64_t)B * Nkv * chunks;
+  if (items > (1LL << 30) || c > (1LL << 30))
+    return fail(FIA_ERR_INNER_TILING, "split plan too large (%lld items)", (long long)items);
+  const int64_t max_chunks_merge = 48 * 1024 / 4 / 8;  // merge weights held in shared memory
+  if (chunks > max_chunks_merge)
+    return fail(FIA_ERR_INNER_TILING, "%lld chunks per sequence exceed the merge limit %lld", (long long)chunks,
+                (long long)max_chunks_merge);
+  plan->chunk_tokens = (int)c;
+  plan->max_items = (int)std::max<int64_t>(items, 1);
+  return FIA_SUCCESS;
+}
+
+int check_decode_shape(int B, int Nq, int* Nkv, int D, int max_kv_len, int block_size, int num_splits) {
+  if (B < 0 || B > 65536) return fail(FIA_ERR_PARAM_INVALID, "B = %d outside [0, 65536]", B);
+  if (Nq < 1 || Nq > 256) return fail(FIA_ERR_PARAM_INVALID, "Nq = %d outside [1, 256]", Nq);
+  if (*Nkv == 0) *Nkv = Nq;
+  if (*Nkv < 0 || Nq % *Nkv != 0)
+    return fail(FIA_ERR_PARAM_INVALID, "Nq = %d is not a multiple of Nkv = %d", Nq, *Nkv);
+  if (Nq / *Nkv > 8) return fail(FIA_ERR_PARAM_INVALID, "GQA group %d > 8 is not supported in this build", Nq / *Nkv);
+  if (D != 64 && D != 128) return fail(FIA_ERR_PARAM_INVALID, "D = %d not supported (64 or 128)", D);
+  if (block_size <= 0 || block_size > 512 || block_size % 16 != 0)
+    return fail(FIA_ERR_PARAM_INVALID, "block_size = %d must be a multiple of 16 in (0, 512]", block_size);
+  if (max_kv_len < 0) return fail(FIA_ERR_PARAM_INVALID, "max_kv_len = %d < 0", max_kv_len);
+  if (num_splits < 0) return fail(FIA_ERR_PARAM_INVALID, "num_splits = %d < 0", num_splits);
+  return FIA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fia_last_error(void) { return g_err; }
+
+int fia_device_status(fia_stream_t stream, unsigned int* flags) {
+  if (!flags) return fail(FIA_ERR_PARAM_NULLPTR, "flags is NULL");
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  unsigned int v = 0;
+  e = cudaMemcpy(&v, d->status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(d->status, 0, sizeof v);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "reading the status word: %s", cudaGetErrorString(e));
+  *flags = v;
+  return ok();
+}
+
+int fia_decode_workspace_size(int B, int Nq, int Nkv, int D, int max_kv_len, int block_size, int num_splits,
+                              size_t* bytes) {
+  if (!bytes) return fail(FIA_ERR_PARAM_NULLPTR, "bytes is NULL");
+  if (int rc = check_decode_shape(B, Nq, &Nkv, D, max_kv_len, block_size, num_splits)) return rc;
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  DecodePlan plan;
+  if (int rc = plan_decode(B, Nkv, max_kv_len, num_splits, d->num_sms, &plan)) return rc;
+  *bytes = fia::decode_workspace_bytes(B, Nkv, Nq / Nkv, D, plan.max_items);
+  return ok();
+}
+
+int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache, fia_dtype kv_dtype,
+               const int32_t* block_table, int64_t bt_stride, const int64_t* actual_seq_lengths, int max_kv_len,
+               int B, int Nq, int Nkv, int D, int block_size, int64_t num_blocks, double scale,
+               const float* antiquant_scale, const float* antiquant_offset, const float* sink, void* out,
+               float* softmax_max, float* softmax_sum, int num_splits, void* workspace, size_t workspace_bytes,
+               fia_stream_t stream) {
+  // -- 161001: required pointers
+  if (!q || !k_cache || !v_cache || !block_table || !actual_seq_lengths || !out)
+    return fail(FIA_ERR_PARAM_NULLPTR, "q, k_cache, v_cache, block_table, actual_seq_lengths and out are required");
+  if (kv_dtype == FIA_I8 && !antiquant_scale)
+    return fail(FIA_ERR_PARAM_NULLPTR, "int8 KV needs antiquant_scale");
+  if (!workspace) return fail(FIA_ERR_PARAM_NULLPTR, "workspace is NULL");
+  // -- 161002: dtypes, shapes, attributes
+  if (q_dtype != FIA_F16 && q_dtype != FIA_BF16)
+    return fail(FIA_ERR_PARAM_INVALID, "query dtype must be fp16 or bf16");
+  if (kv_dtype != q_dtype && kv_dtype != FIA_I8)
+    return fail(FIA_ERR_PARAM_INVALID, "key/value dtype must equal the query dtype or be int8");
+  if (int rc = check_decode_shape(B, Nq, &Nkv, D, max_kv_len, block_size, num_splits)) return rc;
+  if (kv_dtype == FIA_I8 && block_size % 32 != 0)
+    return fail(FIA_ERR_PARAM_INVALID, "int8 KV needs block_size %% 32 == 0 (got %d)", block_size);
+  if (kv_dtype == FIA_I8 && sink)
+    return fail(FIA_ERR_PARAM_INVALID, "the learnable sink is supported only without KV quantisation");
+  if (bt_stride < 1 || (int64_t)max_kv_len > bt_stride * block_size)
+    return fail(FIA_ERR_PARAM_INVALID, "block table too narrow: max_kv_len %d > bt_stride %lld * block_size %d",
+                max_kv_len, (long long)bt_stride, block_size);
+  if (num_blocks < 1) return fail(FIA_ERR_PARAM_INVALID, "num_blocks = %lld < 1", (long long)num_blocks);
+  if (num_blocks * Nkv * (int64_t)block_size >= (1LL << 31))
+    return fail(FIA_ERR_PARAM_INVALID, "KV pool has 2^31 or more rows");
+  if (!std::isfinite(scale)) return fail(FIA_ERR_PARAM_INVALID, "scale is not finite");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return fail(FIA_ERR_PARAM_INVALID, "q, k_cache, v_cache and out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(FIA_ERR_PARAM_INVALID, "workspace must be 256-byte aligned");
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  DecodePlan plan;
+  if (int rc = plan_decode(B, Nkv, max_kv_len, num_splits, d->num_sms, &plan)) return rc;
+  const int G = Nq / Nkv;
+  const size_t need = fia::decode_workspace_bytes(B, Nkv, G, D, plan.max_items);
+  if (workspace_bytes < need)
+    return fail(FIA_ERR_PARAM_INVALID, "workspace of %zu bytes is smaller than the %zu required", workspace_bytes,
+                need);
+  if (B == 0) return ok();  // empty query: nothing to do
+
+  fia::DecodeParams p{};
+  p.q = q;
+  p.out = out;
+  p.softmax_max = softmax_max;
+  p.softmax_sum = softmax_sum;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.seq_lens = actual_seq_lengths;
+  p.aq_scale = antiquant_scale;
+  p.aq_offset = antiquant_offset;
+  p.sink = sink;
+  p.B = B;
+  p.Nq = Nq;
+  p.Nkv = Nkv;
+  p.G = G;
+  p.D = D;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_kv_len = max_kv_len;
+  p.chunk_tokens = plan.chunk_tokens;
+  p.max_items = plan.max_items;
+  p.scale_log2 = (float)(scale * 1.4426950408889634);
+  p.q_dtype = q_dtype;
+  p.kv_dtype = kv_dtype;
+  p.ws = fia::decode_workspace_carve(workspace, B, Nkv, G, D, plan.max_items);
+  p.status = d->status;
+
+  const int elem = kv_dtype == FIA_I8 ? 1 : 2;
+  const uint32_t box_cols = (uint32_t)std::min(D * elem, 128) / elem;
+  const int box_rows = gcd(block_size, fia::kDecodeTile);
+  const uint64_t rows = (uint64_t)num_blocks * Nkv * block_size;
+  CUtensorMap tmK, tmV;
+  if (int rc = make_tmap(&tmK, k_cache, kv_dtype, D, rows, box_cols, box_rows)) return rc;
+  if (int rc = make_tmap(&tmV, v_cache, kv_dtype, D, rows, box_cols, box_rows)) return rc;
+  cudaError_t e = fia::launch_decode(p, tmK, tmV, box_rows, d->num_sms, stream);
+  if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "decode launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int ring_attention_update(const void* prev_out, const float* prev_max, const float* prev_sum, const void* cur_out,
+                          const float* cur_max, const float* cur_sum, fia_dtype out_dtype, int64_t rows, int N,
+                          int D, void* out, float* max_out, float* sum_out, fia_stream_t stream) {
+  if (!prev_out || !prev_max || !prev_sum || !cur_out || !cur_max || !cur_sum || !out || !max_out || !sum_out)
+    return fail(FIA_ERR_PARAM_NULLPTR, "every input and output of ring_attention_update is required");
+  if (out_dtype != FIA_F32 && out_dtype != FIA_F16 && out_dtype != FIA_BF16)
+    return fail(FIA_ERR_PARAM_INVALID, "out dtype must be fp32, fp16 or bf16");
+  if (rows < 0) return fail(FIA_ERR_PARAM_INVALID, "rows = %lld < 0", (long long)rows);
+  if (N < 1 || N > 256) return fail(FIA_ERR_PARAM_INVALID, "N = %d outside [1, 256]", N);
+  if (D < 8 || D > 768 || D % 8 != 0) return fail(FIA_ERR_PARAM_INVALID, "D = %d must be a multiple of 8 <= 768", D);
+  if (!aligned16(prev_out) || !aligned16(cur_out) || !aligned16(out))
+    return fail(FIA_ERR_PARAM_INVALID, "attention outputs must be 16-byte aligned");
+  cudaError_t e = fia::launch_rau(prev_out, prev_max, prev_sum, cur_out, cur_max, cur_sum, out_dtype, rows, N, D,
+                                  out, max_out, sum_out, stream);
+  if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "ring_attention_update launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int fia_debug_dequant(const int8_t* codes, const float* scale, const float* offset, int64_t n, float* out,
+                      fia_stream_t stream) {
+  if (!codes || !scale || !offset || !out) return fail(FIA_ERR_PARAM_NULLPTR, "all pointers are required");
+  if (n < 0) return fail(FIA_ERR_PARAM_INVALID, "n < 0");
+  cudaError_t e = fia::launch_debug_dequant(codes, scale, offset, n, out, stream);
+  if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "dequant probe launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int fia_debug_gather(const void* k_cache, fia_dtype kv_dtype, const int32_t* block_table, int64_t bt_stride,
+                     const int64_t* actual_seq_lengths, int max_kv_len, int B, int Nkv, int D, int block_size,
+                     int64_t num_blocks, int b, int hkv, void* dst, fia_stream_t stream) {
+  if (!k_cache || !block_table || !actual_seq_lengths || !dst)
+    return fail(FIA_ERR_PARAM_NULLPTR, "k_cache, block_table, actual_seq_lengths and dst are required");
+  if (kv_dtype != FIA_F16 && kv_dtype != FIA_BF16 && kv_dtype != FIA_I8)
+    return fail(FIA_ERR_PARAM_INVALID, "kv dtype must be fp16, bf16 or int8");
+  int nkv = Nkv;
+  if (int rc = check_decode_shape(B, std::max(Nkv, 1), &nkv, D, max_kv_len, block_size, 0)) return rc;
+  if (b < 0 || b >= B || hkv < 0 || hkv >= nkv) return fail(FIA_ERR_PARAM_INVALID, "(b, hkv) out of range");
+  if (bt_stride < 1 || (int64_t)max_kv_len > bt_stride * block_size || num_blocks < 1)
+    return fail(FIA_ERR_PARAM_INVALID, "block table / pool shape");
+  if (!aligned16(k_cache)) return fail(FIA_ERR_PARAM_INVALID, "k_cache must be 16-byte aligned");
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  fia::DecodeParams p{};
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.seq_lens = actual_seq_lengths;
+  p.B = B;
+  p.Nkv = nkv;
+  p.D = D;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  p.max_kv_len = max_kv_len;
+  p.kv_dtype = kv_dtype;
+  p.status = d->status;
+  const int elem = kv_dtype == FIA_I8 ? 1 : 2;
+  const uint32_t box_cols = (uint32_t)std::min(D * elem, 128) / elem;
+  const int box_rows = gcd(block_size, fia::kDecodeTile);
+  CUtensorMap tmK;
+  if (int rc = make_tmap(&tmK, k_cache, kv_dtype, D, (uint64_t)num_blocks * nkv * block_size, box_cols, box_rows))
+    return rc;
+  cudaError_t e = fia::launch_debug_gather(p, tmK, box_rows, b, hkv, dst, stream);
+  if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "gather probe launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+}  // extern "C"
+
+extern "C" {
+
+int fia_prefill_workspace_size(int B, int Nq, int Nkv, int D, int max_seqlen_q, size_t* bytes) {
+  if (!bytes) return fail(FIA_ERR_PARAM_NULLPTR, "bytes is NULL");
+  (void)Nkv;
+  (void)D;
+  *bytes = fia::prefill_workspace_bytes(B, Nq, max_seqlen_q);
+  return ok();
+}
+
+int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, const int64_t* cu_seqlens_q,
+                const int64_t* cu_seqlens_kv, int B, int64_t T, int64_t Tkv, int max_seqlen_q, int max_seqlen_kv,
+                int Nq, int Nkv, int D, double scale, int mask, const float* sink, void* out, float* softmax_max,
+                float* softmax_sum, void* workspace, size_t workspace_bytes, fia_stream_t stream) {
+  (void)q; (void)k; (void)v; (void)dtype; (void)cu_seqlens_q; (void)cu_seqlens_kv; (void)B; (void)T; (void)Tkv;
+  (void)max_seqlen_q; (void)max_seqlen_kv; (void)Nq; (void)Nkv; (void)D; (void)scale; (void)mask; (void)sink;
+  (void)out; (void)softmax_max; (void)softmax_sum; (void)workspace; (void)workspace_bytes; (void)stream;
+  return fail(FIA_ERR_PARAM_INVALID, "prefill is not available in this build yet");
+}
+
+}  // extern "C"

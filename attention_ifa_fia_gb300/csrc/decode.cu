@@ -1,0 +1,705 @@
+// decode.cu -- paged GQA decode attention (query S = 1) on CUDA cores.
+//
+// What it computes (aclnnIncreFlashAttentionV3, "Function" and "Constraints /
+// page attention"; aclnnFlashAttentionScoreV4, sink formula): for each batch b
+// and query head h, out = softmax(scale * q K^T) V over the first L_b tokens of
+// the paged cache, token t read from block block_table[b][t / bs], row t % bs of
+// the (blocknum, KV_N, blocksize, D) pool, with kv head h / (Nq / Nkv).
+//
+// Structure (three launches on the caller's stream):
+//   1. plan     -- one CTA splits every (b, kv-head) sequence into work items of
+//                  `chunk_tokens` tokens and resets the work counter.
+//   2. attention -- persistent CTAs (one per SM).  Warp 8 is the producer: it
+//                  takes items from the counter, reads the block table and issues
+//                  TMA tile loads (2-D tensor maps over the pool, 128- or 64-byte
+//                  swizzle) of K and V into a 4-stage mbarrier ring, plus the
+//                  item's G query rows by a 1-D bulk copy.  Warps 0-7 compute, for
+//                  the whole GQA group at once: scores from registers-resident q,
+//                  a warp-shuffle online softmax (max and sum), and P.V.  Each item
+//                  leaves a normalised partial (o, max, sum) in the workspace.
+//   3. merge    -- one CTA per (b, kv-head) folds the item partials in order by the
+//                  RingAttentionUpdate rule, adds the sink once, and writes out,
+//                  softmax max and softmax sum.
+// Scores are kept in log2 units (scale * log2 e folded into the dot product) and
+// converted back to the natural-exp domain for the max output.
+#include "fia_device.cuh"
+
+namespace fia {
+namespace {
+
+constexpr int kTT = kDecodeTile;
+constexpr int kConsumerWarps = kDecodeConsumers / 32;
+constexpr int kThreads = kDecodeConsumers + 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kBarConsumers = 1;  // named barrier id for the 256 math threads
+constexpr int kAqHeads = 8;       // kv heads whose antiquant parameters stay in shared memory
+
+template <int KVT, int D, int GP>
+struct Cfg {
+  static constexpr int kElem = (KVT == kI8) ? 1 : 2;
+  static constexpr int kRowBytes = D * kElem;
+  static constexpr int kBoxBytes = kRowBytes < 128 ? kRowBytes : 128;  // swizzle span of one box
+  static constexpr int kNumBoxes = kRowBytes / kBoxBytes;
+  static constexpr uint32_t kSwzMask = kBoxBytes == 128 ? 7u : 3u;
+  static constexpr int kTileBytes = kTT * kRowBytes;  // K (or V) of one stage
+  // score mapping: each thread owns E channels of one token; P threads per token
+  static constexpr int E = (64 / GP) < D ? (64 / GP) : D;
+  static constexpr int P = D / E;
+  static constexpr int PB = (E * kElem) < 16 ? (E * kElem) : 16;  // bytes per shared load
+  static constexpr int NPC = E * kElem / PB;                      // loads per token
+  static constexpr int PE = PB / kElem;                           // elements per load
+  static constexpr int TPP = kDecodeConsumers / P;                // tokens per pass
+  static constexpr int PASSES = (kTT + TPP - 1) / TPP;
+  static constexpr bool kPartsMinor = P >= 8;
+  static constexpr int TW = 32 / P;  // tokens per warp per pass
+  static constexpr int LOGP = (P >= 32) ? 5 : (P >= 16) ? 4 : (P >= 8) ? 3 : (P >= 4) ? 2 : (P >= 2) ? 1 : 0;
+  static constexpr int LOGG = (GP >= 8) ? 3 : (GP >= 4) ? 2 : (GP >= 2) ? 1 : 0;
+  static constexpr int MS = kPartsMinor ? 1 : TW;  // lane stride between parts of a token
+  // P.V mapping: each thread owns 8 channels (one chunk) for a group of tokens
+  static constexpr int EV = 8;
+  static constexpr int CH = D / EV;
+  static constexpr int NTG = kDecodeConsumers / CH;
+  static constexpr int TPG = kTT / NTG;
+  static_assert(LOGG <= LOGP || P == 1, "score reduction needs at least G lanes per token");
+  static_assert(kTT % NTG == 0, "token groups must tile the stage");
+};
+
+struct __align__(16) StageMeta {
+  int b, hkv, tok0, n;  // tile start token and valid tokens
+  int item, first, last, pad;
+};
+
+template <int KVT, int D, int GP>
+struct Smem {
+  using C = Cfg<KVT, D, GP>;
+  alignas(1024) uint8_t kv[kDecodeStages][2][C::kTileBytes];  // [stage][K|V]
+  alignas(16) uint16_t q[kDecodeStages][GP * D];              // query rows of the item (storage bits)
+  float red[kConsumerWarps][GP * D];                          // end-of-item reduction
+  float s[GP][kTT];                                           // scores (log2 units)
+  float p[kTT][GP];                                           // probabilities
+  float alpha[GP], m_run[GP], l_run[GP];
+  // int8: [k_scale, k_offset, v_scale, v_offset][hkv * D + d] for up to kAqHeads kv heads
+  float aq[KVT == kI8 ? 4 : 1][KVT == kI8 ? D * kAqHeads : 1];
+  StageMeta meta[kDecodeStages];
+  uint64_t full[kDecodeStages], empty[kDecodeStages];
+};
+
+// Pool row of token t of (b, hkv): block_table entry, then the row inside the block.
+__device__ __forceinline__ int64_t pool_row(int32_t blk, int t, int bs, int Nkv, int hkv) {
+  return ((int64_t)blk * Nkv + hkv) * bs + (t % bs);
+}
+
+// Load one 16- or 8-byte piece of a swizzled tile row.
+template <int PB>
+__device__ __forceinline__ void load_piece(uint32_t addr, uint32_t (&w)[4]) {
+  if constexpr (PB == 16) {
+    uint4 v = lds128(addr);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else {
+    uint2 v = lds64(addr);
+    w[0] = v.x; w[1] = v.y; w[2] = 0; w[3] = 0;
+  }
+}
+
+// Widen element e of a loaded piece to fp32 (int8: exact code, not yet dequantised).
+template <int KVT>
+__device__ __forceinline__ float piece_elem(const uint32_t (&w)[4], int e) {
+  if constexpr (KVT == kBF16) return (e & 1) ? bf16hi(w[e >> 1]) : bf16lo(w[e >> 1]);
+  else if constexpr (KVT == kF16) return (e & 1) ? f16hi(w[e >> 1]) : f16lo(w[e >> 1]);
+  else return i8_to_f32(w[e >> 2], e & 3);
+}
+
+__device__ __forceinline__ float q_elem(const uint16_t* q, int idx, int q_dtype) {
+  const uint32_t u = q[idx];
+  return q_dtype == kBF16 ? __uint_as_float(u << 16) : __half2float(__ushort_as_half((unsigned short)u));
+}
+
+// ------------------------------------------------------------------- plan
+__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  const int C = p.chunk_tokens;
+  for (int b0 = 0; b0 < p.B; b0 += 1024) {
+    const int b = b0 + tid;
+    int L = 0, nch = 0;
+    if (b < p.B) {
+      int64_t raw = p.seq_lens[b];
+      if (raw < 0 || raw > p.max_kv_len) raise_status(p.status, kStatusLengthClamped);
+      L = (int)(raw < 0 ? 0 : (raw > p.max_kv_len ? p.max_kv_len : raw));
+      nch = (L + C - 1) / C;
+    }
+    int cnt = nch * p.Nkv;
+    // inclusive warp scan, then across warps
+    int x = cnt;
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int t = warp_tot[lane];
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
+      }
+      warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int base = carry + (warp ? warp_tot[warp - 1] : 0) + x - cnt;
+    if (b < p.B) {
+      p.ws.seg_base[b] = base;
+      for (int h = 0; h < p.Nkv; ++h)
+        for (int j = 0; j < nch; ++j) {
+          const int t0 = j * C, t1 = min(L, t0 + C);
+          p.ws.items[base + h * nch + j] = make_int4(b, h, t0, t1);
+        }
+    }
+    __syncthreads();
+    if (tid == 1023) carry = base + cnt;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    *p.ws.n_items = carry;
+    *p.ws.counter = 0;
+  }
+}
+
+// ------------------------------------------------------------------- attention
+template <int KVT, int D, int GP>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_splitkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const DecodeParams p, const int box_rows) {
+  using C = Cfg<KVT, D, GP>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem<KVT, D, GP>& sm =
+      *reinterpret_cast<Smem<KVT, D, GP>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.G;
+
+  if (tid == 0) {
+    for (int s = 0; s < kDecodeStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  if (KVT == kI8 && p.Nkv <= kAqHeads) {  // per-channel antiquant parameters stay resident
+    for (int i = tid; i < p.Nkv * D; i += kThreads) {
+      sm.aq[0][i] = p.aq_scale[i];
+      sm.aq[1][i] = p.aq_offset ? p.aq_offset[i] : 0.f;
+      sm.aq[2][i] = p.aq_scale[p.Nkv * D + i];
+      sm.aq[3][i] = p.aq_offset ? p.aq_offset[p.Nkv * D + i] : 0.f;
+    }
+  }
+  __syncthreads();
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    const int n_items = *p.ws.n_items;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    int next = 0;
+    if (lane == 0) next = atomicAdd(p.ws.counter, 1);
+    next = __shfl_sync(0xffffffffu, next, 0);
+    const int bs = p.block_size;
+    const uint32_t piece_bytes = (uint32_t)box_rows * C::kBoxBytes * C::kNumBoxes;  // one of K/V
+    while (ok && next < n_items) {
+      const int item = next;
+      const int4 desc = p.ws.items[item];
+      if (lane == 0) next = atomicAdd(p.ws.counter, 1);
+      next = __shfl_sync(0xffffffffu, next, 0);
+      const int b = desc.x, hkv = desc.y, t_begin = desc.z, t_end = desc.w;
+      const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
+      for (int tok0 = t_begin; tok0 < t_end; tok0 += kTT) {
+        const int n = min(kTT, t_end - tok0);
+        const int npieces = (n + box_rows - 1) / box_rows;
+        int32_t blk = 0;
+        bool valid = false;
+        if (lane < npieces) {
+          blk = bt_row[(tok0 + lane * box_rows) / bs];
+          valid = blk >= 0 && (int64_t)blk < p.num_blocks;
+          if (!valid) raise_status(p.status, kStatusBadBlockIndex);
+        }
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        const bool first = tok0 == t_begin;
+        uint32_t bytes = 2u * piece_bytes * __popc(vmask);
+        if (first) bytes += (uint32_t)(G * D * 2);
+        if (!mbar_wait(&sm.empty[stage], phase ^ 1u, p.status)) { ok = false; break; }
+        if (lane == 0) {
+          StageMeta& m = sm.meta[stage];
+          m.b = b; m.hkv = hkv; m.tok0 = tok0; m.n = n;
+          m.item = item; m.first = first; m.last = (tok0 + kTT >= t_end);
+          mbar_arrive_expect_tx(&sm.full[stage], bytes);
+        }
+        __syncwarp();
+        if (valid) {
+          const int64_t row = pool_row(blk, tok0 + lane * box_rows, bs, p.Nkv, hkv);
+          for (int bx = 0; bx < C::kNumBoxes; ++bx) {
+            const uint32_t off = bx * (kTT * C::kBoxBytes) + lane * box_rows * C::kBoxBytes;
+            tma_load_2d(sm.kv[stage][0] + off, &tmK, bx * (C::kBoxBytes / C::kElem), (int32_t)row, &sm.full[stage]);
+            tma_load_2d(sm.kv[stage][1] + off, &tmV, bx * (C::kBoxBytes / C::kElem), (int32_t)row, &sm.full[stage]);
+          }
+        }
+        if (first && lane == 0) {
+          const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) + ((int64_t)b * p.Nq + (int64_t)hkv * G) * D;
+          bulk_load(sm.q[stage], qsrc, (uint32_t)(G * D * 2), &sm.full[stage]);
+        }
+        if (++stage == kDecodeStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    // sentinel: tells the math warps that no item follows
+    if (ok && mbar_wait(&sm.empty[stage], phase ^ 1u, p.status)) {
+      if (lane == 0) {
+        sm.meta[stage].item = -1;
+        mbar_arrive(&sm.full[stage]);
+      }
+    } else {
+      // give every copy already issued a bounded chance to land before exiting
+      for (int s = 0; s < kDecodeStages; ++s) mbar_wait(&sm.full[s], phase, p.status);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  // score mapping
+  const int part = C::kPartsMinor ? (lane % C::P) : (lane / C::TW);
+  const int tok_w = C::kPartsMinor ? (lane / C::P) : (lane % C::TW);
+  // head held after the reduce-scatter, and whether this lane writes it
+  int gh = 0;
+  bool writer = true;
+  {
+    int cnt = GP;
+#pragma unroll
+    for (int l = 0; l < C::LOGP; ++l) {
+      const int mask = C::MS << l;
+      if (cnt > 1) {
+        cnt >>= 1;
+        if (lane & mask) gh += cnt;
+      } else if (lane & mask) {
+        writer = false;
+      }
+    }
+  }
+  // P.V mapping
+  const int pv_c = tid % C::CH, pv_tg = tid / C::CH;
+
+  float qr[GP][C::E];
+  float kdq[2][C::E];  // int8: k scale / offset of this thread's channels
+  float vdq[2][C::EV]; // int8: v scale / offset of this thread's P.V channels
+  float acc[GP][C::EV];
+#pragma unroll
+  for (int g = 0; g < GP; ++g)
+#pragma unroll
+    for (int e = 0; e < C::EV; ++e) acc[g][e] = 0.f;
+
+  int stage = 0;
+  uint32_t phase = 0;
+  while (true) {
+    if (!mbar_wait(&sm.full[stage], phase, p.status)) break;
+    const StageMeta meta = sm.meta[stage];
+    if (meta.item < 0) break;
+    const uint8_t* kt = sm.kv[stage][0];
+    const uint8_t* vt = sm.kv[stage][1];
+    const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+
+    if (meta.first) {
+      const uint16_t* qs = sm.q[stage];
+#pragma unroll
+      for (int g = 0; g < GP; ++g)
+#pragma unroll
+        for (int j = 0; j < C::NPC; ++j)
+#pragma unroll
+          for (int e = 0; e < C::PE; ++e) {
+            const int d = (part + C::P * j) * C::PE + e;
+            qr[g][j * C::PE + e] = (g < G) ? q_elem(qs, g * D + d, p.q_dtype) : 0.f;
+          }
+      if (KVT == kI8) {
+        const bool resident = p.Nkv <= kAqHeads;
+        const int64_t vofs = (int64_t)p.Nkv * D;
+#pragma unroll
+        for (int j = 0; j < C::NPC; ++j)
+#pragma unroll
+          for (int e = 0; e < C::PE; ++e) {
+            const int d = meta.hkv * D + (part + C::P * j) * C::PE + e;
+            kdq[0][j * C::PE + e] = resident ? sm.aq[0][d] : p.aq_scale[d];
+            kdq[1][j * C::PE + e] = resident ? sm.aq[1][d] : (p.aq_offset ? p.aq_offset[d] : 0.f);
+          }
+#pragma unroll
+        for (int e = 0; e < C::EV; ++e) {
+          const int d = meta.hkv * D + pv_c * C::EV + e;
+          vdq[0][e] = resident ? sm.aq[2][d] : p.aq_scale[vofs + d];
+          vdq[1][e] = resident ? sm.aq[3][d] : (p.aq_offset ? p.aq_offset[vofs + d] : 0.f);
+        }
+      }
+    }
+
+    // ---- scores: s[g][t] = scale * log2(e) * q_g . k_t
+#pragma unroll
+    for (int pass = 0; pass < C::PASSES; ++pass) {
+      const int t = pass * C::TPP + warp * C::TW + tok_w;
+      float v[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) v[g] = 0.f;
+      if (t < kTT) {
+#pragma unroll
+        for (int j = 0; j < C::NPC; ++j) {
+          const uint32_t ob = (part + C::P * j) * C::PB;  // byte offset in the row
+          const uint32_t addr = kbase + (ob / C::kBoxBytes) * (kTT * C::kBoxBytes) +
+                                swz(t * C::kBoxBytes + (ob % C::kBoxBytes), C::kSwzMask);
+          uint32_t w[4];
+          load_piece<C::PB>(addr, w);
+#pragma unroll
+          for (int e = 0; e < C::PE; ++e) {
+            float kf = piece_elem<KVT>(w, e);
+            if (KVT == kI8) kf = dequant_i8(kf, kdq[1][j * C::PE + e], kdq[0][j * C::PE + e]);
+#pragma unroll
+            for (int g = 0; g < GP; ++g) v[g] = fmaf(qr[g][j * C::PE + e], kf, v[g]);
+          }
+        }
+      }
+      // reduce-scatter across the P lanes of this token: halve the head set per level
+      int cnt = GP;
+#pragma unroll
+      for (int l = 0; l < C::LOGP; ++l) {
+        const int mask = C::MS << l;
+        const bool upper = lane & mask;
+        if (cnt > 1) {
+          const int half = cnt >> 1;
+#pragma unroll
+          for (int i = 0; i < GP / 2; ++i) {
+            if (i < half) {
+              const float send = upper ? v[i] : v[i + half];
+              const float keep = upper ? v[i + half] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+            }
+          }
+          cnt = half;
+        } else {
+          v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+        }
+      }
+      if (t < kTT && writer) {
+#pragma unroll
+        for (int i = 0; i < GP; ++i)
+          if (i < cnt) sm.s[gh + i][t] = (t < meta.n) ? v[i] * p.scale_log2 : -INFINITY;
+      }
+    }
+    named_bar_sync(kBarConsumers, kDecodeConsumers);
+
+    // ---- online softmax, one warp per head
+    for (int g = warp; g < GP; g += kConsumerWarps) {
+      const float s0 = sm.s[g][lane], s1 = sm.s[g][lane + 32];
+      float mx = fmaxf(s0, s1);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_old = meta.first ? -INFINITY : sm.m_run[g];
+      const float m_new = fmaxf(m_old, mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_use);
+      const float p0 = exp2f(s0 - m_use), p1 = exp2f(s1 - m_use);
+      sm.p[lane][g] = p0;
+      sm.p[lane + 32][g] = p1;
+      float sum = p0 + p1;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (lane == 0) {
+        const float l_old = meta.first ? 0.f : sm.l_run[g];
+        sm.l_run[g] = l_old * alpha + sum;
+        sm.m_run[g] = m_new;
+        sm.alpha[g] = alpha;
+      }
+    }
+    named_bar_sync(kBarConsumers, kDecodeConsumers);
+
+    // ---- acc = acc * alpha + P . V for this thread's 8 channels
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      const float a = sm.alpha[g];
+#pragma unroll
+      for (int e = 0; e < C::EV; ++e) acc[g][e] = meta.first ? 0.f : acc[g][e] * a;
+    }
+#pragma unroll
+    for (int i = 0; i < C::TPG; ++i) {
+      const int t = pv_tg + C::NTG * i;
+      if (t < meta.n) {
+        const uint32_t ob = pv_c * C::EV * C::kElem;
+        const uint32_t addr = vbase + (ob / C::kBoxBytes) * (kTT * C::kBoxBytes) +
+                              swz(t * C::kBoxBytes + (ob % C::kBoxBytes), C::kSwzMask);
+        uint32_t w[4];
+        load_piece<C::EV * C::kElem>(addr, w);
+        float vf[C::EV];
+#pragma unroll
+        for (int e = 0; e < C::EV; ++e) {
+          vf[e] = piece_elem<KVT>(w, e);
+          if (KVT == kI8) vf[e] = dequant_i8(vf[e], vdq[1][e], vdq[0][e]);
+        }
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          const float pg = sm.p[t][g];
+#pragma unroll
+          for (int e = 0; e < C::EV; ++e) acc[g][e] = fmaf(pg, vf[e], acc[g][e]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);
+
+    // ---- end of item: reduce over token groups and write the normalised partial
+    if (meta.last) {
+#pragma unroll
+      for (int mask = C::CH; mask < 32; mask <<= 1)
+#pragma unroll
+        for (int g = 0; g < GP; ++g)
+#pragma unroll
+          for (int e = 0; e < C::EV; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], mask);
+      if (lane < C::CH) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g)
+#pragma unroll
+          for (int e = 0; e < C::EV; ++e) sm.red[warp][g * D + pv_c * C::EV + e] = acc[g][e];
+      }
+      named_bar_sync(kBarConsumers, kDecodeConsumers);
+      float* po = p.ws.part_o + (int64_t)meta.item * G * D;
+      for (int o = tid; o < G * D; o += kDecodeConsumers) {
+        float s = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kConsumerWarps; ++w2) s += sm.red[w2][o];
+        const float l = sm.l_run[o / D];
+        po[o] = l > 0.f ? s / l : 0.f;
+      }
+      if (tid < G) p.ws.part_ml[(int64_t)meta.item * G + tid] = make_float2(sm.m_run[tid], sm.l_run[tid]);
+      named_bar_sync(kBarConsumers, kDecodeConsumers);
+    }
+    if (++stage == kDecodeStages) { stage = 0; phase ^= 1u; }
+  }
+}
+
+// ------------------------------------------------------------------- merge
+template <int QT>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+  extern __shared__ float wts[];  // [G][nch]
+  const int b = blockIdx.x / p.Nkv, hkv = blockIdx.x % p.Nkv;
+  const int G = p.G, D = p.D, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int64_t raw = p.seq_lens[b];
+  const int L = (int)(raw < 0 ? 0 : (raw > p.max_kv_len ? p.max_kv_len : raw));
+  const int nch = (L + p.chunk_tokens - 1) / p.chunk_tokens;
+  const int base = p.ws.seg_base[b] + hkv * nch;
+  for (int g = warp; g < G; g += 8) {
+    const int h = hkv * G + g;
+    float M = -INFINITY;
+    for (int j = lane; j < nch; j += 32) M = fmaxf(M, p.ws.part_ml[(int64_t)(base + j) * G + g].x);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float sink2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+    M = fmaxf(M, sink2);
+    float W = 0.f;
+    if (M != -INFINITY) {
+      for (int j = lane; j < nch; j += 32) {
+        const float2 ml = p.ws.part_ml[(int64_t)(base + j) * G + g];
+        const float w = (ml.x == -INFINITY) ? 0.f : ml.y * exp2f(ml.x - M);
+        wts[g * nch + j] = w;
+        W += w;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+      if (p.sink) W += exp2f(sink2 - M);
+      const float inv = W > 0.f ? 1.f / W : 0.f;
+      for (int j = lane; j < nch; j += 32) wts[g * nch + j] *= inv;
+    } else {
+      for (int j = lane; j < nch; j += 32) wts[g * nch + j] = 0.f;
+    }
+    if (lane == 0) {
+      if (p.softmax_max) p.softmax_max[(int64_t)b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+      if (p.softmax_sum) p.softmax_sum[(int64_t)b * p.Nq + h] = W;
+    }
+  }
+  __syncthreads();
+  for (int o = tid; o < G * D; o += 256) {
+    const int g = o / D;
+    float acc = 0.f;
+    for (int j = 0; j < nch; ++j) acc = fmaf(wts[g * nch + j], p.ws.part_o[(int64_t)(base + j) * G * D + o], acc);
+    store_out<QT>(p.out, ((int64_t)b * p.Nq + hkv * G) * D + o, acc);
+  }
+}
+
+// ------------------------------------------------------------------- probes
+__global__ void debug_dequant_kernel(const int8_t* codes, const float* scale, const float* offset, int64_t n,
+                                     float* out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t w = (uint32_t)(uint8_t)codes[i];
+    out[i] = dequant_i8(i8_to_f32(w, 0), offset[i], scale[i]);
+  }
+}
+
+// Copies the visible K rows of one (b, hkv) sequence into dst (L x D, storage
+// bytes) through the same block-table walk, tensor map, box shape and swizzled
+// read addressing as the attention kernel.
+template <int KVT, int D>
+__global__ void __launch_bounds__(128) debug_gather_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                           const DecodeParams p, const int box_rows, const int b,
+                                                           const int hkv, uint8_t* dst) {
+  using C = Cfg<KVT, D, 1>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* tile = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  int64_t raw = p.seq_lens[b];
+  const int L = (int)(raw < 0 ? 0 : (raw > p.max_kv_len ? p.max_kv_len : raw));
+  const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
+  uint32_t phase = 0;
+  for (int tok0 = 0; tok0 < L; tok0 += kTT) {
+    const int n = min(kTT, L - tok0);
+    const int npieces = (n + box_rows - 1) / box_rows;
+    if (tid == 0) {
+      uint32_t bytes = 0;
+      for (int r = 0; r < npieces; ++r) {
+        const int32_t blk = bt_row[(tok0 + r * box_rows) / p.block_size];
+        if (blk >= 0 && blk < p.num_blocks) bytes += box_rows * C::kBoxBytes * C::kNumBoxes;
+      }
+      mbar_arrive_expect_tx(&bar, bytes);
+      for (int r = 0; r < npieces; ++r) {
+        const int32_t blk = bt_row[(tok0 + r * box_rows) / p.block_size];
+        if (!(blk >= 0 && blk < p.num_blocks)) continue;
+        const int64_t row = pool_row(blk, tok0 + r * box_rows, p.block_size, p.Nkv, hkv);
+        for (int bx = 0; bx < C::kNumBoxes; ++bx)
+          tma_load_2d(tile + bx * (kTT * C::kBoxBytes) + r * box_rows * C::kBoxBytes, &tmK,
+                      bx * (C::kBoxBytes / C::kElem), (int32_t)row, &bar);
+      }
+    }
+    __syncthreads();
+    if (!mbar_wait(&bar, phase, p.status)) return;
+    phase ^= 1u;
+    for (int i = tid; i < n * C::kRowBytes; i += blockDim.x) {
+      const int t = i / C::kRowBytes, ob = i % C::kRowBytes;
+      const uint32_t off = (ob / C::kBoxBytes) * (kTT * C::kBoxBytes) +
+                           swz(t * C::kBoxBytes + (ob % C::kBoxBytes), C::kSwzMask);
+      dst[(int64_t)(tok0 + t) * C::kRowBytes + ob] = tile[off];
+    }
+    __syncthreads();
+  }
+}
+
+template <int KVT, int D, int GP>
+cudaError_t launch_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows,
+                             int grid, cudaStream_t stream) {
+  const size_t smem = sizeof(Smem<KVT, D, GP>) + 1024;
+  auto kern = decode_splitkv_kernel<KVT, D, GP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, stream>>>(tmK, tmV, p, box_rows);
+  return cudaGetLastError();
+}
+
+template <int KVT, int D>
+cudaError_t launch_attention_g(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows,
+                               int grid, cudaStream_t stream) {
+  if (p.G <= 1) return launch_attention<KVT, D, 1>(p, tmK, tmV, box_rows, grid, stream);
+  if (p.G <= 2) return launch_attention<KVT, D, 2>(p, tmK, tmV, box_rows, grid, stream);
+  if (p.G <= 4) return launch_attention<KVT, D, 4>(p, tmK, tmV, box_rows, grid, stream);
+  return launch_attention<KVT, D, 8>(p, tmK, tmV, box_rows, grid, stream);
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int B, int Nkv, int G, int D, int max_items) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  size_t s = 256;                                      // counter, n_items
+  s += up(sizeof(int) * (size_t)(B > 0 ? B : 1));      // seg_base
+  s += up(sizeof(int4) * (size_t)max_items);           // items
+  s += up(sizeof(float) * (size_t)max_items * G * D);  // part_o
+  s += up(sizeof(float2) * (size_t)max_items * G);     // part_ml
+  (void)Nkv;
+  return s;
+}
+
+DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D, int max_items) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  uint8_t* c = static_cast<uint8_t*>(base);
+  DecodeWorkspace w;
+  w.counter = reinterpret_cast<int*>(c);
+  w.n_items = reinterpret_cast<int*>(c + 4);
+  c += 256;
+  w.seg_base = reinterpret_cast<int*>(c);
+  c += up(sizeof(int) * (size_t)(B > 0 ? B : 1));
+  w.items = reinterpret_cast<int4*>(c);
+  c += up(sizeof(int4) * (size_t)max_items);
+  w.part_o = reinterpret_cast<float*>(c);
+  c += up(sizeof(float) * (size_t)max_items * G * D);
+  w.part_ml = reinterpret_cast<float2*>(c);
+  (void)Nkv;
+  return w;
+}
+
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows,
+                          int num_sms, cudaStream_t stream) {
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int grid = num_sms;
+  if (p.kv_dtype == kBF16) {
+    e = (p.D == 64) ? launch_attention_g<kBF16, 64>(p, tmK, tmV, box_rows, grid, stream)
+                    : launch_attention_g<kBF16, 128>(p, tmK, tmV, box_rows, grid, stream);
+  } else if (p.kv_dtype == kF16) {
+    e = (p.D == 64) ? launch_attention_g<kF16, 64>(p, tmK, tmV, box_rows, grid, stream)
+                    : launch_attention_g<kF16, 128>(p, tmK, tmV, box_rows, grid, stream);
+  } else {
+    e = (p.D == 64) ? launch_attention_g<kI8, 64>(p, tmK, tmV, box_rows, grid, stream)
+                    : launch_attention_g<kI8, 128>(p, tmK, tmV, box_rows, grid, stream);
+  }
+  if (e != cudaSuccess) return e;
+  const int max_chunks = (p.max_kv_len + p.chunk_tokens - 1) / p.chunk_tokens;
+  const size_t msmem = sizeof(float) * (size_t)p.G * (max_chunks > 0 ? max_chunks : 1);
+  if (p.q_dtype == kBF16) {
+    if (msmem > 48 * 1024)
+      cudaFuncSetAttribute(decode_merge_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+    decode_merge_kernel<kBF16><<<p.B * p.Nkv, 256, msmem, stream>>>(p);
+  } else {
+    if (msmem > 48 * 1024)
+      cudaFuncSetAttribute(decode_merge_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+    decode_merge_kernel<kF16><<<p.B * p.Nkv, 256, msmem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_dequant(const int8_t* codes, const float* scale, const float* offset, int64_t n,
+                                 float* out, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  debug_dequant_kernel<<<grid, 256, 0, stream>>>(codes, scale, offset, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_gather(const DecodeParams& p, const CUtensorMap& tmK, int box_rows, int b, int hkv,
+                                void* dst, cudaStream_t stream) {
+  auto run = [&](auto kern, int tile_bytes) {
+    const int smem = tile_bytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<1, 128, smem, stream>>>(tmK, p, box_rows, b, hkv, static_cast<uint8_t*>(dst));
+    return cudaGetLastError();
+  };
+  if (p.kv_dtype == kI8)
+    return p.D == 64 ? run(debug_gather_kernel<kI8, 64>, Cfg<kI8, 64, 1>::kTileBytes)
+                     : run(debug_gather_kernel<kI8, 128>, Cfg<kI8, 128, 1>::kTileBytes);
+  if (p.kv_dtype == kF16)
+    return p.D == 64 ? run(debug_gather_kernel<kF16, 64>, Cfg<kF16, 64, 1>::kTileBytes)
+                     : run(debug_gather_kernel<kF16, 128>, Cfg<kF16, 128, 1>::kTileBytes);
+  return p.D == 64 ? run(debug_gather_kernel<kBF16, 64>, Cfg<kBF16, 64, 1>::kTileBytes)
+                   : run(debug_gather_kernel<kBF16, 128>, Cfg<kBF16, 128, 1>::kTileBytes);
+}
+
+}  // namespace fia

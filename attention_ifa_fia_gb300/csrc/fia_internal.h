@@ -1,0 +1,115 @@
+// fia_internal.h -- declarations shared between the C-ABI layer (api.cu) and
+// the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fia {
+
+// storage types (same numbering as fia_dtype in include/fia.h)
+enum : int { kF32 = 0, kF16 = 1, kBF16 = 2, kI8 = 3 };
+
+// bits of the device status word
+enum : unsigned int {
+  kStatusWaitTimeout = 1u << 0,    // a bounded mbarrier wait gave up
+  kStatusBadBlockIndex = 1u << 1,  // a block-table entry outside [0, num_blocks)
+  kStatusLengthClamped = 1u << 2,  // a device length outside [0, max_kv_len] was clamped
+  kStatusBadSeqlens = 1u << 3,     // cumulative sequence lengths not monotone / out of range
+};
+
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
+constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
+
+// ---------------------------------------------------------------------------
+// Decode
+// ---------------------------------------------------------------------------
+constexpr int kDecodeTile = 64;        // tokens per pipeline stage
+constexpr int kDecodeStages = 4;       // stages in the TMA ring
+constexpr int kDecodeConsumers = 256;  // math threads (8 warps)
+
+struct DecodeWorkspace {
+  int* counter;     // dynamic work counter (reset by the plan kernel)
+  int* n_items;     // number of work items written by the plan kernel
+  int* seg_base;    // (B) first item of batch b
+  int4* items;      // (max_items) {b, hkv, tok_begin, tok_end}
+  float* part_o;    // (max_items, G, D) normalised partial outputs
+  float2* part_ml;  // (max_items, G) {max (log2 units), sum}
+};
+
+struct DecodeParams {
+  const void* q;
+  void* out;
+  float* softmax_max;
+  float* softmax_sum;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int64_t* seq_lens;
+  const float* aq_scale;   // (2, Nkv, D) or null
+  const float* aq_offset;  // (2, Nkv, D) or null
+  const float* sink;       // (Nq) or null
+  int B, Nq, Nkv, G, D, block_size;
+  int64_t num_blocks;
+  int max_kv_len;     // device lengths are clamped to [0, max_kv_len]
+  int chunk_tokens;   // tokens per work item (a multiple of kDecodeTile)
+  int max_items;
+  float scale_log2;   // scale * log2(e)
+  int q_dtype, kv_dtype;
+  DecodeWorkspace ws;
+  unsigned int* status;  // device status word
+};
+
+size_t decode_workspace_bytes(int B, int Nkv, int G, int D, int max_items);
+DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D, int max_items);
+
+// Launches plan + attention + merge on `stream`.  tmK / tmV describe the K and V
+// pools as 2-D tensors (D, num_blocks * Nkv * block_size).  Returns a CUDA error.
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows,
+                          int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// RingAttentionUpdate
+// ---------------------------------------------------------------------------
+cudaError_t launch_rau(const void* prev_out, const float* prev_max, const float* prev_sum, const void* cur_out,
+                       const float* cur_max, const float* cur_sum, int out_dtype, int64_t rows, int N, int D,
+                       void* out, float* max_out, float* sum_out, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Prefill
+// ---------------------------------------------------------------------------
+struct PrefillParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* softmax_max;
+  float* softmax_sum;
+  const int64_t* cu_q;
+  const int64_t* cu_kv;
+  const float* sink;
+  int B, Nq, Nkv, G, D;
+  int64_t T, Tkv;
+  int max_seqlen_q, max_seqlen_kv;
+  int causal;
+  float scale_log2;
+  int* tile_list;     // workspace: (n_tiles) packed tile descriptors
+  int* tile_counter;  // workspace: dynamic scheduler counter
+  int max_tiles;
+  unsigned int* status;
+};
+
+size_t prefill_workspace_bytes(int B, int Nq, int max_seqlen_q);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                           const CUtensorMap& tmV, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Probes used by the bit-exactness tests
+// ---------------------------------------------------------------------------
+cudaError_t launch_debug_dequant(const int8_t* codes, const float* scale, const float* offset, int64_t n,
+                                 float* out, cudaStream_t stream);
+cudaError_t launch_debug_gather(const DecodeParams& p, const CUtensorMap& tmK, int box_rows, int b, int hkv,
+                                void* dst, cudaStream_t stream);
+
+}  // namespace fia

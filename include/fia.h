@@ -1,0 +1,186 @@
+/*
+ * fia.h -- C interface of libfia_gb300: fused inference attention on one GB300
+ * (sm_103a).
+ *
+ * Operators (semantics from the operator documentation pages cited per call):
+ *   fia_decode             paged GQA decode attention, query S = 1, optional int8
+ *                          KV antiquant and learnable sink, split-KV partials merged
+ *                          by the RingAttentionUpdate rule
+ *   fia_prefill            causal variable-length attention, TND layout
+ *   ring_attention_update  merge of two attention partials by softmax max/sum
+ *
+ * Conventions shared by every call:
+ *   - Pointers marked "device" are CUDA device addresses; the caller allocates and
+ *     owns all of them, including the workspace.  The library allocates nothing on
+ *     the device and keeps no state between calls except the device status word
+ *     (see fia_device_status).
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Results are valid once the stream has synchronised.
+ *   - Arguments are checked on the host before anything is launched.  On any
+ *     non-zero return nothing was launched and no output was touched, except for
+ *     FIA_ERR_RUNTIME, which reports a failed launch.
+ *   - Results are bitwise reproducible for fixed inputs and arguments (no float
+ *     atomics; partials are merged in a fixed order).
+ *   - Return codes follow the aclnn codes of the pages (aclnnIncreFlashAttentionV3,
+ *     "Return Value"): 0 success; 161001 a required pointer is NULL; 161002 an
+ *     invalid dtype, shape, attribute or alignment, a size this build does not
+ *     support, or a workspace that is too small; 361001 a CUDA runtime error;
+ *     561002 the split planner could not partition the work.
+ *     fia_last_error() returns a text description of the last failure on the
+ *     calling thread.
+ */
+#ifndef FIA_H_
+#define FIA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fia_stream_t; /* identical to cudaStream_t */
+
+typedef enum { FIA_F32 = 0, FIA_F16 = 1, FIA_BF16 = 2, FIA_I8 = 3 } fia_dtype;
+
+enum {
+  FIA_SUCCESS = 0,
+  FIA_ERR_PARAM_NULLPTR = 161001,
+  FIA_ERR_PARAM_INVALID = 161002,
+  FIA_ERR_RUNTIME = 361001,
+  FIA_ERR_INNER_TILING = 561002
+};
+
+/* Bits of the device status word (fia_device_status). */
+enum {
+  FIA_STATUS_WAIT_TIMEOUT = 1,    /* a bounded on-chip wait gave up; results of that launch are invalid */
+  FIA_STATUS_BAD_BLOCK_INDEX = 2, /* a block-table entry in use was outside [0, num_blocks); its tile was skipped */
+  FIA_STATUS_LENGTH_CLAMPED = 4,  /* a device length was outside [0, max_kv_len] and was clamped */
+  FIA_STATUS_BAD_SEQLENS = 8      /* cumulative sequence lengths were not monotone or exceeded T */
+};
+
+/* Text of the last error returned on the calling thread ("" if none). */
+const char* fia_last_error(void);
+
+/* Synchronises `stream`, returns in *flags the device status bits raised by any
+ * launch of this library on the current device since the previous call, and
+ * clears them.  Returns 0, or 361001 if the synchronisation itself failed. */
+int fia_device_status(fia_stream_t stream, unsigned int* flags);
+
+/* ------------------------------------------------------------------------- decode
+ * aclnnIncreFlashAttentionV3 ("Function", parameter table, "Constraints / page
+ * attention"); FusedInferAttentionScore (learnableSink, softmax max/sum for ring
+ * merging); aclnnFlashAttentionScoreV4 (sink formula).
+ *
+ *   out[b][h] = softmax(scale * q[b][h] . K^T) V over the first L_b = actual_seq_lengths[b]
+ *   tokens of batch b, with query head h reading kv head h / (Nq / Nkv).  Token t of batch
+ *   b lives in pool block block_table[b * bt_stride + t / block_size], row t % block_size.
+ *   With a sink s_h:  m = max(s_h, max_t z_t),  out = sum_t e^{z_t - m} v_t / (sum_t e^{z_t - m} + e^{s_h - m}).
+ *   softmax_max[b][h] = m and softmax_sum[b][h] = sum_t e^{z_t - m} (+ e^{s_h - m}), where z_t is
+ *   the scaled logit (natural-exp domain).  A row with no visible key and no sink gives
+ *   out = 0, max = -inf, sum = 0; with a sink, out = 0, max = s_h, sum = 1.
+ *
+ * q, out             device, (B, Nq, D) row-major in q_dtype (FIA_F16 or FIA_BF16); with query
+ *                    length 1 this is the memory of the BNSD, BSND and BSH layouts alike.
+ *                    16-byte aligned.
+ * k_cache, v_cache   device, (num_blocks, Nkv, block_size, D) row-major (the pages'
+ *                    (blocknum, KV_N, blocksize, D) layout), in kv_dtype: q_dtype, or FIA_I8.
+ *                    16-byte aligned.  Only rows of visible tokens are read.
+ * block_table        device int32, B rows of bt_stride entries; entries past
+ *                    ceil(L_b / block_size) are never read.
+ * actual_seq_lengths device int64 (B).  Values are clamped to [0, max_kv_len]
+ *                    (FIA_STATUS_LENGTH_CLAMPED is raised if any is outside).
+ * max_kv_len         host upper bound of the lengths; <= bt_stride * block_size.
+ * Nkv                0 means Nkv = Nq.  Nq % Nkv == 0; Nq / Nkv <= 8 in this build.
+ * D                  64 or 128 in this build.
+ * block_size         > 0, <= 512, a multiple of 16 (16-bit KV) or 32 (int8 KV).
+ * scale              the scaleValue of the pages, usually 1/sqrt(D).
+ * antiquant_scale    device fp32 (2, Nkv, D): [0] for K, [1] for V; required iff kv_dtype is
+ *                    FIA_I8.  Dequantisation is (x - offset) * scale in fp32.
+ * antiquant_offset   device fp32 (2, Nkv, D) or NULL (zero).
+ * sink               device fp32 (Nq) or NULL; not allowed with int8 KV.
+ * softmax_max/sum    device fp32 (B, Nq) or NULL (not written).
+ * num_splits         0 picks the split automatically; n > 0 splits each sequence into at most
+ *                    n chunks of ceil(max_kv_len / n) tokens (rounded up to 64).
+ * workspace          device, at least fia_decode_workspace_size() bytes, 256-byte aligned.
+ *                    Holds the split plan and partials; contents need no initialisation.
+ */
+int fia_decode_workspace_size(int B, int Nq, int Nkv, int D, int max_kv_len, int block_size, int num_splits,
+                              size_t* bytes);
+
+int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache, fia_dtype kv_dtype,
+               const int32_t* block_table, int64_t bt_stride, const int64_t* actual_seq_lengths, int max_kv_len,
+               int B, int Nq, int Nkv, int D, int block_size, int64_t num_blocks, double scale,
+               const float* antiquant_scale, const float* antiquant_offset, const float* sink, void* out,
+               float* softmax_max, float* softmax_sum, int num_splits, void* workspace, size_t workspace_bytes,
+               fia_stream_t stream);
+
+/* ------------------------------------------------------------------------ prefill
+ * FusedInferAttentionScore (prefill mode Q_S > 1, sparseMode 3 rightDownCausal, TND);
+ * aclnnFlashAttentionScoreV4 (TND, cumulative actual_seq_qlen, zero-length sequences).
+ *
+ *   For sequence b with Lq = cu_seqlens_q[b+1] - cu_seqlens_q[b] queries and
+ *   Lkv = cu_seqlens_kv[b+1] - cu_seqlens_kv[b] keys, query i sees key j iff mask == 0, or
+ *   mask == 3 and j <= i + Lkv - Lq (rightDownCausal; lower-triangular when Lq == Lkv).
+ *   Outputs as for decode, per (token, head).
+ *
+ * q, out           device (T, Nq, D) row-major, dtype FIA_BF16 or FIA_F16, 16-byte aligned.
+ * k, v             device (Tkv, Nkv, D) row-major, same dtype, 16-byte aligned.
+ * cu_seqlens_q/kv  device int64 (B + 1), cu[0] = 0, non-decreasing, cu[B] = T (resp. Tkv).
+ * max_seqlen_q/kv  host upper bounds of the per-sequence lengths.
+ * D                128 in this build (64 also accepted); Nq % Nkv == 0.
+ * mask             0 (none) or 3 (rightDownCausal).
+ * sink             device fp32 (Nq) or NULL.
+ * softmax_max/sum  device fp32 (T, Nq) or NULL.
+ * workspace        device, at least fia_prefill_workspace_size() bytes, 256-byte aligned.
+ */
+int fia_prefill_workspace_size(int B, int Nq, int Nkv, int D, int max_seqlen_q, size_t* bytes);
+
+int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, const int64_t* cu_seqlens_q,
+                const int64_t* cu_seqlens_kv, int B, int64_t T, int64_t Tkv, int max_seqlen_q, int max_seqlen_kv,
+                int Nq, int Nkv, int D, double scale, int mask, const float* sink, void* out, float* softmax_max,
+                float* softmax_sum, void* workspace, size_t workspace_bytes, fia_stream_t stream);
+
+/* ---------------------------------------------------------- ring_attention_update
+ * aclnnRingAttentionUpdate ("功能说明 / 计算公式").  Per row r and head n:
+ *   m = max(pm, cm);  wp = ps e^{pm - m};  wc = cs e^{cm - m};  sum = wp + wc;
+ *   out = (prev_out wp + cur_out wc) / sum.
+ * The page prints the formula without the ps / cs factors on the outputs and without cs in
+ * the sum; that form is exact only when both sums are 1.  This library applies the sums,
+ * the form under which merging the partials of any split gives the unsplit result.  A side
+ * with max = -inf weighs 0; if both do, out = 0, max = -inf, sum = 0.
+ *
+ * rows             T for TND, or S * B for SBH (the two layouts are the same elementwise).
+ * prev_out, cur_out, out   device (rows, N, D) in out_dtype (FIA_F32, FIA_F16, FIA_BF16),
+ *                  16-byte aligned.  D % 8 == 0 and D <= 768; N <= 256.
+ * prev/cur_max, prev/cur_sum, max_out, sum_out   device fp32 (rows, N); one value per (row,
+ *                  head) (the pages' trailing axis of 8 equal copies is not stored).
+ * Outputs may alias the prev_* (or cur_*) inputs, so an n-way fold can run in place.
+ */
+int ring_attention_update(const void* prev_out, const float* prev_max, const float* prev_sum, const void* cur_out,
+                          const float* cur_max, const float* cur_sum, fia_dtype out_dtype, int64_t rows, int N,
+                          int D, void* out, float* max_out, float* sum_out, fia_stream_t stream);
+
+/* ------------------------------------------------------------------------- probes
+ * Test hooks for the bit-exact parts of the decode path.  The pages have no
+ * counterpart; they exist so that tests can compare the exact integer and
+ * floating-point steps with the oracle.
+ *
+ * fia_debug_dequant: out[i] = (codes[i] - offset[i]) * scale[i] in fp32 with two roundings,
+ *   through the same device function the attention kernel uses.  All pointers device.
+ * fia_debug_gather: copies the K rows of the first L_b tokens of (b, hkv) into dst (device,
+ *   L_b * D elements of kv_dtype, row-major) through the attention kernel's block-table walk,
+ *   tensor-map tile loads and swizzled addressing.  Other arguments as for fia_decode.
+ */
+int fia_debug_dequant(const int8_t* codes, const float* scale, const float* offset, int64_t n, float* out,
+                      fia_stream_t stream);
+
+int fia_debug_gather(const void* k_cache, fia_dtype kv_dtype, const int32_t* block_table, int64_t bt_stride,
+                     const int64_t* actual_seq_lengths, int max_kv_len, int B, int Nkv, int D, int block_size,
+                     int64_t num_blocks, int b, int hkv, void* dst, fia_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FIA_H_ */

@@ -67,6 +67,10 @@ def _bind(path: str):
     lib.oracle_rau.restype = i32
     lib.oracle_dequant_i8.argtypes = [ctypes.c_int8, ctypes.c_float, ctypes.c_float]
     lib.oracle_dequant_i8.restype = ctypes.c_float
+    lib.oracle_dequant_i8_array.argtypes = [P, P, P, i64, P]
+    lib.oracle_dequant_i8_array.restype = None
+    lib.oracle_gather_rows.argtypes = [P, i32, P, i64, i32, i32, i64, i32, i32, i32, P]
+    lib.oracle_gather_rows.restype = i32
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i32
     return lib
@@ -95,6 +99,27 @@ class Oracle:
     def dequant_i8(self, x: int, offset: float, scale: float) -> float:
         """One fp32 antiquant step, exactly as the oracle's decode uses it."""
         return self._lib.oracle_dequant_i8(int(x), float(offset), float(scale))
+
+    def dequant_i8_array(self, codes, offset, scale):
+        """Element-wise antiquant of int8 codes with per-element fp32 offset and scale."""
+        codes = np.ascontiguousarray(codes, dtype=np.int8)
+        offset = np.ascontiguousarray(np.broadcast_to(offset, codes.shape), dtype=np.float32)
+        scale = np.ascontiguousarray(np.broadcast_to(scale, codes.shape), dtype=np.float32)
+        out = np.zeros(codes.shape, np.float32)
+        self._lib.oracle_dequant_i8_array(_ptr(codes), _ptr(offset), _ptr(scale), codes.size, _ptr(out))
+        return out
+
+    def gather_rows(self, cache, block_table, b, hk, L, block_size):
+        """Stored rows of tokens 0..L-1 of (b, hk) from a paged pool, as raw elements."""
+        cache = np.ascontiguousarray(cache)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        _, Nkv, _, D = cache.shape
+        dst = np.zeros((L, D), cache.dtype)
+        rc = self._lib.oracle_gather_rows(_ptr(cache), cache.dtype.itemsize, _ptr(bt), int(bt.shape[1]), int(b),
+                                          int(hk), int(L), int(Nkv), int(D), int(block_size), _ptr(dst))
+        if rc != 0:
+            raise ValueError("oracle_gather_rows met a negative block index")
+        return dst
 
     def decode(self, q, k_cache, v_cache, seq_lens, *, Nq, Nkv, D, scale, q_dtype=None, kv_dtype=None,
                block_table=None, block_size=0, kv_rows=0, aq_scale=None, aq_offset=None, sink=None,

@@ -99,6 +99,33 @@ float oracle_dequant_i8(int8_t x, float offset, float scale)
     return r;
 }
 
+/* R2 over arrays: out[i] = dequant of x[i] with its own offset and scale. */
+void oracle_dequant_i8_array(const int8_t *x, const float *offset, const float *scale, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_dequant_i8(x[i], offset[i], scale[i]);
+}
+
+/* [IFA] Constraints / page attention, as raw bytes: copies the stored rows of
+ * tokens 0..L-1 of (batch b, kv head hk) out of a (blocknum, KV_N, blocksize, D)
+ * pool into dst (L x D elements of elem_bytes each), token t from block
+ * block_table[b][t / block_size], in-block row t - (t / block_size) * block_size. */
+int oracle_gather_rows(const void *cache, int elem_bytes, const int32_t *block_table, int64_t bt_stride,
+                       int b, int hk, int64_t L, int Nkv, int D, int block_size, void *dst)
+{
+    const int64_t row_bytes = (int64_t)D * elem_bytes;
+    for (int64_t t = 0; t < L; ++t) {
+        const int64_t logical = t / block_size;
+        const int64_t in_block = t - logical * block_size;
+        const int64_t blk = block_table[(int64_t)b * bt_stride + logical];
+        if (blk < 0)
+            return -1;
+        const int64_t row = (blk * Nkv + hk) * block_size + in_block;
+        memcpy((char *)dst + t * row_bytes, (const char *)cache + row * row_bytes, (size_t)row_bytes);
+    }
+    return 0;
+}
+
 /* ---- the attention of one query row over a dense list of visible keys ----
  *
  * [IFA] Function: out = Softmax(scale * q K^T) V, written out as its definition.

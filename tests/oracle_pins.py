@@ -282,6 +282,32 @@ def pin_int8_decode_uses_k_and_v_params(O):
         assert sm[h] == 1.0
 
 
+def pin_dequant_array_matches_numpy(O):
+    """The array form of the antiquant step equals numpy fp32 (x - offset) * scale."""
+    rng = np.random.default_rng(43)
+    codes = np.tile(np.arange(-128, 128, dtype=np.int8), 9)
+    off = rng.uniform(-2, 2, codes.size).astype(np.float32)
+    sc = rng.uniform(0.005, 0.02, codes.size).astype(np.float32)
+    ref = (codes.astype(np.float32) - off) * sc
+    assert np.array_equal(O.dequant_i8_array(codes, off, sc).view(np.uint32), ref.view(np.uint32))
+
+
+def pin_gather_rows_inverts_a_scatter(O):
+    """Scatter a contiguous K into a shuffled pool by hand; the oracle's gather gives it back."""
+    rng = np.random.default_rng(47)
+    Nkv, D, bs, L = 3, 8, 16, 53
+    k = rng.integers(0, 1 << 16, size=(Nkv, L, D)).astype(np.uint16)
+    nblk = (L + bs - 1) // bs
+    perm = rng.permutation(nblk + 4)
+    pool = rng.integers(0, 1 << 16, size=(nblk + 4, Nkv, bs, D)).astype(np.uint16)
+    table = np.full((2, nblk + 2), -1, np.int32)
+    table[1, :nblk] = perm[:nblk]
+    for t in range(L):
+        pool[perm[t // bs], :, t % bs] = k[:, t]
+    for hk in range(Nkv):
+        assert np.array_equal(O.gather_rows(pool, table, 1, hk, L, bs), k[hk])
+
+
 # ------------------------------------------------------------------ split + RingAttentionUpdate
 def _row_partials(O, q, k, v, L, lo, hi, D, sink=None):
     """Decode of one row over keys [lo, hi) of a contiguous cache (1, 1, L, D)."""

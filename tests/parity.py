@@ -1,0 +1,122 @@
+"""Helpers for the GPU parity tests: move seeded inputs to the device, call the
+library through its C interface, and compare with the oracle.
+
+Tolerances (elementwise |gpu - oracle| <= atol + rtol * |oracle|):
+  out   bf16: atol = rtol = 1e-2;  fp16: atol = rtol = 2e-3;  fp32 (RAU): 1e-5
+  max, sum: rtol = 1e-4, plus atol = 1e-5 on max only -- a logit near 0 would make
+  a pure relative bound meaningless; fp32 accumulation of D <= 128 products of
+  O(1) terms times scale <= 1 stays below 1e-5 in absolute terms.
+Integer and byte results (gathered rows, dequantised codes) must be identical.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import fia_workloads as W
+import oracle as OR
+
+OUT_TOL = {W.BF16: (1e-2, 1e-2), W.FP16: (2e-3, 2e-3), "fp32": (1e-5, 1e-5)}
+MAX_TOL = (1e-5, 1e-4)
+SUM_TOL = (0.0, 1e-4)
+
+_TORCH = {W.BF16: torch.bfloat16, W.FP16: torch.float16}
+
+
+def dev_bits(bits: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    """uint16 storage bits -> device tensor of the storage dtype (bit-exact)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+    return t.view(_TORCH[dtype])
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def assert_close(name, got, ref, atol, rtol):
+    """Elementwise bound with -inf == -inf; returns (max abs err, max rel err)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    both_inf = np.isinf(got) & np.isinf(ref) & (np.sign(got) == np.sign(ref))
+    g = np.where(both_inf, 0.0, got)
+    r = np.where(both_inf, 0.0, ref)
+    err = np.abs(g - r)
+    bad = ~(err <= atol + rtol * np.abs(r))
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} outside atol={atol} rtol={rtol}; "
+                             f"first at {tuple(i)}: gpu={got[tuple(i)]!r} oracle={ref[tuple(i)]!r}; "
+                             f"max abs err {float(err.max()):.3g}")
+    rel = err / np.maximum(np.abs(r), 1e-30)
+    return float(err.max()) if err.size else 0.0, float(rel.max()) if rel.size else 0.0
+
+
+# ----------------------------------------------------------------------------- decode
+class DeviceDecode:
+    """A DecodeCase resident on the GPU."""
+
+    def __init__(self, case: W.DecodeCase, device="cuda"):
+        self.case = case
+        self.q = dev_bits(case.q, case.dtype, device)
+        if case.kv_dtype == W.INT8:
+            self.k = torch.from_numpy(case.k_cache).to(device)
+            self.v = torch.from_numpy(case.v_cache).to(device)
+            self.aq_scale = torch.from_numpy(case.aq_scale).to(device)
+            self.aq_offset = torch.from_numpy(case.aq_offset).to(device)
+        else:
+            self.k = dev_bits(case.k_cache, case.kv_dtype, device)
+            self.v = dev_bits(case.v_cache, case.kv_dtype, device)
+            self.aq_scale = self.aq_offset = None
+        self.bt = torch.from_numpy(case.block_table).to(device)
+        self.lens = torch.from_numpy(case.lengths.astype(np.int64)).to(device)
+        self.sink = None if case.sink is None else torch.from_numpy(case.sink).to(device)
+
+
+def run_decode(F, dd: DeviceDecode, num_splits=0, sink="case", max_kv_len=None, lens=None, bt=None):
+    c = dd.case
+    B, Nq = c.B, c.Nq
+    mx = torch.full((B, Nq), float("nan"), dtype=torch.float32, device=dd.q.device)
+    sm = torch.full((B, Nq), float("nan"), dtype=torch.float32, device=dd.q.device)
+    out, mx, sm = F.fia_decode(dd.q, dd.k, dd.v, dd.bt if bt is None else bt, dd.lens if lens is None else lens,
+                               max_kv_len=c.max_len if max_kv_len is None else max_kv_len, num_heads=Nq,
+                               num_kv_heads=c.Nkv, scale=c.scale, antiquant_scale=dd.aq_scale,
+                               antiquant_offset=dd.aq_offset, sink=dd.sink if sink == "case" else sink,
+                               softmax_max=mx, softmax_sum=sm, num_splits=num_splits)
+    return out, mx, sm
+
+
+def oracle_decode(case: W.DecodeCase, rows=None, nthreads=0, sink="case"):
+    code = {W.BF16: OR.BF16, W.FP16: OR.F16}
+    kvc = OR.I8 if case.kv_dtype == W.INT8 else code[case.kv_dtype]
+    return OR.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=case.Nq, Nkv=case.Nkv, D=case.D,
+                     scale=case.scale, q_dtype=code[case.dtype], kv_dtype=kvc, block_table=case.block_table,
+                     block_size=case.block_size, aq_scale=case.aq_scale, aq_offset=case.aq_offset,
+                     sink=case.sink if sink == "case" else sink, rows=rows, nthreads=nthreads)
+
+
+def compare_decode(case: W.DecodeCase, out, mx, sm, rows=None, ref=None):
+    """Compare device results (full tensors) with the oracle on `rows` (b * Nq + h) or all."""
+    if ref is None:
+        ref = oracle_decode(case, rows=rows)
+    o_ref, m_ref, s_ref = ref
+    o = to_f64(out).reshape(case.B * case.Nq, case.D)
+    m = to_f64(mx).reshape(-1)
+    s = to_f64(sm).reshape(-1)
+    if rows is not None:
+        o, m, s = o[rows], m[rows], s[rows]
+    atol, rtol = OUT_TOL[case.dtype]
+    e_out = assert_close("out", o, o_ref, atol, rtol)
+    e_max = assert_close("softmax_max", m, m_ref, *MAX_TOL)
+    e_sum = assert_close("softmax_sum", s, s_ref, *SUM_TOL)
+    return {"out": e_out, "max": e_max, "sum": e_sum}
+
+
+def sample_rows(case: W.DecodeCase, n: int, seed: int = 0) -> np.ndarray:
+    """n random (b * Nq + h) rows plus every head of the shortest and the longest sequence."""
+    rng = np.random.default_rng(seed)
+    total = case.B * case.Nq
+    picks = set(rng.choice(total, size=min(n, total), replace=False).tolist())
+    for b in (int(np.argmin(case.lengths)), int(np.argmax(case.lengths))):
+        picks.update(range(b * case.Nq, (b + 1) * case.Nq))
+    return np.array(sorted(picks), np.int64)

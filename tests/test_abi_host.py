@@ -1,0 +1,75 @@
+"""Host-only checks of the C interface: the library builds and loads, exports
+every function include/fia.h declares, and rejects bad arguments with the
+documented codes before touching a device."""
+import ctypes
+import re
+import subprocess
+
+import pytest
+
+NULLPTR, INVALID = 161001, 161002
+
+
+def test_library_exports_every_declared_function(F, built_lib):
+    names = F.header_functions()
+    assert {"fia_decode", "fia_prefill", "ring_attention_update", "fia_decode_workspace_size",
+            "fia_prefill_workspace_size", "fia_last_error", "fia_device_status"} <= set(names)
+    nm = subprocess.run(["nm", "-D", "--defined-only", built_lib], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\sT\s+(\w+)$", nm.stdout, flags=re.M))
+    missing = [n for n in names if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_library_does_not_link_the_oracle(built_lib):
+    nm = subprocess.run(["nm", "-D", built_lib], capture_output=True, text=True, check=True)
+    assert "oracle_" not in nm.stdout
+    ldd = subprocess.run(["ldd", built_lib], capture_output=True, text=True)
+    assert "liboracle" not in ldd.stdout
+
+
+P = 0x10000  # a non-null, 256-byte aligned fake device address (never dereferenced)
+
+
+def _decode(lib, **kw):
+    a = dict(q=P, q_dtype=2, k=P, v=P, kv_dtype=2, bt=P, bt_stride=4, lens=P, max_kv_len=64, B=2, Nq=4, Nkv=2,
+             D=64, bs=16, num_blocks=8, scale=0.125, aqs=None, aqo=None, sink=None, out=P, mx=None, sm=None,
+             splits=0, ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.fia_decode(a["q"], a["q_dtype"], a["k"], a["v"], a["kv_dtype"], a["bt"], a["bt_stride"], a["lens"],
+                          a["max_kv_len"], a["B"], a["Nq"], a["Nkv"], a["D"], a["bs"], a["num_blocks"], a["scale"],
+                          a["aqs"], a["aqo"], a["sink"], a["out"], a["mx"], a["sm"], a["splits"], a["ws"],
+                          a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), NULLPTR), (dict(k=None), NULLPTR), (dict(bt=None), NULLPTR), (dict(lens=None), NULLPTR),
+    (dict(out=None), NULLPTR), (dict(ws=None), NULLPTR), (dict(kv_dtype=3), NULLPTR),     # int8 without scale
+    (dict(q_dtype=0), INVALID), (dict(q_dtype=3), INVALID), (dict(kv_dtype=1), INVALID),  # fp16 kv, bf16 q
+    (dict(Nq=6, Nkv=4), INVALID), (dict(Nq=32, Nkv=2), INVALID), (dict(Nq=300, Nkv=300), INVALID),
+    (dict(D=96), INVALID), (dict(D=256), INVALID), (dict(bs=0), INVALID), (dict(bs=24), INVALID),
+    (dict(bs=1024), INVALID), (dict(kv_dtype=3, aqs=P, bs=16), INVALID),                  # int8 needs bs % 32
+    (dict(kv_dtype=3, aqs=P, bs=32, sink=P), INVALID),                                      # sink + int8
+    (dict(bt_stride=3), INVALID), (dict(num_blocks=0), INVALID), (dict(B=70000), INVALID),
+    (dict(max_kv_len=-1), INVALID), (dict(splits=-1), INVALID), (dict(scale=float("inf")), INVALID),
+    (dict(q=P + 8), INVALID), (dict(k=P + 2), INVALID), (dict(ws=P + 16), INVALID),
+])
+def test_decode_rejects(F, kw, code):
+    lib = F.library()
+    assert _decode(lib, **kw) == code
+    assert lib.fia_last_error()
+
+
+def test_rau_rejects(F):
+    lib = F.library()
+    assert lib.ring_attention_update(None, P, P, P, P, P, 2, 4, 8, 64, P, P, P, None) == NULLPTR
+    assert lib.ring_attention_update(P, P, P, P, P, P, 3, 4, 8, 64, P, P, P, None) == INVALID
+    assert lib.ring_attention_update(P, P, P, P, P, P, 2, 4, 8, 60, P, P, P, None) == INVALID
+    assert lib.ring_attention_update(P, P, P, P, P, P, 2, 4, 300, 64, P, P, P, None) == INVALID
+    assert lib.ring_attention_update(P, P, P, P, P, P, 2, 4, 8, 776, P, P, P, None) == INVALID
+
+
+def test_workspace_size_needs_output(F):
+    lib = F.library()
+    assert lib.fia_decode_workspace_size(2, 4, 2, 64, 64, 16, 0, None) == NULLPTR
+    n = ctypes.c_size_t(0)
+    assert lib.fia_decode_workspace_size(2, 4, 2, 96, 64, 16, 0, ctypes.byref(n)) == INVALID

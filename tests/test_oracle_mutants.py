@@ -32,6 +32,10 @@ MUTANTS = [
     ("f16_subnormal", "ldexp((double)frac, -24)", "ldexp((double)frac, -25)"),
     ("empty_row_max", "*smax = -INFINITY;\n        *ssum = 0.0;\n        return;",
      "*smax = 0.0;\n        *ssum = 0.0;\n        return;"),
+    ("gather_in_block_row", "const int64_t in_block = t - logical * block_size;",
+     "const int64_t in_block = (t + 1) % block_size;"),
+    ("dequant_array_offset_ignored", "out[i] = oracle_dequant_i8(x[i], offset[i], scale[i]);",
+     "out[i] = oracle_dequant_i8(x[i], 0.0f, scale[i]);"),
     ("prefill_kv_head_index", "const int64_t src = ((cu_kv[b] + j) * Nkv + hk) * D + d;",
      "const int64_t src = ((cu_kv[b] + j) * Nkv + (h % Nkv)) * D + d;"),
 ]
