@@ -52,6 +52,8 @@ def _load() -> ctypes.CDLL:
                          P], i32),
         "ring_attention_update": ([P, P, P, P, P, P, i32, i64, i32, i32, P, P, P, P], i32),
         "fia_debug_dequant": ([P, P, P, i64, P, P], i32),
+        "fia_trace_enable": ([i32], i32),
+        "fia_trace_collect": ([i32, ctypes.POINTER(dbl), ctypes.POINTER(i32)], i32),
         "fia_debug_gather": ([P, i32, P, i64, P, i32, i32, i32, i32, i32, i64, i32, i32, P, P], i32),
     }
     for name, (args, res) in sig.items():
@@ -95,6 +97,20 @@ def _stream(stream) -> Optional[int]:
 
 def dtype_code(t: torch.Tensor) -> int:
     return _TORCH_TO_CODE[t.dtype]
+
+
+KERNEL_DECODE_PLAN, KERNEL_DECODE_ATTENTION, KERNEL_DECODE_MERGE, KERNEL_PREFILL, KERNEL_RAU = 0, 1, 2, 3, 4
+
+
+def fia_trace_enable(on: bool = True) -> None:
+    _check(_lib.fia_trace_enable(1 if on else 0), "fia_trace_enable")
+
+
+def fia_trace_collect(kernel: int) -> Tuple[float, int]:
+    """(summed device ms, launches) of one kernel since the last collect on this thread."""
+    ms, n = ctypes.c_double(0.0), ctypes.c_int(0)
+    _check(_lib.fia_trace_collect(int(kernel), ctypes.byref(ms), ctypes.byref(n)), "fia_trace_collect")
+    return ms.value, n.value
 
 
 def fia_device_status(stream=None) -> int:

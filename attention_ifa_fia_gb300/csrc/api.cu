@@ -9,6 +9,8 @@
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "fia.h"
 #include "fia_internal.h"
@@ -153,11 +155,72 @@ int check_decode_shape(int B, int Nq, int* Nkv, int D, int max_kv_len, int block
   return FIA_SUCCESS;
 }
 
+// ---------------------------------------------------------------- launch tracer
+struct TraceState {
+  bool on = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> marks[fia::kKernelCount];
+  cudaEvent_t pending[fia::kKernelCount] = {};
+  std::vector<cudaEvent_t> pool;
+};
+thread_local TraceState g_trace;
+
+cudaEvent_t trace_event() {
+  if (!g_trace.pool.empty()) {
+    cudaEvent_t e = g_trace.pool.back();
+    g_trace.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
 }  // namespace
+
+namespace fia {
+void trace_mark(int kernel, int phase, cudaStream_t stream) {
+  if (!g_trace.on || kernel < 0 || kernel >= kKernelCount) return;
+  cudaEvent_t e = trace_event();
+  if (!e) return;
+  cudaEventRecord(e, stream);
+  if (phase == 0) {
+    g_trace.pending[kernel] = e;
+  } else if (g_trace.pending[kernel]) {
+    g_trace.marks[kernel].emplace_back(g_trace.pending[kernel], e);
+    g_trace.pending[kernel] = nullptr;
+  }
+}
+}  // namespace fia
 
 extern "C" {
 
 const char* fia_last_error(void) { return g_err; }
+
+int fia_trace_enable(int on) {
+  g_trace.on = on != 0;
+  return ok();
+}
+
+int fia_trace_collect(int kernel, double* total_ms, int* launches) {
+  if (!total_ms || !launches) return fail(FIA_ERR_PARAM_NULLPTR, "total_ms and launches are required");
+  if (kernel < 0 || kernel >= fia::kKernelCount) return fail(FIA_ERR_PARAM_INVALID, "unknown kernel id %d", kernel);
+  double tot = 0.0;
+  int n = 0;
+  for (auto& pr : g_trace.marks[kernel]) {
+    cudaError_t e = cudaEventSynchronize(pr.second);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, pr.first, pr.second);
+    if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "trace events: %s", cudaGetErrorString(e));
+    tot += ms;
+    ++n;
+    g_trace.pool.push_back(pr.first);
+    g_trace.pool.push_back(pr.second);
+  }
+  g_trace.marks[kernel].clear();
+  *total_ms = tot;
+  *launches = n;
+  return ok();
+}
 
 int fia_device_status(fia_stream_t stream, unsigned int* flags) {
   if (!flags) return fail(FIA_ERR_PARAM_NULLPTR, "flags is NULL");

@@ -600,7 +600,9 @@ cudaError_t launch_attention(const DecodeParams& p, const CUtensorMap& tmK, cons
   auto kern = decode_splitkv_kernel<KVT, D, GP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  trace_mark(kKernelDecodeAttention, 0, stream);
   kern<<<grid, kThreads, smem, stream>>>(tmK, tmV, p, box_rows);
+  trace_mark(kKernelDecodeAttention, 1, stream);
   return cudaGetLastError();
 }
 
@@ -646,7 +648,9 @@ DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D,
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows,
                           int num_sms, cudaStream_t stream) {
+  trace_mark(kKernelDecodePlan, 0, stream);
   decode_plan_kernel<<<1, 1024, 0, stream>>>(p);
+  trace_mark(kKernelDecodePlan, 1, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int grid = num_sms;
@@ -663,6 +667,7 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const C
   if (e != cudaSuccess) return e;
   const int max_chunks = (p.max_kv_len + p.chunk_tokens - 1) / p.chunk_tokens;
   const size_t msmem = sizeof(float) * (size_t)p.G * (max_chunks > 0 ? max_chunks : 1);
+  trace_mark(kKernelDecodeMerge, 0, stream);
   if (p.q_dtype == kBF16) {
     if (msmem > 48 * 1024)
       cudaFuncSetAttribute(decode_merge_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
@@ -672,6 +677,7 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const C
       cudaFuncSetAttribute(decode_merge_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
     decode_merge_kernel<kF16><<<p.B * p.Nkv, 256, msmem, stream>>>(p);
   }
+  trace_mark(kKernelDecodeMerge, 1, stream);
   return cudaGetLastError();
 }
 

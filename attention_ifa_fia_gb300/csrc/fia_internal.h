@@ -20,6 +20,14 @@ enum : unsigned int {
   kStatusBadSeqlens = 1u << 3,     // cumulative sequence lengths not monotone / out of range
 };
 
+// kernels known to the launch tracer (fia_trace_enable / fia_trace_collect)
+enum : int { kKernelDecodePlan = 0, kKernelDecodeAttention = 1, kKernelDecodeMerge = 2, kKernelPrefill = 3,
+             kKernelRau = 4, kKernelCount = 5 };
+
+// Records a CUDA event on `stream` before (phase 0) or after (phase 1) a launch
+// of `kernel` when tracing is enabled on the calling thread; otherwise nothing.
+void trace_mark(int kernel, int phase, cudaStream_t stream);
+
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
 

@@ -135,6 +135,7 @@ cudaError_t launch_rau(const void* prev_out, const float* prev_max, const float*
   if (groups == 0) return cudaSuccess;
   int64_t blocks = (groups + 15) / 16;  // 8 warps, up to 2 groups per warp
   if (blocks > 152 * 16) blocks = 152 * 16;
+  trace_mark(kKernelRau, 0, stream);
   if (out_dtype == kF32)
     rau_kernel<kF32><<<(int)blocks, 256, 0, stream>>>(prev_out, prev_max, prev_sum, cur_out, cur_max, cur_sum,
                                                        groups, D, out, max_out, sum_out);
@@ -144,6 +145,7 @@ cudaError_t launch_rau(const void* prev_out, const float* prev_max, const float*
   else
     rau_kernel<kBF16><<<(int)blocks, 256, 0, stream>>>(prev_out, prev_max, prev_sum, cur_out, cur_max, cur_sum,
                                                         groups, D, out, max_out, sum_out);
+  trace_mark(kKernelRau, 1, stream);
   return cudaGetLastError();
 }
 

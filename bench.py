@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Benchmark of the fused inference attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one fia_decode call (split plan, split-KV attention, merge) over the
+whole bf16 paged GQA decode workload: B 32, Nq 32, Nkv 8, D 128, query length 1,
+KV lengths U[1, 4096] (seeded), blockSize 128, shuffled block table.  Inputs are
+resident in HBM and rotated over 4 copies (4 x 268 MB of KV > the 126 MB L2), so
+no step reads KV left in L2 by the previous one.
+
+The JSON line reports the KV-read throughput (algorithmic bytes / time, GB/s)
+as `value`, with queries/s and the fraction of the measured HBM copy bandwidth.
+`roofline` is for the split-KV attention kernel, timed by CUDA events that the
+library records around each of its launches (fia_trace_enable) during the timed
+region.  `e2e` repeats the measurement through the public API with the per-step
+inputs (query, block table, lengths) copied from pinned host memory and the
+results (out, softmax max/sum) copied back inside the timed region; the KV cache
+stays resident, as it does across decode steps.  `cpu_baseline` times the fp64
+oracle on the host cores over a bounded sample of the same workload.
+
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(weak scaling; decode batches are independent, so no data is exchanged); the
+time is the max over ranks.  --impl reference times the oracle alone (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import fia_workloads as W  # noqa: E402
+
+METRIC = "paged decode attn KV-read GB/s (% HBM peak), queries/s; prefill TFLOP/s"
+COPIES = 4
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- workload arithmetic
+def decode_bytes(case: W.DecodeCase) -> dict:
+    """Algorithmic bytes of one decode step: every visible K/V element once, q, out,
+    the block-table entries in use, the lengths, antiquant params, sink and max/sum."""
+    L = case.lengths.astype(np.int64)
+    kv = int(L.sum()) * 2 * case.Nkv * case.D * case.kv_elem_bytes
+    qo = 2 * case.B * case.Nq * case.D * 2
+    bt = int(((L + case.block_size - 1) // case.block_size).sum()) * 4
+    aux = case.B * 8 + 2 * case.B * case.Nq * 4
+    if case.aq_scale is not None:
+        aux += 2 * case.aq_scale.size * 4
+    if case.sink is not None:
+        aux += case.Nq * 4
+    return {"kv": kv, "total": kv + qo + bt + aux}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []  # (host time, sm, max, power, reasons)
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm, mx = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            reasons = [n for n, v in zip(names, parts[3:7]) if v.lower().startswith("active")]
+            self.samples.append((time.time(), sm, mx, parts[2], reasons))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1, pad=1.0):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed region"
+        if len(inside) < 3:
+            inside = [s for s in self.samples if t0 - pad <= s[0] <= t1 + 0.2]
+            window = "timed region and the last second of warm-up"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none sampled"}
+        reasons = sorted({r for s in inside for r in s[4]})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_decode_sample(case: W.DecodeCase, groups):
+    """Run the oracle on every query head of the (b, kv-head) groups given; returns
+    (seconds, algorithmic bytes of that sample, threads)."""
+    import oracle
+    G = case.Nq // case.Nkv
+    rows = np.array([b * case.Nq + hk * G + g for (b, hk) in groups for g in range(G)], np.int64)
+    code = {W.BF16: oracle.BF16, W.FP16: oracle.F16}
+    kvc = oracle.I8 if case.kv_dtype == W.INT8 else code[case.kv_dtype]
+    t = time.perf_counter()
+    oracle.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=case.Nq, Nkv=case.Nkv, D=case.D,
+                  scale=case.scale, q_dtype=code[case.dtype], kv_dtype=kvc, block_table=case.block_table,
+                  block_size=case.block_size, aq_scale=case.aq_scale, aq_offset=case.aq_offset, sink=case.sink,
+                  rows=rows)
+    dt = time.perf_counter() - t
+    kvb = sum(int(case.lengths[b]) for (b, _) in groups) * 2 * case.D * case.kv_elem_bytes
+    nbytes = kvb + len(rows) * case.D * 2 * 2 + len(rows) * 8
+    return dt, nbytes, oracle.max_threads()
+
+
+def cpu_baseline(case: W.DecodeCase, budget_s: float = 15.0, seed: int = 0):
+    rng = np.random.default_rng(seed)
+    all_groups = [(b, h) for b in range(case.B) for h in range(case.Nkv)]
+    order = rng.permutation(len(all_groups))
+    probe = [all_groups[i] for i in order[:4]]
+    dt, nb, cores = oracle_decode_sample(case, probe)
+    per_group = max(dt / len(probe), 1e-4)
+    n = int(min(len(all_groups), max(4, budget_s / per_group)))
+    groups = [all_groups[i] for i in order[:n]]
+    # whole passes are repeated (up to 20) until the budget is spent, for a stable figure
+    dt, nb, passes = 0.0, 0, 0
+    while passes < 20 and (passes == 0 or (n == len(all_groups) and dt < budget_s)):
+        t, b, cores = oracle_decode_sample(case, groups)
+        dt, nb, passes = dt + t, nb + b, passes + 1
+    what = "the whole workload" if n == len(all_groups) else f"{n} of {len(all_groups)} (batch, kv-head) groups"
+    return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{what} x {passes} pass(es), all {case.Nq // case.Nkv} query heads per group; "
+                      f"{dt:.1f} s of fp64 CPU work", "seconds": round(dt, 2)}
+
+
+# ----------------------------------------------------------------------------- our implementation
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import attention_ifa_fia_gb300 as F
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from parity import DeviceDecode
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    make = W.WORKLOADS[args.workload]
+    seed = 1001 + 97 * rank if args.workload == "bf16_gqa_decode" else None
+    case = make(seed) if seed is not None else make()
+    nbytes = decode_bytes(case)
+    copies = [DeviceDecode(case, dev) for _ in range(COPIES)]
+    num_splits = W.LONG_CTX_CHUNKS if args.workload == "long_ctx_sink_decode" else 0
+    ws_bytes = F.fia_decode_workspace_size(case.B, case.Nq, case.Nkv, case.D, case.max_len, case.block_size,
+                                           num_splits)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((case.B, case.Nq, case.D), dtype=copies[0].q.dtype, device=dev)
+    mx = torch.empty((case.B, case.Nq), dtype=torch.float32, device=dev)
+    sm = torch.empty_like(mx)
+
+    def step(i):
+        c = copies[i % COPIES]
+        F.fia_decode(c.q, c.k, c.v, c.bt, c.lens, max_kv_len=case.max_len, num_heads=case.Nq,
+                     num_kv_heads=case.Nkv, scale=case.scale, antiquant_scale=c.aq_scale,
+                     antiquant_offset=c.aq_offset, sink=c.sink, out=out, softmax_max=mx, softmax_sum=sm,
+                     num_splits=num_splits, workspace=ws)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    # warm-up: at least W steps and at least one second of load
+    t_w = time.time()
+    i = 0
+    while i < args.warmup or time.time() - t_w < args.min_warmup_s:
+        step(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    F.fia_device_status()
+
+    # ---- timed region: exactly K steps
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    F.fia_trace_enable(True)
+    for k in (F.KERNEL_DECODE_PLAN, F.KERNEL_DECODE_ATTENTION, F.KERNEL_DECODE_MERGE):
+        F.fia_trace_collect(k)
+    h0 = time.time()
+    e0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    barrier()
+    F.fia_trace_enable(False)
+    ms = e0.elapsed_time(e1)
+    kern = {name: F.fia_trace_collect(kid) for name, kid in
+            (("plan", F.KERNEL_DECODE_PLAN), ("attention", F.KERNEL_DECODE_ATTENTION),
+             ("merge", F.KERNEL_DECODE_MERGE))}
+    status = F.fia_device_status()
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API with host buffers
+    pin_q = [torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory() for c in copies]
+    pin_bt = [torch.empty(c.bt.shape, dtype=c.bt.dtype).pin_memory() for c in copies]
+    pin_len = [torch.empty(c.lens.shape, dtype=c.lens.dtype).pin_memory() for c in copies]
+    for j, c in enumerate(copies):
+        pin_q[j].copy_(c.q)
+        pin_bt[j].copy_(c.bt)
+        pin_len[j].copy_(c.lens)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_mx = torch.empty(mx.shape, dtype=mx.dtype).pin_memory()
+    h_sm = torch.empty(sm.shape, dtype=sm.dtype).pin_memory()
+    h2d = pin_q[0].numel() * pin_q[0].element_size() + pin_bt[0].numel() * 4 + pin_len[0].numel() * 8
+    d2h = h_out.numel() * h_out.element_size() + 2 * h_mx.numel() * 4
+
+    def e2e_step(i):
+        j = i % COPIES
+        c = copies[j]
+        c.q.copy_(pin_q[j], non_blocking=True)
+        c.bt.copy_(pin_bt[j], non_blocking=True)
+        c.lens.copy_(pin_len[j], non_blocking=True)
+        step(i)
+        h_out.copy_(out, non_blocking=True)
+        h_mx.copy_(mx, non_blocking=True)
+        h_sm.copy_(sm, non_blocking=True)
+
+    for k in range(min(args.warmup, 20)):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for k in range(args.steps):
+        e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    sampler.stop()
+
+    if rank != 0:
+        return None
+    hbm, tf_burst, tf_sus, src = peaks()
+    steps = args.steps
+    gbs = world * nbytes["total"] * steps / (ms / 1e3) / 1e9
+    att_ms, att_n = kern["attention"]
+    achieved = nbytes["total"] / (att_ms / att_n / 1e3) / 1e9 if att_n else None
+    traffic = load_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if case.dtype == W.BF16 else "f16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": case.B, "Nq": case.Nq, "Nkv": case.Nkv, "D": case.D,
+                   "block_size": case.block_size, "kv_dtype": case.kv_dtype,
+                   "kv_lengths": f"seeded (sum {int(case.lengths.sum())}, max {case.max_len})",
+                   "kv_bytes_per_step": nbytes["kv"], "algorithmic_bytes_per_step": nbytes["total"],
+                   "l2": f"inputs rotated over {COPIES} device copies ({COPIES} x {nbytes['kv'] / 1e6:.0f} MB of KV > L2)",
+                   "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"},
+        "hbm_frac_of_measured": round(gbs / world / hbm, 4),
+        "queries_per_s": round(world * case.B * steps / (ms / 1e3), 1),
+        "head_queries_per_s": round(world * case.B * case.Nq * steps / (ms / 1e3), 1),
+        "kernels_ms_per_launch": {k: round(v[0] / v[1], 5) if v[1] else None for k, v in kern.items()},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None, "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4) if achieved else None,
+                     "traffic": traffic, "kernel": "decode_splitkv (split-KV attention)",
+                     "peak_source": f"{src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                     else "fallback 6.8 TB/s"},
+        "e2e": {"value": round(world * nbytes["total"] * steps / (ms_e2e / 1e3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "per step: q, block table, lengths host->device; out, max, sum device->host; "
+                        "KV cache resident"},
+        "gpu_launches": sum(v[1] for v in kern.values()),
+        "device_status": status,
+        "clocks": sampler.summary(h0, h1),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    return line
+
+
+def load_traffic(workload):
+    """DRAM bytes (read + write) per launch of the attention kernel from the committed ncu
+    summary, or None if that summary was taken on a different version of the kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    src = os.path.join(ROOT, "attention_ifa_fia_gb300", "csrc", "decode.cu")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        with open(src, "rb") as f:
+            sha = hashlib.sha1(f.read()).hexdigest()[:12]
+        return d.get(workload) if d.get("decode.cu sha1 prefix") == sha else None
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- reference arm: the oracle
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    case = W.WORKLOADS[args.workload]()
+    rng = np.random.default_rng(0)
+    all_groups = [(b, h) for b in range(case.B) for h in range(case.Nkv)]
+    probe = [all_groups[i] for i in rng.permutation(len(all_groups))[:2]]
+    dt, _, _ = oracle_decode_sample(case, probe)
+    per_group = max(dt / len(probe), 1e-4)
+    budget = 120.0 / max(args.steps + args.warmup, 1)
+    n = int(min(len(all_groups), max(1, budget / per_group)))
+    tot_t, tot_b, cores = 0.0, 0, 1
+    for k in range(args.warmup + args.steps):
+        idx = rng.permutation(len(all_groups))[:n]
+        dt, nb, cores = oracle_decode_sample(case, [all_groups[i] for i in idx])
+        if k >= args.warmup:
+            tot_t += dt
+            tot_b += nb
+    value = tot_b / tot_t / 1e9
+    sample = f"each step: {n} of {len(all_groups)} (batch, kv-head) groups of {args.workload}, all query heads"
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload}, "impl": "reference",
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bf16_gqa_decode",
+                    choices=["bf16_gqa_decode", "int8_antiquant_decode", "long_ctx_sink_decode", "tiny_decode"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+                    help="keep warming up for at least this long (clocks settle, the sampler sees load)")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

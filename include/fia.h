@@ -67,6 +67,21 @@ const char* fia_last_error(void);
  * clears them.  Returns 0, or 361001 if the synchronisation itself failed. */
 int fia_device_status(fia_stream_t stream, unsigned int* flags);
 
+/* Launch tracing.  While enabled on the calling thread, every launch of one of the
+ * library's kernels is bracketed by two CUDA events recorded on the launching stream.
+ * fia_trace_collect synchronises on the recorded events, returns the summed device time
+ * (ms) and the number of launches of one kernel since the previous collect, and forgets
+ * them.  Kernel ids: */
+enum {
+  FIA_KERNEL_DECODE_PLAN = 0,      /* per-call split plan (one CTA) */
+  FIA_KERNEL_DECODE_ATTENTION = 1, /* split-KV attention over the paged cache */
+  FIA_KERNEL_DECODE_MERGE = 2,     /* merge of split partials, sink, outputs */
+  FIA_KERNEL_PREFILL = 3,          /* TND prefill */
+  FIA_KERNEL_RAU = 4               /* ring_attention_update */
+};
+int fia_trace_enable(int on);
+int fia_trace_collect(int kernel, double* total_ms, int* launches);
+
 /* ------------------------------------------------------------------------- decode
  * aclnnIncreFlashAttentionV3 ("Function", parameter table, "Constraints / page
  * attention"); FusedInferAttentionScore (learnableSink, softmax max/sum for ring
