@@ -116,7 +116,7 @@ struct DecodePlan {
 // chunk is sized so that the upper bound of the work (every sequence at
 // max_kv_len) gives about 12 items per SM, between one tile and 8192 tokens.
 int plan_decode(int B, int Nkv, int max_kv_len, int num_splits, int num_sms, DecodePlan* plan) {
-  const int64_t T = fia::kDecodeTile;
+  const int64_t T = fia::kDecodeTileTC;  // items are whole tiles of either attention kernel
   int64_t c;
   if (num_splits > 0) {
     c = ((int64_t)max_kv_len + num_splits - 1) / num_splits;
@@ -146,7 +146,8 @@ int check_decode_shape(int B, int Nq, int* Nkv, int D, int max_kv_len, int block
   if (*Nkv == 0) *Nkv = Nq;
   if (*Nkv < 0 || Nq % *Nkv != 0)
     return fail(FIA_ERR_PARAM_INVALID, "Nq = %d is not a multiple of Nkv = %d", Nq, *Nkv);
-  if (Nq / *Nkv > 8) return fail(FIA_ERR_PARAM_INVALID, "GQA group %d > 8 is not supported in this build", Nq / *Nkv);
+  if (Nq / *Nkv > 16)
+    return fail(FIA_ERR_PARAM_INVALID, "GQA group %d > 16 is not supported in this build", Nq / *Nkv);
   if (D != 64 && D != 128) return fail(FIA_ERR_PARAM_INVALID, "D = %d not supported (64 or 128)", D);
   if (block_size <= 0 || block_size > 512 || block_size % 16 != 0)
     return fail(FIA_ERR_PARAM_INVALID, "block_size = %d must be a multiple of 16 in (0, 512]", block_size);
@@ -269,6 +270,8 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
   if (int rc = check_decode_shape(B, Nq, &Nkv, D, max_kv_len, block_size, num_splits)) return rc;
   if (kv_dtype == FIA_I8 && block_size % 32 != 0)
     return fail(FIA_ERR_PARAM_INVALID, "int8 KV needs block_size %% 32 == 0 (got %d)", block_size);
+  if (kv_dtype == FIA_I8 && Nq / Nkv > 8)
+    return fail(FIA_ERR_PARAM_INVALID, "int8 KV supports GQA groups up to 8 in this build (got %d)", Nq / Nkv);
   if (kv_dtype == FIA_I8 && sink)
     return fail(FIA_ERR_PARAM_INVALID, "the learnable sink is supported only without KV quantisation");
   if (bt_stride < 1 || (int64_t)max_kv_len > bt_stride * block_size)
@@ -320,14 +323,19 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
   p.ws = fia::decode_workspace_carve(workspace, B, Nkv, G, D, plan.max_items);
   p.status = d->status;
 
+  // 16-bit KV runs on the tensor-core kernel (128-token tiles); int8 KV on the CUDA-core one.
+  const bool tc = kv_dtype != FIA_I8;
   const int elem = kv_dtype == FIA_I8 ? 1 : 2;
   const uint32_t box_cols = (uint32_t)std::min(D * elem, 128) / elem;
-  const int box_rows = gcd(block_size, fia::kDecodeTile);
+  const int box_rows = gcd(block_size, tc ? fia::kDecodeTileTC : fia::kDecodeTile);
   const uint64_t rows = (uint64_t)num_blocks * Nkv * block_size;
-  CUtensorMap tmK, tmV;
+  CUtensorMap tmK, tmV, tmQ;
   if (int rc = make_tmap(&tmK, k_cache, kv_dtype, D, rows, box_cols, box_rows)) return rc;
   if (int rc = make_tmap(&tmV, v_cache, kv_dtype, D, rows, box_cols, box_rows)) return rc;
-  cudaError_t e = fia::launch_decode(p, tmK, tmV, box_rows, d->num_sms, stream);
+  if (tc) {
+    if (int rc = make_tmap(&tmQ, q, q_dtype, D, (uint64_t)B * Nq, 64, 16)) return rc;
+  }
+  cudaError_t e = fia::launch_decode(p, tmK, tmV, tc ? &tmQ : nullptr, box_rows, d->num_sms, stream);
   if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "decode launch: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -646,15 +646,17 @@ DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D,
   return w;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows,
-                          int num_sms, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream) {
   trace_mark(kKernelDecodePlan, 0, stream);
   decode_plan_kernel<<<1, 1024, 0, stream>>>(p);
   trace_mark(kKernelDecodePlan, 1, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int grid = num_sms;
-  if (p.kv_dtype == kBF16) {
+  if (tmQ) {
+    e = launch_decode_tc_attention(p, tmK, tmV, *tmQ, box_rows, grid, stream);
+  } else if (p.kv_dtype == kBF16) {
     e = (p.D == 64) ? launch_attention_g<kBF16, 64>(p, tmK, tmV, box_rows, grid, stream)
                     : launch_attention_g<kBF16, 128>(p, tmK, tmV, box_rows, grid, stream);
   } else if (p.kv_dtype == kF16) {

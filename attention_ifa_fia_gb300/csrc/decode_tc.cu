@@ -1,0 +1,464 @@
+// decode_tc.cu -- paged GQA decode attention on tcgen05 tensor cores (fp16 / bf16 KV).
+//
+// Same operator, plan, work items, partial format and merge as decode.cu (see the
+// header there); only the attention kernel differs.  Per 128-token tile of one
+// (b, kv-head) work item, the whole GQA group is computed by two MMAs with the
+// tokens on the M dimension ("swap AB"), so that a group of G <= 16 query heads
+// only pads N to 16:
+//
+//   S^T [128 tok x 16] = K [128 x D] . Q^T          A = K tile (K-major, TMA 128B swizzle)
+//                                                    B = Q rows of the group (K-major)
+//   O^T [D x 16]       = V^T [D x 128] . P^T         A = V tile read MN-major
+//                                                    B = P^T written by the softmax warps
+//
+// Both accumulators live in tensor memory (double buffered).  For D = 64 the PV
+// product uses M = 128 by stacking the two 64-token halves of the V tile as the
+// two halves of A (rows 0-63: tokens 0-63, rows 64-127: tokens 64-127) and issuing
+// one MMA per half against the matching half of P^T into separate accumulators.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads (Q of each item, K and V tiles
+// into a 3- or 5-stage ring); warp 1 allocates tensor memory and one thread issues
+// the MMAs; warps 2-5 own TMEM lanes 0-127: online softmax of tile j (one token per
+// lane, warp-shuffle max across lanes) followed by the rescale-and-accumulate of
+// the PV result of tile j-1 (one output channel per lane).
+#include "fia_device.cuh"
+
+namespace fia {
+namespace {
+
+constexpr int kT = 128;          // tokens per tile: the M of the score MMA
+constexpr int kNP = 16;          // query heads per group, padded: the N of both MMAs
+constexpr int kTmemCols = 128;
+constexpr int kThreadsTC = 192;
+constexpr int kBarCompute = 2;   // named barrier of the 128 softmax/correction threads
+
+template <int D>
+struct TcCfg {
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kNumBoxes = kRowBytes / 128;  // 64-element column boxes per row
+  static constexpr int kTileBytes = kT * kRowBytes;   // K or V tile
+  static constexpr int kStages = (D == 128) ? 3 : 5;
+  static constexpr int kQBytes = kNP * kRowBytes;
+  static constexpr int kPBytes = kNP * kT * 2;
+  static constexpr int kKSteps = D / 16;
+  static constexpr bool kStacked = (D == 64);
+  static constexpr uint32_t kColS = 0;                       // S buffers: [0, 32)
+  static constexpr uint32_t kColO = 32;                      // O buffers: [32, 64) or [32, 96)
+  static constexpr uint32_t kOStride = kStacked ? 32 : 16;   // columns per O buffer
+};
+
+struct __align__(16) TileMeta {
+  int b, hkv, tok0, n;
+  int item, first, last, qbuf;
+};
+
+template <int D>
+struct TcSmem {
+  using C = TcCfg<D>;
+  alignas(1024) uint8_t kv[C::kStages][2][C::kTileBytes];
+  alignas(1024) uint8_t q[2][C::kQBytes];
+  alignas(1024) uint8_t p[2][C::kPBytes];
+  float red[2][4][kNP];
+  float lsum[4][kNP];
+  float accx[C::kStacked ? 64 : 1][kNP];
+  TileMeta meta[C::kStages];
+  uint64_t kv_full[C::kStages], kv_empty[C::kStages];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2], p_free[2];
+  uint64_t o_full[2], o_free[2];
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ int64_t tc_pool_row(int32_t blk, int t, int bs, int Nkv, int hkv) {
+  return ((int64_t)blk * Nkv + hkv) * bs + (t % bs);
+}
+
+// Offset of element (row g, token t) of the P^T operand: two 64-token slabs of
+// 16 rows x 128 bytes, 128-byte swizzle (8-row atoms of 1 KB).
+__device__ __forceinline__ uint32_t p_offset(int g, int t) {
+  const uint32_t slab = t >> 6, col = (t & 63) * 2;
+  const uint32_t off = (uint32_t)g * 128 + col;  // within the slab (rows of 128 B)
+  return slab * (kNP * 128) + swz(off, 7);
+}
+
+template <int D, int DT, int GP>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmQ, const DecodeParams p, const int box_rows) {
+  using C = TcCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  TcSmem<D>& sm = *reinterpret_cast<TcSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.G;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.q_full[i], 1);
+      mbar_init(&sm.q_empty[i], 1);
+      mbar_init(&sm.s_full[i], 1);
+      mbar_init(&sm.s_free[i], 4);
+      mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.p_free[i], 1);
+      mbar_init(&sm.o_full[i], 1);
+      mbar_init(&sm.o_free[i], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmQ);
+    }
+    const int n_items = *p.ws.n_items;
+    const int bs = p.block_size;
+    const uint32_t piece_bytes = (uint32_t)box_rows * C::kRowBytes;
+    int j = 0, local_item = 0;
+    bool ok = true;
+    int next = 0;
+    if (lane == 0) next = atomicAdd(p.ws.counter, 1);
+    next = __shfl_sync(0xffffffffu, next, 0);
+    while (ok && next < n_items) {
+      const int item = next;
+      const int4 desc = p.ws.items[item];
+      if (lane == 0) next = atomicAdd(p.ws.counter, 1);
+      next = __shfl_sync(0xffffffffu, next, 0);
+      const int b = desc.x, hkv = desc.y, t_begin = desc.z, t_end = desc.w;
+      const int qb = local_item & 1;
+      if (!mbar_wait(&sm.q_empty[qb], ((local_item >> 1) & 1) ^ 1u, p.status)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sm.q_full[qb], C::kQBytes);
+        const int32_t row = b * p.Nq + hkv * G;
+        for (int bx = 0; bx < C::kNumBoxes; ++bx)
+          tma_load_2d(sm.q[qb] + bx * (kNP * 128), &tmQ, bx * 64, row, &sm.q_full[qb]);
+      }
+      const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
+      for (int tok0 = t_begin; tok0 < t_end; tok0 += kT, ++j) {
+        const int st = j % C::kStages;
+        const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
+        const int n = min(kT, t_end - tok0);
+        const int npieces = (n + box_rows - 1) / box_rows;
+        int32_t blk = 0;
+        bool valid = false;
+        if (lane < npieces) {
+          blk = bt_row[(tok0 + lane * box_rows) / bs];
+          valid = blk >= 0 && (int64_t)blk < p.num_blocks;
+          if (!valid) raise_status(p.status, kStatusBadBlockIndex);
+        }
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        const uint32_t bytes = 2u * piece_bytes * __popc(vmask);
+        if (!mbar_wait(&sm.kv_empty[st], ph ^ 1u, p.status)) { ok = false; break; }
+        if (lane == 0) {
+          TileMeta& m = sm.meta[st];
+          m.b = b; m.hkv = hkv; m.tok0 = tok0; m.n = n;
+          m.item = item; m.first = (tok0 == t_begin); m.last = (tok0 + kT >= t_end); m.qbuf = qb;
+          if (bytes) mbar_arrive_expect_tx(&sm.kv_full[st], bytes);
+          else mbar_arrive(&sm.kv_full[st]);
+        }
+        __syncwarp();
+        if (valid) {
+          const int64_t row = tc_pool_row(blk, tok0 + lane * box_rows, bs, p.Nkv, hkv);
+          for (int bx = 0; bx < C::kNumBoxes; ++bx) {
+            const uint32_t off = bx * (kT * 128) + lane * box_rows * 128;
+            tma_load_2d(sm.kv[st][0] + off, &tmK, bx * 64, (int32_t)row, &sm.kv_full[st]);
+            tma_load_2d(sm.kv[st][1] + off, &tmV, bx * 64, (int32_t)row, &sm.kv_full[st]);
+          }
+        }
+      }
+      ++local_item;
+    }
+    if (ok) {  // sentinel tile: no more work
+      const int st = j % C::kStages;
+      if (mbar_wait(&sm.kv_empty[st], ((uint32_t)(j / C::kStages) & 1u) ^ 1u, p.status) && lane == 0) {
+        sm.meta[st].item = -1;
+        mbar_arrive(&sm.kv_full[st]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = umma_idesc_f16(DT == kBF16, 0, 0, kT, kNP);
+      constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 1, 0, kT, kNP);
+      int local_item = 0;
+      auto issue_pv = [&](int jj) -> bool {
+        const int pb = jj & 1;
+        const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
+        if (!mbar_wait(&sm.p_full[pb], ph, p.status)) return false;
+        if (!mbar_wait(&sm.o_free[pb], ph ^ 1u, p.status)) return false;
+        tc_fence_after();
+        const int st = jj % C::kStages;
+        const uint32_t vbase = smem_u32(sm.kv[st][1]);
+        const uint32_t pbase = smem_u32(sm.p[pb]);
+        const uint32_t ocol = tmem + C::kColO + pb * C::kOStride;
+        if constexpr (!C::kStacked) {
+#pragma unroll
+          for (int s = 0; s < kT / 16; ++s) {
+            const uint64_t a = umma_desc(vbase + s * 16 * 128, kT * 128, 1024);
+            const uint64_t bd = umma_desc(pbase + (s >> 2) * (kNP * 128) + (s & 3) * 32, 16, 1024);
+            umma_f16(ocol, a, bd, idesc_pv, s > 0);
+          }
+        } else {
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint64_t a = umma_desc(vbase + s * 16 * 128, 64 * 128, 1024);
+            const uint64_t b0 = umma_desc(pbase + s * 32, 16, 1024);
+            const uint64_t b1 = umma_desc(pbase + kNP * 128 + s * 32, 16, 1024);
+            umma_f16(ocol, a, b0, idesc_pv, s > 0);
+            umma_f16(ocol + 16, a, b1, idesc_pv, s > 0);
+          }
+        }
+        umma_commit(&sm.o_full[pb]);
+        umma_commit(&sm.p_free[pb]);
+        umma_commit(&sm.kv_empty[st]);
+        return true;
+      };
+      int j = 0;
+      bool ok = true;
+      while (true) {
+        const int st = j % C::kStages;
+        if (!mbar_wait(&sm.kv_full[st], (uint32_t)(j / C::kStages) & 1u, p.status)) { ok = false; break; }
+        const TileMeta meta = sm.meta[st];
+        if (meta.item < 0) {
+          if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+          mbar_arrive(&sm.s_full[j & 1]);  // lets the compute warps see the sentinel
+          break;
+        }
+        const int qb = meta.qbuf;
+        if (meta.first && !mbar_wait(&sm.q_full[qb], (uint32_t)(local_item >> 1) & 1u, p.status)) { ok = false; break; }
+        const int sb = j & 1;
+        if (!mbar_wait(&sm.s_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(sm.kv[st][0]);
+        const uint32_t qbase = smem_u32(sm.q[qb]);
+#pragma unroll
+        for (int s = 0; s < C::kKSteps; ++s) {
+          const uint64_t a = umma_desc(kbase + (s >> 2) * (kT * 128) + (s & 3) * 32, 16, 1024);
+          const uint64_t bd = umma_desc(qbase + (s >> 2) * (kNP * 128) + (s & 3) * 32, 16, 1024);
+          umma_f16(tmem + C::kColS + sb * 16, a, bd, idesc_qk, s > 0);
+        }
+        umma_commit(&sm.s_full[sb]);
+        if (meta.last) {
+          umma_commit(&sm.q_empty[qb]);
+          ++local_item;
+        }
+        if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+        ++j;
+      }
+      (void)ok;
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax + correction
+    // GP (the group size rounded up to a power of two) is a compile-time bound, so the
+    // per-head loops unroll into independent chains the scheduler can interleave.
+    const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+    const int r = quad * 32 + lane;            // TMEM lane: token of S, channel of O
+    const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
+    float m_run[GP], l_part[GP], alpha_prev[GP], acc[GP], m_fin[GP], l_fin[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      m_run[g] = -INFINITY; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_fin[g] = -INFINITY; l_fin[g] = 0.f;
+    }
+    int prev_item = -1;
+    bool prev_first = false, prev_last = false;
+
+    // rescale-and-accumulate of the PV result of tile jj; finalises its item if it was the last tile
+    auto correct = [&](int jj, bool use_fin) -> bool {
+      const int ob = jj & 1;
+      if (!mbar_wait(&sm.o_full[ob], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
+      tc_fence_after();
+      float o[kNP];
+      const uint32_t ocol = tq + C::kColO + ob * C::kOStride + ((C::kStacked && r >= 64) ? 16 : 0);
+      tmem_ld16(ocol, o);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.o_free[ob]);
+#pragma unroll
+      for (int g = 0; g < GP; ++g) acc[g] = prev_first ? o[g] : fmaf(acc[g], alpha_prev[g], o[g]);
+      if (prev_last) {
+        float mm[GP], lv[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          mm[g] = use_fin ? m_fin[g] : m_run[g];
+          lv[g] = use_fin ? l_fin[g] : l_part[g];
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1)
+#pragma unroll
+          for (int g = 0; g < GP; ++g) lv[g] += __shfl_xor_sync(0xffffffffu, lv[g], off);
+        if (lane == 0) {
+#pragma unroll
+          for (int g = 0; g < GP; ++g) sm.lsum[quad][g] = lv[g];
+        }
+        if (C::kStacked && r >= 64) {
+#pragma unroll
+          for (int g = 0; g < GP; ++g) sm.accx[r - 64][g] = acc[g];
+        }
+        named_bar_sync(kBarCompute, 128);
+        float lt[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) lt[g] = sm.lsum[0][g] + sm.lsum[1][g] + sm.lsum[2][g] + sm.lsum[3][g];
+        if (!C::kStacked || r < 64) {
+          float* po = p.ws.part_o + (int64_t)prev_item * G * D;
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            if (g < G) {
+              const float a = C::kStacked ? acc[g] + sm.accx[r][g] : acc[g];
+              po[g * D + r] = lt[g] > 0.f ? a / lt[g] : 0.f;
+            }
+          }
+        }
+        if (r < GP && r < G) {
+          float mv = mm[0], lw = lt[0];
+#pragma unroll
+          for (int g = 1; g < GP; ++g)
+            if (r == g) { mv = mm[g]; lw = lt[g]; }
+          p.ws.part_ml[(int64_t)prev_item * G + r] = make_float2(mv, lw);
+        }
+        named_bar_sync(kBarCompute, 128);
+      }
+      return true;
+    };
+
+    int j = 0;
+    bool ok = true;
+    while (true) {
+      const int sb = j & 1;
+      const uint32_t sph = (uint32_t)(j >> 1) & 1u;
+      if (!mbar_wait(&sm.s_full[sb], sph, p.status)) { ok = false; break; }
+      const int st = j % C::kStages;
+      const TileMeta meta = sm.meta[st];
+      if (meta.item < 0) break;
+      tc_fence_after();
+      float s[kNP];
+      tmem_ld16(tq + C::kColS + sb * 16, s);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.s_free[sb]);
+      if (meta.first) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          m_fin[g] = m_run[g];
+          l_fin[g] = l_part[g];
+          m_run[g] = -INFINITY;
+          l_part[g] = 0.f;
+        }
+      }
+      const bool valid = r < meta.n;
+      // per-head maximum over the tile's tokens: warp butterflies (independent per head),
+      // then across the 4 warps through shared memory
+      float x[GP], mx[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        x[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
+        mx[g] = x[g];
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1)
+#pragma unroll
+        for (int g = 0; g < GP; ++g) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) sm.red[sb][quad][g] = mx[g];
+      }
+      named_bar_sync(kBarCompute, 128);
+      float alpha[GP], pr[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float tmax = fmaxf(fmaxf(sm.red[sb][0][g], sm.red[sb][1][g]), fmaxf(sm.red[sb][2][g], sm.red[sb][3][g]));
+        const float m_new = fmaxf(m_run[g], tmax);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha[g] = fast_exp2(m_run[g] - m_use);   // m_run = -inf gives 0
+        pr[g] = fast_exp2(x[g] - m_use);          // masked tokens (-inf) give 0
+        l_part[g] = fmaf(l_part[g], alpha[g], pr[g]);
+        m_run[g] = m_new;
+      }
+      // P^T (and a zeroed V tail) for the PV MMA
+      if (!mbar_wait(&sm.p_free[sb], sph ^ 1u, p.status)) { ok = false; break; }
+      uint8_t* pbuf = sm.p[sb];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        if (g < G) {
+          uint16_t h;
+          if (DT == kBF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(pr[g]));
+          else h = __half_as_ushort(__float2half_rn(pr[g]));
+          *reinterpret_cast<uint16_t*>(pbuf + p_offset(g, r)) = h;
+        }
+      }
+      if (!valid) {
+        uint8_t* vrow = sm.kv[st][1];
+#pragma unroll
+        for (int bx = 0; bx < C::kNumBoxes; ++bx) {
+          uint4* dst = reinterpret_cast<uint4*>(vrow + bx * (kT * 128) + r * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+      // rescale-and-accumulate the previous tile's PV result
+      if (j > 0 && !correct(j - 1, meta.first)) { ok = false; break; }
+#pragma unroll
+      for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
+      prev_first = meta.first;
+      prev_last = meta.last;
+      prev_item = meta.item;
+      ++j;
+    }
+    if (ok && j > 0) correct(j - 1, false);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, int DT, int GP>
+cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
+                      int box_rows, int grid, cudaStream_t stream) {
+  const size_t smem = sizeof(TcSmem<D>) + 1024;
+  auto kern = decode_tc_kernel<D, DT, GP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  trace_mark(kKernelDecodeAttention, 0, stream);
+  kern<<<grid, kThreadsTC, smem, stream>>>(tmK, tmV, tmQ, p, box_rows);
+  trace_mark(kKernelDecodeAttention, 1, stream);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+template <int D, int DT>
+cudaError_t launch_tc_g(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
+                        int box_rows, int grid, cudaStream_t stream) {
+  if (p.G <= 2) return launch_tc<D, DT, 2>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+  if (p.G <= 4) return launch_tc<D, DT, 4>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+  if (p.G <= 8) return launch_tc<D, DT, 8>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+  return launch_tc<D, DT, 16>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+}
+
+cudaError_t launch_decode_tc_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                       const CUtensorMap& tmQ, int box_rows, int grid, cudaStream_t stream) {
+  if (p.kv_dtype == kBF16)
+    return p.D == 64 ? launch_tc_g<64, kBF16>(p, tmK, tmV, tmQ, box_rows, grid, stream)
+                     : launch_tc_g<128, kBF16>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+  return p.D == 64 ? launch_tc_g<64, kF16>(p, tmK, tmV, tmQ, box_rows, grid, stream)
+                   : launch_tc_g<128, kF16>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+}
+
+}  // namespace fia

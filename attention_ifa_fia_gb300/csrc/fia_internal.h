@@ -73,9 +73,15 @@ size_t decode_workspace_bytes(int B, int Nkv, int G, int D, int max_items);
 DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D, int max_items);
 
 // Launches plan + attention + merge on `stream`.  tmK / tmV describe the K and V
-// pools as 2-D tensors (D, num_blocks * Nkv * block_size).  Returns a CUDA error.
-cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows,
-                          int num_sms, cudaStream_t stream);
+// pools as 2-D tensors (D, num_blocks * Nkv * block_size) with boxes of box_rows
+// rows.  With tmQ (the query as a 2-D tensor (D, B * Nq), 16-row boxes) the
+// tensor-core attention kernel runs (16-bit KV, G <= 16, 128-token tiles);
+// without it the CUDA-core kernel (any KV type, G <= 8, 64-token tiles).
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream);
+cudaError_t launch_decode_tc_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                       const CUtensorMap& tmQ, int box_rows, int grid, cudaStream_t stream);
+constexpr int kDecodeTileTC = 128;  // tokens per tensor-core tile; work items are multiples of it
 
 // ---------------------------------------------------------------------------
 // RingAttentionUpdate

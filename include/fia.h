@@ -106,7 +106,8 @@ int fia_trace_collect(int kernel, double* total_ms, int* launches);
  * actual_seq_lengths device int64 (B).  Values are clamped to [0, max_kv_len]
  *                    (FIA_STATUS_LENGTH_CLAMPED is raised if any is outside).
  * max_kv_len         host upper bound of the lengths; <= bt_stride * block_size.
- * Nkv                0 means Nkv = Nq.  Nq % Nkv == 0; Nq / Nkv <= 8 in this build.
+ * Nkv                0 means Nkv = Nq.  Nq % Nkv == 0; Nq / Nkv <= 16 (<= 8 with int8 KV) in
+ *                    this build.
  * D                  64 or 128 in this build.
  * block_size         > 0, <= 512, a multiple of 16 (16-bit KV) or 32 (int8 KV).
  * scale              the scaleValue of the pages, usually 1/sqrt(D).
@@ -116,7 +117,7 @@ int fia_trace_collect(int kernel, double* total_ms, int* launches);
  * sink               device fp32 (Nq) or NULL; not allowed with int8 KV.
  * softmax_max/sum    device fp32 (B, Nq) or NULL (not written).
  * num_splits         0 picks the split automatically; n > 0 splits each sequence into at most
- *                    n chunks of ceil(max_kv_len / n) tokens (rounded up to 64).
+ *                    n chunks of ceil(max_kv_len / n) tokens (rounded up to 128).
  * workspace          device, at least fia_decode_workspace_size() bytes, 256-byte aligned.
  *                    Holds the split plan and partials; contents need no initialisation.
  */

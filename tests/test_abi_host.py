@@ -45,7 +45,8 @@ def _decode(lib, **kw):
     (dict(q=None), NULLPTR), (dict(k=None), NULLPTR), (dict(bt=None), NULLPTR), (dict(lens=None), NULLPTR),
     (dict(out=None), NULLPTR), (dict(ws=None), NULLPTR), (dict(kv_dtype=3), NULLPTR),     # int8 without scale
     (dict(q_dtype=0), INVALID), (dict(q_dtype=3), INVALID), (dict(kv_dtype=1), INVALID),  # fp16 kv, bf16 q
-    (dict(Nq=6, Nkv=4), INVALID), (dict(Nq=32, Nkv=2), INVALID), (dict(Nq=300, Nkv=300), INVALID),
+    (dict(Nq=6, Nkv=4), INVALID), (dict(Nq=64, Nkv=2), INVALID), (dict(Nq=300, Nkv=300), INVALID),
+    (dict(Nq=32, Nkv=2, kv_dtype=3, aqs=P, bs=32), INVALID),                             # int8, group 16
     (dict(D=96), INVALID), (dict(D=256), INVALID), (dict(bs=0), INVALID), (dict(bs=24), INVALID),
     (dict(bs=1024), INVALID), (dict(kv_dtype=3, aqs=P, bs=16), INVALID),                  # int8 needs bs % 32
     (dict(kv_dtype=3, aqs=P, bs=32, sink=P), INVALID),                                      # sink + int8
