@@ -47,6 +47,8 @@ def _load() -> ctypes.CDLL:
         "fia_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
         "fia_decode": ([P, i32, P, P, i32, P, i64, P, i32, i32, i32, i32, i32, i32, i64, dbl, P, P, P, P, P, P,
                         i32, P, sz, P], i32),
+        "fia_decode_noalloc": ([P, i32, P, P, i32, P, i64, P, i32, i32, i32, i32, i32, i32, i64, dbl, P, P, P, P,
+                                P, P, i32, P], i32),
         "fia_prefill_workspace_size": ([i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
         "fia_prefill": ([P, P, P, i32, P, P, i32, i64, i64, i32, i32, i32, i32, i32, dbl, i32, P, P, P, P, P, sz,
                          P], i32),
@@ -155,6 +157,30 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
                          int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
                          _stream(stream))
     _check(rc, "fia_decode")
+    return out, softmax_max, softmax_sum
+
+
+def fia_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                       actual_seq_lengths: torch.Tensor, *, max_kv_len: int, num_heads: int, num_kv_heads: int = 0,
+                       scale: Optional[float] = None, antiquant_scale=None, antiquant_offset=None, sink=None,
+                       out: Optional[torch.Tensor] = None, softmax_max: Optional[torch.Tensor] = None,
+                       softmax_sum: Optional[torch.Tensor] = None, num_splits: int = 0, stream=None):
+    """fia_decode without a workspace argument: the library uses its own fixed device scratch
+    (for callers that cannot allocate; see include/fia.h).  `out` must be given by callers
+    that may not allocate; when omitted it is created here for convenience."""
+    B, D = int(q.shape[0]), int(q.shape[-1])
+    num_blocks, block_size = int(k_cache.shape[0]), int(k_cache.shape[2])
+    nkv = num_kv_heads if num_kv_heads else num_heads
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty((B, num_heads, D), dtype=q.dtype, device=q.device)
+    rc = _lib.fia_decode_noalloc(_ptr(q), dtype_code(q), _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache),
+                                 _ptr(block_table), int(block_table.shape[1]), _ptr(actual_seq_lengths),
+                                 int(max_kv_len), B, num_heads, nkv, D, block_size, num_blocks, float(scale),
+                                 _ptr(antiquant_scale), _ptr(antiquant_offset), _ptr(sink), _ptr(out),
+                                 _ptr(softmax_max), _ptr(softmax_sum), int(num_splits), _stream(stream))
+    _check(rc, "fia_decode_noalloc")
     return out, softmax_max, softmax_sum
 
 

@@ -179,6 +179,14 @@ cudaEvent_t trace_event() {
 }  // namespace
 
 namespace fia {
+int report_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
 void trace_mark(int kernel, int phase, cudaStream_t stream) {
   if (!g_trace.on || kernel < 0 || kernel >= kKernelCount) return;
   cudaEvent_t e = trace_event();

@@ -24,6 +24,9 @@ enum : unsigned int {
 enum : int { kKernelDecodePlan = 0, kKernelDecodeAttention = 1, kKernelDecodeMerge = 2, kKernelPrefill = 3,
              kKernelRau = 4, kKernelCount = 5 };
 
+// Sets the text fia_last_error() returns on this thread and returns `code`.
+int report_error(int code, const char* fmt, ...);
+
 // Records a CUDA event on `stream` before (phase 0) or after (phase 1) a launch
 // of `kernel` when tracing is enabled on the calling thread; otherwise nothing.
 void trace_mark(int kernel, int phase, cudaStream_t stream);

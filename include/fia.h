@@ -131,6 +131,29 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
                float* softmax_max, float* softmax_sum, int num_splits, void* workspace, size_t workspace_bytes,
                fia_stream_t stream);
 
+/* Allocation-free variant of fia_decode.  The operator pages have no counterpart:
+ * it exists for callers that cannot allocate device memory for the workspace --
+ * plugins whose host application owns all device memory through its own allocator,
+ * modules that may not call the CUDA allocator, and loops in which cudaMalloc's
+ * possible device synchronisation is not allowed.  Arguments and results are those
+ * of fia_decode without the workspace: the workspace is a fixed 16 MiB array in the
+ * library's device memory (every GPU that loads the library holds it until exit).
+ *   - Problems whose fia_decode_workspace_size exceeds 16 MiB return
+ *     FIA_ERR_PARAM_INVALID (fia_last_error names the limit).
+ *   - All calls on a device share the array, which keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls that overlap on the GPU (other
+ *     streams, or unordered host threads) race on it: order them.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make it before any stream
+ *     capture begins.
+ *   - Nothing is allocated or freed by this call. */
+int fia_decode_noalloc(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache,
+                       fia_dtype kv_dtype, const int32_t* block_table, int64_t bt_stride,
+                       const int64_t* actual_seq_lengths, int max_kv_len, int B, int Nq, int Nkv, int D,
+                       int block_size, int64_t num_blocks, double scale, const float* antiquant_scale,
+                       const float* antiquant_offset, const float* sink, void* out, float* softmax_max,
+                       float* softmax_sum, int num_splits, fia_stream_t stream);
+
 /* ------------------------------------------------------------------------ prefill
  * FusedInferAttentionScore (prefill mode Q_S > 1, sparseMode 3 rightDownCausal, TND);
  * aclnnFlashAttentionScoreV4 (TND, cumulative actual_seq_qlen, zero-length sequences).
