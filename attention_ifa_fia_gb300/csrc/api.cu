@@ -415,12 +415,44 @@ int fia_debug_gather(const void* k_cache, fia_dtype kv_dtype, const int32_t* blo
 
 }  // extern "C"
 
+namespace {
+
+// 3-D tensor map over a (rows, heads, D) row-major tensor, box = 64 x 1 x 128 rows,
+// 128-byte swizzle: one head's 128 consecutive rows, 64 channels per box.
+int make_tmap_thd(CUtensorMap* m, const void* base, int dtype, uint64_t D, uint64_t heads, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FIA_ERR_RUNTIME, "cuTensorMapEncodeTiled is not available from the driver");
+  const CUtensorMapDataType t = dtype == fia::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[3] = {D, heads, rows};
+  cuuint64_t strides[2] = {D * 2, heads * D * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FIA_ERR_RUNTIME, "cuTensorMapEncodeTiled (3-D) failed (%d)", (int)r);
+  return FIA_SUCCESS;
+}
+
+int check_prefill_shape(int B, int Nq, int* Nkv, int D, int max_seqlen_q) {
+  if (B < 0 || B > 65536) return fail(FIA_ERR_PARAM_INVALID, "B = %d outside [0, 65536]", B);
+  if (Nq < 1 || Nq > 256) return fail(FIA_ERR_PARAM_INVALID, "Nq = %d outside [1, 256]", Nq);
+  if (*Nkv == 0) *Nkv = Nq;
+  if (*Nkv < 0 || Nq % *Nkv != 0)
+    return fail(FIA_ERR_PARAM_INVALID, "Nq = %d is not a multiple of Nkv = %d", Nq, *Nkv);
+  if (D != 128) return fail(FIA_ERR_PARAM_INVALID, "prefill supports D = 128 in this build (got %d)", D);
+  if (max_seqlen_q < 0) return fail(FIA_ERR_PARAM_INVALID, "max_seqlen_q = %d < 0", max_seqlen_q);
+  if ((int64_t)B * ((max_seqlen_q + 127) / 128) >= (1LL << 31) / 256)
+    return fail(FIA_ERR_PARAM_INVALID, "too many query tiles");
+  return FIA_SUCCESS;
+}
+
+}  // namespace
+
 extern "C" {
 
 int fia_prefill_workspace_size(int B, int Nq, int Nkv, int D, int max_seqlen_q, size_t* bytes) {
   if (!bytes) return fail(FIA_ERR_PARAM_NULLPTR, "bytes is NULL");
-  (void)Nkv;
-  (void)D;
+  if (int rc = check_prefill_shape(B, Nq, &Nkv, D, max_seqlen_q)) return rc;
   *bytes = fia::prefill_workspace_bytes(B, Nq, max_seqlen_q);
   return ok();
 }
@@ -429,10 +461,63 @@ int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, co
                 const int64_t* cu_seqlens_kv, int B, int64_t T, int64_t Tkv, int max_seqlen_q, int max_seqlen_kv,
                 int Nq, int Nkv, int D, double scale, int mask, const float* sink, void* out, float* softmax_max,
                 float* softmax_sum, void* workspace, size_t workspace_bytes, fia_stream_t stream) {
-  (void)q; (void)k; (void)v; (void)dtype; (void)cu_seqlens_q; (void)cu_seqlens_kv; (void)B; (void)T; (void)Tkv;
-  (void)max_seqlen_q; (void)max_seqlen_kv; (void)Nq; (void)Nkv; (void)D; (void)scale; (void)mask; (void)sink;
-  (void)out; (void)softmax_max; (void)softmax_sum; (void)workspace; (void)workspace_bytes; (void)stream;
-  return fail(FIA_ERR_PARAM_INVALID, "prefill is not available in this build yet");
+  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_kv || !out)
+    return fail(FIA_ERR_PARAM_NULLPTR, "q, k, v, cu_seqlens_q, cu_seqlens_kv and out are required");
+  if (!workspace) return fail(FIA_ERR_PARAM_NULLPTR, "workspace is NULL");
+  if (dtype != FIA_F16 && dtype != FIA_BF16) return fail(FIA_ERR_PARAM_INVALID, "dtype must be fp16 or bf16");
+  if (int rc = check_prefill_shape(B, Nq, &Nkv, D, max_seqlen_q)) return rc;
+  if (T < 0 || Tkv < 0 || T >= (1LL << 31) || Tkv >= (1LL << 31))
+    return fail(FIA_ERR_PARAM_INVALID, "T = %lld, Tkv = %lld outside [0, 2^31)", (long long)T, (long long)Tkv);
+  if (max_seqlen_kv < 0 || max_seqlen_kv > (1 << 20))
+    return fail(FIA_ERR_PARAM_INVALID, "max_seqlen_kv = %d outside [0, 2^20] (this build)", max_seqlen_kv);
+  if (mask != 0 && mask != 3)
+    return fail(FIA_ERR_PARAM_INVALID, "mask = %d: 0 (none) and 3 (rightDownCausal) are supported", mask);
+  if (!std::isfinite(scale)) return fail(FIA_ERR_PARAM_INVALID, "scale is not finite");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(FIA_ERR_PARAM_INVALID, "q, k, v and out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(FIA_ERR_PARAM_INVALID, "workspace must be 256-byte aligned");
+  const size_t need = fia::prefill_workspace_bytes(B, Nq, max_seqlen_q);
+  if (workspace_bytes < need)
+    return fail(FIA_ERR_PARAM_INVALID, "workspace of %zu bytes is smaller than the %zu required", workspace_bytes,
+                need);
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  if (B == 0 || T == 0) return ok();
+
+  fia::PrefillParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.softmax_max = softmax_max;
+  p.softmax_sum = softmax_sum;
+  p.cu_q = cu_seqlens_q;
+  p.cu_kv = cu_seqlens_kv;
+  p.sink = sink;
+  p.B = B;
+  p.Nq = Nq;
+  p.Nkv = Nkv;
+  p.G = Nq / Nkv;
+  p.D = D;
+  p.T = T;
+  p.Tkv = Tkv;
+  p.max_seqlen_q = max_seqlen_q;
+  p.max_seqlen_kv = max_seqlen_kv;
+  p.causal = mask == 3;
+  p.dtype = dtype;
+  p.scale_log2 = (float)(scale * 1.4426950408889634);
+  p.tile_counter = static_cast<int*>(workspace);
+  p.tile_list = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + 256);
+  p.max_tiles = (int)((need - 256) / sizeof(int));
+  p.status = d->status;
+  CUtensorMap tmQ, tmK, tmV;
+  if (int rc = make_tmap_thd(&tmQ, q, dtype, D, Nq, T)) return rc;
+  if (int rc = make_tmap_thd(&tmK, k, dtype, D, Nkv, Tkv > 0 ? Tkv : 1)) return rc;
+  if (int rc = make_tmap_thd(&tmV, v, dtype, D, Nkv, Tkv > 0 ? Tkv : 1)) return rc;
+  cudaError_t e = fia::launch_prefill(p, tmQ, tmK, tmV, d->num_sms, stream);
+  if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "prefill launch: %s", cudaGetErrorString(e));
+  return ok();
 }
 
 }  // extern "C"

@@ -110,9 +110,10 @@ struct PrefillParams {
   int64_t T, Tkv;
   int max_seqlen_q, max_seqlen_kv;
   int causal;
+  int dtype;          // kBF16 or kF16
   float scale_log2;
-  int* tile_list;     // workspace: (n_tiles) packed tile descriptors
-  int* tile_counter;  // workspace: dynamic scheduler counter
+  int* tile_list;     // workspace: (sequence << 16 | query tile) pairs, longest first
+  int* tile_counter;  // workspace: [0] unit counter, [1] number of units
   int max_tiles;
   unsigned int* status;
 };

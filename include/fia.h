@@ -166,8 +166,8 @@ int fia_decode_noalloc(const void* q, fia_dtype q_dtype, const void* k_cache, co
  * q, out           device (T, Nq, D) row-major, dtype FIA_BF16 or FIA_F16, 16-byte aligned.
  * k, v             device (Tkv, Nkv, D) row-major, same dtype, 16-byte aligned.
  * cu_seqlens_q/kv  device int64 (B + 1), cu[0] = 0, non-decreasing, cu[B] = T (resp. Tkv).
- * max_seqlen_q/kv  host upper bounds of the per-sequence lengths.
- * D                128 in this build (64 also accepted); Nq % Nkv == 0.
+ * max_seqlen_q/kv  host upper bounds of the per-sequence lengths (max_seqlen_kv <= 2^20 here).
+ * D                128 in this build; Nq % Nkv == 0; max_seqlen_q must bound every Lq.
  * mask             0 (none) or 3 (rightDownCausal).
  * sink             device fp32 (Nq) or NULL.
  * softmax_max/sum  device fp32 (T, Nq) or NULL.

@@ -120,3 +120,60 @@ def sample_rows(case: W.DecodeCase, n: int, seed: int = 0) -> np.ndarray:
     for b in (int(np.argmin(case.lengths)), int(np.argmax(case.lengths))):
         picks.update(range(b * case.Nq, (b + 1) * case.Nq))
     return np.array(sorted(picks), np.int64)
+
+
+# ----------------------------------------------------------------------------- prefill
+class DevicePrefill:
+    """A PrefillCase resident on the GPU."""
+
+    def __init__(self, case: W.PrefillCase, device="cuda"):
+        self.case = case
+        self.q = dev_bits(case.q, case.dtype, device)
+        self.k = dev_bits(case.k, case.dtype, device)
+        self.v = dev_bits(case.v, case.dtype, device)
+        self.cu_q = torch.from_numpy(case.cu_q).to(device)
+        self.cu_kv = torch.from_numpy(case.cu_kv).to(device)
+        self.sink = None if case.sink is None else torch.from_numpy(case.sink).to(device)
+
+
+def run_prefill(F, dp: DevicePrefill, causal=True, sink="case"):
+    c = dp.case
+    mx = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device=dp.q.device)
+    sm = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device=dp.q.device)
+    return F.fia_prefill(dp.q, dp.k, dp.v, dp.cu_q, dp.cu_kv, max_seqlen_q=int(c.lengths_q.max(initial=0)),
+                         max_seqlen_kv=int(c.lengths_kv.max(initial=0)), num_heads=c.Nq, num_kv_heads=c.Nkv,
+                         scale=c.scale, mask=3 if causal else 0, sink=dp.sink if sink == "case" else sink,
+                         softmax_max=mx, softmax_sum=sm)
+
+
+def oracle_prefill(case: W.PrefillCase, rows=None, causal=True, sink="case", nthreads=0):
+    code = {W.BF16: OR.BF16, W.FP16: OR.F16}[case.dtype]
+    return OR.prefill(case.q, case.k, case.v, case.cu_q, case.cu_kv, Nq=case.Nq, Nkv=case.Nkv, D=case.D,
+                      scale=case.scale, causal=causal, dtype=code, sink=case.sink if sink == "case" else sink,
+                      rows=rows, nthreads=nthreads)
+
+
+def compare_prefill(case: W.PrefillCase, out, mx, sm, rows=None, ref=None, causal=True):
+    if ref is None:
+        ref = oracle_prefill(case, rows=rows, causal=causal)
+    o = to_f64(out).reshape(case.T * case.Nq, case.D)
+    m = to_f64(mx).reshape(-1)
+    s = to_f64(sm).reshape(-1)
+    if rows is not None:
+        o, m, s = o[rows], m[rows], s[rows]
+    atol, rtol = OUT_TOL[case.dtype]
+    return {"out": assert_close("out", o, ref[0], atol, rtol),
+            "max": assert_close("softmax_max", m, ref[1], *MAX_TOL),
+            "sum": assert_close("softmax_sum", s, ref[2], *SUM_TOL)}
+
+
+def sample_prefill_rows(case: W.PrefillCase, n: int, seed: int = 0) -> np.ndarray:
+    """n random (t * Nq + h) rows plus all heads of the first and last token of every sequence."""
+    rng = np.random.default_rng(seed)
+    total = case.T * case.Nq
+    picks = set(rng.choice(total, size=min(n, total), replace=False).tolist())
+    for b in range(case.B):
+        for t in {int(case.cu_q[b]), int(case.cu_q[b + 1]) - 1}:
+            if case.cu_q[b] <= t < case.cu_q[b + 1]:
+                picks.update(range(t * case.Nq, (t + 1) * case.Nq))
+    return np.array(sorted(picks), np.int64)

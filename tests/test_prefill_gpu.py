@@ -1,0 +1,64 @@
+"""GPU parity of fia_prefill (TND, causal varlen, tcgen05) against the oracle."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import fia_workloads as W
+from parity import DevicePrefill, compare_prefill, oracle_prefill, run_prefill, sample_prefill_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def test_causal_prefill_full_size(F, cuda):
+    case = W.causal_prefill_tnd()
+    dp = DevicePrefill(case)
+    out, mx, sm = run_prefill(F, dp)
+    rows = sample_prefill_rows(case, 1024, seed=5)
+    compare_prefill(case, out, mx, sm, rows=rows)
+    assert F.fia_device_status() == 0
+
+
+CASES = {
+    # name: make_prefill_case kwargs (+ "causal")
+    "one_tile_each": dict(Nq=4, Nkv=2, D=128, lengths=[1, 127, 128, 129]),
+    "ragged_multi_tile": dict(Nq=8, Nkv=2, D=128, lengths=[300, 513, 5]),
+    "zero_length_seqs": dict(Nq=4, Nkv=4, D=128, lengths=[2, 2, 0, 2, 2]),
+    "q_shorter_than_kv": dict(Nq=4, Nkv=1, D=128, lengths=[100, 200, 7], lengths_kv=[300, 200, 135]),
+    "q_longer_than_kv": dict(Nq=2, Nkv=2, D=128, lengths=[200, 130], lengths_kv=[70, 0]),
+    "gqa8_fp16": dict(Nq=16, Nkv=2, D=128, lengths=[260, 40], dtype=W.FP16),
+    "sink": dict(Nq=4, Nkv=2, D=128, lengths=[150, 290], sink=True),
+    "sink_q_longer": dict(Nq=2, Nkv=1, D=128, lengths=[140], lengths_kv=[20], sink=True),
+    "no_mask": dict(Nq=4, Nkv=2, D=128, lengths=[77, 260], causal=False),
+    "no_mask_lq_ne_lkv": dict(Nq=2, Nkv=1, D=128, lengths=[33, 140], lengths_kv=[500, 1], causal=False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_prefill_case(F, cuda, name):
+    kw = dict(CASES[name])
+    causal = kw.pop("causal", True)
+    case = W.make_prefill_case(seed=zlib.crc32(name.encode()) % (1 << 30), **kw)
+    dp = DevicePrefill(case)
+    out, mx, sm = run_prefill(F, dp, causal=causal)
+    compare_prefill(case, out, mx, sm, causal=causal)
+    assert F.fia_device_status() == 0
+
+
+def test_prefill_deterministic(F, cuda):
+    case = W.make_prefill_case(Nq=8, Nkv=2, D=128, lengths=[700, 333, 1024], seed=3)
+    dp = DevicePrefill(case)
+    a = run_prefill(F, dp)
+    b = run_prefill(F, dp)
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_prefill_rejects_bad_arguments(F, cuda):
+    case = W.make_prefill_case(Nq=4, Nkv=2, D=128, lengths=[5], seed=4)
+    dp = DevicePrefill(case)
+    with pytest.raises(F.FiaError) as ei:
+        F.fia_prefill(dp.q, dp.k, dp.v, dp.cu_q, dp.cu_kv, max_seqlen_q=5, max_seqlen_kv=5, num_heads=4,
+                      num_kv_heads=2, mask=2)
+    assert ei.value.code == 161002
