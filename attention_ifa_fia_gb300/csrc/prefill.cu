@@ -10,14 +10,17 @@
 // CTAs take units from a counter.  Per key tile of 128 keys:
 //
 //   S [128 q x 128 k] = Q . K^T     A = Q tile, B = K tile, both K-major (TMA, 128B swizzle)
-//   O [128 q x D]    += P . V       A = P (bf16, K-major, written by the softmax warps)
+//   O [128 q x D]    += P . V       A = P in tensor memory (16-bit pairs per column)
 //                                   B = V tile read MN-major
 //
-// S (double buffered) and O live in tensor memory.  Warp roles (192 threads): warp 0
-// issues TMA (Q per unit, double buffered; K/V tiles in a 2-stage ring), warp 1 owns
-// TMEM and issues MMAs (QK of tile j+1 overlaps the softmax of tile j), warps 2-5 own one
-// query row each: mask, row max and sum in registers (no cross-thread reduction), P,
-// the rescale of O, and the epilogue.  O is rescaled only when the running row max
+// S (double buffered), P (double buffered) and O all live in tensor memory, so the PV
+// product reads only V from shared memory.  Warp roles (320 threads): warp 0 issues TMA
+// (Q per unit, double buffered; K and V tiles in separate 2-stage rings, each V one tile
+// behind its K); warp 1 owns TMEM and issues MMAs (QK of tile j+1 overlaps the softmax of
+// tile j); warps 2-9 are two warpgroups that split every query row between them (key
+// columns / output channels 0-63 and 64-127): mask, row max and sum in registers with
+// only the per-row maximum exchanged through shared memory, P, the rescale of O, and the
+// epilogue.  O is rescaled only when the running row max
 // grows by more than 8 (log2 units); otherwise the stale max keeps every exponent
 // <= 2^8, and the softmax max/sum outputs are converted to the true max at the end.
 #include "fia_device.cuh"
@@ -28,9 +31,11 @@ namespace {
 constexpr int kQT = 128;           // queries per tile (MMA M)
 constexpr int kKT = 128;           // keys per tile (MMA N of QK, K of PV)
 constexpr int kPD = 128;           // head dim supported by this kernel
-constexpr int kPThreads = 192;
+constexpr int kPThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two column halves)
+constexpr int kSoftmaxThreads = 256;
+constexpr int kBarSoftmax = 3;   // named barrier of the softmax warps
 constexpr int kPStages = 2;
-constexpr int kTileB = kQT * kPD * 2;  // 32 KB: Q, K, V or P tile
+constexpr int kTileB = kQT * kPD * 2;  // 32 KB: a Q, K or V tile
 constexpr uint32_t kRescaleThreshold = 8;  // log2 units
 
 struct __align__(16) PTileMeta {
@@ -39,17 +44,25 @@ struct __align__(16) PTileMeta {
   int first, last, qbuf, unit;
 };
 
+constexpr int kMetaRing = 4;
+
 struct PSmem {
   alignas(1024) uint8_t q[2][kTileB];
-  alignas(1024) uint8_t kv[kPStages][2][kTileB];
-  alignas(1024) uint8_t p[kTileB];
-  PTileMeta meta[kPStages];
+  alignas(1024) uint8_t k[kPStages][kTileB];
+  alignas(1024) uint8_t v[kPStages][kTileB];
+  PTileMeta meta[kMetaRing];
   uint64_t q_full[2], q_empty[2];
-  uint64_t kv_full[kPStages], kv_empty[kPStages];
+  uint64_t k_full[kPStages], k_empty[kPStages];
+  uint64_t v_full[kPStages], v_empty[kPStages];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full, pv_done, o_free;
+  uint64_t p_full[2], p_free[2];
+  uint64_t pv_done, o_free;
+  float rmax[2][2][kQT];  // [tile parity][column half][row]: partial row maxima
+  float lsum[2][kQT];     // [column half][row]: partial row sums at the epilogue
   uint32_t tmem_base;
 };
+// The dynamic shared memory must fit the 227 KB a CTA may use.
+static_assert(sizeof(PSmem) <= 232448, "prefill shared memory exceeds the per-CTA limit");
 
 // per (sequence, query tile): key tiles that hold at least one visible key
 __device__ __forceinline__ int key_tiles(int q0, int Lq, int Lkv, int causal) {
@@ -114,13 +127,6 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
   }
 }
 
-// Offset of (row r, 16-byte chunk c) in a 128-row tile stored as two 64-column
-// boxes of 128-byte rows with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t tile_chunk_offset(int r, int c) {
-  const uint32_t box = c >> 3, cc = c & 7;
-  return box * (kQT * 128) + r * 128 + ((cc ^ (r & 7)) << 4);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -141,29 +147,57 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread (A: rows on lanes, 16-bit pairs per column).
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ attention
 template <int DT>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  PSmem& sm = *reinterpret_cast<PSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  PSmem& sm = *reinterpret_cast<PSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (smem_u32(smem_raw) & 1023u) {  // the swizzled operand layouts need 1 KB alignment
+    if (tid == 0) raise_status(p.status, kStatusWaitTimeout);
+    return;
+  }
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_free[i], 4);
+      mbar_init(&sm.s_free[i], 8);
+      mbar_init(&sm.p_full[i], 8);
+      mbar_init(&sm.p_free[i], 1);
     }
-    for (int s = 0; s < kPStages; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+    for (int st = 0; st < kPStages; ++st) {
+      mbar_init(&sm.k_full[st], 1);
+      mbar_init(&sm.k_empty[st], 1);
+      mbar_init(&sm.v_full[st], 1);
+      mbar_init(&sm.v_empty[st], 1);
     }
-    mbar_init(&sm.p_full, 4);
     mbar_init(&sm.pv_done, 1);
-    mbar_init(&sm.o_free, 4);
+    mbar_init(&sm.o_free, 8);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
@@ -171,7 +205,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  constexpr uint32_t kColS = 0, kColO = 256;
+  constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // S: 2 x 128, O: 128, P: 2 x 64
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -182,7 +216,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int n_units = p.tile_counter[1];
       const int G = p.G;
       int j = 0, u_local = 0;
+      int v_next = 0;             // next tile whose V is to be loaded
+      int v_hkv = 0, v_tk = 0;    // V source of tiles [v_next, j) is recorded in the ring
+      int ring_hkv[kMetaRing], ring_row[kMetaRing];
       bool ok = true;
+      // V of tile jv, one tile behind its K
+      auto load_v = [&](int jv) -> bool {
+        const int st = jv % kPStages;
+        if (!mbar_wait(&sm.v_empty[st], ((uint32_t)(jv / kPStages) & 1u) ^ 1u, p.status)) return false;
+        mbar_arrive_expect_tx(&sm.v_full[st], kTileB);
+        for (int bx = 0; bx < 2; ++bx)
+          tma_load_3d(sm.v[st] + bx * (kKT * 128), &tmV, bx * 64, ring_hkv[jv % kMetaRing], ring_row[jv % kMetaRing],
+                      &sm.v_full[st]);
+        return true;
+      };
+      (void)v_hkv;
+      (void)v_tk;
       while (ok) {
         const int u = atomicAdd(&p.tile_counter[0], 1);
         if (u >= n_units) break;
@@ -200,24 +249,32 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int hkv = h / G;
         for (int kt = 0; kt < nkv; ++kt, ++j) {
           const int st = j % kPStages;
-          if (!mbar_wait(&sm.kv_empty[st], ((uint32_t)(j / kPStages) & 1u) ^ 1u, p.status)) { ok = false; break; }
-          PTileMeta& m = sm.meta[st];
+          if (!mbar_wait(&sm.k_empty[st], ((uint32_t)(j / kPStages) & 1u) ^ 1u, p.status)) { ok = false; break; }
+          PTileMeta& m = sm.meta[j % kMetaRing];
           m.b = b; m.h = h; m.q0 = q0; m.kvt = kt;
           m.tq = tq; m.tk = tk; m.Lq = Lq; m.Lkv = Lkv;
           m.first = kt == 0; m.last = kt == nkv - 1; m.qbuf = qb; m.unit = u;
-          mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileB);
-          for (int bx = 0; bx < 2; ++bx) {
-            tma_load_3d(sm.kv[st][0] + bx * (kKT * 128), &tmK, bx * 64, hkv, tk + kt * kKT, &sm.kv_full[st]);
-            tma_load_3d(sm.kv[st][1] + bx * (kKT * 128), &tmV, bx * 64, hkv, tk + kt * kKT, &sm.kv_full[st]);
+          ring_hkv[j % kMetaRing] = hkv;
+          ring_row[j % kMetaRing] = tk + kt * kKT;
+          mbar_arrive_expect_tx(&sm.k_full[st], kTileB);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_3d(sm.k[st] + bx * (kKT * 128), &tmK, bx * 64, hkv, tk + kt * kKT, &sm.k_full[st]);
+          if (v_next < j) {
+            if (!load_v(v_next)) { ok = false; break; }
+            ++v_next;
           }
         }
         ++u_local;
       }
-      if (ok) {  // sentinel
+      while (ok && v_next < j) {  // V of the last tiles
+        if (!load_v(v_next)) { ok = false; break; }
+        ++v_next;
+      }
+      if (ok) {  // sentinel tile
         const int st = j % kPStages;
-        if (mbar_wait(&sm.kv_empty[st], ((uint32_t)(j / kPStages) & 1u) ^ 1u, p.status)) {
-          sm.meta[st].unit = -1;
-          mbar_arrive(&sm.kv_full[st]);
+        if (mbar_wait(&sm.k_empty[st], ((uint32_t)(j / kPStages) & 1u) ^ 1u, p.status)) {
+          sm.meta[j % kMetaRing].unit = -1;
+          mbar_arrive(&sm.k_full[st]);
         }
       }
     }
@@ -227,23 +284,25 @@ __global__ void __launch_bounds__(kPThreads, 1)
       constexpr uint32_t idesc_qk = umma_idesc_f16(DT == kBF16, 0, 0, kQT, kKT);
       constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 0, 1, kQT, kPD);
       int o_uses = 0;  // units whose first PV (which overwrites O) has been issued
-      // O += P(jj) . V(jj); the first PV of a unit overwrites O, after the previous
-      // unit's epilogue has read it (o_free phase o_uses - 1)
+      // O += P(jj) . V(jj), P from TMEM; the first PV of a unit overwrites O, after the
+      // previous unit's epilogue has read it (o_free phase o_uses - 1)
       auto issue_pv = [&](int jj, bool first_of_unit) -> bool {
-        if (!mbar_wait(&sm.p_full, (uint32_t)jj & 1u, p.status)) return false;
+        const int pb = jj & 1, vs = jj % kPStages;
+        if (!mbar_wait(&sm.p_full[pb], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
+        if (!mbar_wait(&sm.v_full[vs], (uint32_t)(jj / kPStages) & 1u, p.status)) return false;
         if (first_of_unit && o_uses > 0 && !mbar_wait(&sm.o_free, (uint32_t)(o_uses - 1) & 1u, p.status))
           return false;
         tc_fence_after();
-        const int st = jj % kPStages;
-        const uint32_t pbase = smem_u32(sm.p), vbase = smem_u32(sm.kv[st][1]);
+        const uint32_t vbase = smem_u32(sm.v[vs]);
 #pragma unroll
         for (int s = 0; s < kKT / 16; ++s) {
-          const uint64_t a = umma_desc(pbase + (s >> 2) * (kQT * 128) + (s & 3) * 32, 16, 1024);
           const uint64_t bd = umma_desc(vbase + s * 16 * 128, kKT * 128, 1024);
-          umma_f16(tmem + kColO, a, bd, idesc_pv, (first_of_unit && s == 0) ? 0u : 1u);
+          umma_f16_ta(tmem + kColO, tmem + kColP + pb * 64 + s * 8, bd, idesc_pv,
+                      (first_of_unit && s == 0) ? 0u : 1u);
         }
         umma_commit(&sm.pv_done);
-        umma_commit(&sm.kv_empty[st]);
+        umma_commit(&sm.p_free[pb]);
+        umma_commit(&sm.v_empty[vs]);
         if (first_of_unit) ++o_uses;
         return true;
       };
@@ -251,8 +310,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       bool prev_first = false;
       while (true) {
         const int st = j % kPStages;
-        if (!mbar_wait(&sm.kv_full[st], (uint32_t)(j / kPStages) & 1u, p.status)) break;
-        const PTileMeta meta = sm.meta[st];
+        if (!mbar_wait(&sm.k_full[st], (uint32_t)(j / kPStages) & 1u, p.status)) break;
+        const PTileMeta meta = sm.meta[j % kMetaRing];
         if (meta.unit < 0) {
           if (j > 0) issue_pv(j - 1, prev_first);
           mbar_arrive(&sm.s_full[j & 1]);  // lets the softmax warps see the sentinel
@@ -263,7 +322,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int sb = j & 1;
         if (!mbar_wait(&sm.s_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
         tc_fence_after();
-        const uint32_t qbase = smem_u32(sm.q[qb]), kbase = smem_u32(sm.kv[st][0]);
+        const uint32_t qbase = smem_u32(sm.q[qb]), kbase = smem_u32(sm.k[st]);
 #pragma unroll
         for (int s = 0; s < kPD / 16; ++s) {
           const uint64_t a = umma_desc(qbase + (s >> 2) * (kQT * 128) + (s & 3) * 32, 16, 1024);
@@ -271,6 +330,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           umma_f16(tmem + kColS + sb * kKT, a, bd, idesc_qk, s > 0);
         }
         umma_commit(&sm.s_full[sb]);
+        umma_commit(&sm.k_empty[st]);
         if (meta.last) {
           umma_commit(&sm.q_empty[qb]);
           ++u_local;
@@ -282,19 +342,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ softmax, rescale, epilogue
+    // Two warpgroups split each query row: half 0 owns key columns 0-63 of S (and output
+    // channels 0-63 of O), half 1 columns 64-127.  Only the per-row tile maximum (and, at
+    // the end, the row sum) is exchanged through shared memory.
+    const int half = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row of the tile = TMEM lane
     const uint32_t tq_lane = tmem + ((uint32_t)(quad * 32) << 16);
+    const int c_base = half * 64;
     float m_run = -INFINITY;   // max used for the exponents (may lag the true max by < 2^8)
     float m_true = -INFINITY;  // true running max
-    float l_run = 0.f;         // sum of exponents relative to m_run
+    float l_run = 0.f;         // this half's sum of exponents relative to m_run
     int j = 0;
-    bool ok = true;
     while (true) {
       const int sb = j & 1;
-      if (!mbar_wait(&sm.s_full[sb], (uint32_t)(j >> 1) & 1u, p.status)) { ok = false; break; }
-      const int st = j % kPStages;
-      const PTileMeta meta = sm.meta[st];
+      if (!mbar_wait(&sm.s_full[sb], (uint32_t)(j >> 1) & 1u, p.status)) break;
+      const PTileMeta meta = sm.meta[j % kMetaRing];
       if (meta.unit < 0) break;
       tc_fence_after();
       if (meta.first) {
@@ -304,16 +367,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       const int qi = meta.q0 + r;            // query index within the sequence
       const bool row_ok = qi < meta.Lq;
-      const int k0 = meta.kvt * kKT;
-      // visible keys of this row in the tile: [k0, k_hi)
+      const int k0 = meta.kvt * kKT + c_base;
+      // visible keys of this row among this half's columns: [k0, k0 + nvis)
       int k_hi = meta.Lkv;
       if (p.causal) k_hi = min(k_hi, qi + (meta.Lkv - meta.Lq) + 1);
-      const int nvis = row_ok ? max(0, min(k_hi - k0, kKT)) : 0;
-      float s[kKT];
+      const int nvis = row_ok ? max(0, min(k_hi - k0, 64)) : 0;
+      float s[64];
 #pragma unroll
-      for (int c = 0; c < kKT; c += 32) {
+      for (int c = 0; c < 64; c += 32) {
         float v[32];
-        tmem_ld32(tq_lane + kColS + sb * kKT + c, v);
+        tmem_ld32(tq_lane + kColS + sb * kKT + c_base + c, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c + i] = v[i];
       }
@@ -322,10 +385,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (lane == 0) mbar_arrive(&sm.s_free[sb]);
       float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kKT; ++c) {
+      for (int c = 0; c < 64; ++c) {
         s[c] = (c < nvis) ? s[c] * p.scale_log2 : -INFINITY;
         mt = fmaxf(mt, s[c]);
       }
+      sm.rmax[sb][half][r] = mt;
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+      mt = fmaxf(mt, sm.rmax[sb][half ^ 1][r]);
       const float m_old = m_run;
       m_true = fmaxf(m_true, mt);
       bool rescale = false;
@@ -339,62 +405,56 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       float lsum = 0.f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < kKT; ++c) {
-        s[c] = fast_exp2(s[c] - m_use);
-        lsum += s[c];
+      for (int c = 0; c < 64; c += 2) {
+        const float e0 = fast_exp2(s[c] - m_use), e1 = fast_exp2(s[c + 1] - m_use);
+        lsum += e0 + e1;
+        pk[c >> 1] = (DT == kBF16) ? pack_bf16(e0, e1) : pack_f16(e0, e1);
       }
       l_run = fmaf(l_run, alpha, lsum);
-      // the previous tile's PV must be complete before P is overwritten or O rescaled
-      if (j > 0 && !mbar_wait(&sm.pv_done, (uint32_t)(j - 1) & 1u, p.status)) { ok = false; break; }
-      // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp rescales when
-      // any of its rows needs it, the other rows with a factor of 1
+      // O rescale (rare): the previous tile's PV must be complete and this tile's not begun.
+      // tcgen05.ld/st are warp-collective (.sync.aligned), so the whole warp takes part,
+      // rows that do not need it with a factor of 1.
       if (__any_sync(0xffffffffu, rescale && !meta.first)) {
+        if (!mbar_wait(&sm.pv_done, (uint32_t)(j - 1) & 1u, p.status)) break;
         const float f = (rescale && !meta.first) ? alpha : 1.f;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kPD; c += 32) {
+        for (int c = 0; c < 64; c += 32) {
           float o[32];
-          tmem_ld32(tq_lane + kColO + c, o);
+          tmem_ld32(tq_lane + kColO + c_base + c, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= f;
-          tmem_st32(tq_lane + kColO + c, o);
+          tmem_st32(tq_lane + kColO + c_base + c, o);
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      // P row r: 128 keys as 16 chunks of 8 16-bit values
-#pragma unroll
-      for (int c = 0; c < kKT / 8; ++c) {
-        uint4 w;
-        if (DT == kBF16) {
-          w = make_uint4(pack_bf16(s[8 * c], s[8 * c + 1]), pack_bf16(s[8 * c + 2], s[8 * c + 3]),
-                         pack_bf16(s[8 * c + 4], s[8 * c + 5]), pack_bf16(s[8 * c + 6], s[8 * c + 7]));
-        } else {
-          w = make_uint4(pack_f16(s[8 * c], s[8 * c + 1]), pack_f16(s[8 * c + 2], s[8 * c + 3]),
-                         pack_f16(s[8 * c + 4], s[8 * c + 5]), pack_f16(s[8 * c + 6], s[8 * c + 7]));
-        }
-        *reinterpret_cast<uint4*>(sm.p + tile_chunk_offset(r, c)) = w;
-      }
-      fence_proxy_async_smem();
+      // this half of P row r (64 keys = 32 packed columns) into the P buffer of this tile
+      if (!mbar_wait(&sm.p_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
+      tmem_st32u(tq_lane + kColP + sb * 64 + half * 32, pk);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full);
+      if (lane == 0) mbar_arrive(&sm.p_full[sb]);
       if (meta.last) {
         // epilogue: wait for this tile's PV, normalise O and write out, max and sum
-        if (!mbar_wait(&sm.pv_done, (uint32_t)j & 1u, p.status)) { ok = false; break; }
+        if (!mbar_wait(&sm.pv_done, (uint32_t)j & 1u, p.status)) break;
         tc_fence_after();
+        sm.lsum[half][r] = l_run;
+        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        const float l_row = l_run + sm.lsum[half ^ 1][r];  // relative to m_run
         const float sink2 = p.sink ? p.sink[meta.h] * kLog2e : -INFINITY;
         const float m_fin = fmaxf(m_true, sink2);
-        float denom = l_run;  // relative to m_run
+        float denom = l_row;
         if (p.sink && m_run != -INFINITY) denom += fast_exp2(sink2 - m_run);
         const float inv = denom > 0.f ? 1.f / denom : 0.f;
         const int64_t tok = (int64_t)meta.tq + qi;
         // every lane takes part in the (warp-collective) TMEM loads; only valid rows store
-        uint8_t* orow = static_cast<uint8_t*>(p.out) + (tok * p.Nq + meta.h) * (int64_t)kPD * 2;
+        uint8_t* orow = static_cast<uint8_t*>(p.out) + ((tok * p.Nq + meta.h) * (int64_t)kPD + c_base) * 2;
 #pragma unroll
-        for (int c = 0; c < kPD; c += 32) {
+        for (int c = 0; c < 64; c += 32) {
           float o[32];
-          tmem_ld32(tq_lane + kColO + c, o);
+          tmem_ld32(tq_lane + kColO + c_base + c, o);
           if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
@@ -409,10 +469,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
           }
         }
-        if (row_ok) {
+        if (row_ok && half == 0) {
           float sum_true = 0.f;
           if (m_fin != -INFINITY) {
-            sum_true = (m_run == -INFINITY) ? 0.f : l_run * fast_exp2(m_run - m_fin);
+            sum_true = (m_run == -INFINITY) ? 0.f : l_row * fast_exp2(m_run - m_fin);
             if (p.sink) sum_true += fast_exp2(sink2 - m_fin);
           }
           if (p.softmax_max) p.softmax_max[tok * p.Nq + meta.h] = (m_fin == -INFINITY) ? -INFINITY : m_fin * kLn2;
@@ -424,7 +484,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       ++j;
     }
-    (void)ok;
   }
 
   tc_fence_before();
@@ -450,7 +509,7 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const
   prefill_plan_kernel<<<1, 1024, sizeof(int) * (max_key_tiles + 2), stream>>>(p, max_key_tiles);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(PSmem) + 1024;
+  const size_t smem = sizeof(PSmem);
   if (p.dtype == kBF16) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

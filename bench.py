@@ -327,6 +327,173 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+def prefill_flops(case: W.PrefillCase, causal=True) -> int:
+    """Algorithmic FLOPs of one prefill: 4 * D per visible (query, key) pair and query head
+    (2 for the score, 2 for the value product); masked pairs are not counted."""
+    pairs = 0
+    for Lq, Lk in zip(case.lengths_q.tolist(), case.lengths_kv.tolist()):
+        if not causal:
+            pairs += Lq * Lk
+            continue
+        i = np.arange(Lq, dtype=np.int64)
+        pairs += int(np.clip(i + (Lk - Lq) + 1, 0, Lk).sum())
+    return 4 * case.D * case.Nq * pairs
+
+
+def run_prefill_bench(args, rank, world, local_rank):
+    import torch
+    import attention_ifa_fia_gb300 as F
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from parity import DevicePrefill
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    case = W.causal_prefill_tnd(1004 + 97 * rank)
+    flops = prefill_flops(case)
+    copies = [DevicePrefill(case, dev) for _ in range(COPIES)]
+    msq, mskv = int(case.lengths_q.max()), int(case.lengths_kv.max())
+    ws = torch.empty(F.fia_prefill_workspace_size(case.B, case.Nq, case.Nkv, case.D, msq), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty((case.T, case.Nq, case.D), dtype=copies[0].q.dtype, device=dev)
+    mx = torch.empty((case.T, case.Nq), dtype=torch.float32, device=dev)
+    sm = torch.empty_like(mx)
+
+    def step(i):
+        c = copies[i % COPIES]
+        F.fia_prefill(c.q, c.k, c.v, c.cu_q, c.cu_kv, max_seqlen_q=msq, max_seqlen_kv=mskv, num_heads=case.Nq,
+                      num_kv_heads=case.Nkv, scale=case.scale, mask=3, out=out, softmax_max=mx, softmax_sum=sm,
+                      workspace=ws)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    t_w = time.time()
+    i = 0
+    while i < args.warmup or time.time() - t_w < args.min_warmup_s:
+        step(i)
+        i += 1
+        if i % 32 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    F.fia_device_status()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    F.fia_trace_enable(True)
+    F.fia_trace_collect(F.KERNEL_PREFILL)
+    h0 = time.time()
+    e0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    F.fia_trace_enable(False)
+    ms = e0.elapsed_time(e1)
+    pf_ms, pf_n = F.fia_trace_collect(F.KERNEL_PREFILL)
+    status = F.fia_device_status()
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    # end to end: q, k, v and cumulative lengths from pinned host memory, out/max/sum back
+    pins = [(torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory().copy_(c.q),
+             torch.empty(c.k.shape, dtype=c.k.dtype).pin_memory().copy_(c.k),
+             torch.empty(c.v.shape, dtype=c.v.dtype).pin_memory().copy_(c.v),
+             torch.empty(c.cu_q.shape, dtype=c.cu_q.dtype).pin_memory().copy_(c.cu_q)) for c in copies]
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_mx = torch.empty(mx.shape, dtype=mx.dtype).pin_memory()
+    h_sm = torch.empty(sm.shape, dtype=sm.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pins[0]) + pins[0][3].numel() * 8
+    d2h = h_out.numel() * h_out.element_size() + 2 * h_mx.numel() * 4
+
+    def e2e_step(i):
+        j = i % COPIES
+        c, pq = copies[j], pins[j]
+        c.q.copy_(pq[0], non_blocking=True)
+        c.k.copy_(pq[1], non_blocking=True)
+        c.v.copy_(pq[2], non_blocking=True)
+        c.cu_q.copy_(pq[3], non_blocking=True)
+        c.cu_kv.copy_(pq[3], non_blocking=True)
+        step(i)
+        h_out.copy_(out, non_blocking=True)
+        h_mx.copy_(mx, non_blocking=True)
+        h_sm.copy_(sm, non_blocking=True)
+
+    for k in range(min(args.warmup, 10)):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for k in range(args.steps):
+        e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    sampler.stop()
+    if rank != 0:
+        return None
+    hbm, tf_burst, tf_sus, src = peaks()
+    tflops = world * flops * args.steps / (ms / 1e3) / 1e12
+    achieved = flops / (pf_ms / pf_n / 1e3) / 1e12 if pf_n else None
+    line = {
+        "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "causal_prefill_tnd", "B": case.B, "T": case.T, "Nq": case.Nq, "Nkv": case.Nkv,
+                   "D": case.D, "lengths": case.lengths_q.tolist(), "causal_flops_per_step": flops,
+                   "l2": f"inputs rotated over {COPIES} device copies",
+                   "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2) if achieved else None, "peak": tf_burst,
+                     "unit": "TFLOP/s", "frac": round(achieved / tf_burst, 4) if achieved else None,
+                     "traffic": None, "kernel": "prefill_tc (plan + attention, traced together)",
+                     "peak_source": f"{src} bf16 dense burst (MEASURED_PEAKS.json bf16_tflops)"},
+        "e2e": {"value": round(world * flops * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "per step: q, k, v, cumulative lengths host->device; out, max, sum device->host"},
+        "gpu_launches": 2 * pf_n, "device_status": status, "clocks": sampler.summary(h0, h1),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(case)
+    return line
+
+
+def cpu_baseline_prefill(case: W.PrefillCase, budget_s: float = 15.0, seed: int = 0):
+    """The oracle on a sample of (token, head) rows, in algorithmic TFLOP/s of that sample."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    total = case.T * case.Nq
+    n = 256
+    while True:
+        rows = rng.choice(total, size=min(n, total), replace=False).astype(np.int64)
+        t = time.perf_counter()
+        oracle.prefill(case.q, case.k, case.v, case.cu_q, case.cu_kv, Nq=case.Nq, Nkv=case.Nkv, D=case.D,
+                       scale=case.scale, causal=True, dtype=oracle.BF16, rows=rows)
+        dt = time.perf_counter() - t
+        if dt > budget_s / 4 or n >= total:
+            break
+        n = min(total, int(n * max(2.0, budget_s / max(dt, 1e-3) * 0.8)))
+    tok = rows // case.Nq
+    b = np.searchsorted(case.cu_q, tok, side="right") - 1
+    qi = tok - case.cu_q[b]
+    Lq = case.lengths_q[b]
+    Lk = case.lengths_kv[b]
+    vis = np.clip(qi + (Lk - Lq) + 1, 0, Lk)
+    fl = 4 * case.D * int(vis.sum())
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} of {total} (token, head) rows; {dt:.1f} s of fp64 CPU work",
+            "seconds": round(dt, 2)}
+
+
 def load_traffic(workload):
     """DRAM bytes (read + write) per launch of the attention kernel from the committed ncu
     summary, or None if that summary was taken on a different version of the kernel source."""
@@ -380,7 +547,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bf16_gqa_decode",
-                    choices=["bf16_gqa_decode", "int8_antiquant_decode", "long_ctx_sink_decode", "tiny_decode"])
+                    choices=["bf16_gqa_decode", "int8_antiquant_decode", "long_ctx_sink_decode", "tiny_decode",
+                             "causal_prefill_tnd"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep warming up for at least this long (clocks settle, the sampler sees load)")
@@ -396,7 +564,10 @@ def main():
             import torch.distributed as dist
             torch.cuda.set_device(local_rank)
             dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-        line = run_ours(args, rank, world, local_rank)
+        if args.workload == "causal_prefill_tnd":
+            line = run_prefill_bench(args, rank, world, local_rank)
+        else:
+            line = run_ours(args, rank, world, local_rank)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
