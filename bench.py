@@ -311,7 +311,8 @@ def run_ours(args, rank, world, local_rank):
         "kernels_ms_per_launch": {k: round(v[0] / v[1], 5) if v[1] else None for k, v in kern.items()},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None, "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4) if achieved else None,
-                     "traffic": traffic, "kernel": "decode_splitkv (split-KV attention)",
+                     "traffic": traffic, "kernel": "decode_tc (tcgen05 split-KV attention)" if case.kv_dtype != W.INT8
+                     else "decode_splitkv (CUDA-core split-KV attention)",
                      "peak_source": f"{src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(world * nbytes["total"] * steps / (ms_e2e / 1e3) / 1e9, 1), "unit": "GB/s",
@@ -455,7 +456,8 @@ def run_prefill_bench(args, rank, world, local_rank):
                    "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2) if achieved else None, "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": round(achieved / tf_burst, 4) if achieved else None,
-                     "traffic": None, "kernel": "prefill_tc (plan + attention, traced together)",
+                     "traffic": load_traffic("causal_prefill_tnd"),
+                     "kernel": "prefill_tc (plan + attention, traced together)",
                      "peak_source": f"{src} bf16 dense burst (MEASURED_PEAKS.json bf16_tflops)"},
         "e2e": {"value": round(world * flops * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -495,17 +497,24 @@ def cpu_baseline_prefill(case: W.PrefillCase, budget_s: float = 15.0, seed: int 
 
 
 def load_traffic(workload):
-    """DRAM bytes (read + write) per launch of the attention kernel from the committed ncu
-    summary, or None if that summary was taken on a different version of the kernel source."""
+    """DRAM bytes (read + write) per launch of the dominant kernel from the committed ncu summary
+    (profiles/kernel_traffic.json), or None if the kernel source changed since it was taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    src = os.path.join(ROOT, "attention_ifa_fia_gb300", "csrc", "decode.cu")
+    path = os.path.join(ROOT, "profiles", "kernel_traffic.json")
+    csrc = os.path.join(ROOT, "attention_ifa_fia_gb300", "csrc")
     try:
         with open(path) as f:
             d = json.load(f)
-        with open(src, "rb") as f:
-            sha = hashlib.sha1(f.read()).hexdigest()[:12]
-        return d.get(workload) if d.get("decode.cu sha1 prefix") == sha else None
+        if workload == "causal_prefill_tnd":
+            with open(os.path.join(csrc, "prefill.cu"), "rb") as f:
+                sha = hashlib.sha1(f.read()).hexdigest()[:12]
+            return d.get(workload) if d.get("prefill source sha1") == sha else None
+        blob = b""
+        for name in ("decode_tc.cu", "decode.cu"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                blob += f.read()
+        sha = hashlib.sha1(blob).hexdigest()[:12]
+        return d.get(workload) if d.get("decode sources sha1") == sha else None
     except Exception:
         return None
 
