@@ -6,23 +6,28 @@
 // the paged cache, token t read from block block_table[b][t / bs], row t % bs of
 // the (blocknum, KV_N, blocksize, D) pool, with kv head h / (Nq / Nkv).
 //
-// Structure (three launches on the caller's stream):
-//   1. plan     -- one CTA splits every (b, kv-head) sequence into work items of
-//                  `chunk_tokens` tokens and resets the work counter.
-//   2. attention -- persistent CTAs (one per SM).  Warp 8 is the producer: it
-//                  takes items from the counter, reads the block table and issues
-//                  TMA tile loads (2-D tensor maps over the pool, 128- or 64-byte
-//                  swizzle) of K and V into a 4-stage mbarrier ring, plus the
-//                  item's G query rows by a 1-D bulk copy.  Warps 0-7 compute, for
-//                  the whole GQA group at once: scores from registers-resident q,
-//                  a warp-shuffle online softmax (max and sum), and P.V.  Each item
-//                  leaves a normalised partial (o, max, sum) in the workspace.
-//   3. merge    -- one CTA per (b, kv-head) folds the item partials in order by the
-//                  RingAttentionUpdate rule, adds the sink once, and writes out,
-//                  softmax max and softmax sum.
+// Structure (two launches on the caller's stream):
+//   1. plan      -- one CTA splits every (b, kv-head) sequence into work items of
+//                   `chunk_tokens` tokens, zeroes the per-segment completion
+//                   counters and resets the work counter.
+//   2. attention -- persistent CTAs (one per SM), launched with programmatic
+//                   dependent launch so that their prologue overlaps the plan.
+//                   This file holds the CUDA-core variant (used for int8 KV; the
+//                   tensor-core variant for 16-bit KV is in decode_tc.cu).  Warp 8
+//                   is the producer: it takes items from the counter, reads the
+//                   block table and issues TMA tile loads (2-D tensor maps over the
+//                   pool, 128- or 64-byte swizzle) of K and V into a 4-stage
+//                   mbarrier ring, plus the item's G query rows by a 1-D bulk copy.
+//                   Warps 0-7 compute, for the whole GQA group at once: scores from
+//                   register-resident q, a warp-shuffle online softmax (max and
+//                   sum), and P.V.  A segment of one item writes the final output
+//                   directly; otherwise each item leaves a normalised partial
+//                   (o, max, sum) and the CTA that completes a segment's last item
+//                   folds the partials in order by the RingAttentionUpdate rule,
+//                   adds the sink once and writes out, softmax max and sum.
 // Scores are kept in log2 units (scale * log2 e folded into the dot product) and
 // converted back to the natural-exp domain for the max output.
-#include "fia_device.cuh"
+#include "decode_common.cuh"
 
 namespace fia {
 namespace {
@@ -66,7 +71,7 @@ struct Cfg {
 
 struct __align__(16) StageMeta {
   int b, hkv, tok0, n;  // tile start token and valid tokens
-  int item, first, last, pad;
+  int item, first, last, nch;  // nch: items of this (b, kv head) segment
 };
 
 template <int KVT, int D, int GP>
@@ -115,25 +120,44 @@ __device__ __forceinline__ float q_elem(const uint16_t* q, int idx, int q_dtype)
 }
 
 // ------------------------------------------------------------------- plan
+constexpr int kPlanSmemB = 4096;  // batches whose item offsets fit in shared memory
+
+__device__ __forceinline__ int clamp_len(const DecodeParams& p, int b, bool flag) {
+  const int64_t raw = p.seq_lens[b];
+  if (flag && (raw < 0 || raw > p.max_kv_len)) raise_status(p.status, kStatusLengthClamped);
+  return (int)(raw < 0 ? 0 : (raw > p.max_kv_len ? p.max_kv_len : raw));
+}
+
+// Rows of a batch with no visible key: out 0, max -inf and sum 0, or with a sink
+// max = sink and sum 1 (no work item covers them).
+__device__ void write_empty_batch(const DecodeParams& p, int b) {
+  for (int h = 0; h < p.Nq; ++h) {
+    if (p.softmax_max) p.softmax_max[(int64_t)b * p.Nq + h] = p.sink ? p.sink[h] : -INFINITY;
+    if (p.softmax_sum) p.softmax_sum[(int64_t)b * p.Nq + h] = p.sink ? 1.f : 0.f;
+  }
+  uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (int64_t)b * p.Nq * p.D * 2);
+  for (int i = 0; i < p.Nq * p.D * 2 / 16; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
+  griddep_launch_dependents();  // the attention kernel may begin its prologue
+  extern __shared__ int sbase[];  // [B + 1] item offsets when B <= kPlanSmemB
   __shared__ int warp_tot[32];
   __shared__ int carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool in_smem = p.B <= kPlanSmemB;
   if (tid == 0) carry = 0;
   __syncthreads();
   const int C = p.chunk_tokens;
   for (int b0 = 0; b0 < p.B; b0 += 1024) {
     const int b = b0 + tid;
-    int L = 0, nch = 0;
+    int nch = 0;
     if (b < p.B) {
-      int64_t raw = p.seq_lens[b];
-      if (raw < 0 || raw > p.max_kv_len) raise_status(p.status, kStatusLengthClamped);
-      L = (int)(raw < 0 ? 0 : (raw > p.max_kv_len ? p.max_kv_len : raw));
-      nch = (L + C - 1) / C;
+      nch = (clamp_len(p, b, true) + C - 1) / C;
+      if (nch == 0) write_empty_batch(p, b);
     }
-    int cnt = nch * p.Nkv;
-    // inclusive warp scan, then across warps
-    int x = cnt;
+    const int cnt = nch * p.Nkv;
+    int x = cnt;  // inclusive warp scan, then across warps
     for (int o = 1; o < 32; o <<= 1) {
       int y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
@@ -152,18 +176,35 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     const int base = carry + (warp ? warp_tot[warp - 1] : 0) + x - cnt;
     if (b < p.B) {
       p.ws.seg_base[b] = base;
-      for (int h = 0; h < p.Nkv; ++h)
-        for (int j = 0; j < nch; ++j) {
-          const int t0 = j * C, t1 = min(L, t0 + C);
-          p.ws.items[base + h * nch + j] = make_int4(b, h, t0, t1);
-        }
+      if (in_smem) sbase[b] = base;
+      if (!in_smem)  // large batch counts: each thread lists its own batch's items
+        for (int h = 0; h < p.Nkv; ++h)
+          for (int j = 0; j < nch; ++j)
+            p.ws.items[base + h * nch + j] = make_int4(b, h, (nch << 16) | j, min(clamp_len(p, b, false), (j + 1) * C));
     }
     __syncthreads();
     if (tid == 1023) carry = base + cnt;
     __syncthreads();
   }
+  const int total = carry;
+  if (in_smem) {
+    if (tid == 0) sbase[p.B] = total;
+    __syncthreads();
+    for (int i = tid; i < total; i += blockDim.x) {  // all items in parallel
+      int lo = 0, hi = p.B;                          // last b with sbase[b] <= i
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (sbase[mid] <= i) lo = mid;
+        else hi = mid;
+      }
+      const int b = lo, r = i - sbase[b];
+      const int nch = (sbase[b + 1] - sbase[b]) / p.Nkv;
+      const int h = r / nch, j = r - h * nch;
+      p.ws.items[i] = make_int4(b, h, (nch << 16) | j, min(clamp_len(p, b, false), (j + 1) * C));
+    }
+  }
   if (tid == 0) {
-    *p.ws.n_items = carry;
+    *p.ws.n_items = total;
     *p.ws.counter = 0;
   }
 }
@@ -196,6 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  griddep_wait();  // the plan kernel's item list, counters and reset are complete and visible
+  griddep_launch_dependents();  // the merge kernel may be scheduled; it waits for this grid to finish
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer
@@ -214,10 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t piece_bytes = (uint32_t)box_rows * C::kBoxBytes * C::kNumBoxes;  // one of K/V
     while (ok && next < n_items) {
       const int item = next;
-      const int4 desc = p.ws.items[item];
+      const DecodeItem it = decode_item(p.ws.items[item], p.chunk_tokens);
       if (lane == 0) next = atomicAdd(p.ws.counter, 1);
       next = __shfl_sync(0xffffffffu, next, 0);
-      const int b = desc.x, hkv = desc.y, t_begin = desc.z, t_end = desc.w;
+      const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
       const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
       for (int tok0 = t_begin; tok0 < t_end; tok0 += kTT) {
         const int n = min(kTT, t_end - tok0);
@@ -237,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           StageMeta& m = sm.meta[stage];
           m.b = b; m.hkv = hkv; m.tok0 = tok0; m.n = n;
-          m.item = item; m.first = first; m.last = (tok0 + kTT >= t_end);
+          m.item = item; m.first = first; m.last = (tok0 + kTT >= t_end); m.nch = it.nch;
           mbar_arrive_expect_tx(&sm.full[stage], bytes);
         }
         __syncwarp();
@@ -468,15 +511,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < C::EV; ++e) sm.red[warp][g * D + pv_c * C::EV + e] = acc[g][e];
       }
       named_bar_sync(kBarConsumers, kDecodeConsumers);
-      float* po = p.ws.part_o + (int64_t)meta.item * G * D;
-      for (int o = tid; o < G * D; o += kDecodeConsumers) {
-        float s = 0.f;
+      if (meta.nch == 1) {
+        // the segment is this one item: write the final output directly
+        for (int o = tid; o < G * D; o += kDecodeConsumers) {
+          float s = 0.f;
 #pragma unroll
-        for (int w2 = 0; w2 < kConsumerWarps; ++w2) s += sm.red[w2][o];
-        const float l = sm.l_run[o / D];
-        po[o] = l > 0.f ? s / l : 0.f;
+          for (int w2 = 0; w2 < kConsumerWarps; ++w2) s += sm.red[w2][o];
+          const int g = o / D, h = meta.hkv * G + g;
+          float M, W;
+          const float v = single_item_output(s, sm.m_run[g], sm.l_run[g], p.sink, h, &M, &W);
+          const int64_t oi = ((int64_t)meta.b * p.Nq + meta.hkv * G) * D + o;
+          if (p.q_dtype == kBF16) store_out<kBF16>(p.out, oi, v);
+          else store_out<kF16>(p.out, oi, v);
+          if (o % D == 0) {
+            if (p.softmax_max) p.softmax_max[(int64_t)meta.b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+            if (p.softmax_sum) p.softmax_sum[(int64_t)meta.b * p.Nq + h] = W;
+          }
+        }
+      } else {
+        float* po = p.ws.part_o + (int64_t)meta.item * G * D;
+        for (int o = tid; o < G * D; o += kDecodeConsumers) {
+          float s = 0.f;
+#pragma unroll
+          for (int w2 = 0; w2 < kConsumerWarps; ++w2) s += sm.red[w2][o];
+          const float l = sm.l_run[o / D];
+          po[o] = l > 0.f ? s / l : 0.f;
+        }
+        if (tid < G) p.ws.part_ml[(int64_t)meta.item * G + tid] = make_float2(sm.m_run[tid], sm.l_run[tid]);
       }
-      if (tid < G) p.ws.part_ml[(int64_t)meta.item * G + tid] = make_float2(sm.m_run[tid], sm.l_run[tid]);
       named_bar_sync(kBarConsumers, kDecodeConsumers);
     }
     if (++stage == kDecodeStages) { stage = 0; phase ^= 1u; }
@@ -484,50 +546,85 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------- merge
+// One CTA per (b, kv head) segment of two or more work items (segments of one item are
+// written by the attention kernel, empty batches by the plan).  Partials are folded in
+// order by the RingAttentionUpdate rule, each weighted by its own sum, with the sink
+// added once (aclnnRingAttentionUpdate; aclnnFlashAttentionScoreV4 sink formula):
+//   M = max(sink, max_j m_j),  W = sum_j l_j 2^{m_j - M} + 2^{sink - M},
+//   out = sum_j o_j l_j 2^{m_j - M} / W,  softmax_max = M ln 2,  softmax_sum = W.
+// Launched dependent on the attention kernel: its launch overlaps that kernel's tail.
+constexpr int kMergeThreads = 256;
+
 template <int QT>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
-  extern __shared__ float wts[];  // [G][nch]
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
+  griddep_wait();  // every partial of the attention kernel is written and visible
+  extern __shared__ float2 ml[];  // [G][nch]: (max, sum), then (weight, -) per partial
   const int b = blockIdx.x / p.Nkv, hkv = blockIdx.x % p.Nkv;
+  const int C = p.chunk_tokens;
+  const int nch = (clamp_len(p, b, false) + C - 1) / C;
+  if (nch <= 1) return;
   const int G = p.G, D = p.D, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int64_t raw = p.seq_lens[b];
-  const int L = (int)(raw < 0 ? 0 : (raw > p.max_kv_len ? p.max_kv_len : raw));
-  const int nch = (L + p.chunk_tokens - 1) / p.chunk_tokens;
-  const int base = p.ws.seg_base[b] + hkv * nch;
-  for (int g = warp; g < G; g += 8) {
+  const int first = p.ws.seg_base[b] + hkv * nch;
+  for (int i = tid; i < G * nch; i += kMergeThreads) {  // coalesced: partial-major in memory
+    const int j = i / G, g = i - j * G;
+    ml[g * nch + j] = p.ws.part_ml[(int64_t)first * G + i];
+  }
+  __syncthreads();
+  for (int g = warp; g < G; g += kMergeThreads / 32) {
     const int h = hkv * G + g;
+    float2* row = ml + g * nch;
     float M = -INFINITY;
-    for (int j = lane; j < nch; j += 32) M = fmaxf(M, p.ws.part_ml[(int64_t)(base + j) * G + g].x);
+    for (int j = lane; j < nch; j += 32) M = fmaxf(M, row[j].x);
 #pragma unroll
     for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float sink2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
     M = fmaxf(M, sink2);
     float W = 0.f;
-    if (M != -INFINITY) {
-      for (int j = lane; j < nch; j += 32) {
-        const float2 ml = p.ws.part_ml[(int64_t)(base + j) * G + g];
-        const float w = (ml.x == -INFINITY) ? 0.f : ml.y * exp2f(ml.x - M);
-        wts[g * nch + j] = w;
-        W += w;
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
-      if (p.sink) W += exp2f(sink2 - M);
-      const float inv = W > 0.f ? 1.f / W : 0.f;
-      for (int j = lane; j < nch; j += 32) wts[g * nch + j] *= inv;
-    } else {
-      for (int j = lane; j < nch; j += 32) wts[g * nch + j] = 0.f;
+    for (int j = lane; j < nch; j += 32) {
+      const float w = (M == -INFINITY || row[j].x == -INFINITY) ? 0.f : row[j].y * exp2f(row[j].x - M);
+      row[j].x = w;
+      W += w;
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    if (p.sink && M != -INFINITY) W += exp2f(sink2 - M);
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    __syncwarp();
+    for (int j = lane; j < nch; j += 32) row[j].x *= inv;
     if (lane == 0) {
       if (p.softmax_max) p.softmax_max[(int64_t)b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
       if (p.softmax_sum) p.softmax_sum[(int64_t)b * p.Nq + h] = W;
     }
   }
   __syncthreads();
-  for (int o = tid; o < G * D; o += 256) {
-    const int g = o / D;
-    float acc = 0.f;
-    for (int j = 0; j < nch; ++j) acc = fmaf(wts[g * nch + j], p.ws.part_o[(int64_t)(base + j) * G * D + o], acc);
-    store_out<QT>(p.out, ((int64_t)b * p.Nq + hkv * G) * D + o, acc);
+  const float4* po = reinterpret_cast<const float4*>(p.ws.part_o + (int64_t)first * G * D);
+  const int q4n = G * D / 4;  // float4 outputs per partial
+  for (int q4 = tid; q4 < q4n; q4 += kMergeThreads) {
+    const float2* row = ml + ((q4 * 4) / D) * nch;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int j = 0;
+    for (; j + 4 <= nch; j += 4) {  // four independent loads in flight
+      const float4 v0 = po[(int64_t)(j + 0) * q4n + q4], v1 = po[(int64_t)(j + 1) * q4n + q4];
+      const float4 v2 = po[(int64_t)(j + 2) * q4n + q4], v3 = po[(int64_t)(j + 3) * q4n + q4];
+      const float w0 = row[j].x, w1 = row[j + 1].x, w2 = row[j + 2].x, w3 = row[j + 3].x;
+      acc.x = fmaf(w3, v3.x, fmaf(w2, v2.x, fmaf(w1, v1.x, fmaf(w0, v0.x, acc.x))));
+      acc.y = fmaf(w3, v3.y, fmaf(w2, v2.y, fmaf(w1, v1.y, fmaf(w0, v0.y, acc.y))));
+      acc.z = fmaf(w3, v3.z, fmaf(w2, v2.z, fmaf(w1, v1.z, fmaf(w0, v0.z, acc.z))));
+      acc.w = fmaf(w3, v3.w, fmaf(w2, v2.w, fmaf(w1, v1.w, fmaf(w0, v0.w, acc.w))));
+    }
+    for (; j < nch; ++j) {
+      const float4 v = po[(int64_t)j * q4n + q4];
+      const float w = row[j].x;
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    const int64_t o = ((int64_t)b * p.Nq + hkv * G) * D + q4 * 4;
+    store_out<QT>(p.out, o, acc.x);
+    store_out<QT>(p.out, o + 1, acc.y);
+    store_out<QT>(p.out, o + 2, acc.z);
+    store_out<QT>(p.out, o + 3, acc.w);
   }
 }
 
@@ -601,9 +698,9 @@ cudaError_t launch_attention(const DecodeParams& p, const CUtensorMap& tmK, cons
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);
-  kern<<<grid, kThreads, smem, stream>>>(tmK, tmV, p, box_rows);
+  e = launch_dependent(kern, grid, kThreads, smem, stream, tmK, tmV, p, box_rows);
   trace_mark(kKernelDecodeAttention, 1, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 template <int KVT, int D>
@@ -624,7 +721,6 @@ size_t decode_workspace_bytes(int B, int Nkv, int G, int D, int max_items) {
   s += up(sizeof(int4) * (size_t)max_items);           // items
   s += up(sizeof(float) * (size_t)max_items * G * D);  // part_o
   s += up(sizeof(float2) * (size_t)max_items * G);     // part_ml
-  (void)Nkv;
   return s;
 }
 
@@ -642,14 +738,14 @@ DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D,
   w.part_o = reinterpret_cast<float*>(c);
   c += up(sizeof(float) * (size_t)max_items * G * D);
   w.part_ml = reinterpret_cast<float2*>(c);
-  (void)Nkv;
   return w;
 }
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream) {
   trace_mark(kKernelDecodePlan, 0, stream);
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(p);
+  const size_t plan_smem = p.B <= kPlanSmemB ? sizeof(int) * (size_t)(p.B + 1) : 0;
+  decode_plan_kernel<<<1, 1024, plan_smem, stream>>>(p);
   trace_mark(kKernelDecodePlan, 1, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -667,20 +763,19 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const C
                     : launch_attention_g<kI8, 128>(p, tmK, tmV, box_rows, grid, stream);
   }
   if (e != cudaSuccess) return e;
+  // merge of segments with two or more items; dependent launch on the attention kernel
   const int max_chunks = (p.max_kv_len + p.chunk_tokens - 1) / p.chunk_tokens;
-  const size_t msmem = sizeof(float) * (size_t)p.G * (max_chunks > 0 ? max_chunks : 1);
-  trace_mark(kKernelDecodeMerge, 0, stream);
-  if (p.q_dtype == kBF16) {
-    if (msmem > 48 * 1024)
-      cudaFuncSetAttribute(decode_merge_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
-    decode_merge_kernel<kBF16><<<p.B * p.Nkv, 256, msmem, stream>>>(p);
-  } else {
-    if (msmem > 48 * 1024)
-      cudaFuncSetAttribute(decode_merge_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
-    decode_merge_kernel<kF16><<<p.B * p.Nkv, 256, msmem, stream>>>(p);
+  if (max_chunks <= 1) return cudaSuccess;
+  const size_t msmem = sizeof(float2) * (size_t)p.G * max_chunks;
+  auto merge = (p.q_dtype == kBF16) ? decode_merge_kernel<kBF16> : decode_merge_kernel<kF16>;
+  if (msmem > 48 * 1024) {
+    e = cudaFuncSetAttribute(merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+    if (e != cudaSuccess) return e;
   }
+  trace_mark(kKernelDecodeMerge, 0, stream);
+  e = launch_dependent(merge, p.B * p.Nkv, kMergeThreads, msmem, stream, p);
   trace_mark(kKernelDecodeMerge, 1, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_debug_dequant(const int8_t* codes, const float* scale, const float* offset, int64_t n,

@@ -21,7 +21,7 @@
 // the MMAs; warps 2-5 own TMEM lanes 0-127: online softmax of tile j (one token per
 // lane, warp-shuffle max across lanes) followed by the rescale-and-accumulate of
 // the PV result of tile j-1 (one output channel per lane).
-#include "fia_device.cuh"
+#include "decode_common.cuh"
 
 namespace fia {
 namespace {
@@ -50,6 +50,7 @@ struct TcCfg {
 struct __align__(16) TileMeta {
   int b, hkv, tok0, n;
   int item, first, last, qbuf;
+  int nch, pad0, pad1, pad2;  // nch: items of this (b, kv head) segment
 };
 
 template <int D>
@@ -114,6 +115,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  griddep_wait();  // the plan kernel's item list, counters and reset are complete and visible
+  griddep_launch_dependents();  // the merge kernel may be scheduled; it waits for this grid to finish
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -132,10 +135,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     next = __shfl_sync(0xffffffffu, next, 0);
     while (ok && next < n_items) {
       const int item = next;
-      const int4 desc = p.ws.items[item];
+      const DecodeItem it = decode_item(p.ws.items[item], p.chunk_tokens);
       if (lane == 0) next = atomicAdd(p.ws.counter, 1);
       next = __shfl_sync(0xffffffffu, next, 0);
-      const int b = desc.x, hkv = desc.y, t_begin = desc.z, t_end = desc.w;
+      const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
       const int qb = local_item & 1;
       if (!mbar_wait(&sm.q_empty[qb], ((local_item >> 1) & 1) ^ 1u, p.status)) { ok = false; break; }
       if (lane == 0) {
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           TileMeta& m = sm.meta[st];
           m.b = b; m.hkv = hkv; m.tok0 = tok0; m.n = n;
           m.item = item; m.first = (tok0 == t_begin); m.last = (tok0 + kT >= t_end); m.qbuf = qb;
+          m.nch = it.nch;
           if (bytes) mbar_arrive_expect_tx(&sm.kv_full[st], bytes);
           else mbar_arrive(&sm.kv_full[st]);
         }
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     for (int g = 0; g < GP; ++g) {
       m_run[g] = -INFINITY; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_fin[g] = -INFINITY; l_fin[g] = 0.f;
     }
-    int prev_item = -1;
+    int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
     bool prev_first = false, prev_last = false;
 
     // rescale-and-accumulate of the PV result of tile jj; finalises its item if it was the last tile
@@ -309,22 +313,43 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         float lt[GP];
 #pragma unroll
         for (int g = 0; g < GP; ++g) lt[g] = sm.lsum[0][g] + sm.lsum[1][g] + sm.lsum[2][g] + sm.lsum[3][g];
-        if (!C::kStacked || r < 64) {
-          float* po = p.ws.part_o + (int64_t)prev_item * G * D;
+        if (prev_nch == 1) {
+          // the segment is this one item: write the final output directly
+          if (!C::kStacked || r < 64) {
+            const int64_t orow = ((int64_t)prev_b * p.Nq + prev_hkv * G) * D + r;
 #pragma unroll
-          for (int g = 0; g < GP; ++g) {
-            if (g < G) {
-              const float a = C::kStacked ? acc[g] + sm.accx[r][g] : acc[g];
-              po[g * D + r] = lt[g] > 0.f ? a / lt[g] : 0.f;
+            for (int g = 0; g < GP; ++g) {
+              if (g < G) {
+                const float a = C::kStacked ? acc[g] + sm.accx[r][g] : acc[g];
+                const int h = prev_hkv * G + g;
+                float M, W;
+                const float v = single_item_output(a, mm[g], lt[g], p.sink, h, &M, &W);
+                store_out<DT>(p.out, orow + (int64_t)g * D, v);
+                if (r == g) {
+                  if (p.softmax_max) p.softmax_max[(int64_t)prev_b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+                  if (p.softmax_sum) p.softmax_sum[(int64_t)prev_b * p.Nq + h] = W;
+                }
+              }
             }
           }
-        }
-        if (r < GP && r < G) {
-          float mv = mm[0], lw = lt[0];
+        } else {
+          if (!C::kStacked || r < 64) {
+            float* po = p.ws.part_o + (int64_t)prev_item * G * D;
 #pragma unroll
-          for (int g = 1; g < GP; ++g)
-            if (r == g) { mv = mm[g]; lw = lt[g]; }
-          p.ws.part_ml[(int64_t)prev_item * G + r] = make_float2(mv, lw);
+            for (int g = 0; g < GP; ++g) {
+              if (g < G) {
+                const float a = C::kStacked ? acc[g] + sm.accx[r][g] : acc[g];
+                po[g * D + r] = lt[g] > 0.f ? a / lt[g] : 0.f;
+              }
+            }
+          }
+          if (r < GP && r < G) {
+            float mv = mm[0], lw = lt[0];
+#pragma unroll
+            for (int g = 1; g < GP; ++g)
+              if (r == g) { mv = mm[g]; lw = lt[g]; }
+            p.ws.part_ml[(int64_t)prev_item * G + r] = make_float2(mv, lw);
+          }
         }
         named_bar_sync(kBarCompute, 128);
       }
@@ -415,6 +440,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       prev_first = meta.first;
       prev_last = meta.last;
       prev_item = meta.item;
+      prev_b = meta.b;
+      prev_hkv = meta.hkv;
+      prev_nch = meta.nch;
       ++j;
     }
     if (ok && j > 0) correct(j - 1, false);
@@ -436,9 +464,9 @@ cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& tmK, const CUten
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);
-  kern<<<grid, kThreadsTC, smem, stream>>>(tmK, tmV, tmQ, p, box_rows);
+  e = launch_dependent(kern, grid, kThreadsTC, smem, stream, tmK, tmV, tmQ, p, box_rows);
   trace_mark(kKernelDecodeAttention, 1, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

@@ -45,7 +45,7 @@ struct DecodeWorkspace {
   int* counter;     // dynamic work counter (reset by the plan kernel)
   int* n_items;     // number of work items written by the plan kernel
   int* seg_base;    // (B) first item of batch b
-  int4* items;      // (max_items) {b, hkv, tok_begin, tok_end}
+  int4* items;      // (max_items) {b, hkv, nch << 16 | chunk, last token + 1}
   float* part_o;    // (max_items, G, D) normalised partial outputs
   float2* part_ml;  // (max_items, G) {max (log2 units), sum}
 };
