@@ -331,11 +331,13 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
   p.ws = fia::decode_workspace_carve(workspace, B, Nkv, G, D, plan.max_items);
   p.status = d->status;
 
-  // 16-bit KV runs on the tensor-core kernel (128-token tiles); int8 KV on the CUDA-core one.
+  // 16-bit KV runs on the tensor-core kernel (128-token tiles), int8 KV with D = 128 on the
+  // int8 tensor-core kernel (128-token tiles), other int8 shapes on the CUDA-core one.
   const bool tc = kv_dtype != FIA_I8;
+  const bool tile128 = tc || fia::decode_uses_i8tc(kv_dtype, D);
   const int elem = kv_dtype == FIA_I8 ? 1 : 2;
   const uint32_t box_cols = (uint32_t)std::min(D * elem, 128) / elem;
-  const int box_rows = gcd(block_size, tc ? fia::kDecodeTileTC : fia::kDecodeTile);
+  const int box_rows = gcd(block_size, tile128 ? fia::kDecodeTileTC : fia::kDecodeTile);
   const uint64_t rows = (uint64_t)num_blocks * Nkv * block_size;
   CUtensorMap tmK, tmV, tmQ;
   if (int rc = make_tmap(&tmK, k_cache, kv_dtype, D, rows, box_cols, box_rows)) return rc;

@@ -28,6 +28,7 @@
 // Scores are kept in log2 units (scale * log2 e folded into the dot product) and
 // converted back to the natural-exp domain for the max output.
 #include "decode_common.cuh"
+#include "decode_i8.cuh"
 
 namespace fia {
 namespace {
@@ -141,6 +142,11 @@ __device__ void write_empty_batch(const DecodeParams& p, int b) {
 
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   griddep_launch_dependents();  // the attention kernel may begin its prologue
+  if (blockIdx.x > 0) {  // int8 tensor-core path: q' blocks, one warp per (b, kv head, padded row)
+    const int64_t R = (int64_t)(blockIdx.x - 1) * 32 + (threadIdx.x >> 5);
+    if (R < (int64_t)p.B * p.Nkv * kI8Heads) i8_qprep_row(p, R, threadIdx.x & 31);
+    return;
+  }
   extern __shared__ int sbase[];  // [B + 1] item offsets when B <= kPlanSmemB
   __shared__ int warp_tot[32];
   __shared__ int carry;
@@ -721,6 +727,7 @@ size_t decode_workspace_bytes(int B, int Nkv, int G, int D, int max_items) {
   s += up(sizeof(int4) * (size_t)max_items);           // items
   s += up(sizeof(float) * (size_t)max_items * G * D);  // part_o
   s += up(sizeof(float2) * (size_t)max_items * G);     // part_ml
+  if (D == 128) s += up((size_t)kI8QBlockBytes * B * Nkv);  // qprep
   return s;
 }
 
@@ -738,6 +745,8 @@ DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D,
   w.part_o = reinterpret_cast<float*>(c);
   c += up(sizeof(float) * (size_t)max_items * G * D);
   w.part_ml = reinterpret_cast<float2*>(c);
+  c += up(sizeof(float2) * (size_t)max_items * G);
+  w.qprep = (D == 128) ? c : nullptr;
   return w;
 }
 
@@ -745,13 +754,17 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const C
                           const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream) {
   trace_mark(kKernelDecodePlan, 0, stream);
   const size_t plan_smem = p.B <= kPlanSmemB ? sizeof(int) * (size_t)(p.B + 1) : 0;
-  decode_plan_kernel<<<1, 1024, plan_smem, stream>>>(p);
+  const bool i8tc = !tmQ && decode_uses_i8tc(p.kv_dtype, p.D);
+  const int64_t prep_blocks = i8tc ? ((int64_t)p.B * p.Nkv * kI8Heads + 31) / 32 : 0;
+  decode_plan_kernel<<<(unsigned)(1 + prep_blocks), 1024, plan_smem, stream>>>(p);
   trace_mark(kKernelDecodePlan, 1, stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int grid = num_sms;
   if (tmQ) {
     e = launch_decode_tc_attention(p, tmK, tmV, *tmQ, box_rows, grid, stream);
+  } else if (i8tc) {
+    e = launch_decode_i8tc_attention(p, tmK, tmV, box_rows, grid, stream);
   } else if (p.kv_dtype == kBF16) {
     e = (p.D == 64) ? launch_attention_g<kBF16, 64>(p, tmK, tmV, box_rows, grid, stream)
                     : launch_attention_g<kBF16, 128>(p, tmK, tmV, box_rows, grid, stream);

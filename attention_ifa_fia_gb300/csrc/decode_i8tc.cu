@@ -1,0 +1,579 @@
+// decode_i8tc.cu -- paged GQA decode attention over an int8 KV cache on tcgen05 tensor
+// cores (D = 128).
+//
+// Same operator, plan, work items, partial format and merge as decode.cu.  The
+// per-channel antiquant (aclnnIncreFlashAttentionV3, "antiquantScale /
+// antiquantOffset": k^ = (x - offset) * scale, the same for V with its own
+// parameters) is affine, so this kernel never forms k^ or v^ element by element:
+//
+//   scores  S^T [128 tok x 16] = X_K [128 x D] . (Q'hi + Q'lo)^T    (two MMAs, see decode_i8.cuh)
+//           score (log2 units) = S kq + nq
+//   values  O^T [D x 16]       = X_V^T [D x 128] . P^T
+//           out_d              = s_v[d] * (O_d / l - o_v[d])
+//
+// X_K and X_V are the int8 codes, exact as fp16 integers.  The output side uses
+// sum_t p_t (x_td - o_d) s_d = s_d (sum_t p_t x_td - o_d sum_t p_t); the PV MMA
+// weighs with P rounded to fp16, the correction with the fp32 sum l, a difference
+// of at most |o_d s_d| 2^-11 per output.
+//
+// Warp roles (448 threads):
+//   warp 0      TMA producer: the item's q' block (one bulk copy from the workspace),
+//               int8 K and V tiles (128 rows x 128 bytes, 128-byte swizzle) into a
+//               4-stage ring.
+//   warp 1      TMEM allocation; one thread issues the MMAs.
+//   warps 2-5   online softmax of tile j (one token per TMEM lane) and the
+//               rescale-and-accumulate of the PV result of tile j-1 (one channel
+//               per lane), final output or split partial.
+//   warps 6-9   K codes -> fp16 pairs in TMEM (one token row per lane): the A
+//               operand of the score MMA, double buffered.
+//   warps 10-13 V codes -> fp16 in shared memory, in the MN-major layout of the A
+//               operand of the PV MMA, double buffered.
+// Each code takes one integer and one half-precision operation: the byte (plus
+// 128) is placed under the exponent of 1024 and 1152 is subtracted.
+#include "decode_common.cuh"
+#include "decode_i8.cuh"
+
+namespace fia {
+namespace {
+
+constexpr int kT = 128;     // tokens per tile: the M of the score MMA
+constexpr int kNP = 16;     // query heads per group, padded: the N of both MMAs
+constexpr int kD = 128;     // head dim (the M of the PV MMA)
+constexpr int kStages = 4;  // int8 ring
+constexpr int kThreads = 448;
+constexpr int kBarSoftmax = 2;                       // named barrier of the softmax warps
+constexpr uint32_t kColS = 0, kColO = 32, kColK = 64;  // TMEM: S [0,32), O [32,64), K codes [64,192)
+constexpr uint32_t kTmemCols = 256;
+constexpr int kI8Tile = kT * kD;      // bytes of one int8 K or V tile
+constexpr int kVTile = kT * kD * 2;   // fp16 V codes of one tile
+constexpr int kPBytes = kNP * kT * 2;
+
+struct __align__(16) I8Meta {
+  int b, hkv, n, item;
+  int first, last, qbuf, nch;
+};
+
+struct I8Smem {
+  alignas(1024) uint8_t kv[kStages][2][kI8Tile];
+  alignas(1024) uint8_t v16[2][kVTile];
+  alignas(1024) uint8_t q[2][kI8QBytes];
+  alignas(1024) uint8_t p[2][kPBytes];
+  float2 kn[2][kNP];
+  float red[2][4][kNP];
+  float lsum[4][kNP];
+  I8Meta meta[kStages];  // per int8 stage (producer)
+  I8Meta kmeta[2];       // per K buffer (K converters)
+  I8Meta smeta[2];       // per S buffer (MMA thread)
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t k_full[2], k_free[2], v_full[2], v_free[2];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_full[2], o_free[2];
+  uint32_t tmem_base;
+};
+static_assert(sizeof(I8Smem) + 1024 <= 232448, "shared memory of the int8 decode kernel");
+
+__device__ __forceinline__ int64_t i8_pool_row(int32_t blk, int t, int bs, int Nkv, int hkv) {
+  return ((int64_t)blk * Nkv + hkv) * bs + (t % bs);
+}
+
+// Offset of element (row g, token t) of the P^T operand: two 64-token slabs of
+// 16 rows x 128 bytes, 128-byte swizzle.
+__device__ __forceinline__ uint32_t i8_p_offset(int g, int t) {
+  const uint32_t slab = t >> 6, col = (t & 63) * 2;
+  return slab * (kNP * 128) + swz((uint32_t)g * 128 + col, 7);
+}
+
+// Four int8 codes -> two words of fp16 pairs (codes 0,1 and 2,3; lower code in the low half).
+__device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t& h01, uint32_t& h23) {
+  const uint32_t u = w ^ 0x80808080u;  // code + 128 per byte
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  // each half is now 1024 + code + 128; subtract 1152 (0x6480) from both halves
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h01) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h23) : "r"(b), "r"(0x64806480u));
+}
+
+__device__ __forceinline__ void tmem_st32w(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T (A: rows on lanes, 16-bit pairs per column).
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int QT, int GP>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_i8tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const DecodeParams p, const int box_rows) {
+  extern __shared__ uint8_t smem_raw[];
+  I8Smem& sm = *reinterpret_cast<I8Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.G;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 8);  // the four K and four V converter warps
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.k_full[i], 4);
+      mbar_init(&sm.k_free[i], 1);
+      mbar_init(&sm.v_full[i], 4);
+      mbar_init(&sm.v_free[i], 1);
+      mbar_init(&sm.q_full[i], 1);
+      mbar_init(&sm.q_empty[i], 5);  // MMA commit after the item's last score MMA + 4 softmax warps
+                                     // after reading the item's constants at its last tile
+      mbar_init(&sm.s_full[i], 2);   // meta written by the MMA thread + MMA commit
+      mbar_init(&sm.s_free[i], 4);
+      mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.p_free[i], 1);
+      mbar_init(&sm.o_full[i], 1);
+      mbar_init(&sm.o_free[i], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  griddep_wait();               // item list, counters and q' blocks of the plan launch are visible
+  griddep_launch_dependents();  // the merge kernel may be scheduled; it waits for this grid to finish
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    const int n_items = *p.ws.n_items;
+    const int bs = p.block_size;
+    const uint32_t piece_bytes = (uint32_t)box_rows * 128u;
+    int j = 0, local_item = 0;
+    bool ok = true;
+    int next = 0;
+    if (lane == 0) next = atomicAdd(p.ws.counter, 1);
+    next = __shfl_sync(0xffffffffu, next, 0);
+    while (ok && next < n_items) {
+      const int item = next;
+      const DecodeItem it = decode_item(p.ws.items[item], p.chunk_tokens);
+      if (lane == 0) next = atomicAdd(p.ws.counter, 1);
+      next = __shfl_sync(0xffffffffu, next, 0);
+      const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
+      const int qb = local_item & 1;
+      if (!mbar_wait(&sm.q_empty[qb], ((local_item >> 1) & 1) ^ 1u, p.status)) { ok = false; break; }
+      if (lane == 0) {
+        const uint8_t* src = p.ws.qprep + ((int64_t)b * p.Nkv + hkv) * kI8QBlockBytes;
+        mbar_arrive_expect_tx(&sm.q_full[qb], kI8QBlockBytes);
+        bulk_load(sm.q[qb], src, kI8QBytes, &sm.q_full[qb]);
+        bulk_load(sm.kn[qb], src + kI8QBytes, kI8QBlockBytes - kI8QBytes, &sm.q_full[qb]);
+      }
+      const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
+      for (int tok0 = t_begin; tok0 < t_end; tok0 += kT, ++j) {
+        const int st = j % kStages;
+        const uint32_t ph = (uint32_t)(j / kStages) & 1u;
+        const int n = min(kT, t_end - tok0);
+        const int npieces = (n + box_rows - 1) / box_rows;
+        int32_t blk = 0;
+        bool valid = false;
+        if (lane < npieces) {
+          blk = bt_row[(tok0 + lane * box_rows) / bs];
+          valid = blk >= 0 && (int64_t)blk < p.num_blocks;
+          if (!valid) raise_status(p.status, kStatusBadBlockIndex);
+        }
+        const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+        const uint32_t bytes = 2u * piece_bytes * __popc(vmask);
+        if (!mbar_wait(&sm.kv_empty[st], ph ^ 1u, p.status)) { ok = false; break; }
+        if (lane == 0) {
+          I8Meta& m = sm.meta[st];
+          m.b = b; m.hkv = hkv; m.n = n; m.item = item;
+          m.first = (tok0 == t_begin); m.last = (tok0 + kT >= t_end); m.qbuf = qb; m.nch = it.nch;
+          if (bytes) mbar_arrive_expect_tx(&sm.kv_full[st], bytes);
+          else mbar_arrive(&sm.kv_full[st]);
+        }
+        __syncwarp();
+        if (valid) {
+          const int64_t row = i8_pool_row(blk, tok0 + lane * box_rows, bs, p.Nkv, hkv);
+          const uint32_t off = (uint32_t)lane * box_rows * 128u;
+          tma_load_2d(sm.kv[st][0] + off, &tmK, 0, (int32_t)row, &sm.kv_full[st]);
+          tma_load_2d(sm.kv[st][1] + off, &tmV, 0, (int32_t)row, &sm.kv_full[st]);
+        }
+      }
+      ++local_item;
+    }
+    if (ok) {  // sentinel tile: no more work
+      const int st = j % kStages;
+      if (mbar_wait(&sm.kv_empty[st], ((uint32_t)(j / kStages) & 1u) ^ 1u, p.status) && lane == 0) {
+        sm.meta[st].item = -1;
+        mbar_arrive(&sm.kv_full[st]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = umma_idesc_f16(0, 0, 0, kT, kNP);  // fp16, A (TMEM) and B K-major
+      constexpr uint32_t idesc_pv = umma_idesc_f16(0, 1, 0, kT, kNP);  // fp16, A = V^T read MN-major
+      int local_item = 0;
+      auto issue_pv = [&](int jj) -> bool {
+        const int pb = jj & 1;
+        const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
+        if (!mbar_wait(&sm.p_full[pb], ph, p.status)) return false;
+        if (!mbar_wait(&sm.o_free[pb], ph ^ 1u, p.status)) return false;
+        if (!mbar_wait(&sm.v_full[pb], ph, p.status)) return false;
+        tc_fence_after();
+        const uint32_t vbase = smem_u32(sm.v16[pb]);
+        const uint32_t pbase = smem_u32(sm.p[pb]);
+        const uint32_t ocol = tmem + kColO + pb * 16;
+#pragma unroll
+        for (int s = 0; s < kT / 16; ++s) {
+          const uint64_t a = umma_desc(vbase + s * 16 * 128, kT * 128, 1024);
+          const uint64_t bd = umma_desc(pbase + (s >> 2) * (kNP * 128) + (s & 3) * 32, 16, 1024);
+          umma_f16(ocol, a, bd, idesc_pv, s > 0);
+        }
+        umma_commit(&sm.o_full[pb]);
+        umma_commit(&sm.p_free[pb]);
+        umma_commit(&sm.v_free[pb]);
+        return true;
+      };
+      int j = 0;
+      while (true) {
+        const int kb = j & 1;
+        const uint32_t ph2 = (uint32_t)(j >> 1) & 1u;
+        if (!mbar_wait(&sm.k_full[kb], ph2, p.status)) break;
+        tc_fence_after();
+        const I8Meta meta = sm.kmeta[kb];
+        const int sb = j & 1;
+        if (meta.item < 0) {
+          if (j > 0 && !issue_pv(j - 1)) break;
+          if (!mbar_wait(&sm.s_free[sb], ph2 ^ 1u, p.status)) break;
+          sm.smeta[sb] = meta;
+          mbar_arrive(&sm.s_full[sb]);  // both arrivals: the softmax warps see the sentinel
+          mbar_arrive(&sm.s_full[sb]);
+          break;
+        }
+        const int qb = meta.qbuf;
+        if (meta.first && !mbar_wait(&sm.q_full[qb], (uint32_t)(local_item >> 1) & 1u, p.status)) break;
+        if (!mbar_wait(&sm.s_free[sb], ph2 ^ 1u, p.status)) break;
+        tc_fence_after();
+        const uint32_t qbase = smem_u32(sm.q[qb]);
+        const uint32_t tk = tmem + kColK + kb * 64;
+        const uint32_t ts = tmem + kColS + sb * 16;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int s = 0; s < kD / 16; ++s) {
+            const uint64_t bd =
+                umma_desc(qbase + part * kI8QPartBytes + (s >> 2) * (kNP * 128) + (s & 3) * 32, 16, 1024);
+            umma_f16_tmem_a(ts, tk + s * 8, bd, idesc_qk, (part | s) != 0);
+          }
+        }
+        sm.smeta[sb] = meta;
+        mbar_arrive(&sm.s_full[sb]);
+        umma_commit(&sm.s_full[sb]);
+        umma_commit(&sm.k_free[kb]);
+        if (meta.last) {
+          umma_commit(&sm.q_empty[qb]);
+          ++local_item;
+        }
+        if (j > 0 && !issue_pv(j - 1)) break;
+        ++j;
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------------ softmax + correction
+    const int quad = warp & 3;       // TMEM lane quadrant of this warp
+    const int r = quad * 32 + lane;  // TMEM lane: token of S, channel of O
+    const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
+    float m_run[GP], l_part[GP], alpha_prev[GP], acc[GP], m_fin[GP], l_fin[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      m_run[g] = -INFINITY; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_fin[g] = -INFINITY; l_fin[g] = 0.f;
+    }
+    float vs_cur = 0.f, vo_cur = 0.f, vs_new = 0.f, vo_new = 0.f;  // value antiquant of channel r
+    int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
+    bool prev_first = false, prev_last = false;
+
+    auto correct = [&](int jj, bool use_fin) -> bool {
+      const int ob = jj & 1;
+      if (!mbar_wait(&sm.o_full[ob], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
+      tc_fence_after();
+      float o[kNP];
+      tmem_ld16(tq + kColO + ob * 16, o);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.o_free[ob]);
+#pragma unroll
+      for (int g = 0; g < GP; ++g) acc[g] = prev_first ? o[g] : fmaf(acc[g], alpha_prev[g], o[g]);
+      if (prev_last) {
+        float mm[GP], lv[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          mm[g] = use_fin ? m_fin[g] : m_run[g];
+          lv[g] = use_fin ? l_fin[g] : l_part[g];
+        }
+#pragma unroll
+        for (int off = 16; off; off >>= 1)
+#pragma unroll
+          for (int g = 0; g < GP; ++g) lv[g] += __shfl_xor_sync(0xffffffffu, lv[g], off);
+        if (lane == 0) {
+#pragma unroll
+          for (int g = 0; g < GP; ++g) sm.lsum[quad][g] = lv[g];
+        }
+        named_bar_sync(kBarSoftmax, 128);
+        float lt[GP], a[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          lt[g] = sm.lsum[0][g] + sm.lsum[1][g] + sm.lsum[2][g] + sm.lsum[3][g];
+          a[g] = vs_cur * fmaf(-vo_cur, lt[g], acc[g]);  // sum_t p_t v^_t, unnormalised
+        }
+        if (prev_nch == 1) {
+          const int64_t orow = ((int64_t)prev_b * p.Nq + prev_hkv * G) * kD + r;
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            if (g < G) {
+              const int h = prev_hkv * G + g;
+              float M, W;
+              const float v = single_item_output(a[g], mm[g], lt[g], p.sink, h, &M, &W);
+              store_out<QT>(p.out, orow + (int64_t)g * kD, v);
+              if (r == g) {
+                if (p.softmax_max) p.softmax_max[(int64_t)prev_b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+                if (p.softmax_sum) p.softmax_sum[(int64_t)prev_b * p.Nq + h] = W;
+              }
+            }
+          }
+        } else {
+          float* po = p.ws.part_o + (int64_t)prev_item * G * kD;
+#pragma unroll
+          for (int g = 0; g < GP; ++g)
+            if (g < G) po[g * kD + r] = lt[g] > 0.f ? a[g] / lt[g] : 0.f;
+          if (r < GP && r < G) {
+            float mv = mm[0], lw = lt[0];
+#pragma unroll
+            for (int g = 1; g < GP; ++g)
+              if (r == g) { mv = mm[g]; lw = lt[g]; }
+            p.ws.part_ml[(int64_t)prev_item * G + r] = make_float2(mv, lw);
+          }
+        }
+        named_bar_sync(kBarSoftmax, 128);
+      }
+      return true;
+    };
+
+    int j = 0;
+    bool ok = true;
+    while (true) {
+      const int sb = j & 1;
+      const uint32_t sph = (uint32_t)(j >> 1) & 1u;
+      if (!mbar_wait(&sm.s_full[sb], sph, p.status)) { ok = false; break; }
+      const I8Meta meta = sm.smeta[sb];
+      if (meta.item < 0) break;
+      tc_fence_after();
+      float s[kNP];
+      tmem_ld16(tq + kColS + sb * 16, s);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.s_free[sb]);
+      if (meta.first) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          m_fin[g] = m_run[g];
+          l_fin[g] = l_part[g];
+          m_run[g] = -INFINITY;
+          l_part[g] = 0.f;
+        }
+        const int64_t vi = ((int64_t)p.Nkv + meta.hkv) * kD + r;  // value scale/offset: index 1 of (2, Nkv, D)
+        vs_new = p.aq_scale[vi];
+        vo_new = p.aq_offset ? p.aq_offset[vi] : 0.f;
+      }
+      const bool valid = r < meta.n;
+      float x[GP], mx[GP];
+      const float2* kn = sm.kn[meta.qbuf];  // {kq, nq} of the item's heads (decode_i8.cuh)
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float2 c = kn[g];
+        x[g] = valid ? fmaf(s[g], c.x, c.y) : -INFINITY;
+        mx[g] = x[g];
+      }
+      if (meta.last) {  // the q' buffer may be refilled once the MMA thread is done with it too
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.q_empty[meta.qbuf]);
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1)
+#pragma unroll
+        for (int g = 0; g < GP; ++g) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) sm.red[sb][quad][g] = mx[g];
+      }
+      named_bar_sync(kBarSoftmax, 128);
+      float alpha[GP], pr[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float tmax = fmaxf(fmaxf(sm.red[sb][0][g], sm.red[sb][1][g]), fmaxf(sm.red[sb][2][g], sm.red[sb][3][g]));
+        const float m_new = fmaxf(m_run[g], tmax);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha[g] = fast_exp2(m_run[g] - m_use);
+        pr[g] = fast_exp2(x[g] - m_use);
+        l_part[g] = fmaf(l_part[g], alpha[g], pr[g]);
+        m_run[g] = m_new;
+      }
+      if (!mbar_wait(&sm.p_free[sb], sph ^ 1u, p.status)) { ok = false; break; }
+      uint8_t* pbuf = sm.p[sb];
+#pragma unroll
+      for (int g = 0; g < GP; ++g)
+        if (g < G) *reinterpret_cast<uint16_t*>(pbuf + i8_p_offset(g, r)) = __half_as_ushort(__float2half_rn(pr[g]));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+      if (j > 0 && !correct(j - 1, meta.first)) { ok = false; break; }
+      if (meta.first) {
+        vs_cur = vs_new;
+        vo_cur = vo_new;
+      }
+#pragma unroll
+      for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
+      prev_first = meta.first;
+      prev_last = meta.last;
+      prev_item = meta.item;
+      prev_b = meta.b;
+      prev_hkv = meta.hkv;
+      prev_nch = meta.nch;
+      ++j;
+    }
+    if (ok && j > 0) correct(j - 1, false);
+  } else if (warp < 10) {
+    // ------------------------------------------------------------------ K codes -> TMEM
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
+    for (int j = 0;; ++j) {
+      const int st = j % kStages;
+      if (!mbar_wait(&sm.kv_full[st], (uint32_t)(j / kStages) & 1u, p.status)) break;
+      const I8Meta meta = sm.meta[st];
+      const int kb = j & 1;
+      if (!mbar_wait(&sm.k_free[kb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
+      if (meta.item < 0) {
+        if (warp == 6 && lane == 0) sm.kmeta[kb] = meta;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.k_full[kb]);
+        break;
+      }
+      const uint32_t row = smem_u32(sm.kv[st][0]) + r * 128;
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int chunk = half * 4 + c;
+          const uint4 w = lds128(row + ((chunk ^ (r & 7)) << 4));
+          codes_to_f16x2(w.x, v[c * 8 + 0], v[c * 8 + 1]);
+          codes_to_f16x2(w.y, v[c * 8 + 2], v[c * 8 + 3]);
+          codes_to_f16x2(w.z, v[c * 8 + 4], v[c * 8 + 5]);
+          codes_to_f16x2(w.w, v[c * 8 + 6], v[c * 8 + 7]);
+        }
+        tmem_st32w(tq + kColK + kb * 64 + half * 32, v);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (warp == 6) sm.kmeta[kb] = meta;
+        mbar_arrive(&sm.kv_empty[st]);
+        mbar_arrive(&sm.k_full[kb]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ V codes -> shared memory
+    const int r = (warp - 10) * 32 + lane;
+    for (int j = 0;; ++j) {
+      const int st = j % kStages;
+      if (!mbar_wait(&sm.kv_full[st], (uint32_t)(j / kStages) & 1u, p.status)) break;
+      if (sm.meta[st].item < 0) break;
+      const int vb = j & 1;
+      if (!mbar_wait(&sm.v_free[vb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
+      const uint32_t row = smem_u32(sm.kv[st][1]) + r * 128;
+      const uint32_t dst = smem_u32(sm.v16[vb]) + r * 128;
+#pragma unroll
+      for (int chunk = 0; chunk < 8; ++chunk) {
+        const uint4 w = lds128(row + ((chunk ^ (r & 7)) << 4));
+        uint32_t h[8];
+        codes_to_f16x2(w.x, h[0], h[1]);
+        codes_to_f16x2(w.y, h[2], h[3]);
+        codes_to_f16x2(w.z, h[4], h[5]);
+        codes_to_f16x2(w.w, h[6], h[7]);
+        // channels 16 chunk .. +7 and +8 .. +15: fp16 chunks 2 chunk and 2 chunk + 1
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int cc = 2 * chunk + hf;
+          const uint32_t a = dst + (cc >> 3) * (kT * 128) + ((((uint32_t)cc & 7u) ^ ((uint32_t)r & 7u)) << 4);
+          sts128(a, h[hf * 4 + 0], h[hf * 4 + 1], h[hf * 4 + 2], h[hf * 4 + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.kv_empty[st]);
+        mbar_arrive(&sm.v_full[vb]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int QT, int GP>
+cudaError_t launch_i8(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows, int grid,
+                      cudaStream_t stream) {
+  const size_t smem = sizeof(I8Smem) + 1024;
+  auto kern = decode_i8tc_kernel<QT, GP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  trace_mark(kKernelDecodeAttention, 0, stream);
+  e = launch_dependent(kern, grid, kThreads, smem, stream, tmK, tmV, p, box_rows);
+  trace_mark(kKernelDecodeAttention, 1, stream);
+  return e;
+}
+
+template <int QT>
+cudaError_t launch_i8_g(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows, int grid,
+                        cudaStream_t stream) {
+  if (p.G <= 2) return launch_i8<QT, 2>(p, tmK, tmV, box_rows, grid, stream);
+  if (p.G <= 4) return launch_i8<QT, 4>(p, tmK, tmV, box_rows, grid, stream);
+  if (p.G <= 8) return launch_i8<QT, 8>(p, tmK, tmV, box_rows, grid, stream);
+  return cudaErrorInvalidValue;  // int8 groups above 8 are rejected before launch
+}
+
+}  // namespace
+
+cudaError_t launch_decode_i8tc_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                         int box_rows, int grid, cudaStream_t stream) {
+  return p.q_dtype == kBF16 ? launch_i8_g<kBF16>(p, tmK, tmV, box_rows, grid, stream)
+                            : launch_i8_g<kF16>(p, tmK, tmV, box_rows, grid, stream);
+}
+
+}  // namespace fia

@@ -48,6 +48,7 @@ struct DecodeWorkspace {
   int4* items;      // (max_items) {b, hkv, nch << 16 | chunk, last token + 1}
   float* part_o;    // (max_items, G, D) normalised partial outputs
   float2* part_ml;  // (max_items, G) {max (log2 units), sum}
+  uint8_t* qprep;   // (B * Nkv) q' blocks of the int8 tensor-core path (D = 128), else null
 };
 
 struct DecodeParams {
@@ -85,6 +86,12 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const C
 cudaError_t launch_decode_tc_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                        const CUtensorMap& tmQ, int box_rows, int grid, cudaStream_t stream);
 constexpr int kDecodeTileTC = 128;  // tokens per tensor-core tile; work items are multiples of it
+
+// int8 KV with D = 128 runs on the tensor-core kernel of decode_i8tc.cu (128-token
+// tiles, G <= 8); other int8 shapes on the CUDA-core kernel.
+inline bool decode_uses_i8tc(int kv_dtype, int D) { return kv_dtype == kI8 && D == 128; }
+cudaError_t launch_decode_i8tc_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                         int box_rows, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // RingAttentionUpdate

@@ -325,7 +325,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None, "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4) if achieved else None,
                      "traffic": traffic, "kernel": "decode_tc (tcgen05 split-KV attention)" if case.kv_dtype != W.INT8
-                     else "decode_splitkv (CUDA-core split-KV attention)",
+                     else "decode_i8tc (tcgen05 split-KV attention over int8 codes)",
                      "peak_source": f"{src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(world * nbytes["total"] * steps / (ms_e2e / 1e3) / 1e9, 1), "unit": "GB/s",

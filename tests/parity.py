@@ -63,7 +63,7 @@ class DeviceDecode:
             self.k = torch.from_numpy(case.k_cache).to(device)
             self.v = torch.from_numpy(case.v_cache).to(device)
             self.aq_scale = torch.from_numpy(case.aq_scale).to(device)
-            self.aq_offset = torch.from_numpy(case.aq_offset).to(device)
+            self.aq_offset = None if case.aq_offset is None else torch.from_numpy(case.aq_offset).to(device)
         else:
             self.k = dev_bits(case.k_cache, case.kv_dtype, device)
             self.v = dev_bits(case.v_cache, case.kv_dtype, device)

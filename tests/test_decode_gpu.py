@@ -108,6 +108,19 @@ EDGE = {
     "int8_fp16q_g4": (dict(B=2, Nq=4, Nkv=1, D=128, block_size=64, dtype=W.FP16, kv_dtype=W.INT8,
                            lengths=[100, 64], poison=True), [0]),
     "int8_nkv16": (dict(B=1, Nq=16, Nkv=16, D=64, block_size=32, kv_dtype=W.INT8, lengths=[70]), [0]),
+    # int8 KV with D = 128 runs on the tensor-core kernel with the antiquant folded into q and out
+    "int8_tc_ragged_g8": (dict(B=3, Nq=16, Nkv=2, D=128, block_size=128, kv_dtype=W.INT8, lengths=[1, 129, 700]),
+                          [0, 1, 3]),
+    "int8_tc_g1_bs32_fp16": (dict(B=2, Nq=4, Nkv=4, D=128, block_size=32, dtype=W.FP16, kv_dtype=W.INT8,
+                                  lengths=[31, 300]), [0, 2]),
+    "int8_tc_g2_bs256": (dict(B=2, Nq=4, Nkv=2, D=128, block_size=256, kv_dtype=W.INT8, lengths=[255, 1000]),
+                         [0, 4]),
+    "int8_tc_g3": (dict(B=2, Nq=6, Nkv=2, D=128, block_size=64, kv_dtype=W.INT8, lengths=[64, 191]), [0]),
+    "int8_tc_poisoned_g8": (dict(B=3, Nq=8, Nkv=1, D=128, block_size=64, kv_dtype=W.INT8, lengths=[5, 130, 257],
+                                 poison=True, spare_blocks=3, table_pad=2), [0, 2]),
+    "int8_tc_empty_seqs": (dict(B=3, Nq=8, Nkv=2, D=128, block_size=32, kv_dtype=W.INT8, lengths=[0, 40, 0]), [0]),
+    "int8_tc_many_batches": (dict(B=200, Nq=8, Nkv=2, D=128, block_size=128, kv_dtype=W.INT8, len_range=(0, 300)),
+                             [0]),
     "sink_bf16": (dict(B=2, Nq=8, Nkv=2, D=64, block_size=16, lengths=[40, 90], sink=True), [0, 3]),
     "sink_fp16_d128": (dict(B=1, Nq=4, Nkv=4, D=128, block_size=128, dtype=W.FP16, lengths=[300], sink=True),
                        [0]),
@@ -125,6 +138,33 @@ def test_edge_case(F, cuda, name):
     for ns in splits:
         out, mx, sm = run_decode(F, dd, num_splits=ns)
         compare_decode(case, out, mx, sm, ref=ref)
+    assert _status(F) == 0
+
+
+def test_int8_without_offset(F, cuda):
+    """antiquant_offset may be omitted (treated as 0), on both int8 kernels."""
+    for D in (64, 128):
+        case = W.make_decode_case(B=2, Nq=8, Nkv=2, D=D, block_size=64, kv_dtype=W.INT8, lengths=[100, 333], seed=23)
+        case.aq_offset = None
+        dd = DeviceDecode(case)
+        for ns in (0, 3):
+            out, mx, sm = run_decode(F, dd, num_splits=ns)
+            compare_decode(case, out, mx, sm)
+    assert _status(F) == 0
+
+
+@pytest.mark.parametrize("k_scale", [1e4, 1e-6])
+def test_int8_key_scale_extremes(F, cuda, k_scale):
+    """Key scales far from 1 (the softmax scale compensating) move q * scale_k far from
+    the fp16 range; the power-of-two prescale keeps the scores exact."""
+    case = W.make_decode_case(B=2, Nq=16, Nkv=2, D=128, block_size=128, kv_dtype=W.INT8, lengths=[500, 77],
+                              seed=29)
+    case.aq_scale = case.aq_scale.copy()
+    case.aq_scale[0] *= np.float32(k_scale)
+    case.scale = case.scale / k_scale
+    dd = DeviceDecode(case)
+    out, mx, sm = run_decode(F, dd, num_splits=2)
+    compare_decode(case, out, mx, sm)
     assert _status(F) == 0
 
 
