@@ -16,24 +16,26 @@
 // the two MMAs (one per part) accumulate.
 //
 // The block of one (b, kv head) is laid out exactly as the B operand of the score
-// MMA expects it in shared memory (K-major, 128-byte swizzle, 16 rows padded past
-// the group with zeros), so the attention kernel moves it with one bulk copy.
+// MMA expects it in shared memory: 32 rows, the hi parts of the 16 (padded) heads
+// then their lo parts, K-major with the 128-byte swizzle, so that one MMA of N = 32
+// produces both partial scores of every head and the attention kernel moves the
+// block with one bulk copy.
 #pragma once
 
 #include "fia_device.cuh"
 
 namespace fia {
 
-constexpr int kI8Heads = 16;                            // query rows per block (group, padded)
-constexpr int kI8QPartBytes = kI8Heads * 128 * 2;       // one fp16 part of 16 rows x D = 128
-constexpr int kI8QBytes = 2 * kI8QPartBytes;            // hi, then lo
-constexpr int kI8QBlockBytes = kI8QBytes + kI8Heads * 8;  // + {kq, nq} per row
+constexpr int kI8Heads = 16;                              // query heads per block (group, padded)
+constexpr int kI8QRows = 2 * kI8Heads;                    // hi rows, then lo rows
+constexpr int kI8QBytes = kI8QRows * 128 * 2;             // 32 rows x D = 128 fp16
+constexpr int kI8QBlockBytes = kI8QBytes + kI8Heads * 8;  // + {kq, nq} per head
 
-// Byte offset of channel d of row g inside one part: two 64-channel boxes of
-// 16 rows x 128 bytes, the 16-byte chunk index XORed with the row (mod 8).
+// Byte offset of channel d of row g (0..31) of the block: two 64-channel boxes of
+// 32 rows x 128 bytes, the 16-byte chunk index XORed with the row (mod 8).
 __device__ __forceinline__ uint32_t i8q_offset(int g, int d) {
   const uint32_t box = (uint32_t)d >> 6, col = ((uint32_t)d & 63u) * 2u;
-  return box * (kI8Heads * 128) + (uint32_t)g * 128 + ((((col >> 4) ^ ((uint32_t)g & 7u))) << 4) + (col & 15u);
+  return box * (kI8QRows * 128) + (uint32_t)g * 128 + ((((col >> 4) ^ ((uint32_t)g & 7u))) << 4) + (col & 15u);
 }
 
 // One warp prepares row g of block (b, hkv); row index R = (b * Nkv + hkv) * 16 + g.
@@ -88,9 +90,8 @@ __device__ __forceinline__ void i8_qprep_row(const DecodeParams& p, int64_t R, i
     lo_w = make_uint2(lb[0] | ((uint32_t)lb[1] << 16), lb[2] | ((uint32_t)lb[3] << 16));
     kn = make_float2(ldexpf(p.scale_log2, -e), -c * p.scale_log2);
   }
-  const uint32_t off = i8q_offset(g, d0);
-  *reinterpret_cast<uint2*>(base + off) = hi_w;
-  *reinterpret_cast<uint2*>(base + kI8QPartBytes + off) = lo_w;
+  *reinterpret_cast<uint2*>(base + i8q_offset(g, d0)) = hi_w;
+  *reinterpret_cast<uint2*>(base + i8q_offset(kI8Heads + g, d0)) = lo_w;
   if (lane == 0) reinterpret_cast<float2*>(base + kI8QBytes)[g] = kn;
 }
 

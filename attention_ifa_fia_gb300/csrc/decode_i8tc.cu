@@ -6,8 +6,8 @@
 // antiquantOffset": k^ = (x - offset) * scale, the same for V with its own
 // parameters) is affine, so this kernel never forms k^ or v^ element by element:
 //
-//   scores  S^T [128 tok x 16] = X_K [128 x D] . (Q'hi + Q'lo)^T    (two MMAs, see decode_i8.cuh)
-//           score (log2 units) = S kq + nq
+//   scores  S^T [128 tok x 32] = X_K [128 x D] . [Q'hi; Q'lo]^T   (decode_i8.cuh)
+//           score (log2 units) = (S_hi + S_lo) kq + nq
 //   values  O^T [D x 16]       = X_V^T [D x 128] . P^T
 //           out_d              = s_v[d] * (O_d / l - o_v[d])
 //
@@ -42,7 +42,12 @@ constexpr int kD = 128;     // head dim (the M of the PV MMA)
 constexpr int kStages = 4;  // int8 ring
 constexpr int kThreads = 448;
 constexpr int kBarSoftmax = 2;                       // named barrier of the softmax warps
-constexpr uint32_t kColS = 0, kColO = 32, kColK = 64;  // TMEM: S [0,32), O [32,64), K codes [64,192)
+// TMEM columns.  An MMA of M = 128 costs the tensor pipe about the same for any
+// N <= 64, so the hi and lo parts of q' share one MMA of N = 32.
+constexpr int kNS = 2 * kNP;     // N of the score MMA
+constexpr uint32_t kColS = 0;    // S: 2 buffers x 32 columns (hi scores, then lo scores)
+constexpr uint32_t kColO = 64;   // O: 2 buffers x 16 columns
+constexpr uint32_t kColK = 128;  // K codes: 2 buffers x 64 columns
 constexpr uint32_t kTmemCols = 256;
 constexpr int kI8Tile = kT * kD;      // bytes of one int8 K or V tile
 constexpr int kVTile = kT * kD * 2;   // fp16 V codes of one tile
@@ -53,6 +58,8 @@ struct __align__(16) I8Meta {
   int first, last, qbuf, nch;
 };
 
+constexpr int kMetaRing = 4;  // tile descriptors in flight between the K converters, MMA and softmax warps
+
 struct I8Smem {
   alignas(1024) uint8_t kv[kStages][2][kI8Tile];
   alignas(1024) uint8_t v16[2][kVTile];
@@ -61,13 +68,11 @@ struct I8Smem {
   float2 kn[2][kNP];
   float red[2][4][kNP];
   float lsum[4][kNP];
-  I8Meta meta[kStages];  // per int8 stage (producer)
-  I8Meta kmeta[2];       // per K buffer (K converters)
-  I8Meta smeta[2];       // per S buffer (MMA thread)
+  I8Meta meta[kStages];    // per int8 stage (producer)
+  I8Meta tmeta[kMetaRing];  // per tile j at j % kMetaRing (K converters)
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t k_full[2], k_free[2], v_full[2], v_free[2];
-  uint64_t q_full[2], q_empty[2];
-  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_full[2], o_free[2];
+  uint64_t k_full[2], v_full[2], q_full[2], q_empty[2];
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint32_t tmem_base;
 };
 static_assert(sizeof(I8Smem) + 1024 <= 232448, "shared memory of the int8 decode kernel");
@@ -115,6 +120,21 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
+// Scores of one S buffer: hi + lo partial sums of every (padded) head.
+__device__ __forceinline__ void tmem_ld_scores(uint32_t taddr, float (&v)[kNP]) {
+  float a[32];
+  tmem_ld32(taddr, a);
+#pragma unroll
+  for (int i = 0; i < kNP; ++i) v[i] = a[i] + a[kNP + i];
+}
+
+// Maximum over the warp.
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -128,6 +148,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.G;
 
+  // Synchronisation.  Buffers indexed by tile j use slot j & 1 (j % kStages for the
+  // int8 ring); a slot is reused two tiles later, and most "free" signals follow
+  // from program order:
+  //   k_full   K converters -> MMA: codes of tile j in TMEM, descriptor in tmeta
+  //   s_full   MMA commit of QK(j) -> softmax (scores ready) and K converters of
+  //            tile j + 2 (the K buffer may be overwritten)
+  //   p_full   softmax -> MMA: P(j) written.  Each softmax warp arrives after reading
+  //            S(j) and, earlier in its program, O(j - 2): the MMA warp may then also
+  //            overwrite the S and O buffers of those tiles
+  //   v_full   V converters -> MMA: fp16 V codes of tile j
+  //   pv_done  MMA commit of PV(j) -> softmax (O ready; P buffer free) and V
+  //            converters of tile j + 2 (the V buffer may be overwritten)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.kv_full[s], 1);
@@ -135,18 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.k_full[i], 4);
-      mbar_init(&sm.k_free[i], 1);
       mbar_init(&sm.v_full[i], 4);
-      mbar_init(&sm.v_free[i], 1);
       mbar_init(&sm.q_full[i], 1);
-      mbar_init(&sm.q_empty[i], 5);  // MMA commit after the item's last score MMA + 4 softmax warps
+      mbar_init(&sm.q_empty[i], 5);  // MMA commit after the item's last QK + the 4 softmax warps
                                      // after reading the item's constants at its last tile
-      mbar_init(&sm.s_full[i], 2);   // meta written by the MMA thread + MMA commit
-      mbar_init(&sm.s_free[i], 4);
+      mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.p_full[i], 4);
-      mbar_init(&sm.p_free[i], 1);
-      mbar_init(&sm.o_full[i], 1);
-      mbar_init(&sm.o_free[i], 4);
+      mbar_init(&sm.pv_done[i], 1);
     }
     fence_mbar_init();
   }
@@ -229,72 +256,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = umma_idesc_f16(0, 0, 0, kT, kNP);  // fp16, A (TMEM) and B K-major
+      constexpr uint32_t idesc_qk = umma_idesc_f16(0, 0, 0, kT, kNS);  // fp16, A (TMEM) and B K-major
       constexpr uint32_t idesc_pv = umma_idesc_f16(0, 1, 0, kT, kNP);  // fp16, A = V^T read MN-major
       int local_item = 0;
       auto issue_pv = [&](int jj) -> bool {
         const int pb = jj & 1;
         const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
         if (!mbar_wait(&sm.p_full[pb], ph, p.status)) return false;
-        if (!mbar_wait(&sm.o_free[pb], ph ^ 1u, p.status)) return false;
         if (!mbar_wait(&sm.v_full[pb], ph, p.status)) return false;
         tc_fence_after();
-        const uint32_t vbase = smem_u32(sm.v16[pb]);
-        const uint32_t pbase = smem_u32(sm.p[pb]);
-        const uint32_t ocol = tmem + kColO + pb * 16;
+        const uint32_t ocol = tmem + kColO + pb * kNP;
+        const uint64_t a0 = umma_desc(smem_u32(sm.v16[pb]), kT * 128, 1024);
+        const uint64_t b0 = umma_desc(smem_u32(sm.p[pb]), 16, 1024);
 #pragma unroll
-        for (int s = 0; s < kT / 16; ++s) {
-          const uint64_t a = umma_desc(vbase + s * 16 * 128, kT * 128, 1024);
-          const uint64_t bd = umma_desc(pbase + (s >> 2) * (kNP * 128) + (s & 3) * 32, 16, 1024);
-          umma_f16(ocol, a, bd, idesc_pv, s > 0);
-        }
-        umma_commit(&sm.o_full[pb]);
-        umma_commit(&sm.p_free[pb]);
-        umma_commit(&sm.v_free[pb]);
+        for (int s = 0; s < kT / 16; ++s)  // 16 tokens per step
+          umma_f16(ocol, a0 + ((s * 16 * 128) >> 4), b0 + ((((s >> 2) * (kNP * 128)) + (s & 3) * 32) >> 4),
+                   idesc_pv, s > 0);
+        umma_commit(&sm.pv_done[pb]);
         return true;
       };
-      int j = 0;
-      while (true) {
+      for (int j = 0;; ++j) {
         const int kb = j & 1;
-        const uint32_t ph2 = (uint32_t)(j >> 1) & 1u;
-        if (!mbar_wait(&sm.k_full[kb], ph2, p.status)) break;
-        tc_fence_after();
-        const I8Meta meta = sm.kmeta[kb];
-        const int sb = j & 1;
+        if (!mbar_wait(&sm.k_full[kb], (uint32_t)(j >> 1) & 1u, p.status)) break;
+        const I8Meta meta = sm.tmeta[j % kMetaRing];
         if (meta.item < 0) {
-          if (j > 0 && !issue_pv(j - 1)) break;
-          if (!mbar_wait(&sm.s_free[sb], ph2 ^ 1u, p.status)) break;
-          sm.smeta[sb] = meta;
-          mbar_arrive(&sm.s_full[sb]);  // both arrivals: the softmax warps see the sentinel
-          mbar_arrive(&sm.s_full[sb]);
+          if (j > 0) issue_pv(j - 1);
+          mbar_arrive(&sm.s_full[kb]);  // the softmax warps see the sentinel
           break;
         }
         const int qb = meta.qbuf;
         if (meta.first && !mbar_wait(&sm.q_full[qb], (uint32_t)(local_item >> 1) & 1u, p.status)) break;
-        if (!mbar_wait(&sm.s_free[sb], ph2 ^ 1u, p.status)) break;
         tc_fence_after();
-        const uint32_t qbase = smem_u32(sm.q[qb]);
         const uint32_t tk = tmem + kColK + kb * 64;
-        const uint32_t ts = tmem + kColS + sb * 16;
+        const uint32_t ts = tmem + kColS + kb * kNS;
+        const uint64_t b0 = umma_desc(smem_u32(sm.q[qb]), 16, 1024);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-#pragma unroll
-          for (int s = 0; s < kD / 16; ++s) {
-            const uint64_t bd =
-                umma_desc(qbase + part * kI8QPartBytes + (s >> 2) * (kNP * 128) + (s & 3) * 32, 16, 1024);
-            umma_f16_tmem_a(ts, tk + s * 8, bd, idesc_qk, (part | s) != 0);
-          }
-        }
-        sm.smeta[sb] = meta;
-        mbar_arrive(&sm.s_full[sb]);
-        umma_commit(&sm.s_full[sb]);
-        umma_commit(&sm.k_free[kb]);
+        for (int s = 0; s < kD / 16; ++s)  // 16 channels per step
+          umma_f16_tmem_a(ts, tk + s * 8, b0 + ((((s >> 2) * (kI8QRows * 128)) + (s & 3) * 32) >> 4), idesc_qk, s > 0);
+        umma_commit(&sm.s_full[kb]);
         if (meta.last) {
           umma_commit(&sm.q_empty[qb]);
           ++local_item;
         }
         if (j > 0 && !issue_pv(j - 1)) break;
-        ++j;
       }
     }
   } else if (warp < 6) {
@@ -313,13 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     auto correct = [&](int jj, bool use_fin) -> bool {
       const int ob = jj & 1;
-      if (!mbar_wait(&sm.o_full[ob], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
+      if (!mbar_wait(&sm.pv_done[ob], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
       tc_fence_after();
       float o[kNP];
-      tmem_ld16(tq + kColO + ob * 16, o);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.o_free[ob]);
+      tmem_ld16(tq + kColO + ob * kNP, o);  // read before this warp's next p_full arrival
 #pragma unroll
       for (int g = 0; g < GP; ++g) acc[g] = prev_first ? o[g] : fmaf(acc[g], alpha_prev[g], o[g]);
       if (prev_last) {
@@ -383,14 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sb = j & 1;
       const uint32_t sph = (uint32_t)(j >> 1) & 1u;
       if (!mbar_wait(&sm.s_full[sb], sph, p.status)) { ok = false; break; }
-      const I8Meta meta = sm.smeta[sb];
+      const I8Meta meta = sm.tmeta[j % kMetaRing];
       if (meta.item < 0) break;
       tc_fence_after();
       float s[kNP];
-      tmem_ld16(tq + kColS + sb * 16, s);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.s_free[sb]);
+      tmem_ld_scores(tq + kColS + sb * kNS, s);
       if (meta.first) {
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
@@ -417,9 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&sm.q_empty[meta.qbuf]);
       }
 #pragma unroll
-      for (int off = 16; off; off >>= 1)
-#pragma unroll
-        for (int g = 0; g < GP; ++g) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
+      for (int g = 0; g < GP; ++g) mx[g] = warp_max(mx[g]);
       if (lane == 0) {
 #pragma unroll
         for (int g = 0; g < GP; ++g) sm.red[sb][quad][g] = mx[g];
@@ -436,12 +432,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_part[g] = fmaf(l_part[g], alpha[g], pr[g]);
         m_run[g] = m_new;
       }
-      if (!mbar_wait(&sm.p_free[sb], sph ^ 1u, p.status)) { ok = false; break; }
-      uint8_t* pbuf = sm.p[sb];
+      uint8_t* pbuf = sm.p[sb];  // free: PV(j - 2) was waited for in correct(j - 2)
 #pragma unroll
       for (int g = 0; g < GP; ++g)
         if (g < G) *reinterpret_cast<uint16_t*>(pbuf + i8_p_offset(g, r)) = __half_as_ushort(__float2half_rn(pr[g]));
       fence_proxy_async_smem();
+      tc_fence_before();  // the tensor-memory reads of S(j) and O(j - 2) precede the arrival
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[sb]);
       if (j > 0 && !correct(j - 1, meta.first)) { ok = false; break; }
@@ -470,9 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&sm.kv_full[st], (uint32_t)(j / kStages) & 1u, p.status)) break;
       const I8Meta meta = sm.meta[st];
       const int kb = j & 1;
-      if (!mbar_wait(&sm.k_free[kb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
+      // QK(j - 2) has completed: the K buffer is free, and the softmax warps have read tmeta of tile j - 4
+      if (!mbar_wait(&sm.s_full[kb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
+      if (warp == 6 && lane == 0) sm.tmeta[j % kMetaRing] = meta;
       if (meta.item < 0) {
-        if (warp == 6 && lane == 0) sm.kmeta[kb] = meta;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.k_full[kb]);
         break;
@@ -497,7 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (warp == 6) sm.kmeta[kb] = meta;
         mbar_arrive(&sm.kv_empty[st]);
         mbar_arrive(&sm.k_full[kb]);
       }
@@ -510,7 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&sm.kv_full[st], (uint32_t)(j / kStages) & 1u, p.status)) break;
       if (sm.meta[st].item < 0) break;
       const int vb = j & 1;
-      if (!mbar_wait(&sm.v_free[vb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
+      // PV(j - 2) has completed: the fp16 V buffer is free
+      if (!mbar_wait(&sm.pv_done[vb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
       const uint32_t row = smem_u32(sm.kv[st][1]) + r * 128;
       const uint32_t dst = smem_u32(sm.v16[vb]) + r * 128;
 #pragma unroll

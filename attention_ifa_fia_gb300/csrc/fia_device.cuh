@@ -57,6 +57,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Non-blocking probe: true if the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -82,9 +93,12 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 
 // Wait for the phase with the given parity to complete.  Returns false (and
 // raises kStatusWaitTimeout) if it has not completed within kWaitLimitCycles.
-// Waiting threads sleep in the barrier rather than spin, so that they do not
-// take issue slots from the warps doing the work.
+// A phase that has already completed is seen by the non-blocking probe (the
+// potentially blocking try_wait costs far more even then); otherwise the thread
+// sleeps in the barrier rather than spin, so that it does not take issue slots
+// from the warps doing the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* status) {
+  if (mbar_test_wait(bar, parity)) return true;
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait_suspend(bar, parity, 200000u)) {
