@@ -65,9 +65,7 @@ struct TcSmem {
   TileMeta meta[C::kStages];
   uint64_t kv_full[C::kStages], kv_empty[C::kStages];
   uint64_t q_full[2], q_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full[2], p_free[2];
-  uint64_t o_full[2], o_free[2];
+  uint64_t s_full[2], p_full[2];
   uint32_t tmem_base;
 };
 
@@ -93,6 +91,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.G;
 
+  // Synchronisation.  kv_full: TMA -> MMA.  s_full: QK(j) committed -> softmax.
+  // p_full: the four softmax warps -> MMA; each arrives after reading S(j) and, earlier
+  // in its program, O(j - 2), so the MMA warp may then overwrite those S and O buffers
+  // too.  kv_empty: PV(j) committed -> producer (stage free) and softmax (O(j) ready,
+  // P buffer free).  q_empty: the item's last QK committed -> producer.
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&sm.kv_full[s], 1);
@@ -102,11 +105,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_free[i], 4);
       mbar_init(&sm.p_full[i], 4);
-      mbar_init(&sm.p_free[i], 1);
-      mbar_init(&sm.o_full[i], 1);
-      mbar_init(&sm.o_free[i], 4);
     }
     fence_mbar_init();
   }
@@ -200,7 +199,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const int pb = jj & 1;
         const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
         if (!mbar_wait(&sm.p_full[pb], ph, p.status)) return false;
-        if (!mbar_wait(&sm.o_free[pb], ph ^ 1u, p.status)) return false;
         tc_fence_after();
         const int st = jj % C::kStages;
         const uint32_t vbase = smem_u32(sm.kv[st][1]);
@@ -223,8 +221,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             umma_f16(ocol + 16, a, b1, idesc_pv, s > 0);
           }
         }
-        umma_commit(&sm.o_full[pb]);
-        umma_commit(&sm.p_free[pb]);
         umma_commit(&sm.kv_empty[st]);
         return true;
       };
@@ -241,8 +237,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         const int qb = meta.qbuf;
         if (meta.first && !mbar_wait(&sm.q_full[qb], (uint32_t)(local_item >> 1) & 1u, p.status)) { ok = false; break; }
-        const int sb = j & 1;
-        if (!mbar_wait(&sm.s_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) { ok = false; break; }
+        const int sb = j & 1;  // free: p_full(j - 2) was waited for before PV(j - 2)
         tc_fence_after();
         const uint32_t kbase = smem_u32(sm.kv[st][0]);
         const uint32_t qbase = smem_u32(sm.q[qb]);
@@ -280,14 +275,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // rescale-and-accumulate of the PV result of tile jj; finalises its item if it was the last tile
     auto correct = [&](int jj, bool use_fin) -> bool {
       const int ob = jj & 1;
-      if (!mbar_wait(&sm.o_full[ob], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
+      if (!mbar_wait(&sm.kv_empty[jj % C::kStages], (uint32_t)(jj / C::kStages) & 1u, p.status)) return false;
       tc_fence_after();
       float o[kNP];
       const uint32_t ocol = tq + C::kColO + ob * C::kOStride + ((C::kStacked && r >= 64) ? 16 : 0);
-      tmem_ld16(ocol, o);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.o_free[ob]);
+      tmem_ld16(ocol, o);  // read before this warp's next p_full arrival
 #pragma unroll
       for (int g = 0; g < GP; ++g) acc[g] = prev_first ? o[g] : fmaf(acc[g], alpha_prev[g], o[g]);
       if (prev_last) {
@@ -368,9 +360,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       tc_fence_after();
       float s[kNP];
       tmem_ld16(tq + C::kColS + sb * 16, s);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.s_free[sb]);
       if (meta.first) {
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
@@ -409,8 +398,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         l_part[g] = fmaf(l_part[g], alpha[g], pr[g]);
         m_run[g] = m_new;
       }
-      // P^T (and a zeroed V tail) for the PV MMA
-      if (!mbar_wait(&sm.p_free[sb], sph ^ 1u, p.status)) { ok = false; break; }
+      // P^T (and a zeroed V tail) for the PV MMA; the P buffer is free since PV(j - 2)
+      // was waited for in correct(j - 2)
       uint8_t* pbuf = sm.p[sb];
 #pragma unroll
       for (int g = 0; g < GP; ++g) {
@@ -431,6 +420,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
       }
       fence_proxy_async_smem();
+      tc_fence_before();  // the tensor-memory reads of S(j) and O(j - 2) precede the arrival
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[sb]);
       // rescale-and-accumulate the previous tile's PV result
