@@ -121,7 +121,8 @@ __device__ __forceinline__ float q_elem(const uint16_t* q, int idx, int q_dtype)
 }
 
 // ------------------------------------------------------------------- plan
-constexpr int kPlanSmemB = 4096;  // batches whose item offsets fit in shared memory
+constexpr int kPlanSmemB = 4096;  // batches whose item offsets and order slots fit in shared memory
+constexpr int kPlanMaxTiles = 64;  // size classes of the execution order (tiles per item, capped)
 
 __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b, bool flag) {
   const int64_t raw = p.seq_lens[b];
@@ -141,15 +142,22 @@ __device__ void write_empty_batch(const DecodeParams& p, int b) {
 }
 
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
+  // Launched as a dependent of whatever precedes it on the stream (often the previous
+  // call's merge), so that its launch overlaps that kernel's end: nothing is read or
+  // written before the preceding work is complete.
+  griddep_wait();
   griddep_launch_dependents();  // the attention kernel may begin its prologue
   if (blockIdx.x > 0) {  // int8 tensor-core path: q' blocks, one warp per (b, kv head, padded row)
     const int64_t R = (int64_t)(blockIdx.x - 1) * 32 + (threadIdx.x >> 5);
     if (R < (int64_t)p.B * p.Nkv * kI8Heads) i8_qprep_row(p, R, threadIdx.x & 31);
     return;
   }
-  extern __shared__ int sbase[];  // [B + 1] item offsets when B <= kPlanSmemB
+  // When B <= kPlanSmemB: sbase[B + 1] item offsets, then fpos[B] and tpos[B], the
+  // first execution-order slots of each batch's full chunks and of its last chunks.
+  extern __shared__ int sbase[];
   __shared__ int warp_tot[32];
   __shared__ int carry;
+  __shared__ int bucket[kPlanMaxTiles + 1];  // items per size (tiles), then the next free slot
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool in_smem = p.B <= kPlanSmemB;
   if (tid == 0) carry = 0;
@@ -194,7 +202,41 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   }
   const int total = carry;
   if (in_smem) {
+    // Execution order, longest first (a persistent CTA that takes a long item last
+    // would finish late): a counting sort of the items by their number of tiles.
+    // Full chunks all have kt = C / 128 tiles; the last chunk of a batch has
+    // ceil((L - (nch - 1) C) / 128).  Slots inside a size class are claimed in any
+    // order, which changes only the order in which CTAs pick up the items.
+    int* fpos = sbase + p.B + 1;
+    int* tpos = fpos + p.B;
+    const int kt = min(C / kDecodeTileTC, kPlanMaxTiles);  // larger items share the top class
+    for (int k = tid; k <= kPlanMaxTiles; k += blockDim.x) bucket[k] = 0;
     if (tid == 0) sbase[p.B] = total;
+    __syncthreads();
+    for (int b = tid; b < p.B; b += blockDim.x) {
+      const int nch = (sbase[b + 1] - sbase[b]) / p.Nkv;
+      if (nch == 0) continue;
+      const int last = clamp_len(p, b, false) - (nch - 1) * C;
+      atomicAdd(&bucket[kt], (nch - 1) * p.Nkv);
+      atomicAdd(&bucket[min((last + kDecodeTileTC - 1) / kDecodeTileTC, kPlanMaxTiles)], p.Nkv);
+    }
+    __syncthreads();
+    if (tid == 0) {  // first slot of each size class, largest class first
+      int run = 0;
+      for (int k = kPlanMaxTiles; k >= 1; --k) {
+        const int c = bucket[k];
+        bucket[k] = run;
+        run += c;
+      }
+    }
+    __syncthreads();
+    for (int b = tid; b < p.B; b += blockDim.x) {
+      const int nch = (sbase[b + 1] - sbase[b]) / p.Nkv;
+      if (nch == 0) continue;
+      const int last = clamp_len(p, b, false) - (nch - 1) * C;
+      fpos[b] = atomicAdd(&bucket[kt], (nch - 1) * p.Nkv);
+      tpos[b] = atomicAdd(&bucket[min((last + kDecodeTileTC - 1) / kDecodeTileTC, kPlanMaxTiles)], p.Nkv);
+    }
     __syncthreads();
     for (int i = tid; i < total; i += blockDim.x) {  // all items in parallel
       int lo = 0, hi = p.B;                          // last b with sbase[b] <= i
@@ -207,7 +249,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
       const int nch = (sbase[b + 1] - sbase[b]) / p.Nkv;
       const int h = r / nch, j = r - h * nch;
       p.ws.items[i] = make_int4(b, h, (nch << 16) | j, min(clamp_len(p, b, false), (j + 1) * C));
+      p.ws.order[j < nch - 1 ? fpos[b] + h * (nch - 1) + j : tpos[b] + h] = i;
     }
+  } else {
+    for (int i = tid; i < total; i += blockDim.x) p.ws.order[i] = i;  // item order
   }
   if (tid == 0) {
     *p.ws.n_items = total;
@@ -252,20 +297,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
     }
-    const int n_items = *p.ws.n_items;
+    ItemQueue queue;
+    queue.start(p, lane);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    int next = 0;
-    if (lane == 0) next = atomicAdd(p.ws.counter, 1);
-    next = __shfl_sync(0xffffffffu, next, 0);
     const int bs = p.block_size;
     const uint32_t piece_bytes = (uint32_t)box_rows * C::kBoxBytes * C::kNumBoxes;  // one of K/V
-    while (ok && next < n_items) {
-      const int item = next;
-      const DecodeItem it = decode_item(p.ws.items[item], p.chunk_tokens);
-      if (lane == 0) next = atomicAdd(p.ws.counter, 1);
-      next = __shfl_sync(0xffffffffu, next, 0);
+    while (ok) {
+      int4 desc;
+      const int item = queue.pop(p, lane, &desc);
+      if (item < 0) break;
+      const DecodeItem it = decode_item(desc, p.chunk_tokens);
       const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
       const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
       for (int tok0 = t_begin; tok0 < t_end; tok0 += kTT) {
@@ -302,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) + ((int64_t)b * p.Nq + (int64_t)hkv * G) * D;
           bulk_load(sm.q[stage], qsrc, (uint32_t)(G * D * 2), &sm.full[stage]);
         }
+        if (first) queue.prefetch(p, lane);
         if (++stage == kDecodeStages) { stage = 0; phase ^= 1u; }
       }
     }
@@ -564,6 +608,7 @@ constexpr int kMergeThreads = 256;
 template <int QT>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
   griddep_wait();  // every partial of the attention kernel is written and visible
+  griddep_launch_dependents();  // a following plan kernel may launch; it waits for this grid
   extern __shared__ float2 ml[];  // [G][nch]: (max, sum), then (weight, -) per partial
   const int b = blockIdx.x / p.Nkv, hkv = blockIdx.x % p.Nkv;
   const int C = p.chunk_tokens;
@@ -725,6 +770,7 @@ size_t decode_workspace_bytes(int B, int Nkv, int G, int D, int max_items) {
   size_t s = 256;                                      // counter, n_items
   s += up(sizeof(int) * (size_t)(B > 0 ? B : 1));      // seg_base
   s += up(sizeof(int4) * (size_t)max_items);           // items
+  s += up(sizeof(int) * (size_t)max_items);            // order
   s += up(sizeof(float) * (size_t)max_items * G * D);  // part_o
   s += up(sizeof(float2) * (size_t)max_items * G);     // part_ml
   if (D == 128) s += up((size_t)kI8QBlockBytes * B * Nkv);  // qprep
@@ -742,6 +788,8 @@ DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D,
   c += up(sizeof(int) * (size_t)(B > 0 ? B : 1));
   w.items = reinterpret_cast<int4*>(c);
   c += up(sizeof(int4) * (size_t)max_items);
+  w.order = reinterpret_cast<int*>(c);
+  c += up(sizeof(int) * (size_t)max_items);
   w.part_o = reinterpret_cast<float*>(c);
   c += up(sizeof(float) * (size_t)max_items * G * D);
   w.part_ml = reinterpret_cast<float2*>(c);
@@ -753,12 +801,16 @@ DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D,
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream) {
   trace_mark(kKernelDecodePlan, 0, stream);
-  const size_t plan_smem = p.B <= kPlanSmemB ? sizeof(int) * (size_t)(p.B + 1) : 0;
+  const size_t plan_smem = p.B <= kPlanSmemB ? sizeof(int) * (size_t)(3 * p.B + 1) : 0;
+  if (plan_smem > 48 * 1024) {
+    cudaError_t e0 = cudaFuncSetAttribute(decode_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)(sizeof(int) * (3 * kPlanSmemB + 1)));
+    if (e0 != cudaSuccess) return e0;
+  }
   const bool i8tc = !tmQ && decode_uses_i8tc(p.kv_dtype, p.D);
   const int64_t prep_blocks = i8tc ? ((int64_t)p.B * p.Nkv * kI8Heads + 31) / 32 : 0;
-  decode_plan_kernel<<<(unsigned)(1 + prep_blocks), 1024, plan_smem, stream>>>(p);
+  cudaError_t e = launch_dependent(decode_plan_kernel, (int)(1 + prep_blocks), 1024, plan_smem, stream, p);
   trace_mark(kKernelDecodePlan, 1, stream);
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int grid = num_sms;
   if (tmQ) {

@@ -24,6 +24,39 @@ __device__ __forceinline__ DecodeItem decode_item(int4 d, int chunk_tokens) {
   return it;
 }
 
+// Work items for the producer warp of a persistent CTA.  Slots are claimed from the
+// global counter one item ahead and resolved through the execution order (longest
+// first), so that the latency of the claim and of the two dependent loads overlaps
+// the current item's tiles.  All lanes call every member; lane 0 holds the state.
+struct ItemQueue {
+  int n_items, claimed, next;
+  int4 next_desc;
+
+  __device__ __forceinline__ void start(const DecodeParams& p, int lane) {
+    n_items = *p.ws.n_items;
+    if (lane == 0) resolve(p, atomicAdd(p.ws.counter, 1));
+  }
+  __device__ __forceinline__ void resolve(const DecodeParams& p, int slot) {
+    next = slot < n_items ? p.ws.order[slot] : -1;
+    next_desc = next >= 0 ? p.ws.items[next] : make_int4(0, 0, 0, 0);
+  }
+  // The next item (-1 when the work is exhausted) and its descriptor; claims the
+  // slot after it.
+  __device__ __forceinline__ int pop(const DecodeParams& p, int lane, int4* desc) {
+    const int item = __shfl_sync(0xffffffffu, next, 0);
+    desc->x = __shfl_sync(0xffffffffu, next_desc.x, 0);
+    desc->y = __shfl_sync(0xffffffffu, next_desc.y, 0);
+    desc->z = __shfl_sync(0xffffffffu, next_desc.z, 0);
+    desc->w = __shfl_sync(0xffffffffu, next_desc.w, 0);
+    if (item >= 0 && lane == 0) claimed = atomicAdd(p.ws.counter, 1);
+    return item;
+  }
+  // Resolves the claimed slot; call once per popped item, after its first tile is issued.
+  __device__ __forceinline__ void prefetch(const DecodeParams& p, int lane) {
+    if (lane == 0) resolve(p, claimed);
+  }
+};
+
 // Output of a segment made of one item, straight from the item's running state:
 // acc = sum_t 2^{s_t - m} v_t (not normalised), l = sum_t 2^{s_t - m}, m in log2 units.
 // Returns the value to store for one output channel; *M_out / *W_out receive the

@@ -124,19 +124,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmQ);
     }
-    const int n_items = *p.ws.n_items;
+    ItemQueue queue;
+    queue.start(p, lane);
     const int bs = p.block_size;
     const uint32_t piece_bytes = (uint32_t)box_rows * C::kRowBytes;
     int j = 0, local_item = 0;
     bool ok = true;
-    int next = 0;
-    if (lane == 0) next = atomicAdd(p.ws.counter, 1);
-    next = __shfl_sync(0xffffffffu, next, 0);
-    while (ok && next < n_items) {
-      const int item = next;
-      const DecodeItem it = decode_item(p.ws.items[item], p.chunk_tokens);
-      if (lane == 0) next = atomicAdd(p.ws.counter, 1);
-      next = __shfl_sync(0xffffffffu, next, 0);
+    while (ok) {
+      int4 desc;
+      const int item = queue.pop(p, lane, &desc);
+      if (item < 0) break;
+      const DecodeItem it = decode_item(desc, p.chunk_tokens);
       const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
       const int qb = local_item & 1;
       if (!mbar_wait(&sm.q_empty[qb], ((local_item >> 1) & 1) ^ 1u, p.status)) { ok = false; break; }
@@ -179,6 +177,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             tma_load_2d(sm.kv[st][1] + off, &tmV, bx * 64, (int32_t)row, &sm.kv_full[st]);
           }
         }
+        if (tok0 == t_begin) queue.prefetch(p, lane);
       }
       ++local_item;
     }

@@ -46,6 +46,7 @@ struct DecodeWorkspace {
   int* n_items;     // number of work items written by the plan kernel
   int* seg_base;    // (B) first item of batch b
   int4* items;      // (max_items) {b, hkv, nch << 16 | chunk, last token + 1}
+  int* order;       // (max_items) execution order: order[k] is the k-th item to be claimed
   float* part_o;    // (max_items, G, D) normalised partial outputs
   float2* part_ml;  // (max_items, G) {max (log2 units), sum}
   uint8_t* qprep;   // (B * Nkv) q' blocks of the int8 tensor-core path (D = 128), else null
