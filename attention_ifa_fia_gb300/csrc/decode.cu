@@ -6,25 +6,28 @@
 // the paged cache, token t read from block block_table[b][t / bs], row t % bs of
 // the (blocknum, KV_N, blocksize, D) pool, with kv head h / (Nq / Nkv).
 //
-// Structure (two launches on the caller's stream):
+// Structure (three launches on the caller's stream, each a programmatic dependent
+// launch of the one before, so that launches and prologues overlap):
 //   1. plan      -- one CTA splits every (b, kv-head) sequence into work items of
-//                   `chunk_tokens` tokens, zeroes the per-segment completion
-//                   counters and resets the work counter.
-//   2. attention -- persistent CTAs (one per SM), launched with programmatic
-//                   dependent launch so that their prologue overlaps the plan.
-//                   This file holds the CUDA-core variant (used for int8 KV; the
-//                   tensor-core variant for 16-bit KV is in decode_tc.cu).  Warp 8
-//                   is the producer: it takes items from the counter, reads the
+//                   `chunk_tokens` tokens, writes their execution order (longest
+//                   first) and resets the work counter; rows of empty sequences are
+//                   written here.  For int8 KV with D = 128, further CTAs prepare the
+//                   query operand of the tensor-core kernel (decode_i8.cuh).
+//   2. attention -- persistent CTAs (one per SM) claim items from the counter
+//                   (ItemQueue, decode_common.cuh).  Three variants: tcgen05 for
+//                   16-bit KV (decode_tc.cu), tcgen05 for int8 KV with D = 128
+//                   (decode_i8tc.cu), and the CUDA-core kernel of this file for the
+//                   remaining int8 shapes.  Here warp 8 is the producer: it reads the
 //                   block table and issues TMA tile loads (2-D tensor maps over the
-//                   pool, 128- or 64-byte swizzle) of K and V into a 4-stage
-//                   mbarrier ring, plus the item's G query rows by a 1-D bulk copy.
-//                   Warps 0-7 compute, for the whole GQA group at once: scores from
-//                   register-resident q, a warp-shuffle online softmax (max and
-//                   sum), and P.V.  A segment of one item writes the final output
-//                   directly; otherwise each item leaves a normalised partial
-//                   (o, max, sum) and the CTA that completes a segment's last item
-//                   folds the partials in order by the RingAttentionUpdate rule,
-//                   adds the sink once and writes out, softmax max and sum.
+//                   pool, 128- or 64-byte swizzle) of K and V into a 4-stage mbarrier
+//                   ring, plus the item's G query rows by a 1-D bulk copy.  Warps 0-7
+//                   compute, for the whole GQA group at once: scores from
+//                   register-resident q, a warp-shuffle online softmax (max and sum),
+//                   and P.V.  A segment of one item writes the final output directly;
+//                   otherwise each item leaves a normalised partial (o, max, sum).
+//   3. merge     -- one CTA per (b, kv head) with two or more items folds the
+//                   partials in order by the RingAttentionUpdate rule, adds the sink
+//                   once and writes out, softmax max and sum.
 // Scores are kept in log2 units (scale * log2 e folded into the dot product) and
 // converted back to the natural-exp domain for the max output.
 #include "decode_common.cuh"
