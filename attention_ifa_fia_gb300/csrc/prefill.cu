@@ -86,8 +86,9 @@ __device__ __forceinline__ void seq_bounds(const PrefillParams& p, int b, int& t
 
 // ------------------------------------------------------------------ plan
 // Lists (sequence, query tile) pairs ordered by decreasing number of key tiles
-// (counting sort), resets the unit counter.  Units are list entry x query head.
-__global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int max_key_tiles) {
+// (counting sort), resets the unit counter.  Units are list entry x query head, or
+// list entry x pair of query heads for the head-pair kernel.
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int max_key_tiles, int unit_heads) {
   extern __shared__ int hist[];  // [max_key_tiles + 2]
   const int tid = threadIdx.x;
   for (int i = tid; i < max_key_tiles + 2; i += blockDim.x) hist[i] = 0;
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
   __syncthreads();
   if (tid == 0) {
     p.tile_counter[0] = 0;
-    p.tile_counter[1] = min(hist[0], p.max_tiles) * p.Nq;  // number of units
+    p.tile_counter[1] = min(hist[0], p.max_tiles) * (p.Nq / unit_heads);  // number of units
   }
 }
 
@@ -155,6 +156,15 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[3
       "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
       "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 
@@ -494,6 +504,371 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ head-pair kernel
+// For an even GQA group: a work unit is (sequence, 128-query tile, pair of query heads
+// 2hp and 2hp + 1), and both heads share the kv head, so each K and V tile is loaded
+// once for two heads.  Tensor memory holds S and O of both heads (4 x 128 columns);
+// P of a head is written over the first 64 columns of its own S once they have been
+// read.  The MMA warp alternates between the heads:
+//
+//   QK_A(0) QK_B(0) | PV_A(0) QK_A(1) PV_B(0) QK_B(1) | PV_A(1) QK_A(2) ...
+//
+// so that the softmax of one head overlaps the products of the other.  The MMAs of one
+// thread execute in issue order, so QK_X(j+1) may overwrite P_X(j) as soon as PV_X(j)
+// is issued.  Warp roles (320 threads): warp 0 TMA, warp 1 MMA, warps 2-5 head A and
+// warps 6-9 head B: one query row per thread with the whole S row in registers, the
+// softmax of every tile and, after a unit's last tile, its epilogue (normalise O, write
+// out, max and sum), during which the other head keeps the tensor cores busy.
+constexpr int kP2Threads = 320;
+constexpr int kP2TmaWarp = 0, kP2MmaWarp = 1;
+
+// 64 consecutive 32-bit TMEM columns of this thread's lane, load and wait in one statement.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,"
+      "%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]),
+        "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]),
+        "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+        "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct P2Smem {
+  alignas(1024) uint8_t q[2][kTileB];  // head A, head B of the current unit
+  alignas(1024) uint8_t k[kPStages][kTileB];
+  alignas(1024) uint8_t v[kPStages][kTileB];
+  PTileMeta meta[kMetaRing];
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kPStages], k_empty[kPStages];
+  uint64_t v_full[kPStages], v_empty[kPStages];
+  uint64_t s_full[2], p_full[2], pv_done[2];  // per head, one phase per key tile
+  uint64_t o_ready[2], o_free[2];             // per head, one phase per unit
+  int stop;                                   // set by the MMA warp after the last tile
+  uint32_t tmem_base;
+};
+static_assert(sizeof(P2Smem) <= 232448, "prefill shared memory exceeds the per-CTA limit");
+
+template <int DT>
+__global__ void __launch_bounds__(kP2Threads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  P2Smem& sm = *reinterpret_cast<P2Smem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (smem_u32(smem_raw) & 1023u) {  // the swizzled operand layouts need 1 KB alignment
+    if (tid == 0) raise_status(p.status, kStatusWaitTimeout);
+    return;
+  }
+  if (tid == 0) {
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    for (int st = 0; st < kPStages; ++st) {
+      mbar_init(&sm.k_full[st], 1);
+      mbar_init(&sm.k_empty[st], 1);
+      mbar_init(&sm.v_full[st], 1);
+      mbar_init(&sm.v_empty[st], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sm.s_full[x], 1);
+      mbar_init(&sm.p_full[x], 4);
+      mbar_init(&sm.pv_done[x], 1);
+      mbar_init(&sm.o_ready[x], 1);
+      mbar_init(&sm.o_free[x], 4);
+    }
+    sm.stop = 0;
+    fence_mbar_init();
+  }
+  if (warp == kP2MmaWarp) tmem_alloc(&sm.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  constexpr uint32_t kColS[2] = {0, 128}, kColO[2] = {256, 384};
+
+  if (warp == kP2TmaWarp) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int n_units = p.tile_counter[1];
+      const int npairs = p.Nq / 2;
+      int j = 0, u_local = 0, v_next = 0;
+      int ring_hkv[kMetaRing], ring_row[kMetaRing];
+      bool ok = true;
+      auto load_v = [&](int jv) -> bool {  // V of tile jv, one tile behind its K
+        const int st = jv % kPStages;
+        if (!mbar_wait(&sm.v_empty[st], ((uint32_t)(jv / kPStages) & 1u) ^ 1u, p.status)) return false;
+        mbar_arrive_expect_tx(&sm.v_full[st], kTileB);
+        for (int bx = 0; bx < 2; ++bx)
+          tma_load_3d(sm.v[st] + bx * (kKT * 128), &tmV, bx * 64, ring_hkv[jv % kMetaRing], ring_row[jv % kMetaRing],
+                      &sm.v_full[st]);
+        return true;
+      };
+      while (ok) {
+        const int u = atomicAdd(&p.tile_counter[0], 1);
+        if (u >= n_units) break;
+        const int pair = p.tile_list[u / npairs];
+        const int hp = u % npairs, b = pair >> 16, qt = pair & 0xffff;
+        const int h0 = 2 * hp;
+        int tq, Lq, tk, Lkv;
+        seq_bounds(p, b, tq, Lq, tk, Lkv);
+        const int q0 = qt * kQT;
+        const int nkv = max(key_tiles(q0, Lq, Lkv, p.causal), 1);
+        // both Q tiles; the previous unit's last QK_B has completed
+        if (!mbar_wait(&sm.q_empty, ((uint32_t)u_local & 1u) ^ 1u, p.status)) { ok = false; break; }
+        mbar_arrive_expect_tx(&sm.q_full, 2 * kTileB);
+        for (int x = 0; x < 2; ++x)
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_3d(sm.q[x] + bx * (kQT * 128), &tmQ, bx * 64, h0 + x, tq + q0, &sm.q_full);
+        const int hkv = h0 / p.G;
+        for (int kt = 0; kt < nkv; ++kt, ++j) {
+          const int st = j % kPStages;
+          if (!mbar_wait(&sm.k_empty[st], ((uint32_t)(j / kPStages) & 1u) ^ 1u, p.status)) { ok = false; break; }
+          PTileMeta& m = sm.meta[j % kMetaRing];
+          m.b = b; m.h = h0; m.q0 = q0; m.kvt = kt;
+          m.tq = tq; m.tk = tk; m.Lq = Lq; m.Lkv = Lkv;
+          m.first = kt == 0; m.last = kt == nkv - 1; m.qbuf = 0; m.unit = u;
+          ring_hkv[j % kMetaRing] = hkv;
+          ring_row[j % kMetaRing] = tk + kt * kKT;
+          mbar_arrive_expect_tx(&sm.k_full[st], kTileB);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_load_3d(sm.k[st] + bx * (kKT * 128), &tmK, bx * 64, hkv, tk + kt * kKT, &sm.k_full[st]);
+          if (v_next < j) {
+            if (!load_v(v_next)) { ok = false; break; }
+            ++v_next;
+          }
+        }
+        ++u_local;
+      }
+      while (ok && v_next < j) {
+        if (!load_v(v_next)) { ok = false; break; }
+        ++v_next;
+      }
+      if (ok) {  // sentinel tile
+        const int st = j % kPStages;
+        if (mbar_wait(&sm.k_empty[st], ((uint32_t)(j / kPStages) & 1u) ^ 1u, p.status)) {
+          sm.meta[j % kMetaRing].unit = -1;
+          mbar_arrive(&sm.k_full[st]);
+        }
+      }
+    }
+  } else if (warp == kP2MmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = umma_idesc_f16(DT == kBF16, 0, 0, kQT, kKT);
+      constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 0, 1, kQT, kPD);
+      const uint64_t qdesc[2] = {umma_desc(smem_u32(sm.q[0]), 16, 1024), umma_desc(smem_u32(sm.q[1]), 16, 1024)};
+      int o_units0 = 0, o_units1 = 0;  // units whose first PV into O_A / O_B has been issued
+      int u_local = 0;
+      auto qk = [&](int x, int jj) {
+        const uint64_t b0 = umma_desc(smem_u32(sm.k[jj % kPStages]), 16, 1024);
+#pragma unroll
+        for (int s = 0; s < kPD / 16; ++s) {
+          const uint32_t off = (uint32_t)(((s >> 2) * (kQT * 128) + (s & 3) * 32) >> 4);
+          umma_f16(tmem + kColS[x], qdesc[x] + off, b0 + off, idesc_qk, s > 0);
+        }
+        umma_commit(&sm.s_full[x]);
+      };
+      // flags of a tile: bit 0 first, bit 1 last
+      auto pv = [&](int x, int jj, int flags) -> bool {
+        if (!mbar_wait(&sm.p_full[x], (uint32_t)jj & 1u, p.status)) return false;
+        if (!mbar_wait(&sm.v_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return false;
+        int& ou = x ? o_units1 : o_units0;
+        if ((flags & 1) && ou > 0 && !mbar_wait(&sm.o_free[x], (uint32_t)(ou - 1) & 1u, p.status)) return false;
+        tc_fence_after();
+        const uint64_t b0 = umma_desc(smem_u32(sm.v[jj % kPStages]), kKT * 128, 1024);
+#pragma unroll
+        for (int s = 0; s < kKT / 16; ++s)
+          umma_f16_ta(tmem + kColO[x], tmem + kColS[x] + s * 8, b0 + (uint64_t)((s * 16 * 128) >> 4), idesc_pv,
+                      ((flags & 1) && s == 0) ? 0u : 1u);
+        umma_commit(&sm.pv_done[x]);
+        if (flags & 2) umma_commit(&sm.o_ready[x]);
+        if (x == 1) umma_commit(&sm.v_empty[jj % kPStages]);
+        if (flags & 1) ++ou;
+        return true;
+      };
+      // waits for K of tile jj; returns its flags, -1 at the sentinel, -2 on error
+      auto load_tile = [&](int jj) -> int {
+        if (!mbar_wait(&sm.k_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return -2;
+        const PTileMeta& m = sm.meta[jj % kMetaRing];
+        if (m.unit < 0) return -1;
+        const int flags = (m.first ? 1 : 0) | (m.last ? 2 : 0);
+        if ((flags & 1) && !mbar_wait(&sm.q_full, (uint32_t)u_local & 1u, p.status)) return -2;
+        tc_fence_after();
+        return flags;
+      };
+      int cur = load_tile(0);
+      if (cur >= 0) {
+        qk(0, 0);
+        qk(1, 0);
+        umma_commit(&sm.k_empty[0]);
+        if (cur & 2) { umma_commit(&sm.q_empty); ++u_local; }
+      }
+      for (int j = 0; cur >= 0; ++j) {
+        if (!pv(0, j, cur)) break;
+        const int nxt = load_tile(j + 1);
+        if (nxt == -2) break;
+        if (nxt >= 0) qk(0, j + 1);
+        if (!pv(1, j, cur)) break;
+        if (nxt >= 0) {
+          qk(1, j + 1);
+          umma_commit(&sm.k_empty[(j + 1) % kPStages]);
+          if (nxt & 2) { umma_commit(&sm.q_empty); ++u_local; }
+        }
+        cur = nxt;
+      }
+      // No more tiles.  The softmax warps have consumed every S phase (PV of the last tile
+      // waited for their P), so a plain arrival completes the next one and they see the flag.
+      sm.stop = 1;
+      for (int x = 0; x < 2; ++x) mbar_arrive(&sm.s_full[x]);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax and epilogue of head x
+    const int x = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // query row of the tile = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+    float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
+    int units = 0;  // units finished by this warp group
+    for (int j = 0;; ++j) {
+      if (!mbar_wait(&sm.s_full[x], (uint32_t)j & 1u, p.status)) break;
+      if (sm.stop) break;
+      const PTileMeta meta = sm.meta[j % kMetaRing];
+      tc_fence_after();
+      if (meta.first) {
+        m_run = -INFINITY;
+        m_true = -INFINITY;
+        l_run = 0.f;
+      }
+      const int qi = meta.q0 + r;
+      const bool row_ok = qi < meta.Lq;
+      const int k0 = meta.kvt * kKT;
+      int k_hi = meta.Lkv;
+      if (p.causal) k_hi = min(k_hi, qi + (meta.Lkv - meta.Lq) + 1);
+      const int nvis = row_ok ? max(0, min(k_hi - k0, kKT)) : 0;
+      // the S row in registers, scaled to log2 units, keys past the visible range at -inf
+      float s[kKT];
+      tmem_ld64(tl + kColS[x], *reinterpret_cast<float(*)[64]>(&s[0]));
+      tmem_ld64(tl + kColS[x] + 64, *reinterpret_cast<float(*)[64]>(&s[64]));
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kKT; ++i) {
+        s[i] = (i < nvis) ? s[i] * p.scale_log2 : -INFINITY;
+        mt = fmaxf(mt, s[i]);
+      }
+      const float m_old = m_run;
+      m_true = fmaxf(m_true, mt);
+      bool rescale = false;
+      float alpha = 1.f;
+      if (mt > m_run + (float)kRescaleThreshold || (m_run == -INFINITY && mt != -INFINITY)) {
+        m_run = mt;
+        if (m_old != -INFINITY) {
+          rescale = true;
+          alpha = fast_exp2(m_old - m_run);
+        }
+      }
+      // P = 2^(s - m) in 16-bit pairs, written over the first 64 columns of S
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kKT; c += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float e0 = fast_exp2(s[c + i] - m_use), e1 = fast_exp2(s[c + i + 1] - m_use);
+          lsum += e0 + e1;
+          pk[i >> 1] = (DT == kBF16) ? pack_bf16(e0, e1) : pack_f16(e0, e1);
+        }
+        tmem_st16u(tl + kColS[x] + (c >> 1), pk);
+      }
+      // O rescale (rare): PV(j - 1) complete, PV(j) not begun (it waits for this warp's P)
+      if (__any_sync(0xffffffffu, rescale && !meta.first)) {
+        if (!mbar_wait(&sm.pv_done[x], (uint32_t)(j - 1) & 1u, p.status)) break;
+        const float f = (rescale && !meta.first) ? alpha : 1.f;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kPD; c += 32) {
+          float o[32];
+          tmem_ld32(tl + kColO[x] + c, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= f;
+          tmem_st32(tl + kColO[x] + c, o);
+        }
+      }
+      l_run = fmaf(l_run, alpha, lsum);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[x]);
+      if (meta.last) {
+        // epilogue: PV of this tile complete, normalise O, write out, max and sum, release O
+        if (!mbar_wait(&sm.o_ready[x], (uint32_t)units & 1u, p.status)) break;
+        tc_fence_after();
+        const int h = meta.h + x;
+        const float sink2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+        const float m_fin = fmaxf(m_true, sink2);
+        float denom = l_run;
+        if (p.sink && m_run != -INFINITY) denom += fast_exp2(sink2 - m_run);
+        const float inv = denom > 0.f ? 1.f / denom : 0.f;
+        const int64_t tok = (int64_t)meta.tq + qi;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (tok * p.Nq + h) * (int64_t)kPD * 2);
+#pragma unroll
+        for (int c = 0; c < kPD; c += 32) {  // 32 channels at a time: load, normalise, store
+          float o[32];
+          tmem_ld32(tl + kColO[x] + c, o);
+          if (c == kPD - 32) {  // every read of O_x is done: the next unit may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.o_free[x]);
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 w;
+              if (DT == kBF16)
+                w = make_uint4(pack_bf16(o[i] * inv, o[i + 1] * inv), pack_bf16(o[i + 2] * inv, o[i + 3] * inv),
+                               pack_bf16(o[i + 4] * inv, o[i + 5] * inv), pack_bf16(o[i + 6] * inv, o[i + 7] * inv));
+              else
+                w = make_uint4(pack_f16(o[i] * inv, o[i + 1] * inv), pack_f16(o[i + 2] * inv, o[i + 3] * inv),
+                               pack_f16(o[i + 4] * inv, o[i + 5] * inv), pack_f16(o[i + 6] * inv, o[i + 7] * inv));
+              orow[(c + i) / 8] = w;
+            }
+          }
+        }
+        if (row_ok) {
+          float sum_true = 0.f;
+          if (m_fin != -INFINITY) {
+            sum_true = (m_run == -INFINITY) ? 0.f : l_run * fast_exp2(m_run - m_fin);
+            if (p.sink) sum_true += fast_exp2(sink2 - m_fin);
+          }
+          if (p.softmax_max) p.softmax_max[tok * p.Nq + h] = (m_fin == -INFINITY) ? -INFINITY : m_fin * kLn2;
+          if (p.softmax_sum) p.softmax_sum[tok * p.Nq + h] = sum_true;
+        }
+        ++units;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kP2MmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 
 size_t prefill_workspace_bytes(int B, int Nq, int max_seqlen_q) {
@@ -506,9 +881,19 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const
                            const CUtensorMap& tmV, int num_sms, cudaStream_t stream) {
   const int max_key_tiles = (p.max_seqlen_kv + kKT - 1) / kKT + 1;
   trace_mark(kKernelPrefill, 0, stream);
-  prefill_plan_kernel<<<1, 1024, sizeof(int) * (max_key_tiles + 2), stream>>>(p, max_key_tiles);
+  const bool pairs = p.G % 2 == 0;  // heads 2hp and 2hp + 1 share a kv head
+  prefill_plan_kernel<<<1, 1024, sizeof(int) * (max_key_tiles + 2), stream>>>(p, max_key_tiles, pairs ? 2 : 1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (pairs) {
+    const size_t smem2 = sizeof(P2Smem);
+    auto kern = p.dtype == kBF16 ? prefill_pair_kernel<kBF16> : prefill_pair_kernel<kF16>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+    if (e != cudaSuccess) return e;
+    kern<<<num_sms, kP2Threads, smem2, stream>>>(tmQ, tmK, tmV, p);
+    trace_mark(kKernelPrefill, 1, stream);
+    return cudaGetLastError();
+  }
   const size_t smem = sizeof(PSmem);
   if (p.dtype == kBF16) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
