@@ -159,6 +159,13 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[3
       : "memory");
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -758,15 +765,27 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       int k_hi = meta.Lkv;
       if (p.causal) k_hi = min(k_hi, qi + (meta.Lkv - meta.Lq) + 1);
       const int nvis = row_ok ? max(0, min(k_hi - k0, kKT)) : 0;
-      // the S row in registers, scaled to log2 units, keys past the visible range at -inf
+      // the S row in registers, in log2 units, keys past the visible range at -inf.  When
+      // every row of the warp sees all 128 keys and the scale is positive, the row max is
+      // taken on the raw scores (three-input max) and the scale applied once.
       float s[kKT];
       tmem_ld64(tl + kColS[x], *reinterpret_cast<float(*)[64]>(&s[0]));
       tmem_ld64(tl + kColS[x] + 64, *reinterpret_cast<float(*)[64]>(&s[64]));
+      const float sc = p.scale_log2;
+      const bool full = __all_sync(0xffffffffu, nvis == kKT) && sc > 0.f;
       float mt = -INFINITY;
+      if (full) {
+        float e = s[0];
 #pragma unroll
-      for (int i = 0; i < kKT; ++i) {
-        s[i] = (i < nvis) ? s[i] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, s[i]);
+        for (int i = 1; i + 1 < kKT; i += 2) e = fmax3(e, s[i], s[i + 1]);
+        e = fmaxf(e, s[kKT - 1]);
+        mt = e * sc;
+      } else {
+#pragma unroll
+        for (int i = 0; i < kKT; ++i) {
+          s[i] = (i < nvis) ? s[i] * sc : -INFINITY;
+          mt = fmaxf(mt, s[i]);
+        }
       }
       const float m_old = m_run;
       m_true = fmaxf(m_true, mt);
@@ -781,13 +800,14 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       }
       // P = 2^(s - m) in 16-bit pairs, written over the first 64 columns of S
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      const float mul = full ? sc : 1.f;  // raw scores on the fast path, scaled ones otherwise
       float lsum = 0.f;
 #pragma unroll
       for (int c = 0; c < kKT; c += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float e0 = fast_exp2(s[c + i] - m_use), e1 = fast_exp2(s[c + i + 1] - m_use);
+          const float e0 = fast_exp2(fmaf(s[c + i], mul, -m_use)), e1 = fast_exp2(fmaf(s[c + i + 1], mul, -m_use));
           lsum += e0 + e1;
           pk[i >> 1] = (DT == kBF16) ? pack_bf16(e0, e1) : pack_f16(e0, e1);
         }
