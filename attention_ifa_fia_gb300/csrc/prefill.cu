@@ -774,12 +774,13 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       const float sc = p.scale_log2;
       const bool full = __all_sync(0xffffffffu, nvis == kKT) && sc > 0.f;
       float mt = -INFINITY;
-      if (full) {
-        float e = s[0];
+      if (full) {  // four independent chains
+        float e[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int i = 1; i + 1 < kKT; i += 2) e = fmax3(e, s[i], s[i + 1]);
-        e = fmaxf(e, s[kKT - 1]);
-        mt = e * sc;
+        for (int i = 4; i < kKT; i += 8)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) e[k] = fmax3(e[k], s[i + 2 * k], s[i + 2 * k + 1]);
+        mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]) * sc;
       } else {
 #pragma unroll
         for (int i = 0; i < kKT; ++i) {
@@ -801,18 +802,19 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       // P = 2^(s - m) in 16-bit pairs, written over the first 64 columns of S
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       const float mul = full ? sc : 1.f;  // raw scores on the fast path, scaled ones otherwise
-      float lsum = 0.f;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
 #pragma unroll
       for (int c = 0; c < kKT; c += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const float e0 = fast_exp2(fmaf(s[c + i], mul, -m_use)), e1 = fast_exp2(fmaf(s[c + i + 1], mul, -m_use));
-          lsum += e0 + e1;
+          ls[(i >> 1) & 3] += e0 + e1;
           pk[i >> 1] = (DT == kBF16) ? pack_bf16(e0, e1) : pack_f16(e0, e1);
         }
         tmem_st16u(tl + kColS[x] + (c >> 1), pk);
       }
+      const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
       // O rescale (rare): PV(j - 1) complete, PV(j) not begun (it waits for this warp's P)
       if (__any_sync(0xffffffffu, rescale && !meta.first)) {
         if (!mbar_wait(&sm.pv_done[x], (uint32_t)(j - 1) & 1u, p.status)) break;
