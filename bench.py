@@ -509,25 +509,36 @@ def cpu_baseline_prefill(case: W.PrefillCase, budget_s: float = 15.0, seed: int 
             "seconds": round(dt, 2)}
 
 
+# Sources of the kernel whose DRAM traffic bench.py reports, per workload; a recorded
+# figure is used only while the sha1 of these files matches the one taken with it.
+TRAFFIC_SOURCES = {
+    "bf16_gqa_decode": ("decode_tc.cu", "decode.cu", "decode_common.cuh", "fia_device.cuh", "fia_internal.h"),
+    "long_ctx_sink_decode": ("decode_tc.cu", "decode.cu", "decode_common.cuh", "fia_device.cuh", "fia_internal.h"),
+    "int8_antiquant_decode": ("decode_i8tc.cu", "decode_i8.cuh", "decode.cu", "decode_common.cuh", "fia_device.cuh",
+                              "fia_internal.h"),
+    "causal_prefill_tnd": ("prefill.cu", "fia_device.cuh", "fia_internal.h"),
+}
+
+
+def traffic_sha(workload):
+    import hashlib
+    csrc = os.path.join(ROOT, "attention_ifa_fia_gb300", "csrc")
+    h = hashlib.sha1()
+    for name in TRAFFIC_SOURCES[workload]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
 def load_traffic(workload):
     """DRAM bytes (read + write) per launch of the dominant kernel from the committed ncu summary
-    (profiles/kernel_traffic.json), or None if the kernel source changed since it was taken."""
-    import hashlib
-    path = os.path.join(ROOT, "profiles", "kernel_traffic.json")
-    csrc = os.path.join(ROOT, "attention_ifa_fia_gb300", "csrc")
+    (profiles/kernel_traffic.json), or None if the kernel's sources changed since it was taken."""
     try:
-        with open(path) as f:
-            d = json.load(f)
-        if workload == "causal_prefill_tnd":
-            with open(os.path.join(csrc, "prefill.cu"), "rb") as f:
-                sha = hashlib.sha1(f.read()).hexdigest()[:12]
-            return d.get(workload) if d.get("prefill source sha1") == sha else None
-        blob = b""
-        for name in ("decode_tc.cu", "decode.cu", "decode_common.cuh"):
-            with open(os.path.join(csrc, name), "rb") as f:
-                blob += f.read()
-        sha = hashlib.sha1(blob).hexdigest()[:12]
-        return d.get(workload) if d.get("decode sources sha1") == sha else None
+        with open(os.path.join(ROOT, "profiles", "kernel_traffic.json")) as f:
+            entry = json.load(f).get(workload)
+        if not entry or entry.get("sources_sha1") != traffic_sha(workload):
+            return None
+        return entry.get("bytes_per_launch")
     except Exception:
         return None
 
