@@ -16,11 +16,13 @@
 // weighs with P rounded to fp16, the correction with the fp32 sum l, a difference
 // of at most |o_d s_d| 2^-11 per output.
 //
-// Warp roles (448 threads):
+// Warp roles (480 threads):
 //   warp 0      TMA producer: the item's q' block (one bulk copy from the workspace),
 //               int8 K and V tiles (128 rows x 128 bytes, 128-byte swizzle) into a
 //               4-stage ring.
-//   warp 1      TMEM allocation; one thread issues the MMAs.
+//   warp 1      TMEM allocation; one thread issues the score MMAs.
+//   warp 14     one thread issues the PV MMAs (a second issue stream on another SM
+//               sub-partition: an MMA blocks its issuing thread for about 50 cycles).
 //   warps 2-5   online softmax of tile j (one token per TMEM lane) and the
 //               rescale-and-accumulate of the PV result of tile j-1 (one channel
 //               per lane), final output or split partial.
@@ -40,7 +42,8 @@ constexpr int kT = 128;     // tokens per tile: the M of the score MMA
 constexpr int kNP = 16;     // query heads per group, padded: the N of both MMAs
 constexpr int kD = 128;     // head dim (the M of the PV MMA)
 constexpr int kStages = 4;  // int8 ring
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
+constexpr int kPvWarp = 14;  // issues the PV MMAs (warp 1 the score MMAs)
 constexpr int kBarSoftmax = 2;                       // named barrier of the softmax warps
 // TMEM columns.  An MMA of M = 128 costs the tensor pipe about the same for any
 // N <= 64, so the hi and lo parts of q' share one MMA of N = 32.
@@ -73,6 +76,7 @@ struct I8Smem {
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t k_full[2], v_full[2], q_full[2], q_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
+  int pv_stop;  // set by the softmax warps at the sentinel tile
   uint32_t tmem_base;
 };
 static_assert(sizeof(I8Smem) + 1024 <= 232448, "shared memory of the int8 decode kernel");
@@ -175,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.p_full[i], 4);
       mbar_init(&sm.pv_done[i], 1);
     }
+    sm.pv_stop = 0;
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -253,33 +258,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ score MMAs
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_f16(0, 0, 0, kT, kNS);  // fp16, A (TMEM) and B K-major
-      constexpr uint32_t idesc_pv = umma_idesc_f16(0, 1, 0, kT, kNP);  // fp16, A = V^T read MN-major
       int local_item = 0;
-      auto issue_pv = [&](int jj) -> bool {
-        const int pb = jj & 1;
-        const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
-        if (!mbar_wait(&sm.p_full[pb], ph, p.status)) return false;
-        if (!mbar_wait(&sm.v_full[pb], ph, p.status)) return false;
-        tc_fence_after();
-        const uint32_t ocol = tmem + kColO + pb * kNP;
-        const uint64_t a0 = umma_desc(smem_u32(sm.v16[pb]), kT * 128, 1024);
-        const uint64_t b0 = umma_desc(smem_u32(sm.p[pb]), 16, 1024);
-#pragma unroll
-        for (int s = 0; s < kT / 16; ++s)  // 16 tokens per step
-          umma_f16(ocol, a0 + ((s * 16 * 128) >> 4), b0 + ((((s >> 2) * (kNP * 128)) + (s & 3) * 32) >> 4),
-                   idesc_pv, s > 0);
-        umma_commit(&sm.pv_done[pb]);
-        return true;
-      };
       for (int j = 0;; ++j) {
         const int kb = j & 1;
         if (!mbar_wait(&sm.k_full[kb], (uint32_t)(j >> 1) & 1u, p.status)) break;
+        // the S buffer of tile j - 2 has been read (its P written)
+        if (j >= 2 && !mbar_wait(&sm.p_full[kb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
         const I8Meta meta = sm.tmeta[j % kMetaRing];
         if (meta.item < 0) {
-          if (j > 0) issue_pv(j - 1);
           mbar_arrive(&sm.s_full[kb]);  // the softmax warps see the sentinel
           break;
         }
@@ -297,7 +286,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&sm.q_empty[qb]);
           ++local_item;
         }
-        if (j > 0 && !issue_pv(j - 1)) break;
+      }
+    }
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------------ PV MMAs
+    // A warp of its own on another SM sub-partition, so that the two product streams
+    // are issued in parallel; the tensor pipe runs them interleaved.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = umma_idesc_f16(0, 1, 0, kT, kNP);  // fp16, A = V^T read MN-major
+      for (int j = 0;; ++j) {
+        const int pb = j & 1;
+        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+        if (!mbar_wait(&sm.p_full[pb], ph, p.status)) break;
+        if (sm.pv_stop) break;  // the softmax warps reached the sentinel tile
+        if (!mbar_wait(&sm.v_full[pb], ph, p.status)) break;
+        tc_fence_after();
+        const uint32_t ocol = tmem + kColO + pb * kNP;
+        const uint64_t a0 = umma_desc(smem_u32(sm.v16[pb]), kT * 128, 1024);
+        const uint64_t b0 = umma_desc(smem_u32(sm.p[pb]), 16, 1024);
+#pragma unroll
+        for (int s = 0; s < kT / 16; ++s)  // 16 tokens per step
+          umma_f16(ocol, a0 + ((s * 16 * 128) >> 4), b0 + ((((s >> 2) * (kNP * 128)) + (s & 3) * 32) >> 4),
+                   idesc_pv, s > 0);
+        umma_commit(&sm.pv_done[pb]);
       }
     }
   } else if (warp < 6) {
@@ -384,7 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sph = (uint32_t)(j >> 1) & 1u;
       if (!mbar_wait(&sm.s_full[sb], sph, p.status)) { ok = false; break; }
       const I8Meta meta = sm.tmeta[j % kMetaRing];
-      if (meta.item < 0) break;
+      if (meta.item < 0) {  // no more tiles: wake the PV warp, which stops
+        if (tid == 64) sm.pv_stop = 1;
+        named_bar_sync(kBarSoftmax, 128);
+        if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+        break;
+      }
       tc_fence_after();
       float s[kNP];
       tmem_ld_scores(tq + kColS + sb * kNS, s);
@@ -497,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sm.k_full[kb]);
       }
     }
-  } else {
+  } else if (warp < 14) {
     // ------------------------------------------------------------------ V codes -> shared memory
     const int r = (warp - 10) * 32 + lane;
     for (int j = 0;; ++j) {
