@@ -76,7 +76,7 @@ struct I8Smem {
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t k_full[2], v_full[2], q_full[2], q_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
-  int pv_stop;  // set by the softmax warps at the sentinel tile
+  int pv_stop;  // index of the sentinel tile, set by the softmax warps when they reach it
   uint32_t tmem_base;
 };
 static_assert(sizeof(I8Smem) + 1024 <= 232448, "shared memory of the int8 decode kernel");
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.p_full[i], 4);
       mbar_init(&sm.pv_done[i], 1);
     }
-    sm.pv_stop = 0;
+    sm.pv_stop = 0x7fffffff;
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pb = j & 1;
         const uint32_t ph = (uint32_t)(j >> 1) & 1u;
         if (!mbar_wait(&sm.p_full[pb], ph, p.status)) break;
-        if (sm.pv_stop) break;  // the softmax warps reached the sentinel tile
+        if (j >= *static_cast<volatile int*>(&sm.pv_stop)) break;  // tile j is the sentinel
         if (!mbar_wait(&sm.v_full[pb], ph, p.status)) break;
         tc_fence_after();
         const uint32_t ocol = tmem + kColO + pb * kNP;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&sm.s_full[sb], sph, p.status)) { ok = false; break; }
       const I8Meta meta = sm.tmeta[j % kMetaRing];
       if (meta.item < 0) {  // no more tiles: wake the PV warp, which stops
-        if (tid == 64) sm.pv_stop = 1;
+        if (tid == 64) sm.pv_stop = j;
         named_bar_sync(kBarSoftmax, 128);
         if (lane == 0) mbar_arrive(&sm.p_full[sb]);
         break;

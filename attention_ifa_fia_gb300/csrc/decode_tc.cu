@@ -16,9 +16,9 @@
 // two halves of A (rows 0-63: tokens 0-63, rows 64-127: tokens 64-127) and issuing
 // one MMA per half against the matching half of P^T into separate accumulators.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads (Q of each item, K and V tiles
+// Warp roles (224 threads): warp 0 issues TMA loads (Q of each item, K and V tiles
 // into a 3- or 5-stage ring); warp 1 allocates tensor memory and one thread issues
-// the MMAs; warps 2-5 own TMEM lanes 0-127: online softmax of tile j (one token per
+// the score MMAs, one thread of warp 6 the PV MMAs; warps 2-5 own TMEM lanes 0-127: online softmax of tile j (one token per
 // lane, warp-shuffle max across lanes) followed by the rescale-and-accumulate of
 // the PV result of tile j-1 (one output channel per lane).
 #include "decode_common.cuh"
@@ -29,7 +29,8 @@ namespace {
 constexpr int kT = 128;          // tokens per tile: the M of the score MMA
 constexpr int kNP = 16;          // query heads per group, padded: the N of both MMAs
 constexpr int kTmemCols = 128;
-constexpr int kThreadsTC = 192;
+constexpr int kThreadsTC = 224;
+constexpr int kPvWarpTC = 6;     // issues the PV MMAs (warp 1 the score MMAs)
 constexpr int kBarCompute = 2;   // named barrier of the 128 softmax/correction threads
 
 template <int D>
@@ -66,6 +67,7 @@ struct TcSmem {
   uint64_t kv_full[C::kStages], kv_empty[C::kStages];
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[2], p_full[2];
+  int pv_stop;  // index of the sentinel tile, set by the softmax warps when they reach it
   uint32_t tmem_base;
 };
 
@@ -91,11 +93,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.G;
 
-  // Synchronisation.  kv_full: TMA -> MMA.  s_full: QK(j) committed -> softmax.
-  // p_full: the four softmax warps -> MMA; each arrives after reading S(j) and, earlier
-  // in its program, O(j - 2), so the MMA warp may then overwrite those S and O buffers
-  // too.  kv_empty: PV(j) committed -> producer (stage free) and softmax (O(j) ready,
-  // P buffer free).  q_empty: the item's last QK committed -> producer.
+  // Synchronisation.  kv_full: TMA -> score warp.  s_full: QK(j) committed -> softmax.
+  // p_full: the four softmax warps -> PV warp (P(j) written) and score warp; each warp
+  // arrives after reading S(j) and, earlier in its program, O(j - 2), so QK(j + 2) and
+  // PV(j) may overwrite those S and O buffers.  kv_empty: PV(j) committed -> producer
+  // (stage free) and softmax (O(j) ready, P buffer free).  q_empty: the item's last QK
+  // committed -> producer.
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&sm.kv_full[s], 1);
@@ -107,6 +110,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.p_full[i], 4);
     }
+    sm.pv_stop = 0x7fffffff;
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -189,17 +193,51 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ score MMAs
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_f16(DT == kBF16, 0, 0, kT, kNP);
-      constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 1, 0, kT, kNP);
       int local_item = 0;
-      auto issue_pv = [&](int jj) -> bool {
-        const int pb = jj & 1;
-        const uint32_t ph = (uint32_t)(jj >> 1) & 1u;
-        if (!mbar_wait(&sm.p_full[pb], ph, p.status)) return false;
+      for (int j = 0;; ++j) {
+        const int st = j % C::kStages;
+        const int sb = j & 1;
+        if (!mbar_wait(&sm.kv_full[st], (uint32_t)(j / C::kStages) & 1u, p.status)) break;
+        // the S buffer of tile j - 2 has been read (its P written)
+        if (j >= 2 && !mbar_wait(&sm.p_full[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
+        const TileMeta meta = sm.meta[st];
+        if (meta.item < 0) {
+          mbar_arrive(&sm.s_full[sb]);  // lets the compute warps see the sentinel
+          break;
+        }
+        const int qb = meta.qbuf;
+        if (meta.first && !mbar_wait(&sm.q_full[qb], (uint32_t)(local_item >> 1) & 1u, p.status)) break;
         tc_fence_after();
-        const int st = jj % C::kStages;
+        const uint32_t kbase = smem_u32(sm.kv[st][0]);
+        const uint32_t qbase = smem_u32(sm.q[qb]);
+#pragma unroll
+        for (int s = 0; s < C::kKSteps; ++s) {
+          const uint64_t a = umma_desc(kbase + (s >> 2) * (kT * 128) + (s & 3) * 32, 16, 1024);
+          const uint64_t bd = umma_desc(qbase + (s >> 2) * (kNP * 128) + (s & 3) * 32, 16, 1024);
+          umma_f16(tmem + C::kColS + sb * 16, a, bd, idesc_qk, s > 0);
+        }
+        umma_commit(&sm.s_full[sb]);
+        if (meta.last) {
+          umma_commit(&sm.q_empty[qb]);
+          ++local_item;
+        }
+      }
+    }
+  } else if (warp == kPvWarpTC) {
+    // ------------------------------------------------------------------ PV MMAs
+    // A second issue stream on another SM sub-partition (an MMA blocks its issuing
+    // thread for about 50 cycles); the tensor pipe runs the two streams interleaved.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 1, 0, kT, kNP);
+      for (int j = 0;; ++j) {
+        const int pb = j & 1;
+        if (!mbar_wait(&sm.p_full[pb], (uint32_t)(j >> 1) & 1u, p.status)) break;
+        if (j >= *static_cast<volatile int*>(&sm.pv_stop)) break;  // tile j is the sentinel
+        tc_fence_after();
+        const int st = j % C::kStages;
         const uint32_t vbase = smem_u32(sm.kv[st][1]);
         const uint32_t pbase = smem_u32(sm.p[pb]);
         const uint32_t ocol = tmem + C::kColO + pb * C::kOStride;
@@ -221,40 +259,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           }
         }
         umma_commit(&sm.kv_empty[st]);
-        return true;
-      };
-      int j = 0;
-      bool ok = true;
-      while (true) {
-        const int st = j % C::kStages;
-        if (!mbar_wait(&sm.kv_full[st], (uint32_t)(j / C::kStages) & 1u, p.status)) { ok = false; break; }
-        const TileMeta meta = sm.meta[st];
-        if (meta.item < 0) {
-          if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
-          mbar_arrive(&sm.s_full[j & 1]);  // lets the compute warps see the sentinel
-          break;
-        }
-        const int qb = meta.qbuf;
-        if (meta.first && !mbar_wait(&sm.q_full[qb], (uint32_t)(local_item >> 1) & 1u, p.status)) { ok = false; break; }
-        const int sb = j & 1;  // free: p_full(j - 2) was waited for before PV(j - 2)
-        tc_fence_after();
-        const uint32_t kbase = smem_u32(sm.kv[st][0]);
-        const uint32_t qbase = smem_u32(sm.q[qb]);
-#pragma unroll
-        for (int s = 0; s < C::kKSteps; ++s) {
-          const uint64_t a = umma_desc(kbase + (s >> 2) * (kT * 128) + (s & 3) * 32, 16, 1024);
-          const uint64_t bd = umma_desc(qbase + (s >> 2) * (kNP * 128) + (s & 3) * 32, 16, 1024);
-          umma_f16(tmem + C::kColS + sb * 16, a, bd, idesc_qk, s > 0);
-        }
-        umma_commit(&sm.s_full[sb]);
-        if (meta.last) {
-          umma_commit(&sm.q_empty[qb]);
-          ++local_item;
-        }
-        if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
-        ++j;
       }
-      (void)ok;
     }
   } else {
     // ------------------------------------------------------------------ softmax + correction
@@ -355,7 +360,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (!mbar_wait(&sm.s_full[sb], sph, p.status)) { ok = false; break; }
       const int st = j % C::kStages;
       const TileMeta meta = sm.meta[st];
-      if (meta.item < 0) break;
+      if (meta.item < 0) {  // no more tiles: wake the PV warp, which stops
+        if (tid == 64) sm.pv_stop = j;
+        named_bar_sync(kBarCompute, 128);
+        if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+        break;
+      }
       tc_fence_after();
       float s[kNP];
       tmem_ld16(tq + C::kColS + sb * 16, s);

@@ -119,6 +119,9 @@ EDGE = {
     "int8_tc_poisoned_g8": (dict(B=3, Nq=8, Nkv=1, D=128, block_size=64, kv_dtype=W.INT8, lengths=[5, 130, 257],
                                  poison=True, spare_blocks=3, table_pad=2), [0, 2]),
     "int8_tc_empty_seqs": (dict(B=3, Nq=8, Nkv=2, D=128, block_size=32, kv_dtype=W.INT8, lengths=[0, 40, 0]), [0]),
+    "int8_tc_one_tile_items": (dict(B=4, Nq=8, Nkv=2, D=128, block_size=64, kv_dtype=W.INT8, lengths=[1, 60, 128, 5]),
+                               [0]),
+    "one_tile_items_bf16": (dict(B=4, Nq=8, Nkv=2, D=128, block_size=64, lengths=[1, 60, 128, 5]), [0]),
     "int8_tc_many_batches": (dict(B=200, Nq=8, Nkv=2, D=128, block_size=128, kv_dtype=W.INT8, len_range=(0, 300)),
                              [0]),
     "sink_bf16": (dict(B=2, Nq=8, Nkv=2, D=64, block_size=16, lengths=[40, 90], sink=True), [0, 3]),
