@@ -16,7 +16,7 @@
 // weighs with P rounded to fp16, the correction with the fp32 sum l, a difference
 // of at most |o_d s_d| 2^-11 per output.
 //
-// Warp roles (480 threads):
+// Warp roles (608 threads):
 //   warp 0      TMA producer: the item's q' block (one bulk copy from the workspace),
 //               int8 K and V tiles (128 rows x 128 bytes, 128-byte swizzle) into a
 //               4-stage ring.
@@ -24,8 +24,9 @@
 //   warp 14     one thread issues the PV MMAs (a second issue stream on another SM
 //               sub-partition: an MMA blocks its issuing thread for about 50 cycles).
 //   warps 2-5   online softmax of tile j (one token per TMEM lane) and the
-//               rescale-and-accumulate of the PV result of tile j-1 (one channel
-//               per lane), final output or split partial.
+//   and 15-18   rescale-and-accumulate of the PV result of tile j-1 (one channel
+//               per lane), final output or split partial; each group takes half of
+//               the heads.
 //   warps 6-9   K codes -> fp16 pairs in TMEM (one token row per lane): the A
 //               operand of the score MMA, double buffered.
 //   warps 10-13 V codes -> fp16 in shared memory, in the MN-major layout of the A
@@ -42,8 +43,10 @@ constexpr int kT = 128;     // tokens per tile: the M of the score MMA
 constexpr int kNP = 16;     // query heads per group, padded: the N of both MMAs
 constexpr int kD = 128;     // head dim (the M of the PV MMA)
 constexpr int kStages = 4;  // int8 ring
-constexpr int kThreads = 480;
-constexpr int kPvWarp = 14;  // issues the PV MMAs (warp 1 the score MMAs)
+constexpr int kThreads = 608;
+constexpr int kPvWarp = 14;     // issues the PV MMAs (warp 1 the score MMAs)
+constexpr int kSm2Warp0 = 15;   // warps 15-18: the second softmax warp group
+constexpr int kSoftmaxThreads = 256;
 constexpr int kBarSoftmax = 2;                       // named barrier of the softmax warps
 // TMEM columns.  An MMA of M = 128 costs the tensor pipe about the same for any
 // N <= 64, so the hi and lo parts of q' share one MMA of N = 32.
@@ -68,8 +71,8 @@ struct I8Smem {
   alignas(1024) uint8_t v16[2][kVTile];
   alignas(1024) uint8_t q[2][kI8QBytes];
   alignas(1024) uint8_t p[2][kPBytes];
-  float2 kn[2][kNP];
-  float red[2][4][kNP];
+  alignas(16) float2 kn[2][kNP];
+  alignas(16) float red[2][kNP][4];  // [S buffer][head][warp]: per-warp maxima
   float lsum[4][kNP];
   I8Meta meta[kStages];    // per int8 stage (producer)
   I8Meta tmeta[kMetaRing];  // per tile j at j % kMetaRing (K converters)
@@ -173,10 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.k_full[i], 4);
       mbar_init(&sm.v_full[i], 4);
       mbar_init(&sm.q_full[i], 1);
-      mbar_init(&sm.q_empty[i], 5);  // MMA commit after the item's last QK + the 4 softmax warps
+      mbar_init(&sm.q_empty[i], 9);  // MMA commit after the item's last QK + the 8 softmax warps
                                      // after reading the item's constants at its last tile
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.p_full[i], 8);
       mbar_init(&sm.pv_done[i], 1);
     }
     sm.pv_stop = 0x7fffffff;
@@ -311,14 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&sm.pv_done[pb]);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 6 || warp >= kSm2Warp0) {
     // ------------------------------------------------------------------ softmax + correction
+    // Two warp groups share the work of each tile: group 0 (warps 2-5) takes heads
+    // [0, GH), group 1 (warps 15-18) heads [GH, 2 GH), so that each thread's chain of
+    // dependent steps per tile is half as long.
+    constexpr int GH = GP / 2;
+    const bool upper = warp >= kSm2Warp0;
+    const int h0 = upper ? GH : 0;
     const int quad = warp & 3;       // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;  // TMEM lane: token of S, channel of O
     const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
-    float m_run[GP], l_part[GP], alpha_prev[GP], acc[GP], m_fin[GP], l_fin[GP];
+    float m_run[GH], l_part[GH], alpha_prev[GH], acc[GH], m_fin[GH], l_fin[GH];
 #pragma unroll
-    for (int g = 0; g < GP; ++g) {
+    for (int g = 0; g < GH; ++g) {
       m_run[g] = -INFINITY; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_fin[g] = -INFINITY; l_fin[g] = 0.f;
     }
     float vs_cur = 0.f, vo_cur = 0.f, vs_new = 0.f, vo_new = 0.f;  // value antiquant of channel r
@@ -332,39 +341,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       float o[kNP];
       tmem_ld16(tq + kColO + ob * kNP, o);  // read before this warp's next p_full arrival
 #pragma unroll
-      for (int g = 0; g < GP; ++g) acc[g] = prev_first ? o[g] : fmaf(acc[g], alpha_prev[g], o[g]);
+      for (int g = 0; g < GH; ++g) {
+        const float og = upper ? o[GH + g] : o[g];  // compile-time indices
+        acc[g] = prev_first ? og : fmaf(acc[g], alpha_prev[g], og);
+      }
       if (prev_last) {
-        float mm[GP], lv[GP];
+        float mm[GH], lv[GH];
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
+        for (int g = 0; g < GH; ++g) {
           mm[g] = use_fin ? m_fin[g] : m_run[g];
           lv[g] = use_fin ? l_fin[g] : l_part[g];
         }
 #pragma unroll
         for (int off = 16; off; off >>= 1)
 #pragma unroll
-          for (int g = 0; g < GP; ++g) lv[g] += __shfl_xor_sync(0xffffffffu, lv[g], off);
+          for (int g = 0; g < GH; ++g) lv[g] += __shfl_xor_sync(0xffffffffu, lv[g], off);
         if (lane == 0) {
 #pragma unroll
-          for (int g = 0; g < GP; ++g) sm.lsum[quad][g] = lv[g];
+          for (int g = 0; g < GH; ++g) sm.lsum[quad][h0 + g] = lv[g];
         }
-        named_bar_sync(kBarSoftmax, 128);
-        float lt[GP], a[GP];
+        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        float lt[GH], a[GH];
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          lt[g] = sm.lsum[0][g] + sm.lsum[1][g] + sm.lsum[2][g] + sm.lsum[3][g];
+        for (int g = 0; g < GH; ++g) {
+          lt[g] = sm.lsum[0][h0 + g] + sm.lsum[1][h0 + g] + sm.lsum[2][h0 + g] + sm.lsum[3][h0 + g];
           a[g] = vs_cur * fmaf(-vo_cur, lt[g], acc[g]);  // sum_t p_t v^_t, unnormalised
         }
         if (prev_nch == 1) {
           const int64_t orow = ((int64_t)prev_b * p.Nq + prev_hkv * G) * kD + r;
 #pragma unroll
-          for (int g = 0; g < GP; ++g) {
-            if (g < G) {
-              const int h = prev_hkv * G + g;
+          for (int g = 0; g < GH; ++g) {
+            const int hg = h0 + g;
+            if (hg < G) {
+              const int h = prev_hkv * G + hg;
               float M, W;
               const float v = single_item_output(a[g], mm[g], lt[g], p.sink, h, &M, &W);
-              store_out<QT>(p.out, orow + (int64_t)g * kD, v);
-              if (r == g) {
+              store_out<QT>(p.out, orow + (int64_t)hg * kD, v);
+              if (r == hg) {
                 if (p.softmax_max) p.softmax_max[(int64_t)prev_b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
                 if (p.softmax_sum) p.softmax_sum[(int64_t)prev_b * p.Nq + h] = W;
               }
@@ -373,17 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           float* po = p.ws.part_o + (int64_t)prev_item * G * kD;
 #pragma unroll
-          for (int g = 0; g < GP; ++g)
-            if (g < G) po[g * kD + r] = lt[g] > 0.f ? a[g] / lt[g] : 0.f;
-          if (r < GP && r < G) {
+          for (int g = 0; g < GH; ++g)
+            if (h0 + g < G) po[(h0 + g) * kD + r] = lt[g] > 0.f ? a[g] / lt[g] : 0.f;
+          if (r >= h0 && r < h0 + GH && r < G) {
             float mv = mm[0], lw = lt[0];
 #pragma unroll
-            for (int g = 1; g < GP; ++g)
-              if (r == g) { mv = mm[g]; lw = lt[g]; }
+            for (int g = 1; g < GH; ++g)
+              if (r == h0 + g) { mv = mm[g]; lw = lt[g]; }
             p.ws.part_ml[(int64_t)prev_item * G + r] = make_float2(mv, lw);
           }
         }
-        named_bar_sync(kBarSoftmax, 128);
+        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
       }
       return true;
     };
@@ -397,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const I8Meta meta = sm.tmeta[j % kMetaRing];
       if (meta.item < 0) {  // no more tiles: wake the PV warp, which stops
         if (tid == 64) sm.pv_stop = j;
-        named_bar_sync(kBarSoftmax, 128);
+        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
         if (lane == 0) mbar_arrive(&sm.p_full[sb]);
         break;
       }
@@ -406,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_scores(tq + kColS + sb * kNS, s);
       if (meta.first) {
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
+        for (int g = 0; g < GH; ++g) {
           m_fin[g] = m_run[g];
           l_fin[g] = l_part[g];
           m_run[g] = -INFINITY;
@@ -417,29 +430,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         vo_new = p.aq_offset ? p.aq_offset[vi] : 0.f;
       }
       const bool valid = r < meta.n;
-      float x[GP], mx[GP];
-      const float2* kn = sm.kn[meta.qbuf];  // {kq, nq} of the item's heads (decode_i8.cuh)
+      float x[GH], mx[GH];
+      const float2* kn = sm.kn[meta.qbuf] + h0;  // {kq, nq} of this group's heads (decode_i8.cuh)
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
+      for (int g = 0; g < GH; ++g) {
         const float2 c = kn[g];
-        x[g] = valid ? fmaf(s[g], c.x, c.y) : -INFINITY;
-        mx[g] = x[g];
+        const float sg = upper ? s[GH + g] : s[g];  // compile-time indices
+        x[g] = valid ? fmaf(sg, c.x, c.y) : -INFINITY;
+        mx[g] = warp_max(x[g]);
       }
       if (meta.last) {  // the q' buffer may be refilled once the MMA thread is done with it too
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.q_empty[meta.qbuf]);
       }
-#pragma unroll
-      for (int g = 0; g < GP; ++g) mx[g] = warp_max(mx[g]);
       if (lane == 0) {
 #pragma unroll
-        for (int g = 0; g < GP; ++g) sm.red[sb][quad][g] = mx[g];
+        for (int g = 0; g < GH; ++g) sm.red[sb][h0 + g][quad] = mx[g];
       }
-      named_bar_sync(kBarSoftmax, 128);
-      float alpha[GP], pr[GP];
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+      float alpha[GH], pr[GH];
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        const float tmax = fmaxf(fmaxf(sm.red[sb][0][g], sm.red[sb][1][g]), fmaxf(sm.red[sb][2][g], sm.red[sb][3][g]));
+      for (int g = 0; g < GH; ++g) {
+        const float4 rq = *reinterpret_cast<const float4*>(sm.red[sb][h0 + g]);  // the four quadrants' maxima
+        const float tmax = fmax3(fmaxf(rq.x, rq.y), rq.z, rq.w);
         const float m_new = fmaxf(m_run[g], tmax);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         alpha[g] = fast_exp2(m_run[g] - m_use);
@@ -449,8 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint8_t* pbuf = sm.p[sb];  // free: PV(j - 2) was waited for in correct(j - 2)
 #pragma unroll
-      for (int g = 0; g < GP; ++g)
-        if (g < G) *reinterpret_cast<uint16_t*>(pbuf + i8_p_offset(g, r)) = __half_as_ushort(__float2half_rn(pr[g]));
+      for (int g = 0; g < GH; ++g)
+        if (h0 + g < G)
+          *reinterpret_cast<uint16_t*>(pbuf + i8_p_offset(h0 + g, r)) = __half_as_ushort(__float2half_rn(pr[g]));
       fence_proxy_async_smem();
       tc_fence_before();  // the tensor-memory reads of S(j) and O(j - 2) precede the arrival
       __syncwarp();
@@ -461,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         vo_cur = vo_new;
       }
 #pragma unroll
-      for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
+      for (int g = 0; g < GH; ++g) alpha_prev[g] = alpha[g];
       prev_first = meta.first;
       prev_last = meta.last;
       prev_item = meta.item;

@@ -60,7 +60,7 @@ struct TcSmem {
   alignas(1024) uint8_t kv[C::kStages][2][C::kTileBytes];
   alignas(1024) uint8_t q[2][C::kQBytes];
   alignas(1024) uint8_t p[2][C::kPBytes];
-  float red[2][4][kNP];
+  alignas(16) float red[2][kNP][4];  // [S buffer][head][warp]: per-warp maxima
   float lsum[4][kNP];
   float accx[C::kStacked ? 64 : 1][kNP];
   TileMeta meta[C::kStages];
@@ -393,13 +393,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         for (int g = 0; g < GP; ++g) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
       if (lane == 0) {
 #pragma unroll
-        for (int g = 0; g < GP; ++g) sm.red[sb][quad][g] = mx[g];
+        for (int g = 0; g < GP; ++g) sm.red[sb][g][quad] = mx[g];
       }
       named_bar_sync(kBarCompute, 128);
       float alpha[GP], pr[GP];
 #pragma unroll
       for (int g = 0; g < GP; ++g) {
-        const float tmax = fmaxf(fmaxf(sm.red[sb][0][g], sm.red[sb][1][g]), fmaxf(sm.red[sb][2][g], sm.red[sb][3][g]));
+        const float4 rq = *reinterpret_cast<const float4*>(sm.red[sb][g]);  // the four warps' maxima
+        const float tmax = fmax3(fmaxf(rq.x, rq.y), rq.z, rq.w);
         const float m_new = fmaxf(m_run[g], tmax);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         alpha[g] = fast_exp2(m_run[g] - m_use);   // m_run = -inf gives 0
