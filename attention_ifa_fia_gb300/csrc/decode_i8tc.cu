@@ -135,13 +135,6 @@ __device__ __forceinline__ void tmem_ld_scores(uint32_t taddr, float (&v)[kNP]) 
   for (int i = 0; i < kNP; ++i) v[i] = a[i] + a[kNP + i];
 }
 
-// Maximum over the warp.
-__device__ __forceinline__ float warp_max(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
-
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }

@@ -16,11 +16,12 @@
 // two halves of A (rows 0-63: tokens 0-63, rows 64-127: tokens 64-127) and issuing
 // one MMA per half against the matching half of P^T into separate accumulators.
 //
-// Warp roles (224 threads): warp 0 issues TMA loads (Q of each item, K and V tiles
+// Warp roles (352 threads): warp 0 issues TMA loads (Q of each item, K and V tiles
 // into a 3- or 5-stage ring); warp 1 allocates tensor memory and one thread issues
-// the score MMAs, one thread of warp 6 the PV MMAs; warps 2-5 own TMEM lanes 0-127: online softmax of tile j (one token per
-// lane, warp-shuffle max across lanes) followed by the rescale-and-accumulate of
-// the PV result of tile j-1 (one output channel per lane).
+// the score MMAs, one thread of warp 6 the PV MMAs.  Warps 2-5 and warps 7-10 are
+// two groups that each own TMEM lanes 0-127 for half of the query heads: online
+// softmax of tile j (one token per lane, warp max across lanes) followed by the
+// rescale-and-accumulate of the PV result of tile j-1 (one output channel per lane).
 #include "decode_common.cuh"
 
 namespace fia {
@@ -29,9 +30,11 @@ namespace {
 constexpr int kT = 128;          // tokens per tile: the M of the score MMA
 constexpr int kNP = 16;          // query heads per group, padded: the N of both MMAs
 constexpr int kTmemCols = 128;
-constexpr int kThreadsTC = 224;
+constexpr int kThreadsTC = 352;
 constexpr int kPvWarpTC = 6;     // issues the PV MMAs (warp 1 the score MMAs)
-constexpr int kBarCompute = 2;   // named barrier of the 128 softmax/correction threads
+constexpr int kSm2Warp0 = 7;     // warps 7-10: the second softmax warp group
+constexpr int kSoftmaxThreadsTC = 256;
+constexpr int kBarCompute = 2;   // named barrier of the 256 softmax/correction threads
 
 template <int D>
 struct TcCfg {
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.p_full[i], 8);
     }
     sm.pv_stop = 0x7fffffff;
     fence_mbar_init();
@@ -263,14 +266,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     }
   } else {
     // ------------------------------------------------------------------ softmax + correction
-    // GP (the group size rounded up to a power of two) is a compile-time bound, so the
-    // per-head loops unroll into independent chains the scheduler can interleave.
+    // Two warp groups share the work of each tile: group 0 (warps 2-5) takes heads
+    // [0, GH), group 1 (warps 7-10) heads [GH, 2 GH), so that each thread's chain of
+    // dependent steps per tile is half as long.  GP (the group size rounded up to a
+    // power of two) is a compile-time bound, so the per-head loops unroll into
+    // independent chains the scheduler can interleave.
+    constexpr int GH = GP / 2;
+    const bool upper = warp >= kSm2Warp0;
+    const int h0 = upper ? GH : 0;
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;            // TMEM lane: token of S, channel of O
     const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
-    float m_run[GP], l_part[GP], alpha_prev[GP], acc[GP], m_fin[GP], l_fin[GP];
+    float m_run[GH], l_part[GH], alpha_prev[GH], acc[GH], m_fin[GH], l_fin[GH];
 #pragma unroll
-    for (int g = 0; g < GP; ++g) {
+    for (int g = 0; g < GH; ++g) {
       m_run[g] = -INFINITY; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_fin[g] = -INFINITY; l_fin[g] = 0.f;
     }
     int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
@@ -285,43 +294,48 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const uint32_t ocol = tq + C::kColO + ob * C::kOStride + ((C::kStacked && r >= 64) ? 16 : 0);
       tmem_ld16(ocol, o);  // read before this warp's next p_full arrival
 #pragma unroll
-      for (int g = 0; g < GP; ++g) acc[g] = prev_first ? o[g] : fmaf(acc[g], alpha_prev[g], o[g]);
+      for (int g = 0; g < GH; ++g) {
+        const float og = upper ? o[GH + g] : o[g];  // compile-time indices
+        acc[g] = prev_first ? og : fmaf(acc[g], alpha_prev[g], og);
+      }
       if (prev_last) {
-        float mm[GP], lv[GP];
+        float mm[GH], lv[GH];
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
+        for (int g = 0; g < GH; ++g) {
           mm[g] = use_fin ? m_fin[g] : m_run[g];
           lv[g] = use_fin ? l_fin[g] : l_part[g];
         }
 #pragma unroll
         for (int off = 16; off; off >>= 1)
 #pragma unroll
-          for (int g = 0; g < GP; ++g) lv[g] += __shfl_xor_sync(0xffffffffu, lv[g], off);
+          for (int g = 0; g < GH; ++g) lv[g] += __shfl_xor_sync(0xffffffffu, lv[g], off);
         if (lane == 0) {
 #pragma unroll
-          for (int g = 0; g < GP; ++g) sm.lsum[quad][g] = lv[g];
+          for (int g = 0; g < GH; ++g) sm.lsum[quad][h0 + g] = lv[g];
         }
         if (C::kStacked && r >= 64) {
 #pragma unroll
-          for (int g = 0; g < GP; ++g) sm.accx[r - 64][g] = acc[g];
+          for (int g = 0; g < GH; ++g) sm.accx[r - 64][h0 + g] = acc[g];
         }
-        named_bar_sync(kBarCompute, 128);
-        float lt[GP];
+        named_bar_sync(kBarCompute, kSoftmaxThreadsTC);
+        float lt[GH];
 #pragma unroll
-        for (int g = 0; g < GP; ++g) lt[g] = sm.lsum[0][g] + sm.lsum[1][g] + sm.lsum[2][g] + sm.lsum[3][g];
+        for (int g = 0; g < GH; ++g)
+          lt[g] = sm.lsum[0][h0 + g] + sm.lsum[1][h0 + g] + sm.lsum[2][h0 + g] + sm.lsum[3][h0 + g];
         if (prev_nch == 1) {
           // the segment is this one item: write the final output directly
           if (!C::kStacked || r < 64) {
             const int64_t orow = ((int64_t)prev_b * p.Nq + prev_hkv * G) * D + r;
 #pragma unroll
-            for (int g = 0; g < GP; ++g) {
-              if (g < G) {
-                const float a = C::kStacked ? acc[g] + sm.accx[r][g] : acc[g];
-                const int h = prev_hkv * G + g;
+            for (int g = 0; g < GH; ++g) {
+              const int hg = h0 + g;
+              if (hg < G) {
+                const float a = C::kStacked ? acc[g] + sm.accx[r][hg] : acc[g];
+                const int h = prev_hkv * G + hg;
                 float M, W;
                 const float v = single_item_output(a, mm[g], lt[g], p.sink, h, &M, &W);
-                store_out<DT>(p.out, orow + (int64_t)g * D, v);
-                if (r == g) {
+                store_out<DT>(p.out, orow + (int64_t)hg * D, v);
+                if (r == hg) {
                   if (p.softmax_max) p.softmax_max[(int64_t)prev_b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
                   if (p.softmax_sum) p.softmax_sum[(int64_t)prev_b * p.Nq + h] = W;
                 }
@@ -332,22 +346,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           if (!C::kStacked || r < 64) {
             float* po = p.ws.part_o + (int64_t)prev_item * G * D;
 #pragma unroll
-            for (int g = 0; g < GP; ++g) {
-              if (g < G) {
-                const float a = C::kStacked ? acc[g] + sm.accx[r][g] : acc[g];
-                po[g * D + r] = lt[g] > 0.f ? a / lt[g] : 0.f;
+            for (int g = 0; g < GH; ++g) {
+              const int hg = h0 + g;
+              if (hg < G) {
+                const float a = C::kStacked ? acc[g] + sm.accx[r][hg] : acc[g];
+                po[hg * D + r] = lt[g] > 0.f ? a / lt[g] : 0.f;
               }
             }
           }
-          if (r < GP && r < G) {
+          if (r >= h0 && r < h0 + GH && r < G) {
             float mv = mm[0], lw = lt[0];
 #pragma unroll
-            for (int g = 1; g < GP; ++g)
-              if (r == g) { mv = mm[g]; lw = lt[g]; }
+            for (int g = 1; g < GH; ++g)
+              if (r == h0 + g) { mv = mm[g]; lw = lt[g]; }
             p.ws.part_ml[(int64_t)prev_item * G + r] = make_float2(mv, lw);
           }
         }
-        named_bar_sync(kBarCompute, 128);
+        named_bar_sync(kBarCompute, kSoftmaxThreadsTC);
       }
       return true;
     };
@@ -362,7 +377,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const TileMeta meta = sm.meta[st];
       if (meta.item < 0) {  // no more tiles: wake the PV warp, which stops
         if (tid == 64) sm.pv_stop = j;
-        named_bar_sync(kBarCompute, 128);
+        named_bar_sync(kBarCompute, kSoftmaxThreadsTC);
         if (lane == 0) mbar_arrive(&sm.p_full[sb]);
         break;
       }
@@ -371,7 +386,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       tmem_ld16(tq + C::kColS + sb * 16, s);
       if (meta.first) {
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
+        for (int g = 0; g < GH; ++g) {
           m_fin[g] = m_run[g];
           l_fin[g] = l_part[g];
           m_run[g] = -INFINITY;
@@ -379,27 +394,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
       }
       const bool valid = r < meta.n;
-      // per-head maximum over the tile's tokens: warp butterflies (independent per head),
-      // then across the 4 warps through shared memory
-      float x[GP], mx[GP];
+      // per-head maximum over the tile's tokens: a warp reduction per head, then across
+      // the 4 lane quadrants through shared memory
+      float x[GH], mx[GH];
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        x[g] = valid ? s[g] * p.scale_log2 : -INFINITY;
-        mx[g] = x[g];
+      for (int g = 0; g < GH; ++g) {
+        const float sg = upper ? s[GH + g] : s[g];  // compile-time indices
+        x[g] = valid ? sg * p.scale_log2 : -INFINITY;
+        mx[g] = warp_max(x[g]);
       }
-#pragma unroll
-      for (int off = 16; off; off >>= 1)
-#pragma unroll
-        for (int g = 0; g < GP; ++g) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
       if (lane == 0) {
 #pragma unroll
-        for (int g = 0; g < GP; ++g) sm.red[sb][g][quad] = mx[g];
+        for (int g = 0; g < GH; ++g) sm.red[sb][h0 + g][quad] = mx[g];
       }
-      named_bar_sync(kBarCompute, 128);
-      float alpha[GP], pr[GP];
+      named_bar_sync(kBarCompute, kSoftmaxThreadsTC);
+      float alpha[GH], pr[GH];
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        const float4 rq = *reinterpret_cast<const float4*>(sm.red[sb][g]);  // the four warps' maxima
+      for (int g = 0; g < GH; ++g) {
+        const float4 rq = *reinterpret_cast<const float4*>(sm.red[sb][h0 + g]);  // the four quadrants' maxima
         const float tmax = fmax3(fmaxf(rq.x, rq.y), rq.z, rq.w);
         const float m_new = fmaxf(m_run[g], tmax);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -408,19 +420,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         l_part[g] = fmaf(l_part[g], alpha[g], pr[g]);
         m_run[g] = m_new;
       }
-      // P^T (and a zeroed V tail) for the PV MMA; the P buffer is free since PV(j - 2)
-      // was waited for in correct(j - 2)
+      // P^T (and, from group 0, a zeroed V tail) for the PV MMA; the P buffer is free since
+      // PV(j - 2) was waited for in correct(j - 2)
       uint8_t* pbuf = sm.p[sb];
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        if (g < G) {
+      for (int g = 0; g < GH; ++g) {
+        if (h0 + g < G) {
           uint16_t h;
           if (DT == kBF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(pr[g]));
           else h = __half_as_ushort(__float2half_rn(pr[g]));
-          *reinterpret_cast<uint16_t*>(pbuf + p_offset(g, r)) = h;
+          *reinterpret_cast<uint16_t*>(pbuf + p_offset(h0 + g, r)) = h;
         }
       }
-      if (!valid) {
+      if (!valid && !upper) {
         uint8_t* vrow = sm.kv[st][1];
 #pragma unroll
         for (int bx = 0; bx < C::kNumBoxes; ++bx) {
@@ -436,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       // rescale-and-accumulate the previous tile's PV result
       if (j > 0 && !correct(j - 1, meta.first)) { ok = false; break; }
 #pragma unroll
-      for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
+      for (int g = 0; g < GH; ++g) alpha_prev[g] = alpha[g];
       prev_first = meta.first;
       prev_last = meta.last;
       prev_item = meta.item;
