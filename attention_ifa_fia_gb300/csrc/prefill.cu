@@ -178,6 +178,16 @@ __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// As umma_f16_ta, executed by a whole converged warp (one elected lane issues).
+__device__ __forceinline__ void umma_f16_ta_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ attention
 template <int DT>
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -650,6 +660,12 @@ __global__ void __launch_bounds__(kP2Threads, 1)
             ++v_next;
           }
         }
+        // the unit's remaining V tiles before the next unit's Q, whose buffer frees only
+        // after the unit's last QK
+        while (ok && v_next < j) {
+          if (!load_v(v_next)) { ok = false; break; }
+          ++v_next;
+        }
         ++u_local;
       }
       while (ok && v_next < j) {
@@ -665,8 +681,8 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       }
     }
   } else if (warp == kP2MmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer (whole warp)
+    {
       constexpr uint32_t idesc_qk = umma_idesc_f16(DT == kBF16, 0, 0, kQT, kKT);
       constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 0, 1, kQT, kPD);
       const uint64_t qdesc[2] = {umma_desc(smem_u32(sm.q[0]), 16, 1024), umma_desc(smem_u32(sm.q[1]), 16, 1024)};
@@ -677,35 +693,35 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 #pragma unroll
         for (int s = 0; s < kPD / 16; ++s) {
           const uint32_t off = (uint32_t)(((s >> 2) * (kQT * 128) + (s & 3) * 32) >> 4);
-          umma_f16(tmem + kColS[x], qdesc[x] + off, b0 + off, idesc_qk, s > 0);
+          umma_f16_w(tmem + kColS[x], qdesc[x] + off, b0 + off, idesc_qk, s > 0);
         }
-        umma_commit(&sm.s_full[x]);
+        umma_commit_w(&sm.s_full[x]);
       };
       // flags of a tile: bit 0 first, bit 1 last
       auto pv = [&](int x, int jj, int flags) -> bool {
-        if (!mbar_wait(&sm.p_full[x], (uint32_t)jj & 1u, p.status)) return false;
-        if (!mbar_wait(&sm.v_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return false;
+        if (!mbar_wait_warp(&sm.p_full[x], (uint32_t)jj & 1u, p.status)) return false;
+        if (!mbar_wait_warp(&sm.v_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return false;
         int& ou = x ? o_units1 : o_units0;
-        if ((flags & 1) && ou > 0 && !mbar_wait(&sm.o_free[x], (uint32_t)(ou - 1) & 1u, p.status)) return false;
+        if ((flags & 1) && ou > 0 && !mbar_wait_warp(&sm.o_free[x], (uint32_t)(ou - 1) & 1u, p.status)) return false;
         tc_fence_after();
         const uint64_t b0 = umma_desc(smem_u32(sm.v[jj % kPStages]), kKT * 128, 1024);
 #pragma unroll
         for (int s = 0; s < kKT / 16; ++s)
-          umma_f16_ta(tmem + kColO[x], tmem + kColS[x] + s * 8, b0 + (uint64_t)((s * 16 * 128) >> 4), idesc_pv,
-                      ((flags & 1) && s == 0) ? 0u : 1u);
-        umma_commit(&sm.pv_done[x]);
-        if (flags & 2) umma_commit(&sm.o_ready[x]);
-        if (x == 1) umma_commit(&sm.v_empty[jj % kPStages]);
+          umma_f16_ta_w(tmem + kColO[x], tmem + kColS[x] + s * 8, b0 + (uint64_t)((s * 16 * 128) >> 4), idesc_pv,
+                        ((flags & 1) && s == 0) ? 0u : 1u);
+        umma_commit_w(&sm.pv_done[x]);
+        if (flags & 2) umma_commit_w(&sm.o_ready[x]);
+        if (x == 1) umma_commit_w(&sm.v_empty[jj % kPStages]);
         if (flags & 1) ++ou;
         return true;
       };
       // waits for K of tile jj; returns its flags, -1 at the sentinel, -2 on error
       auto load_tile = [&](int jj) -> int {
-        if (!mbar_wait(&sm.k_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return -2;
+        if (!mbar_wait_warp(&sm.k_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return -2;
         const PTileMeta& m = sm.meta[jj % kMetaRing];
         if (m.unit < 0) return -1;
         const int flags = (m.first ? 1 : 0) | (m.last ? 2 : 0);
-        if ((flags & 1) && !mbar_wait(&sm.q_full, (uint32_t)u_local & 1u, p.status)) return -2;
+        if ((flags & 1) && !mbar_wait_warp(&sm.q_full, (uint32_t)u_local & 1u, p.status)) return -2;
         tc_fence_after();
         return flags;
       };
@@ -713,8 +729,8 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       if (cur >= 0) {
         qk(0, 0);
         qk(1, 0);
-        umma_commit(&sm.k_empty[0]);
-        if (cur & 2) { umma_commit(&sm.q_empty); ++u_local; }
+        umma_commit_w(&sm.k_empty[0]);
+        if (cur & 2) { umma_commit_w(&sm.q_empty); ++u_local; }
       }
       for (int j = 0; cur >= 0; ++j) {
         if (!pv(0, j, cur)) break;
@@ -724,15 +740,17 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         if (!pv(1, j, cur)) break;
         if (nxt >= 0) {
           qk(1, j + 1);
-          umma_commit(&sm.k_empty[(j + 1) % kPStages]);
-          if (nxt & 2) { umma_commit(&sm.q_empty); ++u_local; }
+          umma_commit_w(&sm.k_empty[(j + 1) % kPStages]);
+          if (nxt & 2) { umma_commit_w(&sm.q_empty); ++u_local; }
         }
         cur = nxt;
       }
       // No more tiles.  The softmax warps have consumed every S phase (PV of the last tile
       // waited for their P), so a plain arrival completes the next one and they see the flag.
-      sm.stop = 1;
-      for (int x = 0; x < 2; ++x) mbar_arrive(&sm.s_full[x]);
+      if (lane == 0) {
+        sm.stop = 1;
+        for (int x = 0; x < 2; ++x) mbar_arrive(&sm.s_full[x]);
+      }
     }
   } else {
     // ------------------------------------------------------------------ softmax and epilogue of head x
