@@ -23,7 +23,7 @@
 // epilogue.  O is rescaled only when the running row max
 // grows by more than 8 (log2 units); otherwise the stale max keeps every exponent
 // <= 2^8, and the softmax max/sum outputs are converted to the true max at the end.
-#include "fia_device.cuh"
+#include "decode_common.cuh"
 
 namespace fia {
 namespace {
@@ -87,41 +87,60 @@ __device__ __forceinline__ void seq_bounds(const PrefillParams& p, int b, int& t
 // ------------------------------------------------------------------ plan
 // Lists (sequence, query tile) pairs ordered by decreasing number of key tiles
 // (counting sort), resets the unit counter.  Units are list entry x query head, or
-// list entry x pair of query heads for the head-pair kernel.
+// list entry x pair of query heads for the head-pair kernel.  The bounds of a chunk of
+// sequences are read once into shared memory (the two passes would otherwise wait on
+// dependent global loads sequence after sequence); warp w handles sequences w, w + 32, ...
+// of the chunk, its lanes the query tiles.  Launched as a dependent of the preceding
+// kernel: it waits for that kernel before touching memory and lets the attention kernel
+// start its prologue at once.
+constexpr int kPlanChunk = 256;  // sequences whose bounds are staged at a time
+
+size_t prefill_plan_smem(int max_key_tiles) {
+  return sizeof(int) * (size_t)((max_key_tiles + 2 + 3) & ~3) + sizeof(int4) * kPlanChunk;
+}
+
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int max_key_tiles, int unit_heads) {
-  extern __shared__ int hist[];  // [max_key_tiles + 2]
-  const int tid = threadIdx.x;
+  extern __shared__ int sh[];
+  int* hist = sh;                                                          // [max_key_tiles + 2]
+  int4* bounds = reinterpret_cast<int4*>(sh + ((max_key_tiles + 2 + 3) & ~3));  // {tq, Lq, tk, Lkv}
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  griddep_wait();
+  griddep_launch_dependents();
   for (int i = tid; i < max_key_tiles + 2; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  for (int b = 0; b < p.B; ++b) {  // pass 1: histogram of key-tile counts
-    int tq, Lq, tk, Lkv;
-    seq_bounds(p, b, tq, Lq, tk, Lkv);
-    for (int qt = tid; qt * kQT < Lq; qt += blockDim.x) {
-      const int n = min(max(key_tiles(qt * kQT, Lq, Lkv, p.causal), 1), max_key_tiles);
-      atomicAdd(&hist[n], 1);
+  for (int pass = 0; pass < 2; ++pass) {  // pass 0: histogram of key-tile counts; pass 1: scatter
+    for (int b0 = 0; b0 < p.B; b0 += kPlanChunk) {
+      const int nb = min(kPlanChunk, p.B - b0);
+      __syncthreads();  // the previous chunk's bounds are no longer read
+      for (int i = tid; i < nb; i += blockDim.x) {
+        int tq, Lq, tk, Lkv;
+        seq_bounds(p, b0 + i, tq, Lq, tk, Lkv);
+        bounds[i] = make_int4(tq, Lq, tk, Lkv);
+      }
+      __syncthreads();
+      for (int i = warp; i < nb; i += nwarps) {
+        const int4 bd = bounds[i];
+        for (int qt = lane; qt * kQT < bd.y; qt += 32) {
+          const int n = min(max(key_tiles(qt * kQT, bd.y, bd.w, p.causal), 1), max_key_tiles);
+          if (pass == 0) {
+            atomicAdd(&hist[n], 1);
+          } else {
+            const int pos = atomicAdd(&hist[n], 1);
+            if (pos < p.max_tiles) p.tile_list[pos] = ((b0 + i) << 16) | qt;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (pass == 0 && tid == 0) {  // exclusive offsets, largest count first
+      int run = 0;
+      for (int n = max_key_tiles; n >= 1; --n) {
+        const int c = hist[n];
+        hist[n] = run;
+        run += c;
+      }
+      hist[0] = run;  // total pairs
     }
   }
-  __syncthreads();
-  if (tid == 0) {  // exclusive offsets, largest count first
-    int run = 0;
-    for (int n = max_key_tiles; n >= 1; --n) {
-      const int c = hist[n];
-      hist[n] = run;
-      run += c;
-    }
-    hist[0] = run;  // total pairs
-  }
-  __syncthreads();
-  for (int b = 0; b < p.B; ++b) {  // pass 2: scatter
-    int tq, Lq, tk, Lkv;
-    seq_bounds(p, b, tq, Lq, tk, Lkv);
-    for (int qt = tid; qt * kQT < Lq; qt += blockDim.x) {
-      const int n = min(max(key_tiles(qt * kQT, Lq, Lkv, p.causal), 1), max_key_tiles);
-      const int pos = atomicAdd(&hist[n], 1);
-      if (pos < p.max_tiles) p.tile_list[pos] = (b << 16) | qt;
-    }
-  }
-  __syncthreads();
   if (tid == 0) {
     p.tile_counter[0] = 0;
     p.tile_counter[1] = min(hist[0], p.max_tiles) * (p.Nq / unit_heads);  // number of units
@@ -603,6 +622,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_wait();  // the plan's unit list (this kernel is a dependent launch)
   const uint32_t tmem = sm.tmem_base;
   constexpr uint32_t kColS[2] = {0, 128}, kColO[2] = {256, 384};
 
@@ -915,15 +935,21 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const
   const int max_key_tiles = (p.max_seqlen_kv + kKT - 1) / kKT + 1;
   trace_mark(kKernelPrefill, 0, stream);
   const bool pairs = p.G % 2 == 0;  // heads 2hp and 2hp + 1 share a kv head
-  prefill_plan_kernel<<<1, 1024, sizeof(int) * (max_key_tiles + 2), stream>>>(p, max_key_tiles, pairs ? 2 : 1);
-  cudaError_t e = cudaGetLastError();
+  const size_t plan_smem = prefill_plan_smem(max_key_tiles);
+  cudaError_t e = cudaSuccess;
+  if (plan_smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_dependent(prefill_plan_kernel, 1, 1024, plan_smem, stream, p, max_key_tiles, pairs ? 2 : 1);
   if (e != cudaSuccess) return e;
   if (pairs) {
     const size_t smem2 = sizeof(P2Smem);
     auto kern = p.dtype == kBF16 ? prefill_pair_kernel<kBF16> : prefill_pair_kernel<kF16>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
     if (e != cudaSuccess) return e;
-    kern<<<num_sms, kP2Threads, smem2, stream>>>(tmQ, tmK, tmV, p);
+    e = launch_dependent(kern, num_sms, kP2Threads, smem2, stream, tmQ, tmK, tmV, p);
+    if (e != cudaSuccess) return e;
     trace_mark(kKernelPrefill, 1, stream);
     return cudaGetLastError();
   }

@@ -32,6 +32,9 @@ CASES = {
     "sink_q_longer": dict(Nq=2, Nkv=1, D=128, lengths=[140], lengths_kv=[20], sink=True),
     "no_mask": dict(Nq=4, Nkv=2, D=128, lengths=[77, 260], causal=False),
     "no_mask_lq_ne_lkv": dict(Nq=2, Nkv=1, D=128, lengths=[33, 140], lengths_kv=[500, 1], causal=False),
+    # more sequences than the plan stages at a time (256), short ones and a long tail
+    "many_seqs": dict(Nq=2, Nkv=1, D=128, lengths=[(i * 37) % 23 for i in range(600)] + [300]),
+    "many_seqs_g1": dict(Nq=1, Nkv=1, D=128, lengths=[(i * 11) % 19 for i in range(300)] + [260, 0]),
 }
 
 
