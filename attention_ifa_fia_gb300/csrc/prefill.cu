@@ -577,6 +577,7 @@ struct P2Smem {
   alignas(1024) uint8_t q[2][kTileB];  // head A, head B of the current unit
   alignas(1024) uint8_t k[kPStages][kTileB];
   alignas(1024) uint8_t v[kPStages][kTileB];
+  alignas(128) uint8_t ostage[8][32 * 128];  // per softmax warp: 32 rows x 64 channels of out
   PTileMeta meta[kMetaRing];
   uint64_t q_full, q_empty;
   uint64_t k_full[kPStages], k_empty[kPStages];
@@ -812,12 +813,18 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) e[k] = fmax3(e[k], s[i + 2 * k], s[i + 2 * k + 1]);
         mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]) * sc;
-      } else {
+      } else {  // scaled scores, masked keys at -inf; four independent chains
+        float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < kKT; ++i) {
-          s[i] = (i < nvis) ? s[i] * sc : -INFINITY;
-          mt = fmaxf(mt, s[i]);
-        }
+        for (int i = 0; i < kKT; i += 8)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int i0 = i + 2 * k, i1 = i0 + 1;
+            s[i0] = (i0 < nvis) ? s[i0] * sc : -INFINITY;
+            s[i1] = (i1 < nvis) ? s[i1] * sc : -INFINITY;
+            e[k] = fmax3(e[k], s[i0], s[i1]);
+          }
+        mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]);
       }
       const float m_old = m_run;
       m_true = fmaxf(m_true, mt);
@@ -876,29 +883,43 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         if (p.sink && m_run != -INFINITY) denom += fast_exp2(sink2 - m_run);
         const float inv = denom > 0.f ? 1.f / denom : 0.f;
         const int64_t tok = (int64_t)meta.tq + qi;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (tok * p.Nq + h) * (int64_t)kPD * 2);
+        // out, 64 channels at a time: normalise and pack the warp's 32 rows into its staging
+        // slot (16-byte chunk c of row l at position c ^ (l & 7): no bank conflicts either
+        // way), then store 4 rows x 128 bytes per instruction
+        uint8_t* stg = sm.ostage[warp - 2];
+        const int row0 = meta.q0 + quad * 32;  // query row of lane 0
+        const int rows_ok = min(max(meta.Lq - row0, 0), 32);
+        uint8_t* obase = static_cast<uint8_t*>(p.out) + (((int64_t)meta.tq + row0) * p.Nq + h) * (int64_t)kPD * 2;
+        const int64_t orow_stride = (int64_t)p.Nq * kPD * 2;
 #pragma unroll
-        for (int c = 0; c < kPD; c += 32) {  // 32 channels at a time: load, normalise, store
-          float o[32];
-          tmem_ld32(tl + kColO[x] + c, o);
-          if (c == kPD - 32) {  // every read of O_x is done: the next unit may overwrite it
+        for (int half = 0; half < 2; ++half) {
+          float o[64];
+          tmem_ld64(tl + kColO[x] + half * 64, o);
+          if (half == 1) {  // every read of O_x is done: the next unit may overwrite it
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.o_free[x]);
           }
-          if (row_ok) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 w;
-              if (DT == kBF16)
-                w = make_uint4(pack_bf16(o[i] * inv, o[i + 1] * inv), pack_bf16(o[i + 2] * inv, o[i + 3] * inv),
-                               pack_bf16(o[i + 4] * inv, o[i + 5] * inv), pack_bf16(o[i + 6] * inv, o[i + 7] * inv));
-              else
-                w = make_uint4(pack_f16(o[i] * inv, o[i + 1] * inv), pack_f16(o[i + 2] * inv, o[i + 3] * inv),
-                               pack_f16(o[i + 4] * inv, o[i + 5] * inv), pack_f16(o[i + 6] * inv, o[i + 7] * inv));
-              orow[(c + i) / 8] = w;
-            }
+          for (int c = 0; c < 8; ++c) {
+            const float* v = o + 8 * c;
+            uint4 w;
+            if (DT == kBF16)
+              w = make_uint4(pack_bf16(v[0] * inv, v[1] * inv), pack_bf16(v[2] * inv, v[3] * inv),
+                             pack_bf16(v[4] * inv, v[5] * inv), pack_bf16(v[6] * inv, v[7] * inv));
+            else
+              w = make_uint4(pack_f16(v[0] * inv, v[1] * inv), pack_f16(v[2] * inv, v[3] * inv),
+                             pack_f16(v[4] * inv, v[5] * inv), pack_f16(v[6] * inv, v[7] * inv));
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
           }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + (lane >> 3), c = lane & 7;
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
+            if (rr < rows_ok) *reinterpret_cast<uint4*>(obase + rr * orow_stride + half * 128 + c * 16) = w;
+          }
+          __syncwarp();
         }
         if (row_ok) {
           float sum_true = 0.f;
