@@ -46,8 +46,7 @@ constexpr int kStages = 4;  // int8 ring
 constexpr int kThreads = 608;
 constexpr int kPvWarp = 14;     // issues the PV MMAs (warp 1 the score MMAs)
 constexpr int kSm2Warp0 = 15;   // warps 15-18: the second softmax warp group
-constexpr int kSoftmaxThreads = 256;
-constexpr int kBarSoftmax = 2;                       // named barrier of the softmax warps
+constexpr int kBarSoftmax = 2;  // named barriers 2 and 3: the two softmax warp groups (128 threads each)
 // TMEM columns.  An MMA of M = 128 costs the tensor pipe about the same for any
 // N <= 64, so the hi and lo parts of q' share one MMA of N = 32.
 constexpr int kNS = 2 * kNP;     // N of the score MMA
@@ -315,6 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int GH = GP / 2;
     const bool upper = warp >= kSm2Warp0;
     const int h0 = upper ? GH : 0;
+    // The groups exchange maxima and sums only among their own four warps.  (At the
+    // sentinel, the PV thread sees pv_stop: thread 64 writes it before its warp arrives.)
+    const int bar_group = kBarSoftmax + (upper ? 1 : 0);
     const int quad = warp & 3;       // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;  // TMEM lane: token of S, channel of O
     const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
@@ -353,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int g = 0; g < GH; ++g) sm.lsum[quad][h0 + g] = lv[g];
         }
-        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        named_bar_sync(bar_group, 128);
         float lt[GH], a[GH];
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.ws.part_ml[(int64_t)prev_item * G + r] = make_float2(mv, lw);
           }
         }
-        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        named_bar_sync(bar_group, 128);
       }
       return true;
     };
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const I8Meta meta = sm.tmeta[j % kMetaRing];
       if (meta.item < 0) {  // no more tiles: wake the PV warp, which stops
         if (tid == 64) sm.pv_stop = j;
-        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        named_bar_sync(bar_group, 128);
         if (lane == 0) mbar_arrive(&sm.p_full[sb]);
         break;
       }
@@ -440,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int g = 0; g < GH; ++g) sm.red[sb][h0 + g][quad] = mx[g];
       }
-      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+      named_bar_sync(bar_group, 128);
       float alpha[GH], pr[GH];
 #pragma unroll
       for (int g = 0; g < GH; ++g) {
