@@ -33,8 +33,7 @@ constexpr int kTmemCols = 128;
 constexpr int kThreadsTC = 352;
 constexpr int kPvWarpTC = 6;     // issues the PV MMAs (warp 1 the score MMAs)
 constexpr int kSm2Warp0 = 7;     // warps 7-10: the second softmax warp group
-constexpr int kSoftmaxThreadsTC = 256;
-constexpr int kBarCompute = 2;   // named barrier of the 256 softmax/correction threads
+constexpr int kBarCompute = 2;   // named barriers 2 and 3: the two softmax warp groups (128 threads each)
 
 template <int D>
 struct TcCfg {
@@ -274,6 +273,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     constexpr int GH = GP / 2;
     const bool upper = warp >= kSm2Warp0;
     const int h0 = upper ? GH : 0;
+    // The groups exchange maxima and sums only among their own four warps.  (At the
+    // sentinel, the PV thread sees pv_stop: thread 64 writes it before its warp arrives.)
+    const int bar_group = kBarCompute + (upper ? 1 : 0);
     const int quad = warp & 3;                 // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;            // TMEM lane: token of S, channel of O
     const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
           for (int g = 0; g < GH; ++g) sm.accx[r - 64][h0 + g] = acc[g];
         }
-        named_bar_sync(kBarCompute, kSoftmaxThreadsTC);
+        named_bar_sync(bar_group, 128);
         float lt[GH];
 #pragma unroll
         for (int g = 0; g < GH; ++g)
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             p.ws.part_ml[(int64_t)prev_item * G + r] = make_float2(mv, lw);
           }
         }
-        named_bar_sync(kBarCompute, kSoftmaxThreadsTC);
+        named_bar_sync(bar_group, 128);
       }
       return true;
     };
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const TileMeta meta = sm.meta[st];
       if (meta.item < 0) {  // no more tiles: wake the PV warp, which stops
         if (tid == 64) sm.pv_stop = j;
-        named_bar_sync(kBarCompute, kSoftmaxThreadsTC);
+        named_bar_sync(bar_group, 128);
         if (lane == 0) mbar_arrive(&sm.p_full[sb]);
         break;
       }
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
         for (int g = 0; g < GH; ++g) sm.red[sb][h0 + g][quad] = mx[g];
       }
-      named_bar_sync(kBarCompute, kSoftmaxThreadsTC);
+      named_bar_sync(bar_group, 128);
       float alpha[GH], pr[GH];
 #pragma unroll
       for (int g = 0; g < GH; ++g) {
