@@ -516,7 +516,7 @@ TRAFFIC_SOURCES = {
     "long_ctx_sink_decode": ("decode_tc.cu", "decode.cu", "decode_common.cuh", "fia_device.cuh", "fia_internal.h"),
     "int8_antiquant_decode": ("decode_i8tc.cu", "decode_i8.cuh", "decode.cu", "decode_common.cuh", "fia_device.cuh",
                               "fia_internal.h"),
-    "causal_prefill_tnd": ("prefill.cu", "fia_device.cuh", "fia_internal.h"),
+    "causal_prefill_tnd": ("prefill.cu", "decode_common.cuh", "fia_device.cuh", "fia_internal.h"),
 }
 
 
