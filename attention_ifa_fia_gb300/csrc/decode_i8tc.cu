@@ -46,6 +46,7 @@ constexpr int kStages = 4;  // int8 ring
 constexpr int kThreads = 608;
 constexpr int kPvWarp = 14;     // issues the PV MMAs (warp 1 the score MMAs)
 constexpr int kSm2Warp0 = 15;   // warps 15-18: the second softmax warp group
+constexpr float kLazyMax = 8.f;  // log2 units: P stays below 2^8 between exchanges of maxima
 constexpr int kBarSoftmax = 2;  // named barriers 2 and 3: the two softmax warp groups (128 threads each)
 // TMEM columns.  An MMA of M = 128 costs the tensor pipe about the same for any
 // N <= 64, so the hi and lo parts of q' share one MMA of N = 32.
@@ -73,6 +74,7 @@ struct I8Smem {
   alignas(16) float2 kn[2][kNP];
   alignas(16) float red[2][kNP][4];  // [S buffer][head][warp]: per-warp maxima
   float lsum[4][kNP];
+  float lmax[4][kNP];  // [warp][head]: per-warp true maxima at an item's end
   I8Meta meta[kStages];    // per int8 stage (producer)
   I8Meta tmeta[kMetaRing];  // per tile j at j % kMetaRing (K converters)
   uint64_t kv_full[kStages], kv_empty[kStages];
@@ -320,16 +322,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;       // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;  // TMEM lane: token of S, channel of O
     const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
-    float m_run[GH], l_part[GH], alpha_prev[GH], acc[GH], m_fin[GH], l_fin[GH];
+    // Lazy maximum: m_run is a reference for each head, the same in all threads of the group,
+    // and P = 2^(score - m_run).  A tile whose scores all stay below m_run + kLazyMax (one
+    // barrier-reduction tells) keeps the reference, with no exchange of maxima; otherwise
+    // the tile's exact maximum is exchanged and the reference raised.  m_thr is each
+    // thread's true maximum, combined at the item's end for the max and sum outputs.
+    float m_run[GH], l_part[GH], alpha_prev[GH], acc[GH], m_thr[GH];
 #pragma unroll
     for (int g = 0; g < GH; ++g) {
-      m_run[g] = -INFINITY; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_fin[g] = -INFINITY; l_fin[g] = 0.f;
+      m_run[g] = -INFINITY; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_thr[g] = -INFINITY;
     }
-    float vs_cur = 0.f, vo_cur = 0.f, vs_new = 0.f, vo_new = 0.f;  // value antiquant of channel r
+    float vs_cur = 0.f, vo_cur = 0.f;  // value antiquant of channel r for the current item
     int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
     bool prev_first = false, prev_last = false;
 
-    auto correct = [&](int jj, bool use_fin) -> bool {
+    // Folds in the PV result of tile jj; finishes the item if jj was its last tile.  Called
+    // after the softmax of tile jj + 1, or before it when that tile starts a new item (the
+    // item's state is then still in m_run, l_part and m_thr).
+    auto correct = [&](int jj) -> bool {
       const int ob = jj & 1;
       if (!mbar_wait(&sm.pv_done[ob], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
       tc_fence_after();
@@ -341,26 +351,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[g] = prev_first ? og : fmaf(acc[g], alpha_prev[g], og);
       }
       if (prev_last) {
-        float mm[GH], lv[GH];
+        float lv[GH], mt[GH];
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
-          mm[g] = use_fin ? m_fin[g] : m_run[g];
-          lv[g] = use_fin ? l_fin[g] : l_part[g];
+          lv[g] = l_part[g];
+          mt[g] = m_thr[g];
         }
 #pragma unroll
         for (int off = 16; off; off >>= 1)
 #pragma unroll
-          for (int g = 0; g < GH; ++g) lv[g] += __shfl_xor_sync(0xffffffffu, lv[g], off);
+          for (int g = 0; g < GH; ++g) {
+            lv[g] += __shfl_xor_sync(0xffffffffu, lv[g], off);
+            mt[g] = fmaxf(mt[g], __shfl_xor_sync(0xffffffffu, mt[g], off));
+          }
         if (lane == 0) {
 #pragma unroll
-          for (int g = 0; g < GH; ++g) sm.lsum[quad][h0 + g] = lv[g];
+          for (int g = 0; g < GH; ++g) {
+            sm.lsum[quad][h0 + g] = lv[g];
+            sm.lmax[quad][h0 + g] = mt[g];
+          }
         }
         named_bar_sync(bar_group, 128);
-        float lt[GH], a[GH];
+        // (mm, lt): the head's true maximum and the sum relative to it; a relative to it too
+        float mm[GH], lt[GH], a[GH];
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
-          lt[g] = sm.lsum[0][h0 + g] + sm.lsum[1][h0 + g] + sm.lsum[2][h0 + g] + sm.lsum[3][h0 + g];
-          a[g] = vs_cur * fmaf(-vo_cur, lt[g], acc[g]);  // sum_t p_t v^_t, unnormalised
+          mm[g] = fmax3(fmaxf(sm.lmax[0][h0 + g], sm.lmax[1][h0 + g]), sm.lmax[2][h0 + g], sm.lmax[3][h0 + g]);
+          const float sc = (mm[g] == -INFINITY) ? 0.f : exp2f(m_run[g] - mm[g]);
+          lt[g] = (sm.lsum[0][h0 + g] + sm.lsum[1][h0 + g] + sm.lsum[2][h0 + g] + sm.lsum[3][h0 + g]) * sc;
+          a[g] = vs_cur * fmaf(-vo_cur, lt[g], acc[g] * sc);  // sum_t 2^(s_t - mm) v^_t, unnormalised
         }
         if (prev_nch == 1) {
           const int64_t orow = ((int64_t)prev_b * p.Nq + prev_hkv * G) * kD + r;
@@ -409,51 +428,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&sm.p_full[sb]);
         break;
       }
+      if (meta.first) {  // finish the previous item first, then start this one
+        if (j > 0 && !correct(j - 1)) { ok = false; break; }
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+          m_run[g] = -INFINITY;
+          l_part[g] = 0.f;
+          m_thr[g] = -INFINITY;
+        }
+        const int64_t vi = ((int64_t)p.Nkv + meta.hkv) * kD + r;  // value scale/offset: index 1 of (2, Nkv, D)
+        vs_cur = p.aq_scale[vi];
+        vo_cur = p.aq_offset ? p.aq_offset[vi] : 0.f;
+      }
       tc_fence_after();
       float s[kNP];
       tmem_ld_scores(tq + kColS + sb * kNS, s);
-      if (meta.first) {
-#pragma unroll
-        for (int g = 0; g < GH; ++g) {
-          m_fin[g] = m_run[g];
-          l_fin[g] = l_part[g];
-          m_run[g] = -INFINITY;
-          l_part[g] = 0.f;
-        }
-        const int64_t vi = ((int64_t)p.Nkv + meta.hkv) * kD + r;  // value scale/offset: index 1 of (2, Nkv, D)
-        vs_new = p.aq_scale[vi];
-        vo_new = p.aq_offset ? p.aq_offset[vi] : 0.f;
-      }
       const bool valid = r < meta.n;
-      float x[GH], mx[GH];
+      float x[GH];
       const float2* kn = sm.kn[meta.qbuf] + h0;  // {kq, nq} of this group's heads (decode_i8.cuh)
+      bool above = false;  // a score of this thread exceeds its head's reference by kLazyMax
 #pragma unroll
       for (int g = 0; g < GH; ++g) {
         const float2 c = kn[g];
         const float sg = upper ? s[GH + g] : s[g];  // compile-time indices
         x[g] = valid ? fmaf(sg, c.x, c.y) : -INFINITY;
-        mx[g] = warp_max(x[g]);
+        above |= x[g] > m_run[g] + kLazyMax;  // (an unset reference, -inf, is exceeded by any score)
+        m_thr[g] = fmaxf(m_thr[g], x[g]);
       }
       if (meta.last) {  // the q' buffer may be refilled once the MMA thread is done with it too
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.q_empty[meta.qbuf]);
       }
-      if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < GH; ++g) sm.red[sb][h0 + g][quad] = mx[g];
-      }
-      named_bar_sync(bar_group, 128);
       float alpha[GH], pr[GH];
+      if (named_bar_or(bar_group, 128, above)) {  // exact maximum of the tile, reference raised
+        float mx[GH];
 #pragma unroll
-      for (int g = 0; g < GH; ++g) {
-        const float4 rq = *reinterpret_cast<const float4*>(sm.red[sb][h0 + g]);  // the four quadrants' maxima
-        const float tmax = fmax3(fmaxf(rq.x, rq.y), rq.z, rq.w);
-        const float m_new = fmaxf(m_run[g], tmax);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        alpha[g] = fast_exp2(m_run[g] - m_use);
-        pr[g] = fast_exp2(x[g] - m_use);
-        l_part[g] = fmaf(l_part[g], alpha[g], pr[g]);
-        m_run[g] = m_new;
+        for (int g = 0; g < GH; ++g) mx[g] = warp_max(x[g]);
+        if (lane == 0) {
+#pragma unroll
+          for (int g = 0; g < GH; ++g) sm.red[sb][h0 + g][quad] = mx[g];
+        }
+        named_bar_sync(bar_group, 128);
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+          const float4 rq = *reinterpret_cast<const float4*>(sm.red[sb][h0 + g]);  // the four quadrants' maxima
+          const float tmax = fmax3(fmaxf(rq.x, rq.y), rq.z, rq.w);
+          const float m_new = fmaxf(m_run[g], tmax);
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          alpha[g] = fast_exp2(m_run[g] - m_use);
+          pr[g] = fast_exp2(x[g] - m_use);
+          l_part[g] = fmaf(l_part[g], alpha[g], pr[g]);
+          m_run[g] = m_new;
+        }
+      } else {  // every score within 2^kLazyMax of the reference: keep it
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+          alpha[g] = 1.f;
+          pr[g] = fast_exp2(x[g] - m_run[g]);
+          l_part[g] += pr[g];
+        }
       }
       uint8_t* pbuf = sm.p[sb];  // free: PV(j - 2) was waited for in correct(j - 2)
 #pragma unroll
@@ -464,11 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();  // the tensor-memory reads of S(j) and O(j - 2) precede the arrival
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[sb]);
-      if (j > 0 && !correct(j - 1, meta.first)) { ok = false; break; }
-      if (meta.first) {
-        vs_cur = vs_new;
-        vo_cur = vo_new;
-      }
+      if (j > 0 && !meta.first && !correct(j - 1)) { ok = false; break; }
 #pragma unroll
       for (int g = 0; g < GH; ++g) alpha_prev[g] = alpha[g];
       prev_first = meta.first;
@@ -479,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prev_nch = meta.nch;
       ++j;
     }
-    if (ok && j > 0) correct(j - 1, false);
+    if (ok && j > 0) correct(j - 1);
   } else if (warp < 10) {
     // ------------------------------------------------------------------ K codes -> TMEM
     const int quad = warp & 3;
