@@ -156,13 +156,15 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     return;
   }
   // When B <= kPlanSmemB: sbase[B + 1] item offsets, then fpos[B] and tpos[B], the
-  // first execution-order slots of each batch's full chunks and of its last chunks.
+  // first execution-order slots of each batch's full chunks and of its last chunks, then
+  // slen[B], the clamped lengths (read from global memory once, not in every pass).
   extern __shared__ int sbase[];
   __shared__ int warp_tot[32];
   __shared__ int carry;
   __shared__ int bucket[kPlanMaxTiles + 1];  // items per size (tiles), then the next free slot
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool in_smem = p.B <= kPlanSmemB;
+  int* slen = sbase + 3 * p.B + 1;
   if (tid == 0) carry = 0;
   __syncthreads();
   const int C = p.chunk_tokens;
@@ -170,7 +172,9 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     const int b = b0 + tid;
     int nch = 0;
     if (b < p.B) {
-      nch = (clamp_len(p, b, true) + C - 1) / C;
+      const int L = clamp_len(p, b, true);
+      if (in_smem) slen[b] = L;
+      nch = (L + C - 1) / C;
       if (nch == 0) write_empty_batch(p, b);
     }
     const int cnt = nch * p.Nkv;
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     for (int b = tid; b < p.B; b += blockDim.x) {
       const int nch = (sbase[b + 1] - sbase[b]) / p.Nkv;
       if (nch == 0) continue;
-      const int last = clamp_len(p, b, false) - (nch - 1) * C;
+      const int last = slen[b] - (nch - 1) * C;
       atomicAdd(&bucket[kt], (nch - 1) * p.Nkv);
       atomicAdd(&bucket[min((last + kDecodeTileTC - 1) / kDecodeTileTC, kPlanMaxTiles)], p.Nkv);
     }
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     for (int b = tid; b < p.B; b += blockDim.x) {
       const int nch = (sbase[b + 1] - sbase[b]) / p.Nkv;
       if (nch == 0) continue;
-      const int last = clamp_len(p, b, false) - (nch - 1) * C;
+      const int last = slen[b] - (nch - 1) * C;
       fpos[b] = atomicAdd(&bucket[kt], (nch - 1) * p.Nkv);
       tpos[b] = atomicAdd(&bucket[min((last + kDecodeTileTC - 1) / kDecodeTileTC, kPlanMaxTiles)], p.Nkv);
     }
@@ -251,7 +255,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
       const int b = lo, r = i - sbase[b];
       const int nch = (sbase[b + 1] - sbase[b]) / p.Nkv;
       const int h = r / nch, j = r - h * nch;
-      p.ws.items[i] = make_int4(b, h, (nch << 16) | j, min(clamp_len(p, b, false), (j + 1) * C));
+      p.ws.items[i] = make_int4(b, h, (nch << 16) | j, min(slen[b], (j + 1) * C));
       p.ws.order[j < nch - 1 ? fpos[b] + h * (nch - 1) + j : tpos[b] + h] = i;
     }
   } else {
@@ -804,10 +808,10 @@ DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D,
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream) {
   trace_mark(kKernelDecodePlan, 0, stream);
-  const size_t plan_smem = p.B <= kPlanSmemB ? sizeof(int) * (size_t)(3 * p.B + 1) : 0;
+  const size_t plan_smem = p.B <= kPlanSmemB ? sizeof(int) * (size_t)(4 * p.B + 1) : 0;
   if (plan_smem > 48 * 1024) {
     cudaError_t e0 = cudaFuncSetAttribute(decode_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)(sizeof(int) * (3 * kPlanSmemB + 1)));
+                                          (int)(sizeof(int) * (4 * kPlanSmemB + 1)));
     if (e0 != cudaSuccess) return e0;
   }
   const bool i8tc = !tmQ && decode_uses_i8tc(p.kv_dtype, p.D);
