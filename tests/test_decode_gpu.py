@@ -216,3 +216,29 @@ def test_length_above_bound_is_clamped(F, cuda):
     from parity import assert_close, OUT_TOL
     assert_close("out row 0", to_f64(out)[0], ref[0], *OUT_TOL[case.dtype])
     F.fia_device_status()
+
+
+def test_int8_scores_rising_along_the_sequence(F, cuda):
+    """Key codes aligned with the query and growing tile after tile make each 128-token
+    tile's scores exceed the previous maximum by about 2^9: the int8 kernel must raise
+    its reference maximum and rescale in the middle of an item (random inputs almost
+    never reach that path).  Values stay random."""
+    case = W.make_decode_case(B=2, Nq=8, Nkv=2, D=128, block_size=128, kv_dtype=W.INT8, lengths=[700, 450],
+                              seed=11)
+    G = case.Nq // case.Nkv
+    q = W.bits_to_f32(case.q, case.dtype)                       # (B, Nq, D)
+    case.aq_scale[0] = 0.005                                     # key scale
+    case.aq_offset[0] = 0.0
+    for b in range(case.B):
+        for h in range(case.Nkv):
+            sign = np.where(q[b, h * G:(h + 1) * G].sum(axis=0) >= 0, 1, -1).astype(np.int32)
+            for t in range(int(case.lengths[b])):
+                c = min(127, 2 + 14 * (t // 128))              # about 9.5 log2 units more per tile
+                blk, row = case.block_table[b, t // case.block_size], t % case.block_size
+                case.k_cache[blk, h, row] = (sign * c).astype(np.int8)
+    dd = DeviceDecode(case)
+    ref = oracle_decode(case)
+    for ns in (0, 3):
+        out, mx, sm = run_decode(F, dd, num_splits=ns)
+        compare_decode(case, out, mx, sm, ref=ref)
+    assert _status(F) == 0

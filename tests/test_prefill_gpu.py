@@ -65,3 +65,23 @@ def test_prefill_rejects_bad_arguments(F, cuda):
         F.fia_prefill(dp.q, dp.k, dp.v, dp.cu_q, dp.cu_kv, max_seqlen_q=5, max_seqlen_kv=5, num_heads=4,
                       num_kv_heads=2, mask=2)
     assert ei.value.code == 161002
+
+
+def test_prefill_scores_rising_along_the_keys(F, cuda):
+    """Queries along one direction u and keys along u with a norm growing with the key
+    index: every 128-key tile raises a row's maximum by far more than 2^8, so the
+    kernel's lazy O rescale runs on every tile of every row (random inputs rarely)."""
+    case = W.make_prefill_case(Nq=4, Nkv=2, D=128, lengths=[600, 300], seed=21)
+    rng = np.random.default_rng(21)
+    u = np.where(rng.random(case.D) < 0.5, -1.0, 1.0).astype(np.float32)
+    q = np.broadcast_to(u, (case.T, case.Nq, case.D)) * 0.5
+    case.q[...] = W.to_bits(np.ascontiguousarray(q, dtype=np.float32), case.dtype)
+    k = np.empty((case.Tkv, case.Nkv, case.D), np.float32)
+    for b in range(case.B):
+        for j in range(int(case.lengths_kv[b])):
+            k[case.cu_kv[b] + j] = u * (1.0 + j / 32.0)
+    case.k[...] = W.to_bits(k, case.dtype)
+    dp = DevicePrefill(case)
+    out, mx, sm = run_prefill(F, dp)
+    compare_prefill(case, out, mx, sm)
+    assert F.fia_device_status() == 0
