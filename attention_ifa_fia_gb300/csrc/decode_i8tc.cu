@@ -128,13 +128,47 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
-// Scores of one S buffer: hi + lo partial sums of every (padded) head.
-__device__ __forceinline__ void tmem_ld_scores(uint32_t taddr, float (&v)[kNP]) {
-  float a[32];
-  tmem_ld32(taddr, a);
-#pragma unroll
-  for (int i = 0; i < kNP; ++i) v[i] = a[i] + a[kNP + i];
+// N consecutive 32-bit TMEM columns of this thread's lane (32x32b shape, N = 1, 2 or 4), no wait.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld_n<1>(uint32_t taddr, float (&v)[1]) {
+  uint32_t a;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(a) : "r"(taddr) : "memory");
+  v[0] = __uint_as_float(a);
 }
+template <>
+__device__ __forceinline__ void tmem_ld_n<2>(uint32_t taddr, float (&v)[2]) {
+  uint32_t a, b;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(taddr) : "memory");
+  v[0] = __uint_as_float(a);
+  v[1] = __uint_as_float(b);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_n<4>(uint32_t taddr, float (&v)[4]) {
+  uint32_t a, b, c, d;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(taddr)
+               : "memory");
+  v[0] = __uint_as_float(a);
+  v[1] = __uint_as_float(b);
+  v[2] = __uint_as_float(c);
+  v[3] = __uint_as_float(d);
+}
+
+// Scores of GH heads h0 .. h0 + GH - 1 from one S buffer (hi partial sums in columns 0-15,
+// lo in 16-31): only the columns of the calling warp group's heads are read.
+template <int GH>
+__device__ __forceinline__ void tmem_ld_scores_part(uint32_t taddr, int h0, float (&v)[GH]) {
+  float hi[GH], lo[GH];
+  tmem_ld_n<GH>(taddr + h0, hi);
+  tmem_ld_n<GH>(taddr + kNP + h0, lo);
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < GH; ++i) v[i] = hi[i] + lo[i];
+}
+
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -441,8 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         vo_cur = p.aq_offset ? p.aq_offset[vi] : 0.f;
       }
       tc_fence_after();
-      float s[kNP];
-      tmem_ld_scores(tq + kColS + sb * kNS, s);
+      float s[GH];  // scores of this group's heads
+      tmem_ld_scores_part<GH>(tq + kColS + sb * kNS, h0, s);
       const bool valid = r < meta.n;
       float x[GH];
       const float2* kn = sm.kn[meta.qbuf] + h0;  // {kq, nq} of this group's heads (decode_i8.cuh)
@@ -450,8 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int g = 0; g < GH; ++g) {
         const float2 c = kn[g];
-        const float sg = upper ? s[GH + g] : s[g];  // compile-time indices
-        x[g] = valid ? fmaf(sg, c.x, c.y) : -INFINITY;
+        x[g] = valid ? fmaf(s[g], c.x, c.y) : -INFINITY;
         above |= x[g] > m_run[g] + kLazyMax;  // (an unset reference, -inf, is exceeded by any score)
         m_thr[g] = fmaxf(m_thr[g], x[g]);
       }
