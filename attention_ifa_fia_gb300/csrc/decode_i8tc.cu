@@ -128,35 +128,6 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
-// N consecutive 32-bit TMEM columns of this thread's lane (32x32b shape, N = 1, 2 or 4), no wait.
-template <int N>
-__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float (&v)[N]);
-template <>
-__device__ __forceinline__ void tmem_ld_n<1>(uint32_t taddr, float (&v)[1]) {
-  uint32_t a;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(a) : "r"(taddr) : "memory");
-  v[0] = __uint_as_float(a);
-}
-template <>
-__device__ __forceinline__ void tmem_ld_n<2>(uint32_t taddr, float (&v)[2]) {
-  uint32_t a, b;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(taddr) : "memory");
-  v[0] = __uint_as_float(a);
-  v[1] = __uint_as_float(b);
-}
-template <>
-__device__ __forceinline__ void tmem_ld_n<4>(uint32_t taddr, float (&v)[4]) {
-  uint32_t a, b, c, d;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-               : "r"(taddr)
-               : "memory");
-  v[0] = __uint_as_float(a);
-  v[1] = __uint_as_float(b);
-  v[2] = __uint_as_float(c);
-  v[3] = __uint_as_float(d);
-}
-
 // Scores of GH heads h0 .. h0 + GH - 1 from one S buffer (hi partial sums in columns 0-15,
 // lo in 16-31): only the columns of the calling warp group's heads are read.
 template <int GH>

@@ -254,6 +254,46 @@ __device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
       : "memory");
 }
 
+// N consecutive 32-bit TMEM columns of this thread's lane (32x32b shape, N = 1, 2, 4 or 8); the
+// caller waits (tcgen05.wait::ld) before using them.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld_n<1>(uint32_t taddr, float (&v)[1]) {
+  uint32_t a;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(a) : "r"(taddr) : "memory");
+  v[0] = __uint_as_float(a);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_n<2>(uint32_t taddr, float (&v)[2]) {
+  uint32_t a, b;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(taddr) : "memory");
+  v[0] = __uint_as_float(a);
+  v[1] = __uint_as_float(b);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_n<4>(uint32_t taddr, float (&v)[4]) {
+  uint32_t a, b, c, d;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(taddr)
+               : "memory");
+  v[0] = __uint_as_float(a);
+  v[1] = __uint_as_float(b);
+  v[2] = __uint_as_float(c);
+  v[3] = __uint_as_float(d);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_n<8>(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 16 consecutive 32-bit TMEM columns of this thread's lane (32x32b shape).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
