@@ -348,13 +348,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ob = jj & 1;
       if (!mbar_wait(&sm.pv_done[ob], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
       tc_fence_after();
-      float o[kNP];
-      tmem_ld16(tq + kColO + ob * kNP, o);  // read before this warp's next p_full arrival
+      float o[GH];  // this group's heads only; read before this warp's next p_full arrival
+      tmem_ld_n<GH>(tq + kColO + ob * kNP + h0, o);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-      for (int g = 0; g < GH; ++g) {
-        const float og = upper ? o[GH + g] : o[g];  // compile-time indices
-        acc[g] = prev_first ? og : fmaf(acc[g], alpha_prev[g], og);
-      }
+      for (int g = 0; g < GH; ++g) acc[g] = prev_first ? o[g] : fmaf(acc[g], alpha_prev[g], o[g]);
       if (prev_last) {
         float lv[GH], mt[GH];
 #pragma unroll
