@@ -34,6 +34,11 @@ class FiaError(RuntimeError):
         self.code = code
 
 
+class DecodeOptions(ctypes.Structure):
+    """fia_decode_options of include/fia.h."""
+    _fields_ = [("kv_layout", ctypes.c_int), ("antiquant_mode", ctypes.c_int), ("softmax_lse", ctypes.c_void_p)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with attention_ifa_fia_gb300.build.build() "
@@ -49,6 +54,8 @@ def _load() -> ctypes.CDLL:
                         i32, P, sz, P], i32),
         "fia_decode_noalloc": ([P, i32, P, P, i32, P, i64, P, i32, i32, i32, i32, i32, i32, i64, dbl, P, P, P, P,
                                 P, P, i32, P], i32),
+        "fia_decode_ex": ([P, i32, P, P, i32, P, i64, P, i32, i32, i32, i32, i32, i32, i64, dbl, P, P, P, P, P, P,
+                           i32, P, sz, P, ctypes.POINTER(DecodeOptions)], i32),
         "fia_prefill_workspace_size": ([i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
         "fia_prefill": ([P, P, P, i32, P, P, i32, i64, i64, i32, i32, i32, i32, i32, dbl, i32, P, P, P, P, P, sz,
                          P], i32),
@@ -122,6 +129,10 @@ def fia_device_status(stream=None) -> int:
 
 
 # ----------------------------------------------------------------------------- decode
+KV_BNNBSD, KV_BNBSH = 0, 1            # k/v cache (num_blocks, Nkv, bs, D) or (num_blocks, bs, Nkv * D)
+AQ_PER_CHANNEL, AQ_PER_TENSOR = 0, 1  # antiquant scale/offset (2, Nkv, D) or (2,)
+
+
 def fia_decode_workspace_size(B: int, Nq: int, Nkv: int, D: int, max_kv_len: int, block_size: int,
                               num_splits: int = 0) -> int:
     n = ctypes.c_size_t(0)
@@ -135,13 +146,17 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
                scale: Optional[float] = None, antiquant_scale=None, antiquant_offset=None, sink=None,
                out: Optional[torch.Tensor] = None, softmax_max: Optional[torch.Tensor] = None,
                softmax_sum: Optional[torch.Tensor] = None, num_splits: int = 0,
-               workspace: Optional[torch.Tensor] = None, stream=None
-               ) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
+               workspace: Optional[torch.Tensor] = None, stream=None, kv_layout: int = KV_BNNBSD,
+               antiquant_mode: int = AQ_PER_CHANNEL, softmax_lse: Optional[torch.Tensor] = None,
+               _force_ex: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
     """Paged decode attention.  q: (B, Nq, D) (any layout of that memory); k/v_cache:
-    (num_blocks, Nkv, block_size, D); block_table int32 (B, width); actual_seq_lengths
-    int64 (B,) on the device.  Returns (out, softmax_max, softmax_sum)."""
+    (num_blocks, Nkv, block_size, D), or with kv_layout=KV_BNBSH (num_blocks, block_size,
+    Nkv * D); block_table int32 (B, width); actual_seq_lengths int64 (B,) on the device.
+    antiquant_mode=AQ_PER_TENSOR takes scale/offset of shape (2,); softmax_lse (B, Nq)
+    receives max + ln(sum).  Returns (out, softmax_max, softmax_sum)."""
     B, D = int(q.shape[0]), int(q.shape[-1])
-    num_blocks, block_size = int(k_cache.shape[0]), int(k_cache.shape[2])
+    num_blocks = int(k_cache.shape[0])
+    block_size = int(k_cache.shape[1] if kv_layout == KV_BNBSH else k_cache.shape[2])
     nkv = num_kv_heads if num_kv_heads else num_heads
     if scale is None:
         scale = D ** -0.5
@@ -150,14 +165,27 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     if workspace is None:
         nbytes = fia_decode_workspace_size(B, num_heads, nkv, D, max_kv_len, block_size, num_splits)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    rc = _lib.fia_decode(_ptr(q), dtype_code(q), _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache),
-                         _ptr(block_table), int(block_table.shape[1]), _ptr(actual_seq_lengths), int(max_kv_len),
-                         B, num_heads, nkv, D, block_size, num_blocks, float(scale), _ptr(antiquant_scale),
-                         _ptr(antiquant_offset), _ptr(sink), _ptr(out), _ptr(softmax_max), _ptr(softmax_sum),
-                         int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                         _stream(stream))
-    _check(rc, "fia_decode")
+    args = (_ptr(q), dtype_code(q), _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache), _ptr(block_table),
+            int(block_table.shape[1]), _ptr(actual_seq_lengths), int(max_kv_len), B, num_heads, nkv, D, block_size,
+            num_blocks, float(scale), _ptr(antiquant_scale), _ptr(antiquant_offset), _ptr(sink), _ptr(out),
+            _ptr(softmax_max), _ptr(softmax_sum), int(num_splits), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    if kv_layout == KV_BNNBSD and antiquant_mode == AQ_PER_CHANNEL and softmax_lse is None and not _force_ex:
+        _check(_lib.fia_decode(*args), "fia_decode")
+    else:
+        opts = DecodeOptions(int(kv_layout), int(antiquant_mode), _ptr(softmax_lse))
+        _check(_lib.fia_decode_ex(*args, ctypes.byref(opts)), "fia_decode_ex")
     return out, softmax_max, softmax_sum
+
+
+def fia_decode_ex(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                  actual_seq_lengths: torch.Tensor, *, kv_layout: int = KV_BNNBSD, antiquant_mode: int = AQ_PER_CHANNEL,
+                  softmax_lse: Optional[torch.Tensor] = None, **kw):
+    """fia_decode_ex: fia_decode with the decode options (KV layout, antiquant mode,
+    log-sum-exp output); other arguments as for fia_decode.  Always calls the C
+    fia_decode_ex entry point."""
+    return fia_decode(q, k_cache, v_cache, block_table, actual_seq_lengths, kv_layout=kv_layout,
+                      antiquant_mode=antiquant_mode, softmax_lse=softmax_lse, _force_ex=True, **kw)
 
 
 def fia_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,

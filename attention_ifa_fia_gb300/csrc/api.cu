@@ -258,12 +258,16 @@ int fia_decode_workspace_size(int B, int Nq, int Nkv, int D, int max_kv_len, int
   return ok();
 }
 
-int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache, fia_dtype kv_dtype,
-               const int32_t* block_table, int64_t bt_stride, const int64_t* actual_seq_lengths, int max_kv_len,
-               int B, int Nq, int Nkv, int D, int block_size, int64_t num_blocks, double scale,
-               const float* antiquant_scale, const float* antiquant_offset, const float* sink, void* out,
-               float* softmax_max, float* softmax_sum, int num_splits, void* workspace, size_t workspace_bytes,
-               fia_stream_t stream) {
+static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache,
+                       fia_dtype kv_dtype, const int32_t* block_table, int64_t bt_stride,
+                       const int64_t* actual_seq_lengths, int max_kv_len, int B, int Nq, int Nkv, int D,
+                       int block_size, int64_t num_blocks, double scale, const float* antiquant_scale,
+                       const float* antiquant_offset, const float* sink, void* out, float* softmax_max,
+                       float* softmax_sum, int num_splits, void* workspace, size_t workspace_bytes,
+                       fia_stream_t stream, const fia_decode_options* opt) {
+  const int kv_layout = opt ? opt->kv_layout : FIA_KV_BNNBSD;
+  const int aq_mode = opt ? opt->antiquant_mode : FIA_AQ_PER_CHANNEL;
+  float* lse = opt ? opt->softmax_lse : nullptr;
   // -- 161001: required pointers
   if (!q || !k_cache || !v_cache || !block_table || !actual_seq_lengths || !out)
     return fail(FIA_ERR_PARAM_NULLPTR, "q, k_cache, v_cache, block_table, actual_seq_lengths and out are required");
@@ -282,6 +286,12 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
     return fail(FIA_ERR_PARAM_INVALID, "int8 KV supports GQA groups up to 8 in this build (got %d)", Nq / Nkv);
   if (kv_dtype == FIA_I8 && sink)
     return fail(FIA_ERR_PARAM_INVALID, "the learnable sink is supported only without KV quantisation");
+  if (kv_layout != FIA_KV_BNNBSD && kv_layout != FIA_KV_BNBSH)
+    return fail(FIA_ERR_PARAM_INVALID, "unknown KV layout %d", kv_layout);
+  if (aq_mode != FIA_AQ_PER_CHANNEL && aq_mode != FIA_AQ_PER_TENSOR)
+    return fail(FIA_ERR_PARAM_INVALID, "unknown antiquant mode %d", aq_mode);
+  if (aq_mode == FIA_AQ_PER_TENSOR && kv_dtype != FIA_I8)
+    return fail(FIA_ERR_PARAM_INVALID, "per-tensor antiquant needs int8 KV");
   if (bt_stride < 1 || (int64_t)max_kv_len > bt_stride * block_size)
     return fail(FIA_ERR_PARAM_INVALID, "block table too narrow: max_kv_len %d > bt_stride %lld * block_size %d",
                 max_kv_len, (long long)bt_stride, block_size);
@@ -328,8 +338,21 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
   p.scale_log2 = (float)(scale * 1.4426950408889634);
   p.q_dtype = q_dtype;
   p.kv_dtype = kv_dtype;
+  p.kv_layout = kv_layout;
   p.ws = fia::decode_workspace_carve(workspace, B, Nkv, G, D, plan.max_items);
   p.status = d->status;
+  if (aq_mode == FIA_AQ_PER_TENSOR) {  // the kernels read the per-channel form
+    float* sc = p.ws.aux;
+    float* of = antiquant_offset ? p.ws.aux + 2 * Nkv * D : nullptr;
+    cudaError_t e0 = fia::launch_aq_expand(antiquant_scale, antiquant_offset, Nkv, D, sc, of, stream);
+    if (e0 != cudaSuccess) return fail(FIA_ERR_RUNTIME, "antiquant expansion: %s", cudaGetErrorString(e0));
+    p.aq_scale = sc;
+    p.aq_offset = of;
+  }
+  if (lse) {  // max and sum are needed for the log-sum-exp; scratch if not requested
+    if (!p.softmax_max) p.softmax_max = p.ws.aux + 4 * Nkv * D;
+    if (!p.softmax_sum) p.softmax_sum = p.ws.aux + 4 * Nkv * D + (size_t)B * Nq;
+  }
 
   // 16-bit KV runs on the tensor-core kernel (128-token tiles), int8 KV with D = 128 on the
   // int8 tensor-core kernel (128-token tiles), other int8 shapes on the CUDA-core one.
@@ -338,16 +361,46 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
   const int elem = kv_dtype == FIA_I8 ? 1 : 2;
   const uint32_t box_cols = (uint32_t)std::min(D * elem, 128) / elem;
   const int box_rows = gcd(block_size, tile128 ? fia::kDecodeTileTC : fia::kDecodeTile);
-  const uint64_t rows = (uint64_t)num_blocks * Nkv * block_size;
+  // layout 0: a row of D channels per (block, kv head, token); layout 1: a row of Nkv * D
+  // channels per (block, token), the kernels adding the head's column offset
+  const uint64_t cols = kv_layout == FIA_KV_BNBSH ? (uint64_t)Nkv * D : (uint64_t)D;
+  const uint64_t rows = kv_layout == FIA_KV_BNBSH ? (uint64_t)num_blocks * block_size
+                                                  : (uint64_t)num_blocks * Nkv * block_size;
   CUtensorMap tmK, tmV, tmQ;
-  if (int rc = make_tmap(&tmK, k_cache, kv_dtype, D, rows, box_cols, box_rows)) return rc;
-  if (int rc = make_tmap(&tmV, v_cache, kv_dtype, D, rows, box_cols, box_rows)) return rc;
+  if (int rc = make_tmap(&tmK, k_cache, kv_dtype, cols, rows, box_cols, box_rows)) return rc;
+  if (int rc = make_tmap(&tmV, v_cache, kv_dtype, cols, rows, box_cols, box_rows)) return rc;
   if (tc) {
     if (int rc = make_tmap(&tmQ, q, q_dtype, D, (uint64_t)B * Nq, 64, 16)) return rc;
   }
   cudaError_t e = fia::launch_decode(p, tmK, tmV, tc ? &tmQ : nullptr, box_rows, d->num_sms, stream);
   if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "decode launch: %s", cudaGetErrorString(e));
+  if (lse) {
+    e = fia::launch_lse(p.softmax_max, p.softmax_sum, lse, (int64_t)B * Nq, stream);
+    if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "log-sum-exp launch: %s", cudaGetErrorString(e));
+  }
   return ok();
+}
+
+int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache, fia_dtype kv_dtype,
+               const int32_t* block_table, int64_t bt_stride, const int64_t* actual_seq_lengths, int max_kv_len,
+               int B, int Nq, int Nkv, int D, int block_size, int64_t num_blocks, double scale,
+               const float* antiquant_scale, const float* antiquant_offset, const float* sink, void* out,
+               float* softmax_max, float* softmax_sum, int num_splits, void* workspace, size_t workspace_bytes,
+               fia_stream_t stream) {
+  return decode_impl(q, q_dtype, k_cache, v_cache, kv_dtype, block_table, bt_stride, actual_seq_lengths, max_kv_len,
+                     B, Nq, Nkv, D, block_size, num_blocks, scale, antiquant_scale, antiquant_offset, sink, out,
+                     softmax_max, softmax_sum, num_splits, workspace, workspace_bytes, stream, nullptr);
+}
+
+int fia_decode_ex(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache, fia_dtype kv_dtype,
+                  const int32_t* block_table, int64_t bt_stride, const int64_t* actual_seq_lengths, int max_kv_len,
+                  int B, int Nq, int Nkv, int D, int block_size, int64_t num_blocks, double scale,
+                  const float* antiquant_scale, const float* antiquant_offset, const float* sink, void* out,
+                  float* softmax_max, float* softmax_sum, int num_splits, void* workspace, size_t workspace_bytes,
+                  fia_stream_t stream, const fia_decode_options* options) {
+  return decode_impl(q, q_dtype, k_cache, v_cache, kv_dtype, block_table, bt_stride, actual_seq_lengths, max_kv_len,
+                     B, Nq, Nkv, D, block_size, num_blocks, scale, antiquant_scale, antiquant_offset, sink, out,
+                     softmax_max, softmax_sum, num_splits, workspace, workspace_bytes, stream, options);
 }
 
 int ring_attention_update(const void* prev_out, const float* prev_max, const float* prev_sum, const void* cur_out,

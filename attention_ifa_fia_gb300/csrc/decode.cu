@@ -94,10 +94,6 @@ struct Smem {
 };
 
 // Pool row of token t of (b, hkv): block_table entry, then the row inside the block.
-__device__ __forceinline__ int64_t pool_row(int32_t blk, int t, int bs, int Nkv, int hkv) {
-  return ((int64_t)blk * Nkv + hkv) * bs + (t % bs);
-}
-
 // Load one 16- or 8-byte piece of a swizzled tile row.
 template <int PB>
 __device__ __forceinline__ void load_piece(uint32_t addr, uint32_t (&w)[4]) {
@@ -341,11 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (valid) {
-          const int64_t row = pool_row(blk, tok0 + lane * box_rows, bs, p.Nkv, hkv);
+          const KvCoord kc = kv_coord(p, blk, tok0 + lane * box_rows, hkv);
           for (int bx = 0; bx < C::kNumBoxes; ++bx) {
             const uint32_t off = bx * (kTT * C::kBoxBytes) + lane * box_rows * C::kBoxBytes;
-            tma_load_2d(sm.kv[stage][0] + off, &tmK, bx * (C::kBoxBytes / C::kElem), (int32_t)row, &sm.full[stage]);
-            tma_load_2d(sm.kv[stage][1] + off, &tmV, bx * (C::kBoxBytes / C::kElem), (int32_t)row, &sm.full[stage]);
+            const int32_t x = kc.x0 + bx * (C::kBoxBytes / C::kElem);
+            tma_load_2d(sm.kv[stage][0] + off, &tmK, x, kc.row, &sm.full[stage]);
+            tma_load_2d(sm.kv[stage][1] + off, &tmV, x, kc.row, &sm.full[stage]);
           }
         }
         if (first && lane == 0) {
@@ -729,10 +726,10 @@ __global__ void __launch_bounds__(128) debug_gather_kernel(const __grid_constant
       for (int r = 0; r < npieces; ++r) {
         const int32_t blk = bt_row[(tok0 + r * box_rows) / p.block_size];
         if (!(blk >= 0 && blk < p.num_blocks)) continue;
-        const int64_t row = pool_row(blk, tok0 + r * box_rows, p.block_size, p.Nkv, hkv);
+        const KvCoord kc = kv_coord(p, blk, tok0 + r * box_rows, hkv);
         for (int bx = 0; bx < C::kNumBoxes; ++bx)
           tma_load_2d(tile + bx * (kTT * C::kBoxBytes) + r * box_rows * C::kBoxBytes, &tmK,
-                      bx * (C::kBoxBytes / C::kElem), (int32_t)row, &bar);
+                      kc.x0 + bx * (C::kBoxBytes / C::kElem), kc.row, &bar);
       }
     }
     __syncthreads();
@@ -781,6 +778,7 @@ size_t decode_workspace_bytes(int B, int Nkv, int G, int D, int max_items) {
   s += up(sizeof(float) * (size_t)max_items * G * D);  // part_o
   s += up(sizeof(float2) * (size_t)max_items * G);     // part_ml
   if (D == 128) s += up((size_t)kI8QBlockBytes * B * Nkv);  // qprep
+  s += up(sizeof(float) * ((size_t)4 * Nkv * D + (size_t)2 * (B > 0 ? B : 1) * Nkv * G));  // aux
   return s;
 }
 
@@ -802,7 +800,42 @@ DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D,
   w.part_ml = reinterpret_cast<float2*>(c);
   c += up(sizeof(float2) * (size_t)max_items * G);
   w.qprep = (D == 128) ? c : nullptr;
+  if (D == 128) c += up((size_t)kI8QBlockBytes * B * Nkv);
+  w.aux = reinterpret_cast<float*>(c);
   return w;
+}
+
+// Per-tensor antiquant (scale and offset of shape (2): keys, values) written out as the
+// per-channel (2, Nkv, D) arrays the kernels read: the same dequantisation, (x - o) s.
+__global__ void aq_expand_kernel(const float* scale2, const float* offset2, int n_per, float* dst_scale,
+                                 float* dst_offset) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= 2 * n_per) return;
+  const int sel = i / n_per;  // 0 keys, 1 values
+  dst_scale[i] = scale2[sel];
+  if (dst_offset) dst_offset[i] = offset2 ? offset2[sel] : 0.f;
+}
+
+// softmaxLse = ln(sum_t e^{z_t}) = max + ln(sum), the max and sum of the same row
+// (natural-exp units); -inf for a row with an empty sum.
+__global__ void lse_kernel(const float* mx, const float* sm, float* lse, int64_t n) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float m = mx[i], s = sm[i];
+  lse[i] = (s > 0.f && m != -INFINITY) ? m + logf(s) : -INFINITY;
+}
+
+cudaError_t launch_aq_expand(const float* scale2, const float* offset2, int Nkv, int D, float* dst_scale,
+                             float* dst_offset, cudaStream_t stream) {
+  const int n = 2 * Nkv * D;
+  aq_expand_kernel<<<(n + 255) / 256, 256, 0, stream>>>(scale2, offset2, Nkv * D, dst_scale, dst_offset);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse(const float* mx, const float* sm, float* lse, int64_t n, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  lse_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(mx, sm, lse, n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,

@@ -7,6 +7,26 @@
 
 namespace fia {
 
+// Tensor-map coordinates of the tile row of token t of kv head hkv in pool block blk: the
+// row, and the column of the head's first channel.  Layout 0, (num_blocks, Nkv,
+// block_size, D): a row of D channels per (block, head, token).  Layout 1, (num_blocks,
+// block_size, Nkv * D): a row of Nkv * D channels per (block, token), the head selecting a
+// column range (aclnnIncreFlashAttentionV3, "Constraints / page attention").
+struct KvCoord {
+  int32_t x0, row;
+};
+__device__ __forceinline__ KvCoord kv_coord(const DecodeParams& p, int32_t blk, int t, int hkv) {
+  KvCoord c;
+  if (p.kv_layout == 1) {
+    c.x0 = hkv * p.D;
+    c.row = (int32_t)((int64_t)blk * p.block_size + t % p.block_size);
+  } else {
+    c.x0 = 0;
+    c.row = (int32_t)(((int64_t)blk * p.Nkv + hkv) * p.block_size + t % p.block_size);
+  }
+  return c;
+}
+
 // Work item {b, kv head, (chunk count of the segment) << 16 | chunk index, last token + 1};
 // the first token is chunk index * chunk_tokens.
 struct DecodeItem {

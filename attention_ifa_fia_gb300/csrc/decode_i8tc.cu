@@ -85,9 +85,6 @@ struct I8Smem {
 };
 static_assert(sizeof(I8Smem) + 1024 <= 232448, "shared memory of the int8 decode kernel");
 
-__device__ __forceinline__ int64_t i8_pool_row(int32_t blk, int t, int bs, int Nkv, int hkv) {
-  return ((int64_t)blk * Nkv + hkv) * bs + (t % bs);
-}
 
 // Offset of element (row g, token t) of the P^T operand: two 64-token slabs of
 // 16 rows x 128 bytes, 128-byte swizzle.
@@ -243,10 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (valid) {
-          const int64_t row = i8_pool_row(blk, tok0 + lane * box_rows, bs, p.Nkv, hkv);
+          const KvCoord kc = kv_coord(p, blk, tok0 + lane * box_rows, hkv);
           const uint32_t off = (uint32_t)lane * box_rows * 128u;
-          tma_load_2d(sm.kv[st][0] + off, &tmK, 0, (int32_t)row, &sm.kv_full[st]);
-          tma_load_2d(sm.kv[st][1] + off, &tmV, 0, (int32_t)row, &sm.kv_full[st]);
+          tma_load_2d(sm.kv[st][0] + off, &tmK, kc.x0, kc.row, &sm.kv_full[st]);
+          tma_load_2d(sm.kv[st][1] + off, &tmV, kc.x0, kc.row, &sm.kv_full[st]);
         }
         if (tok0 == t_begin) queue.prefetch(p, lane);
       }

@@ -73,10 +73,6 @@ struct TcSmem {
   uint32_t tmem_base;
 };
 
-__device__ __forceinline__ int64_t tc_pool_row(int32_t blk, int t, int bs, int Nkv, int hkv) {
-  return ((int64_t)blk * Nkv + hkv) * bs + (t % bs);
-}
-
 // Offset of element (row g, token t) of the P^T operand: two 64-token slabs of
 // 16 rows x 128 bytes, 128-byte swizzle (8-row atoms of 1 KB).
 __device__ __forceinline__ uint32_t p_offset(int g, int t) {
@@ -176,11 +172,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         __syncwarp();
         if (valid) {
-          const int64_t row = tc_pool_row(blk, tok0 + lane * box_rows, bs, p.Nkv, hkv);
+          const KvCoord kc = kv_coord(p, blk, tok0 + lane * box_rows, hkv);
           for (int bx = 0; bx < C::kNumBoxes; ++bx) {
             const uint32_t off = bx * (kT * 128) + lane * box_rows * 128;
-            tma_load_2d(sm.kv[st][0] + off, &tmK, bx * 64, (int32_t)row, &sm.kv_full[st]);
-            tma_load_2d(sm.kv[st][1] + off, &tmV, bx * 64, (int32_t)row, &sm.kv_full[st]);
+            tma_load_2d(sm.kv[st][0] + off, &tmK, kc.x0 + bx * 64, kc.row, &sm.kv_full[st]);
+            tma_load_2d(sm.kv[st][1] + off, &tmV, kc.x0 + bx * 64, kc.row, &sm.kv_full[st]);
           }
         }
         if (tok0 == t_begin) queue.prefetch(p, lane);

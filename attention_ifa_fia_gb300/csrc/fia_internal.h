@@ -50,6 +50,8 @@ struct DecodeWorkspace {
   float* part_o;    // (max_items, G, D) normalised partial outputs
   float2* part_ml;  // (max_items, G) {max (log2 units), sum}
   uint8_t* qprep;   // (B * Nkv) q' blocks of the int8 tensor-core path (D = 128), else null
+  float* aux;       // (4 Nkv D + 2 B Nq): per-tensor antiquant expanded to (2, Nkv, D) scale and
+                    // offset, then max and sum scratch for the log-sum-exp output
 };
 
 struct DecodeParams {
@@ -70,11 +72,17 @@ struct DecodeParams {
   int max_items;
   float scale_log2;   // scale * log2(e)
   int q_dtype, kv_dtype;
+  int kv_layout;      // 0: (num_blocks, Nkv, block_size, D); 1: (num_blocks, block_size, Nkv * D)
   DecodeWorkspace ws;
   unsigned int* status;  // device status word
 };
 
 size_t decode_workspace_bytes(int B, int Nkv, int G, int D, int max_items);
+// (2) per-tensor antiquant scale and offset (offset may be null) -> (2, Nkv, D) in dst_scale,
+// dst_offset; log-sum-exp of n rows from their max and sum.
+cudaError_t launch_aq_expand(const float* scale2, const float* offset2, int Nkv, int D, float* dst_scale,
+                             float* dst_offset, cudaStream_t stream);
+cudaError_t launch_lse(const float* mx, const float* sm, float* lse, int64_t n, cudaStream_t stream);
 DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D, int max_items);
 
 // Launches plan + attention + merge on `stream`.  tmK / tmV describe the K and V

@@ -131,6 +131,39 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
                float* softmax_max, float* softmax_sum, int num_splits, void* workspace, size_t workspace_bytes,
                fia_stream_t stream);
 
+/* fia_decode with decode variants of the same kernels (aclnnIncreFlashAttentionV3,
+ * "Constraints / page attention": the (blocknum, blocksize, H) KV layout beside
+ * (blocknum, KV_N, blocksize, D); the per-tensor antiquant of shape (2);
+ * FusedInferAttentionScore's softmaxLse output).  Arguments as for fia_decode, plus:
+ *
+ * options->kv_layout        FIA_KV_BNNBSD: k_cache/v_cache are (num_blocks, Nkv, block_size, D)
+ *                           as for fia_decode.  FIA_KV_BNBSH: (num_blocks, block_size, Nkv * D)
+ *                           row-major (H = Nkv * D): token t of a block is one row holding
+ *                           every kv head's channels, head h at columns [h * D, (h + 1) * D).
+ * options->antiquant_mode   FIA_AQ_PER_CHANNEL: antiquant_scale/offset are (2, Nkv, D) as for
+ *                           fia_decode.  FIA_AQ_PER_TENSOR: they are (2): one scale (offset)
+ *                           for all keys, one for all values.  Int8 KV only.
+ * options->softmax_lse      device fp32 (B, Nq) or NULL: ln(sum_t e^{z_t}) (+ e^{s_h} with a
+ *                           sink) = softmax_max + ln(softmax_sum); -inf for a row with
+ *                           neither a visible key nor a sink.
+ * options == NULL behaves as fia_decode.  The workspace is fia_decode_workspace_size()
+ * bytes, as for fia_decode.  Errors: an unknown layout or mode, or the per-tensor mode
+ * without int8 KV, is FIA_ERR_PARAM_INVALID. */
+typedef enum { FIA_KV_BNNBSD = 0, FIA_KV_BNBSH = 1 } fia_kv_layout;
+typedef enum { FIA_AQ_PER_CHANNEL = 0, FIA_AQ_PER_TENSOR = 1 } fia_antiquant_mode;
+typedef struct {
+  int kv_layout;       /* fia_kv_layout */
+  int antiquant_mode;  /* fia_antiquant_mode */
+  float* softmax_lse;  /* device fp32 (B, Nq) or NULL */
+} fia_decode_options;
+
+int fia_decode_ex(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache, fia_dtype kv_dtype,
+                  const int32_t* block_table, int64_t bt_stride, const int64_t* actual_seq_lengths, int max_kv_len,
+                  int B, int Nq, int Nkv, int D, int block_size, int64_t num_blocks, double scale,
+                  const float* antiquant_scale, const float* antiquant_offset, const float* sink, void* out,
+                  float* softmax_max, float* softmax_sum, int num_splits, void* workspace, size_t workspace_bytes,
+                  fia_stream_t stream, const fia_decode_options* options);
+
 /* Allocation-free variant of fia_decode.  The operator pages have no counterpart:
  * it exists for callers that cannot allocate device memory for the workspace --
  * plugins whose host application owns all device memory through its own allocator,
