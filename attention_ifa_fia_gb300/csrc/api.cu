@@ -339,6 +339,9 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   p.q_dtype = q_dtype;
   p.kv_dtype = kv_dtype;
   p.kv_layout = kv_layout;
+  p.kv_row_blk = kv_layout == FIA_KV_BNBSH ? block_size : Nkv * block_size;
+  p.kv_row_h = kv_layout == FIA_KV_BNBSH ? 0 : block_size;
+  p.kv_x_h = kv_layout == FIA_KV_BNBSH ? D : 0;
   p.ws = fia::decode_workspace_carve(workspace, B, Nkv, G, D, plan.max_items);
   p.status = d->status;
   if (aq_mode == FIA_AQ_PER_TENSOR) {  // the kernels read the per-channel form
@@ -453,6 +456,8 @@ int fia_debug_gather(const void* k_cache, fia_dtype kv_dtype, const int32_t* blo
   p.Nkv = nkv;
   p.D = D;
   p.block_size = block_size;
+  p.kv_row_blk = nkv * block_size;  // (num_blocks, Nkv, block_size, D)
+  p.kv_row_h = block_size;
   p.num_blocks = num_blocks;
   p.max_kv_len = max_kv_len;
   p.kv_dtype = kv_dtype;

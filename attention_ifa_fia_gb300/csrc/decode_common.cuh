@@ -16,14 +16,9 @@ struct KvCoord {
   int32_t x0, row;
 };
 __device__ __forceinline__ KvCoord kv_coord(const DecodeParams& p, int32_t blk, int t, int hkv) {
-  KvCoord c;
-  if (p.kv_layout == 1) {
-    c.x0 = hkv * p.D;
-    c.row = (int32_t)((int64_t)blk * p.block_size + t % p.block_size);
-  } else {
-    c.x0 = 0;
-    c.row = (int32_t)(((int64_t)blk * p.Nkv + hkv) * p.block_size + t % p.block_size);
-  }
+  KvCoord c;  // (rows < 2^31 is checked by the host)
+  c.x0 = hkv * p.kv_x_h;
+  c.row = blk * p.kv_row_blk + hkv * p.kv_row_h + t % p.block_size;
   return c;
 }
 

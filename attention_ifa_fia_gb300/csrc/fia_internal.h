@@ -73,6 +73,9 @@ struct DecodeParams {
   float scale_log2;   // scale * log2(e)
   int q_dtype, kv_dtype;
   int kv_layout;      // 0: (num_blocks, Nkv, block_size, D); 1: (num_blocks, block_size, Nkv * D)
+  // tensor-map coordinates of a pool token: row = blk * kv_row_blk + hkv * kv_row_h + t % block_size,
+  // column of the head's first channel = hkv * kv_x_h (set from kv_layout by the host)
+  int kv_row_blk, kv_row_h, kv_x_h;
   DecodeWorkspace ws;
   unsigned int* status;  // device status word
 };
