@@ -16,6 +16,10 @@ Functions and the passages they follow:
 * ``rau``      -- aclnnRingAttentionUpdate "计算公式", read with each partial
   weighted by its own softmax sum (the printed formula drops those factors).
 * ``dequant_i8`` -- per-channel antiquant (x - offset) * scale in fp32.
+* ``decode(mask=...)`` -- aclnnIncreFlashAttentionV3 parameter table, attenMask
+  (B, 1, 1, S): nonzero bytes remove keys from the softmax.
+* ``post_quant`` -- aclnnIncreFlashAttentionV3 parameter table and constraints,
+  quantScale2 / quantOffset2 (int8 output, per tensor or per channel).
 """
 from __future__ import annotations
 
@@ -58,7 +62,7 @@ def _bind(path: str):
     P = ctypes.c_void_p
     i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
     lib.oracle_decode.argtypes = [P, i32, P, P, i32, P, i64, P, i32, i32, i32, i32, i32, i64,
-                                  dbl, P, P, P, P, i64, i32, P, P, P]
+                                  dbl, P, P, P, P, i64, P, i64, i32, P, P, P]
     lib.oracle_decode.restype = i32
     lib.oracle_prefill.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, dbl, i32, P,
                                    P, i64, i32, P, P, P]
@@ -71,6 +75,8 @@ def _bind(path: str):
     lib.oracle_dequant_i8_array.restype = None
     lib.oracle_gather_rows.argtypes = [P, i32, P, i64, i32, i32, i64, i32, i32, i32, P]
     lib.oracle_gather_rows.restype = i32
+    lib.oracle_post_quant.argtypes = [P, i64, i64, P, P, i32, P, P]
+    lib.oracle_post_quant.restype = None
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = i32
     return lib
@@ -123,13 +129,14 @@ class Oracle:
 
     def decode(self, q, k_cache, v_cache, seq_lens, *, Nq, Nkv, D, scale, q_dtype=None, kv_dtype=None,
                block_table=None, block_size=0, kv_rows=0, aq_scale=None, aq_offset=None, sink=None,
-               rows=None, nthreads=0):
+               mask=None, rows=None, nthreads=0):
         """Decode attention (query S = 1).
 
         q: (B, Nq, D) array (uint16 bits with q_dtype=F16/BF16, or float32/float64).
         k_cache, v_cache: paged (num_blocks, Nkv, block_size, D) when block_table is
         given, else contiguous (B, Nkv, kv_rows, D).  int8 caches need aq_scale
-        (2, Nkv, D) float32 and optionally aq_offset.  Returns (out, max, sum) as
+        (2, Nkv, D) float32 and optionally aq_offset.  mask: (B, S) bytes (bool,
+        int8 or uint8; S >= every length), nonzero = key masked out.  Returns (out, max, sum) as
         float64 arrays of shape (R, D), (R,), (R,) where R = len(rows) or B * Nq.
         """
         q = np.ascontiguousarray(q)
@@ -143,6 +150,9 @@ class Oracle:
         R = B * Nq if rows_a is None else int(rows_a.shape[0])
         f32 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float32)
         aq_scale, aq_offset, sink = f32(aq_scale), f32(aq_offset), f32(sink)
+        if mask is not None:
+            mask = np.ascontiguousarray(np.asarray(mask).reshape(B, -1).view(np.uint8) != 0, dtype=np.uint8)
+        mask_stride = 0 if mask is None else int(mask.shape[1])
         out = np.zeros((R, D), np.float64)
         mx = np.zeros(R, np.float64)
         sm = np.zeros(R, np.float64)
@@ -150,7 +160,7 @@ class Oracle:
             _ptr(q), _dtype_code(q, q_dtype), _ptr(k_cache), _ptr(v_cache),
             _dtype_code(k_cache, kv_dtype), _ptr(bt), bt_stride, _ptr(seq_lens),
             B, Nq, Nkv, D, block_size, kv_rows, float(scale), _ptr(aq_scale),
-            _ptr(aq_offset), _ptr(sink), _ptr(rows_a), 0 if rows_a is None else R,
+            _ptr(aq_offset), _ptr(sink), _ptr(mask), mask_stride, _ptr(rows_a), 0 if rows_a is None else R,
             nthreads, _ptr(out), _ptr(mx), _ptr(sm))
         if rc != 0:
             raise ValueError("oracle_decode rejected its arguments")
@@ -179,6 +189,23 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_prefill rejected its arguments")
         return out, mx, sm
+
+    def post_quant(self, x, scale2, offset2=None):
+        """int8 output quantisation of x (rows, N, D) or (rows, C): returns (y, code), y the
+        unrounded fp64 value and code the int8 result.  scale2/offset2: one value (per
+        tensor) or N * D values (per channel)."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        rows = int(x.shape[0])
+        C = int(x.size // max(rows, 1))
+        s2 = np.ascontiguousarray(np.asarray(scale2, dtype=np.float32).reshape(-1))
+        o2 = None if offset2 is None else np.ascontiguousarray(np.asarray(offset2, dtype=np.float32).reshape(-1))
+        per_channel = int(s2.size != 1)
+        if per_channel and s2.size != C or (o2 is not None and o2.size != s2.size):
+            raise ValueError("post_quant: scale2/offset2 must hold 1 or N * D values")
+        y = np.zeros(x.shape, np.float64)
+        code = np.zeros(x.shape, np.int8)
+        self._lib.oracle_post_quant(_ptr(x), rows, C, _ptr(s2), _ptr(o2), per_channel, _ptr(y), _ptr(code))
+        return y, code
 
     def rau(self, prev_out, prev_max, prev_sum, cur_out, cur_max, cur_sum):
         """RingAttentionUpdate on fp64 arrays: out (rows, N, D), max/sum (rows, N)."""
@@ -219,3 +246,7 @@ def prefill(*args, **kw):
 
 def rau(*args, **kw):
     return default().rau(*args, **kw)
+
+
+def post_quant(*args, **kw):
+    return default().post_quant(*args, **kw)

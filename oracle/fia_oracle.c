@@ -37,6 +37,13 @@
  *       With a sink: out = 0, max = sink, sum = 1.
  *   R7  Causal mask (rightDownCausal): key j is visible to query i of a sequence
  *       iff j <= i + (Lkv - Lq).
+ *   R8  attenMask (decode): a byte per (batch, key); nonzero = the key is masked
+ *       out (the causal forms the pages describe keep the diagonal at 0), and a
+ *       masked key is left out of the softmax entirely.
+ *   R9  Post-quant output: y = out * quantScale2 + quantOffset2 in the
+ *       attention's own precision, rounded to nearest with ties to even and
+ *       saturated to int8; per-channel parameters index the output's N * D
+ *       channels (N = query heads, the heads of attentionOut).
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -shared -fPIC.
  * -ffp-contract=off is required: R2 forbids contracting the dequant into an FMA.
@@ -180,6 +187,10 @@ static void attend_row(const double *q, const double *K, const double *V, int64_
  * for OR_I8 the codes are dequantised with aq_scale / aq_offset of shape
  * (2, Nkv, D), index 0 for K and 1 for V ([IFA] parameter table, per-channel);
  * aq_offset may be NULL (zero).  sink: fp32 (Nq) or NULL.
+ * mask: [IFA] attenMask of shape (B, 1, 1, S), one byte per (b, t) at
+ * mask[b * mask_stride + t], or NULL; a nonzero byte removes key t of batch b
+ * from the attention (1 = masked out, 0 = attended), so a batch whose keys are
+ * all masked is handled like one of length 0.
  * rows: the (b * Nq + h) rows to compute, or NULL for all B * Nq rows; results
  * are written compactly: out[i * D + d], smax[i], ssum[i] for the i-th row.
  * Returns 0, or -1 on an argument it cannot handle. */
@@ -189,7 +200,7 @@ int oracle_decode(const void *q, int q_dtype,
                   const int64_t *seq_lens,
                   int B, int Nq, int Nkv, int D, int block_size, int64_t kv_rows,
                   double scale, const float *aq_scale, const float *aq_offset,
-                  const float *sink,
+                  const float *sink, const uint8_t *mask, int64_t mask_stride,
                   const int64_t *rows, int64_t n_rows, int nthreads,
                   double *out, double *smax, double *ssum)
 {
@@ -231,8 +242,12 @@ int oracle_decode(const void *q, int q_dtype,
             const int64_t L = seq_lens[b];
             for (int d = 0; d < D; ++d)
                 qd[d] = load_elem(q, q_dtype, r * D + d);
-            /* gather the visible keys/values of (b, hk) into dense rows */
+            /* gather the visible keys/values of (b, hk) into dense rows; n of them
+             * survive the mask */
+            int64_t n = 0;
             for (int64_t t = 0; t < L; ++t) {
+                if (mask && mask[(int64_t)b * mask_stride + t] != 0)
+                    continue;
                 int64_t src;                                    /* element offset of row t */
                 if (block_table) {
                     const int64_t blk = block_table[(int64_t)b * bt_stride + t / block_size];
@@ -244,18 +259,19 @@ int oracle_decode(const void *q, int q_dtype,
                     if (kv_dtype == OR_I8) {
                         const float ko = aq_offset ? aq_offset[(0 * Nkv + hk) * D + d] : 0.0f;
                         const float vo = aq_offset ? aq_offset[(1 * Nkv + hk) * D + d] : 0.0f;
-                        Kd[t * D + d] = (double)oracle_dequant_i8(((const int8_t *)k_cache)[src + d],
+                        Kd[n * D + d] = (double)oracle_dequant_i8(((const int8_t *)k_cache)[src + d],
                                                                   ko, aq_scale[(0 * Nkv + hk) * D + d]);
-                        Vd[t * D + d] = (double)oracle_dequant_i8(((const int8_t *)v_cache)[src + d],
+                        Vd[n * D + d] = (double)oracle_dequant_i8(((const int8_t *)v_cache)[src + d],
                                                                   vo, aq_scale[(1 * Nkv + hk) * D + d]);
                     } else {
-                        Kd[t * D + d] = load_elem(k_cache, kv_dtype, src + d);
-                        Vd[t * D + d] = load_elem(v_cache, kv_dtype, src + d);
+                        Kd[n * D + d] = load_elem(k_cache, kv_dtype, src + d);
+                        Vd[n * D + d] = load_elem(v_cache, kv_dtype, src + d);
                     }
                 }
+                ++n;
             }
             double sk;
-            attend_row(qd, Kd, Vd, L, D, scale, sink ? (sk = sink[h], &sk) : NULL, sc,
+            attend_row(qd, Kd, Vd, n, D, scale, sink ? (sk = sink[h], &sk) : NULL, sc,
                        out + i * D, smax + i, ssum + i);
         }
         free(Kd);
@@ -382,6 +398,34 @@ int oracle_rau(const double *prev_out, const double *prev_max, const double *pre
         sum_out[r] = l;
     }
     return 0;
+}
+
+/* ---- int8 post-quant output ----------------------------------------------
+ *
+ * [IFA] quantScale2 / quantOffset2 (output quantisation, symmetric without an
+ * offset, asymmetric with one): y = out * scale2[c] + offset2[c] for channel
+ * c = h * D + d of the (N, D) output row, rounded to the nearest integer with
+ * ties to even and saturated to [-128, 127].  per_channel = 0 reads scale2[0]
+ * (and offset2[0]) for every channel.  x: rows x C in fp64 (C = N * D);
+ * offset2 may be NULL.  y (the unrounded value, may be NULL) and code get
+ * rows x C entries. */
+void oracle_post_quant(const double *x, int64_t rows, int64_t C, const float *scale2,
+                       const float *offset2, int per_channel, double *y, int8_t *code)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < C; ++c) {
+            const int64_t i = r * C + c;
+            const int64_t pc = per_channel ? c : 0;
+            const double v = x[i] * (double)scale2[pc] + (offset2 ? (double)offset2[pc] : 0.0);
+            double q = nearbyint(v);                    /* default rounding: ties to even */
+            if (q > 127.0)
+                q = 127.0;
+            if (q < -128.0)
+                q = -128.0;
+            if (y)
+                y[i] = v;
+            code[i] = (int8_t)q;
+        }
 }
 
 int oracle_max_threads(void)

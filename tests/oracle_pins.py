@@ -247,6 +247,79 @@ def pin_empty_kv(O):
     assert np.all(out[2:] == 0) and np.array_equal(mx[2:], [0.5, -2.0]) and np.all(sm[2:] == 1)
 
 
+def pin_decode_mask_matches_sdpa(O):
+    """attenMask (B, 1, 1, S): a nonzero byte removes the key; equals torch SDPA with the
+    boolean mask (True = attend) over the paged keys gathered by the block table."""
+    rng = np.random.default_rng(23)
+    B, Nq, Nkv, D, bs = 3, 4, 2, 16, 8
+    lengths = [13, 30, 7]
+    case = W.make_decode_case(B=B, Nq=Nq, Nkv=Nkv, D=D, block_size=bs, lengths=lengths, seed=23, scale=0.41)
+    S = 32                                              # mask row longer than every length
+    mask = rng.random((B, S)) < 0.35
+    mask[2, :7] = True                                  # batch 2: every key masked
+    out, mx, sm = O.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=Nq, Nkv=Nkv, D=D,
+                           scale=case.scale, q_dtype=OR.BF16, kv_dtype=OR.BF16,
+                           block_table=case.block_table, block_size=bs, mask=mask.astype(np.uint8))
+    q32 = W.bits_to_f32(case.q, W.BF16).astype(np.float64)
+    kc = W.bits_to_f32(case.k_cache, W.BF16).astype(np.float64)
+    vc = W.bits_to_f32(case.v_cache, W.BF16).astype(np.float64)
+    G = Nq // Nkv
+    for b in range(2):
+        L = lengths[b]
+        blocks = case.block_table[b, :(L + bs - 1) // bs]
+        K = np.repeat(np.concatenate([kc[p] for p in blocks], axis=1)[:, :L], G, axis=0)
+        V = np.repeat(np.concatenate([vc[p] for p in blocks], axis=1)[:, :L], G, axis=0)
+        keep = np.broadcast_to(~mask[b, :L], (Nq, 1, L))
+        ref = sdpa_rows(q32[b][:, None, :], K, V, case.scale, bool_mask=keep)[:, 0, :]
+        sc = case.scale * np.einsum("hd,hld->hl", q32[b], K)[:, ~mask[b, :L]]
+        m_ref, s_ref = lse_max_sum(sc)
+        rows = slice(b * Nq, (b + 1) * Nq)
+        np.testing.assert_allclose(out[rows], ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(mx[rows], m_ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(sm[rows], s_ref, rtol=1e-12, atol=1e-12)
+    rows = slice(2 * Nq, 3 * Nq)                        # fully masked: the empty-row values
+    assert np.all(out[rows] == 0) and np.all(mx[rows] == -np.inf) and np.all(sm[rows] == 0)
+    # an all-zero mask is no mask, bit for bit; bool, int8 and uint8 masks agree
+    ref = O.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=Nq, Nkv=Nkv, D=D, scale=case.scale,
+                   q_dtype=OR.BF16, kv_dtype=OR.BF16, block_table=case.block_table, block_size=bs)
+    zero = O.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=Nq, Nkv=Nkv, D=D, scale=case.scale,
+                    q_dtype=OR.BF16, kv_dtype=OR.BF16, block_table=case.block_table, block_size=bs,
+                    mask=np.zeros((B, S), np.int8))
+    assert all(np.array_equal(x, y) for x, y in zip(ref, zero))
+    asb = O.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=Nq, Nkv=Nkv, D=D, scale=case.scale,
+                   q_dtype=OR.BF16, kv_dtype=OR.BF16, block_table=case.block_table, block_size=bs, mask=mask)
+    assert all(np.array_equal(x, y) for x, y in zip(asb, (out, mx, sm)))
+
+
+# ------------------------------------------------------------------ post-quant output
+def pin_post_quant_closed_forms(O):
+    """Ties go to the even integer, values past the int8 range saturate, the offset is added."""
+    x = np.array([[0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 0.49, 126.5, 127.5, 128.0, 1e6,
+                   -127.5, -128.5, -129.0, -1e6, 3.2]])
+    y, code = O.post_quant(x, [1.0])
+    assert np.array_equal(y, x)
+    assert code.tolist() == [[0, 2, 2, 0, -2, -2, 0, 126, 127, 127, 127, -128, -128, -128, -128, 3]]
+    _, code = O.post_quant(np.array([[1.0, -1.0, 0.25]]), [2.0], [0.5])   # 2.5, -1.5, 1.0
+    assert code.tolist() == [[2, -2, 1]]
+
+
+def pin_post_quant_matches_numpy(O):
+    """Per-tensor and per-channel (channel h * D + d of an (N, D) row) against numpy's rint
+    (ties to even) and clip."""
+    rng = np.random.default_rng(29)
+    R, N, D = 5, 3, 8
+    x = rng.standard_normal((R, N, D)) * 40
+    s_c = rng.uniform(0.5, 3.0, N * D).astype(np.float32)
+    o_c = rng.uniform(-20, 20, N * D).astype(np.float32)
+    for s2, o2 in [(s_c[:1], None), (s_c[:1], o_c[:1]), (s_c, None), (s_c, o_c)]:
+        y, code = O.post_quant(x, s2, o2)
+        s_b = np.broadcast_to(s2.astype(np.float64), (N * D,)).reshape(N, D)
+        o_b = 0.0 if o2 is None else np.broadcast_to(o2.astype(np.float64), (N * D,)).reshape(N, D)
+        y_ref = x * s_b + o_b
+        np.testing.assert_allclose(y, y_ref, rtol=1e-15, atol=0)
+        assert np.array_equal(code, np.clip(np.rint(y_ref), -128, 127).astype(np.int8))
+
+
 # ------------------------------------------------------------------ int8 antiquant
 def pin_dequant_fp32_semantics(O):
     """(x - offset) * scale as two fp32 round-to-nearest operations, for all 256 codes."""

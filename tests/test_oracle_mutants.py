@@ -36,6 +36,18 @@ MUTANTS = [
      "const int64_t in_block = (t + 1) % block_size;"),
     ("dequant_array_offset_ignored", "out[i] = oracle_dequant_i8(x[i], offset[i], scale[i]);",
      "out[i] = oracle_dequant_i8(x[i], 0.0f, scale[i]);"),
+    ("mask_ignored", "if (mask && mask[(int64_t)b * mask_stride + t] != 0)",
+     "if (0 && mask && mask[(int64_t)b * mask_stride + t] != 0)"),
+    ("mask_polarity", "mask[(int64_t)b * mask_stride + t] != 0)", "mask[(int64_t)b * mask_stride + t] == 0)"),
+    ("mask_batch_row", "mask[(int64_t)b * mask_stride + t]", "mask[t]"),
+    ("post_quant_ties_away", "double q = nearbyint(v);", "double q = round(v);"),
+    ("post_quant_truncates", "double q = nearbyint(v);", "double q = trunc(v);"),
+    ("post_quant_no_upper_saturation", "if (q > 127.0)\n                q = 127.0;",
+     "if (q > 255.0)\n                q = 127.0;"),
+    ("post_quant_low_clamp", "q = -128.0;", "q = -127.0;"),
+    ("post_quant_channel_by_row", "const int64_t pc = per_channel ? c : 0;",
+     "const int64_t pc = per_channel ? r : 0;"),
+    ("post_quant_offset_sign", "x[i] * (double)scale2[pc] + (offset2", "x[i] * (double)scale2[pc] - (offset2"),
     ("prefill_kv_head_index", "const int64_t src = ((cu_kv[b] + j) * Nkv + hk) * D + d;",
      "const int64_t src = ((cu_kv[b] + j) * Nkv + (h % Nkv)) * D + d;"),
 ]
