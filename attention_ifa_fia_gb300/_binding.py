@@ -36,7 +36,10 @@ class FiaError(RuntimeError):
 
 class DecodeOptions(ctypes.Structure):
     """fia_decode_options of include/fia.h."""
-    _fields_ = [("kv_layout", ctypes.c_int), ("antiquant_mode", ctypes.c_int), ("softmax_lse", ctypes.c_void_p)]
+    _fields_ = [("kv_layout", ctypes.c_int), ("antiquant_mode", ctypes.c_int), ("softmax_lse", ctypes.c_void_p),
+                ("atten_mask", ctypes.c_void_p), ("atten_mask_stride", ctypes.c_int64),
+                ("quant_scale2", ctypes.c_void_p), ("quant_offset2", ctypes.c_void_p),
+                ("quant2_per_channel", ctypes.c_int)]
 
 
 def _load() -> ctypes.CDLL:
@@ -148,12 +151,16 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
                softmax_sum: Optional[torch.Tensor] = None, num_splits: int = 0,
                workspace: Optional[torch.Tensor] = None, stream=None, kv_layout: int = KV_BNNBSD,
                antiquant_mode: int = AQ_PER_CHANNEL, softmax_lse: Optional[torch.Tensor] = None,
+               atten_mask: Optional[torch.Tensor] = None, quant_scale2: Optional[torch.Tensor] = None,
+               quant_offset2: Optional[torch.Tensor] = None,
                _force_ex: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
     """Paged decode attention.  q: (B, Nq, D) (any layout of that memory); k/v_cache:
     (num_blocks, Nkv, block_size, D), or with kv_layout=KV_BNBSH (num_blocks, block_size,
     Nkv * D); block_table int32 (B, width); actual_seq_lengths int64 (B,) on the device.
     antiquant_mode=AQ_PER_TENSOR takes scale/offset of shape (2,); softmax_lse (B, Nq)
-    receives max + ln(sum).  Returns (out, softmax_max, softmax_sum)."""
+    receives max + ln(sum).  atten_mask: (B, S) / (B, 1, S) / (B, 1, 1, S) bool, int8 or
+    uint8, 1 = key masked out, S >= max_kv_len.  quant_scale2 (and quant_offset2): fp32 of
+    1 or Nq * D values; out is then int8.  Returns (out, softmax_max, softmax_sum)."""
     B, D = int(q.shape[0]), int(q.shape[-1])
     num_blocks = int(k_cache.shape[0])
     block_size = int(k_cache.shape[1] if kv_layout == KV_BNBSH else k_cache.shape[2])
@@ -161,7 +168,23 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     if scale is None:
         scale = D ** -0.5
     if out is None:
-        out = torch.empty((B, num_heads, D), dtype=q.dtype, device=q.device)
+        out = torch.empty((B, num_heads, D), dtype=torch.int8 if quant_scale2 is not None else q.dtype,
+                          device=q.device)
+    mask_stride = 0
+    if atten_mask is not None:
+        if atten_mask.dtype not in (torch.bool, torch.int8, torch.uint8) or not atten_mask.is_contiguous():
+            raise ValueError("atten_mask must be a contiguous bool, int8 or uint8 tensor")
+        mask_stride = int(atten_mask.shape[-1])
+        if atten_mask.numel() != B * mask_stride:
+            raise ValueError("atten_mask must have shape (B, S), (B, 1, S) or (B, 1, 1, S)")
+    q2_per_channel = 0
+    if quant_scale2 is not None:
+        n2 = quant_scale2.numel()
+        if n2 not in (1, num_heads * D) or quant_scale2.dtype != torch.float32:
+            raise ValueError("quant_scale2 must be fp32 with 1 or Nq * D values")
+        if quant_offset2 is not None and (quant_offset2.numel() != n2 or quant_offset2.dtype != torch.float32):
+            raise ValueError("quant_offset2 must match quant_scale2")
+        q2_per_channel = int(n2 != 1)
     if workspace is None:
         nbytes = fia_decode_workspace_size(B, num_heads, nkv, D, max_kv_len, block_size, num_splits)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
@@ -170,22 +193,27 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
             num_blocks, float(scale), _ptr(antiquant_scale), _ptr(antiquant_offset), _ptr(sink), _ptr(out),
             _ptr(softmax_max), _ptr(softmax_sum), int(num_splits), _ptr(workspace),
             workspace.numel() * workspace.element_size(), _stream(stream))
-    if kv_layout == KV_BNNBSD and antiquant_mode == AQ_PER_CHANNEL and softmax_lse is None and not _force_ex:
+    plain = (kv_layout == KV_BNNBSD and antiquant_mode == AQ_PER_CHANNEL and softmax_lse is None
+             and atten_mask is None and quant_scale2 is None and quant_offset2 is None)
+    if plain and not _force_ex:
         _check(_lib.fia_decode(*args), "fia_decode")
     else:
-        opts = DecodeOptions(int(kv_layout), int(antiquant_mode), _ptr(softmax_lse))
+        opts = DecodeOptions(int(kv_layout), int(antiquant_mode), _ptr(softmax_lse), _ptr(atten_mask), mask_stride,
+                             _ptr(quant_scale2), _ptr(quant_offset2), q2_per_channel)
         _check(_lib.fia_decode_ex(*args, ctypes.byref(opts)), "fia_decode_ex")
     return out, softmax_max, softmax_sum
 
 
 def fia_decode_ex(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
                   actual_seq_lengths: torch.Tensor, *, kv_layout: int = KV_BNNBSD, antiquant_mode: int = AQ_PER_CHANNEL,
-                  softmax_lse: Optional[torch.Tensor] = None, **kw):
+                  softmax_lse: Optional[torch.Tensor] = None, atten_mask: Optional[torch.Tensor] = None,
+                  quant_scale2: Optional[torch.Tensor] = None, quant_offset2: Optional[torch.Tensor] = None, **kw):
     """fia_decode_ex: fia_decode with the decode options (KV layout, antiquant mode,
-    log-sum-exp output); other arguments as for fia_decode.  Always calls the C
-    fia_decode_ex entry point."""
+    log-sum-exp output, attenMask, int8 post-quant output); other arguments as for
+    fia_decode.  Always calls the C fia_decode_ex entry point."""
     return fia_decode(q, k_cache, v_cache, block_table, actual_seq_lengths, kv_layout=kv_layout,
-                      antiquant_mode=antiquant_mode, softmax_lse=softmax_lse, _force_ex=True, **kw)
+                      antiquant_mode=antiquant_mode, softmax_lse=softmax_lse, atten_mask=atten_mask,
+                      quant_scale2=quant_scale2, quant_offset2=quant_offset2, _force_ex=True, **kw)
 
 
 def fia_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,

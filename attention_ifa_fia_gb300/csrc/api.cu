@@ -268,6 +268,11 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   const int kv_layout = opt ? opt->kv_layout : FIA_KV_BNNBSD;
   const int aq_mode = opt ? opt->antiquant_mode : FIA_AQ_PER_CHANNEL;
   float* lse = opt ? opt->softmax_lse : nullptr;
+  const uint8_t* mask = opt ? opt->atten_mask : nullptr;
+  const int64_t mask_stride = opt ? opt->atten_mask_stride : 0;
+  const float* qs2 = opt ? opt->quant_scale2 : nullptr;
+  const float* qo2 = opt ? opt->quant_offset2 : nullptr;
+  const int q2_per_channel = opt ? opt->quant2_per_channel : 0;
   // -- 161001: required pointers
   if (!q || !k_cache || !v_cache || !block_table || !actual_seq_lengths || !out)
     return fail(FIA_ERR_PARAM_NULLPTR, "q, k_cache, v_cache, block_table, actual_seq_lengths and out are required");
@@ -292,6 +297,12 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
     return fail(FIA_ERR_PARAM_INVALID, "unknown antiquant mode %d", aq_mode);
   if (aq_mode == FIA_AQ_PER_TENSOR && kv_dtype != FIA_I8)
     return fail(FIA_ERR_PARAM_INVALID, "per-tensor antiquant needs int8 KV");
+  if (mask && mask_stride < (int64_t)max_kv_len)
+    return fail(FIA_ERR_PARAM_INVALID, "atten_mask rows of %lld bytes are shorter than max_kv_len %d",
+                (long long)mask_stride, max_kv_len);
+  if (qo2 && !qs2) return fail(FIA_ERR_PARAM_INVALID, "quant_offset2 without quant_scale2");
+  if (q2_per_channel != 0 && q2_per_channel != 1)
+    return fail(FIA_ERR_PARAM_INVALID, "quant2_per_channel must be 0 or 1 (got %d)", q2_per_channel);
   if (bt_stride < 1 || (int64_t)max_kv_len > bt_stride * block_size)
     return fail(FIA_ERR_PARAM_INVALID, "block table too narrow: max_kv_len %d > bt_stride %lld * block_size %d",
                 max_kv_len, (long long)bt_stride, block_size);
@@ -342,6 +353,12 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   p.kv_row_blk = kv_layout == FIA_KV_BNBSH ? block_size : Nkv * block_size;
   p.kv_row_h = kv_layout == FIA_KV_BNBSH ? 0 : block_size;
   p.kv_x_h = kv_layout == FIA_KV_BNBSH ? D : 0;
+  p.atten_mask = mask;
+  p.mask_stride = mask ? mask_stride : 0;
+  p.pq_scale = qs2;
+  p.pq_offset = qo2;
+  p.pq_stride = q2_per_channel;
+  p.partials_only = qs2 != nullptr;
   p.ws = fia::decode_workspace_carve(workspace, B, Nkv, G, D, plan.max_items);
   p.status = d->status;
   if (aq_mode == FIA_AQ_PER_TENSOR) {  // the kernels read the per-channel form

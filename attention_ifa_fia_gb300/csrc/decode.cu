@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
       const int L = clamp_len(p, b, true);
       if (in_smem) slen[b] = L;
       nch = (L + C - 1) / C;
-      if (nch == 0) write_empty_batch(p, b);
+      if (nch == 0 && !p.partials_only) write_empty_batch(p, b);
     }
     const int cnt = nch * p.Nkv;
     int x = cnt;  // inclusive warp scan, then across warps
@@ -487,7 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t < kTT && writer) {
 #pragma unroll
         for (int i = 0; i < GP; ++i)
-          if (i < cnt) sm.s[gh + i][t] = (t < meta.n) ? v[i] * p.scale_log2 : -INFINITY;
+          if (i < cnt)
+            sm.s[gh + i][t] = (t < meta.n && !key_masked(p, meta.b, meta.tok0 + t)) ? v[i] * p.scale_log2 : -INFINITY;
       }
     }
     named_bar_sync(kBarConsumers, kDecodeConsumers);
@@ -565,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < C::EV; ++e) sm.red[warp][g * D + pv_c * C::EV + e] = acc[g][e];
       }
       named_bar_sync(kBarConsumers, kDecodeConsumers);
-      if (meta.nch == 1) {
+      if (meta.nch == 1 && !p.partials_only) {
         // the segment is this one item: write the final output directly
         for (int o = tid; o < G * D; o += kDecodeConsumers) {
           float s = 0.f;
@@ -601,11 +602,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------- merge
 // One CTA per (b, kv head) segment of two or more work items (segments of one item are
-// written by the attention kernel, empty batches by the plan).  Partials are folded in
+// written by the attention kernel, empty batches by the plan; with partials_only, for the
+// int8 output, every segment is finished here, an empty one as zero partials).
+// Partials are folded in
 // order by the RingAttentionUpdate rule, each weighted by its own sum, with the sink
 // added once (aclnnRingAttentionUpdate; aclnnFlashAttentionScoreV4 sink formula):
 //   M = max(sink, max_j m_j),  W = sum_j l_j 2^{m_j - M} + 2^{sink - M},
 //   out = sum_j o_j l_j 2^{m_j - M} / W,  softmax_max = M ln 2,  softmax_sum = W.
+// The int8 output (aclnnIncreFlashAttentionV3 quantScale2 / quantOffset2) is taken from the
+// fp32 out: code = saturate(round-to-nearest-even(out * scale2 + offset2)) to [-128, 127].
 // Launched dependent on the attention kernel: its launch overlaps that kernel's tail.
 constexpr int kMergeThreads = 256;
 
@@ -617,7 +622,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const int b = blockIdx.x / p.Nkv, hkv = blockIdx.x % p.Nkv;
   const int C = p.chunk_tokens;
   const int nch = (clamp_len(p, b, false) + C - 1) / C;
-  if (nch <= 1) return;
+  if (nch <= 1 && !p.partials_only) return;
   const int G = p.G, D = p.D, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int first = p.ws.seg_base[b] + hkv * nch;
   for (int i = tid; i < G * nch; i += kMergeThreads) {  // coalesced: partial-major in memory
@@ -676,10 +681,24 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
       acc.w = fmaf(w, v.w, acc.w);
     }
     const int64_t o = ((int64_t)b * p.Nq + hkv * G) * D + q4 * 4;
-    store_out<QT>(p.out, o, acc.x);
-    store_out<QT>(p.out, o + 1, acc.y);
-    store_out<QT>(p.out, o + 2, acc.z);
-    store_out<QT>(p.out, o + 3, acc.w);
+    if (p.pq_scale) {
+      const int c = hkv * G * D + q4 * 4;  // channel of acc.x within the (Nq, D) row
+      const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+      uint32_t w = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int pc = (c + i) * p.pq_stride;
+        const float y = fmaf(a[i], p.pq_scale[pc], p.pq_offset ? p.pq_offset[pc] : 0.f);
+        const int v = min(max(__float2int_rn(y), -128), 127);
+        w |= (uint32_t)(v & 0xff) << (8 * i);
+      }
+      *reinterpret_cast<uint32_t*>(static_cast<int8_t*>(p.out) + o) = w;  // o % 4 == 0 (D % 4 == 0)
+    } else {
+      store_out<QT>(p.out, o, acc.x);
+      store_out<QT>(p.out, o + 1, acc.y);
+      store_out<QT>(p.out, o + 2, acc.z);
+      store_out<QT>(p.out, o + 3, acc.w);
+    }
   }
 }
 
@@ -868,10 +887,11 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const C
                     : launch_attention_g<kI8, 128>(p, tmK, tmV, box_rows, grid, stream);
   }
   if (e != cudaSuccess) return e;
-  // merge of segments with two or more items; dependent launch on the attention kernel
+  // merge of segments with two or more items (of every segment with partials_only);
+  // dependent launch on the attention kernel
   const int max_chunks = (p.max_kv_len + p.chunk_tokens - 1) / p.chunk_tokens;
-  if (max_chunks <= 1) return cudaSuccess;
-  const size_t msmem = sizeof(float2) * (size_t)p.G * max_chunks;
+  if (max_chunks <= 1 && !p.partials_only) return cudaSuccess;
+  const size_t msmem = sizeof(float2) * (size_t)p.G * (max_chunks > 1 ? max_chunks : 1);
   auto merge = (p.q_dtype == kBF16) ? decode_merge_kernel<kBF16> : decode_merge_kernel<kF16>;
   if (msmem > 48 * 1024) {
     e = cudaFuncSetAttribute(merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);

@@ -76,6 +76,11 @@ struct ItemQueue {
 // acc = sum_t 2^{s_t - m} v_t (not normalised), l = sum_t 2^{s_t - m}, m in log2 units.
 // Returns the value to store for one output channel; *M_out / *W_out receive the
 // softmax max (log2 units) and sum for the head.
+// attenMask: a nonzero byte at (b, t) removes key t of batch b from the softmax.
+__device__ __forceinline__ bool key_masked(const DecodeParams& p, int b, int t) {
+  return p.atten_mask != nullptr && __ldg(p.atten_mask + (int64_t)b * p.mask_stride + t) != 0;
+}
+
 __device__ __forceinline__ float single_item_output(float acc, float m, float l, const float* sink, int h,
                                                     float* M_out, float* W_out) {
   const float sink2 = sink ? sink[h] * kLog2e : -INFINITY;

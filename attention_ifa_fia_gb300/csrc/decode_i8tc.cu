@@ -47,6 +47,10 @@ constexpr int kThreads = 608;
 constexpr int kPvWarp = 14;     // issues the PV MMAs (warp 1 the score MMAs)
 constexpr int kSm2Warp0 = 15;   // warps 15-18: the second softmax warp group
 constexpr float kLazyMax = 8.f;  // log2 units: P stays below 2^8 between exchanges of maxima
+// The reference of an item before any exchange: finite, so that a tile whose keys are all
+// masked (scores -inf) gives P = 2^(-inf - kNoRef) = 0 on the no-exchange path, and below
+// any real score by far more than kLazyMax, so that the first unmasked score exchanges.
+constexpr float kNoRef = -1e30f;
 constexpr int kBarSoftmax = 2;  // named barriers 2 and 3: the two softmax warp groups (128 threads each)
 // TMEM columns.  An MMA of M = 128 costs the tensor pipe about the same for any
 // N <= 64, so the hi and lo parts of q' share one MMA of N = 32.
@@ -62,6 +66,7 @@ constexpr int kPBytes = kNP * kT * 2;
 struct __align__(16) I8Meta {
   int b, hkv, n, item;
   int first, last, qbuf, nch;
+  int tok0, pad0, pad1, pad2;  // tok0: the tile's first token
 };
 
 constexpr int kMetaRing = 4;  // tile descriptors in flight between the K converters, MMA and softmax warps
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           I8Meta& m = sm.meta[st];
           m.b = b; m.hkv = hkv; m.n = n; m.item = item;
-          m.first = (tok0 == t_begin); m.last = (tok0 + kT >= t_end); m.qbuf = qb; m.nch = it.nch;
+          m.first = (tok0 == t_begin); m.last = (tok0 + kT >= t_end); m.qbuf = qb; m.nch = it.nch; m.tok0 = tok0;
           if (bytes) mbar_arrive_expect_tx(&sm.kv_full[st], bytes);
           else mbar_arrive(&sm.kv_full[st]);
         }
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run[GH], l_part[GH], alpha_prev[GH], acc[GH], m_thr[GH];
 #pragma unroll
     for (int g = 0; g < GH; ++g) {
-      m_run[g] = -INFINITY; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_thr[g] = -INFINITY;
+      m_run[g] = kNoRef; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_thr[g] = -INFINITY;
     }
     float vs_cur = 0.f, vo_cur = 0.f;  // value antiquant of channel r for the current item
     int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           lt[g] = (sm.lsum[0][h0 + g] + sm.lsum[1][h0 + g] + sm.lsum[2][h0 + g] + sm.lsum[3][h0 + g]) * sc;
           a[g] = vs_cur * fmaf(-vo_cur, lt[g], acc[g] * sc);  // sum_t 2^(s_t - mm) v^_t, unnormalised
         }
-        if (prev_nch == 1) {
+        if (prev_nch == 1 && !p.partials_only) {
           const int64_t orow = ((int64_t)prev_b * p.Nq + prev_hkv * G) * kD + r;
 #pragma unroll
           for (int g = 0; g < GH; ++g) {
@@ -432,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j > 0 && !correct(j - 1)) { ok = false; break; }
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
-          m_run[g] = -INFINITY;
+          m_run[g] = kNoRef;
           l_part[g] = 0.f;
           m_thr[g] = -INFINITY;
         }
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float s[GH];  // scores of this group's heads
       tmem_ld_scores_part<GH>(tq + kColS + sb * kNS, h0, s);
-      const bool valid = r < meta.n;
+      const bool valid = r < meta.n && !key_masked(p, meta.b, meta.tok0 + r);
       float x[GH];
       const float2* kn = sm.kn[meta.qbuf] + h0;  // {kq, nq} of this group's heads (decode_i8.cuh)
       bool above = false;  // a score of this thread exceeds its head's reference by kLazyMax
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int g = 0; g < GH; ++g) {
         const float2 c = kn[g];
         x[g] = valid ? fmaf(s[g], c.x, c.y) : -INFINITY;
-        above |= x[g] > m_run[g] + kLazyMax;  // (an unset reference, -inf, is exceeded by any score)
+        above |= x[g] > m_run[g] + kLazyMax;  // (the unset reference, kNoRef, is exceeded by any score)
         m_thr[g] = fmaxf(m_thr[g], x[g]);
       }
       if (meta.last) {  // the q' buffer may be refilled once the MMA thread is done with it too

@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
         for (int g = 0; g < GH; ++g)
           lt[g] = sm.lsum[0][h0 + g] + sm.lsum[1][h0 + g] + sm.lsum[2][h0 + g] + sm.lsum[3][h0 + g];
-        if (prev_nch == 1) {
+        if (prev_nch == 1 && !p.partials_only) {
           // the segment is this one item: write the final output directly
           if (!C::kStacked || r < 64) {
             const int64_t orow = ((int64_t)prev_b * p.Nq + prev_hkv * G) * D + r;
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           l_part[g] = 0.f;
         }
       }
-      const bool valid = r < meta.n;
+      const bool valid = r < meta.n && !key_masked(p, meta.b, meta.tok0 + r);
       // per-head maximum over the tile's tokens: a warp reduction per head, then across
       // the 4 lane quadrants through shared memory
       float x[GH], mx[GH];
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           *reinterpret_cast<uint16_t*>(pbuf + p_offset(h0 + g, r)) = h;
         }
       }
-      if (!valid && !upper) {
+      if (r >= meta.n && !upper) {  // rows past the keys (masked keys hold finite values)
         uint8_t* vrow = sm.kv[st][1];
 #pragma unroll
         for (int bx = 0; bx < C::kNumBoxes; ++bx) {

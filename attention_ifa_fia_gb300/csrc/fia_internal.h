@@ -76,6 +76,15 @@ struct DecodeParams {
   // tensor-map coordinates of a pool token: row = blk * kv_row_blk + hkv * kv_row_h + t % block_size,
   // column of the head's first channel = hkv * kv_x_h (set from kv_layout by the host)
   int kv_row_blk, kv_row_h, kv_x_h;
+  const uint8_t* atten_mask;  // (B, mask_stride) bytes, nonzero = key masked out; or null
+  int64_t mask_stride;
+  // int8 output: code = sat8(rint(out * pq_scale[c * pq_stride] + pq_offset[c * pq_stride])) for
+  // channel c = h * D + d; pq_scale null for a 16-bit output.  With it every segment, of one
+  // item or none, is finished by the merge kernel (partials_only).
+  const float* pq_scale;
+  const float* pq_offset;  // or null
+  int pq_stride;           // 0: one value for the tensor; 1: one per channel
+  int partials_only;
   DecodeWorkspace ws;
   unsigned int* status;  // device status word
 };

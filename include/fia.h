@@ -133,8 +133,9 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
 
 /* fia_decode with decode variants of the same kernels (aclnnIncreFlashAttentionV3,
  * "Constraints / page attention": the (blocknum, blocksize, H) KV layout beside
- * (blocknum, KV_N, blocksize, D); the per-tensor antiquant of shape (2);
- * FusedInferAttentionScore's softmaxLse output).  Arguments as for fia_decode, plus:
+ * (blocknum, KV_N, blocksize, D); the per-tensor antiquant of shape (2); the parameter
+ * table's attenMask and quantScale2 / quantOffset2; FusedInferAttentionScore's
+ * softmaxLse output).  Arguments as for fia_decode, plus:
  *
  * options->kv_layout        FIA_KV_BNNBSD: k_cache/v_cache are (num_blocks, Nkv, block_size, D)
  *                           as for fia_decode.  FIA_KV_BNBSH: (num_blocks, block_size, Nkv * D)
@@ -146,15 +147,34 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
  * options->softmax_lse      device fp32 (B, Nq) or NULL: ln(sum_t e^{z_t}) (+ e^{s_h} with a
  *                           sink) = softmax_max + ln(softmax_sum); -inf for a row with
  *                           neither a visible key nor a sink.
+ * options->atten_mask       device bytes (B, 1, 1, S) -- bool, int8 or uint8 holding 0 or 1 --
+ *                           or NULL: byte b * atten_mask_stride + t nonzero removes key t of
+ *                           batch b from the softmax (1 = masked out).  A batch whose keys are
+ *                           all masked gives the rows of an empty sequence (out 0, max -inf,
+ *                           sum 0, or the sink's values).  Masked keys' values are still read
+ *                           (weighted by 0): they must be finite.
+ * options->atten_mask_stride  S, bytes per mask row; >= max_kv_len.
+ * options->quant_scale2     device fp32 or NULL.  Non-NULL makes out an int8 (B, Nq, D) tensor:
+ *                           out = saturate(round-half-even(o * quant_scale2[c] +
+ *                           quant_offset2[c])) to [-128, 127], o the fp32 attention output and
+ *                           c = h * D + d with quant2_per_channel = 1 (Nq * D values), c = 0
+ *                           with quant2_per_channel = 0 (one value).
+ * options->quant_offset2    device fp32, as many values as quant_scale2, or NULL (zero).
  * options == NULL behaves as fia_decode.  The workspace is fia_decode_workspace_size()
- * bytes, as for fia_decode.  Errors: an unknown layout or mode, or the per-tensor mode
- * without int8 KV, is FIA_ERR_PARAM_INVALID. */
+ * bytes, as for fia_decode.  Errors: an unknown layout or mode, the per-tensor mode
+ * without int8 KV, a mask row shorter than max_kv_len, quant_offset2 without
+ * quant_scale2, or quant2_per_channel outside {0, 1} is FIA_ERR_PARAM_INVALID. */
 typedef enum { FIA_KV_BNNBSD = 0, FIA_KV_BNBSH = 1 } fia_kv_layout;
 typedef enum { FIA_AQ_PER_CHANNEL = 0, FIA_AQ_PER_TENSOR = 1 } fia_antiquant_mode;
 typedef struct {
   int kv_layout;       /* fia_kv_layout */
   int antiquant_mode;  /* fia_antiquant_mode */
   float* softmax_lse;  /* device fp32 (B, Nq) or NULL */
+  const uint8_t* atten_mask;   /* device (B, atten_mask_stride) bytes or NULL */
+  int64_t atten_mask_stride;   /* bytes per mask row, >= max_kv_len */
+  const float* quant_scale2;   /* device fp32, 1 or Nq * D values, or NULL (16-bit out) */
+  const float* quant_offset2;  /* device fp32, as quant_scale2, or NULL */
+  int quant2_per_channel;      /* 0: one value; 1: Nq * D values */
 } fia_decode_options;
 
 int fia_decode_ex(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache, fia_dtype kv_dtype,

@@ -4,6 +4,8 @@ aclnnIncreFlashAttentionV3, "Constraints / page attention": besides (blocknum, K
 blocksize, D), the paged cache may be laid out (blocknum, blocksize, H), H = KV_N * D;
 "antiquantScale / antiquantOffset": a per-tensor form of shape (2).
 FusedInferAttentionScore: the softmaxLse output, ln of the softmax denominator.
+aclnnIncreFlashAttentionV3 parameter table: attenMask (B, 1, 1, S), 1 = key masked out;
+quantScale2 / quantOffset2, an int8 output quantised per tensor or per channel.
 
 The oracle is the definition in the (blocknum, KV_N, blocksize, D) layout with
 per-channel parameters: the layout only moves bytes, and per-tensor parameters are the
@@ -17,7 +19,8 @@ import pytest
 import torch
 
 import fia_workloads as W
-from parity import MAX_TOL, DeviceDecode, assert_close, compare_decode, oracle_decode, run_decode
+import oracle as OR
+from parity import MAX_TOL, OUT_TOL, SUM_TOL, DeviceDecode, assert_close, compare_decode, oracle_decode, run_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -120,4 +123,148 @@ def test_softmax_lse(F, cuda, sink, with_max_sum):
     assert np.array_equal(np.isfinite(got), fin)
     assert np.all(got[~fin] == -np.inf)
     assert_close("softmax_lse", got[fin], lse_ref[fin], *MAX_TOL)
+    assert F.fia_device_status() == 0
+
+
+# ------------------------------------------------------------------ attenMask (B, 1, 1, S)
+MASK_CASES = {
+    # bf16/fp16 tensor-core kernel (D 128 and stacked D 64 with a sink), the int8 tensor-core
+    # kernel (D 128) and the CUDA-core int8 kernel (D 64)
+    "bf16_d128_g4": dict(B=4, Nq=8, Nkv=2, D=128, block_size=128, lengths=[700, 129, 1000, 300]),
+    "fp16_d64_g8_sink": dict(B=3, Nq=8, Nkv=1, D=64, block_size=64, dtype=W.FP16, lengths=[450, 31, 260],
+                             sink=True),
+    "int8_d128_g8": dict(B=4, Nq=16, Nkv=2, D=128, block_size=128, kv_dtype=W.INT8, lengths=[900, 130, 600, 257]),
+    "int8_d64_g2": dict(B=3, Nq=4, Nkv=2, D=64, block_size=64, kv_dtype=W.INT8, lengths=[300, 65, 190]),
+}
+
+
+def _mask_for(case, seed, S):
+    """Random keys masked (about 30%), batch 1 fully masked, the first 256 keys of batch 0
+    masked (whole leading tiles: no reference maximum yet) and batch 2's last tile masked."""
+    rng = np.random.default_rng(seed)
+    m = rng.random((case.B, S)) < 0.3
+    m[1, :] = True
+    m[0, :256] = True
+    L2 = int(case.lengths[2])
+    m[2, max(0, L2 - 100):] = True
+    return m
+
+
+@pytest.mark.parametrize("num_splits", [0, 3])
+@pytest.mark.parametrize("name", sorted(MASK_CASES))
+def test_atten_mask(F, cuda, name, num_splits):
+    case = _case("mask_" + name, **MASK_CASES[name])
+    dd = DeviceDecode(case)
+    S = case.max_len + 40  # mask rows longer than max_kv_len
+    m = _mask_for(case, zlib.crc32(name.encode()) & 0xffff, S)
+    ref = oracle_decode(case, mask=m.astype(np.uint8))
+    for dtype in (torch.bool, torch.uint8):
+        mask = torch.from_numpy(m).to(dtype).reshape(case.B, 1, 1, S).cuda()
+        out, mx, sm = _run(F, dd, num_splits, atten_mask=mask)
+        compare_decode(case, out, mx, sm, ref=ref)
+    # an all-zero mask is no mask, bit for bit
+    zero = torch.zeros((case.B, S), dtype=torch.int8, device="cuda")
+    out, mx, sm = _run(F, dd, num_splits, atten_mask=zero)
+    base = run_decode(F, dd, num_splits=num_splits)
+    assert torch.equal(out.view(torch.int16), base[0].view(torch.int16))
+    assert torch.equal(mx, base[1]) and torch.equal(sm, base[2])
+    assert F.fia_device_status() == 0
+
+
+def test_atten_mask_rows_too_short(F, cuda):
+    case = _case("mask_short", B=2, Nq=4, Nkv=2, D=128, block_size=128, lengths=[300, 20])
+    dd = DeviceDecode(case)
+    mask = torch.zeros((case.B, case.max_len - 1), dtype=torch.bool, device="cuda")
+    with pytest.raises(F.FiaError):
+        _run(F, dd, atten_mask=mask)
+
+
+# ------------------------------------------------------------------ int8 post-quant output
+def _check_codes(code, y, out_ref, s_c, atol, rtol):
+    """code (rows, C) int8 against the oracle's unrounded y = out_ref * s + o: the kernel
+    quantises its own fp32 output, which is within (atol + rtol |out|) of out_ref, so its
+    code lies within 0.5 + s (atol + rtol |out_ref|) of y after saturation."""
+    c = code.astype(np.float64)
+    margin = np.abs(s_c) * (atol + rtol * np.abs(out_ref))
+    lo = np.clip(np.rint(y - margin), -128, 127)
+    hi = np.clip(np.rint(y + margin), -128, 127)
+    bad = (c < lo) | (c > hi)
+    assert not bad.any(), f"{bad.sum()} codes outside the tolerance band, e.g. {np.argwhere(bad)[:4].tolist()}"
+
+
+PQ_CASES = {
+    "bf16_d128_g4_empty": dict(B=4, Nq=8, Nkv=2, D=128, block_size=128, lengths=[700, 0, 1000, 129]),
+    "fp16_d64_g8_sink": dict(B=3, Nq=8, Nkv=1, D=64, block_size=64, dtype=W.FP16, lengths=[450, 0, 260],
+                             sink=True),
+    "int8_d128_g8": dict(B=3, Nq=16, Nkv=2, D=128, block_size=128, kv_dtype=W.INT8, lengths=[900, 130, 0]),
+    "int8_d64_g2": dict(B=2, Nq=4, Nkv=2, D=64, block_size=64, kv_dtype=W.INT8, lengths=[300, 65]),
+}
+
+
+@pytest.mark.parametrize("num_splits", [0, 3])
+@pytest.mark.parametrize("name", sorted(PQ_CASES))
+def test_post_quant_int8_output(F, cuda, name, num_splits):
+    case = _case("pq_" + name, **PQ_CASES[name])
+    dd = DeviceDecode(case)
+    o_ref, m_ref, s_ref = oracle_decode(case)
+    C = case.Nq * case.D
+    rng = np.random.default_rng(zlib.crc32(name.encode()) & 0xffff)
+    amax = max(float(np.abs(o_ref).max()), 1e-3)
+    atol, rtol = OUT_TOL[case.dtype]
+    per_channel = (rng.uniform(0.5, 1.5, C) * 60.0 / amax).astype(np.float32)
+    offsets = rng.uniform(-20, 20, C).astype(np.float32)
+    variants = [  # (scale2, offset2): per tensor / per channel, symmetric / asymmetric, saturating
+        (np.array([60.0 / amax], np.float32), None),
+        (np.array([60.0 / amax], np.float32), np.array([-7.5], np.float32)),
+        (per_channel, None),
+        (per_channel, offsets),
+        (np.array([1000.0 / amax], np.float32), np.array([3.0], np.float32)),
+    ]
+    for s2, o2 in variants:
+        y, _ = OR.post_quant(o_ref, s2, o2)
+        out, mx, sm = _run(F, dd, num_splits, quant_scale2=torch.from_numpy(s2).cuda(),
+                           quant_offset2=None if o2 is None else torch.from_numpy(o2).cuda())
+        assert out.dtype == torch.int8 and tuple(out.shape) == (case.B, case.Nq, case.D)
+        s_c = np.broadcast_to(s2.astype(np.float64), (C,))
+        _check_codes(out.cpu().numpy().reshape(-1, C), y.reshape(-1, C), o_ref.reshape(-1, C), s_c, atol, rtol)
+        assert_close("softmax_max", mx.double().cpu().numpy().reshape(-1), m_ref, *MAX_TOL)
+        assert_close("softmax_sum", sm.double().cpu().numpy().reshape(-1), s_ref, *SUM_TOL)
+    assert F.fia_device_status() == 0
+
+
+def test_post_quant_offset_without_scale(F, cuda):
+    case = _case("pq_bad", B=1, Nq=2, Nkv=1, D=64, block_size=16, lengths=[20])
+    dd = DeviceDecode(case)
+    with pytest.raises(F.FiaError):
+        F.fia_decode_ex(dd.q, dd.k, dd.v, dd.bt, dd.lens, max_kv_len=case.max_len, num_heads=case.Nq,
+                        num_kv_heads=case.Nkv, scale=case.scale, quant_offset2=torch.zeros(1, device="cuda"),
+                        out=torch.empty((1, 2, 64), dtype=torch.int8, device="cuda"))
+
+
+@pytest.mark.parametrize("D,num_splits", [(128, 0), (64, 0), (128, 2)])
+def test_post_quant_ties_and_saturation_exact(F, cuda, D, num_splits):
+    """Sequences of one key: the attention output is that key's value row, exactly in fp32.
+    Values are multiples of 0.25 (exact in bf16), so with scale2 = 2 half of y = 2v + o
+    fall on ties (rounded to even) and with scale2 = 4 the large ones saturate: the int8
+    output must equal the oracle's codes bit for bit.  Batch 3 is empty: code = q(0)."""
+    lengths = [1, 1, 1, 0, 1, 1]
+    case = _case(f"pq_exact_{D}", B=6, Nq=8, Nkv=2, D=D, block_size=64, lengths=lengths)
+    rng = np.random.default_rng(D)
+    vals = rng.integers(-255, 256, case.v_cache.shape).astype(np.float32) * 0.25   # |v| <= 63.75
+    case.v_cache = W.to_bits(vals, case.dtype)
+    assert np.array_equal(W.bits_to_f32(case.v_cache, case.dtype), vals)
+    dd = DeviceDecode(case)
+    o_ref, _, _ = oracle_decode(case)
+    for s2, o2 in [(2.0, 0.0), (2.0, 0.5), (4.0, -1.0), (0.5, 0.25)]:
+        y, code_ref = OR.post_quant(o_ref, [s2], [o2])
+        out, _, _ = _run(F, dd, num_splits, quant_scale2=torch.tensor([s2], device="cuda"),
+                         quant_offset2=torch.tensor([o2], device="cuda"))
+        got = out.cpu().numpy().reshape(code_ref.shape)
+        assert np.array_equal(got, code_ref), np.argwhere(got != code_ref)[:4].tolist()
+        if s2 == 4.0:
+            assert not np.any(y == np.floor(y) + 0.5)
+        else:
+            assert np.any(y == np.floor(y) + 0.5)      # ties present
+        if s2 == 4.0:
+            assert np.any(code_ref == 127) and np.any(code_ref == -128)
     assert F.fia_device_status() == 0
