@@ -37,10 +37,10 @@
  *       With a sink: out = 0, max = sink, sum = 1.
  *   R7  Causal mask (rightDownCausal): key j is visible to query i of a sequence
  *       iff j <= i + (Lkv - Lq).
- *   R8  attenMask (decode): a byte per (batch, key); nonzero = the key is masked
+ *   R13 attenMask (decode): a byte per (batch, key); nonzero = the key is masked
  *       out (the causal forms the pages describe keep the diagonal at 0), and a
  *       masked key is left out of the softmax entirely.
- *   R9  Post-quant output: y = out * quantScale2 + quantOffset2 in the
+ *   R14 Post-quant output: y = out * quantScale2 + quantOffset2 in the
  *       attention's own precision, rounded to nearest with ties to even and
  *       saturated to int8; per-channel parameters index the output's N * D
  *       channels (N = query heads, the heads of attentionOut).

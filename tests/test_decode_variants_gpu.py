@@ -221,7 +221,7 @@ def test_post_quant_int8_output(F, cuda, name, num_splits):
         (np.array([1000.0 / amax], np.float32), np.array([3.0], np.float32)),
     ]
     for s2, o2 in variants:
-        y, _ = OR.post_quant(o_ref, s2, o2)
+        y, _ = OR.post_quant(o_ref.reshape(case.B, C), s2, o2)   # channels h * D + d of a batch row
         out, mx, sm = _run(F, dd, num_splits, quant_scale2=torch.from_numpy(s2).cuda(),
                            quant_offset2=None if o2 is None else torch.from_numpy(o2).cuda())
         assert out.dtype == torch.int8 and tuple(out.shape) == (case.B, case.Nq, case.D)
@@ -256,7 +256,7 @@ def test_post_quant_ties_and_saturation_exact(F, cuda, D, num_splits):
     dd = DeviceDecode(case)
     o_ref, _, _ = oracle_decode(case)
     for s2, o2 in [(2.0, 0.0), (2.0, 0.5), (4.0, -1.0), (0.5, 0.25)]:
-        y, code_ref = OR.post_quant(o_ref, [s2], [o2])
+        y, code_ref = OR.post_quant(o_ref.reshape(case.B, -1), [s2], [o2])
         out, _, _ = _run(F, dd, num_splits, quant_scale2=torch.tensor([s2], device="cuda"),
                          quant_offset2=torch.tensor([o2], device="cuda"))
         got = out.cpu().numpy().reshape(code_ref.shape)
