@@ -64,7 +64,7 @@ def _bind(path: str):
     lib.oracle_decode.argtypes = [P, i32, P, P, i32, P, i64, P, i32, i32, i32, i32, i32, i64,
                                   dbl, P, P, P, P, i64, P, i64, i32, P, P, P]
     lib.oracle_decode.restype = i32
-    lib.oracle_prefill.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, dbl, i32, P,
+    lib.oracle_prefill.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, dbl, i32, i64, i64, P,
                                    P, i64, i32, P, P, P]
     lib.oracle_prefill.restype = i32
     lib.oracle_rau.argtypes = [P, P, P, P, P, P, i64, i32, i32, P, P, P]
@@ -167,9 +167,10 @@ class Oracle:
         return out, mx, sm
 
     def prefill(self, q, k, v, cu_q, cu_kv, *, Nq, Nkv, D, scale, causal=True, dtype=None, sink=None,
-                rows=None, nthreads=0):
+                rows=None, nthreads=0, band=None):
         """Prefill attention in TND layout.  q: (T, Nq, D); k, v: (Tkv, Nkv, D);
-        cu_q / cu_kv: B + 1 cumulative lengths from 0.  Returns (out, max, sum) in
+        cu_q / cu_kv: B + 1 cumulative lengths from 0.  band=(pre_tokens, next_tokens)
+        selects sparseMode 4 (and overrides causal).  Returns (out, max, sum) in
         float64 for the rows (t * Nq + h) asked for, or for all T * Nq rows."""
         q, k, v = (np.ascontiguousarray(a) for a in (q, k, v))
         cu_q = np.ascontiguousarray(cu_q, dtype=np.int64)
@@ -184,7 +185,8 @@ class Oracle:
         sm = np.zeros(R, np.float64)
         rc = self._lib.oracle_prefill(
             _ptr(q), _ptr(k), _ptr(v), _dtype_code(q, dtype), _ptr(cu_q), _ptr(cu_kv),
-            B, Nq, Nkv, D, float(scale), int(bool(causal)), _ptr(sink), _ptr(rows_a),
+            B, Nq, Nkv, D, float(scale), 4 if band is not None else (3 if causal else 0),
+            int(band[0]) if band is not None else 0, int(band[1]) if band is not None else 0, _ptr(sink), _ptr(rows_a),
             0 if rows_a is None else R, nthreads, _ptr(out), _ptr(mx), _ptr(sm))
         if rc != 0:
             raise ValueError("oracle_prefill rejected its arguments")

@@ -44,6 +44,9 @@
  *       attention's own precision, rounded to nearest with ties to even and
  *       saturated to int8; per-channel parameters index the output's N * D
  *       channels (N = query heads, the heads of attentionOut).
+ *   R15 Band (sparseMode 4, preTokens / nextTokens): aligned on the same
+ *       diagonal as rightDownCausal: key j is visible to query i iff
+ *       i + (Lkv - Lq) - preTokens <= j <= i + (Lkv - Lq) + nextTokens.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -shared -fPIC.
  * -ffp-contract=off is required: R2 forbids contracting the dequant into an FMA.
@@ -288,17 +291,22 @@ int oracle_decode(const void *q, int q_dtype,
  * the tokens of all sequences are concatenated; cu_q / cu_kv hold B + 1
  * cumulative lengths starting at 0 (the RingAttentionUpdate page's form of
  * actual_seq_qlen).  q/out: (T, Nq, D); k, v: (Tkv, Nkv, D).
- * causal != 0 applies R7.  rows: (t * Nq + h) rows or NULL for all. */
+ * sparse_mode ([FIA] sparseMode): 0 no mask, 3 rightDownCausal (R7), 4 band (R15):
+ * with d = Lkv - Lq, key j is visible to query i iff
+ *     i + d - pre_tokens <= j <= i + d + next_tokens.
+ * rows: (t * Nq + h) rows or NULL for all. */
 int oracle_prefill(const void *q, const void *k, const void *v, int dtype,
                    const int64_t *cu_q, const int64_t *cu_kv,
-                   int B, int Nq, int Nkv, int D, double scale, int causal,
-                   const float *sink,
+                   int B, int Nq, int Nkv, int D, double scale, int sparse_mode,
+                   int64_t pre_tokens, int64_t next_tokens, const float *sink,
                    const int64_t *rows, int64_t n_rows, int nthreads,
                    double *out, double *smax, double *ssum)
 {
     if (Nkv == 0)
         Nkv = Nq;
     if (Nq <= 0 || Nkv <= 0 || Nq % Nkv != 0 || D <= 0 || B <= 0)
+        return -1;
+    if (sparse_mode != 0 && sparse_mode != 3 && sparse_mode != 4)
         return -1;
     const int G = Nq / Nkv;
     const int64_t T = cu_q[B];
@@ -340,16 +348,24 @@ int oracle_prefill(const void *q, const void *k, const void *v, int dtype,
             }
             const int64_t qi = t - cu_q[b];
             const int64_t Lq = cu_q[b + 1] - cu_q[b], Lkv = cu_kv[b + 1] - cu_kv[b];
-            int64_t n = Lkv;
-            if (causal) {                                   /* R7 */
+            int64_t first = 0, n = Lkv;                     /* keys first .. first + n - 1 */
+            if (sparse_mode == 3) {                         /* R7 */
                 const int64_t last = qi + (Lkv - Lq);       /* last visible key index */
                 n = last + 1 < 0 ? 0 : (last + 1 < Lkv ? last + 1 : Lkv);
+            } else if (sparse_mode == 4) {                  /* R15 */
+                int64_t lo = qi + (Lkv - Lq) - pre_tokens, hi = qi + (Lkv - Lq) + next_tokens;
+                if (lo < 0)
+                    lo = 0;
+                if (hi > Lkv - 1)
+                    hi = Lkv - 1;
+                first = lo;
+                n = hi >= lo ? hi - lo + 1 : 0;
             }
             for (int d = 0; d < D; ++d)
                 qd[d] = load_elem(q, dtype, r * D + d);
             for (int64_t j = 0; j < n; ++j)
                 for (int d = 0; d < D; ++d) {
-                    const int64_t src = ((cu_kv[b] + j) * Nkv + hk) * D + d;
+                    const int64_t src = ((cu_kv[b] + first + j) * Nkv + hk) * D + d;
                     Kd[j * D + d] = load_elem(k, dtype, src);
                     Vd[j * D + d] = load_elem(v, dtype, src);
                 }

@@ -480,6 +480,53 @@ def pin_prefill_matches_sdpa_causal(O):
             np.testing.assert_allclose(sm[q0:q1], s_ref.T, rtol=1e-12, atol=1e-12)
 
 
+def pin_prefill_band_matches_sdpa(O):
+    """sparseMode 4: the band i + d - pre <= j <= i + d + next (d = Lkv - Lq) equals torch SDPA
+    under a boolean mask built with numpy's triu/tril (k = d - pre and d + next); rows with
+    no key in the band give the empty-row values; band(huge, 0) is the causal mode and
+    band(huge, huge) no mask, bit for bit."""
+    rng = np.random.default_rng(31)
+    Nq, Nkv, D = 4, 2, 16
+    lq, lkv = [9, 1, 14, 6], [9, 5, 20, 3]          # Lq = Lkv, Lq < Lkv and Lq > Lkv
+    cu_q = np.concatenate([[0], np.cumsum(lq)])
+    cu_kv = np.concatenate([[0], np.cumsum(lkv)])
+    T, Tkv = int(cu_q[-1]), int(cu_kv[-1])
+    q = W.to_bits(rng.standard_normal((T, Nq, D), dtype=np.float32), W.BF16)
+    k = W.to_bits(rng.standard_normal((Tkv, Nkv, D), dtype=np.float32), W.BF16)
+    v = W.to_bits(rng.standard_normal((Tkv, Nkv, D), dtype=np.float32), W.BF16)
+    f = lambda a: W.bits_to_f32(a, W.BF16).astype(np.float64)
+    qf, kf, vf = f(q), np.repeat(f(k), Nq // Nkv, axis=1), np.repeat(f(v), Nq // Nkv, axis=1)
+    scale = 0.3
+    kw = dict(Nq=Nq, Nkv=Nkv, D=D, scale=scale, dtype=OR.BF16)
+    for pre, nxt in [(3, 0), (2, 1), (0, 0), (4, -1), (-1, 2), (1000, 5)]:
+        out, mx, sm = O.prefill(q, k, v, cu_q, cu_kv, band=(pre, nxt), **kw)
+        for b in range(len(lq)):
+            Lq, Lkv = lq[b], lkv[b]
+            d = Lkv - Lq
+            ones = np.ones((Lq, Lkv), bool)
+            allowed = np.triu(ones, k=d - pre) & np.tril(ones, k=d + nxt)
+            Q = qf[cu_q[b]:cu_q[b + 1]].transpose(1, 0, 2)
+            K = kf[cu_kv[b]:cu_kv[b + 1]].transpose(1, 0, 2)
+            V = vf[cu_kv[b]:cu_kv[b + 1]].transpose(1, 0, 2)
+            rows = np.arange(cu_q[b] * Nq, cu_q[b + 1] * Nq).reshape(Lq, Nq).T     # (Nq, Lq)
+            has = allowed.any(axis=1)
+            if has.any():
+                ref = sdpa_rows(Q[:, has], K, V, scale, bool_mask=np.broadcast_to(allowed[has], (Nq,) + allowed[has].shape))
+                np.testing.assert_allclose(out[rows[:, has]], ref, rtol=1e-12, atol=1e-12)
+                s = scale * np.einsum("hid,hjd->hij", Q[:, has], K)
+                s = np.where(allowed[has][None], s, -np.inf)
+                m_ref, s_ref = lse_max_sum(s)
+                np.testing.assert_allclose(mx[rows[:, has]], m_ref, rtol=1e-12, atol=1e-12)
+                np.testing.assert_allclose(sm[rows[:, has]], s_ref, rtol=1e-12, atol=1e-12)
+            e = rows[:, ~has]
+            assert np.all(out[e] == 0) and np.all(mx[e] == -np.inf) and np.all(sm[e] == 0)
+    big = 1 << 40
+    causal = O.prefill(q, k, v, cu_q, cu_kv, causal=True, **kw)
+    assert all(np.array_equal(x, y) for x, y in zip(causal, O.prefill(q, k, v, cu_q, cu_kv, band=(big, 0), **kw)))
+    full = O.prefill(q, k, v, cu_q, cu_kv, causal=False, **kw)
+    assert all(np.array_equal(x, y) for x, y in zip(full, O.prefill(q, k, v, cu_q, cu_kv, band=(big, big), **kw)))
+
+
 def pin_prefill_causal_counts(O):
     """Equal scores under the causal mask: query i averages exactly keys 0..i."""
     L, D = 7, 8

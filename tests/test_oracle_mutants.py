@@ -48,8 +48,13 @@ MUTANTS = [
     ("post_quant_channel_by_row", "const int64_t pc = per_channel ? c : 0;",
      "const int64_t pc = per_channel ? r : 0;"),
     ("post_quant_offset_sign", "x[i] * (double)scale2[pc] + (offset2", "x[i] * (double)scale2[pc] - (offset2"),
-    ("prefill_kv_head_index", "const int64_t src = ((cu_kv[b] + j) * Nkv + hk) * D + d;",
-     "const int64_t src = ((cu_kv[b] + j) * Nkv + (h % Nkv)) * D + d;"),
+    ("band_lower_off_by_one", "int64_t lo = qi + (Lkv - Lq) - pre_tokens,", "int64_t lo = qi + (Lkv - Lq) - pre_tokens + 1,"),
+    ("band_not_shifted", "int64_t lo = qi + (Lkv - Lq) - pre_tokens, hi = qi + (Lkv - Lq) + next_tokens;",
+     "int64_t lo = qi - pre_tokens, hi = qi + next_tokens;"),
+    ("band_next_ignored", "hi = qi + (Lkv - Lq) + next_tokens;", "hi = qi + (Lkv - Lq);"),
+    ("band_first_key_dropped", "((cu_kv[b] + first + j) * Nkv + hk) * D + d", "((cu_kv[b] + j) * Nkv + hk) * D + d"),
+    ("prefill_kv_head_index", "const int64_t src = ((cu_kv[b] + first + j) * Nkv + hk) * D + d;",
+     "const int64_t src = ((cu_kv[b] + first + j) * Nkv + (h % Nkv)) * D + d;"),
 ]
 
 
