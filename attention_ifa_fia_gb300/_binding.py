@@ -34,6 +34,11 @@ class FiaError(RuntimeError):
         self.code = code
 
 
+class PrefillOptions(ctypes.Structure):
+    """fia_prefill_options of include/fia.h."""
+    _fields_ = [("pre_tokens", ctypes.c_int64), ("next_tokens", ctypes.c_int64)]
+
+
 class DecodeOptions(ctypes.Structure):
     """fia_decode_options of include/fia.h."""
     _fields_ = [("kv_layout", ctypes.c_int), ("antiquant_mode", ctypes.c_int), ("softmax_lse", ctypes.c_void_p),
@@ -62,6 +67,8 @@ def _load() -> ctypes.CDLL:
         "fia_prefill_workspace_size": ([i32, i32, i32, i32, i32, ctypes.POINTER(sz)], i32),
         "fia_prefill": ([P, P, P, i32, P, P, i32, i64, i64, i32, i32, i32, i32, i32, dbl, i32, P, P, P, P, P, sz,
                          P], i32),
+        "fia_prefill_ex": ([P, P, P, i32, P, P, i32, i64, i64, i32, i32, i32, i32, i32, dbl, i32, P, P, P, P, P,
+                            sz, P, ctypes.POINTER(PrefillOptions)], i32),
         "ring_attention_update": ([P, P, P, P, P, P, i32, i64, i32, i32, P, P, P, P], i32),
         "fia_debug_dequant": ([P, P, P, i64, P, P], i32),
         "fia_trace_enable": ([i32], i32),
@@ -252,9 +259,12 @@ def fia_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q:
                 cu_seqlens_kv: torch.Tensor, *, max_seqlen_q: int, max_seqlen_kv: int, num_heads: int,
                 num_kv_heads: int = 0, scale: Optional[float] = None, mask: int = 3, sink=None,
                 out: Optional[torch.Tensor] = None, softmax_max=None, softmax_sum=None,
-                workspace: Optional[torch.Tensor] = None, stream=None):
+                workspace: Optional[torch.Tensor] = None, stream=None, pre_tokens: Optional[int] = None,
+                next_tokens: Optional[int] = None):
     """Prefill attention, TND.  q: (T, Nq, D); k, v: (Tkv, Nkv, D); cu_seqlens int64 (B + 1,)
-    on the device.  mask 3 = rightDownCausal, 0 = none.  Returns (out, softmax_max, softmax_sum)."""
+    on the device.  mask 3 = rightDownCausal, 0 = none, 4 = band (pre_tokens, next_tokens
+    around the rightDownCausal diagonal, through fia_prefill_ex).  Returns (out, softmax_max,
+    softmax_sum)."""
     T, D = int(q.shape[0]), int(q.shape[-1])
     Tkv = int(k.shape[0])
     B = int(cu_seqlens_q.shape[0]) - 1
@@ -266,11 +276,16 @@ def fia_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q:
     if workspace is None:
         nbytes = fia_prefill_workspace_size(B, num_heads, nkv, D, max_seqlen_q)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    rc = _lib.fia_prefill(_ptr(q), _ptr(k), _ptr(v), dtype_code(q), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B,
-                          T, Tkv, int(max_seqlen_q), int(max_seqlen_kv), num_heads, nkv, D, float(scale), int(mask),
-                          _ptr(sink), _ptr(out), _ptr(softmax_max), _ptr(softmax_sum), _ptr(workspace),
-                          workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(rc, "fia_prefill")
+    args = (_ptr(q), _ptr(k), _ptr(v), dtype_code(q), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), B, T, Tkv,
+            int(max_seqlen_q), int(max_seqlen_kv), num_heads, nkv, D, float(scale), int(mask), _ptr(sink), _ptr(out),
+            _ptr(softmax_max), _ptr(softmax_sum), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream))
+    if pre_tokens is None and next_tokens is None:
+        _check(_lib.fia_prefill(*args), "fia_prefill")
+    else:
+        opts = PrefillOptions(int(pre_tokens if pre_tokens is not None else 1 << 40),
+                              int(next_tokens if next_tokens is not None else 1 << 40))
+        _check(_lib.fia_prefill_ex(*args, ctypes.byref(opts)), "fia_prefill_ex")
     return out, softmax_max, softmax_sum
 
 

@@ -534,10 +534,11 @@ int fia_prefill_workspace_size(int B, int Nq, int Nkv, int D, int max_seqlen_q, 
   return ok();
 }
 
-int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, const int64_t* cu_seqlens_q,
-                const int64_t* cu_seqlens_kv, int B, int64_t T, int64_t Tkv, int max_seqlen_q, int max_seqlen_kv,
-                int Nq, int Nkv, int D, double scale, int mask, const float* sink, void* out, float* softmax_max,
-                float* softmax_sum, void* workspace, size_t workspace_bytes, fia_stream_t stream) {
+static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype dtype, const int64_t* cu_seqlens_q,
+                        const int64_t* cu_seqlens_kv, int B, int64_t T, int64_t Tkv, int max_seqlen_q,
+                        int max_seqlen_kv, int Nq, int Nkv, int D, double scale, int mask, const float* sink,
+                        void* out, float* softmax_max, float* softmax_sum, void* workspace, size_t workspace_bytes,
+                        fia_stream_t stream, const fia_prefill_options* opt) {
   if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_kv || !out)
     return fail(FIA_ERR_PARAM_NULLPTR, "q, k, v, cu_seqlens_q, cu_seqlens_kv and out are required");
   if (!workspace) return fail(FIA_ERR_PARAM_NULLPTR, "workspace is NULL");
@@ -547,8 +548,20 @@ int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, co
     return fail(FIA_ERR_PARAM_INVALID, "T = %lld, Tkv = %lld outside [0, 2^31)", (long long)T, (long long)Tkv);
   if (max_seqlen_kv < 0 || max_seqlen_kv > (1 << 20))
     return fail(FIA_ERR_PARAM_INVALID, "max_seqlen_kv = %d outside [0, 2^20] (this build)", max_seqlen_kv);
-  if (mask != 0 && mask != 3)
-    return fail(FIA_ERR_PARAM_INVALID, "mask = %d: 0 (none) and 3 (rightDownCausal) are supported", mask);
+  if (mask != 0 && mask != 3 && mask != 4)
+    return fail(FIA_ERR_PARAM_INVALID, "mask = %d: 0 (none), 3 (rightDownCausal) and 4 (band) are supported", mask);
+  // the band in keys around the rightDownCausal diagonal, clamped to +-2^30 (no sequence is
+  // longer than 2^21 here, so clamping changes no visible set)
+  constexpr int64_t kBandCap = 1LL << 30;
+  int64_t pre = kBandCap, next = mask == 3 ? 0 : kBandCap;
+  if (mask == 4) {
+    if (!opt) return fail(FIA_ERR_PARAM_NULLPTR, "mask 4 (band) needs options with pre_tokens and next_tokens");
+    pre = std::min(std::max(opt->pre_tokens, -kBandCap), kBandCap);
+    next = std::min(std::max(opt->next_tokens, -kBandCap), kBandCap);
+    if (pre + next < 0)
+      return fail(FIA_ERR_PARAM_INVALID, "band with pre_tokens %lld and next_tokens %lld holds no key",
+                  (long long)opt->pre_tokens, (long long)opt->next_tokens);
+  }
   if (!std::isfinite(scale)) return fail(FIA_ERR_PARAM_INVALID, "scale is not finite");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(FIA_ERR_PARAM_INVALID, "q, k, v and out must be 16-byte aligned");
@@ -581,7 +594,8 @@ int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, co
   p.Tkv = Tkv;
   p.max_seqlen_q = max_seqlen_q;
   p.max_seqlen_kv = max_seqlen_kv;
-  p.causal = mask == 3;
+  p.pre = (int)pre;
+  p.next = (int)next;
   p.dtype = dtype;
   p.scale_log2 = (float)(scale * 1.4426950408889634);
   p.tile_counter = static_cast<int*>(workspace);
@@ -595,6 +609,25 @@ int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, co
   cudaError_t e = fia::launch_prefill(p, tmQ, tmK, tmV, d->num_sms, stream);
   if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "prefill launch: %s", cudaGetErrorString(e));
   return ok();
+}
+
+int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, const int64_t* cu_seqlens_q,
+                const int64_t* cu_seqlens_kv, int B, int64_t T, int64_t Tkv, int max_seqlen_q, int max_seqlen_kv,
+                int Nq, int Nkv, int D, double scale, int mask, const float* sink, void* out, float* softmax_max,
+                float* softmax_sum, void* workspace, size_t workspace_bytes, fia_stream_t stream) {
+  return prefill_impl(q, k, v, dtype, cu_seqlens_q, cu_seqlens_kv, B, T, Tkv, max_seqlen_q, max_seqlen_kv, Nq, Nkv,
+                      D, scale, mask, sink, out, softmax_max, softmax_sum, workspace, workspace_bytes, stream,
+                      nullptr);
+}
+
+int fia_prefill_ex(const void* q, const void* k, const void* v, fia_dtype dtype, const int64_t* cu_seqlens_q,
+                   const int64_t* cu_seqlens_kv, int B, int64_t T, int64_t Tkv, int max_seqlen_q, int max_seqlen_kv,
+                   int Nq, int Nkv, int D, double scale, int mask, const float* sink, void* out, float* softmax_max,
+                   float* softmax_sum, void* workspace, size_t workspace_bytes, fia_stream_t stream,
+                   const fia_prefill_options* options) {
+  return prefill_impl(q, k, v, dtype, cu_seqlens_q, cu_seqlens_kv, B, T, Tkv, max_seqlen_q, max_seqlen_kv, Nq, Nkv,
+                      D, scale, mask, sink, out, softmax_max, softmax_sum, workspace, workspace_bytes, stream,
+                      options);
 }
 
 }  // extern "C"

@@ -137,7 +137,10 @@ struct PrefillParams {
   int B, Nq, Nkv, G, D;
   int64_t T, Tkv;
   int max_seqlen_q, max_seqlen_kv;
-  int causal;
+  // band on the rightDownCausal diagonal: key j is visible to query i of a sequence iff
+  // i + d - pre <= j <= i + d + next, d = Lkv - Lq (pre + next >= 0, both within
+  // [-2^30, 2^30]); rightDownCausal is (2^30, 0), no mask (2^30, 2^30)
+  int pre, next;
   int dtype;          // kBF16 or kF16
   float scale_log2;
   int* tile_list;     // workspace: (sequence << 16 | query tile) pairs, longest first

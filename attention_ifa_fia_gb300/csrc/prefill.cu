@@ -1,4 +1,4 @@
-// prefill.cu -- causal variable-length prefill attention (TND) on tcgen05 tensor cores.
+// prefill.cu -- causal / band variable-length prefill attention (TND) on tcgen05 tensor cores.
 //
 // What it computes (FusedInferAttentionScore: prefill mode with query length > 1 and
 // sparseMode 3 = rightDownCausal; aclnnFlashAttentionScoreV4: TND layout, cumulative
@@ -64,12 +64,16 @@ struct PSmem {
 // The dynamic shared memory must fit the 227 KB a CTA may use.
 static_assert(sizeof(PSmem) <= 232448, "prefill shared memory exceeds the per-CTA limit");
 
-// per (sequence, query tile): key tiles that hold at least one visible key
-__device__ __forceinline__ int key_tiles(int q0, int Lq, int Lkv, int causal) {
+// per (sequence, query tile): the key tiles holding at least one visible key, {first,
+// count}.  A row's visible keys form one interval of the band; the rows' intervals shift
+// by one key per row and hold pre + next + 1 >= 1 keys, so their union is one interval.
+__device__ __forceinline__ int2 key_tile_range(const PrefillParams& p, int q0, int Lq, int Lkv) {
   const int q_last = min(q0 + kQT - 1, Lq - 1);
-  int k_max = causal ? q_last + (Lkv - Lq) : Lkv - 1;
-  k_max = min(k_max, Lkv - 1);
-  return k_max < 0 ? 0 : k_max / kKT + 1;
+  const int d = Lkv - Lq;
+  const int k_min = max(q0 + d - p.pre, 0);
+  const int k_max = min(q_last + d + p.next, Lkv - 1);
+  if (k_max < k_min) return make_int2(0, 0);
+  return make_int2(k_min / kKT, k_max / kKT - k_min / kKT + 1);
 }
 
 __device__ __forceinline__ void seq_bounds(const PrefillParams& p, int b, int& tq, int& Lq, int& tk, int& Lkv) {
@@ -120,7 +124,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
       for (int i = warp; i < nb; i += nwarps) {
         const int4 bd = bounds[i];
         for (int qt = lane; qt * kQT < bd.y; qt += 32) {
-          const int n = min(max(key_tiles(qt * kQT, bd.y, bd.w, p.causal), 1), max_key_tiles);
+          const int n = min(max(key_tile_range(p, qt * kQT, bd.y, bd.w).y, 1), max_key_tiles);
           if (pass == 0) {
             atomicAdd(&hist[n], 1);
           } else {
@@ -279,20 +283,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
         int tq, Lq, tk, Lkv;
         seq_bounds(p, b, tq, Lq, tk, Lkv);
         const int q0 = qt * kQT;
-        const int nkv = max(key_tiles(q0, Lq, Lkv, p.causal), 1);
+        const int2 kr = key_tile_range(p, q0, Lq, Lkv);  // a query tile with no key still runs one
+        const int nkv = max(kr.y, 1);                     // (all-masked) tile
         const int qb = u_local & 1;
         if (!mbar_wait(&sm.q_empty[qb], ((uint32_t)(u_local >> 1) & 1u) ^ 1u, p.status)) { ok = false; break; }
         mbar_arrive_expect_tx(&sm.q_full[qb], kTileB);
         for (int bx = 0; bx < 2; ++bx)
           tma_load_3d(sm.q[qb] + bx * (kQT * 128), &tmQ, bx * 64, h, tq + q0, &sm.q_full[qb]);
         const int hkv = h / G;
-        for (int kt = 0; kt < nkv; ++kt, ++j) {
+        for (int i = 0; i < nkv; ++i, ++j) {
+          const int kt = kr.x + i;
           const int st = j % kPStages;
           if (!mbar_wait(&sm.k_empty[st], ((uint32_t)(j / kPStages) & 1u) ^ 1u, p.status)) { ok = false; break; }
           PTileMeta& m = sm.meta[j % kMetaRing];
           m.b = b; m.h = h; m.q0 = q0; m.kvt = kt;
           m.tq = tq; m.tk = tk; m.Lq = Lq; m.Lkv = Lkv;
-          m.first = kt == 0; m.last = kt == nkv - 1; m.qbuf = qb; m.unit = u;
+          m.first = i == 0; m.last = i == nkv - 1; m.qbuf = qb; m.unit = u;
           ring_hkv[j % kMetaRing] = hkv;
           ring_row[j % kMetaRing] = tk + kt * kKT;
           mbar_arrive_expect_tx(&sm.k_full[st], kTileB);
@@ -407,10 +413,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int qi = meta.q0 + r;            // query index within the sequence
       const bool row_ok = qi < meta.Lq;
       const int k0 = meta.kvt * kKT + c_base;
-      // visible keys of this row among this half's columns: [k0, k0 + nvis)
-      int k_hi = meta.Lkv;
-      if (p.causal) k_hi = min(k_hi, qi + (meta.Lkv - meta.Lq) + 1);
+      // visible keys of this row among this half's columns: [k0 + nlo, k0 + nvis)
+      const int dq = qi + (meta.Lkv - meta.Lq);
+      const int k_hi = min(meta.Lkv, dq + p.next + 1);
       const int nvis = row_ok ? max(0, min(k_hi - k0, 64)) : 0;
+      const int nlo = min(max(dq - p.pre - k0, 0), 64);
       float s[64];
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
@@ -423,10 +430,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.s_free[sb]);
       float mt = -INFINITY;
+      if (__any_sync(0xffffffffu, nlo > 0)) {  // a band's lower edge crosses the tile
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        s[c] = (c < nvis) ? s[c] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, s[c]);
+        for (int c = 0; c < 64; ++c) {
+          s[c] = (c >= nlo && c < nvis) ? s[c] * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          s[c] = (c < nvis) ? s[c] * p.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, s[c]);
+        }
       }
       sm.rmax[sb][half][r] = mt;
       named_bar_sync(kBarSoftmax, kSoftmaxThreads);
@@ -656,7 +671,8 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         int tq, Lq, tk, Lkv;
         seq_bounds(p, b, tq, Lq, tk, Lkv);
         const int q0 = qt * kQT;
-        const int nkv = max(key_tiles(q0, Lq, Lkv, p.causal), 1);
+        const int2 kr = key_tile_range(p, q0, Lq, Lkv);  // a query tile with no key still runs one
+        const int nkv = max(kr.y, 1);                     // (all-masked) tile
         // both Q tiles; the previous unit's last QK_B has completed
         if (!mbar_wait(&sm.q_empty, ((uint32_t)u_local & 1u) ^ 1u, p.status)) { ok = false; break; }
         mbar_arrive_expect_tx(&sm.q_full, 2 * kTileB);
@@ -664,13 +680,14 @@ __global__ void __launch_bounds__(kP2Threads, 1)
           for (int bx = 0; bx < 2; ++bx)
             tma_load_3d(sm.q[x] + bx * (kQT * 128), &tmQ, bx * 64, h0 + x, tq + q0, &sm.q_full);
         const int hkv = h0 / p.G;
-        for (int kt = 0; kt < nkv; ++kt, ++j) {
+        for (int i = 0; i < nkv; ++i, ++j) {
+          const int kt = kr.x + i;
           const int st = j % kPStages;
           if (!mbar_wait(&sm.k_empty[st], ((uint32_t)(j / kPStages) & 1u) ^ 1u, p.status)) { ok = false; break; }
           PTileMeta& m = sm.meta[j % kMetaRing];
           m.b = b; m.h = h0; m.q0 = q0; m.kvt = kt;
           m.tq = tq; m.tk = tk; m.Lq = Lq; m.Lkv = Lkv;
-          m.first = kt == 0; m.last = kt == nkv - 1; m.qbuf = 0; m.unit = u;
+          m.first = i == 0; m.last = i == nkv - 1; m.qbuf = 0; m.unit = u;
           ring_hkv[j % kMetaRing] = hkv;
           ring_row[j % kMetaRing] = tk + kt * kKT;
           mbar_arrive_expect_tx(&sm.k_full[st], kTileB);
@@ -794,9 +811,10 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       const int qi = meta.q0 + r;
       const bool row_ok = qi < meta.Lq;
       const int k0 = meta.kvt * kKT;
-      int k_hi = meta.Lkv;
-      if (p.causal) k_hi = min(k_hi, qi + (meta.Lkv - meta.Lq) + 1);
-      const int nvis = row_ok ? max(0, min(k_hi - k0, kKT)) : 0;
+      const int dq = qi + (meta.Lkv - meta.Lq);
+      const int k_hi = min(meta.Lkv, dq + p.next + 1);
+      const int nvis = row_ok ? max(0, min(k_hi - k0, kKT)) : 0;  // visible: [k0 + nlo, k0 + nvis)
+      const int nlo = min(max(dq - p.pre - k0, 0), kKT);
       // the S row in registers, in log2 units, keys past the visible range at -inf.  When
       // every row of the warp sees all 128 keys and the scale is positive, the row max is
       // taken on the raw scores (three-input max) and the scale applied once.
@@ -804,7 +822,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       tmem_ld64(tl + kColS[x], *reinterpret_cast<float(*)[64]>(&s[0]));
       tmem_ld64(tl + kColS[x] + 64, *reinterpret_cast<float(*)[64]>(&s[64]));
       const float sc = p.scale_log2;
-      const bool full = __all_sync(0xffffffffu, nvis == kKT) && sc > 0.f;
+      const bool full = __all_sync(0xffffffffu, nvis == kKT && nlo == 0) && sc > 0.f;
       float mt = -INFINITY;
       if (full) {  // four independent chains
         float e[4] = {s[0], s[1], s[2], s[3]};
@@ -813,7 +831,19 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) e[k] = fmax3(e[k], s[i + 2 * k], s[i + 2 * k + 1]);
         mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]) * sc;
-      } else {  // scaled scores, masked keys at -inf; four independent chains
+      } else if (__any_sync(0xffffffffu, nlo > 0)) {  // a band's lower edge crosses the tile
+        float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < kKT; i += 8)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int i0 = i + 2 * k, i1 = i0 + 1;
+            s[i0] = (i0 >= nlo && i0 < nvis) ? s[i0] * sc : -INFINITY;
+            s[i1] = (i1 >= nlo && i1 < nvis) ? s[i1] * sc : -INFINITY;
+            e[k] = fmax3(e[k], s[i0], s[i1]);
+          }
+        mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]);
+      } else {  // scaled scores, keys past the visible range at -inf; four independent chains
         float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int i = 0; i < kKT; i += 8)

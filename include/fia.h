@@ -7,6 +7,7 @@
  *                          KV antiquant and learnable sink, split-KV partials merged
  *                          by the RingAttentionUpdate rule
  *   fia_prefill            causal variable-length attention, TND layout
+ *   fia_prefill_ex         the same with the band mask (preTokens / nextTokens)
  *   ring_attention_update  merge of two attention partials by softmax max/sum
  *
  * Conventions shared by every call:
@@ -221,7 +222,7 @@ int fia_decode_noalloc(const void* q, fia_dtype q_dtype, const void* k_cache, co
  * cu_seqlens_q/kv  device int64 (B + 1), cu[0] = 0, non-decreasing, cu[B] = T (resp. Tkv).
  * max_seqlen_q/kv  host upper bounds of the per-sequence lengths (max_seqlen_kv <= 2^20 here).
  * D                128 in this build; Nq % Nkv == 0; max_seqlen_q must bound every Lq.
- * mask             0 (none) or 3 (rightDownCausal).
+ * mask             0 (none) or 3 (rightDownCausal); 4 (band) through fia_prefill_ex.
  * sink             device fp32 (Nq) or NULL.
  * softmax_max/sum  device fp32 (T, Nq) or NULL.
  * workspace        device, at least fia_prefill_workspace_size() bytes, 256-byte aligned.
@@ -232,6 +233,29 @@ int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, co
                 const int64_t* cu_seqlens_kv, int B, int64_t T, int64_t Tkv, int max_seqlen_q, int max_seqlen_kv,
                 int Nq, int Nkv, int D, double scale, int mask, const float* sink, void* out, float* softmax_max,
                 float* softmax_sum, void* workspace, size_t workspace_bytes, fia_stream_t stream);
+
+/* fia_prefill with the band mask (FusedInferAttentionScore sparseMode 4 with preTokens /
+ * nextTokens).  Arguments as for fia_prefill; mask may also be 4 (band), which needs options:
+ *
+ *   query i of a sequence sees key j iff
+ *     i + (Lkv - Lq) - pre_tokens <= j <= i + (Lkv - Lq) + next_tokens,
+ *   the band around the rightDownCausal diagonal (pre_tokens = large, next_tokens = 0 is
+ *   mask 3; pre_tokens = W - 1, next_tokens = 0 a causal sliding window of W keys).  Values
+ *   beyond +-2^30 are clamped; pre_tokens + next_tokens < 0 (a band that holds no key, which
+ *   the pages forbid) is FIA_ERR_PARAM_INVALID.  Rows with no key in the band get the
+ *   empty-row outputs.  Only key tiles that meet a query tile's band are read.
+ *
+ * options is read only for mask 4 (NULL there is FIA_ERR_PARAM_NULLPTR). */
+typedef struct {
+  int64_t pre_tokens;
+  int64_t next_tokens;
+} fia_prefill_options;
+
+int fia_prefill_ex(const void* q, const void* k, const void* v, fia_dtype dtype, const int64_t* cu_seqlens_q,
+                   const int64_t* cu_seqlens_kv, int B, int64_t T, int64_t Tkv, int max_seqlen_q, int max_seqlen_kv,
+                   int Nq, int Nkv, int D, double scale, int mask, const float* sink, void* out, float* softmax_max,
+                   float* softmax_sum, void* workspace, size_t workspace_bytes, fia_stream_t stream,
+                   const fia_prefill_options* options);
 
 /* ---------------------------------------------------------- ring_attention_update
  * aclnnRingAttentionUpdate ("功能说明 / 计算公式").  Per row r and head n:

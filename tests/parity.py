@@ -136,26 +136,27 @@ class DevicePrefill:
         self.sink = None if case.sink is None else torch.from_numpy(case.sink).to(device)
 
 
-def run_prefill(F, dp: DevicePrefill, causal=True, sink="case"):
+def run_prefill(F, dp: DevicePrefill, causal=True, sink="case", band=None):
     c = dp.case
     mx = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device=dp.q.device)
     sm = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device=dp.q.device)
     return F.fia_prefill(dp.q, dp.k, dp.v, dp.cu_q, dp.cu_kv, max_seqlen_q=int(c.lengths_q.max(initial=0)),
                          max_seqlen_kv=int(c.lengths_kv.max(initial=0)), num_heads=c.Nq, num_kv_heads=c.Nkv,
-                         scale=c.scale, mask=3 if causal else 0, sink=dp.sink if sink == "case" else sink,
-                         softmax_max=mx, softmax_sum=sm)
+                         scale=c.scale, mask=4 if band is not None else (3 if causal else 0),
+                         sink=dp.sink if sink == "case" else sink, softmax_max=mx, softmax_sum=sm,
+                         pre_tokens=None if band is None else band[0], next_tokens=None if band is None else band[1])
 
 
-def oracle_prefill(case: W.PrefillCase, rows=None, causal=True, sink="case", nthreads=0):
+def oracle_prefill(case: W.PrefillCase, rows=None, causal=True, sink="case", nthreads=0, band=None):
     code = {W.BF16: OR.BF16, W.FP16: OR.F16}[case.dtype]
     return OR.prefill(case.q, case.k, case.v, case.cu_q, case.cu_kv, Nq=case.Nq, Nkv=case.Nkv, D=case.D,
                       scale=case.scale, causal=causal, dtype=code, sink=case.sink if sink == "case" else sink,
-                      rows=rows, nthreads=nthreads)
+                      rows=rows, nthreads=nthreads, band=band)
 
 
-def compare_prefill(case: W.PrefillCase, out, mx, sm, rows=None, ref=None, causal=True):
+def compare_prefill(case: W.PrefillCase, out, mx, sm, rows=None, ref=None, causal=True, band=None):
     if ref is None:
-        ref = oracle_prefill(case, rows=rows, causal=causal)
+        ref = oracle_prefill(case, rows=rows, causal=causal, band=band)
     o = to_f64(out).reshape(case.T * case.Nq, case.D)
     m = to_f64(mx).reshape(-1)
     s = to_f64(sm).reshape(-1)

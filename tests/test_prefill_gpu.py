@@ -1,4 +1,5 @@
-"""GPU parity of fia_prefill (TND, causal varlen, tcgen05) against the oracle."""
+"""GPU parity of fia_prefill (TND, causal varlen, tcgen05) against the oracle, and of the
+band mask of fia_prefill_ex (FusedInferAttentionScore sparseMode 4, preTokens/nextTokens)."""
 import zlib
 
 import numpy as np
@@ -85,3 +86,63 @@ def test_prefill_scores_rising_along_the_keys(F, cuda):
     out, mx, sm = run_prefill(F, dp)
     compare_prefill(case, out, mx, sm)
     assert F.fia_device_status() == 0
+
+
+# ------------------------------------------------------------------ band (sparseMode 4)
+BAND_CASES = {
+    # name: (make_prefill_case kwargs, (pre_tokens, next_tokens)); even G runs the head-pair
+    # kernel, odd G the single-head one
+    "sliding_256_pair": (dict(Nq=8, Nkv=2, D=128, lengths=[700, 300, 129]), (255, 0)),
+    "sliding_100_odd_g": (dict(Nq=3, Nkv=1, D=128, lengths=[500, 260]), (99, 0)),
+    "both_sides": (dict(Nq=4, Nkv=2, D=128, lengths=[400, 3]), (50, 70)),
+    "diagonal_only": (dict(Nq=4, Nkv=2, D=128, lengths=[130, 257]), (0, 0)),
+    "lq_ne_lkv": (dict(Nq=4, Nkv=1, D=128, lengths=[100, 300], lengths_kv=[400, 200]), (150, 20)),
+    "previous_5_only": (dict(Nq=2, Nkv=2, D=128, lengths=[260, 40]), (5, -1)),
+    "future_only_odd_g": (dict(Nq=1, Nkv=1, D=128, lengths=[300]), (-3, 10)),
+    "fp16_sink": (dict(Nq=4, Nkv=2, D=128, lengths=[333, 129], dtype=W.FP16, sink=True), (63, 0)),
+    "sink_odd_g": (dict(Nq=3, Nkv=3, D=128, lengths=[200], sink=True), (17, 2)),
+    "many_short_seqs": (dict(Nq=2, Nkv=1, D=128, lengths=[(i * 37) % 23 for i in range(300)] + [300]), (10, 0)),
+    "wide_band_no_mask": (dict(Nq=4, Nkv=2, D=128, lengths=[77, 260], lengths_kv=[90, 260]), (1 << 40, 1 << 40)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BAND_CASES))
+def test_prefill_band(F, cuda, name):
+    kw, band = BAND_CASES[name]
+    case = W.make_prefill_case(seed=zlib.crc32(("band_" + name).encode()) % (1 << 30), **kw)
+    dp = DevicePrefill(case)
+    out, mx, sm = run_prefill(F, dp, band=band)
+    compare_prefill(case, out, mx, sm, band=band)
+    assert F.fia_device_status() == 0
+
+
+def test_prefill_band_huge_pre_is_causal(F, cuda):
+    """band(2^40, 0) is the rightDownCausal mask: the same kernels, bit for bit."""
+    case = W.make_prefill_case(Nq=8, Nkv=2, D=128, lengths=[700, 333, 50], lengths_kv=[800, 333, 20], seed=41)
+    dp = DevicePrefill(case)
+    a = run_prefill(F, dp)
+    b = run_prefill(F, dp, band=(1 << 40, 0))
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_prefill_band_full_size_sampled(F, cuda):
+    """A causal sliding window of 512 keys on the full-size prefill workload, sampled rows."""
+    case = W.causal_prefill_tnd()
+    dp = DevicePrefill(case)
+    out, mx, sm = run_prefill(F, dp, band=(511, 0))
+    rows = sample_prefill_rows(case, 1024, seed=6)
+    compare_prefill(case, out, mx, sm, rows=rows, band=(511, 0))
+    assert F.fia_device_status() == 0
+
+
+def test_prefill_band_rejects(F, cuda):
+    case = W.make_prefill_case(Nq=4, Nkv=2, D=128, lengths=[5], seed=4)
+    dp = DevicePrefill(case)
+    with pytest.raises(F.FiaError) as ei:   # a band holding no key
+        run_prefill(F, dp, band=(3, -4))
+    assert ei.value.code == 161002
+    with pytest.raises(F.FiaError) as ei:   # mask 4 without the band's options
+        F.fia_prefill(dp.q, dp.k, dp.v, dp.cu_q, dp.cu_kv, max_seqlen_q=5, max_seqlen_kv=5, num_heads=4,
+                      num_kv_heads=2, mask=4)
+    assert ei.value.code == 161001
