@@ -212,7 +212,10 @@ __device__ __forceinline__ void umma_f16_ta_w(uint32_t d_tmem, uint32_t a_tmem, 
 }
 
 // ------------------------------------------------------------------ attention
-template <int DT>
+// kBand: a band's lower edge may fall inside a key tile (pre_tokens below the longest key
+// sequence); without it the lower edge is never inside a tile and the softmax masks the
+// upper edge only.
+template <int DT, bool kBand>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -417,7 +420,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int dq = qi + (meta.Lkv - meta.Lq);
       const int k_hi = min(meta.Lkv, dq + p.next + 1);
       const int nvis = row_ok ? max(0, min(k_hi - k0, 64)) : 0;
-      const int nlo = min(max(dq - p.pre - k0, 0), 64);
+      const int nlo = kBand ? min(max(dq - p.pre - k0, 0), 64) : 0;
       float s[64];
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.s_free[sb]);
       float mt = -INFINITY;
-      if (__any_sync(0xffffffffu, nlo > 0)) {  // a band's lower edge crosses the tile
+      if (kBand && __any_sync(0xffffffffu, nlo > 0)) {  // a band's lower edge crosses the tile
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           s[c] = (c >= nlo && c < nvis) ? s[c] * p.scale_log2 : -INFINITY;
@@ -604,7 +607,7 @@ struct P2Smem {
 };
 static_assert(sizeof(P2Smem) <= 232448, "prefill shared memory exceeds the per-CTA limit");
 
-template <int DT>
+template <int DT, bool kBand>
 __global__ void __launch_bounds__(kP2Threads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -814,7 +817,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       const int dq = qi + (meta.Lkv - meta.Lq);
       const int k_hi = min(meta.Lkv, dq + p.next + 1);
       const int nvis = row_ok ? max(0, min(k_hi - k0, kKT)) : 0;  // visible: [k0 + nlo, k0 + nvis)
-      const int nlo = min(max(dq - p.pre - k0, 0), kKT);
+      const int nlo = kBand ? min(max(dq - p.pre - k0, 0), kKT) : 0;
       // the S row in registers, in log2 units, keys past the visible range at -inf.  When
       // every row of the warp sees all 128 keys and the scale is positive, the row max is
       // taken on the raw scores (three-input max) and the scale applied once.
@@ -831,7 +834,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k) e[k] = fmax3(e[k], s[i + 2 * k], s[i + 2 * k + 1]);
         mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]) * sc;
-      } else if (__any_sync(0xffffffffu, nlo > 0)) {  // a band's lower edge crosses the tile
+      } else if (kBand && __any_sync(0xffffffffu, nlo > 0)) {  // a band's lower edge crosses the tile
         float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int i = 0; i < kKT; i += 8)
@@ -994,9 +997,13 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const
   }
   e = launch_dependent(prefill_plan_kernel, 1, 1024, plan_smem, stream, p, max_key_tiles, pairs ? 2 : 1);
   if (e != cudaSuccess) return e;
+  // a query sees keys d + i - pre.. with d + i <= Lkv - 1: a lower edge inside the keys needs
+  // pre < the longest key sequence
+  const bool band = p.pre < p.max_seqlen_kv;
   if (pairs) {
     const size_t smem2 = sizeof(P2Smem);
-    auto kern = p.dtype == kBF16 ? prefill_pair_kernel<kBF16> : prefill_pair_kernel<kF16>;
+    auto kern = p.dtype == kBF16 ? (band ? prefill_pair_kernel<kBF16, true> : prefill_pair_kernel<kBF16, false>)
+                                 : (band ? prefill_pair_kernel<kF16, true> : prefill_pair_kernel<kF16, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
     if (e != cudaSuccess) return e;
     e = launch_dependent(kern, num_sms, kP2Threads, smem2, stream, tmQ, tmK, tmV, p);
@@ -1005,15 +1012,11 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const
     return cudaGetLastError();
   }
   const size_t smem = sizeof(PSmem);
-  if (p.dtype == kBF16) {
-    e = cudaFuncSetAttribute(prefill_tc_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    prefill_tc_kernel<kBF16><<<num_sms, kPThreads, smem, stream>>>(tmQ, tmK, tmV, p);
-  } else {
-    e = cudaFuncSetAttribute(prefill_tc_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    prefill_tc_kernel<kF16><<<num_sms, kPThreads, smem, stream>>>(tmQ, tmK, tmV, p);
-  }
+  auto kern = p.dtype == kBF16 ? (band ? prefill_tc_kernel<kBF16, true> : prefill_tc_kernel<kBF16, false>)
+                               : (band ? prefill_tc_kernel<kF16, true> : prefill_tc_kernel<kF16, false>);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms, kPThreads, smem, stream>>>(tmQ, tmK, tmV, p);
   trace_mark(kKernelPrefill, 1, stream);
   return cudaGetLastError();
 }

@@ -116,14 +116,18 @@ def test_prefill_band(F, cuda, name):
     assert F.fia_device_status() == 0
 
 
-def test_prefill_band_huge_pre_is_causal(F, cuda):
-    """band(2^40, 0) is the rightDownCausal mask: the same kernels, bit for bit."""
-    case = W.make_prefill_case(Nq=8, Nkv=2, D=128, lengths=[700, 333, 50], lengths_kv=[800, 333, 20], seed=41)
+@pytest.mark.parametrize("Nq", [8, 6])  # head-pair and single-head kernels
+def test_prefill_band_wide_pre_is_causal(F, cuda, Nq):
+    """band(2^40, 0) is the rightDownCausal mask (the kernels without a lower edge), and so
+    is band(max Lkv - 1, 0), which runs the kernels with a lower edge that excludes no key:
+    both bit for bit the causal result."""
+    case = W.make_prefill_case(Nq=Nq, Nkv=2, D=128, lengths=[700, 333, 50], lengths_kv=[800, 333, 20], seed=41)
     dp = DevicePrefill(case)
     a = run_prefill(F, dp)
-    b = run_prefill(F, dp, band=(1 << 40, 0))
-    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
-    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    for band in [(1 << 40, 0), (int(case.lengths_kv.max()) - 1, 0)]:
+        b = run_prefill(F, dp, band=band)
+        assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+        assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
 
 
 def test_prefill_band_full_size_sampled(F, cuda):
