@@ -194,6 +194,9 @@ static void attend_row(const double *q, const double *K, const double *V, int64_
  * mask[b * mask_stride + t], or NULL; a nonzero byte removes key t of batch b
  * from the attention (1 = masked out, 0 = attended), so a batch whose keys are
  * all masked is handled like one of length 0.
+ * pre_tokens / next_tokens: the band of R15 for the one query (i = 0, Lq = 1): key
+ * t of a batch of length L is visible iff L - 1 - pre_tokens <= t <= L - 1 + next_tokens
+ * (large values: no band).
  * rows: the (b * Nq + h) rows to compute, or NULL for all B * Nq rows; results
  * are written compactly: out[i * D + d], smax[i], ssum[i] for the i-th row.
  * Returns 0, or -1 on an argument it cannot handle. */
@@ -204,6 +207,7 @@ int oracle_decode(const void *q, int q_dtype,
                   int B, int Nq, int Nkv, int D, int block_size, int64_t kv_rows,
                   double scale, const float *aq_scale, const float *aq_offset,
                   const float *sink, const uint8_t *mask, int64_t mask_stride,
+                  int64_t pre_tokens, int64_t next_tokens,
                   const int64_t *rows, int64_t n_rows, int nthreads,
                   double *out, double *smax, double *ssum)
 {
@@ -250,6 +254,8 @@ int oracle_decode(const void *q, int q_dtype,
             int64_t n = 0;
             for (int64_t t = 0; t < L; ++t) {
                 if (mask && mask[(int64_t)b * mask_stride + t] != 0)
+                    continue;
+                if (t < L - 1 - pre_tokens || t > L - 1 + next_tokens)      /* R15 with Lq = 1 */
                     continue;
                 int64_t src;                                    /* element offset of row t */
                 if (block_table) {

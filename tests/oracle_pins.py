@@ -291,6 +291,37 @@ def pin_decode_mask_matches_sdpa(O):
     assert all(np.array_equal(x, y) for x, y in zip(asb, (out, mx, sm)))
 
 
+def pin_decode_band_is_prefill_band_of_one_query(O):
+    """Decode with a band (pre, next) over a shuffled paged cache equals the prefill oracle's
+    band (pinned against SDPA with triu/tril masks) for one query per sequence over the
+    gathered keys, and an attenMask that masks the keys outside the window."""
+    B, Nq, Nkv, D, bs = 3, 4, 2, 16, 8
+    lengths = [30, 5, 17]
+    case = W.make_decode_case(B=B, Nq=Nq, Nkv=Nkv, D=D, block_size=bs, lengths=lengths, seed=37, scale=0.45)
+    kc = case.k_cache.transpose(0, 2, 1, 3)   # (blocks, bs, Nkv, D)
+    vc = case.v_cache.transpose(0, 2, 1, 3)
+    k = np.concatenate([np.concatenate([kc[p] for p in case.block_table[b, :(L + bs - 1) // bs]])[:L]
+                        for b, L in enumerate(lengths)])
+    v = np.concatenate([np.concatenate([vc[p] for p in case.block_table[b, :(L + bs - 1) // bs]])[:L]
+                        for b, L in enumerate(lengths)])
+    cu_q = np.arange(B + 1)
+    cu_kv = np.concatenate([[0], np.cumsum(lengths)])
+    for pre, nxt in [(7, 0), (0, 0), (3, -1), (100, 0), (12, -10)]:
+        dec = O.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=Nq, Nkv=Nkv, D=D, scale=case.scale,
+                       q_dtype=OR.BF16, kv_dtype=OR.BF16, block_table=case.block_table, block_size=bs,
+                       band=(pre, nxt))
+        pf = O.prefill(case.q, k, v, cu_q, cu_kv, Nq=Nq, Nkv=Nkv, D=D, scale=case.scale, dtype=OR.BF16,
+                       band=(pre, nxt))
+        for x, y in zip(dec, pf):
+            np.testing.assert_allclose(x, y, rtol=1e-13, atol=1e-13)
+        mask = np.ones((B, 32), np.uint8)
+        for b, L in enumerate(lengths):
+            mask[b, max(0, L - 1 - pre):max(0, min(L, L + nxt))] = 0
+        msk = O.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=Nq, Nkv=Nkv, D=D, scale=case.scale,
+                       q_dtype=OR.BF16, kv_dtype=OR.BF16, block_table=case.block_table, block_size=bs, mask=mask)
+        assert all(np.array_equal(x, y) for x, y in zip(dec, msk))
+
+
 # ------------------------------------------------------------------ post-quant output
 def pin_post_quant_closed_forms(O):
     """Ties go to the even integer, values past the int8 range saturate, the offset is added."""
