@@ -44,7 +44,8 @@ class DecodeOptions(ctypes.Structure):
     _fields_ = [("kv_layout", ctypes.c_int), ("antiquant_mode", ctypes.c_int), ("softmax_lse", ctypes.c_void_p),
                 ("atten_mask", ctypes.c_void_p), ("atten_mask_stride", ctypes.c_int64),
                 ("quant_scale2", ctypes.c_void_p), ("quant_offset2", ctypes.c_void_p),
-                ("quant2_per_channel", ctypes.c_int)]
+                ("quant2_per_channel", ctypes.c_int), ("band", ctypes.c_int), ("pre_tokens", ctypes.c_int64),
+                ("next_tokens", ctypes.c_int64)]
 
 
 def _load() -> ctypes.CDLL:
@@ -159,7 +160,8 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
                workspace: Optional[torch.Tensor] = None, stream=None, kv_layout: int = KV_BNNBSD,
                antiquant_mode: int = AQ_PER_CHANNEL, softmax_lse: Optional[torch.Tensor] = None,
                atten_mask: Optional[torch.Tensor] = None, quant_scale2: Optional[torch.Tensor] = None,
-               quant_offset2: Optional[torch.Tensor] = None,
+               quant_offset2: Optional[torch.Tensor] = None, pre_tokens: Optional[int] = None,
+               next_tokens: Optional[int] = None,
                _force_ex: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
     """Paged decode attention.  q: (B, Nq, D) (any layout of that memory); k/v_cache:
     (num_blocks, Nkv, block_size, D), or with kv_layout=KV_BNBSH (num_blocks, block_size,
@@ -167,7 +169,8 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     antiquant_mode=AQ_PER_TENSOR takes scale/offset of shape (2,); softmax_lse (B, Nq)
     receives max + ln(sum).  atten_mask: (B, S) / (B, 1, S) / (B, 1, 1, S) bool, int8 or
     uint8, 1 = key masked out, S >= max_kv_len.  quant_scale2 (and quant_offset2): fp32 of
-    1 or Nq * D values; out is then int8.  Returns (out, softmax_max, softmax_sum)."""
+    1 or Nq * D values; out is then int8.  pre_tokens / next_tokens: the band around the
+    query (keys L - 1 - pre .. L - 1 + next).  Returns (out, softmax_max, softmax_sum)."""
     B, D = int(q.shape[0]), int(q.shape[-1])
     num_blocks = int(k_cache.shape[0])
     block_size = int(k_cache.shape[1] if kv_layout == KV_BNBSH else k_cache.shape[2])
@@ -200,13 +203,16 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
             num_blocks, float(scale), _ptr(antiquant_scale), _ptr(antiquant_offset), _ptr(sink), _ptr(out),
             _ptr(softmax_max), _ptr(softmax_sum), int(num_splits), _ptr(workspace),
             workspace.numel() * workspace.element_size(), _stream(stream))
+    band = pre_tokens is not None or next_tokens is not None
     plain = (kv_layout == KV_BNNBSD and antiquant_mode == AQ_PER_CHANNEL and softmax_lse is None
-             and atten_mask is None and quant_scale2 is None and quant_offset2 is None)
+             and atten_mask is None and quant_scale2 is None and quant_offset2 is None and not band)
     if plain and not _force_ex:
         _check(_lib.fia_decode(*args), "fia_decode")
     else:
         opts = DecodeOptions(int(kv_layout), int(antiquant_mode), _ptr(softmax_lse), _ptr(atten_mask), mask_stride,
-                             _ptr(quant_scale2), _ptr(quant_offset2), q2_per_channel)
+                             _ptr(quant_scale2), _ptr(quant_offset2), q2_per_channel, int(band),
+                             int(pre_tokens if pre_tokens is not None else 1 << 40),
+                             int(next_tokens if next_tokens is not None else 1 << 40))
         _check(_lib.fia_decode_ex(*args, ctypes.byref(opts)), "fia_decode_ex")
     return out, softmax_max, softmax_sum
 
@@ -214,13 +220,15 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
 def fia_decode_ex(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
                   actual_seq_lengths: torch.Tensor, *, kv_layout: int = KV_BNNBSD, antiquant_mode: int = AQ_PER_CHANNEL,
                   softmax_lse: Optional[torch.Tensor] = None, atten_mask: Optional[torch.Tensor] = None,
-                  quant_scale2: Optional[torch.Tensor] = None, quant_offset2: Optional[torch.Tensor] = None, **kw):
+                  quant_scale2: Optional[torch.Tensor] = None, quant_offset2: Optional[torch.Tensor] = None,
+                  pre_tokens: Optional[int] = None, next_tokens: Optional[int] = None, **kw):
     """fia_decode_ex: fia_decode with the decode options (KV layout, antiquant mode,
     log-sum-exp output, attenMask, int8 post-quant output); other arguments as for
     fia_decode.  Always calls the C fia_decode_ex entry point."""
     return fia_decode(q, k_cache, v_cache, block_table, actual_seq_lengths, kv_layout=kv_layout,
                       antiquant_mode=antiquant_mode, softmax_lse=softmax_lse, atten_mask=atten_mask,
-                      quant_scale2=quant_scale2, quant_offset2=quant_offset2, _force_ex=True, **kw)
+                      quant_scale2=quant_scale2, quant_offset2=quant_offset2, pre_tokens=pre_tokens,
+                      next_tokens=next_tokens, _force_ex=True, **kw)
 
 
 def fia_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,

@@ -273,6 +273,7 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   const float* qs2 = opt ? opt->quant_scale2 : nullptr;
   const float* qo2 = opt ? opt->quant_offset2 : nullptr;
   const int q2_per_channel = opt ? opt->quant2_per_channel : 0;
+  const bool windowed = opt && opt->band;
   // -- 161001: required pointers
   if (!q || !k_cache || !v_cache || !block_table || !actual_seq_lengths || !out)
     return fail(FIA_ERR_PARAM_NULLPTR, "q, k_cache, v_cache, block_table, actual_seq_lengths and out are required");
@@ -303,6 +304,16 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   if (qo2 && !qs2) return fail(FIA_ERR_PARAM_INVALID, "quant_offset2 without quant_scale2");
   if (q2_per_channel != 0 && q2_per_channel != 1)
     return fail(FIA_ERR_PARAM_INVALID, "quant2_per_channel must be 0 or 1 (got %d)", q2_per_channel);
+  // the band in keys around the query (position L - 1), clamped to +-2^30 (no length is that large)
+  constexpr int64_t kBandCap = 1LL << 30;
+  int64_t win_pre = kBandCap, win_next = kBandCap;
+  if (windowed) {
+    win_pre = std::min(std::max(opt->pre_tokens, -kBandCap), kBandCap);
+    win_next = std::min(std::max(opt->next_tokens, -kBandCap), kBandCap);
+    if (win_pre + win_next < 0)
+      return fail(FIA_ERR_PARAM_INVALID, "band with pre_tokens %lld and next_tokens %lld holds no key",
+                  (long long)opt->pre_tokens, (long long)opt->next_tokens);
+  }
   if (bt_stride < 1 || (int64_t)max_kv_len > bt_stride * block_size)
     return fail(FIA_ERR_PARAM_INVALID, "block table too narrow: max_kv_len %d > bt_stride %lld * block_size %d",
                 max_kv_len, (long long)bt_stride, block_size);
@@ -359,6 +370,9 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   p.pq_offset = qo2;
   p.pq_stride = q2_per_channel;
   p.partials_only = qs2 != nullptr;
+  p.windowed = windowed ? 1 : 0;
+  p.win_pre = (int)win_pre;
+  p.win_next = (int)win_next;
   p.ws = fia::decode_workspace_carve(workspace, B, Nkv, G, D, plan.max_items);
   p.status = d->status;
   if (aq_mode == FIA_AQ_PER_TENSOR) {  // the kernels read the per-channel form

@@ -76,6 +76,7 @@ struct Cfg {
 struct __align__(16) StageMeta {
   int b, hkv, tok0, n;  // tile start token and valid tokens
   int item, first, last, nch;  // nch: items of this (b, kv head) segment
+  int nlo, pad0, pad1, pad2;   // tokens below tok0 + nlo lie before the window (masked)
 };
 
 template <int KVT, int D, int GP>
@@ -153,24 +154,30 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   }
   // When B <= kPlanSmemB: sbase[B + 1] item offsets, then fpos[B] and tpos[B], the
   // first execution-order slots of each batch's full chunks and of its last chunks, then
-  // slen[B], the clamped lengths (read from global memory once, not in every pass).
+  // send[B] and slo[B], the end and first key of each batch's span (its clamped length,
+  // windowed by a band; read from global memory once, not in every pass).
   extern __shared__ int sbase[];
   __shared__ int warp_tot[32];
   __shared__ int carry;
   __shared__ int bucket[kPlanMaxTiles + 1];  // items per size (tiles), then the next free slot
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool in_smem = p.B <= kPlanSmemB;
-  int* slen = sbase + 3 * p.B + 1;
+  int* send = sbase + 3 * p.B + 1;
+  int* slo = send + p.B;
   if (tid == 0) carry = 0;
   __syncthreads();
   const int C = p.chunk_tokens;
   for (int b0 = 0; b0 < p.B; b0 += 1024) {
     const int b = b0 + tid;
     int nch = 0;
+    DecodeSpan sp{0, 0, 0};
     if (b < p.B) {
-      const int L = clamp_len(p, b, true);
-      if (in_smem) slen[b] = L;
-      nch = (L + C - 1) / C;
+      sp = decode_span(p, clamp_len(p, b, true));
+      if (in_smem) {
+        send[b] = sp.end;
+        slo[b] = sp.lo;
+      }
+      nch = span_chunks(sp, C);
       if (nch == 0 && !p.partials_only) write_empty_batch(p, b);
     }
     const int cnt = nch * p.Nkv;
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
       if (!in_smem)  // large batch counts: each thread lists its own batch's items
         for (int h = 0; h < p.Nkv; ++h)
           for (int j = 0; j < nch; ++j)
-            p.ws.items[base + h * nch + j] = make_int4(b, h, (nch << 16) | j, min(clamp_len(p, b, false), (j + 1) * C));
+            p.ws.items[base + h * nch + j] = span_item(sp, C, b, h, nch, j);
     }
     __syncthreads();
     if (tid == 1023) carry = base + cnt;
@@ -208,7 +215,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     // Execution order, longest first (a persistent CTA that takes a long item last
     // would finish late): a counting sort of the items by their number of tiles.
     // Full chunks all have kt = C / 128 tiles; the last chunk of a batch has
-    // ceil((L - (nch - 1) C) / 128).  Slots inside a size class are claimed in any
+    // ceil((end - base - (nch - 1) C) / 128) for its span [base, end).  Slots inside a size class are claimed in any
     // order, which changes only the order in which CTAs pick up the items.
     int* fpos = sbase + p.B + 1;
     int* tpos = fpos + p.B;
@@ -219,7 +226,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     for (int b = tid; b < p.B; b += blockDim.x) {
       const int nch = (sbase[b + 1] - sbase[b]) / p.Nkv;
       if (nch == 0) continue;
-      const int last = slen[b] - (nch - 1) * C;
+      const int last = send[b] - (slo[b] & ~(kDecodeTileTC - 1)) - (nch - 1) * C;  // tokens of the last chunk
       atomicAdd(&bucket[kt], (nch - 1) * p.Nkv);
       atomicAdd(&bucket[min((last + kDecodeTileTC - 1) / kDecodeTileTC, kPlanMaxTiles)], p.Nkv);
     }
@@ -236,7 +243,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     for (int b = tid; b < p.B; b += blockDim.x) {
       const int nch = (sbase[b + 1] - sbase[b]) / p.Nkv;
       if (nch == 0) continue;
-      const int last = slen[b] - (nch - 1) * C;
+      const int last = send[b] - (slo[b] & ~(kDecodeTileTC - 1)) - (nch - 1) * C;
       fpos[b] = atomicAdd(&bucket[kt], (nch - 1) * p.Nkv);
       tpos[b] = atomicAdd(&bucket[min((last + kDecodeTileTC - 1) / kDecodeTileTC, kPlanMaxTiles)], p.Nkv);
     }
@@ -251,7 +258,8 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
       const int b = lo, r = i - sbase[b];
       const int nch = (sbase[b + 1] - sbase[b]) / p.Nkv;
       const int h = r / nch, j = r - h * nch;
-      p.ws.items[i] = make_int4(b, h, (nch << 16) | j, min(slen[b], (j + 1) * C));
+      const DecodeSpan sp{slo[b], send[b], slo[b] & ~(kDecodeTileTC - 1)};
+      p.ws.items[i] = span_item(sp, C, b, h, nch, j);
       p.ws.order[j < nch - 1 ? fpos[b] + h * (nch - 1) + j : tpos[b] + h] = i;
     }
   } else {
@@ -311,10 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int4 desc;
       const int item = queue.pop(p, lane, &desc);
       if (item < 0) break;
-      const DecodeItem it = decode_item(desc, p.chunk_tokens);
+      const DecodeItem it = decode_item(desc);
       const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
+      const int t0 = t_begin & ~(kTT - 1);  // the first tile (t_begin is aligned but for a window)
       const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
-      for (int tok0 = t_begin; tok0 < t_end; tok0 += kTT) {
+      for (int tok0 = t0; tok0 < t_end; tok0 += kTT) {
         const int n = min(kTT, t_end - tok0);
         const int npieces = (n + box_rows - 1) / box_rows;
         int32_t blk = 0;
@@ -325,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!valid) raise_status(p.status, kStatusBadBlockIndex);
         }
         const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-        const bool first = tok0 == t_begin;
+        const bool first = tok0 == t0;
         uint32_t bytes = 2u * piece_bytes * __popc(vmask);
         if (first) bytes += (uint32_t)(G * D * 2);
         if (!mbar_wait(&sm.empty[stage], phase ^ 1u, p.status)) { ok = false; break; }
@@ -333,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           StageMeta& m = sm.meta[stage];
           m.b = b; m.hkv = hkv; m.tok0 = tok0; m.n = n;
           m.item = item; m.first = first; m.last = (tok0 + kTT >= t_end); m.nch = it.nch;
+          m.nlo = max(t_begin - tok0, 0);
           mbar_arrive_expect_tx(&sm.full[stage], bytes);
         }
         __syncwarp();
@@ -488,7 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < GP; ++i)
           if (i < cnt)
-            sm.s[gh + i][t] = (t < meta.n && !key_masked(p, meta.b, meta.tok0 + t)) ? v[i] * p.scale_log2 : -INFINITY;
+            sm.s[gh + i][t] = (t < meta.n && t >= meta.nlo && !key_masked(p, meta.b, meta.tok0 + t))
+                                  ? v[i] * p.scale_log2 : -INFINITY;
       }
     }
     named_bar_sync(kBarConsumers, kDecodeConsumers);
@@ -621,7 +632,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   extern __shared__ float2 ml[];  // [G][nch]: (max, sum), then (weight, -) per partial
   const int b = blockIdx.x / p.Nkv, hkv = blockIdx.x % p.Nkv;
   const int C = p.chunk_tokens;
-  const int nch = (clamp_len(p, b, false) + C - 1) / C;
+  const int nch = span_chunks(decode_span(p, clamp_len(p, b, false)), C);
   if (nch <= 1 && !p.partials_only) return;
   const int G = p.G, D = p.D, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int first = p.ws.seg_base[b] + hkv * nch;
@@ -860,10 +871,10 @@ cudaError_t launch_lse(const float* mx, const float* sm, float* lse, int64_t n, 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream) {
   trace_mark(kKernelDecodePlan, 0, stream);
-  const size_t plan_smem = p.B <= kPlanSmemB ? sizeof(int) * (size_t)(4 * p.B + 1) : 0;
+  const size_t plan_smem = p.B <= kPlanSmemB ? sizeof(int) * (size_t)(5 * p.B + 1) : 0;
   if (plan_smem > 48 * 1024) {
     cudaError_t e0 = cudaFuncSetAttribute(decode_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)(sizeof(int) * (4 * kPlanSmemB + 1)));
+                                          (int)(sizeof(int) * (5 * kPlanSmemB + 1)));
     if (e0 != cudaSuccess) return e0;
   }
   const bool i8tc = !tmQ && decode_uses_i8tc(p.kv_dtype, p.D);

@@ -22,21 +22,46 @@ __device__ __forceinline__ KvCoord kv_coord(const DecodeParams& p, int32_t blk, 
   return c;
 }
 
-// Work item {b, kv head, (chunk count of the segment) << 16 | chunk index, last token + 1};
-// the first token is chunk index * chunk_tokens.
+// Work item {b, kv head | (chunk count of the segment) << 16, first token, last token + 1}.
+// A segment's chunks start at its span's base, a multiple of 128 tokens, so the tiles of
+// every chunk are aligned; the first chunk starts at the span's first key (which the
+// producer rounds down to its tile, masking the keys below it).
 struct DecodeItem {
-  int b, hkv, j, nch, t_begin, t_end;
+  int b, hkv, nch, t_begin, t_end;
 };
 
-__device__ __forceinline__ DecodeItem decode_item(int4 d, int chunk_tokens) {
+__device__ __forceinline__ DecodeItem decode_item(int4 d) {
   DecodeItem it;
   it.b = d.x;
-  it.hkv = d.y;
-  it.j = d.z & 0xffff;
-  it.nch = (unsigned)d.z >> 16;
-  it.t_begin = it.j * chunk_tokens;
+  it.hkv = d.y & 0xffff;
+  it.nch = (unsigned)d.y >> 16;
+  it.t_begin = d.z;
   it.t_end = d.w;
   return it;
+}
+
+// The keys [lo, end) the query of a batch of length L sees, and base = lo rounded down to a
+// 128-token tile, where the batch's chunks start: [0, L) without a window; with the band
+// (FusedInferAttentionScore preTokens / nextTokens, one query at position L - 1) keys
+// L - 1 - win_pre .. L - 1 + win_next.  An empty window is [0, 0).
+struct DecodeSpan {
+  int lo, end, base;
+};
+__device__ __forceinline__ DecodeSpan decode_span(const DecodeParams& p, int L) {
+  DecodeSpan s{0, L, 0};
+  if (p.windowed) {
+    s.lo = max(L - 1 - p.win_pre, 0);
+    s.end = min(L, L + p.win_next);
+    if (s.end <= s.lo) s.lo = s.end = 0;
+    s.base = s.lo & ~(kDecodeTileTC - 1);
+  }
+  return s;
+}
+// chunks of a span
+__device__ __forceinline__ int span_chunks(const DecodeSpan& s, int C) { return (s.end - s.base + C - 1) / C; }
+// item j of a span: first and last + 1 token
+__device__ __forceinline__ int4 span_item(const DecodeSpan& s, int C, int b, int hkv, int nch, int j) {
+  return make_int4(b, hkv | (nch << 16), j == 0 ? s.lo : s.base + j * C, min(s.end, s.base + (j + 1) * C));
 }
 
 // Work items for the producer warp of a persistent CTA.  Slots are claimed from the

@@ -66,7 +66,7 @@ constexpr int kPBytes = kNP * kT * 2;
 struct __align__(16) I8Meta {
   int b, hkv, n, item;
   int first, last, qbuf, nch;
-  int tok0, pad0, pad1, pad2;  // tok0: the tile's first token
+  int tok0, nlo, pad1, pad2;  // tok0: the tile's first token; tokens below tok0 + nlo are masked
 };
 
 constexpr int kMetaRing = 4;  // tile descriptors in flight between the K converters, MMA and softmax warps
@@ -210,8 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int4 desc;
       const int item = queue.pop(p, lane, &desc);
       if (item < 0) break;
-      const DecodeItem it = decode_item(desc, p.chunk_tokens);
+      const DecodeItem it = decode_item(desc);
       const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
+      const int t0 = t_begin & ~(kT - 1);  // the first tile (t_begin is aligned but for a window)
       const int qb = local_item & 1;
       if (!mbar_wait(&sm.q_empty[qb], ((local_item >> 1) & 1) ^ 1u, p.status)) { ok = false; break; }
       if (lane == 0) {
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(sm.kn[qb], src + kI8QBytes, kI8QBlockBytes - kI8QBytes, &sm.q_full[qb]);
       }
       const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
-      for (int tok0 = t_begin; tok0 < t_end; tok0 += kT, ++j) {
+      for (int tok0 = t0; tok0 < t_end; tok0 += kT, ++j) {
         const int st = j % kStages;
         const uint32_t ph = (uint32_t)(j / kStages) & 1u;
         const int n = min(kT, t_end - tok0);
@@ -239,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           I8Meta& m = sm.meta[st];
           m.b = b; m.hkv = hkv; m.n = n; m.item = item;
-          m.first = (tok0 == t_begin); m.last = (tok0 + kT >= t_end); m.qbuf = qb; m.nch = it.nch; m.tok0 = tok0;
+          m.first = (tok0 == t0); m.last = (tok0 + kT >= t_end); m.qbuf = qb; m.nch = it.nch; m.tok0 = tok0;
+          m.nlo = max(t_begin - tok0, 0);
           if (bytes) mbar_arrive_expect_tx(&sm.kv_full[st], bytes);
           else mbar_arrive(&sm.kv_full[st]);
         }
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sm.kv[st][0] + off, &tmK, kc.x0, kc.row, &sm.kv_full[st]);
           tma_load_2d(sm.kv[st][1] + off, &tmV, kc.x0, kc.row, &sm.kv_full[st]);
         }
-        if (tok0 == t_begin) queue.prefetch(p, lane);
+        if (tok0 == t0) queue.prefetch(p, lane);
       }
       ++local_item;
     }
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float s[GH];  // scores of this group's heads
       tmem_ld_scores_part<GH>(tq + kColS + sb * kNS, h0, s);
-      const bool valid = r < meta.n && !key_masked(p, meta.b, meta.tok0 + r);
+      const bool valid = r < meta.n && r >= meta.nlo && !key_masked(p, meta.b, meta.tok0 + r);
       float x[GH];
       const float2* kn = sm.kn[meta.qbuf] + h0;  // {kq, nq} of this group's heads (decode_i8.cuh)
       bool above = false;  // a score of this thread exceeds its head's reference by kLazyMax

@@ -53,7 +53,8 @@ struct TcCfg {
 struct __align__(16) TileMeta {
   int b, hkv, tok0, n;
   int item, first, last, qbuf;
-  int nch, pad0, pad1, pad2;  // nch: items of this (b, kv head) segment
+  int nch, nlo, pad1, pad2;  // nch: items of this (b, kv head) segment; tokens tok0 .. tok0 + nlo - 1
+                             // lie before the window and are masked
 };
 
 template <int D>
@@ -136,8 +137,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       int4 desc;
       const int item = queue.pop(p, lane, &desc);
       if (item < 0) break;
-      const DecodeItem it = decode_item(desc, p.chunk_tokens);
+      const DecodeItem it = decode_item(desc);
       const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
+      const int t0 = t_begin & ~(kT - 1);  // the first tile (t_begin is aligned but for a window)
       const int qb = local_item & 1;
       if (!mbar_wait(&sm.q_empty[qb], ((local_item >> 1) & 1) ^ 1u, p.status)) { ok = false; break; }
       if (lane == 0) {
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           tma_load_2d(sm.q[qb] + bx * (kNP * 128), &tmQ, bx * 64, row, &sm.q_full[qb]);
       }
       const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
-      for (int tok0 = t_begin; tok0 < t_end; tok0 += kT, ++j) {
+      for (int tok0 = t0; tok0 < t_end; tok0 += kT, ++j) {
         const int st = j % C::kStages;
         const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
         const int n = min(kT, t_end - tok0);
@@ -165,8 +167,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         if (lane == 0) {
           TileMeta& m = sm.meta[st];
           m.b = b; m.hkv = hkv; m.tok0 = tok0; m.n = n;
-          m.item = item; m.first = (tok0 == t_begin); m.last = (tok0 + kT >= t_end); m.qbuf = qb;
-          m.nch = it.nch;
+          m.item = item; m.first = (tok0 == t0); m.last = (tok0 + kT >= t_end); m.qbuf = qb;
+          m.nch = it.nch; m.nlo = max(t_begin - tok0, 0);
           if (bytes) mbar_arrive_expect_tx(&sm.kv_full[st], bytes);
           else mbar_arrive(&sm.kv_full[st]);
         }
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             tma_load_2d(sm.kv[st][1] + off, &tmV, kc.x0 + bx * 64, kc.row, &sm.kv_full[st]);
           }
         }
-        if (tok0 == t_begin) queue.prefetch(p, lane);
+        if (tok0 == t0) queue.prefetch(p, lane);
       }
       ++local_item;
     }
@@ -391,7 +393,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           l_part[g] = 0.f;
         }
       }
-      const bool valid = r < meta.n && !key_masked(p, meta.b, meta.tok0 + r);
+      const bool valid = r < meta.n && r >= meta.nlo && !key_masked(p, meta.b, meta.tok0 + r);
       // per-head maximum over the tile's tokens: a warp reduction per head, then across
       // the 4 lane quadrants through shared memory
       float x[GH], mx[GH];

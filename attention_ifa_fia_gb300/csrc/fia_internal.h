@@ -45,7 +45,7 @@ struct DecodeWorkspace {
   int* counter;     // dynamic work counter (reset by the plan kernel)
   int* n_items;     // number of work items written by the plan kernel
   int* seg_base;    // (B) first item of batch b
-  int4* items;      // (max_items) {b, hkv, nch << 16 | chunk, last token + 1}
+  int4* items;      // (max_items) {b, hkv | nch << 16, first token, last token + 1}
   int* order;       // (max_items) execution order: order[k] is the k-th item to be claimed
   float* part_o;    // (max_items, G, D) normalised partial outputs
   float2* part_ml;  // (max_items, G) {max (log2 units), sum}
@@ -85,6 +85,9 @@ struct DecodeParams {
   const float* pq_offset;  // or null
   int pq_stride;           // 0: one value for the tensor; 1: one per channel
   int partials_only;
+  // band of the one query (windowed != 0): batch b of length L sees keys
+  // L - 1 - win_pre .. L - 1 + win_next (both within [-2^30, 2^30], win_pre + win_next >= 0)
+  int windowed, win_pre, win_next;
   DecodeWorkspace ws;
   unsigned int* status;  // device status word
 };

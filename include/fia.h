@@ -161,10 +161,17 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
  *                           c = h * D + d with quant2_per_channel = 1 (Nq * D values), c = 0
  *                           with quant2_per_channel = 0 (one value).
  * options->quant_offset2    device fp32, as many values as quant_scale2, or NULL (zero).
+ * options->band             nonzero: FusedInferAttentionScore's band (sparseMode 4) for the one
+ *                           query, at position L - 1 of a batch of length L: keys
+ *                           L - 1 - pre_tokens .. L - 1 + next_tokens are visible (a sliding
+ *                           window of W keys is pre_tokens = W - 1, next_tokens = 0).  Only
+ *                           the window's tiles are read.  Values beyond +-2^30 are clamped;
+ *                           pre_tokens + next_tokens < 0 is FIA_ERR_PARAM_INVALID.  A batch
+ *                           with no key in the window gets the empty-row outputs.
  * options == NULL behaves as fia_decode.  The workspace is fia_decode_workspace_size()
  * bytes, as for fia_decode.  Errors: an unknown layout or mode, the per-tensor mode
  * without int8 KV, a mask row shorter than max_kv_len, quant_offset2 without
- * quant_scale2, or quant2_per_channel outside {0, 1} is FIA_ERR_PARAM_INVALID. */
+ * quant_scale2, quant2_per_channel outside {0, 1}, or an empty band is FIA_ERR_PARAM_INVALID. */
 typedef enum { FIA_KV_BNNBSD = 0, FIA_KV_BNBSH = 1 } fia_kv_layout;
 typedef enum { FIA_AQ_PER_CHANNEL = 0, FIA_AQ_PER_TENSOR = 1 } fia_antiquant_mode;
 typedef struct {
@@ -176,6 +183,9 @@ typedef struct {
   const float* quant_scale2;   /* device fp32, 1 or Nq * D values, or NULL (16-bit out) */
   const float* quant_offset2;  /* device fp32, as quant_scale2, or NULL */
   int quant2_per_channel;      /* 0: one value; 1: Nq * D values */
+  int band;                    /* nonzero: keys L-1-pre_tokens .. L-1+next_tokens only */
+  int64_t pre_tokens;
+  int64_t next_tokens;
 } fia_decode_options;
 
 int fia_decode_ex(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache, fia_dtype kv_dtype,

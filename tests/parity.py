@@ -86,13 +86,13 @@ def run_decode(F, dd: DeviceDecode, num_splits=0, sink="case", max_kv_len=None, 
     return out, mx, sm
 
 
-def oracle_decode(case: W.DecodeCase, rows=None, nthreads=0, sink="case", mask=None):
+def oracle_decode(case: W.DecodeCase, rows=None, nthreads=0, sink="case", mask=None, band=None):
     code = {W.BF16: OR.BF16, W.FP16: OR.F16}
     kvc = OR.I8 if case.kv_dtype == W.INT8 else code[case.kv_dtype]
     return OR.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=case.Nq, Nkv=case.Nkv, D=case.D,
                      scale=case.scale, q_dtype=code[case.dtype], kv_dtype=kvc, block_table=case.block_table,
                      block_size=case.block_size, aq_scale=case.aq_scale, aq_offset=case.aq_offset,
-                     sink=case.sink if sink == "case" else sink, mask=mask, rows=rows, nthreads=nthreads)
+                     sink=case.sink if sink == "case" else sink, mask=mask, band=band, rows=rows, nthreads=nthreads)
 
 
 def compare_decode(case: W.DecodeCase, out, mx, sm, rows=None, ref=None):

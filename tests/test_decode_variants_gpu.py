@@ -268,3 +268,68 @@ def test_post_quant_ties_and_saturation_exact(F, cuda, D, num_splits):
         if s2 == 4.0:
             assert np.any(code_ref == 127) and np.any(code_ref == -128)
     assert F.fia_device_status() == 0
+
+
+# ------------------------------------------------------------------ band window (one query)
+WINDOW_CASES = {
+    "bf16_d128_g4": dict(B=4, Nq=8, Nkv=2, D=128, block_size=128, lengths=[700, 129, 1000, 3]),
+    "fp16_d64_g8_sink": dict(B=3, Nq=8, Nkv=1, D=64, block_size=64, dtype=W.FP16, lengths=[450, 31, 260],
+                             sink=True),
+    "int8_d128_g8": dict(B=3, Nq=16, Nkv=2, D=128, block_size=128, kv_dtype=W.INT8, lengths=[900, 130, 600]),
+    "int8_d64_g2": dict(B=3, Nq=4, Nkv=2, D=64, block_size=32, kv_dtype=W.INT8, lengths=[300, 65, 190]),
+}
+WINDOWS = [(255, 0), (100, 0), (0, 0), (1000, -5), (7, -3), (130, 3)]
+
+
+@pytest.mark.parametrize("num_splits", [0, 3])
+@pytest.mark.parametrize("name", sorted(WINDOW_CASES))
+def test_decode_band_window(F, cuda, name, num_splits):
+    """Keys L - 1 - pre .. L - 1 + next: windows that start inside a tile, end before the
+    last key, hold one key, or cover a whole short batch; chunked windows (splits 3)."""
+    case = _case("window_" + name, **WINDOW_CASES[name])
+    dd = DeviceDecode(case)
+    for pre, nxt in WINDOWS:
+        out, mx, sm = _run(F, dd, num_splits, pre_tokens=pre, next_tokens=nxt)
+        compare_decode(case, out, mx, sm, ref=oracle_decode(case, band=(pre, nxt)))
+    # a band wider than every sequence is no band, bit for bit
+    out, mx, sm = _run(F, dd, num_splits, pre_tokens=1 << 40, next_tokens=1 << 40)
+    base = run_decode(F, dd, num_splits=num_splits)
+    assert torch.equal(out.view(torch.int16), base[0].view(torch.int16))
+    assert torch.equal(mx, base[1]) and torch.equal(sm, base[2])
+    assert F.fia_device_status() == 0
+
+
+def test_decode_band_window_with_mask_and_int8_out(F, cuda):
+    """The window composes with the attenMask and with the int8 output."""
+    case = _case("window_mix", B=3, Nq=8, Nkv=2, D=128, block_size=64, lengths=[600, 200, 90])
+    dd = DeviceDecode(case)
+    S = case.max_len
+    m = np.random.default_rng(5).random((case.B, S)) < 0.25
+    mask = torch.from_numpy(m).cuda()
+    out, mx, sm = _run(F, dd, 2, pre_tokens=300, next_tokens=0, atten_mask=mask)
+    ref = oracle_decode(case, band=(300, 0), mask=m.astype(np.uint8))
+    compare_decode(case, out, mx, sm, ref=ref)
+    s2 = np.array([40.0 / max(float(np.abs(ref[0]).max()), 1e-3)], np.float32)
+    y, _ = OR.post_quant(ref[0].reshape(case.B, -1), s2, None)
+    code, _, _ = _run(F, dd, 2, pre_tokens=300, next_tokens=0, atten_mask=mask, quant_scale2=torch.from_numpy(s2).cuda())
+    C = case.Nq * case.D
+    _check_codes(code.cpu().numpy().reshape(-1, C), y.reshape(-1, C), ref[0].reshape(-1, C),
+                 np.broadcast_to(s2.astype(np.float64), (C,)), *OUT_TOL[case.dtype])
+    assert F.fia_device_status() == 0
+
+
+def test_decode_band_window_full_size_sampled(F, cuda):
+    """A window of 1024 keys on the full-size bf16 GQA decode workload, sampled rows."""
+    case = W.bf16_gqa_decode()
+    dd = DeviceDecode(case)
+    out, mx, sm = _run(F, dd, 0, pre_tokens=1023, next_tokens=0)
+    rows = np.random.default_rng(9).choice(case.B * case.Nq, 96, replace=False)
+    compare_decode(case, out, mx, sm, rows=rows, ref=oracle_decode(case, rows=rows, band=(1023, 0)))
+    assert F.fia_device_status() == 0
+
+
+def test_decode_band_rejects_empty_band(F, cuda):
+    case = _case("window_bad", B=1, Nq=2, Nkv=1, D=64, block_size=16, lengths=[20])
+    dd = DeviceDecode(case)
+    with pytest.raises(F.FiaError):
+        _run(F, dd, pre_tokens=2, next_tokens=-3)
