@@ -147,7 +147,9 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int QT, int GP>
+// kKeyMask: an attenMask or a band window removes keys inside the tiles (the softmax tests
+// each token against them); without it a tile's first n tokens are its keys.
+template <int QT, int GP, bool kKeyMask>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_i8tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const DecodeParams p, const int box_rows) {
@@ -450,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float s[GH];  // scores of this group's heads
       tmem_ld_scores_part<GH>(tq + kColS + sb * kNS, h0, s);
-      const bool valid = r < meta.n && r >= meta.nlo && !key_masked(p, meta.b, meta.tok0 + r);
+      const bool valid = r < meta.n && (!kKeyMask || (r >= meta.nlo && !key_masked(p, meta.b, meta.tok0 + r)));
       float x[GH];
       const float2* kn = sm.kn[meta.qbuf] + h0;  // {kq, nq} of this group's heads (decode_i8.cuh)
       bool above = false;  // a score of this thread exceeds its head's reference by kLazyMax
@@ -606,7 +608,7 @@ template <int QT, int GP>
 cudaError_t launch_i8(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows, int grid,
                       cudaStream_t stream) {
   const size_t smem = sizeof(I8Smem) + 1024;
-  auto kern = decode_i8tc_kernel<QT, GP>;
+  auto kern = (p.atten_mask || p.windowed) ? decode_i8tc_kernel<QT, GP, true> : decode_i8tc_kernel<QT, GP, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);

@@ -82,7 +82,9 @@ __device__ __forceinline__ uint32_t p_offset(int g, int t) {
   return slab * (kNP * 128) + swz(off, 7);
 }
 
-template <int D, int DT, int GP>
+// kKeyMask: an attenMask or a band window removes keys inside the tiles (the softmax tests
+// each token against them); without it a tile's first n tokens are its keys.
+template <int D, int DT, int GP, bool kKeyMask>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmQ, const DecodeParams p, const int box_rows) {
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           l_part[g] = 0.f;
         }
       }
-      const bool valid = r < meta.n && r >= meta.nlo && !key_masked(p, meta.b, meta.tok0 + r);
+      const bool valid = r < meta.n && (!kKeyMask || (r >= meta.nlo && !key_masked(p, meta.b, meta.tok0 + r)));
       // per-head maximum over the tile's tokens: a warp reduction per head, then across
       // the 4 lane quadrants through shared memory
       float x[GH], mx[GH];
@@ -472,7 +474,7 @@ template <int D, int DT, int GP>
 cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
                       int box_rows, int grid, cudaStream_t stream) {
   const size_t smem = sizeof(TcSmem<D>) + 1024;
-  auto kern = decode_tc_kernel<D, DT, GP>;
+  auto kern = (p.atten_mask || p.windowed) ? decode_tc_kernel<D, DT, GP, true> : decode_tc_kernel<D, DT, GP, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);
