@@ -36,7 +36,9 @@ class FiaError(RuntimeError):
 
 class PrefillOptions(ctypes.Structure):
     """fia_prefill_options of include/fia.h."""
-    _fields_ = [("pre_tokens", ctypes.c_int64), ("next_tokens", ctypes.c_int64)]
+    _fields_ = [("pre_tokens", ctypes.c_int64), ("next_tokens", ctypes.c_int64), ("block_table", ctypes.c_void_p),
+                ("bt_stride", ctypes.c_int64), ("seq_lens_kv", ctypes.c_void_p), ("block_size", ctypes.c_int),
+                ("num_blocks", ctypes.c_int64), ("kv_layout", ctypes.c_int)]
 
 
 class DecodeOptions(ctypes.Structure):
@@ -268,13 +270,17 @@ def fia_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q:
                 num_kv_heads: int = 0, scale: Optional[float] = None, mask: int = 3, sink=None,
                 out: Optional[torch.Tensor] = None, softmax_max=None, softmax_sum=None,
                 workspace: Optional[torch.Tensor] = None, stream=None, pre_tokens: Optional[int] = None,
-                next_tokens: Optional[int] = None):
+                next_tokens: Optional[int] = None, block_table: Optional[torch.Tensor] = None,
+                seq_lens_kv: Optional[torch.Tensor] = None, kv_layout: int = KV_BNNBSD):
     """Prefill attention, TND.  q: (T, Nq, D); k, v: (Tkv, Nkv, D); cu_seqlens int64 (B + 1,)
     on the device.  mask 3 = rightDownCausal, 0 = none, 4 = band (pre_tokens, next_tokens
-    around the rightDownCausal diagonal, through fia_prefill_ex).  Returns (out, softmax_max,
-    softmax_sum)."""
+    around the rightDownCausal diagonal, through fia_prefill_ex).  With block_table (int32
+    (B, width)) and seq_lens_kv (int64 (B,)), k and v are paged pools (num_blocks, Nkv,
+    block_size, D), or with kv_layout=KV_BNBSH (num_blocks, block_size, Nkv * D), and
+    cu_seqlens_kv may be None.  Returns (out, softmax_max, softmax_sum)."""
     T, D = int(q.shape[0]), int(q.shape[-1])
-    Tkv = int(k.shape[0])
+    paged = block_table is not None
+    Tkv = 0 if paged else int(k.shape[0])
     B = int(cu_seqlens_q.shape[0]) - 1
     nkv = num_kv_heads if num_kv_heads else num_heads
     if scale is None:
@@ -288,11 +294,14 @@ def fia_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q:
             int(max_seqlen_q), int(max_seqlen_kv), num_heads, nkv, D, float(scale), int(mask), _ptr(sink), _ptr(out),
             _ptr(softmax_max), _ptr(softmax_sum), _ptr(workspace), workspace.numel() * workspace.element_size(),
             _stream(stream))
-    if pre_tokens is None and next_tokens is None:
+    if pre_tokens is None and next_tokens is None and not paged:
         _check(_lib.fia_prefill(*args), "fia_prefill")
     else:
+        bs = (int(k.shape[1]) if kv_layout == KV_BNBSH else int(k.shape[2])) if paged else 0
         opts = PrefillOptions(int(pre_tokens if pre_tokens is not None else 1 << 40),
-                              int(next_tokens if next_tokens is not None else 1 << 40))
+                              int(next_tokens if next_tokens is not None else 1 << 40),
+                              _ptr(block_table), int(block_table.shape[1]) if paged else 0, _ptr(seq_lens_kv), bs,
+                              int(k.shape[0]) if paged else 0, int(kv_layout))
         _check(_lib.fia_prefill_ex(*args, ctypes.byref(opts)), "fia_prefill_ex")
     return out, softmax_max, softmax_sum
 

@@ -524,6 +524,23 @@ int make_tmap_thd(CUtensorMap* m, const void* base, int dtype, uint64_t D, uint6
   return FIA_SUCCESS;
 }
 
+// A paged K or V pool as a 3-D tensor (cols channels, block_size rows, zs blocks [x kv
+// heads]) read in boxes of 64 channels x 128 rows x 1 block: the box lands in shared
+// memory as the (64, 1, 128) box of the TND map does, 128 rows of 128 bytes.
+int make_tmap_paged(CUtensorMap* m, const void* base, int dtype, uint64_t cols, int block_size, uint64_t zs) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FIA_ERR_RUNTIME, "cuTensorMapEncodeTiled is not available from the driver");
+  const CUtensorMapDataType t = dtype == fia::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[3] = {cols, (cuuint64_t)block_size, zs};
+  cuuint64_t strides[2] = {cols * 2, (cuuint64_t)block_size * cols * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FIA_ERR_RUNTIME, "cuTensorMapEncodeTiled (paged 3-D) failed (%d)", (int)r);
+  return FIA_SUCCESS;
+}
+
 int check_prefill_shape(int B, int Nq, int* Nkv, int D, int max_seqlen_q) {
   if (B < 0 || B > 65536) return fail(FIA_ERR_PARAM_INVALID, "B = %d outside [0, 65536]", B);
   if (Nq < 1 || Nq > 256) return fail(FIA_ERR_PARAM_INVALID, "Nq = %d outside [1, 256]", Nq);
@@ -553,8 +570,10 @@ static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype d
                         int max_seqlen_kv, int Nq, int Nkv, int D, double scale, int mask, const float* sink,
                         void* out, float* softmax_max, float* softmax_sum, void* workspace, size_t workspace_bytes,
                         fia_stream_t stream, const fia_prefill_options* opt) {
-  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_kv || !out)
-    return fail(FIA_ERR_PARAM_NULLPTR, "q, k, v, cu_seqlens_q, cu_seqlens_kv and out are required");
+  const bool paged = opt && opt->block_table;
+  if (!q || !k || !v || !cu_seqlens_q || !out || (!paged && !cu_seqlens_kv))
+    return fail(FIA_ERR_PARAM_NULLPTR, "q, k, v, cu_seqlens_q, cu_seqlens_kv (unless paged) and out are required");
+  if (paged && !opt->seq_lens_kv) return fail(FIA_ERR_PARAM_NULLPTR, "paged keys need seq_lens_kv");
   if (!workspace) return fail(FIA_ERR_PARAM_NULLPTR, "workspace is NULL");
   if (dtype != FIA_F16 && dtype != FIA_BF16) return fail(FIA_ERR_PARAM_INVALID, "dtype must be fp16 or bf16");
   if (int rc = check_prefill_shape(B, Nq, &Nkv, D, max_seqlen_q)) return rc;
@@ -575,6 +594,18 @@ static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype d
     if (pre + next < 0)
       return fail(FIA_ERR_PARAM_INVALID, "band with pre_tokens %lld and next_tokens %lld holds no key",
                   (long long)opt->pre_tokens, (long long)opt->next_tokens);
+  }
+  if (paged) {
+    const int bs = opt->block_size;
+    if (bs < 128 || bs > 512 || bs % 128 != 0)
+      return fail(FIA_ERR_PARAM_INVALID, "paged prefill needs block_size 128, 256 or 512 in this build (got %d)", bs);
+    if (opt->kv_layout != FIA_KV_BNNBSD && opt->kv_layout != FIA_KV_BNBSH)
+      return fail(FIA_ERR_PARAM_INVALID, "unknown KV layout %d", opt->kv_layout);
+    if (opt->num_blocks < 1 || opt->num_blocks * Nkv >= (1LL << 31))
+      return fail(FIA_ERR_PARAM_INVALID, "num_blocks = %lld outside [1, 2^31 / Nkv)", (long long)opt->num_blocks);
+    if (opt->bt_stride < 1 || (int64_t)max_seqlen_kv > opt->bt_stride * bs)
+      return fail(FIA_ERR_PARAM_INVALID, "block table too narrow: max_seqlen_kv %d > bt_stride %lld * block_size %d",
+                  max_seqlen_kv, (long long)opt->bt_stride, bs);
   }
   if (!std::isfinite(scale)) return fail(FIA_ERR_PARAM_INVALID, "scale is not finite");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
@@ -610,6 +641,17 @@ static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype d
   p.max_seqlen_kv = max_seqlen_kv;
   p.pre = (int)pre;
   p.next = (int)next;
+  if (paged) {
+    const bool bsh = opt->kv_layout == FIA_KV_BNBSH;
+    p.block_table = opt->block_table;
+    p.bt_stride = opt->bt_stride;
+    p.seq_lens_kv = opt->seq_lens_kv;
+    p.block_size = opt->block_size;
+    p.num_blocks = opt->num_blocks;
+    p.kv_x_h = bsh ? D : 0;
+    p.kv_z_blk = bsh ? 1 : Nkv;
+    p.kv_z_h = bsh ? 0 : 1;
+  }
   p.dtype = dtype;
   p.scale_log2 = (float)(scale * 1.4426950408889634);
   p.tile_counter = static_cast<int*>(workspace);
@@ -618,8 +660,16 @@ static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype d
   p.status = d->status;
   CUtensorMap tmQ, tmK, tmV;
   if (int rc = make_tmap_thd(&tmQ, q, dtype, D, Nq, T)) return rc;
-  if (int rc = make_tmap_thd(&tmK, k, dtype, D, Nkv, Tkv > 0 ? Tkv : 1)) return rc;
-  if (int rc = make_tmap_thd(&tmV, v, dtype, D, Nkv, Tkv > 0 ? Tkv : 1)) return rc;
+  if (paged) {  // (channels, rows of a block, block [x kv head]) with (64, 128, 1) boxes
+    const bool bsh = opt->kv_layout == FIA_KV_BNBSH;
+    const uint64_t cols = bsh ? (uint64_t)Nkv * D : (uint64_t)D;
+    const uint64_t zs = bsh ? (uint64_t)opt->num_blocks : (uint64_t)opt->num_blocks * Nkv;
+    if (int rc = make_tmap_paged(&tmK, k, dtype, cols, opt->block_size, zs)) return rc;
+    if (int rc = make_tmap_paged(&tmV, v, dtype, cols, opt->block_size, zs)) return rc;
+  } else {
+    if (int rc = make_tmap_thd(&tmK, k, dtype, D, Nkv, Tkv > 0 ? Tkv : 1)) return rc;
+    if (int rc = make_tmap_thd(&tmV, v, dtype, D, Nkv, Tkv > 0 ? Tkv : 1)) return rc;
+  }
   cudaError_t e = fia::launch_prefill(p, tmQ, tmK, tmV, d->num_sms, stream);
   if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "prefill launch: %s", cudaGetErrorString(e));
   return ok();

@@ -144,6 +144,17 @@ struct PrefillParams {
   // i + d - pre <= j <= i + d + next, d = Lkv - Lq (pre + next >= 0, both within
   // [-2^30, 2^30]); rightDownCausal is (2^30, 0), no mask (2^30, 2^30)
   int pre, next;
+  // paged K/V (block_table non-null): k and v are pools of blocks of block_size tokens (a
+  // multiple of 128, so a key tile lies in one block); key tile kt of sequence b is rows
+  // (128 kt) % block_size .. of block block_table[b][128 kt / block_size], at tensor-map
+  // coordinates (x = hkv * kv_x_h + channel, y = row in block, z = blk * kv_z_blk + hkv * kv_z_h);
+  // sequence b has seq_lens_kv[b] keys (clamped to [0, max_seqlen_kv]); cu_kv is unused
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int64_t* seq_lens_kv;
+  int block_size;
+  int64_t num_blocks;
+  int kv_x_h, kv_z_blk, kv_z_h;
   int dtype;          // kBF16 or kF16
   float scale_log2;
   int* tile_list;     // workspace: (sequence << 16 | query tile) pairs, longest first

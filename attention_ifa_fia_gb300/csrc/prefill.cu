@@ -77,8 +77,18 @@ __device__ __forceinline__ int2 key_tile_range(const PrefillParams& p, int q0, i
 }
 
 __device__ __forceinline__ void seq_bounds(const PrefillParams& p, int b, int& tq, int& Lq, int& tk, int& Lkv) {
-  int64_t q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = p.cu_kv[b], k1 = p.cu_kv[b + 1];
-  if (q0 < 0 || q1 < q0 || q1 > p.T || k0 < 0 || k1 < k0 || k1 > p.Tkv) {
+  int64_t q0 = p.cu_q[b], q1 = p.cu_q[b + 1], k0 = 0, k1;
+  if (p.block_table) {  // paged keys: a length per sequence
+    k1 = p.seq_lens_kv[b];
+    if (k1 < 0 || k1 > p.max_seqlen_kv) {
+      raise_status(p.status, kStatusLengthClamped);
+      k1 = k1 < 0 ? 0 : p.max_seqlen_kv;
+    }
+  } else {
+    k0 = p.cu_kv[b];
+    k1 = p.cu_kv[b + 1];
+  }
+  if (q0 < 0 || q1 < q0 || q1 > p.T || k0 < 0 || k1 < k0 || (!p.block_table && k1 > p.Tkv)) {
     raise_status(p.status, kStatusBadSeqlens);
     q0 = q1 = k0 = k1 = 0;
   }
@@ -86,6 +96,24 @@ __device__ __forceinline__ void seq_bounds(const PrefillParams& p, int b, int& t
   Lq = (int)(q1 - q0);
   tk = (int)k0;
   Lkv = (int)(k1 - k0);
+}
+
+// Tensor-map coordinates {x, y, z} of key tile kt of kv head hkv of sequence b (keys from
+// tk in the TND layout, or Lkv keys in the paged pool).  A paged tile past the keys (the
+// one tile of a query tile that sees none) reads block 0: it is masked entirely.  A block
+// index outside the pool raises the status flag and reads block 0 instead.
+__device__ __forceinline__ int3 key_tile_coord(const PrefillParams& p, int b, int tk, int Lkv, int kt, int hkv) {
+  if (!p.block_table) return make_int3(0, hkv, tk + kt * kKT);
+  const int tok = kt * kKT;
+  int blk = 0;
+  if (tok < Lkv) {
+    blk = p.block_table[(int64_t)b * p.bt_stride + tok / p.block_size];
+    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+      raise_status(p.status, kStatusBadBlockIndex);
+      blk = 0;
+    }
+  }
+  return make_int3(hkv * p.kv_x_h, tok % p.block_size, blk * p.kv_z_blk + hkv * p.kv_z_h);
 }
 
 // ------------------------------------------------------------------ plan
@@ -263,8 +291,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int G = p.G;
       int j = 0, u_local = 0;
       int v_next = 0;             // next tile whose V is to be loaded
-      int v_hkv = 0, v_tk = 0;    // V source of tiles [v_next, j) is recorded in the ring
-      int ring_hkv[kMetaRing], ring_row[kMetaRing];
+      int3 ring_xyz[kMetaRing];  // tensor-map coordinates of the K and V tiles in flight
       bool ok = true;
       // V of tile jv, one tile behind its K
       auto load_v = [&](int jv) -> bool {
@@ -272,12 +299,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (!mbar_wait(&sm.v_empty[st], ((uint32_t)(jv / kPStages) & 1u) ^ 1u, p.status)) return false;
         mbar_arrive_expect_tx(&sm.v_full[st], kTileB);
         for (int bx = 0; bx < 2; ++bx)
-          tma_load_3d(sm.v[st] + bx * (kKT * 128), &tmV, bx * 64, ring_hkv[jv % kMetaRing], ring_row[jv % kMetaRing],
-                      &sm.v_full[st]);
+          tma_load_3d(sm.v[st] + bx * (kKT * 128), &tmV, ring_xyz[jv % kMetaRing].x + bx * 64,
+                      ring_xyz[jv % kMetaRing].y, ring_xyz[jv % kMetaRing].z, &sm.v_full[st]);
         return true;
       };
-      (void)v_hkv;
-      (void)v_tk;
       while (ok) {
         const int u = atomicAdd(&p.tile_counter[0], 1);
         if (u >= n_units) break;
@@ -302,11 +327,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
           m.b = b; m.h = h; m.q0 = q0; m.kvt = kt;
           m.tq = tq; m.tk = tk; m.Lq = Lq; m.Lkv = Lkv;
           m.first = i == 0; m.last = i == nkv - 1; m.qbuf = qb; m.unit = u;
-          ring_hkv[j % kMetaRing] = hkv;
-          ring_row[j % kMetaRing] = tk + kt * kKT;
+          const int3 c = key_tile_coord(p, b, tk, Lkv, kt, hkv);
+          ring_xyz[j % kMetaRing] = c;
           mbar_arrive_expect_tx(&sm.k_full[st], kTileB);
           for (int bx = 0; bx < 2; ++bx)
-            tma_load_3d(sm.k[st] + bx * (kKT * 128), &tmK, bx * 64, hkv, tk + kt * kKT, &sm.k_full[st]);
+            tma_load_3d(sm.k[st] + bx * (kKT * 128), &tmK, c.x + bx * 64, c.y, c.z, &sm.k_full[st]);
           if (v_next < j) {
             if (!load_v(v_next)) { ok = false; break; }
             ++v_next;
@@ -654,15 +679,15 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       const int n_units = p.tile_counter[1];
       const int npairs = p.Nq / 2;
       int j = 0, u_local = 0, v_next = 0;
-      int ring_hkv[kMetaRing], ring_row[kMetaRing];
+      int3 ring_xyz[kMetaRing];  // tensor-map coordinates of the K and V tiles in flight
       bool ok = true;
       auto load_v = [&](int jv) -> bool {  // V of tile jv, one tile behind its K
         const int st = jv % kPStages;
         if (!mbar_wait(&sm.v_empty[st], ((uint32_t)(jv / kPStages) & 1u) ^ 1u, p.status)) return false;
         mbar_arrive_expect_tx(&sm.v_full[st], kTileB);
         for (int bx = 0; bx < 2; ++bx)
-          tma_load_3d(sm.v[st] + bx * (kKT * 128), &tmV, bx * 64, ring_hkv[jv % kMetaRing], ring_row[jv % kMetaRing],
-                      &sm.v_full[st]);
+          tma_load_3d(sm.v[st] + bx * (kKT * 128), &tmV, ring_xyz[jv % kMetaRing].x + bx * 64,
+                      ring_xyz[jv % kMetaRing].y, ring_xyz[jv % kMetaRing].z, &sm.v_full[st]);
         return true;
       };
       while (ok) {
@@ -691,11 +716,11 @@ __global__ void __launch_bounds__(kP2Threads, 1)
           m.b = b; m.h = h0; m.q0 = q0; m.kvt = kt;
           m.tq = tq; m.tk = tk; m.Lq = Lq; m.Lkv = Lkv;
           m.first = i == 0; m.last = i == nkv - 1; m.qbuf = 0; m.unit = u;
-          ring_hkv[j % kMetaRing] = hkv;
-          ring_row[j % kMetaRing] = tk + kt * kKT;
+          const int3 c = key_tile_coord(p, b, tk, Lkv, kt, hkv);
+          ring_xyz[j % kMetaRing] = c;
           mbar_arrive_expect_tx(&sm.k_full[st], kTileB);
           for (int bx = 0; bx < 2; ++bx)
-            tma_load_3d(sm.k[st] + bx * (kKT * 128), &tmK, bx * 64, hkv, tk + kt * kKT, &sm.k_full[st]);
+            tma_load_3d(sm.k[st] + bx * (kKT * 128), &tmK, c.x + bx * 64, c.y, c.z, &sm.k_full[st]);
           if (v_next < j) {
             if (!load_v(v_next)) { ok = false; break; }
             ++v_next;

@@ -245,7 +245,9 @@ int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, co
                 float* softmax_sum, void* workspace, size_t workspace_bytes, fia_stream_t stream);
 
 /* fia_prefill with the band mask (FusedInferAttentionScore sparseMode 4 with preTokens /
- * nextTokens).  Arguments as for fia_prefill; mask may also be 4 (band), which needs options:
+ * nextTokens) and keys in a paged cache (FusedInferAttentionScore PagedAttention: blockTable,
+ * blockSize, actualSeqLengthsKv; a chunk of queries against a long cached context).
+ * Arguments as for fia_prefill; mask may also be 4 (band), which needs options:
  *
  *   query i of a sequence sees key j iff
  *     i + (Lkv - Lq) - pre_tokens <= j <= i + (Lkv - Lq) + next_tokens,
@@ -255,10 +257,29 @@ int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, co
  *   the pages forbid) is FIA_ERR_PARAM_INVALID.  Rows with no key in the band get the
  *   empty-row outputs.  Only key tiles that meet a query tile's band are read.
  *
- * options is read only for mask 4 (NULL there is FIA_ERR_PARAM_NULLPTR). */
+ * options->block_table non-NULL: k and v are paged pools instead of TND tensors --
+ *   (num_blocks, Nkv, block_size, D) with kv_layout FIA_KV_BNNBSD, or (num_blocks,
+ *   block_size, Nkv * D) with FIA_KV_BNBSH -- key j of sequence b is row j % block_size of
+ *   block block_table[b * bt_stride + j / block_size]; sequence b has seq_lens_kv[b] keys
+ *   (device int64 (B), clamped to [0, max_seqlen_kv] with FIA_STATUS_LENGTH_CLAMPED);
+ *   cu_seqlens_kv and Tkv are not used.  block_size is 128, 256 or 512 in this build (a key
+ *   tile of 128 then lies in one block); max_seqlen_kv <= bt_stride * block_size.  A block
+ *   index outside [0, num_blocks) raises FIA_STATUS_BAD_BLOCK_INDEX.  Queries stay TND: a
+ *   sequence's Lq queries are its last Lq positions (the rightDownCausal diagonal).  The
+ *   rows of a sequence's last block past its length are read and weighted by 0, so they
+ *   must hold finite values (a cache cleared once at allocation satisfies this).
+ *
+ * options may be NULL for masks 0 and 3 without paging (NULL with mask 4 is
+ * FIA_ERR_PARAM_NULLPTR). */
 typedef struct {
-  int64_t pre_tokens;
-  int64_t next_tokens;
+  int64_t pre_tokens;           /* mask 4 only */
+  int64_t next_tokens;          /* mask 4 only */
+  const int32_t* block_table;   /* NULL: k, v are TND (Tkv, Nkv, D) */
+  int64_t bt_stride;
+  const int64_t* seq_lens_kv;   /* device int64 (B) */
+  int block_size;
+  int64_t num_blocks;
+  int kv_layout;                /* fia_kv_layout */
 } fia_prefill_options;
 
 int fia_prefill_ex(const void* q, const void* k, const void* v, fia_dtype dtype, const int64_t* cu_seqlens_q,

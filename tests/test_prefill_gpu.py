@@ -150,3 +150,81 @@ def test_prefill_band_rejects(F, cuda):
         F.fia_prefill(dp.q, dp.k, dp.v, dp.cu_q, dp.cu_kv, max_seqlen_q=5, max_seqlen_kv=5, num_heads=4,
                       num_kv_heads=2, mask=4)
     assert ei.value.code == 161001
+
+
+# ------------------------------------------------------------------ paged keys (chunked prefill)
+def _paged_pool(case, block_size, layout, seed):
+    """The case's TND keys and values scattered into a shuffled pool with a few unused blocks;
+    rows past a sequence's length hold finite garbage.  Returns device (k_pool, v_pool,
+    block_table, seq_lens_kv)."""
+    rng = np.random.default_rng(seed)
+    nblk = [-(-int(L) // block_size) for L in case.lengths_kv]
+    total = sum(nblk) + 3
+    perm = rng.permutation(total)
+    width = max(max(nblk), 1)
+    bt = np.full((case.B, width + 1), -1, np.int32)     # entries past the used ones are never read
+    shape = (total, case.Nkv, block_size, case.D)
+    pools = []
+    for src in (case.k, case.v):
+        pool = W.to_bits(rng.standard_normal(shape, dtype=np.float32) * 3, case.dtype)
+        n = 0
+        for b in range(case.B):
+            for i in range(nblk[b]):
+                blk = int(perm[n + i])
+                bt[b, i] = blk
+                t0, t1 = i * block_size, min(int(case.lengths_kv[b]), (i + 1) * block_size)
+                pool[blk, :, :t1 - t0, :] = src[case.cu_kv[b] + t0:case.cu_kv[b] + t1].transpose(1, 0, 2)
+            n += nblk[b]
+        if layout == "bsh":
+            pool = np.ascontiguousarray(pool.transpose(0, 2, 1, 3).reshape(total, block_size, case.Nkv * case.D))
+        pools.append(torch.from_numpy(pool.view(np.int16)).cuda().view(torch.bfloat16 if case.dtype == W.BF16
+                                                                           else torch.float16))
+    return pools[0], pools[1], torch.from_numpy(bt).cuda(), torch.from_numpy(case.lengths_kv.astype(np.int64)).cuda()
+
+
+PAGED_CASES = {
+    # name: (make_prefill_case kwargs, block_size, layout, band); the query chunk of each
+    # sequence is its last Lq positions
+    "chunk_after_context_pair": (dict(Nq=8, Nkv=2, D=128, lengths=[128, 300, 1], lengths_kv=[1000, 300, 257]),
+                                 128, "bnnbsd", None),
+    "chunk_odd_g_bs256": (dict(Nq=3, Nkv=1, D=128, lengths=[200, 64], lengths_kv=[700, 64]), 256, "bnnbsd", None),
+    "bsh_layout_bs512": (dict(Nq=4, Nkv=2, D=128, lengths=[333, 17], lengths_kv=[1300, 600]), 512, "bsh", None),
+    "paged_band_fp16_sink": (dict(Nq=4, Nkv=2, D=128, lengths=[150, 290], lengths_kv=[900, 290], dtype=W.FP16,
+                                  sink=True), 128, "bnnbsd", (255, 0)),
+    "empty_kv_sequence": (dict(Nq=2, Nkv=1, D=128, lengths=[40, 70], lengths_kv=[0, 500]), 128, "bnnbsd", None),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PAGED_CASES))
+def test_prefill_paged_keys(F, cuda, name):
+    """Paged keys give the oracle's result and, tile for tile the same arithmetic, the TND
+    run's result bit for bit."""
+    kw, bs, layout, band = PAGED_CASES[name]
+    case = W.make_prefill_case(seed=zlib.crc32(("paged_" + name).encode()) % (1 << 30), **kw)
+    dp = DevicePrefill(case)
+    kp, vp, bt, lens = _paged_pool(case, bs, layout, seed=zlib.crc32(name.encode()) & 0xffff)
+    c = case
+    mx = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device="cuda")
+    sm = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device="cuda")
+    out, mx, sm = F.fia_prefill(dp.q, kp, vp, dp.cu_q, None, max_seqlen_q=int(c.lengths_q.max()),
+                                max_seqlen_kv=int(c.lengths_kv.max()), num_heads=c.Nq, num_kv_heads=c.Nkv,
+                                scale=c.scale, mask=4 if band else 3, sink=dp.sink, softmax_max=mx, softmax_sum=sm,
+                                pre_tokens=band[0] if band else None, next_tokens=band[1] if band else None,
+                                block_table=bt, seq_lens_kv=lens, kv_layout=F.KV_BNBSH if layout == "bsh" else 0)
+    compare_prefill(case, out, mx, sm, band=band)
+    ref = run_prefill(F, dp, band=band)
+    assert torch.equal(out.view(torch.int16), ref[0].view(torch.int16))
+    assert torch.equal(mx, ref[1]) and torch.equal(sm, ref[2])
+    assert F.fia_device_status() == 0
+
+
+def test_prefill_paged_rejects_small_blocks(F, cuda):
+    case = W.make_prefill_case(Nq=4, Nkv=2, D=128, lengths=[5], lengths_kv=[100], seed=4)
+    dp = DevicePrefill(case)
+    kp = torch.zeros((8, 2, 64, 128), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    lens = torch.tensor([100], dtype=torch.int64, device="cuda")
+    with pytest.raises(F.FiaError) as ei:
+        F.fia_prefill(dp.q, kp, kp, dp.cu_q, None, max_seqlen_q=5, max_seqlen_kv=100, num_heads=4, num_kv_heads=2,
+                      block_table=bt, seq_lens_kv=lens)
+    assert ei.value.code == 161002
