@@ -598,7 +598,7 @@ static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype d
   if (paged) {
     const int bs = opt->block_size;
     if (bs < 128 || bs > 512 || bs % 128 != 0)
-      return fail(FIA_ERR_PARAM_INVALID, "paged prefill needs block_size 128, 256 or 512 in this build (got %d)", bs);
+      return fail(FIA_ERR_PARAM_INVALID, "paged prefill needs block_size a multiple of 128 up to 512 in this build (got %d)", bs);
     if (opt->kv_layout != FIA_KV_BNNBSD && opt->kv_layout != FIA_KV_BNBSH)
       return fail(FIA_ERR_PARAM_INVALID, "unknown KV layout %d", opt->kv_layout);
     if (opt->num_blocks < 1 || opt->num_blocks * Nkv >= (1LL << 31))

@@ -262,8 +262,8 @@ int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, co
  *   block_size, Nkv * D) with FIA_KV_BNBSH -- key j of sequence b is row j % block_size of
  *   block block_table[b * bt_stride + j / block_size]; sequence b has seq_lens_kv[b] keys
  *   (device int64 (B), clamped to [0, max_seqlen_kv] with FIA_STATUS_LENGTH_CLAMPED);
- *   cu_seqlens_kv and Tkv are not used.  block_size is 128, 256 or 512 in this build (a key
- *   tile of 128 then lies in one block); max_seqlen_kv <= bt_stride * block_size.  A block
+ *   cu_seqlens_kv and Tkv are not used.  block_size is a multiple of 128 up to 512 in this
+ *   build (a key tile of 128 then lies in one block); max_seqlen_kv <= bt_stride * block_size.  A block
  *   index outside [0, num_blocks) raises FIA_STATUS_BAD_BLOCK_INDEX.  Queries stay TND: a
  *   sequence's Lq queries are its last Lq positions (the rightDownCausal diagonal).  The
  *   rows of a sequence's last block past its length are read and weighted by 0, so they

@@ -74,3 +74,91 @@ def test_workspace_size_needs_output(F):
     assert lib.fia_decode_workspace_size(2, 4, 2, 64, 64, 16, 0, None) == NULLPTR
     n = ctypes.c_size_t(0)
     assert lib.fia_decode_workspace_size(2, 4, 2, 96, 64, 16, 0, ctypes.byref(n)) == INVALID
+
+
+def test_options_structs_match_the_header(F, tmp_path):
+    """The binding's ctypes mirrors of fia_decode_options and fia_prefill_options have the
+    C layout: size and every field's offset, as gcc lays the header's structs out."""
+    import os
+    from attention_ifa_fia_gb300 import _binding as B
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    structs = {"fia_decode_options": B.DecodeOptions, "fia_prefill_options": B.PrefillOptions}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "fia.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", inc, str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l}
+    for cname, cls in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for fname, _ in cls._fields_:
+            assert got[(cname, fname)] == getattr(cls, fname).offset, (cname, fname)
+
+
+def _decode_ex(lib, B_, opts, **kw):
+    a = dict(q=P, q_dtype=2, k=P, v=P, kv_dtype=2, bt=P, bt_stride=4, lens=P, max_kv_len=64, B=2, Nq=4, Nkv=2,
+             D=64, bs=16, num_blocks=8, scale=0.125, aqs=None, aqo=None, sink=None, out=P, mx=None, sm=None,
+             splits=0, ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.fia_decode_ex(a["q"], a["q_dtype"], a["k"], a["v"], a["kv_dtype"], a["bt"], a["bt_stride"], a["lens"],
+                             a["max_kv_len"], a["B"], a["Nq"], a["Nkv"], a["D"], a["bs"], a["num_blocks"], a["scale"],
+                             a["aqs"], a["aqo"], a["sink"], a["out"], a["mx"], a["sm"], a["splits"], a["ws"],
+                             a["ws_bytes"], a["stream"], ctypes.byref(opts))
+
+
+@pytest.mark.parametrize("fields,kw,code", [
+    (dict(kv_layout=2), {}, INVALID),                                  # unknown layout
+    (dict(antiquant_mode=2), {}, INVALID),                             # unknown antiquant mode
+    (dict(antiquant_mode=1), {}, INVALID),                             # per-tensor without int8 KV
+    (dict(atten_mask=P, atten_mask_stride=63), {}, INVALID),           # mask rows shorter than max_kv_len
+    (dict(quant_offset2=P), {}, INVALID),                              # offset without scale
+    (dict(quant_scale2=P, quant2_per_channel=2), {}, INVALID),
+    (dict(band=1, pre_tokens=3, next_tokens=-4), {}, INVALID),         # a band holding no key
+])
+def test_decode_ex_rejects(F, fields, kw, code):
+    from attention_ifa_fia_gb300 import _binding as B
+    lib = F.library()
+    opts = B.DecodeOptions()
+    for k, v in fields.items():
+        setattr(opts, k, v)
+    assert _decode_ex(lib, None, opts, **kw) == code
+    assert lib.fia_last_error()
+
+
+def _prefill_ex(lib, opts, **kw):
+    a = dict(q=P, k=P, v=P, dtype=2, cu_q=P, cu_kv=P, B=2, T=100, Tkv=100, msq=64, mskv=64, Nq=4, Nkv=2, D=128,
+             scale=0.088, mask=3, sink=None, out=P, mx=None, sm=None, ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.fia_prefill_ex(a["q"], a["k"], a["v"], a["dtype"], a["cu_q"], a["cu_kv"], a["B"], a["T"], a["Tkv"],
+                              a["msq"], a["mskv"], a["Nq"], a["Nkv"], a["D"], a["scale"], a["mask"], a["sink"],
+                              a["out"], a["mx"], a["sm"], a["ws"], a["ws_bytes"], a["stream"],
+                              None if opts is None else ctypes.byref(opts))
+
+
+@pytest.mark.parametrize("fields,kw,code", [
+    (None, dict(mask=4), NULLPTR),                                                   # band without options
+    (dict(pre_tokens=2, next_tokens=-3), dict(mask=4), INVALID),                     # empty band
+    ({}, dict(mask=2), INVALID),                                                     # leftUpCausal: not built
+    (dict(block_table=P, bt_stride=1, block_size=128, num_blocks=4), dict(cu_kv=None), NULLPTR),  # no seq_lens_kv
+    (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=64, num_blocks=4), {}, INVALID),  # block < 128
+    (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=640, num_blocks=4), {}, INVALID),
+    (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=128, num_blocks=0), {}, INVALID),
+    (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=128, num_blocks=4, kv_layout=5), {}, INVALID),
+    (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=128, num_blocks=4), dict(mskv=129), INVALID),
+])
+def test_prefill_ex_rejects(F, fields, kw, code):
+    from attention_ifa_fia_gb300 import _binding as B
+    lib = F.library()
+    opts = None
+    if fields is not None:
+        opts = B.PrefillOptions()
+        for k, v in fields.items():
+            setattr(opts, k, v)
+    assert _prefill_ex(lib, opts, **kw) == code
+    assert lib.fia_last_error()
