@@ -62,7 +62,7 @@ def _bind(path: str):
     P = ctypes.c_void_p
     i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
     lib.oracle_decode.argtypes = [P, i32, P, P, i32, P, i64, P, i32, i32, i32, i32, i32, i64,
-                                  dbl, P, P, P, P, i64, i64, i64, P, i64, i32, P, P, P]
+                                  dbl, P, P, P, P, i64, i64, i64, i32, P, i64, i32, P, P, P]
     lib.oracle_decode.restype = i32
     lib.oracle_prefill.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, dbl, i32, i64, i64, P,
                                    P, i64, i32, P, P, P]
@@ -129,7 +129,7 @@ class Oracle:
 
     def decode(self, q, k_cache, v_cache, seq_lens, *, Nq, Nkv, D, scale, q_dtype=None, kv_dtype=None,
                block_table=None, block_size=0, kv_rows=0, aq_scale=None, aq_offset=None, sink=None,
-               mask=None, band=None, rows=None, nthreads=0):
+               mask=None, band=None, q_len=1, rows=None, nthreads=0):
         """Decode attention (query S = 1).
 
         q: (B, Nq, D) array (uint16 bits with q_dtype=F16/BF16, or float32/float64).
@@ -137,7 +137,9 @@ class Oracle:
         given, else contiguous (B, Nkv, kv_rows, D).  int8 caches need aq_scale
         (2, Nkv, D) float32 and optionally aq_offset.  mask: (B, S) bytes (bool,
         int8 or uint8; S >= every length), nonzero = key masked out.  band: (pre_tokens,
-        next_tokens), keys L - 1 - pre .. L - 1 + next of each batch.  Returns (out, max, sum) as
+        next_tokens), keys L - 1 - pre .. L - 1 + next of each batch.  q_len = s > 1: q is
+        (B, s, Nq, D), position i of a batch at L - s + i sees keys up to it, and rows run
+        over B * s * Nq.  Returns (out, max, sum) as
         float64 arrays of shape (R, D), (R,), (R,) where R = len(rows) or B * Nq.
         """
         q = np.ascontiguousarray(q)
@@ -148,7 +150,7 @@ class Oracle:
         bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
         bt_stride = 0 if bt is None else int(bt.shape[1])
         rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
-        R = B * Nq if rows_a is None else int(rows_a.shape[0])
+        R = B * int(q_len) * Nq if rows_a is None else int(rows_a.shape[0])
         f32 = lambda a: None if a is None else np.ascontiguousarray(a, dtype=np.float32)
         aq_scale, aq_offset, sink = f32(aq_scale), f32(aq_offset), f32(sink)
         if mask is not None:
@@ -162,8 +164,8 @@ class Oracle:
             _dtype_code(k_cache, kv_dtype), _ptr(bt), bt_stride, _ptr(seq_lens),
             B, Nq, Nkv, D, block_size, kv_rows, float(scale), _ptr(aq_scale),
             _ptr(aq_offset), _ptr(sink), _ptr(mask), mask_stride,
-            int(band[0]) if band is not None else 1 << 62, int(band[1]) if band is not None else 1 << 62,
-            _ptr(rows_a), 0 if rows_a is None else R,
+            int(band[0]) if band is not None else 1 << 62, int(band[1]) if band is not None else 0,
+            int(q_len), _ptr(rows_a), 0 if rows_a is None else R,
             nthreads, _ptr(out), _ptr(mx), _ptr(sm))
         if rc != 0:
             raise ValueError("oracle_decode rejected its arguments")

@@ -40,6 +40,9 @@
  *   R13 attenMask (decode): a byte per (batch, key); nonzero = the key is masked
  *       out (the causal forms the pages describe keep the diagonal at 0), and a
  *       masked key is left out of the softmax entirely.
+ *   R16 Decode with several query positions (speculative drafts, Q_S > 1 over the
+ *       paged cache): the s queries of a batch are its last s positions, each seeing
+ *       the keys up to its own position (rightDownCausal with Lq = s).
  *   R14 Post-quant output: y = out * quantScale2 + quantOffset2 in the
  *       attention's own precision, rounded to nearest with ties to even and
  *       saturated to int8; per-channel parameters index the output's N * D
@@ -194,9 +197,12 @@ static void attend_row(const double *q, const double *K, const double *V, int64_
  * mask[b * mask_stride + t], or NULL; a nonzero byte removes key t of batch b
  * from the attention (1 = masked out, 0 = attended), so a batch whose keys are
  * all masked is handled like one of length 0.
- * pre_tokens / next_tokens: the band of R15 for the one query (i = 0, Lq = 1): key
- * t of a batch of length L is visible iff L - 1 - pre_tokens <= t <= L - 1 + next_tokens
- * (large values: no band).
+ * q_len (R16): s >= 1 query positions per batch, q laid out (B, s, Nq, D); position i
+ * sits at qp = L - s + i of a batch of length L; rows run over B * s * Nq.  A mask needs
+ * s = 1.
+ * pre_tokens / next_tokens: the band of R15, key t visible iff
+ * qp - pre_tokens <= t <= qp + next_tokens; (large, 0) is rightDownCausal with Lq = s
+ * (for s = 1: every key), the default.
  * rows: the (b * Nq + h) rows to compute, or NULL for all B * Nq rows; results
  * are written compactly: out[i * D + d], smax[i], ssum[i] for the i-th row.
  * Returns 0, or -1 on an argument it cannot handle. */
@@ -207,7 +213,7 @@ int oracle_decode(const void *q, int q_dtype,
                   int B, int Nq, int Nkv, int D, int block_size, int64_t kv_rows,
                   double scale, const float *aq_scale, const float *aq_offset,
                   const float *sink, const uint8_t *mask, int64_t mask_stride,
-                  int64_t pre_tokens, int64_t next_tokens,
+                  int64_t pre_tokens, int64_t next_tokens, int q_len,
                   const int64_t *rows, int64_t n_rows, int nthreads,
                   double *out, double *smax, double *ssum)
 {
@@ -217,8 +223,12 @@ int oracle_decode(const void *q, int q_dtype,
         return -1;
     if (kv_dtype == OR_I8 && !aq_scale)
         return -1;
+    if (q_len < 1)
+        q_len = 1;
+    if (mask && q_len != 1)
+        return -1;
     const int G = Nq / Nkv;
-    const int64_t total = rows ? n_rows : (int64_t)B * Nq;
+    const int64_t total = rows ? n_rows : (int64_t)B * q_len * Nq;
     int64_t max_len = 0;
     for (int b = 0; b < B; ++b)
         if (seq_lens[b] > max_len)
@@ -244,9 +254,12 @@ int oracle_decode(const void *q, int q_dtype,
             if (bad)
                 continue;
             const int64_t r = rows ? rows[i] : i;
-            const int b = (int)(r / Nq), h = (int)(r % Nq);
+            const int64_t bi = r / Nq;                          /* b * q_len + position */
+            const int b = (int)(bi / q_len), h = (int)(r % Nq);
+            const int64_t pos = bi % q_len;
             const int hk = h / G;                               /* R1 */
             const int64_t L = seq_lens[b];
+            const int64_t qp = L - q_len + pos;                 /* the query's position, R16 */
             for (int d = 0; d < D; ++d)
                 qd[d] = load_elem(q, q_dtype, r * D + d);
             /* gather the visible keys/values of (b, hk) into dense rows; n of them
@@ -255,7 +268,7 @@ int oracle_decode(const void *q, int q_dtype,
             for (int64_t t = 0; t < L; ++t) {
                 if (mask && mask[(int64_t)b * mask_stride + t] != 0)
                     continue;
-                if (t < L - 1 - pre_tokens || t > L - 1 + next_tokens)      /* R15 with Lq = 1 */
+                if (t < qp - pre_tokens || t > qp + next_tokens)            /* R15, R16 */
                     continue;
                 int64_t src;                                    /* element offset of row t */
                 if (block_table) {

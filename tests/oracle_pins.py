@@ -322,6 +322,54 @@ def pin_decode_band_is_prefill_band_of_one_query(O):
         assert all(np.array_equal(x, y) for x, y in zip(dec, msk))
 
 
+def pin_decode_query_positions(O):
+    """s query positions per batch (the last s of each sequence): equal to the prefill oracle
+    with Lq = s over the gathered keys (causal, and with a band), and to torch SDPA under a
+    mask built with numpy's tril (k = L - s); a position before the first key gets the empty
+    row."""
+    rng = np.random.default_rng(41)
+    B, Nq, Nkv, D, bs, s = 3, 4, 2, 16, 8, 3
+    lengths = [30, 2, 17]
+    case = W.make_decode_case(B=B, Nq=Nq, Nkv=Nkv, D=D, block_size=bs, lengths=lengths, seed=41, scale=0.4)
+    q = W.to_bits(rng.standard_normal((B, s, Nq, D), dtype=np.float32), W.BF16)
+    kc = case.k_cache.transpose(0, 2, 1, 3)
+    vc = case.v_cache.transpose(0, 2, 1, 3)
+    k = np.concatenate([np.concatenate([kc[p] for p in case.block_table[b, :(L + bs - 1) // bs]])[:L]
+                        for b, L in enumerate(lengths)])
+    v = np.concatenate([np.concatenate([vc[p] for p in case.block_table[b, :(L + bs - 1) // bs]])[:L]
+                        for b, L in enumerate(lengths)])
+    cu_q = np.arange(B + 1) * s
+    cu_kv = np.concatenate([[0], np.cumsum(lengths)])
+    kw = dict(Nq=Nq, Nkv=Nkv, D=D, scale=case.scale)
+    for band in [None, (4, 0), (1, -1)]:
+        dec = O.decode(q, case.k_cache, case.v_cache, case.lengths, q_dtype=OR.BF16, kv_dtype=OR.BF16,
+                       block_table=case.block_table, block_size=bs, band=band, q_len=s, **kw)
+        pf = O.prefill(q.reshape(B * s, Nq, D), k, v, cu_q, cu_kv, dtype=OR.BF16, causal=True, band=band, **kw)
+        for x, y in zip(dec, pf):
+            np.testing.assert_allclose(x, y, rtol=1e-13, atol=1e-13)
+    out, mx, sm = O.decode(q, case.k_cache, case.v_cache, case.lengths, q_dtype=OR.BF16, kv_dtype=OR.BF16,
+                           block_table=case.block_table, block_size=bs, q_len=s, **kw)
+    qf = W.bits_to_f32(q, W.BF16).astype(np.float64)
+    kf = np.repeat(W.bits_to_f32(k, W.BF16).astype(np.float64), Nq // Nkv, axis=1)
+    vf = np.repeat(W.bits_to_f32(v, W.BF16).astype(np.float64), Nq // Nkv, axis=1)
+    for b, L in enumerate(lengths):
+        allowed = np.tril(np.ones((s, L), bool), k=L - s)
+        has = allowed.any(axis=1)
+        rows = (np.arange(s)[:, None] + b * s) * Nq + np.arange(Nq)[None, :]    # (s, Nq)
+        K = kf[cu_kv[b]:cu_kv[b + 1]].transpose(1, 0, 2)
+        V = vf[cu_kv[b]:cu_kv[b + 1]].transpose(1, 0, 2)
+        Q = qf[b][has].transpose(1, 0, 2)                                        # (Nq, s', D)
+        ref = sdpa_rows(Q, K, V, case.scale, bool_mask=np.broadcast_to(allowed[has], (Nq,) + allowed[has].shape))
+        np.testing.assert_allclose(out[rows[has].T], ref, rtol=1e-12, atol=1e-12)
+        e = rows[~has]
+        assert np.all(out[e] == 0) and np.all(mx[e] == -np.inf) and np.all(sm[e] == 0)
+    one = O.decode(case.q, case.k_cache, case.v_cache, case.lengths, q_dtype=OR.BF16, kv_dtype=OR.BF16,
+                   block_table=case.block_table, block_size=bs, q_len=1, **kw)
+    ref = O.decode(case.q, case.k_cache, case.v_cache, case.lengths, q_dtype=OR.BF16, kv_dtype=OR.BF16,
+                   block_table=case.block_table, block_size=bs, **kw)
+    assert all(np.array_equal(x, y) for x, y in zip(one, ref))
+
+
 # ------------------------------------------------------------------ post-quant output
 def pin_post_quant_closed_forms(O):
     """Ties go to the even integer, values past the int8 range saturate, the offset is added."""

@@ -40,8 +40,12 @@ MUTANTS = [
      "if (0 && mask && mask[(int64_t)b * mask_stride + t] != 0)"),
     ("mask_polarity", "mask[(int64_t)b * mask_stride + t] != 0)", "mask[(int64_t)b * mask_stride + t] == 0)"),
     ("mask_batch_row", "mask[(int64_t)b * mask_stride + t]", "mask[t]"),
-    ("decode_band_lower_off_by_one", "if (t < L - 1 - pre_tokens ||", "if (t <= L - 1 - pre_tokens ||"),
-    ("decode_band_upper_ignored", "|| t > L - 1 + next_tokens)", "|| t > L - 1 + 1000000)"),
+    ("decode_band_lower_off_by_one", "if (t < qp - pre_tokens ||", "if (t <= qp - pre_tokens ||"),
+    ("decode_band_upper_ignored", "|| t > qp + next_tokens)", "|| t > qp + 1000000)"),
+    ("decode_positions_off_by_one", "const int64_t qp = L - q_len + pos;", "const int64_t qp = L - q_len + pos + 1;"),
+    ("decode_positions_all_last", "const int64_t qp = L - q_len + pos;", "const int64_t qp = L - 1;"),
+    ("decode_positions_batch_index", "const int b = (int)(bi / q_len), h = (int)(r % Nq);",
+     "const int b = (int)(bi % q_len), h = (int)(r % Nq);"),
     ("post_quant_ties_away", "double q = nearbyint(v);", "double q = round(v);"),
     ("post_quant_truncates", "double q = nearbyint(v);", "double q = trunc(v);"),
     ("post_quant_no_upper_saturation", "if (q > 127.0)\n                q = 127.0;",
