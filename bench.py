@@ -72,6 +72,17 @@ def decode_bytes(case: W.DecodeCase) -> dict:
     return {"kv": kv, "total": kv + qo + bt + aux}
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (each rank's timed duration: the job is as slow as its
+    slowest rank); x itself when there is one rank (dist None)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -249,10 +260,7 @@ def run_ours(args, rank, world, local_rank):
     ms_traced = e0.elapsed_time(e1)
     kern = {name: F.fia_trace_collect(kid) for name, kid in kern_ids}
     status = F.fia_device_status()
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
 
     # ---- end to end through the public API with host buffers
     pin_q = [torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory() for c in copies]
@@ -290,10 +298,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     ms_e2e = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(ms_e2e, dist, dev)
     sampler.stop()
 
     if rank != 0:
@@ -412,10 +417,7 @@ def run_prefill_bench(args, rank, world, local_rank):
     ms = e0.elapsed_time(e1)
     pf_ms, pf_n = F.fia_trace_collect(F.KERNEL_PREFILL)
     status = F.fia_device_status()
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     # end to end: q, k, v and cumulative lengths from pinned host memory, out/max/sum back
     pins = [(torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory().copy_(c.q),
              torch.empty(c.k.shape, dtype=c.k.dtype).pin_memory().copy_(c.k),
@@ -449,10 +451,7 @@ def run_prefill_bench(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(ms_e2e, dist, dev)
     sampler.stop()
     if rank != 0:
         return None
