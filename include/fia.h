@@ -6,8 +6,14 @@
  *   fia_decode             paged GQA decode attention, query S = 1, optional int8
  *                          KV antiquant and learnable sink, split-KV partials merged
  *                          by the RingAttentionUpdate rule
+ *   fia_decode_ex          the same with the operator's variants: the (blocknum,
+ *                          blocksize, H) cache layout, per-tensor antiquant, attenMask,
+ *                          softmaxLse, an int8 output (quantScale2 / quantOffset2) and
+ *                          a band window (preTokens / nextTokens)
+ *   fia_decode_noalloc     fia_decode without a workspace argument
  *   fia_prefill            causal variable-length attention, TND layout
- *   fia_prefill_ex         the same with the band mask (preTokens / nextTokens)
+ *   fia_prefill_ex         the same with the band mask (preTokens / nextTokens) and
+ *                          keys and values in a paged cache (chunked prefill)
  *   ring_attention_update  merge of two attention partials by softmax max/sum
  *
  * Conventions shared by every call:
