@@ -77,6 +77,8 @@ def _load() -> ctypes.CDLL:
         "fia_trace_enable": ([i32], i32),
         "fia_trace_collect": ([i32, ctypes.POINTER(dbl), ctypes.POINTER(i32)], i32),
         "fia_debug_gather": ([P, i32, P, i64, P, i32, i32, i32, i32, i32, i64, i32, i32, P, P], i32),
+        "fia_debug_i8_codes": ([P, i64, P, P], i32),
+        "fia_debug_i8_qprep": ([P, i32, P, P, i32, i32, i32, dbl, P, sz, P, P, P, P], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -339,3 +341,31 @@ def fia_debug_gather(k_cache: torch.Tensor, block_table: torch.Tensor, actual_se
                                  _ptr(actual_seq_lengths), int(max_kv_len), B, nkv, D, block_size, num_blocks, b,
                                  hkv, _ptr(dst), _stream(stream)), "fia_debug_gather")
     return dst
+
+
+I8_QPREP_BLOCK_BYTES = 8320  # one (b, kv head) block of the int8 tensor-core query operand
+
+
+def fia_debug_i8_codes(codes: torch.Tensor, stream=None) -> torch.Tensor:
+    """The int8 tensor-core kernel's code -> binary16 conversion; returns int16 bit patterns."""
+    out = torch.empty(codes.shape, dtype=torch.int16, device=codes.device)
+    _check(_lib.fia_debug_i8_codes(_ptr(codes), codes.numel(), _ptr(out), _stream(stream)), "fia_debug_i8_codes")
+    return out
+
+
+def fia_debug_i8_qprep(q: torch.Tensor, antiquant_scale: torch.Tensor, antiquant_offset=None, *, num_heads: int,
+                       num_kv_heads: int, scale: Optional[float] = None, stream=None):
+    """The query operand of the int8 tensor-core kernel: (hi, lo) int16 bit patterns of
+    shape (B, Nkv, 16, 128) and {kq, nq} fp32 of shape (B, Nkv, 16, 2)."""
+    B, D = int(q.shape[0]), int(q.shape[-1])
+    if scale is None:
+        scale = D ** -0.5
+    nblk = B * num_kv_heads
+    blocks = torch.empty(max(nblk, 1) * I8_QPREP_BLOCK_BYTES, dtype=torch.uint8, device=q.device)
+    hi = torch.empty((B, num_kv_heads, 16, 128), dtype=torch.int16, device=q.device)
+    lo = torch.empty_like(hi)
+    kn = torch.empty((B, num_kv_heads, 16, 2), dtype=torch.float32, device=q.device)
+    _check(_lib.fia_debug_i8_qprep(_ptr(q), dtype_code(q), _ptr(antiquant_scale), _ptr(antiquant_offset), B,
+                                   num_heads, num_kv_heads, float(scale), _ptr(blocks), blocks.numel(), _ptr(hi),
+                                   _ptr(lo), _ptr(kn), _stream(stream)), "fia_debug_i8_qprep")
+    return hi, lo, kn

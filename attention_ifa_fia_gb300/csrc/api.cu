@@ -38,25 +38,32 @@ __device__ unsigned int g_status_word;
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool init = false;
+  void* ctx = nullptr;  // the context the cached addresses belong to
   int num_sms = 0;
   unsigned int* status = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-// Per-device set-up with that device current: SM count and the status word's address.
+// Per-device set-up with that device current: SM count and the status word's address,
+// looked up again whenever the device's current context changes (a device reset destroys
+// the context and the module; the next context loads the module at new addresses).
 int device_info(DeviceInfo** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(FIA_ERR_RUNTIME, "device ordinal %d out of range", dev);
+  void* ctx = nullptr;
+  if (int rc = fia::current_context(&ctx)) return rc;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = g_dev[dev];
-  if (!d.init) {
+  if (!d.init || d.ctx != ctx) {
+    d.init = false;
     e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
     if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    if (int rc = fia::current_context(&d.ctx)) return rc;  // current now, if it was not before
     d.init = true;
   }
   *out = &d;
@@ -179,6 +186,26 @@ cudaEvent_t trace_event() {
 }  // namespace
 
 namespace fia {
+int current_context(void** ctx) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  static GetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<GetCurrent>(p);
+  });
+  if (!fn) return report_error(FIA_ERR_RUNTIME, "cuCtxGetCurrent is not available from the driver");
+  // NULL until the runtime has made the device's primary context current (it does so on the
+  // first runtime call that needs a context, e.g. cudaGetSymbolAddress)
+  CUcontext c = nullptr;
+  if (fn(&c) != CUDA_SUCCESS) return report_error(FIA_ERR_RUNTIME, "cuCtxGetCurrent failed");
+  *ctx = c;
+  return FIA_SUCCESS;
+}
+
 int report_error(int code, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -264,7 +291,7 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
                        int block_size, int64_t num_blocks, double scale, const float* antiquant_scale,
                        const float* antiquant_offset, const float* sink, void* out, float* softmax_max,
                        float* softmax_sum, int num_splits, void* workspace, size_t workspace_bytes,
-                       fia_stream_t stream, const fia_decode_options* opt) {
+                       fia_stream_t stream, const fia_decode_options* opt, bool check_only = false) {
   const int kv_layout = opt ? opt->kv_layout : FIA_KV_BNNBSD;
   const int aq_mode = opt ? opt->antiquant_mode : FIA_AQ_PER_CHANNEL;
   float* lse = opt ? opt->softmax_lse : nullptr;
@@ -279,7 +306,7 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
     return fail(FIA_ERR_PARAM_NULLPTR, "q, k_cache, v_cache, block_table, actual_seq_lengths and out are required");
   if (kv_dtype == FIA_I8 && !antiquant_scale)
     return fail(FIA_ERR_PARAM_NULLPTR, "int8 KV needs antiquant_scale");
-  if (!workspace) return fail(FIA_ERR_PARAM_NULLPTR, "workspace is NULL");
+  if (!workspace && !check_only) return fail(FIA_ERR_PARAM_NULLPTR, "workspace is NULL");
   // -- 161002: dtypes, shapes, attributes
   if (q_dtype != FIA_F16 && q_dtype != FIA_BF16)
     return fail(FIA_ERR_PARAM_INVALID, "query dtype must be fp16 or bf16");
@@ -331,6 +358,7 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   if (int rc = plan_decode(B, Nkv, max_kv_len, num_splits, d->num_sms, &plan)) return rc;
   const int G = Nq / Nkv;
   const size_t need = fia::decode_workspace_bytes(B, Nkv, G, D, plan.max_items);
+  if (check_only) return ok();
   if (workspace_bytes < need)
     return fail(FIA_ERR_PARAM_INVALID, "workspace of %zu bytes is smaller than the %zu required", workspace_bytes,
                 need);
@@ -414,6 +442,22 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   }
   return ok();
 }
+
+}  // extern "C"
+
+namespace fia {
+int decode_check(const void* q, int q_dtype, const void* k_cache, const void* v_cache, int kv_dtype,
+                 const int32_t* block_table, int64_t bt_stride, const int64_t* actual_seq_lengths, int max_kv_len,
+                 int B, int Nq, int Nkv, int D, int block_size, int64_t num_blocks, double scale,
+                 const float* antiquant_scale, const float* antiquant_offset, const float* sink, void* out,
+                 float* softmax_max, float* softmax_sum, int num_splits) {
+  return decode_impl(q, static_cast<fia_dtype>(q_dtype), k_cache, v_cache, static_cast<fia_dtype>(kv_dtype), block_table, bt_stride, actual_seq_lengths, max_kv_len,
+                     B, Nq, Nkv, D, block_size, num_blocks, scale, antiquant_scale, antiquant_offset, sink, out,
+                     softmax_max, softmax_sum, num_splits, nullptr, 0, nullptr, nullptr, true);
+}
+}  // namespace fia
+
+extern "C" {
 
 int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache, fia_dtype kv_dtype,
                const int32_t* block_table, int64_t bt_stride, const int64_t* actual_seq_lengths, int max_kv_len,
@@ -504,6 +548,48 @@ int fia_debug_gather(const void* k_cache, fia_dtype kv_dtype, const int32_t* blo
   return ok();
 }
 
+int fia_debug_i8_codes(const int8_t* codes, int64_t n, uint16_t* out, fia_stream_t stream) {
+  if (!codes || !out) return fail(FIA_ERR_PARAM_NULLPTR, "codes and out are required");
+  if (n < 0 || n % 4 != 0) return fail(FIA_ERR_PARAM_INVALID, "n = %lld must be a non-negative multiple of 4",
+                                       (long long)n);
+  if ((reinterpret_cast<uintptr_t>(codes) & 3u) || (reinterpret_cast<uintptr_t>(out) & 7u))
+    return fail(FIA_ERR_PARAM_INVALID, "codes must be 4-byte and out 8-byte aligned");
+  cudaError_t e = fia::launch_debug_i8_codes(codes, n, out, stream);
+  if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "code conversion probe launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int fia_debug_i8_qprep(const void* q, fia_dtype q_dtype, const float* antiquant_scale, const float* antiquant_offset,
+                       int B, int Nq, int Nkv, double scale, void* blocks, size_t blocks_bytes, uint16_t* q_hi,
+                       uint16_t* q_lo, float* kq_nq, fia_stream_t stream) {
+  if (!q || !antiquant_scale || !blocks || !q_hi || !q_lo || !kq_nq)
+    return fail(FIA_ERR_PARAM_NULLPTR, "q, antiquant_scale, blocks, q_hi, q_lo and kq_nq are required");
+  if (q_dtype != FIA_F16 && q_dtype != FIA_BF16) return fail(FIA_ERR_PARAM_INVALID, "query dtype must be fp16 or bf16");
+  int nkv = Nkv;
+  if (int rc = check_decode_shape(B, Nq, &nkv, 128, 0, 128, 0)) return rc;
+  if (!std::isfinite(scale)) return fail(FIA_ERR_PARAM_INVALID, "scale is not finite");
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(blocks) & 255u))
+    return fail(FIA_ERR_PARAM_INVALID, "q must be 16-byte and blocks 256-byte aligned");
+  const size_t need = fia::debug_i8_qprep_block_bytes() * (size_t)B * nkv;
+  if (blocks_bytes < need)
+    return fail(FIA_ERR_PARAM_INVALID, "blocks of %zu bytes are smaller than the %zu required", blocks_bytes, need);
+  fia::DecodeParams p{};
+  p.q = q;
+  p.q_dtype = q_dtype;
+  p.aq_scale = antiquant_scale;
+  p.aq_offset = antiquant_offset;
+  p.B = B;
+  p.Nq = Nq;
+  p.Nkv = nkv;
+  p.G = Nq / nkv;
+  p.D = 128;
+  p.scale_log2 = (float)(scale * 1.4426950408889634);
+  p.ws.qprep = static_cast<uint8_t*>(blocks);
+  cudaError_t e = fia::launch_debug_i8_qprep(p, q_hi, q_lo, kq_nq, stream);
+  if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "query preparation probe launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 }  // extern "C"
 
 namespace {
@@ -525,15 +611,17 @@ int make_tmap_thd(CUtensorMap* m, const void* base, int dtype, uint64_t D, uint6
 }
 
 // A paged K or V pool as a 3-D tensor (cols channels, block_size rows, zs blocks [x kv
-// heads]) read in boxes of 64 channels x 128 rows x 1 block: the box lands in shared
-// memory as the (64, 1, 128) box of the TND map does, 128 rows of 128 bytes.
-int make_tmap_paged(CUtensorMap* m, const void* base, int dtype, uint64_t cols, int block_size, uint64_t zs) {
+// heads]) read in boxes of 64 channels x box_rows rows x 1 block: 128 / box_rows boxes side
+// by side land in shared memory as the (64, 1, 128) box of the TND map does, 128 rows of 128
+// bytes (box_rows is a multiple of 16, so every box starts on a whole swizzle pattern).
+int make_tmap_paged(CUtensorMap* m, const void* base, int dtype, uint64_t cols, int block_size, uint64_t zs,
+                    int box_rows) {
   auto fn = encode_fn();
   if (!fn) return fail(FIA_ERR_RUNTIME, "cuTensorMapEncodeTiled is not available from the driver");
   const CUtensorMapDataType t = dtype == fia::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cuuint64_t dims[3] = {cols, (cuuint64_t)block_size, zs};
   cuuint64_t strides[2] = {cols * 2, (cuuint64_t)block_size * cols * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -547,7 +635,7 @@ int check_prefill_shape(int B, int Nq, int* Nkv, int D, int max_seqlen_q) {
   if (*Nkv == 0) *Nkv = Nq;
   if (*Nkv < 0 || Nq % *Nkv != 0)
     return fail(FIA_ERR_PARAM_INVALID, "Nq = %d is not a multiple of Nkv = %d", Nq, *Nkv);
-  if (D != 128) return fail(FIA_ERR_PARAM_INVALID, "prefill supports D = 128 in this build (got %d)", D);
+  if (D != 64 && D != 128) return fail(FIA_ERR_PARAM_INVALID, "prefill supports D = 64 or 128 in this build (got %d)", D);
   if (max_seqlen_q < 0) return fail(FIA_ERR_PARAM_INVALID, "max_seqlen_q = %d < 0", max_seqlen_q);
   if ((int64_t)B * ((max_seqlen_q + 127) / 128) >= (1LL << 31) / 256)
     return fail(FIA_ERR_PARAM_INVALID, "too many query tiles");
@@ -597,8 +685,8 @@ static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype d
   }
   if (paged) {
     const int bs = opt->block_size;
-    if (bs < 128 || bs > 512 || bs % 128 != 0)
-      return fail(FIA_ERR_PARAM_INVALID, "paged prefill needs block_size a multiple of 128 up to 512 in this build (got %d)", bs);
+    if (bs < 16 || bs > 512 || bs % 16 != 0)
+      return fail(FIA_ERR_PARAM_INVALID, "paged prefill needs block_size a multiple of 16 up to 512 (got %d)", bs);
     if (opt->kv_layout != FIA_KV_BNNBSD && opt->kv_layout != FIA_KV_BNBSH)
       return fail(FIA_ERR_PARAM_INVALID, "unknown KV layout %d", opt->kv_layout);
     if (opt->num_blocks < 1 || opt->num_blocks * Nkv >= (1LL << 31))
@@ -647,6 +735,7 @@ static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype d
     p.bt_stride = opt->bt_stride;
     p.seq_lens_kv = opt->seq_lens_kv;
     p.block_size = opt->block_size;
+    p.box_rows = gcd(opt->block_size, 128);
     p.num_blocks = opt->num_blocks;
     p.kv_x_h = bsh ? D : 0;
     p.kv_z_blk = bsh ? 1 : Nkv;
@@ -664,8 +753,8 @@ static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype d
     const bool bsh = opt->kv_layout == FIA_KV_BNBSH;
     const uint64_t cols = bsh ? (uint64_t)Nkv * D : (uint64_t)D;
     const uint64_t zs = bsh ? (uint64_t)opt->num_blocks : (uint64_t)opt->num_blocks * Nkv;
-    if (int rc = make_tmap_paged(&tmK, k, dtype, cols, opt->block_size, zs)) return rc;
-    if (int rc = make_tmap_paged(&tmV, v, dtype, cols, opt->block_size, zs)) return rc;
+    if (int rc = make_tmap_paged(&tmK, k, dtype, cols, opt->block_size, zs, p.box_rows)) return rc;
+    if (int rc = make_tmap_paged(&tmV, v, dtype, cols, opt->block_size, zs, p.box_rows)) return rc;
   } else {
     if (int rc = make_tmap_thd(&tmK, k, dtype, D, Nkv, Tkv > 0 ? Tkv : 1)) return rc;
     if (int rc = make_tmap_thd(&tmV, v, dtype, D, Nkv, Tkv > 0 ? Tkv : 1)) return rc;

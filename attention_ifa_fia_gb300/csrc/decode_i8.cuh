@@ -38,6 +38,22 @@ __device__ __forceinline__ uint32_t i8q_offset(int g, int d) {
   return box * (kI8QRows * 128) + (uint32_t)g * 128 + ((((col >> 4) ^ ((uint32_t)g & 7u))) << 4) + (col & 15u);
 }
 
+// Four int8 codes (the bytes of w, two's complement) -> two words of fp16 pairs (codes 0,1
+// and 2,3; lower code in the low half), exactly: each byte plus 128 is placed under the
+// exponent of 1024 (0x6400 | u is the half 1024 + u for u in [0, 255]), and 1152 = 1024 + 128
+// is subtracted, which leaves the code itself (an integer of at most 8 bits, exact in fp16).
+// The K and V converter warps of the int8 tensor-core kernel and the fia_debug_i8_codes
+// probe use this one function.
+__device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t& h01, uint32_t& h23) {
+  const uint32_t u = w ^ 0x80808080u;  // code + 128 per byte
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  // each half is now 1024 + code + 128; subtract 1152 (0x6480) from both halves
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h01) : "r"(a), "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h23) : "r"(b), "r"(0x64806480u));
+}
+
 // One warp prepares row g of block (b, hkv); row index R = (b * Nkv + hkv) * 16 + g.
 // Lane l handles channels 4l .. 4l + 3.
 __device__ __forceinline__ void i8_qprep_row(const DecodeParams& p, int64_t R, int lane) {

@@ -33,6 +33,8 @@
 //               operand of the PV MMA, double buffered.
 // Each code takes one integer and one half-precision operation: the byte (plus
 // 128) is placed under the exponent of 1024 and 1152 is subtracted.
+#include <algorithm>
+
 #include "decode_common.cuh"
 #include "decode_i8.cuh"
 
@@ -96,17 +98,6 @@ static_assert(sizeof(I8Smem) + 1024 <= 232448, "shared memory of the int8 decode
 __device__ __forceinline__ uint32_t i8_p_offset(int g, int t) {
   const uint32_t slab = t >> 6, col = (t & 63) * 2;
   return slab * (kNP * 128) + swz((uint32_t)g * 128 + col, 7);
-}
-
-// Four int8 codes -> two words of fp16 pairs (codes 0,1 and 2,3; lower code in the low half).
-__device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t& h01, uint32_t& h23) {
-  const uint32_t u = w ^ 0x80808080u;  // code + 128 per byte
-  uint32_t a, b;
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
-  // each half is now 1024 + code + 128; subtract 1152 (0x6480) from both halves
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h01) : "r"(a), "r"(0x64806480u));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h23) : "r"(b), "r"(0x64806480u));
 }
 
 __device__ __forceinline__ void tmem_st32w(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -632,6 +623,68 @@ cudaError_t launch_decode_i8tc_attention(const DecodeParams& p, const CUtensorMa
                                          int box_rows, int grid, cudaStream_t stream) {
   return p.q_dtype == kBF16 ? launch_i8_g<kBF16>(p, tmK, tmV, box_rows, grid, stream)
                             : launch_i8_g<kF16>(p, tmK, tmV, box_rows, grid, stream);
+}
+
+// ------------------------------------------------------------------- probes
+// The exact steps of this kernel on their own: the code -> fp16 conversion of the K and V
+// converter warps, and the query operand (q' = q * s_K as an fp16 hi + lo pair after the
+// power-of-two prescale, and the per-head constants) that the plan kernel prepares.
+namespace {
+
+__global__ void debug_i8_codes_kernel(const uint32_t* words, int64_t nw, uint2* out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nw; i += (int64_t)gridDim.x * blockDim.x) {
+    uint32_t h01, h23;
+    codes_to_f16x2(words[i], h01, h23);
+    out[i] = make_uint2(h01, h23);
+  }
+}
+
+// One warp per row of a q' block, as in the plan kernel's extra CTAs.
+__global__ void debug_i8_qprep_kernel(const DecodeParams p) {
+  const int64_t R = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (R < (int64_t)p.B * p.Nkv * kI8Heads) i8_qprep_row(p, R, threadIdx.x & 31);
+}
+
+// The blocks read back through the same layout function: hi and lo parts of row g, channel d,
+// and the {kq, nq} pair of head g.
+__global__ void debug_i8_qunpack_kernel(const uint8_t* blocks, int64_t nblk, uint16_t* hi, uint16_t* lo,
+                                        float2* kn) {
+  const int64_t n = nblk * kI8Heads * 128;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t blk = i / (kI8Heads * 128);
+    const int g = (int)(i / 128 % kI8Heads), d = (int)(i % 128);
+    const uint8_t* base = blocks + blk * kI8QBlockBytes;
+    hi[i] = *reinterpret_cast<const uint16_t*>(base + i8q_offset(g, d));
+    lo[i] = *reinterpret_cast<const uint16_t*>(base + i8q_offset(kI8Heads + g, d));
+    if (d == 0) kn[blk * kI8Heads + g] = reinterpret_cast<const float2*>(base + kI8QBytes)[g];
+  }
+}
+
+}  // namespace
+
+size_t debug_i8_qprep_block_bytes() { return kI8QBlockBytes; }
+
+cudaError_t launch_debug_i8_codes(const int8_t* codes, int64_t n, uint16_t* out, cudaStream_t stream) {
+  const int64_t nw = n / 4;
+  if (nw <= 0) return cudaSuccess;
+  const int grid = (int)std::min<int64_t>((nw + 255) / 256, 4096);
+  debug_i8_codes_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint32_t*>(codes), nw,
+                                                   reinterpret_cast<uint2*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_i8_qprep(const DecodeParams& p, uint16_t* hi, uint16_t* lo, float* kn,
+                                  cudaStream_t stream) {
+  const int64_t rows = (int64_t)p.B * p.Nkv * kI8Heads;
+  if (rows <= 0) return cudaSuccess;
+  debug_i8_qprep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t n = rows * 128;
+  const int grid = (int)std::min<int64_t>((n + 255) / 256, 4096);
+  debug_i8_qunpack_kernel<<<grid, 256, 0, stream>>>(p.ws.qprep, (int64_t)p.B * p.Nkv, hi, lo,
+                                                    reinterpret_cast<float2*>(kn));
+  return cudaGetLastError();
 }
 
 }  // namespace fia

@@ -21,7 +21,12 @@
 //     results.  Issue them on one stream, or order them.
 //   * The first call on each device looks up the array's device address with
 //     cudaGetSymbolAddress while that device is current.  Make that first call
-//     before any stream capture begins.
+//     before any stream capture begins.  The address is kept per device together
+//     with the device's context; a call that finds another context current (after
+//     a device reset, which reloads the module) looks it up again, so the first
+//     call after a reset must also come before any stream capture.
+//   * Arguments are checked exactly as fia_decode checks them (same codes, same
+//     order) before the workspace size is compared with the scratch.
 // Nothing here calls cudaMalloc, cudaFree or any allocating routine.
 #include <cstdio>
 #include <mutex>
@@ -38,26 +43,35 @@ constexpr size_t kScratchBytes = size_t(16) << 20;  // 16 MiB per device
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+  void* ctx = nullptr;  // the context the address belongs to
+  void* ptr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
-// Device address of this device's scratch array, looked up once per device with
-// the device current.  Returns 0, or a non-zero fia status.
+// Device address of this device's scratch array, looked up with the device current
+// the first time and again whenever the device's current context has changed.
+// Returns 0, or a non-zero fia status.
 int scratch_for_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fia::report_error(FIA_ERR_RUNTIME, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fia::report_error(FIA_ERR_RUNTIME, "device ordinal %d out of range", dev);
+  void* ctx = nullptr;
+  if (int rc = fia::current_context(&ctx)) return rc;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchAddr& a = g_scratch[dev];
+  if (!a.ptr || a.ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess || !p)
       return fia::report_error(FIA_ERR_RUNTIME, "cudaGetSymbolAddress of the decode scratch: %s",
                                cudaGetErrorString(e));
-    g_scratch_ptr[dev] = p;
+    if (int rc = fia::current_context(&a.ctx)) return rc;  // current now, if it was not before
+    a.ptr = p;
   }
-  *out = g_scratch_ptr[dev];
+  *out = a.ptr;
   return FIA_SUCCESS;
 }
 
@@ -69,8 +83,12 @@ extern "C" int fia_decode_noalloc(const void* q, fia_dtype q_dtype, const void* 
                                   int block_size, int64_t num_blocks, double scale, const float* antiquant_scale,
                                   const float* antiquant_offset, const float* sink, void* out, float* softmax_max,
                                   float* softmax_sum, int num_splits, fia_stream_t stream) {
+  int rc = fia::decode_check(q, q_dtype, k_cache, v_cache, kv_dtype, block_table, bt_stride, actual_seq_lengths,
+                             max_kv_len, B, Nq, Nkv, D, block_size, num_blocks, scale, antiquant_scale,
+                             antiquant_offset, sink, out, softmax_max, softmax_sum, num_splits);
+  if (rc != FIA_SUCCESS) return rc;  // the code and message fia_decode would give
   size_t need = 0;
-  int rc = fia_decode_workspace_size(B, Nq, Nkv, D, max_kv_len, block_size, num_splits, &need);
+  rc = fia_decode_workspace_size(B, Nq, Nkv, D, max_kv_len, block_size, num_splits, &need);
   if (rc != FIA_SUCCESS) return rc;  // fia_last_error() describes the bad argument
   if (need > kScratchBytes)
     return fia::report_error(FIA_ERR_PARAM_INVALID,

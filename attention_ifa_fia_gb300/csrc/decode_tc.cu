@@ -434,7 +434,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           *reinterpret_cast<uint16_t*>(pbuf + p_offset(h0 + g, r)) = h;
         }
       }
-      if (r >= meta.n && !upper) {  // rows past the keys (masked keys hold finite values)
+      // V rows of tokens that are not keys -- past the item's end, and with a key mask also
+      // masked keys and keys below a window -- are zeroed: the cache may hold anything there,
+      // NaN included, and a weight of 0 would not cancel it in the product
+      if ((r >= meta.n || (kKeyMask && !valid)) && !upper) {
         uint8_t* vrow = sm.kv[st][1];
 #pragma unroll
         for (int bx = 0; bx < C::kNumBoxes; ++bx) {

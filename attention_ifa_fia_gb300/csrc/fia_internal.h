@@ -27,6 +27,18 @@ enum : int { kKernelDecodePlan = 0, kKernelDecodeAttention = 1, kKernelDecodeMer
 // Sets the text fia_last_error() returns on this thread and returns `code`.
 int report_error(int code, const char* fmt, ...);
 
+// The calling thread's current CUDA context (a CUcontext; NULL if none is current yet).
+// Returns 0 or a non-zero fia status.
+int current_context(void** ctx);
+
+// Every check fia_decode makes on these arguments, in the same order and with the same
+// codes and messages, except those on the workspace; launches nothing.
+int decode_check(const void* q, int q_dtype, const void* k_cache, const void* v_cache, int kv_dtype,
+                 const int32_t* block_table, int64_t bt_stride, const int64_t* actual_seq_lengths, int max_kv_len,
+                 int B, int Nq, int Nkv, int D, int block_size, int64_t num_blocks, double scale,
+                 const float* antiquant_scale, const float* antiquant_offset, const float* sink, void* out,
+                 float* softmax_max, float* softmax_sum, int num_splits);
+
 // Records a CUDA event on `stream` before (phase 0) or after (phase 1) a launch
 // of `kernel` when tracing is enabled on the calling thread; otherwise nothing.
 void trace_mark(int kernel, int phase, cudaStream_t stream);
@@ -145,14 +157,16 @@ struct PrefillParams {
   // [-2^30, 2^30]); rightDownCausal is (2^30, 0), no mask (2^30, 2^30)
   int pre, next;
   // paged K/V (block_table non-null): k and v are pools of blocks of block_size tokens (a
-  // multiple of 128, so a key tile lies in one block); key tile kt of sequence b is rows
-  // (128 kt) % block_size .. of block block_table[b][128 kt / block_size], at tensor-map
-  // coordinates (x = hkv * kv_x_h + channel, y = row in block, z = blk * kv_z_blk + hkv * kv_z_h);
-  // sequence b has seq_lens_kv[b] keys (clamped to [0, max_seqlen_kv]); cu_kv is unused
+  // multiple of 16); key t of sequence b is row t % block_size of block
+  // block_table[b][t / block_size], at tensor-map coordinates (x = hkv * kv_x_h + channel,
+  // y = row in block, z = blk * kv_z_blk + hkv * kv_z_h); a key tile of 128 keys arrives as
+  // 128 / box_rows boxes of box_rows rows, each inside one block; sequence b has
+  // seq_lens_kv[b] keys (clamped to [0, max_seqlen_kv]); cu_kv is unused
   const int32_t* block_table;
   int64_t bt_stride;
   const int64_t* seq_lens_kv;
   int block_size;
+  int box_rows;  // rows of one tensor-map box: gcd(block_size, 128), so a box lies in one block
   int64_t num_blocks;
   int kv_x_h, kv_z_blk, kv_z_h;
   int dtype;          // kBF16 or kF16
@@ -174,5 +188,12 @@ cudaError_t launch_debug_dequant(const int8_t* codes, const float* scale, const 
                                  float* out, cudaStream_t stream);
 cudaError_t launch_debug_gather(const DecodeParams& p, const CUtensorMap& tmK, int box_rows, int b, int hkv,
                                 void* dst, cudaStream_t stream);
+// The int8 tensor-core kernel's exact steps: n codes (n % 4 == 0) -> fp16 bit patterns; the
+// q' blocks of p (written to p.ws.qprep, B * Nkv blocks of debug_i8_qprep_block_bytes()) and
+// their hi / lo parts (B * Nkv * 16 rows x 128) and {kq, nq} pairs (B * Nkv * 16) read back.
+size_t debug_i8_qprep_block_bytes();
+cudaError_t launch_debug_i8_codes(const int8_t* codes, int64_t n, uint16_t* out, cudaStream_t stream);
+cudaError_t launch_debug_i8_qprep(const DecodeParams& p, uint16_t* hi, uint16_t* lo, float* kn,
+                                  cudaStream_t stream);
 
 }  // namespace fia

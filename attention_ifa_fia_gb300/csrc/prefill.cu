@@ -23,6 +23,13 @@
 // epilogue.  O is rescaled only when the running row max
 // grows by more than 8 (log2 units); otherwise the stale max keeps every exponent
 // <= 2^8, and the softmax max/sum outputs are converted to the true max at the end.
+//
+// Head dim D = 64 or 128 (template parameter kD): tiles are 128 rows of D channels in
+// boxes of 64 channels; the QK product takes D / 16 K-steps and the PV product N = D.
+// Keys from a paged cache (FusedInferAttentionScore PagedAttention) arrive in boxes of
+// gcd(blockSize, 128) rows, each from its own block; rows of a key tile past the
+// sequence's keys are masked in S, and in V they are zeroed before the PV product (a
+// cache may hold anything there, NaN included, and P = 0 would not cancel a NaN).
 #include "decode_common.cuh"
 
 namespace fia {
@@ -30,23 +37,28 @@ namespace {
 
 constexpr int kQT = 128;           // queries per tile (MMA M)
 constexpr int kKT = 128;           // keys per tile (MMA N of QK, K of PV)
-constexpr int kPD = 128;           // head dim supported by this kernel
 constexpr int kPThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two column halves)
 constexpr int kSoftmaxThreads = 256;
 constexpr int kBarSoftmax = 3;   // named barrier of the softmax warps
 constexpr int kPStages = 2;
-constexpr int kTileB = kQT * kPD * 2;  // 32 KB: a Q, K or V tile
 constexpr uint32_t kRescaleThreshold = 8;  // log2 units
+
+// a Q, K or V tile: 128 rows of kD channels (kD / 64 boxes of 128 rows x 128 bytes)
+template <int kD>
+constexpr int tile_bytes() { return kQT * kD * 2; }
 
 struct __align__(16) PTileMeta {
   int b, h, q0, kvt;      // sequence, query head, first query (within the sequence), key tile
   int tq, tk, Lq, Lkv;    // first token of the sequence in q / kv, sequence lengths
   int first, last, qbuf, unit;
+  int vrows, pad0, pad1, pad2;  // rows of the V tile to keep; rows from vrows on are zeroed
 };
 
 constexpr int kMetaRing = 4;
 
+template <int kD>
 struct PSmem {
+  static constexpr int kTileB = tile_bytes<kD>();
   alignas(1024) uint8_t q[2][kTileB];
   alignas(1024) uint8_t k[kPStages][kTileB];
   alignas(1024) uint8_t v[kPStages][kTileB];
@@ -56,13 +68,16 @@ struct PSmem {
   uint64_t v_full[kPStages], v_empty[kPStages];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], p_free[2];
-  uint64_t pv_done, o_free;
+  // PV(j) completes phase j >> 1 of pv_done[j & 1]: a waiter for PV(j) is then never two
+  // phases behind (PV(j - 2) has completed once S(j) is ready) nor ahead (PV(j + 2) needs
+  // this tile's successor's P), which a parity wait on one barrier could not ensure
+  uint64_t pv_done[2], o_free;
   float rmax[2][2][kQT];  // [tile parity][column half][row]: partial row maxima
   float lsum[2][kQT];     // [column half][row]: partial row sums at the epilogue
   uint32_t tmem_base;
 };
 // The dynamic shared memory must fit the 227 KB a CTA may use.
-static_assert(sizeof(PSmem) <= 232448, "prefill shared memory exceeds the per-CTA limit");
+static_assert(sizeof(PSmem<128>) <= 232448, "prefill shared memory exceeds the per-CTA limit");
 
 // per (sequence, query tile): the key tiles holding at least one visible key, {first,
 // count}.  A row's visible keys form one interval of the band; the rows' intervals shift
@@ -98,22 +113,61 @@ __device__ __forceinline__ void seq_bounds(const PrefillParams& p, int b, int& t
   Lkv = (int)(k1 - k0);
 }
 
-// Tensor-map coordinates {x, y, z} of key tile kt of kv head hkv of sequence b (keys from
-// tk in the TND layout, or Lkv keys in the paged pool).  A paged tile past the keys (the
-// one tile of a query tile that sees none) reads block 0: it is masked entirely.  A block
-// index outside the pool raises the status flag and reads block 0 instead.
-__device__ __forceinline__ int3 key_tile_coord(const PrefillParams& p, int b, int tk, int Lkv, int kt, int hkv) {
-  if (!p.block_table) return make_int3(0, hkv, tk + kt * kKT);
-  const int tok = kt * kKT;
-  int blk = 0;
-  if (tok < Lkv) {
-    blk = p.block_table[(int64_t)b * p.bt_stride + tok / p.block_size];
-    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-      raise_status(p.status, kStatusBadBlockIndex);
-      blk = 0;
-    }
+// Issues the TMA loads of key tile kt of kv head hkv of sequence b (keys from tk in the TND
+// layout, or Lkv keys in the paged pool) into dst, completing on bar: kD / 64 boxes of 64
+// channels, and in the paged pool 128 / box_rows boxes of box_rows rows along the tile, each
+// from its own block.  A paged box past the keys (rows the tile masks) reads block 0; a block
+// index outside the pool raises the status flag and reads block 0 instead.  The bytes that
+// land are always tile_bytes<kD>().
+template <int kD>
+__device__ __forceinline__ void load_key_tile(uint8_t* dst, const CUtensorMap* m, const PrefillParams& p, int b,
+                                              int tk, int Lkv, int kt, int hkv, uint64_t* bar) {
+  constexpr int kBoxes = kD / 64;
+  if (!p.block_table) {
+#pragma unroll
+    for (int bx = 0; bx < kBoxes; ++bx) tma_load_3d(dst + bx * (kKT * 128), m, bx * 64, hkv, tk + kt * kKT, bar);
+    return;
   }
-  return make_int3(hkv * p.kv_x_h, tok % p.block_size, blk * p.kv_z_blk + hkv * p.kv_z_h);
+  const int rows = p.box_rows, n = kKT / rows;
+  int32_t blk[8];  // block of each box (at most 8: box_rows >= 16); the table loads are independent
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int tok = kt * kKT + i * rows;
+    blk[i] = (i < n && tok < Lkv) ? p.block_table[(int64_t)b * p.bt_stride + tok / p.block_size] : 0;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i >= n) break;
+    if (blk[i] < 0 || (int64_t)blk[i] >= p.num_blocks) {
+      raise_status(p.status, kStatusBadBlockIndex);
+      blk[i] = 0;
+    }
+    const int tok = kt * kKT + i * rows;
+    const int z = blk[i] * p.kv_z_blk + hkv * p.kv_z_h;
+#pragma unroll
+    for (int bx = 0; bx < kBoxes; ++bx)
+      tma_load_3d(dst + bx * (kKT * 128) + i * rows * 128, m, hkv * p.kv_x_h + bx * 64, tok % p.block_size, z, bar);
+  }
+}
+
+// Rows of key tile kt that hold keys of a paged sequence of Lkv keys (the rest are zeroed in
+// V); a TND tile keeps every row (rows past the sequence are the next sequence's keys, or
+// zeros that TMA fills past the tensor's end).
+__device__ __forceinline__ int v_rows_kept(const PrefillParams& p, int Lkv, int kt) {
+  return p.block_table ? min(max(Lkv - kt * kKT, 0), kKT) : kKT;
+}
+
+// Zeroes rows [vrows, 128) of a V tile in shared memory (every box), by the 32 lanes of a
+// warp, and makes the stores visible to the tensor cores (async proxy).
+template <int kD>
+__device__ __forceinline__ void zero_v_rows(uint8_t* vt, int vrows, int lane) {
+  const int n16 = (kKT - vrows) * 8;  // 16-byte chunks per box (a row is 128 bytes of a box)
+#pragma unroll
+  for (int bx = 0; bx < kD / 64; ++bx)
+    for (int i = lane; i < n16; i += 32)
+      *reinterpret_cast<uint4*>(vt + bx * (kKT * 128) + vrows * 128 + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ plan
@@ -243,12 +297,15 @@ __device__ __forceinline__ void umma_f16_ta_w(uint32_t d_tmem, uint32_t a_tmem, 
 // kBand: a band's lower edge may fall inside a key tile (pre_tokens below the longest key
 // sequence); without it the lower edge is never inside a tile and the softmax masks the
 // upper edge only.
-template <int DT, bool kBand>
+template <int kD, int DT, bool kBand>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+  using Sm = PSmem<kD>;
+  constexpr int kTileB = Sm::kTileB;
+  constexpr int kOH = kD / 2;  // output channels per softmax half
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  PSmem& sm = *reinterpret_cast<PSmem*>(smem_raw);
+  Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (smem_u32(smem_raw) & 1023u) {  // the swizzled operand layouts need 1 KB alignment
     if (tid == 0) raise_status(p.status, kStatusWaitTimeout);
@@ -270,7 +327,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&sm.v_full[st], 1);
       mbar_init(&sm.v_empty[st], 1);
     }
-    mbar_init(&sm.pv_done, 1);
+    mbar_init(&sm.pv_done[0], 1);
+    mbar_init(&sm.pv_done[1], 1);
     mbar_init(&sm.o_free, 8);
     fence_mbar_init();
   }
@@ -279,7 +337,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // S: 2 x 128, O: 128, P: 2 x 64
+  constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // S: 2 x 128, O: kD, P: 2 x 64
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -290,17 +348,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int n_units = p.tile_counter[1];
       const int G = p.G;
       int j = 0, u_local = 0;
-      int v_next = 0;             // next tile whose V is to be loaded
-      int3 ring_xyz[kMetaRing];  // tensor-map coordinates of the K and V tiles in flight
+      int v_next = 0;  // next tile whose V is to be loaded
       bool ok = true;
       // V of tile jv, one tile behind its K
       auto load_v = [&](int jv) -> bool {
         const int st = jv % kPStages;
         if (!mbar_wait(&sm.v_empty[st], ((uint32_t)(jv / kPStages) & 1u) ^ 1u, p.status)) return false;
+        const PTileMeta& m = sm.meta[jv % kMetaRing];
         mbar_arrive_expect_tx(&sm.v_full[st], kTileB);
-        for (int bx = 0; bx < 2; ++bx)
-          tma_load_3d(sm.v[st] + bx * (kKT * 128), &tmV, ring_xyz[jv % kMetaRing].x + bx * 64,
-                      ring_xyz[jv % kMetaRing].y, ring_xyz[jv % kMetaRing].z, &sm.v_full[st]);
+        load_key_tile<kD>(sm.v[st], &tmV, p, m.b, m.tk, m.Lkv, m.kvt, m.h / G, &sm.v_full[st]);
         return true;
       };
       while (ok) {
@@ -316,7 +372,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int qb = u_local & 1;
         if (!mbar_wait(&sm.q_empty[qb], ((uint32_t)(u_local >> 1) & 1u) ^ 1u, p.status)) { ok = false; break; }
         mbar_arrive_expect_tx(&sm.q_full[qb], kTileB);
-        for (int bx = 0; bx < 2; ++bx)
+        for (int bx = 0; bx < kD / 64; ++bx)
           tma_load_3d(sm.q[qb] + bx * (kQT * 128), &tmQ, bx * 64, h, tq + q0, &sm.q_full[qb]);
         const int hkv = h / G;
         for (int i = 0; i < nkv; ++i, ++j) {
@@ -327,11 +383,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
           m.b = b; m.h = h; m.q0 = q0; m.kvt = kt;
           m.tq = tq; m.tk = tk; m.Lq = Lq; m.Lkv = Lkv;
           m.first = i == 0; m.last = i == nkv - 1; m.qbuf = qb; m.unit = u;
-          const int3 c = key_tile_coord(p, b, tk, Lkv, kt, hkv);
-          ring_xyz[j % kMetaRing] = c;
+          m.vrows = v_rows_kept(p, Lkv, kt);
           mbar_arrive_expect_tx(&sm.k_full[st], kTileB);
-          for (int bx = 0; bx < 2; ++bx)
-            tma_load_3d(sm.k[st] + bx * (kKT * 128), &tmK, c.x + bx * 64, c.y, c.z, &sm.k_full[st]);
+          load_key_tile<kD>(sm.k[st], &tmK, p, b, tk, Lkv, kt, hkv, &sm.k_full[st]);
           if (v_next < j) {
             if (!load_v(v_next)) { ok = false; break; }
             ++v_next;
@@ -352,30 +406,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer (whole warp)
+    // All lanes wait; one elected lane issues and commits (a converged warp issues sooner than
+    // one thread in a divergent branch), and the lanes together zero V rows when needed.
+    {
       constexpr uint32_t idesc_qk = umma_idesc_f16(DT == kBF16, 0, 0, kQT, kKT);
-      constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 0, 1, kQT, kPD);
+      constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 0, 1, kQT, kD);
       int o_uses = 0;  // units whose first PV (which overwrites O) has been issued
       // O += P(jj) . V(jj), P from TMEM; the first PV of a unit overwrites O, after the
       // previous unit's epilogue has read it (o_free phase o_uses - 1)
       auto issue_pv = [&](int jj, bool first_of_unit) -> bool {
         const int pb = jj & 1, vs = jj % kPStages;
-        if (!mbar_wait(&sm.p_full[pb], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
-        if (!mbar_wait(&sm.v_full[vs], (uint32_t)(jj / kPStages) & 1u, p.status)) return false;
-        if (first_of_unit && o_uses > 0 && !mbar_wait(&sm.o_free, (uint32_t)(o_uses - 1) & 1u, p.status))
+        const int vrows = sm.meta[jj % kMetaRing].vrows;  // (slot not yet reused: see the producer)
+        if (!mbar_wait_warp(&sm.p_full[pb], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
+        if (!mbar_wait_warp(&sm.v_full[vs], (uint32_t)(jj / kPStages) & 1u, p.status)) return false;
+        if (first_of_unit && o_uses > 0 && !mbar_wait_warp(&sm.o_free, (uint32_t)(o_uses - 1) & 1u, p.status))
           return false;
+        if (vrows < kKT) zero_v_rows<kD>(sm.v[vs], vrows, lane);
         tc_fence_after();
         const uint32_t vbase = smem_u32(sm.v[vs]);
 #pragma unroll
         for (int s = 0; s < kKT / 16; ++s) {
           const uint64_t bd = umma_desc(vbase + s * 16 * 128, kKT * 128, 1024);
-          umma_f16_ta(tmem + kColO, tmem + kColP + pb * 64 + s * 8, bd, idesc_pv,
-                      (first_of_unit && s == 0) ? 0u : 1u);
+          umma_f16_ta_w(tmem + kColO, tmem + kColP + pb * 64 + s * 8, bd, idesc_pv,
+                        (first_of_unit && s == 0) ? 0u : 1u);
         }
-        umma_commit(&sm.pv_done);
-        umma_commit(&sm.p_free[pb]);
-        umma_commit(&sm.v_empty[vs]);
+        umma_commit_w(&sm.pv_done[pb]);
+        umma_commit_w(&sm.p_free[pb]);
+        umma_commit_w(&sm.v_empty[vs]);
         if (first_of_unit) ++o_uses;
         return true;
       };
@@ -383,46 +441,47 @@ __global__ void __launch_bounds__(kPThreads, 1)
       bool prev_first = false;
       while (true) {
         const int st = j % kPStages;
-        if (!mbar_wait(&sm.k_full[st], (uint32_t)(j / kPStages) & 1u, p.status)) break;
-        const PTileMeta meta = sm.meta[j % kMetaRing];
-        if (meta.unit < 0) {
+        if (!mbar_wait_warp(&sm.k_full[st], (uint32_t)(j / kPStages) & 1u, p.status)) break;
+        const PTileMeta& meta = sm.meta[j % kMetaRing];
+        const int unit = meta.unit, first = meta.first, last = meta.last, qb = meta.qbuf;
+        if (unit < 0) {
           if (j > 0) issue_pv(j - 1, prev_first);
-          mbar_arrive(&sm.s_full[j & 1]);  // lets the softmax warps see the sentinel
+          if (lane == 0) mbar_arrive(&sm.s_full[j & 1]);  // lets the softmax warps see the sentinel
           break;
         }
-        const int qb = meta.qbuf;
-        if (meta.first && !mbar_wait(&sm.q_full[qb], (uint32_t)(u_local >> 1) & 1u, p.status)) break;
+        if (first && !mbar_wait_warp(&sm.q_full[qb], (uint32_t)(u_local >> 1) & 1u, p.status)) break;
         const int sb = j & 1;
-        if (!mbar_wait(&sm.s_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
+        if (!mbar_wait_warp(&sm.s_free[sb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
         tc_fence_after();
         const uint32_t qbase = smem_u32(sm.q[qb]), kbase = smem_u32(sm.k[st]);
 #pragma unroll
-        for (int s = 0; s < kPD / 16; ++s) {
+        for (int s = 0; s < kD / 16; ++s) {
           const uint64_t a = umma_desc(qbase + (s >> 2) * (kQT * 128) + (s & 3) * 32, 16, 1024);
           const uint64_t bd = umma_desc(kbase + (s >> 2) * (kKT * 128) + (s & 3) * 32, 16, 1024);
-          umma_f16(tmem + kColS + sb * kKT, a, bd, idesc_qk, s > 0);
+          umma_f16_w(tmem + kColS + sb * kKT, a, bd, idesc_qk, s > 0);
         }
-        umma_commit(&sm.s_full[sb]);
-        umma_commit(&sm.k_empty[st]);
-        if (meta.last) {
-          umma_commit(&sm.q_empty[qb]);
+        umma_commit_w(&sm.s_full[sb]);
+        umma_commit_w(&sm.k_empty[st]);
+        if (last) {
+          umma_commit_w(&sm.q_empty[qb]);
           ++u_local;
         }
         if (j > 0 && !issue_pv(j - 1, prev_first)) break;
-        prev_first = meta.first;
+        prev_first = first;
         ++j;
       }
     }
   } else {
     // ------------------------------------------------------------------ softmax, rescale, epilogue
     // Two warpgroups split each query row: half 0 owns key columns 0-63 of S (and output
-    // channels 0-63 of O), half 1 columns 64-127.  Only the per-row tile maximum (and, at
-    // the end, the row sum) is exchanged through shared memory.
+    // channels [0, kD/2) of O), half 1 columns 64-127 (and channels [kD/2, kD)).  Only the
+    // per-row tile maximum (and, at the end, the row sum) is exchanged through shared memory.
     const int half = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // query row of the tile = TMEM lane
     const uint32_t tq_lane = tmem + ((uint32_t)(quad * 32) << 16);
-    const int c_base = half * 64;
+    const int c_base = half * 64;   // key columns of this half
+    const int o_base = half * kOH;  // output channels of this half
     float m_run = -INFINITY;   // max used for the exponents (may lag the true max by < 2^8)
     float m_true = -INFINITY;  // true running max
     float l_run = 0.f;         // this half's sum of exponents relative to m_run
@@ -499,16 +558,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // tcgen05.ld/st are warp-collective (.sync.aligned), so the whole warp takes part,
       // rows that do not need it with a factor of 1.
       if (__any_sync(0xffffffffu, rescale && !meta.first)) {
-        if (!mbar_wait(&sm.pv_done, (uint32_t)(j - 1) & 1u, p.status)) break;
+        if (!mbar_wait(&sm.pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, p.status)) break;
         const float f = (rescale && !meta.first) ? alpha : 1.f;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
+        for (int c = 0; c < kOH; c += 32) {
           float o[32];
-          tmem_ld32(tq_lane + kColO + c_base + c, o);
+          tmem_ld32(tq_lane + kColO + o_base + c, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= f;
-          tmem_st32(tq_lane + kColO + c_base + c, o);
+          tmem_st32(tq_lane + kColO + o_base + c, o);
         }
       }
       // this half of P row r (64 keys = 32 packed columns) into the P buffer of this tile
@@ -520,7 +579,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (lane == 0) mbar_arrive(&sm.p_full[sb]);
       if (meta.last) {
         // epilogue: wait for this tile's PV, normalise O and write out, max and sum
-        if (!mbar_wait(&sm.pv_done, (uint32_t)j & 1u, p.status)) break;
+        if (!mbar_wait(&sm.pv_done[j & 1], (uint32_t)(j >> 1) & 1u, p.status)) break;
         tc_fence_after();
         sm.lsum[half][r] = l_run;
         named_bar_sync(kBarSoftmax, kSoftmaxThreads);
@@ -532,11 +591,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const float inv = denom > 0.f ? 1.f / denom : 0.f;
         const int64_t tok = (int64_t)meta.tq + qi;
         // every lane takes part in the (warp-collective) TMEM loads; only valid rows store
-        uint8_t* orow = static_cast<uint8_t*>(p.out) + ((tok * p.Nq + meta.h) * (int64_t)kPD + c_base) * 2;
+        uint8_t* orow = static_cast<uint8_t*>(p.out) + ((tok * p.Nq + meta.h) * (int64_t)kD + o_base) * 2;
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
+        for (int c = 0; c < kOH; c += 32) {
           float o[32];
-          tmem_ld32(tq_lane + kColO + c_base + c, o);
+          tmem_ld32(tq_lane + kColO + o_base + c, o);
           if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
@@ -616,7 +675,9 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+template <int kD>
 struct P2Smem {
+  static constexpr int kTileB = tile_bytes<kD>();
   alignas(1024) uint8_t q[2][kTileB];  // head A, head B of the current unit
   alignas(1024) uint8_t k[kPStages][kTileB];
   alignas(1024) uint8_t v[kPStages][kTileB];
@@ -630,14 +691,16 @@ struct P2Smem {
   int stop;                                   // set by the MMA warp after the last tile
   uint32_t tmem_base;
 };
-static_assert(sizeof(P2Smem) <= 232448, "prefill shared memory exceeds the per-CTA limit");
+static_assert(sizeof(P2Smem<128>) <= 232448, "prefill shared memory exceeds the per-CTA limit");
 
-template <int DT, bool kBand>
+template <int kD, int DT, bool kBand>
 __global__ void __launch_bounds__(kP2Threads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+  using Sm = P2Smem<kD>;
+  constexpr int kTileB = Sm::kTileB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  P2Smem& sm = *reinterpret_cast<P2Smem*>(smem_raw);
+  Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (smem_u32(smem_raw) & 1023u) {  // the swizzled operand layouts need 1 KB alignment
     if (tid == 0) raise_status(p.status, kStatusWaitTimeout);
@@ -679,15 +742,13 @@ __global__ void __launch_bounds__(kP2Threads, 1)
       const int n_units = p.tile_counter[1];
       const int npairs = p.Nq / 2;
       int j = 0, u_local = 0, v_next = 0;
-      int3 ring_xyz[kMetaRing];  // tensor-map coordinates of the K and V tiles in flight
       bool ok = true;
       auto load_v = [&](int jv) -> bool {  // V of tile jv, one tile behind its K
         const int st = jv % kPStages;
         if (!mbar_wait(&sm.v_empty[st], ((uint32_t)(jv / kPStages) & 1u) ^ 1u, p.status)) return false;
+        const PTileMeta& m = sm.meta[jv % kMetaRing];
         mbar_arrive_expect_tx(&sm.v_full[st], kTileB);
-        for (int bx = 0; bx < 2; ++bx)
-          tma_load_3d(sm.v[st] + bx * (kKT * 128), &tmV, ring_xyz[jv % kMetaRing].x + bx * 64,
-                      ring_xyz[jv % kMetaRing].y, ring_xyz[jv % kMetaRing].z, &sm.v_full[st]);
+        load_key_tile<kD>(sm.v[st], &tmV, p, m.b, m.tk, m.Lkv, m.kvt, m.h / p.G, &sm.v_full[st]);
         return true;
       };
       while (ok) {
@@ -705,7 +766,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         if (!mbar_wait(&sm.q_empty, ((uint32_t)u_local & 1u) ^ 1u, p.status)) { ok = false; break; }
         mbar_arrive_expect_tx(&sm.q_full, 2 * kTileB);
         for (int x = 0; x < 2; ++x)
-          for (int bx = 0; bx < 2; ++bx)
+          for (int bx = 0; bx < kD / 64; ++bx)
             tma_load_3d(sm.q[x] + bx * (kQT * 128), &tmQ, bx * 64, h0 + x, tq + q0, &sm.q_full);
         const int hkv = h0 / p.G;
         for (int i = 0; i < nkv; ++i, ++j) {
@@ -716,11 +777,9 @@ __global__ void __launch_bounds__(kP2Threads, 1)
           m.b = b; m.h = h0; m.q0 = q0; m.kvt = kt;
           m.tq = tq; m.tk = tk; m.Lq = Lq; m.Lkv = Lkv;
           m.first = i == 0; m.last = i == nkv - 1; m.qbuf = 0; m.unit = u;
-          const int3 c = key_tile_coord(p, b, tk, Lkv, kt, hkv);
-          ring_xyz[j % kMetaRing] = c;
+          m.vrows = v_rows_kept(p, Lkv, kt);
           mbar_arrive_expect_tx(&sm.k_full[st], kTileB);
-          for (int bx = 0; bx < 2; ++bx)
-            tma_load_3d(sm.k[st] + bx * (kKT * 128), &tmK, c.x + bx * 64, c.y, c.z, &sm.k_full[st]);
+          load_key_tile<kD>(sm.k[st], &tmK, p, b, tk, Lkv, kt, hkv, &sm.k_full[st]);
           if (v_next < j) {
             if (!load_v(v_next)) { ok = false; break; }
             ++v_next;
@@ -750,25 +809,27 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     // ------------------------------------------------------------------ MMA issuer (whole warp)
     {
       constexpr uint32_t idesc_qk = umma_idesc_f16(DT == kBF16, 0, 0, kQT, kKT);
-      constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 0, 1, kQT, kPD);
+      constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 0, 1, kQT, kD);
       const uint64_t qdesc[2] = {umma_desc(smem_u32(sm.q[0]), 16, 1024), umma_desc(smem_u32(sm.q[1]), 16, 1024)};
       int o_units0 = 0, o_units1 = 0;  // units whose first PV into O_A / O_B has been issued
       int u_local = 0;
       auto qk = [&](int x, int jj) {
         const uint64_t b0 = umma_desc(smem_u32(sm.k[jj % kPStages]), 16, 1024);
 #pragma unroll
-        for (int s = 0; s < kPD / 16; ++s) {
+        for (int s = 0; s < kD / 16; ++s) {
           const uint32_t off = (uint32_t)(((s >> 2) * (kQT * 128) + (s & 3) * 32) >> 4);
           umma_f16_w(tmem + kColS[x], qdesc[x] + off, b0 + off, idesc_qk, s > 0);
         }
         umma_commit_w(&sm.s_full[x]);
       };
-      // flags of a tile: bit 0 first, bit 1 last
-      auto pv = [&](int x, int jj, int flags) -> bool {
+      // flags of a tile: bit 0 first, bit 1 last; vrows: rows of its V tile to keep (head A
+      // zeroes the rest, once, before its product)
+      auto pv = [&](int x, int jj, int flags, int vrows) -> bool {
         if (!mbar_wait_warp(&sm.p_full[x], (uint32_t)jj & 1u, p.status)) return false;
         if (!mbar_wait_warp(&sm.v_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return false;
         int& ou = x ? o_units1 : o_units0;
         if ((flags & 1) && ou > 0 && !mbar_wait_warp(&sm.o_free[x], (uint32_t)(ou - 1) & 1u, p.status)) return false;
+        if (x == 0 && vrows < kKT) zero_v_rows<kD>(sm.v[jj % kPStages], vrows, lane);
         tc_fence_after();
         const uint64_t b0 = umma_desc(smem_u32(sm.v[jj % kPStages]), kKT * 128, 1024);
 #pragma unroll
@@ -781,17 +842,20 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         if (flags & 1) ++ou;
         return true;
       };
-      // waits for K of tile jj; returns its flags, -1 at the sentinel, -2 on error
-      auto load_tile = [&](int jj) -> int {
+      // waits for K of tile jj; returns its flags, -1 at the sentinel, -2 on error; *vrows
+      // receives the rows of its V tile to keep
+      auto load_tile = [&](int jj, int* vrows) -> int {
         if (!mbar_wait_warp(&sm.k_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return -2;
         const PTileMeta& m = sm.meta[jj % kMetaRing];
         if (m.unit < 0) return -1;
         const int flags = (m.first ? 1 : 0) | (m.last ? 2 : 0);
+        *vrows = m.vrows;
         if ((flags & 1) && !mbar_wait_warp(&sm.q_full, (uint32_t)u_local & 1u, p.status)) return -2;
         tc_fence_after();
         return flags;
       };
-      int cur = load_tile(0);
+      int vr_cur = kKT, vr_nxt = kKT;
+      int cur = load_tile(0, &vr_cur);
       if (cur >= 0) {
         qk(0, 0);
         qk(1, 0);
@@ -799,17 +863,18 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         if (cur & 2) { umma_commit_w(&sm.q_empty); ++u_local; }
       }
       for (int j = 0; cur >= 0; ++j) {
-        if (!pv(0, j, cur)) break;
-        const int nxt = load_tile(j + 1);
+        if (!pv(0, j, cur, vr_cur)) break;
+        const int nxt = load_tile(j + 1, &vr_nxt);
         if (nxt == -2) break;
         if (nxt >= 0) qk(0, j + 1);
-        if (!pv(1, j, cur)) break;
+        if (!pv(1, j, cur, vr_cur)) break;
         if (nxt >= 0) {
           qk(1, j + 1);
           umma_commit_w(&sm.k_empty[(j + 1) % kPStages]);
           if (nxt & 2) { umma_commit_w(&sm.q_empty); ++u_local; }
         }
         cur = nxt;
+        vr_cur = vr_nxt;
       }
       // No more tiles.  The softmax warps have consumed every S phase (PV of the last tile
       // waited for their P), so a plain arrival completes the next one and they see the flag.
@@ -917,7 +982,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         const float f = (rescale && !meta.first) ? alpha : 1.f;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kPD; c += 32) {
+        for (int c = 0; c < kD; c += 32) {
           float o[32];
           tmem_ld32(tl + kColO[x] + c, o);
 #pragma unroll
@@ -947,13 +1012,13 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         uint8_t* stg = sm.ostage[warp - 2];
         const int row0 = meta.q0 + quad * 32;  // query row of lane 0
         const int rows_ok = min(max(meta.Lq - row0, 0), 32);
-        uint8_t* obase = static_cast<uint8_t*>(p.out) + (((int64_t)meta.tq + row0) * p.Nq + h) * (int64_t)kPD * 2;
-        const int64_t orow_stride = (int64_t)p.Nq * kPD * 2;
+        uint8_t* obase = static_cast<uint8_t*>(p.out) + (((int64_t)meta.tq + row0) * p.Nq + h) * (int64_t)kD * 2;
+        const int64_t orow_stride = (int64_t)p.Nq * kD * 2;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int half = 0; half < kD / 64; ++half) {
           float o[64];
           tmem_ld64(tl + kColO[x] + half * 64, o);
-          if (half == 1) {  // every read of O_x is done: the next unit may overwrite it
+          if (half == kD / 64 - 1) {  // every read of O_x is done: the next unit may overwrite it
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.o_free[x]);
@@ -1009,11 +1074,36 @@ size_t prefill_workspace_bytes(int B, int Nq, int max_seqlen_q) {
   return 256 + (size_t)(pairs > 0 ? pairs : 1) * sizeof(int);
 }
 
+namespace {
+
+template <int kD, int DT>
+cudaError_t launch_prefill_attention(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                     const CUtensorMap& tmV, int num_sms, cudaStream_t stream) {
+  // a query sees keys d + i - pre.. with d + i <= Lkv - 1: a lower edge inside the keys needs
+  // pre < the longest key sequence
+  const bool band = p.pre < p.max_seqlen_kv;
+  if (p.G % 2 == 0) {  // heads 2hp and 2hp + 1 share a kv head
+    const size_t smem = sizeof(P2Smem<kD>);
+    auto kern = band ? prefill_pair_kernel<kD, DT, true> : prefill_pair_kernel<kD, DT, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(kern, num_sms, kP2Threads, smem, stream, tmQ, tmK, tmV, p);
+  }
+  const size_t smem = sizeof(PSmem<kD>);
+  auto kern = band ? prefill_tc_kernel<kD, DT, true> : prefill_tc_kernel<kD, DT, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms, kPThreads, smem, stream>>>(tmQ, tmK, tmV, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                            const CUtensorMap& tmV, int num_sms, cudaStream_t stream) {
   const int max_key_tiles = (p.max_seqlen_kv + kKT - 1) / kKT + 1;
   trace_mark(kKernelPrefill, 0, stream);
-  const bool pairs = p.G % 2 == 0;  // heads 2hp and 2hp + 1 share a kv head
+  const bool pairs = p.G % 2 == 0;
   const size_t plan_smem = prefill_plan_smem(max_key_tiles);
   cudaError_t e = cudaSuccess;
   if (plan_smem > 48 * 1024) {
@@ -1022,28 +1112,14 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const
   }
   e = launch_dependent(prefill_plan_kernel, 1, 1024, plan_smem, stream, p, max_key_tiles, pairs ? 2 : 1);
   if (e != cudaSuccess) return e;
-  // a query sees keys d + i - pre.. with d + i <= Lkv - 1: a lower edge inside the keys needs
-  // pre < the longest key sequence
-  const bool band = p.pre < p.max_seqlen_kv;
-  if (pairs) {
-    const size_t smem2 = sizeof(P2Smem);
-    auto kern = p.dtype == kBF16 ? (band ? prefill_pair_kernel<kBF16, true> : prefill_pair_kernel<kBF16, false>)
-                                 : (band ? prefill_pair_kernel<kF16, true> : prefill_pair_kernel<kF16, false>);
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-    if (e != cudaSuccess) return e;
-    e = launch_dependent(kern, num_sms, kP2Threads, smem2, stream, tmQ, tmK, tmV, p);
-    if (e != cudaSuccess) return e;
-    trace_mark(kKernelPrefill, 1, stream);
-    return cudaGetLastError();
-  }
-  const size_t smem = sizeof(PSmem);
-  auto kern = p.dtype == kBF16 ? (band ? prefill_tc_kernel<kBF16, true> : prefill_tc_kernel<kBF16, false>)
-                               : (band ? prefill_tc_kernel<kF16, true> : prefill_tc_kernel<kF16, false>);
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  kern<<<num_sms, kPThreads, smem, stream>>>(tmQ, tmK, tmV, p);
+  if (p.D == 64)
+    e = p.dtype == kBF16 ? launch_prefill_attention<64, kBF16>(p, tmQ, tmK, tmV, num_sms, stream)
+                         : launch_prefill_attention<64, kF16>(p, tmQ, tmK, tmV, num_sms, stream);
+  else
+    e = p.dtype == kBF16 ? launch_prefill_attention<128, kBF16>(p, tmQ, tmK, tmV, num_sms, stream)
+                         : launch_prefill_attention<128, kF16>(p, tmQ, tmK, tmV, num_sms, stream);
   trace_mark(kKernelPrefill, 1, stream);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace fia

@@ -182,8 +182,7 @@ def cpu_baseline(case: W.DecodeCase, budget_s: float = 15.0, seed: int = 0):
 def run_ours(args, rank, world, local_rank):
     import torch
     import attention_ifa_fia_gb300 as F
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from parity import DeviceDecode
+    from fia_workloads import DeviceDecode
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -362,8 +361,7 @@ def prefill_flops(case: W.PrefillCase, causal=True) -> int:
 def run_prefill_bench(args, rank, world, local_rank):
     import torch
     import attention_ifa_fia_gb300 as F
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from parity import DevicePrefill
+    from fia_workloads import DevicePrefill
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)

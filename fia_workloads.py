@@ -271,6 +271,54 @@ def causal_prefill_tnd(seed: int = 1004) -> PrefillCase:
     return make_prefill_case(Nq=32, Nkv=8, D=128, dtype=BF16, B=8, len_range=(1, 2048), seed=seed)
 
 
+# ---------------------------------------------------------------- device copies
+# Upload of a case's arrays to a CUDA device, bit for bit (torch is imported only here, so
+# the oracle's CPU tests need no GPU stack).  No arithmetic of the method happens here.
+_TORCH_NAME = {BF16: "bfloat16", FP16: "float16"}
+
+
+def device_bits(bits: np.ndarray, dtype: str, device="cuda"):
+    """uint16 storage bits -> device tensor of the storage dtype (bit-exact)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+    return t.view(getattr(torch, _TORCH_NAME[dtype]))
+
+
+class DeviceDecode:
+    """A DecodeCase resident on a CUDA device."""
+
+    def __init__(self, case: DecodeCase, device="cuda"):
+        import torch
+        self.case = case
+        self.q = device_bits(case.q, case.dtype, device)
+        if case.kv_dtype == INT8:
+            self.k = torch.from_numpy(case.k_cache).to(device)
+            self.v = torch.from_numpy(case.v_cache).to(device)
+            self.aq_scale = torch.from_numpy(case.aq_scale).to(device)
+            self.aq_offset = None if case.aq_offset is None else torch.from_numpy(case.aq_offset).to(device)
+        else:
+            self.k = device_bits(case.k_cache, case.kv_dtype, device)
+            self.v = device_bits(case.v_cache, case.kv_dtype, device)
+            self.aq_scale = self.aq_offset = None
+        self.bt = torch.from_numpy(case.block_table).to(device)
+        self.lens = torch.from_numpy(case.lengths.astype(np.int64)).to(device)
+        self.sink = None if case.sink is None else torch.from_numpy(case.sink).to(device)
+
+
+class DevicePrefill:
+    """A PrefillCase resident on a CUDA device."""
+
+    def __init__(self, case: PrefillCase, device="cuda"):
+        import torch
+        self.case = case
+        self.q = device_bits(case.q, case.dtype, device)
+        self.k = device_bits(case.k, case.dtype, device)
+        self.v = device_bits(case.v, case.dtype, device)
+        self.cu_q = torch.from_numpy(case.cu_q).to(device)
+        self.cu_kv = torch.from_numpy(case.cu_kv).to(device)
+        self.sink = None if case.sink is None else torch.from_numpy(case.sink).to(device)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "bf16_gqa_decode": bf16_gqa_decode,

@@ -158,8 +158,8 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
  *                           or NULL: byte b * atten_mask_stride + t nonzero removes key t of
  *                           batch b from the softmax (1 = masked out).  A batch whose keys are
  *                           all masked gives the rows of an empty sequence (out 0, max -inf,
- *                           sum 0, or the sink's values).  Masked keys' values are still read
- *                           (weighted by 0): they must be finite.
+ *                           sum 0, or the sink's values).  Masked keys contribute nothing,
+ *                           whatever the cache holds for them (NaN included).
  * options->atten_mask_stride  S, bytes per mask row; >= max_kv_len.
  * options->quant_scale2     device fp32 or NULL.  Non-NULL makes out an int8 (B, Nq, D) tensor:
  *                           out = saturate(round-half-even(o * quant_scale2[c] +
@@ -237,7 +237,7 @@ int fia_decode_noalloc(const void* q, fia_dtype q_dtype, const void* k_cache, co
  * k, v             device (Tkv, Nkv, D) row-major, same dtype, 16-byte aligned.
  * cu_seqlens_q/kv  device int64 (B + 1), cu[0] = 0, non-decreasing, cu[B] = T (resp. Tkv).
  * max_seqlen_q/kv  host upper bounds of the per-sequence lengths (max_seqlen_kv <= 2^20 here).
- * D                128 in this build; Nq % Nkv == 0; max_seqlen_q must bound every Lq.
+ * D                64 or 128 in this build; Nq % Nkv == 0; max_seqlen_q must bound every Lq.
  * mask             0 (none) or 3 (rightDownCausal); 4 (band) through fia_prefill_ex.
  * sink             device fp32 (Nq) or NULL.
  * softmax_max/sum  device fp32 (T, Nq) or NULL.
@@ -268,12 +268,14 @@ int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, co
  *   block_size, Nkv * D) with FIA_KV_BNBSH -- key j of sequence b is row j % block_size of
  *   block block_table[b * bt_stride + j / block_size]; sequence b has seq_lens_kv[b] keys
  *   (device int64 (B), clamped to [0, max_seqlen_kv] with FIA_STATUS_LENGTH_CLAMPED);
- *   cu_seqlens_kv and Tkv are not used.  block_size is a multiple of 128 up to 512 in this
- *   build (a key tile of 128 then lies in one block); max_seqlen_kv <= bt_stride * block_size.  A block
+ *   cu_seqlens_kv and Tkv are not used.  block_size is a multiple of 16 up to 512
+ *   (aclnnIncreFlashAttentionV3, "Constraints / page attention"); a key tile of 128 keys is
+ *   read in gcd(block_size, 128)-row pieces, one block each.  max_seqlen_kv <= bt_stride *
+ *   block_size.  A block
  *   index outside [0, num_blocks) raises FIA_STATUS_BAD_BLOCK_INDEX.  Queries stay TND: a
- *   sequence's Lq queries are its last Lq positions (the rightDownCausal diagonal).  The
- *   rows of a sequence's last block past its length are read and weighted by 0, so they
- *   must hold finite values (a cache cleared once at allocation satisfies this).
+ *   sequence's Lq queries are its last Lq positions (the rightDownCausal diagonal).  Rows
+ *   of a sequence's last block past its length, and blocks past it, may hold anything
+ *   (NaN included): they are masked in the scores and zeroed in the values.
  *
  * options may be NULL for masks 0 and 3 without paging (NULL with mask 4 is
  * FIA_ERR_PARAM_NULLPTR). */
@@ -320,7 +322,10 @@ int ring_attention_update(const void* prev_out, const float* prev_max, const flo
  * floating-point steps with the oracle.
  *
  * fia_debug_dequant: out[i] = (codes[i] - offset[i]) * scale[i] in fp32 with two roundings,
- *   through the same device function the attention kernel uses.  All pointers device.
+ *   through the element-wise antiquant function of the CUDA-core decode kernel, the one that
+ *   serves int8 KV with D = 64.  The int8 tensor-core kernel (D = 128) never forms a
+ *   dequantised element: it applies the affine map to the query and to the output, and its
+ *   exact steps have the two probes below.  All pointers device.
  * fia_debug_gather: copies the K rows of the first L_b tokens of (b, hkv) into dst (device,
  *   L_b * D elements of kv_dtype, row-major) through the attention kernel's block-table walk,
  *   tensor-map tile loads and swizzled addressing.  Other arguments as for fia_decode.
@@ -331,6 +336,30 @@ int fia_debug_dequant(const int8_t* codes, const float* scale, const float* offs
 int fia_debug_gather(const void* k_cache, fia_dtype kv_dtype, const int32_t* block_table, int64_t bt_stride,
                      const int64_t* actual_seq_lengths, int max_kv_len, int B, int Nkv, int D, int block_size,
                      int64_t num_blocks, int b, int hkv, void* dst, fia_stream_t stream);
+
+/* The int8 tensor-core decode kernel (int8 KV, D = 128) computes a score as
+ *   sum_d q_d (x_td - o_d) s_d = sum_d (q_d s_d) x_td - sum_d q_d s_d o_d
+ * with the codes x_td entering the tensor-core product as fp16 and q'_d = q_d s_d as an fp16
+ * pair hi + lo (aclnnIncreFlashAttentionV3, "antiquantScale / antiquantOffset").  These probes
+ * run those steps through the kernel's own device functions.
+ *
+ * fia_debug_i8_codes: out[i] = the binary16 bit pattern the kernel's converter warps produce
+ *   for codes[i]; n % 4 == 0, codes 4-byte and out 8-byte aligned.  The conversion is exact.
+ * fia_debug_i8_qprep: the query operand of every (b, kv head) as the plan kernel prepares it,
+ *   read back through the kernel's shared-memory layout.  q (B, Nq, 128) as for fia_decode;
+ *   antiquant_scale / offset (2, Nkv, 128) (the key half [0] is used; offset may be NULL).
+ *   blocks: device scratch of at least B * Nkv * 8320 bytes, 256-byte aligned (the blocks in
+ *   the kernel's layout).  q_hi, q_lo: device (B, Nkv, 16, 128) binary16 bit patterns of the
+ *   two parts of q'_d 2^e for query head hkv * G + g in row g (rows g >= G are zero), e the
+ *   power of two, chosen per row, that puts the row's largest |q'_d| in [2^14, 2^15).  kq_nq: device
+ *   (B, Nkv, 16, 2) fp32: kq = scale log2(e) 2^-e and nq = -scale log2(e) sum_d q'_d o_d, so
+ *   that the score in log2 units is (sum_d (hi_d + lo_d) x_td) kq + nq.
+ */
+int fia_debug_i8_codes(const int8_t* codes, int64_t n, uint16_t* out, fia_stream_t stream);
+
+int fia_debug_i8_qprep(const void* q, fia_dtype q_dtype, const float* antiquant_scale, const float* antiquant_offset,
+                       int B, int Nq, int Nkv, double scale, void* blocks, size_t blocks_bytes, uint16_t* q_hi,
+                       uint16_t* q_lo, float* kq_nq, fia_stream_t stream);
 
 #ifdef __cplusplus
 }

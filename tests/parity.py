@@ -3,30 +3,37 @@ library through its C interface, and compare with the oracle.
 
 Tolerances (elementwise |gpu - oracle| <= atol + rtol * |oracle|):
   out   bf16: atol = rtol = 1e-2;  fp16: atol = rtol = 2e-3;  fp32 (RAU): 1e-5
-  max, sum: rtol = 1e-4, plus atol = 1e-5 on max only -- a logit near 0 would make
-  a pure relative bound meaningless; fp32 accumulation of D <= 128 products of
-  O(1) terms times scale <= 1 stays below 1e-5 in absolute terms.
+  max, sum: rtol = 1e-4 (relative only, as stated for the fp32 softmax max and sum).
+  A softmax maximum close to zero can miss a purely relative bound although the
+  score behind it is as accurate as any other: a dot product of D <= 128 fp32
+  products of O(1) terms carries an absolute error near 1e-7, whatever its value.
+  Such rows -- |max| < 0.1 with an absolute error <= 1e-5 -- are accepted and
+  recorded (NEAR_ZERO_MAX_ROWS, printed at the end of the session), so that the
+  rows that need more than the relative bound are listed, not hidden.
 Integer and byte results (gathered rows, dequantised codes) must be identical.
 """
 from __future__ import annotations
+
+import os
 
 import numpy as np
 import torch
 
 import fia_workloads as W
 import oracle as OR
+from fia_workloads import DeviceDecode, DevicePrefill  # noqa: F401  (re-exported for the tests)
 
 OUT_TOL = {W.BF16: (1e-2, 1e-2), W.FP16: (2e-3, 2e-3), "fp32": (1e-5, 1e-5)}
-MAX_TOL = (1e-5, 1e-4)
+MAX_RTOL = 1e-4
 SUM_TOL = (0.0, 1e-4)
-
-_TORCH = {W.BF16: torch.bfloat16, W.FP16: torch.float16}
+NEAR_ZERO_MAX = 0.1          # |max| below which the absolute term below may be used
+NEAR_ZERO_MAX_ATOL = 1e-5
+NEAR_ZERO_MAX_ROWS = []      # (test, quantity, flat index, |oracle|, abs error)
 
 
 def dev_bits(bits: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
     """uint16 storage bits -> device tensor of the storage dtype (bit-exact)."""
-    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
-    return t.view(_TORCH[dtype])
+    return W.device_bits(bits, dtype, device)
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
@@ -52,27 +59,31 @@ def assert_close(name, got, ref, atol, rtol):
     return float(err.max()) if err.size else 0.0, float(rel.max()) if rel.size else 0.0
 
 
+def assert_close_max(name, got, ref, rtol=MAX_RTOL):
+    """The softmax max (or log-sum-exp) within rtol; a row near zero (|ref| < NEAR_ZERO_MAX)
+    may instead be within NEAR_ZERO_MAX_ATOL, and every such row is recorded."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    both_inf = np.isinf(got) & np.isinf(ref) & (np.sign(got) == np.sign(ref))
+    g = np.where(both_inf, 0.0, got)
+    r = np.where(both_inf, 0.0, ref)
+    err = np.abs(g - r)
+    rel_ok = err <= rtol * np.abs(r)
+    near = ~rel_ok & (np.abs(r) < NEAR_ZERO_MAX) & (err <= NEAR_ZERO_MAX_ATOL)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    for i in np.argwhere(near.reshape(-1)).reshape(-1):
+        NEAR_ZERO_MAX_ROWS.append((test, name, int(i), float(abs(r.reshape(-1)[i])), float(err.reshape(-1)[i])))
+    bad = ~(rel_ok | near)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{name}: {int(bad.sum())} of {bad.size} outside rtol={rtol}; first at {tuple(i)}: "
+                             f"gpu={got[tuple(i)]!r} oracle={ref[tuple(i)]!r}; max abs err {float(err.max()):.3g}")
+    rel = err / np.maximum(np.abs(r), 1e-30)
+    return float(err.max()) if err.size else 0.0, float(rel.max()) if rel.size else 0.0
+
+
 # ----------------------------------------------------------------------------- decode
-class DeviceDecode:
-    """A DecodeCase resident on the GPU."""
-
-    def __init__(self, case: W.DecodeCase, device="cuda"):
-        self.case = case
-        self.q = dev_bits(case.q, case.dtype, device)
-        if case.kv_dtype == W.INT8:
-            self.k = torch.from_numpy(case.k_cache).to(device)
-            self.v = torch.from_numpy(case.v_cache).to(device)
-            self.aq_scale = torch.from_numpy(case.aq_scale).to(device)
-            self.aq_offset = None if case.aq_offset is None else torch.from_numpy(case.aq_offset).to(device)
-        else:
-            self.k = dev_bits(case.k_cache, case.kv_dtype, device)
-            self.v = dev_bits(case.v_cache, case.kv_dtype, device)
-            self.aq_scale = self.aq_offset = None
-        self.bt = torch.from_numpy(case.block_table).to(device)
-        self.lens = torch.from_numpy(case.lengths.astype(np.int64)).to(device)
-        self.sink = None if case.sink is None else torch.from_numpy(case.sink).to(device)
-
-
 def run_decode(F, dd: DeviceDecode, num_splits=0, sink="case", max_kv_len=None, lens=None, bt=None):
     c = dd.case
     B, Nq = c.B, c.Nq
@@ -107,7 +118,7 @@ def compare_decode(case: W.DecodeCase, out, mx, sm, rows=None, ref=None):
         o, m, s = o[rows], m[rows], s[rows]
     atol, rtol = OUT_TOL[case.dtype]
     e_out = assert_close("out", o, o_ref, atol, rtol)
-    e_max = assert_close("softmax_max", m, m_ref, *MAX_TOL)
+    e_max = assert_close_max("softmax_max", m, m_ref)
     e_sum = assert_close("softmax_sum", s, s_ref, *SUM_TOL)
     return {"out": e_out, "max": e_max, "sum": e_sum}
 
@@ -123,19 +134,6 @@ def sample_rows(case: W.DecodeCase, n: int, seed: int = 0) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------- prefill
-class DevicePrefill:
-    """A PrefillCase resident on the GPU."""
-
-    def __init__(self, case: W.PrefillCase, device="cuda"):
-        self.case = case
-        self.q = dev_bits(case.q, case.dtype, device)
-        self.k = dev_bits(case.k, case.dtype, device)
-        self.v = dev_bits(case.v, case.dtype, device)
-        self.cu_q = torch.from_numpy(case.cu_q).to(device)
-        self.cu_kv = torch.from_numpy(case.cu_kv).to(device)
-        self.sink = None if case.sink is None else torch.from_numpy(case.sink).to(device)
-
-
 def run_prefill(F, dp: DevicePrefill, causal=True, sink="case", band=None):
     c = dp.case
     mx = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device=dp.q.device)
@@ -164,7 +162,7 @@ def compare_prefill(case: W.PrefillCase, out, mx, sm, rows=None, ref=None, causa
         o, m, s = o[rows], m[rows], s[rows]
     atol, rtol = OUT_TOL[case.dtype]
     return {"out": assert_close("out", o, ref[0], atol, rtol),
-            "max": assert_close("softmax_max", m, ref[1], *MAX_TOL),
+            "max": assert_close_max("softmax_max", m, ref[1]),
             "sum": assert_close("softmax_sum", s, ref[2], *SUM_TOL)}
 
 

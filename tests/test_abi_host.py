@@ -60,6 +60,33 @@ def test_decode_rejects(F, kw, code):
     assert lib.fia_last_error()
 
 
+def _noalloc(lib, **kw):
+    a = dict(q=P, q_dtype=2, k=P, v=P, kv_dtype=2, bt=P, bt_stride=4, lens=P, max_kv_len=64, B=2, Nq=4, Nkv=2,
+             D=64, bs=16, num_blocks=8, scale=0.125, aqs=None, aqo=None, sink=None, out=P, mx=None, sm=None,
+             splits=0, stream=None)
+    a.update(kw)
+    return lib.fia_decode_noalloc(a["q"], a["q_dtype"], a["k"], a["v"], a["kv_dtype"], a["bt"], a["bt_stride"],
+                                  a["lens"], a["max_kv_len"], a["B"], a["Nq"], a["Nkv"], a["D"], a["bs"],
+                                  a["num_blocks"], a["scale"], a["aqs"], a["aqo"], a["sink"], a["out"], a["mx"],
+                                  a["sm"], a["splits"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(out=None), dict(q=None), dict(lens=None), dict(kv_dtype=3), dict(out=None, D=96), dict(q=None, q_dtype=0),
+    dict(q_dtype=0), dict(kv_dtype=1), dict(Nq=6, Nkv=4), dict(D=96), dict(bs=24), dict(bt_stride=3),
+    dict(kv_dtype=3, aqs=P, bs=32, sink=P), dict(q=P + 8), dict(scale=float("inf")), dict(splits=-1),
+])
+def test_noalloc_reports_the_codes_of_fia_decode(F, kw):
+    """The allocation-free entry point checks its arguments as fia_decode does, in the same
+    order: the same bad argument gives the same code and message from both."""
+    lib = F.library()
+    rc = _decode(lib, **kw)
+    msg = lib.fia_last_error()
+    assert rc in (NULLPTR, INVALID)
+    assert _noalloc(lib, **kw) == rc
+    assert lib.fia_last_error() == msg
+
+
 def test_rau_rejects(F):
     lib = F.library()
     assert lib.ring_attention_update(None, P, P, P, P, P, 2, 4, 8, 64, P, P, P, None) == NULLPTR
@@ -146,7 +173,9 @@ def _prefill_ex(lib, opts, **kw):
     (dict(pre_tokens=2, next_tokens=-3), dict(mask=4), INVALID),                     # empty band
     ({}, dict(mask=2), INVALID),                                                     # leftUpCausal: not built
     (dict(block_table=P, bt_stride=1, block_size=128, num_blocks=4), dict(cu_kv=None), NULLPTR),  # no seq_lens_kv
-    (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=64, num_blocks=4), {}, INVALID),  # block < 128
+    (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=24, num_blocks=4), {}, INVALID),  # not % 16
+    (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=8, num_blocks=4), {}, INVALID),
+    ({}, dict(D=96), INVALID), ({}, dict(D=256), INVALID),                           # D outside {64, 128}
     (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=640, num_blocks=4), {}, INVALID),
     (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=128, num_blocks=0), {}, INVALID),
     (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=128, num_blocks=4, kv_layout=5), {}, INVALID),

@@ -47,9 +47,21 @@ def test_decode_bytes_by_hand():
 
 
 def test_traffic_entry_is_gated_by_the_source_hash(monkeypatch):
+    """A recorded DRAM-traffic figure is reported only while the kernel sources hash to the
+    value recorded with it; with any other hash it is null."""
+    import json
     B = _bench()
+    with open(os.path.join(ROOT, "profiles", "kernel_traffic.json")) as f:
+        rec = json.load(f)
     for w in B.TRAFFIC_SOURCES:
-        assert isinstance(B.load_traffic(w), int)     # the committed capture matches the sources
+        entry = rec.get(w)
+        if entry and entry.get("sources_sha1") == B.traffic_sha(w):
+            assert B.load_traffic(w) == entry["bytes_per_launch"]
+        else:
+            assert B.load_traffic(w) is None
+        if entry:
+            monkeypatch.setattr(B, "traffic_sha", lambda _w, sha=entry["sources_sha1"]: sha)
+            assert B.load_traffic(w) == entry["bytes_per_launch"]
     monkeypatch.setattr(B, "traffic_sha", lambda w: "000000000000")
     assert all(B.load_traffic(w) is None for w in B.TRAFFIC_SOURCES)
 

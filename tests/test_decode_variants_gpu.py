@@ -20,7 +20,7 @@ import torch
 
 import fia_workloads as W
 import oracle as OR
-from parity import MAX_TOL, OUT_TOL, SUM_TOL, DeviceDecode, assert_close, compare_decode, oracle_decode, run_decode
+from parity import OUT_TOL, SUM_TOL, DeviceDecode, assert_close, assert_close_max, compare_decode, oracle_decode, run_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -122,7 +122,7 @@ def test_softmax_lse(F, cuda, sink, with_max_sum):
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(got), fin)
     assert np.all(got[~fin] == -np.inf)
-    assert_close("softmax_lse", got[fin], lse_ref[fin], *MAX_TOL)
+    assert_close_max("softmax_lse", got[fin], lse_ref[fin])
     assert F.fia_device_status() == 0
 
 
@@ -168,6 +168,50 @@ def test_atten_mask(F, cuda, name, num_splits):
     base = run_decode(F, dd, num_splits=num_splits)
     assert torch.equal(out.view(torch.int16), base[0].view(torch.int16))
     assert torch.equal(mx, base[1]) and torch.equal(sm, base[2])
+    assert F.fia_device_status() == 0
+
+
+def _poison_keys(case, drop):
+    """NaN into the K and V rows of every key t of batch b with drop(b, t) true."""
+    k, v = case.k_cache.copy(), case.v_cache.copy()
+    nan = W.NAN_BITS[case.kv_dtype]
+    for b in range(case.B):
+        for t in range(int(case.lengths[b])):
+            if drop(b, t):
+                blk, row = case.block_table[b, t // case.block_size], t % case.block_size
+                k[blk, :, row] = nan
+                v[blk, :, row] = nan
+    case.k_cache, case.v_cache = k, v
+
+
+@pytest.mark.parametrize("num_splits", [0, 3])
+@pytest.mark.parametrize("name", ["bf16_d128_g4", "fp16_d64_g8_sink"])
+def test_atten_mask_nan_in_masked_keys(F, cuda, name, num_splits):
+    """A masked key contributes nothing even when its cache rows hold NaN (16-bit KV; int8
+    codes cannot be NaN)."""
+    case = _case("mask_" + name, **MASK_CASES[name])
+    S = case.max_len + 40
+    m = _mask_for(case, zlib.crc32(name.encode()) & 0xffff, S)
+    ref = oracle_decode(case, mask=m.astype(np.uint8))
+    _poison_keys(case, lambda b, t: m[b, t])
+    dd = DeviceDecode(case)
+    mask = torch.from_numpy(m).reshape(case.B, 1, 1, S).cuda()
+    out, mx, sm = _run(F, dd, num_splits, atten_mask=mask)
+    compare_decode(case, out, mx, sm, ref=ref)
+    assert F.fia_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["bf16_d128_g4", "fp16_d64_g8_sink"])
+def test_decode_band_window_nan_outside(F, cuda, name):
+    """Keys before the window (in the window's first tile and before it) hold NaN."""
+    case = _case("window_" + name, **WINDOW_CASES[name])
+    pre, nxt = 100, 0
+    ref = oracle_decode(case, band=(pre, nxt))
+    _poison_keys(case, lambda b, t: t < int(case.lengths[b]) - 1 - pre)
+    dd = DeviceDecode(case)
+    for ns in (0, 3):
+        out, mx, sm = _run(F, dd, ns, pre_tokens=pre, next_tokens=nxt)
+        compare_decode(case, out, mx, sm, ref=ref)
     assert F.fia_device_status() == 0
 
 
@@ -227,7 +271,7 @@ def test_post_quant_int8_output(F, cuda, name, num_splits):
         assert out.dtype == torch.int8 and tuple(out.shape) == (case.B, case.Nq, case.D)
         s_c = np.broadcast_to(s2.astype(np.float64), (C,))
         _check_codes(out.cpu().numpy().reshape(-1, C), y.reshape(-1, C), o_ref.reshape(-1, C), s_c, atol, rtol)
-        assert_close("softmax_max", mx.double().cpu().numpy().reshape(-1), m_ref, *MAX_TOL)
+        assert_close_max("softmax_max", mx.double().cpu().numpy().reshape(-1), m_ref)
         assert_close("softmax_sum", sm.double().cpu().numpy().reshape(-1), s_ref, *SUM_TOL)
     assert F.fia_device_status() == 0
 

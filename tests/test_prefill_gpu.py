@@ -36,6 +36,14 @@ CASES = {
     # more sequences than the plan stages at a time (256), short ones and a long tail
     "many_seqs": dict(Nq=2, Nkv=1, D=128, lengths=[(i * 37) % 23 for i in range(600)] + [300]),
     "many_seqs_g1": dict(Nq=1, Nkv=1, D=128, lengths=[(i * 11) % 19 for i in range(300)] + [260, 0]),
+    # head dim 64 (aclnnIncreFlashAttentionV3 "Constraints": D up to 512; 64 and 128 here) on
+    # both kernels (even and odd GQA groups)
+    "d64_pair": dict(Nq=8, Nkv=2, D=64, lengths=[300, 513, 5, 128]),
+    "d64_odd_g": dict(Nq=3, Nkv=1, D=64, lengths=[129, 260, 1]),
+    "d64_q_shorter_fp16_sink": dict(Nq=4, Nkv=2, D=64, lengths=[100, 7], lengths_kv=[300, 135], dtype=W.FP16,
+                                    sink=True),
+    "d64_no_mask_odd_g": dict(Nq=5, Nkv=5, D=64, lengths=[77, 200], causal=False),
+    "d64_zero_length_seqs": dict(Nq=4, Nkv=4, D=64, lengths=[2, 0, 130, 0]),
 }
 
 
@@ -103,6 +111,8 @@ BAND_CASES = {
     "sink_odd_g": (dict(Nq=3, Nkv=3, D=128, lengths=[200], sink=True), (17, 2)),
     "many_short_seqs": (dict(Nq=2, Nkv=1, D=128, lengths=[(i * 37) % 23 for i in range(300)] + [300]), (10, 0)),
     "wide_band_no_mask": (dict(Nq=4, Nkv=2, D=128, lengths=[77, 260], lengths_kv=[90, 260]), (1 << 40, 1 << 40)),
+    "d64_sliding_pair": (dict(Nq=8, Nkv=2, D=64, lengths=[700, 129]), (200, 0)),
+    "d64_both_sides_odd_g": (dict(Nq=3, Nkv=1, D=64, lengths=[400, 60], lengths_kv=[450, 60]), (50, 70)),
 }
 
 
@@ -153,10 +163,10 @@ def test_prefill_band_rejects(F, cuda):
 
 
 # ------------------------------------------------------------------ paged keys (chunked prefill)
-def _paged_pool(case, block_size, layout, seed):
+def _paged_pool(case, block_size, layout, seed, poison=False):
     """The case's TND keys and values scattered into a shuffled pool with a few unused blocks;
-    rows past a sequence's length hold finite garbage.  Returns device (k_pool, v_pool,
-    block_table, seq_lens_kv)."""
+    rows past a sequence's length hold finite garbage, or NaN with poison=True (a cache taken
+    from uninitialised memory).  Returns device (k_pool, v_pool, block_table, seq_lens_kv)."""
     rng = np.random.default_rng(seed)
     nblk = [-(-int(L) // block_size) for L in case.lengths_kv]
     total = sum(nblk) + 3
@@ -166,7 +176,10 @@ def _paged_pool(case, block_size, layout, seed):
     shape = (total, case.Nkv, block_size, case.D)
     pools = []
     for src in (case.k, case.v):
-        pool = W.to_bits(rng.standard_normal(shape, dtype=np.float32) * 3, case.dtype)
+        if poison:
+            pool = np.full(shape, W.NAN_BITS[case.dtype], np.uint16)
+        else:
+            pool = W.to_bits(rng.standard_normal(shape, dtype=np.float32) * 3, case.dtype)
         n = 0
         for b in range(case.B):
             for i in range(nblk[b]):
@@ -192,17 +205,28 @@ PAGED_CASES = {
     "paged_band_fp16_sink": (dict(Nq=4, Nkv=2, D=128, lengths=[150, 290], lengths_kv=[900, 290], dtype=W.FP16,
                                   sink=True), 128, "bnnbsd", (255, 0)),
     "empty_kv_sequence": (dict(Nq=2, Nkv=1, D=128, lengths=[40, 70], lengths_kv=[0, 500]), 128, "bnnbsd", None),
+    # blocks smaller than a key tile: several boxes per 128-key tile, one block each
+    # (aclnnIncreFlashAttentionV3, "Constraints / page attention": blockSize a multiple of 16)
+    "bs16_pair": (dict(Nq=8, Nkv=2, D=128, lengths=[100, 37], lengths_kv=[700, 300]), 16, "bnnbsd", None),
+    "bs32_odd_g_bsh": (dict(Nq=3, Nkv=1, D=128, lengths=[64, 200], lengths_kv=[500, 200]), 32, "bsh", None),
+    "bs48_band": (dict(Nq=4, Nkv=2, D=128, lengths=[130, 20], lengths_kv=[600, 333]), 48, "bnnbsd", (199, 0)),
+    "bs64_fp16_sink": (dict(Nq=4, Nkv=4, D=128, lengths=[129, 1], lengths_kv=[257, 1], dtype=W.FP16, sink=True),
+                       64, "bnnbsd", None),
+    "d64_bs16_pair": (dict(Nq=8, Nkv=2, D=64, lengths=[100, 64], lengths_kv=[450, 64]), 16, "bnnbsd", None),
+    "d64_bs256_odd_g_bsh": (dict(Nq=3, Nkv=3, D=64, lengths=[77, 130], lengths_kv=[600, 130]), 256, "bsh", None),
 }
 
 
+@pytest.mark.parametrize("poison", [False, True], ids=["finite_garbage", "nan_poisoned"])
 @pytest.mark.parametrize("name", sorted(PAGED_CASES))
-def test_prefill_paged_keys(F, cuda, name):
+def test_prefill_paged_keys(F, cuda, name, poison):
     """Paged keys give the oracle's result and, tile for tile the same arithmetic, the TND
-    run's result bit for bit."""
+    run's result bit for bit -- also when every pool row that holds no key of a sequence
+    (unused blocks, rows of a last block past the length) is NaN."""
     kw, bs, layout, band = PAGED_CASES[name]
     case = W.make_prefill_case(seed=zlib.crc32(("paged_" + name).encode()) % (1 << 30), **kw)
     dp = DevicePrefill(case)
-    kp, vp, bt, lens = _paged_pool(case, bs, layout, seed=zlib.crc32(name.encode()) & 0xffff)
+    kp, vp, bt, lens = _paged_pool(case, bs, layout, seed=zlib.crc32(name.encode()) & 0xffff, poison=poison)
     c = case
     mx = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device="cuda")
     sm = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device="cuda")
@@ -218,11 +242,13 @@ def test_prefill_paged_keys(F, cuda, name):
     assert F.fia_device_status() == 0
 
 
-def test_prefill_paged_rejects_small_blocks(F, cuda):
+@pytest.mark.parametrize("bs", [8, 24, 1024])
+def test_prefill_paged_rejects_block_sizes(F, cuda, bs):
+    """blockSize must be a multiple of 16 up to 512."""
     case = W.make_prefill_case(Nq=4, Nkv=2, D=128, lengths=[5], lengths_kv=[100], seed=4)
     dp = DevicePrefill(case)
-    kp = torch.zeros((8, 2, 64, 128), dtype=torch.bfloat16, device="cuda")
-    bt = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    kp = torch.zeros((8, 2, bs, 128), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((1, 100 // bs + 1), dtype=torch.int32, device="cuda")
     lens = torch.tensor([100], dtype=torch.int64, device="cuda")
     with pytest.raises(F.FiaError) as ei:
         F.fia_prefill(dp.q, kp, kp, dp.cu_q, None, max_seqlen_q=5, max_seqlen_kv=100, num_heads=4, num_kv_heads=2,

@@ -5,7 +5,7 @@ import torch
 
 import fia_workloads as W
 import oracle
-from parity import OUT_TOL, SUM_TOL, MAX_TOL, assert_close, to_f64
+from parity import OUT_TOL, SUM_TOL, assert_close, assert_close_max, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ def test_rau_matches_oracle(F, cuda, dtype, N, D):
     ref = oracle.rau(*(to_f64(t) for t in prev), *(to_f64(t) for t in cur))
     key = dtype if dtype != "fp32" else "fp32"
     assert_close("out", to_f64(out), ref[0], *OUT_TOL[key if key in OUT_TOL else "fp32"])
-    assert_close("max", to_f64(mx), ref[1], *MAX_TOL)
+    assert_close_max("max", to_f64(mx), ref[1])
     assert_close("sum", to_f64(sm), ref[2], *SUM_TOL)
 
 

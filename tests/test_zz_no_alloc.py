@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import fia_workloads as W
-from parity import MAX_TOL, OUT_TOL, SUM_TOL, DeviceDecode, assert_close, run_decode, to_f64
+from parity import OUT_TOL, SUM_TOL, DeviceDecode, assert_close, assert_close_max, run_decode, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +42,7 @@ def test_noalloc_matches_fia_decode_twice(F, cuda, make):
         got = _noalloc(F, dd)
         torch.cuda.synchronize()
         assert_close("out", to_f64(got[0]), to_f64(ref[0]), *tol)
-        assert_close("softmax_max", to_f64(got[1]), to_f64(ref[1]), *MAX_TOL)
+        assert_close_max("softmax_max", to_f64(got[1]), to_f64(ref[1]))
         assert_close("softmax_sum", to_f64(got[2]), to_f64(ref[2]), *SUM_TOL)
     assert F.fia_device_status() == 0
 
