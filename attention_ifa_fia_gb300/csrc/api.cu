@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <map>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -206,6 +207,20 @@ int current_context(void** ctx) {
   return FIA_SUCCESS;
 }
 
+cudaError_t ensure_smem(const void* func, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<void*, const void*>, size_t> done;  // (context, function) -> limit set
+  void* ctx = nullptr;
+  if (current_context(&ctx) != FIA_SUCCESS) ctx = nullptr;  // unknown context: always set
+  std::lock_guard<std::mutex> lk(mu);
+  auto key = std::make_pair(ctx, func);
+  auto it = done.find(key);
+  if (ctx && it != done.end() && it->second >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && ctx) done[key] = bytes;
+  return e;
+}
+
 int report_error(int code, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -399,6 +414,9 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   p.pq_stride = q2_per_channel;
   p.partials_only = qs2 != nullptr;
   p.windowed = windowed ? 1 : 0;
+  // 16-bit KV runs on the tensor-core kernel, which schedules its own work when the batch
+  // fits its shared-memory schedule (otherwise a plan launch precedes it)
+  p.fused_plan = (kv_dtype != FIA_I8 && B <= fia::kFusedPlanMaxB) ? 1 : 0;
   p.win_pre = (int)win_pre;
   p.win_next = (int)win_next;
   p.ws = fia::decode_workspace_carve(workspace, B, Nkv, G, D, plan.max_items);

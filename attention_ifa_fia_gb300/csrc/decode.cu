@@ -122,24 +122,6 @@ __device__ __forceinline__ float q_elem(const uint16_t* q, int idx, int q_dtype)
 
 // ------------------------------------------------------------------- plan
 constexpr int kPlanSmemB = 4096;  // batches whose item offsets and order slots fit in shared memory
-constexpr int kPlanMaxTiles = 64;  // size classes of the execution order (tiles per item, capped)
-
-__device__ __forceinline__ int clamp_len(const DecodeParams& p, int b, bool flag) {
-  const int64_t raw = p.seq_lens[b];
-  if (flag && (raw < 0 || raw > p.max_kv_len)) raise_status(p.status, kStatusLengthClamped);
-  return (int)(raw < 0 ? 0 : (raw > p.max_kv_len ? p.max_kv_len : raw));
-}
-
-// Rows of a batch with no visible key: out 0, max -inf and sum 0, or with a sink
-// max = sink and sum 1 (no work item covers them).
-__device__ void write_empty_batch(const DecodeParams& p, int b) {
-  for (int h = 0; h < p.Nq; ++h) {
-    if (p.softmax_max) p.softmax_max[(int64_t)b * p.Nq + h] = p.sink ? p.sink[h] : -INFINITY;
-    if (p.softmax_sum) p.softmax_sum[(int64_t)b * p.Nq + h] = p.sink ? 1.f : 0.f;
-  }
-  uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (int64_t)b * p.Nq * p.D * 2);
-  for (int i = 0; i < p.Nq * p.D * 2 / 16; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
-}
 
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   // Launched as a dependent of whatever precedes it on the stream (often the previous
@@ -268,6 +250,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   if (tid == 0) {
     *p.ws.n_items = total;
     *p.ws.counter = 0;
+    p.ws.seg_base[p.B] = total;
   }
 }
 
@@ -631,11 +614,20 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   griddep_launch_dependents();  // a following plan kernel may launch; it waits for this grid
   extern __shared__ float2 ml[];  // [G][nch]: (max, sum), then (weight, -) per partial
   const int b = blockIdx.x / p.Nkv, hkv = blockIdx.x % p.Nkv;
-  const int C = p.chunk_tokens;
-  const int nch = span_chunks(decode_span(p, clamp_len(p, b, false)), C);
+  const int seg0 = p.ws.seg_base[b], seg1 = p.ws.seg_base[b + 1];  // batch b's items, all kv heads
+  const int nch = (seg1 - seg0) / p.Nkv;
   if (nch <= 1 && !p.partials_only) return;
   const int G = p.G, D = p.D, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int first = p.ws.seg_base[b] + hkv * nch;
+  const int first = seg0 + hkv * nch;
+  const float4* po = reinterpret_cast<const float4*>(p.ws.part_o + (int64_t)first * G * D);
+  const int q4n = G * D / 4;  // float4 outputs per partial
+  // this thread's outputs of the first kPre partials, loaded now so that their latency overlaps
+  // that of the maxima and sums
+  constexpr int kPre = 8;
+  float4 pre[kPre];
+#pragma unroll
+  for (int j = 0; j < kPre; ++j)
+    pre[j] = (tid < q4n && j < nch) ? po[(int64_t)j * q4n + tid] : make_float4(0.f, 0.f, 0.f, 0.f);
   for (int i = tid; i < G * nch; i += kMergeThreads) {  // coalesced: partial-major in memory
     const int j = i / G, g = i - j * G;
     ml[g * nch + j] = p.ws.part_ml[(int64_t)first * G + i];
@@ -668,12 +660,22 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     }
   }
   __syncthreads();
-  const float4* po = reinterpret_cast<const float4*>(p.ws.part_o + (int64_t)first * G * D);
-  const int q4n = G * D / 4;  // float4 outputs per partial
   for (int q4 = tid; q4 < q4n; q4 += kMergeThreads) {
     const float2* row = ml + ((q4 * 4) / D) * nch;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int j = 0;
+    if (q4 == tid) {  // the prefetched partials
+#pragma unroll
+      for (int k = 0; k < kPre; ++k)
+        if (k < nch) {
+          const float w = row[k].x;
+          acc.x = fmaf(w, pre[k].x, acc.x);
+          acc.y = fmaf(w, pre[k].y, acc.y);
+          acc.z = fmaf(w, pre[k].z, acc.z);
+          acc.w = fmaf(w, pre[k].w, acc.w);
+        }
+      j = min(nch, kPre);
+    }
     for (; j + 4 <= nch; j += 4) {  // four independent loads in flight
       const float4 v0 = po[(int64_t)(j + 0) * q4n + q4], v1 = po[(int64_t)(j + 1) * q4n + q4];
       const float4 v2 = po[(int64_t)(j + 2) * q4n + q4], v3 = po[(int64_t)(j + 3) * q4n + q4];
@@ -780,7 +782,7 @@ cudaError_t launch_attention(const DecodeParams& p, const CUtensorMap& tmK, cons
                              int grid, cudaStream_t stream) {
   const size_t smem = sizeof(Smem<KVT, D, GP>) + 1024;
   auto kern = decode_splitkv_kernel<KVT, D, GP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem(kern, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);
   e = launch_dependent(kern, grid, kThreads, smem, stream, tmK, tmV, p, box_rows);
@@ -802,7 +804,7 @@ cudaError_t launch_attention_g(const DecodeParams& p, const CUtensorMap& tmK, co
 size_t decode_workspace_bytes(int B, int Nkv, int G, int D, int max_items) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t s = 256;                                      // counter, n_items
-  s += up(sizeof(int) * (size_t)(B > 0 ? B : 1));      // seg_base
+  s += up(sizeof(int) * (size_t)(B + 1));              // seg_base
   s += up(sizeof(int4) * (size_t)max_items);           // items
   s += up(sizeof(int) * (size_t)max_items);            // order
   s += up(sizeof(float) * (size_t)max_items * G * D);  // part_o
@@ -820,7 +822,7 @@ DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D,
   w.n_items = reinterpret_cast<int*>(c + 4);
   c += 256;
   w.seg_base = reinterpret_cast<int*>(c);
-  c += up(sizeof(int) * (size_t)(B > 0 ? B : 1));
+  c += up(sizeof(int) * (size_t)(B + 1));
   w.items = reinterpret_cast<int4*>(c);
   c += up(sizeof(int4) * (size_t)max_items);
   w.order = reinterpret_cast<int*>(c);
@@ -870,11 +872,15 @@ cudaError_t launch_lse(const float* mx, const float* sm, float* lse, int64_t n, 
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream) {
+  if (tmQ && p.fused_plan) {  // the tensor-core kernel plans for itself: attention, then merge
+    cudaError_t e = launch_decode_tc_attention(p, tmK, tmV, *tmQ, box_rows, num_sms, stream);
+    if (e != cudaSuccess) return e;
+    return launch_merge(p, stream);
+  }
   trace_mark(kKernelDecodePlan, 0, stream);
   const size_t plan_smem = p.B <= kPlanSmemB ? sizeof(int) * (size_t)(5 * p.B + 1) : 0;
   if (plan_smem > 48 * 1024) {
-    cudaError_t e0 = cudaFuncSetAttribute(decode_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)(sizeof(int) * (5 * kPlanSmemB + 1)));
+    cudaError_t e0 = ensure_smem(decode_plan_kernel, (int)(sizeof(int) * (5 * kPlanSmemB + 1)));
     if (e0 != cudaSuccess) return e0;
   }
   const bool i8tc = !tmQ && decode_uses_i8tc(p.kv_dtype, p.D);
@@ -898,14 +904,19 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const C
                     : launch_attention_g<kI8, 128>(p, tmK, tmV, box_rows, grid, stream);
   }
   if (e != cudaSuccess) return e;
-  // merge of segments with two or more items (of every segment with partials_only);
-  // dependent launch on the attention kernel
+  return launch_merge(p, stream);
+}
+
+// merge of segments with two or more items (of every segment with partials_only);
+// dependent launch on the attention kernel
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
   const int max_chunks = (p.max_kv_len + p.chunk_tokens - 1) / p.chunk_tokens;
   if (max_chunks <= 1 && !p.partials_only) return cudaSuccess;
   const size_t msmem = sizeof(float2) * (size_t)p.G * (max_chunks > 1 ? max_chunks : 1);
   auto merge = (p.q_dtype == kBF16) ? decode_merge_kernel<kBF16> : decode_merge_kernel<kF16>;
   if (msmem > 48 * 1024) {
-    e = cudaFuncSetAttribute(merge, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+    e = ensure_smem(merge, (int)msmem);
     if (e != cudaSuccess) return e;
   }
   trace_mark(kKernelDecodeMerge, 0, stream);
@@ -926,7 +937,7 @@ cudaError_t launch_debug_gather(const DecodeParams& p, const CUtensorMap& tmK, i
                                 void* dst, cudaStream_t stream) {
   auto run = [&](auto kern, int tile_bytes) {
     const int smem = tile_bytes + 1024;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<1, 128, smem, stream>>>(tmK, p, box_rows, b, hkv, static_cast<uint8_t*>(dst));
     return cudaGetLastError();

@@ -64,6 +64,160 @@ __device__ __forceinline__ int4 span_item(const DecodeSpan& s, int C, int b, int
   return make_int4(b, hkv | (nch << 16), j == 0 ? s.lo : s.base + j * C, min(s.end, s.base + (j + 1) * C));
 }
 
+constexpr int kPlanMaxTiles = 64;  // size classes of the execution order (tiles per item, capped)
+
+// A batch's key count from the device array, clamped to [0, max_kv_len] (flag: raise the
+// status bit if it was outside).
+__device__ __forceinline__ int clamp_len(const DecodeParams& p, int b, bool flag) {
+  const int64_t raw = p.seq_lens[b];
+  if (flag && (raw < 0 || raw > p.max_kv_len)) raise_status(p.status, kStatusLengthClamped);
+  return (int)(raw < 0 ? 0 : (raw > p.max_kv_len ? p.max_kv_len : raw));
+}
+
+// Rows of a batch with no visible key: out 0, max -inf and sum 0, or with a sink
+// max = sink and sum 1 (no work item covers them).
+__device__ inline void write_empty_batch(const DecodeParams& p, int b) {
+  for (int h = 0; h < p.Nq; ++h) {
+    if (p.softmax_max) p.softmax_max[(int64_t)b * p.Nq + h] = p.sink ? p.sink[h] : -INFINITY;
+    if (p.softmax_sum) p.softmax_sum[(int64_t)b * p.Nq + h] = p.sink ? 1.f : 0.f;
+  }
+  uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (int64_t)b * p.Nq * p.D * 2);
+  for (int i = 0; i < p.Nq * p.D * 2 / 16; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// ----------------------------------------------------------------------------
+// In-kernel schedule.  With p.fused_plan the attention kernel plans for itself, with no
+// plan launch and no claim counter: every CTA derives from the lengths, in shared memory,
+// the same longest-first order of the work items -- first every full chunk (batch, kv
+// head, chunk in order), then each batch's last chunk, batches sorted by that chunk's
+// tiles, most first -- and takes the slots c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... of it
+// (a snake over the G CTAs).  For items ordered longest first this balances the CTAs as
+// well as claiming items from a counter (the per-CTA tile counts come out the same), and
+// saves the plan launch, its completion and the first claim's round trips.
+struct FusedPlan {
+  int lo[kFusedPlanMaxB], end[kFusedPlanMaxB];  // span of keys [lo, end) of each batch
+  int nch[kFusedPlanMaxB];                       // chunks (items per kv head) of each batch
+  int lastk[kFusedPlanMaxB];                     // tiles of each batch's last chunk (0: no key)
+  int nat[kFusedPlanMaxB + 1];                   // first item of batch b in (b, h, j) order
+  int full[kFusedPlanMaxB + 1];                  // first full-chunk slot of batch b
+  int last_ord[kFusedPlanMaxB];                  // batches with keys, longest last chunk first
+  int cls[kPlanMaxTiles + 2];                    // batches per last-chunk size, then class starts
+  int n_full, n_items;
+};
+
+// Builds the schedule; called by every thread of the CTA (nthreads of them), with
+// __syncthreads inside.  CTA 0 also writes the rows of batches without keys (unless every
+// segment goes through the merge kernel), raises the clamped-length flag, and writes each
+// batch's first item index for the merge kernel.
+__device__ inline void fused_plan_build(const DecodeParams& p, FusedPlan& fp, int tid, int nthreads) {
+  const int C = p.chunk_tokens, lane = tid & 31, warp = tid >> 5;
+  const bool cta0 = blockIdx.x == 0;
+  for (int i = tid; i < kPlanMaxTiles + 2; i += nthreads) fp.cls[i] = 0;
+  __syncthreads();
+  for (int b = tid; b < p.B; b += nthreads) {
+    const DecodeSpan sp = decode_span(p, clamp_len(p, b, cta0));
+    const int nch = span_chunks(sp, C);
+    fp.lo[b] = sp.lo;
+    fp.end[b] = sp.end;
+    fp.nch[b] = nch;
+    const int lk = nch ? min((sp.end - sp.base - (nch - 1) * C + kDecodeTileTC - 1) / kDecodeTileTC, kPlanMaxTiles) : 0;
+    fp.lastk[b] = lk;
+    if (nch) atomicAdd(&fp.cls[lk], 1);
+    if (!nch && cta0 && !p.partials_only) write_empty_batch(p, b);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // prefix sums over the batches, 8 consecutive batches per lane (B <= 256)
+    int nat_run = 0, full_run = 0, nat_l[8], full_l[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int b = lane * 8 + i;
+      const int nch = b < p.B ? fp.nch[b] : 0;
+      nat_l[i] = nat_run;
+      full_l[i] = full_run;
+      nat_run += nch * p.Nkv;
+      full_run += (nch ? nch - 1 : 0) * p.Nkv;
+    }
+    // and the class starts, largest class first: lane l holds classes 64 - 2l and 63 - 2l
+    const int k0 = kPlanMaxTiles - 2 * lane, k1 = k0 - 1;
+    const int c0 = fp.cls[k0], c1 = k1 >= 1 ? fp.cls[k1] : 0;
+    int nat_x = nat_run, full_x = full_run, cls_x = c0 + c1;  // inclusive warp scans
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, nat_x, o), f = __shfl_up_sync(0xffffffffu, full_x, o);
+      const int c = __shfl_up_sync(0xffffffffu, cls_x, o);
+      if (lane >= o) { nat_x += a; full_x += f; cls_x += c; }
+    }
+    __syncwarp();
+    fp.cls[k0] = cls_x - c0 - c1;
+    if (k1 >= 1) fp.cls[k1] = cls_x - c1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int b = lane * 8 + i;
+      if (b <= p.B) {
+        fp.nat[b] = nat_x - nat_run + nat_l[i];
+        fp.full[b] = full_x - full_run + full_l[i];
+      }
+    }
+    if (lane == 31) {
+      fp.nat[p.B] = nat_x;
+      fp.full[p.B] = full_x;
+      fp.n_full = full_x;
+      fp.n_items = nat_x;  // every item: the full chunks and one last chunk per batch and kv head
+    }
+    __syncwarp();
+    // batches with keys in order of their last chunk's tiles (descending), by index within a
+    // class: each group of equal sizes among 32 batches takes consecutive places
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      const int k = (b < p.B) ? fp.lastk[b] : 0;
+      const unsigned peers = __match_any_sync(0xffffffffu, k);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (k > 0) fp.last_ord[fp.cls[k] + rank] = b;
+      __syncwarp();
+      if (k > 0 && rank == 0) fp.cls[k] += __popc(peers);
+      __syncwarp();
+    }
+    if (cta0)
+      for (int b = lane; b <= p.B; b += 32) p.ws.seg_base[b] = fp.nat[b];
+  }
+  __syncthreads();
+}
+
+// The work item at slot `slot` of the schedule: its descriptor and its index in (b, h, j)
+// order (where its partial goes).
+__device__ inline int fused_plan_item(const DecodeParams& p, const FusedPlan& fp, int slot, int4* desc) {
+  const int C = p.chunk_tokens;
+  int b, h, j, nch;
+  if (slot < fp.n_full) {  // a full chunk: the last batch whose first full slot is <= slot
+    int lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (fp.full[mid] <= slot) lo = mid;
+      else hi = mid;
+    }
+    b = lo;
+    nch = fp.nch[b];
+    const int r = slot - fp.full[b];
+    h = r / (nch - 1);
+    j = r - h * (nch - 1);
+  } else {  // a last chunk
+    const int i = slot - fp.n_full;
+    b = fp.last_ord[i / p.Nkv];
+    h = i % p.Nkv;
+    nch = fp.nch[b];
+    j = nch - 1;
+  }
+  const DecodeSpan sp{fp.lo[b], fp.end[b], fp.lo[b] & ~(kDecodeTileTC - 1)};
+  *desc = span_item(sp, C, b, h, nch, j);
+  return fp.nat[b] + h * nch + j;
+}
+
+// Slot of round r for this CTA in the snake over G CTAs.
+__device__ __forceinline__ int fused_plan_slot(int r, int G) {
+  return r * G + ((r & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
 // Work items for the producer warp of a persistent CTA.  Slots are claimed from the
 // global counter one item ahead and resolved through the execution order (longest
 // first), so that the latency of the claim and of the two dependent loads overlaps

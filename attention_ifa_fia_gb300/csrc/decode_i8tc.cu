@@ -600,7 +600,7 @@ cudaError_t launch_i8(const DecodeParams& p, const CUtensorMap& tmK, const CUten
                       cudaStream_t stream) {
   const size_t smem = sizeof(I8Smem) + 1024;
   auto kern = (p.atten_mask || p.windowed) ? decode_i8tc_kernel<QT, GP, true> : decode_i8tc_kernel<QT, GP, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem(kern, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);
   e = launch_dependent(kern, grid, kThreads, smem, stream, tmK, tmV, p, box_rows);

@@ -72,6 +72,7 @@ struct TcSmem {
   uint64_t s_full[2], p_full[2];
   int pv_stop;  // index of the sentinel tile, set by the softmax warps when they reach it
   uint32_t tmem_base;
+  FusedPlan plan;  // the in-kernel schedule (p.fused_plan)
 };
 
 // Offset of element (row g, token t) of the P^T operand: two 64-token slabs of
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const uint32_t tmem = sm.tmem_base;
   griddep_wait();  // the plan kernel's item list, counters and reset are complete and visible
   griddep_launch_dependents();  // the merge kernel may be scheduled; it waits for this grid to finish
+  if (p.fused_plan) fused_plan_build(p, sm.plan, tid, kThreadsTC);  // (no plan launch preceded)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -130,14 +132,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       tma_prefetch_desc(&tmQ);
     }
     ItemQueue queue;
-    queue.start(p, lane);
+    if (!p.fused_plan) queue.start(p, lane);
     const int bs = p.block_size;
     const uint32_t piece_bytes = (uint32_t)box_rows * C::kRowBytes;
     int j = 0, local_item = 0;
     bool ok = true;
-    while (ok) {
+    for (int round = 0; ok; ++round) {
       int4 desc;
-      const int item = queue.pop(p, lane, &desc);
+      int item;
+      if (p.fused_plan) {  // this CTA's next slot of the in-kernel schedule
+        const int slot = fused_plan_slot(round, gridDim.x);
+        item = slot < sm.plan.n_items ? fused_plan_item(p, sm.plan, slot, &desc) : -1;
+      } else {
+        item = queue.pop(p, lane, &desc);
+      }
       if (item < 0) break;
       const DecodeItem it = decode_item(desc);
       const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             tma_load_2d(sm.kv[st][1] + off, &tmV, kc.x0 + bx * 64, kc.row, &sm.kv_full[st]);
           }
         }
-        if (tok0 == t0) queue.prefetch(p, lane);
+        if (tok0 == t0 && !p.fused_plan) queue.prefetch(p, lane);
       }
       ++local_item;
     }
@@ -478,7 +486,7 @@ cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& tmK, const CUten
                       int box_rows, int grid, cudaStream_t stream) {
   const size_t smem = sizeof(TcSmem<D>) + 1024;
   auto kern = (p.atten_mask || p.windowed) ? decode_tc_kernel<D, DT, GP, true> : decode_tc_kernel<D, DT, GP, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem(kern, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);
   e = launch_dependent(kern, grid, kThreadsTC, smem, stream, tmK, tmV, tmQ, p, box_rows);

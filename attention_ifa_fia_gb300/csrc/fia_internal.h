@@ -27,6 +27,15 @@ enum : int { kKernelDecodePlan = 0, kKernelDecodeAttention = 1, kKernelDecodeMer
 // Sets the text fia_last_error() returns on this thread and returns `code`.
 int report_error(int code, const char* fmt, ...);
 
+// Raises the dynamic shared-memory limit of kernel `func` to at least `bytes`, calling
+// cudaFuncSetAttribute only the first time a (context, function) pair needs a larger value,
+// so that repeated launches (and stream capture) do not repeat it.
+cudaError_t ensure_smem(const void* func, size_t bytes);
+template <typename K>
+inline cudaError_t ensure_smem(K* kern, size_t bytes) {
+  return ensure_smem(reinterpret_cast<const void*>(kern), bytes);
+}
+
 // The calling thread's current CUDA context (a CUcontext; NULL if none is current yet).
 // Returns 0 or a non-zero fia status.
 int current_context(void** ctx);
@@ -56,7 +65,7 @@ constexpr int kDecodeConsumers = 256;  // math threads (8 warps)
 struct DecodeWorkspace {
   int* counter;     // dynamic work counter (reset by the plan kernel)
   int* n_items;     // number of work items written by the plan kernel
-  int* seg_base;    // (B) first item of batch b
+  int* seg_base;    // (B + 1) first item of batch b; [B] = the number of items
   int4* items;      // (max_items) {b, hkv | nch << 16, first token, last token + 1}
   int* order;       // (max_items) execution order: order[k] is the k-th item to be claimed
   float* part_o;    // (max_items, G, D) normalised partial outputs
@@ -100,6 +109,9 @@ struct DecodeParams {
   // band of the one query (windowed != 0): batch b of length L sees keys
   // L - 1 - win_pre .. L - 1 + win_next (both within [-2^30, 2^30], win_pre + win_next >= 0)
   int windowed, win_pre, win_next;
+  // nonzero: the tensor-core attention kernel schedules its own work items (no plan launch;
+  // B <= kFusedPlanMaxB)
+  int fused_plan;
   DecodeWorkspace ws;
   unsigned int* status;  // device status word
 };
@@ -121,7 +133,9 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const C
                           const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode_tc_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                        const CUtensorMap& tmQ, int box_rows, int grid, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
 constexpr int kDecodeTileTC = 128;  // tokens per tensor-core tile; work items are multiples of it
+constexpr int kFusedPlanMaxB = 256;  // batches the in-kernel schedule of the 16-bit kernel holds
 
 // int8 KV with D = 128 runs on the tensor-core kernel of decode_i8tc.cu (128-token
 // tiles, G <= 8); other int8 shapes on the CUDA-core kernel.

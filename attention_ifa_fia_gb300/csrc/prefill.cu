@@ -1085,13 +1085,13 @@ cudaError_t launch_prefill_attention(const PrefillParams& p, const CUtensorMap& 
   if (p.G % 2 == 0) {  // heads 2hp and 2hp + 1 share a kv head
     const size_t smem = sizeof(P2Smem<kD>);
     auto kern = band ? prefill_pair_kernel<kD, DT, true> : prefill_pair_kernel<kD, DT, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem(kern, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_dependent(kern, num_sms, kP2Threads, smem, stream, tmQ, tmK, tmV, p);
   }
   const size_t smem = sizeof(PSmem<kD>);
   auto kern = band ? prefill_tc_kernel<kD, DT, true> : prefill_tc_kernel<kD, DT, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem(kern, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms, kPThreads, smem, stream>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
@@ -1107,7 +1107,7 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const
   const size_t plan_smem = prefill_plan_smem(max_key_tiles);
   cudaError_t e = cudaSuccess;
   if (plan_smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem);
+    e = ensure_smem(prefill_plan_kernel, (int)plan_smem);
     if (e != cudaSuccess) return e;
   }
   e = launch_dependent(prefill_plan_kernel, 1, 1024, plan_smem, stream, p, max_key_tiles, pairs ? 2 : 1);

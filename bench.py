@@ -83,6 +83,78 @@ def max_over_ranks(x: float, dist, device) -> float:
     return float(t.item())
 
 
+def e2e_pipeline(torch, stream, call, dev_in, pin_in, outs, warmup, steps, barrier):
+    """Times `steps` end-to-end steps: step i copies its inputs host -> device (pin_in[j] ->
+    dev_in[j], j = i mod len(dev_in)) on a copy stream, runs call(i, j, o) on `stream`, and
+    copies its results device -> host (outs[o], o = i mod 2) on a second copy stream.  Events
+    keep every buffer's copy and use in order, so the copies of one step overlap the compute
+    of its neighbours.  Returns the milliseconds from the first copy to the last result on
+    the host side of the copy (CUDA events)."""
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    nin = len(dev_in)
+    in_ready = [torch.cuda.Event() for _ in range(nin)]
+    in_free = [None] * nin
+    out_ready = [torch.cuda.Event() for _ in range(2)]
+    out_free = [None, None]
+
+    def one(i):
+        j, o = i % nin, i % 2
+        with torch.cuda.stream(h2d):
+            if in_free[j] is not None:
+                h2d.wait_event(in_free[j])
+            dev_in[j].copy_(pin_in[j], non_blocking=True)
+            in_ready[j].record(h2d)
+        stream.wait_event(in_ready[j])
+        if out_free[o] is not None:
+            stream.wait_event(out_free[o])
+        call(i, j, o)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        in_free[j] = ev
+        out_ready[o].record(stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(out_ready[o])
+            outs[o][1].copy_(outs[o][0], non_blocking=True)
+            ev2 = torch.cuda.Event()
+            ev2.record(d2h)
+            out_free[o] = ev2
+
+    for k in range(min(warmup, 20)):
+        one(k)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    h2d.wait_event(e0)
+    for k in range(steps):
+        one(k)
+    stream.wait_stream(d2h)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return e0.elapsed_time(e1)
+
+
+def staged(tensors, dev, torch):
+    """One device buffer holding copies of `tensors` (each at a 256-byte aligned offset) and a
+    pinned host buffer of the same bytes; returns (device buffer, host buffer, views of the
+    device buffer shaped and typed as the tensors)."""
+    offs, n = [], 0
+    for t in tensors:
+        offs.append(n)
+        n += (t.numel() * t.element_size() + 255) // 256 * 256
+    d = torch.zeros(n, dtype=torch.uint8, device=dev)
+    views = []
+    for t, o in zip(tensors, offs):
+        nb = t.numel() * t.element_size()
+        v = d[o:o + nb].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    h.copy_(d)
+    return d, h, tuple(views)
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -186,9 +258,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    make = W.WORKLOADS[args.workload]
-    seed = 1001 + 97 * rank if args.workload == "bf16_gqa_decode" else None
-    case = make(seed) if seed is not None else make()
+    case = W.WORKLOADS[args.workload]()  # every rank runs the same workload (independent replicas)
     nbytes = decode_bytes(case)
     copies = [DeviceDecode(case, dev) for _ in range(COPIES)]
     num_splits = W.LONG_CTX_CHUNKS if args.workload == "long_ctx_sink_decode" else 0
@@ -240,6 +310,7 @@ def run_ours(args, rank, world, local_rank):
     for k in range(args.steps):
         step(k)
     e1.record(stream)
+    host_s = time.time() - h0  # host time to issue the K steps (asynchronous launches)
     torch.cuda.synchronize()
     h1 = time.time()
     barrier()
@@ -261,42 +332,30 @@ def run_ours(args, rank, world, local_rank):
     status = F.fia_device_status()
     ms = max_over_ranks(ms, dist, dev)
 
-    # ---- end to end through the public API with host buffers
-    pin_q = [torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory() for c in copies]
-    pin_bt = [torch.empty(c.bt.shape, dtype=c.bt.dtype).pin_memory() for c in copies]
-    pin_len = [torch.empty(c.lens.shape, dtype=c.lens.dtype).pin_memory() for c in copies]
-    for j, c in enumerate(copies):
-        pin_q[j].copy_(c.q)
-        pin_bt[j].copy_(c.bt)
-        pin_len[j].copy_(c.lens)
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_mx = torch.empty(mx.shape, dtype=mx.dtype).pin_memory()
-    h_sm = torch.empty(sm.shape, dtype=sm.dtype).pin_memory()
-    h2d = pin_q[0].numel() * pin_q[0].element_size() + pin_bt[0].numel() * 4 + pin_len[0].numel() * 8
-    d2h = h_out.numel() * h_out.element_size() + 2 * h_mx.numel() * 4
+    # ---- end to end through the public API with host buffers: per step the query, block
+    # table and lengths go host -> device in one copy (one pinned staging buffer, one device
+    # buffer whose views are the call's inputs), and out, max and sum come back in one copy
+    in_views = [(c.q, c.bt, c.lens) for c in copies]
+    dev_in, pin_in, e2e_in = [], [], []
+    for views in in_views:
+        d, h, v = staged(views, dev, torch)
+        dev_in.append(d)
+        pin_in.append(h)
+        e2e_in.append(v)
+    outs = [staged((out, mx, sm), dev, torch) for _ in range(2)]  # results double-buffered
+    h2d = dev_in[0].numel()
+    d2h = outs[0][0].numel()
 
-    def e2e_step(i):
-        j = i % COPIES
+    def e2e_call(i, j, o):
         c = copies[j]
-        c.q.copy_(pin_q[j], non_blocking=True)
-        c.bt.copy_(pin_bt[j], non_blocking=True)
-        c.lens.copy_(pin_len[j], non_blocking=True)
-        step(i)
-        h_out.copy_(out, non_blocking=True)
-        h_mx.copy_(mx, non_blocking=True)
-        h_sm.copy_(sm, non_blocking=True)
+        q_e, bt_e, len_e = e2e_in[j]
+        o_e, mx_e, sm_e = outs[o][2]
+        F.fia_decode(q_e, c.k, c.v, bt_e, len_e, max_kv_len=case.max_len, num_heads=case.Nq,
+                     num_kv_heads=case.Nkv, scale=case.scale, antiquant_scale=c.aq_scale,
+                     antiquant_offset=c.aq_offset, sink=c.sink, out=o_e, softmax_max=mx_e, softmax_sum=sm_e,
+                     num_splits=num_splits, workspace=ws)
 
-    for k in range(min(args.warmup, 20)):
-        e2e_step(k)
-    torch.cuda.synchronize()
-    barrier()
-    e0.record(stream)
-    for k in range(args.steps):
-        e2e_step(k)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    ms_e2e = e0.elapsed_time(e1)
+    ms_e2e = e2e_pipeline(torch, stream, e2e_call, dev_in, pin_in, outs, args.warmup, args.steps, barrier)
     ms_e2e = max_over_ranks(ms_e2e, dist, dev)
     sampler.stop()
 
@@ -334,9 +393,11 @@ def run_ours(args, rank, world, local_rank):
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": round(world * nbytes["total"] * steps / (ms_e2e / 1e3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "per step: q, block table, lengths host->device; out, max, sum device->host; "
-                        "KV cache resident"},
+                "note": "per step: q, block table and lengths host->device in one copy; out, max and sum "
+                        "device->host in one copy; copies on their own streams, overlapping neighbouring "
+                        "steps' compute (inputs over 4 buffers, results over 2); KV cache resident"},
         "gpu_launches": sum(v[1] for v in kern.values()),
+        "host_us_per_step": round(host_s / steps * 1e6, 2),
         "device_status": status,
         "clocks": sampler.summary(h0, h1),
     }
@@ -365,7 +426,7 @@ def run_prefill_bench(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    case = W.causal_prefill_tnd(1004 + 97 * rank)
+    case = W.WORKLOADS[args.workload]()  # every rank runs the same workload (independent replicas)
     flops = prefill_flops(case)
     copies = [DevicePrefill(case, dev) for _ in range(COPIES)]
     msq, mskv = int(case.lengths_q.max()), int(case.lengths_kv.max())
@@ -416,39 +477,28 @@ def run_prefill_bench(args, rank, world, local_rank):
     pf_ms, pf_n = F.fia_trace_collect(F.KERNEL_PREFILL)
     status = F.fia_device_status()
     ms = max_over_ranks(ms, dist, dev)
-    # end to end: q, k, v and cumulative lengths from pinned host memory, out/max/sum back
-    pins = [(torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory().copy_(c.q),
-             torch.empty(c.k.shape, dtype=c.k.dtype).pin_memory().copy_(c.k),
-             torch.empty(c.v.shape, dtype=c.v.dtype).pin_memory().copy_(c.v),
-             torch.empty(c.cu_q.shape, dtype=c.cu_q.dtype).pin_memory().copy_(c.cu_q)) for c in copies]
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_mx = torch.empty(mx.shape, dtype=mx.dtype).pin_memory()
-    h_sm = torch.empty(sm.shape, dtype=sm.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in pins[0]) + pins[0][3].numel() * 8
-    d2h = h_out.numel() * h_out.element_size() + 2 * h_mx.numel() * 4
+    # end to end: q, k, v and both cumulative lengths host -> device in one copy (one pinned
+    # staging buffer, one device buffer whose views are the call's inputs); out, max and sum
+    # device -> host in one copy
+    dev_in, pin_in, e2e_in = [], [], []
+    for c in copies:
+        d, h, v = staged((c.q, c.k, c.v, c.cu_q, c.cu_kv), dev, torch)
+        dev_in.append(d)
+        pin_in.append(h)
+        e2e_in.append(v)
+    outs = [staged((out, mx, sm), dev, torch) for _ in range(2)]  # results double-buffered
+    h2d = dev_in[0].numel()
+    d2h = outs[0][0].numel()
 
-    def e2e_step(i):
-        j = i % COPIES
-        c, pq = copies[j], pins[j]
-        c.q.copy_(pq[0], non_blocking=True)
-        c.k.copy_(pq[1], non_blocking=True)
-        c.v.copy_(pq[2], non_blocking=True)
-        c.cu_q.copy_(pq[3], non_blocking=True)
-        c.cu_kv.copy_(pq[3], non_blocking=True)
-        step(i)
-        h_out.copy_(out, non_blocking=True)
-        h_mx.copy_(mx, non_blocking=True)
-        h_sm.copy_(sm, non_blocking=True)
+    def e2e_call(i, j, o):
+        q_e, k_e, v_e, cuq_e, cukv_e = e2e_in[j]
+        o_e, mx_e, sm_e = outs[o][2]
+        F.fia_prefill(q_e, k_e, v_e, cuq_e, cukv_e, max_seqlen_q=msq, max_seqlen_kv=mskv, num_heads=case.Nq,
+                      num_kv_heads=case.Nkv, scale=case.scale, mask=3, out=o_e, softmax_max=mx_e, softmax_sum=sm_e,
+                      workspace=ws)
 
-    for k in range(min(args.warmup, 10)):
-        e2e_step(k)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for k in range(args.steps):
-        e2e_step(k)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1)
+    ms_e2e = e2e_pipeline(torch, stream, e2e_call, dev_in, pin_in, outs, args.warmup, args.steps,
+                          (lambda: dist.barrier()) if dist is not None else (lambda: None))
     ms_e2e = max_over_ranks(ms_e2e, dist, dev)
     sampler.stop()
     if rank != 0:
@@ -460,18 +510,20 @@ def run_prefill_bench(args, rank, world, local_rank):
         "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "causal_prefill_tnd", "B": case.B, "T": case.T, "Nq": case.Nq, "Nkv": case.Nkv,
+        "config": {"workload": args.workload, "B": case.B, "T": case.T, "Nq": case.Nq, "Nkv": case.Nkv,
                    "D": case.D, "lengths": case.lengths_q.tolist(), "causal_flops_per_step": flops,
                    "l2": f"inputs rotated over {COPIES} device copies",
                    "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2) if achieved else None, "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": round(achieved / tf_burst, 4) if achieved else None,
                      "traffic": load_traffic("causal_prefill_tnd"),
-                     "kernel": "prefill_tc (plan + attention, traced together)",
+                     "kernel": "prefill_pair (tcgen05 head-pair attention; plan and attention traced together)",
                      "peak_source": f"{src} bf16 dense burst (MEASURED_PEAKS.json bf16_tflops)"},
         "e2e": {"value": round(world * flops * args.steps / (ms_e2e / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "per step: q, k, v, cumulative lengths host->device; out, max, sum device->host"},
+                "note": "per step: q, k, v and cumulative lengths host->device in one copy; out, max and sum "
+                        "device->host in one copy; copies on their own streams, overlapping neighbouring "
+                        "steps' compute (inputs over 4 buffers, results over 2)"},
         "gpu_launches": 2 * pf_n, "device_status": status, "clocks": sampler.summary(h0, h1),
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -506,6 +558,91 @@ def cpu_baseline_prefill(case: W.PrefillCase, budget_s: float = 15.0, seed: int 
             "seconds": round(dt, 2)}
 
 
+def run_ring_bench(args, rank, world, local_rank):
+    """The context-parallel ring (attention_ifa_fia_gb300.ring) on one GPU: the long-context
+    workload's KV cache split into --ring-shards shards, one per simulated rank (a CUDA
+    stream); a step is fia_decode over every shard, then the ring of partial exchanges
+    (device copies) and RingAttentionUpdate merges, every rank ending with the full result.
+    value = the workload's algorithmic bytes / step time."""
+    import torch
+    import attention_ifa_fia_gb300 as F
+    from attention_ifa_fia_gb300.ring import RingDecodeGraph
+    from fia_workloads import DeviceDecode
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    case = W.long_ctx_sink_decode()
+    nbytes = decode_bytes(case)
+    ncopies = 2  # 2 x 1.07 GB of KV > L2
+    copies = [DeviceDecode(case, dev) for _ in range(ncopies)]
+    shards = args.ring_shards
+    # one CUDA graph per input copy: a step is one graph launch (the ring's few hundred
+    # operations issued from Python would otherwise bound it)
+    graphs = [RingDecodeGraph(c.q, c.k, c.v, c.bt, c.lens, world=shards, max_kv_len=case.max_len,
+                              num_heads=case.Nq, num_kv_heads=case.Nkv, scale=case.scale, sink=c.sink)
+              for c in copies]
+
+    def step(i):
+        return graphs[i % ncopies].replay()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    t_w = time.time()
+    i = 0
+    while i < args.warmup or time.time() - t_w < args.min_warmup_s:
+        step(i)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    F.fia_device_status()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    h0 = time.time()
+    e0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    # kernels of one step: per shard the decode's plan, attention and merge, then one merge
+    # (ring_attention_update) per rank and ring step
+    launches = 3 * shards + shards * (shards - 1)
+    status = F.fia_device_status()
+    sampler.stop()
+    if rank != 0:
+        return None
+    hbm, _, _, src = peaks()
+    gbs = world * nbytes["total"] * args.steps / (ms / 1e3) / 1e9
+    return {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "long_ctx_sink_ring", "B": case.B, "Nq": case.Nq, "Nkv": case.Nkv, "D": case.D,
+                   "block_size": case.block_size, "kv_lengths": "131072 each", "ring_shards": shards,
+                   "algorithmic_bytes_per_step": nbytes["total"],
+                   "l2": f"inputs rotated over {ncopies} device copies ({ncopies} x {nbytes['kv'] / 1e6:.0f} MB of KV > L2)",
+                   "parallelism": f"{shards} ranks simulated as CUDA streams of one GPU"
+                                  + (f", independent replicas x{world}" if world > 1 else "")},
+        "hbm_frac_of_measured": round(gbs / world / hbm, 4),
+        "roofline": {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs / world / hbm, 4), "traffic": None,
+                     "kernel": "whole ring step (attention on every shard, exchanges and merges)",
+                     "peak_source": f"{src} HBM copy bandwidth"},
+        "gpu_launches": launches * args.steps, "device_status": status, "clocks": sampler.summary(h0, h1),
+        "graph": "each step one CUDA graph launch of the captured ring",
+    }
+
+
 # Sources of the kernel whose DRAM traffic bench.py reports, per workload; a recorded
 # figure is used only while the sha1 of these files matches the one taken with it.
 TRAFFIC_SOURCES = {
@@ -514,6 +651,7 @@ TRAFFIC_SOURCES = {
     "int8_antiquant_decode": ("decode_i8tc.cu", "decode_i8.cuh", "decode.cu", "decode_common.cuh", "fia_device.cuh",
                               "fia_internal.h"),
     "causal_prefill_tnd": ("prefill.cu", "decode_common.cuh", "fia_device.cuh", "fia_internal.h"),
+    "causal_prefill_tnd_t8k": ("prefill.cu", "decode_common.cuh", "fia_device.cuh", "fia_internal.h"),
 }
 
 
@@ -541,10 +679,48 @@ def load_traffic(workload):
 
 
 # ----------------------------------------------------------------------------- reference arm: the oracle
+def run_reference_prefill(args):
+    """The oracle's prefill on a bounded sample of (token, head) rows per step."""
+    import oracle
+    case = W.WORKLOADS[args.workload]()
+    rng = np.random.default_rng(0)
+    total = case.T * case.Nq
+    t = time.perf_counter()
+    oracle.prefill(case.q, case.k, case.v, case.cu_q, case.cu_kv, Nq=case.Nq, Nkv=case.Nkv, D=case.D,
+                   scale=case.scale, causal=True, dtype=oracle.BF16, rows=np.arange(64, dtype=np.int64))
+    per_row = max((time.perf_counter() - t) / 64, 1e-5)
+    n = int(min(total, max(16, 120.0 / max(args.steps + args.warmup, 1) / per_row)))
+    tot_t, tot_f = 0.0, 0
+    for k in range(args.warmup + args.steps):
+        rows = rng.choice(total, size=n, replace=False).astype(np.int64)
+        t = time.perf_counter()
+        oracle.prefill(case.q, case.k, case.v, case.cu_q, case.cu_kv, Nq=case.Nq, Nkv=case.Nkv, D=case.D,
+                       scale=case.scale, causal=True, dtype=oracle.BF16, rows=rows)
+        dt = time.perf_counter() - t
+        tok = rows // case.Nq
+        b = np.searchsorted(case.cu_q, tok, side="right") - 1
+        qi = tok - case.cu_q[b]
+        vis = np.clip(qi + (case.lengths_kv[b] - case.lengths_q[b]) + 1, 0, case.lengths_kv[b])
+        if k >= args.warmup:
+            tot_t += dt
+            tot_f += 4 * case.D * int(vis.sum())
+    value = tot_f / tot_t / 1e12
+    sample = f"each step: {n} of {total} (token, head) rows of {args.workload}"
+    return {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload}, "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    case = W.WORKLOADS[args.workload]()
+    if args.workload.startswith("causal_prefill_tnd"):
+        return run_reference_prefill(args)
+    case = W.WORKLOADS["long_ctx_sink_decode" if args.workload == "long_ctx_sink_ring" else args.workload]()
     rng = np.random.default_rng(0)
     all_groups = [(b, h) for b in range(case.B) for h in range(case.Nkv)]
     probe = [all_groups[i] for i in rng.permutation(len(all_groups))[:2]]
@@ -578,7 +754,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="bf16_gqa_decode",
                     choices=["bf16_gqa_decode", "int8_antiquant_decode", "long_ctx_sink_decode", "tiny_decode",
-                             "causal_prefill_tnd"])
+                             "causal_prefill_tnd", "causal_prefill_tnd_t8k", "long_ctx_sink_ring"])
+    ap.add_argument("--ring-shards", type=int, default=8,
+                    help="long_ctx_sink_ring: KV shards (ranks simulated as CUDA streams of one GPU)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep warming up for at least this long (clocks settle, the sampler sees load)")
@@ -594,8 +772,10 @@ def main():
             import torch.distributed as dist
             torch.cuda.set_device(local_rank)
             dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-        if args.workload == "causal_prefill_tnd":
+        if args.workload.startswith("causal_prefill_tnd"):
             line = run_prefill_bench(args, rank, world, local_rank)
+        elif args.workload == "long_ctx_sink_ring":
+            line = run_ring_bench(args, rank, world, local_rank)
         else:
             line = run_ours(args, rank, world, local_rank)
         if world > 1:

@@ -271,6 +271,12 @@ def causal_prefill_tnd(seed: int = 1004) -> PrefillCase:
     return make_prefill_case(Nq=32, Nkv=8, D=128, dtype=BF16, B=8, len_range=(1, 2048), seed=seed)
 
 
+def causal_prefill_tnd_t8k(seed: int = 1010) -> PrefillCase:
+    """The causal prefill workload at its nominal size: the same recipe, with the first seed
+    from 1004 up whose eight lengths total within 2% of T = 8192 (seed 1010: T = 8267)."""
+    return causal_prefill_tnd(seed)
+
+
 # ---------------------------------------------------------------- device copies
 # Upload of a case's arrays to a CUDA device, bit for bit (torch is imported only here, so
 # the oracle's CPU tests need no GPU stack).  No arithmetic of the method happens here.
@@ -325,5 +331,6 @@ WORKLOADS = {
     "int8_antiquant_decode": int8_antiquant_decode,
     "long_ctx_sink_decode": long_ctx_sink_decode,
     "causal_prefill_tnd": causal_prefill_tnd,
+    "causal_prefill_tnd_t8k": causal_prefill_tnd_t8k,
 }
 LONG_CTX_CHUNKS = 32

@@ -52,8 +52,9 @@ def test_long_context_recipe_without_generating_it():
     assert W.pool_blocks([131072] * 4, 128) == 4 * 1024
 
 
-def test_prefill_workload_recipe():
-    case = W.causal_prefill_tnd()
+@pytest.mark.parametrize("name", ["causal_prefill_tnd", "causal_prefill_tnd_t8k"])
+def test_prefill_workload_recipe(name):
+    case = W.WORKLOADS[name]()
     assert (case.B, case.Nq, case.Nkv, case.D) == (8, 32, 8, 128)
     assert case.lengths_q.min() >= 1 and case.lengths_q.max() <= 2048
     assert np.array_equal(case.lengths_q, case.lengths_kv)
@@ -72,3 +73,10 @@ def test_poisoned_slots_are_exactly_the_unused_ones():
             used[case.block_table[b, t // 8], t % 8] = True
     nan = np.isnan(f).all(axis=(1, 3))          # (blocks, rows): every head and channel NaN
     assert np.array_equal(nan, ~used)
+
+
+def test_nominal_size_prefill_is_the_first_seed_near_8192():
+    """The T = 8192 variant is the first seed from 1004 whose draw totals within 2% of 8192."""
+    totals = {seed: int(W.causal_prefill_tnd(seed).cu_q[-1]) for seed in range(1004, 1011)}
+    assert [s for s, t in totals.items() if abs(t - 8192) <= 0.02 * 8192] == [1010]
+    assert int(W.causal_prefill_tnd_t8k().cu_q[-1]) == totals[1010] == 8267
