@@ -47,7 +47,7 @@ class DecodeOptions(ctypes.Structure):
                 ("atten_mask", ctypes.c_void_p), ("atten_mask_stride", ctypes.c_int64),
                 ("quant_scale2", ctypes.c_void_p), ("quant_offset2", ctypes.c_void_p),
                 ("quant2_per_channel", ctypes.c_int), ("band", ctypes.c_int), ("pre_tokens", ctypes.c_int64),
-                ("next_tokens", ctypes.c_int64)]
+                ("next_tokens", ctypes.c_int64), ("q_len", ctypes.c_int)]
 
 
 def _load() -> ctypes.CDLL:
@@ -165,7 +165,7 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
                antiquant_mode: int = AQ_PER_CHANNEL, softmax_lse: Optional[torch.Tensor] = None,
                atten_mask: Optional[torch.Tensor] = None, quant_scale2: Optional[torch.Tensor] = None,
                quant_offset2: Optional[torch.Tensor] = None, pre_tokens: Optional[int] = None,
-               next_tokens: Optional[int] = None,
+               next_tokens: Optional[int] = None, q_len: int = 1,
                _force_ex: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
     """Paged decode attention.  q: (B, Nq, D) (any layout of that memory); k/v_cache:
     (num_blocks, Nkv, block_size, D), or with kv_layout=KV_BNBSH (num_blocks, block_size,
@@ -174,7 +174,9 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     receives max + ln(sum).  atten_mask: (B, S) / (B, 1, S) / (B, 1, 1, S) bool, int8 or
     uint8, 1 = key masked out, S >= max_kv_len.  quant_scale2 (and quant_offset2): fp32 of
     1 or Nq * D values; out is then int8.  pre_tokens / next_tokens: the band around the
-    query (keys L - 1 - pre .. L - 1 + next).  Returns (out, softmax_max, softmax_sum)."""
+    query (keys L - 1 - pre .. L - 1 + next).  q_len = s > 1: q is (B, s, Nq, D), s query
+    positions per batch, position i at key L - s + i seeing keys up to it; out (B, s, Nq, D)
+    and max / sum / lse (B, s, Nq).  Returns (out, softmax_max, softmax_sum)."""
     B, D = int(q.shape[0]), int(q.shape[-1])
     num_blocks = int(k_cache.shape[0])
     block_size = int(k_cache.shape[1] if kv_layout == KV_BNBSH else k_cache.shape[2])
@@ -182,8 +184,8 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     if scale is None:
         scale = D ** -0.5
     if out is None:
-        out = torch.empty((B, num_heads, D), dtype=torch.int8 if quant_scale2 is not None else q.dtype,
-                          device=q.device)
+        shape = (B, num_heads, D) if q_len <= 1 else (B, q_len, num_heads, D)
+        out = torch.empty(shape, dtype=torch.int8 if quant_scale2 is not None else q.dtype, device=q.device)
     mask_stride = 0
     if atten_mask is not None:
         if atten_mask.dtype not in (torch.bool, torch.int8, torch.uint8) or not atten_mask.is_contiguous():
@@ -200,7 +202,7 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
             raise ValueError("quant_offset2 must match quant_scale2")
         q2_per_channel = int(n2 != 1)
     if workspace is None:
-        nbytes = fia_decode_workspace_size(B, num_heads, nkv, D, max_kv_len, block_size, num_splits)
+        nbytes = fia_decode_workspace_size(B, num_heads * max(q_len, 1), nkv, D, max_kv_len, block_size, num_splits)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     args = (_ptr(q), dtype_code(q), _ptr(k_cache), _ptr(v_cache), dtype_code(k_cache), _ptr(block_table),
             int(block_table.shape[1]), _ptr(actual_seq_lengths), int(max_kv_len), B, num_heads, nkv, D, block_size,
@@ -209,14 +211,15 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
             workspace.numel() * workspace.element_size(), _stream(stream))
     band = pre_tokens is not None or next_tokens is not None
     plain = (kv_layout == KV_BNNBSD and antiquant_mode == AQ_PER_CHANNEL and softmax_lse is None
-             and atten_mask is None and quant_scale2 is None and quant_offset2 is None and not band)
+             and atten_mask is None and quant_scale2 is None and quant_offset2 is None and not band
+             and q_len <= 1)
     if plain and not _force_ex:
         _check(_lib.fia_decode(*args), "fia_decode")
     else:
         opts = DecodeOptions(int(kv_layout), int(antiquant_mode), _ptr(softmax_lse), _ptr(atten_mask), mask_stride,
                              _ptr(quant_scale2), _ptr(quant_offset2), q2_per_channel, int(band),
                              int(pre_tokens if pre_tokens is not None else 1 << 40),
-                             int(next_tokens if next_tokens is not None else 1 << 40))
+                             int(next_tokens if next_tokens is not None else 1 << 40), int(q_len))
         _check(_lib.fia_decode_ex(*args, ctypes.byref(opts)), "fia_decode_ex")
     return out, softmax_max, softmax_sum
 

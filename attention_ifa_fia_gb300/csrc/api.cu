@@ -111,6 +111,24 @@ int make_tmap(CUtensorMap* m, const void* base, int dtype, uint64_t cols, uint64
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// 3-D tensor map over queries (rows, Nq, D) -> dims (D, Nq, rows), boxes of 64 channels x G
+// heads x qs rows, 128-byte swizzle: one kv head's G query heads at qs consecutive positions,
+// landing as qs * G rows of 128 bytes (row i * G + g).
+int make_tmap_q3(CUtensorMap* m, const void* base, int dtype, uint64_t D, uint64_t Nq, uint64_t rows, uint32_t G,
+                 uint32_t qs) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FIA_ERR_RUNTIME, "cuTensorMapEncodeTiled is not available from the driver");
+  const CUtensorMapDataType t = dtype == fia::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[3] = {D, Nq, rows};
+  cuuint64_t strides[2] = {D * 2, Nq * D * 2};
+  cuuint32_t box[3] = {64, G, qs};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FIA_ERR_RUNTIME, "cuTensorMapEncodeTiled (queries) failed (%d)", (int)r);
+  return FIA_SUCCESS;
+}
+
 int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
 
 // ---------------------------------------------------------------- decode planner
@@ -316,6 +334,7 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   const float* qo2 = opt ? opt->quant_offset2 : nullptr;
   const int q2_per_channel = opt ? opt->quant2_per_channel : 0;
   const bool windowed = opt && opt->band;
+  const int qs = (opt && opt->q_len > 1) ? opt->q_len : 1;  // query positions per batch
   // -- 161001: required pointers
   if (!q || !k_cache || !v_cache || !block_table || !actual_seq_lengths || !out)
     return fail(FIA_ERR_PARAM_NULLPTR, "q, k_cache, v_cache, block_table, actual_seq_lengths and out are required");
@@ -346,6 +365,15 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   if (qo2 && !qs2) return fail(FIA_ERR_PARAM_INVALID, "quant_offset2 without quant_scale2");
   if (q2_per_channel != 0 && q2_per_channel != 1)
     return fail(FIA_ERR_PARAM_INVALID, "quant2_per_channel must be 0 or 1 (got %d)", q2_per_channel);
+  if (opt && (opt->q_len < 0 || opt->q_len > 16))
+    return fail(FIA_ERR_PARAM_INVALID, "q_len = %d outside [0, 16]", opt->q_len);
+  if (qs > 1 && (Nq / Nkv) * qs > (kv_dtype == FIA_I8 ? 8 : 16))
+    return fail(FIA_ERR_PARAM_INVALID, "GQA group %d x q_len %d exceeds %d in this build", Nq / Nkv, qs,
+                kv_dtype == FIA_I8 ? 8 : 16);
+  if (qs > 1 && Nq * qs > 256)
+    return fail(FIA_ERR_PARAM_INVALID, "Nq x q_len = %d exceeds 256", Nq * qs);
+  if (qs > 1 && (mask || windowed))
+    return fail(FIA_ERR_PARAM_INVALID, "q_len > 1 takes the causal cut only (no attenMask or band) in this build");
   // the band in keys around the query (position L - 1), clamped to +-2^30 (no length is that large)
   constexpr int64_t kBandCap = 1LL << 30;
   int64_t win_pre = kBandCap, win_next = kBandCap;
@@ -372,7 +400,7 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   DecodePlan plan;
   if (int rc = plan_decode(B, Nkv, max_kv_len, num_splits, d->num_sms, &plan)) return rc;
   const int G = Nq / Nkv;
-  const size_t need = fia::decode_workspace_bytes(B, Nkv, G, D, plan.max_items);
+  const size_t need = fia::decode_workspace_bytes(B, Nkv, G * qs, D, plan.max_items);
   if (check_only) return ok();
   if (workspace_bytes < need)
     return fail(FIA_ERR_PARAM_INVALID, "workspace of %zu bytes is smaller than the %zu required", workspace_bytes,
@@ -394,6 +422,8 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   p.Nq = Nq;
   p.Nkv = Nkv;
   p.G = G;
+  p.qs = qs;
+  p.GV = G * qs;
   p.D = D;
   p.block_size = block_size;
   p.num_blocks = num_blocks;
@@ -419,7 +449,7 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   p.fused_plan = (kv_dtype != FIA_I8 && B <= fia::kFusedPlanMaxB) ? 1 : 0;
   p.win_pre = (int)win_pre;
   p.win_next = (int)win_next;
-  p.ws = fia::decode_workspace_carve(workspace, B, Nkv, G, D, plan.max_items);
+  p.ws = fia::decode_workspace_carve(workspace, B, Nkv, G * qs, D, plan.max_items);
   p.status = d->status;
   if (aq_mode == FIA_AQ_PER_TENSOR) {  // the kernels read the per-channel form
     float* sc = p.ws.aux;
@@ -431,7 +461,7 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   }
   if (lse) {  // max and sum are needed for the log-sum-exp; scratch if not requested
     if (!p.softmax_max) p.softmax_max = p.ws.aux + 4 * Nkv * D;
-    if (!p.softmax_sum) p.softmax_sum = p.ws.aux + 4 * Nkv * D + (size_t)B * Nq;
+    if (!p.softmax_sum) p.softmax_sum = p.ws.aux + 4 * Nkv * D + (size_t)B * qs * Nq;
   }
 
   // 16-bit KV runs on the tensor-core kernel (128-token tiles), int8 KV with D = 128 on the
@@ -450,12 +480,16 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   if (int rc = make_tmap(&tmK, k_cache, kv_dtype, cols, rows, box_cols, box_rows)) return rc;
   if (int rc = make_tmap(&tmV, v_cache, kv_dtype, cols, rows, box_cols, box_rows)) return rc;
   if (tc) {
-    if (int rc = make_tmap(&tmQ, q, q_dtype, D, (uint64_t)B * Nq, 64, 16)) return rc;
+    if (qs == 1) {
+      if (int rc = make_tmap(&tmQ, q, q_dtype, D, (uint64_t)B * Nq, 64, 16)) return rc;
+    } else {  // (D, Nq, B * q_len) with (64, G, q_len) boxes: a kv head's G x q_len query rows
+      if (int rc = make_tmap_q3(&tmQ, q, q_dtype, D, Nq, (uint64_t)B * qs, G, qs)) return rc;
+    }
   }
   cudaError_t e = fia::launch_decode(p, tmK, tmV, tc ? &tmQ : nullptr, box_rows, d->num_sms, stream);
   if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "decode launch: %s", cudaGetErrorString(e));
   if (lse) {
-    e = fia::launch_lse(p.softmax_max, p.softmax_sum, lse, (int64_t)B * Nq, stream);
+    e = fia::launch_lse(p.softmax_max, p.softmax_sum, lse, (int64_t)B * qs * Nq, stream);
     if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "log-sum-exp launch: %s", cudaGetErrorString(e));
   }
   return ok();
@@ -600,6 +634,8 @@ int fia_debug_i8_qprep(const void* q, fia_dtype q_dtype, const float* antiquant_
   p.Nq = Nq;
   p.Nkv = nkv;
   p.G = Nq / nkv;
+  p.qs = 1;
+  p.GV = p.G;
   p.D = 128;
   p.scale_log2 = (float)(scale * 1.4426950408889634);
   p.ws.qprep = static_cast<uint8_t*>(blocks);

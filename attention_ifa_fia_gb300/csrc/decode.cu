@@ -76,7 +76,8 @@ struct Cfg {
 struct __align__(16) StageMeta {
   int b, hkv, tok0, n;  // tile start token and valid tokens
   int item, first, last, nch;  // nch: items of this (b, kv head) segment
-  int nlo, pad0, pad1, pad2;   // tokens below tok0 + nlo lie before the window (masked)
+  int nlo, qlim, pad1, pad2;   // tokens below tok0 + nlo lie before the window (masked); query
+                               // position i sees tokens up to qlim + i
 };
 
 template <int KVT, int D, int GP>
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem<KVT, D, GP>& sm =
       *reinterpret_cast<Smem<KVT, D, GP>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = p.G;
+  const int G = p.GV;  // virtual heads (query heads x query positions) of a kv head
 
   if (tid == 0) {
     for (int s = 0; s < kDecodeStages; ++s) {
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const DecodeItem it = decode_item(desc);
       const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
       const int t0 = t_begin & ~(kTT - 1);  // the first tile (t_begin is aligned but for a window)
+      const int qlim = p.qs > 1 ? clamp_len(p, b, false) - p.qs : (1 << 30);  // position 0's last key
       const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
       for (int tok0 = t0; tok0 < t_end; tok0 += kTT) {
         const int n = min(kTT, t_end - tok0);
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m.b = b; m.hkv = hkv; m.tok0 = tok0; m.n = n;
           m.item = item; m.first = first; m.last = (tok0 + kTT >= t_end); m.nch = it.nch;
           m.nlo = max(t_begin - tok0, 0);
+          m.qlim = qlim;
           mbar_arrive_expect_tx(&sm.full[stage], bytes);
         }
         __syncwarp();
@@ -338,9 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sm.kv[stage][1] + off, &tmV, x, kc.row, &sm.full[stage]);
           }
         }
-        if (first && lane == 0) {
-          const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) + ((int64_t)b * p.Nq + (int64_t)hkv * G) * D;
-          bulk_load(sm.q[stage], qsrc, (uint32_t)(G * D * 2), &sm.full[stage]);
+        if (first && lane == 0) {  // the G query rows of each query position
+          for (int i = 0; i < p.qs; ++i) {
+            const uint16_t* qsrc = static_cast<const uint16_t*>(p.q) + q_row(p, b, hkv, i * p.G) * D;
+            bulk_load(sm.q[stage] + i * p.G * D, qsrc, (uint32_t)(p.G * D * 2), &sm.full[stage]);
+          }
         }
         if (first) queue.prefetch(p, lane);
         if (++stage == kDecodeStages) { stage = 0; phase ^= 1u; }
@@ -481,7 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < GP; ++i)
           if (i < cnt)
-            sm.s[gh + i][t] = (t < meta.n && t >= meta.nlo && !key_masked(p, meta.b, meta.tok0 + t))
+            sm.s[gh + i][t] = (t < meta.n && t >= meta.nlo && !key_masked(p, meta.b, meta.tok0 + t) &&
+                               meta.tok0 + t <= meta.qlim + (gh + i) / p.G)
                                   ? v[i] * p.scale_log2 : -INFINITY;
       }
     }
@@ -566,15 +572,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           float s = 0.f;
 #pragma unroll
           for (int w2 = 0; w2 < kConsumerWarps; ++w2) s += sm.red[w2][o];
-          const int g = o / D, h = meta.hkv * G + g;
+          const int g = o / D;
+          const int64_t row = q_row(p, meta.b, meta.hkv, g);
           float M, W;
-          const float v = single_item_output(s, sm.m_run[g], sm.l_run[g], p.sink, h, &M, &W);
-          const int64_t oi = ((int64_t)meta.b * p.Nq + meta.hkv * G) * D + o;
+          const float v = single_item_output(s, sm.m_run[g], sm.l_run[g], p.sink, q_head(p, meta.hkv, g), &M, &W);
+          const int64_t oi = row * D + (o - g * D);
           if (p.q_dtype == kBF16) store_out<kBF16>(p.out, oi, v);
           else store_out<kF16>(p.out, oi, v);
           if (o % D == 0) {
-            if (p.softmax_max) p.softmax_max[(int64_t)meta.b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
-            if (p.softmax_sum) p.softmax_sum[(int64_t)meta.b * p.Nq + h] = W;
+            if (p.softmax_max) p.softmax_max[row] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+            if (p.softmax_sum) p.softmax_sum[row] = W;
           }
         }
       } else {
@@ -617,7 +624,8 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   const int seg0 = p.ws.seg_base[b], seg1 = p.ws.seg_base[b + 1];  // batch b's items, all kv heads
   const int nch = (seg1 - seg0) / p.Nkv;
   if (nch <= 1 && !p.partials_only) return;
-  const int G = p.G, D = p.D, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // G: virtual heads (query heads x query positions) of the kv head
+  const int G = p.GV, D = p.D, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int first = seg0 + hkv * nch;
   const float4* po = reinterpret_cast<const float4*>(p.ws.part_o + (int64_t)first * G * D);
   const int q4n = G * D / 4;  // float4 outputs per partial
@@ -634,7 +642,8 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
   }
   __syncthreads();
   for (int g = warp; g < G; g += kMergeThreads / 32) {
-    const int h = hkv * G + g;
+    const int h = q_head(p, hkv, g);
+    const int64_t orow = q_row(p, b, hkv, g);
     float2* row = ml + g * nch;
     float M = -INFINITY;
     for (int j = lane; j < nch; j += 32) M = fmaxf(M, row[j].x);
@@ -655,8 +664,8 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     __syncwarp();
     for (int j = lane; j < nch; j += 32) row[j].x *= inv;
     if (lane == 0) {
-      if (p.softmax_max) p.softmax_max[(int64_t)b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
-      if (p.softmax_sum) p.softmax_sum[(int64_t)b * p.Nq + h] = W;
+      if (p.softmax_max) p.softmax_max[orow] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+      if (p.softmax_sum) p.softmax_sum[orow] = W;
     }
   }
   __syncthreads();
@@ -693,9 +702,10 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
       acc.z = fmaf(w, v.z, acc.z);
       acc.w = fmaf(w, v.w, acc.w);
     }
-    const int64_t o = ((int64_t)b * p.Nq + hkv * G) * D + q4 * 4;
+    const int v = (q4 * 4) / D, d = q4 * 4 - v * D;
+    const int64_t o = q_row(p, b, hkv, v) * D + d;
     if (p.pq_scale) {
-      const int c = hkv * G * D + q4 * 4;  // channel of acc.x within the (Nq, D) row
+      const int c = q_head(p, hkv, v) * D + d;  // channel of acc.x within the (Nq, D) row
       const float a[4] = {acc.x, acc.y, acc.z, acc.w};
       uint32_t w = 0;
 #pragma unroll
@@ -793,9 +803,9 @@ cudaError_t launch_attention(const DecodeParams& p, const CUtensorMap& tmK, cons
 template <int KVT, int D>
 cudaError_t launch_attention_g(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows,
                                int grid, cudaStream_t stream) {
-  if (p.G <= 1) return launch_attention<KVT, D, 1>(p, tmK, tmV, box_rows, grid, stream);
-  if (p.G <= 2) return launch_attention<KVT, D, 2>(p, tmK, tmV, box_rows, grid, stream);
-  if (p.G <= 4) return launch_attention<KVT, D, 4>(p, tmK, tmV, box_rows, grid, stream);
+  if (p.GV <= 1) return launch_attention<KVT, D, 1>(p, tmK, tmV, box_rows, grid, stream);
+  if (p.GV <= 2) return launch_attention<KVT, D, 2>(p, tmK, tmV, box_rows, grid, stream);
+  if (p.GV <= 4) return launch_attention<KVT, D, 4>(p, tmK, tmV, box_rows, grid, stream);
   return launch_attention<KVT, D, 8>(p, tmK, tmV, box_rows, grid, stream);
 }
 
@@ -913,7 +923,7 @@ cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
   const int max_chunks = (p.max_kv_len + p.chunk_tokens - 1) / p.chunk_tokens;
   if (max_chunks <= 1 && !p.partials_only) return cudaSuccess;
-  const size_t msmem = sizeof(float2) * (size_t)p.G * (max_chunks > 1 ? max_chunks : 1);
+  const size_t msmem = sizeof(float2) * (size_t)p.GV * (max_chunks > 1 ? max_chunks : 1);
   auto merge = (p.q_dtype == kBF16) ? decode_merge_kernel<kBF16> : decode_merge_kernel<kF16>;
   if (msmem > 48 * 1024) {
     e = ensure_smem(merge, (int)msmem);

@@ -22,6 +22,17 @@ __device__ __forceinline__ KvCoord kv_coord(const DecodeParams& p, int32_t blk, 
   return c;
 }
 
+// Row of virtual head v (position v / G, query head hkv * G + v % G) of batch b in the
+// (B, qs, Nq) rows of q, out, softmax max and sum; and its query head.
+__device__ __forceinline__ int64_t q_row(const DecodeParams& p, int b, int hkv, int v) {
+  if (p.qs == 1) return (int64_t)b * p.Nq + hkv * p.G + v;
+  const int i = v / p.G;
+  return ((int64_t)b * p.qs + i) * p.Nq + hkv * p.G + (v - i * p.G);
+}
+__device__ __forceinline__ int q_head(const DecodeParams& p, int hkv, int v) {
+  return hkv * p.G + (p.qs == 1 ? v : v % p.G);
+}
+
 // Work item {b, kv head | (chunk count of the segment) << 16, first token, last token + 1}.
 // A segment's chunks start at its span's base, a multiple of 128 tokens, so the tiles of
 // every chunk are aligned; the first chunk starts at the span's first key (which the

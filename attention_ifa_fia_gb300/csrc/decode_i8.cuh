@@ -22,7 +22,7 @@
 // block with one bulk copy.
 #pragma once
 
-#include "fia_device.cuh"
+#include "decode_common.cuh"
 
 namespace fia {
 
@@ -54,8 +54,9 @@ __device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t& h01, uint32
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h23) : "r"(b), "r"(0x64806480u));
 }
 
-// One warp prepares row g of block (b, hkv); row index R = (b * Nkv + hkv) * 16 + g.
-// Lane l handles channels 4l .. 4l + 3.
+// One warp prepares row g of block (b, hkv); row index R = (b * Nkv + hkv) * 16 + g.  Row g
+// is virtual head g: the query of head hkv * G + g % G at position g / G (one position: head
+// hkv * G + g).  Lane l handles channels 4l .. 4l + 3.
 __device__ __forceinline__ void i8_qprep_row(const DecodeParams& p, int64_t R, int lane) {
   const int64_t blk = R / kI8Heads;
   const int g = (int)(R % kI8Heads);
@@ -64,9 +65,8 @@ __device__ __forceinline__ void i8_qprep_row(const DecodeParams& p, int64_t R, i
   const int d0 = lane * 4;
   uint2 hi_w = make_uint2(0u, 0u), lo_w = make_uint2(0u, 0u);
   float2 kn = make_float2(0.f, 0.f);
-  if (g < p.G) {
-    const int h = hkv * p.G + g;
-    const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.q) + ((int64_t)b * p.Nq + h) * 128 + d0);
+  if (g < p.GV) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.q) + q_row(p, b, hkv, g) * 128 + d0);
     float q[4];
     if (p.q_dtype == kBF16) {
       q[0] = bf16lo(raw.x); q[1] = bf16hi(raw.x); q[2] = bf16lo(raw.y); q[3] = bf16hi(raw.y);

@@ -68,7 +68,8 @@ constexpr int kPBytes = kNP * kT * 2;
 struct __align__(16) I8Meta {
   int b, hkv, n, item;
   int first, last, qbuf, nch;
-  int tok0, nlo, pad1, pad2;  // tok0: the tile's first token; tokens below tok0 + nlo are masked
+  int tok0, nlo, qlim, pad2;  // tok0: the tile's first token; tokens below tok0 + nlo are masked;
+                              // query position i sees tokens up to qlim + i
 };
 
 constexpr int kMetaRing = 4;  // tile descriptors in flight between the K converters, MMA and softmax warps
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   I8Smem& sm = *reinterpret_cast<I8Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = p.G;
+  const int G = p.GV;  // virtual heads (query heads x query positions) of a kv head
 
   // Synchronisation.  Buffers indexed by tile j use slot j & 1 (j % kStages for the
   // int8 ring); a slot is reused two tiles later, and most "free" signals follow
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
       const int t0 = t_begin & ~(kT - 1);  // the first tile (t_begin is aligned but for a window)
       const int qb = local_item & 1;
+      const int qlim = p.qs > 1 ? clamp_len(p, b, false) - p.qs : (1 << 30);  // position 0's last key
       if (!mbar_wait(&sm.q_empty[qb], ((local_item >> 1) & 1) ^ 1u, p.status)) { ok = false; break; }
       if (lane == 0) {
         const uint8_t* src = p.ws.qprep + ((int64_t)b * p.Nkv + hkv) * kI8QBlockBytes;
@@ -235,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m.b = b; m.hkv = hkv; m.n = n; m.item = item;
           m.first = (tok0 == t0); m.last = (tok0 + kT >= t_end); m.qbuf = qb; m.nch = it.nch; m.tok0 = tok0;
           m.nlo = max(t_begin - tok0, 0);
+          m.qlim = qlim;
           if (bytes) mbar_arrive_expect_tx(&sm.kv_full[st], bytes);
           else mbar_arrive(&sm.kv_full[st]);
         }
@@ -330,9 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the tile's exact maximum is exchanged and the reference raised.  m_thr is each
     // thread's true maximum, combined at the item's end for the max and sum outputs.
     float m_run[GH], l_part[GH], alpha_prev[GH], acc[GH], m_thr[GH];
+    int vpos[GH];  // query position of each of this group's virtual heads
 #pragma unroll
     for (int g = 0; g < GH; ++g) {
       m_run[g] = kNoRef; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_thr[g] = -INFINITY;
+      vpos[g] = (h0 + g) / p.G;
     }
     float vs_cur = 0.f, vo_cur = 0.f;  // value antiquant of channel r for the current item
     int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
@@ -382,18 +387,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           a[g] = vs_cur * fmaf(-vo_cur, lt[g], acc[g] * sc);  // sum_t 2^(s_t - mm) v^_t, unnormalised
         }
         if (prev_nch == 1 && !p.partials_only) {
-          const int64_t orow = ((int64_t)prev_b * p.Nq + prev_hkv * G) * kD + r;
 #pragma unroll
           for (int g = 0; g < GH; ++g) {
             const int hg = h0 + g;
             if (hg < G) {
-              const int h = prev_hkv * G + hg;
+              const int64_t row = q_row(p, prev_b, prev_hkv, hg);
               float M, W;
-              const float v = single_item_output(a[g], mm[g], lt[g], p.sink, h, &M, &W);
-              store_out<QT>(p.out, orow + (int64_t)hg * kD, v);
+              const float v = single_item_output(a[g], mm[g], lt[g], p.sink, q_head(p, prev_hkv, hg), &M, &W);
+              store_out<QT>(p.out, row * kD + r, v);
               if (r == hg) {
-                if (p.softmax_max) p.softmax_max[(int64_t)prev_b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
-                if (p.softmax_sum) p.softmax_sum[(int64_t)prev_b * p.Nq + h] = W;
+                if (p.softmax_max) p.softmax_max[row] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+                if (p.softmax_sum) p.softmax_sum[row] = W;
               }
             }
           }
@@ -450,7 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int g = 0; g < GH; ++g) {
         const float2 c = kn[g];
-        x[g] = valid ? fmaf(s[g], c.x, c.y) : -INFINITY;
+        // (several query positions: position i sees tokens up to qlim + i)
+        const bool vis = valid && (!kKeyMask || meta.tok0 + r <= meta.qlim + vpos[g]);
+        x[g] = vis ? fmaf(s[g], c.x, c.y) : -INFINITY;
         above |= x[g] > m_run[g] + kLazyMax;  // (the unset reference, kNoRef, is exceeded by any score)
         m_thr[g] = fmaxf(m_thr[g], x[g]);
       }
@@ -599,7 +605,8 @@ template <int QT, int GP>
 cudaError_t launch_i8(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows, int grid,
                       cudaStream_t stream) {
   const size_t smem = sizeof(I8Smem) + 1024;
-  auto kern = (p.atten_mask || p.windowed) ? decode_i8tc_kernel<QT, GP, true> : decode_i8tc_kernel<QT, GP, false>;
+  auto kern = (p.atten_mask || p.windowed || p.qs > 1) ? decode_i8tc_kernel<QT, GP, true>
+                                                       : decode_i8tc_kernel<QT, GP, false>;
   cudaError_t e = ensure_smem(kern, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);
@@ -611,9 +618,9 @@ cudaError_t launch_i8(const DecodeParams& p, const CUtensorMap& tmK, const CUten
 template <int QT>
 cudaError_t launch_i8_g(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows, int grid,
                         cudaStream_t stream) {
-  if (p.G <= 2) return launch_i8<QT, 2>(p, tmK, tmV, box_rows, grid, stream);
-  if (p.G <= 4) return launch_i8<QT, 4>(p, tmK, tmV, box_rows, grid, stream);
-  if (p.G <= 8) return launch_i8<QT, 8>(p, tmK, tmV, box_rows, grid, stream);
+  if (p.GV <= 2) return launch_i8<QT, 2>(p, tmK, tmV, box_rows, grid, stream);
+  if (p.GV <= 4) return launch_i8<QT, 4>(p, tmK, tmV, box_rows, grid, stream);
+  if (p.GV <= 8) return launch_i8<QT, 8>(p, tmK, tmV, box_rows, grid, stream);
   return cudaErrorInvalidValue;  // int8 groups above 8 are rejected before launch
 }
 

@@ -53,8 +53,9 @@ struct TcCfg {
 struct __align__(16) TileMeta {
   int b, hkv, tok0, n;
   int item, first, last, qbuf;
-  int nch, nlo, pad1, pad2;  // nch: items of this (b, kv head) segment; tokens tok0 .. tok0 + nlo - 1
-                             // lie before the window and are masked
+  int nch, nlo, qlim, pad2;  // nch: items of this (b, kv head) segment; tokens tok0 .. tok0 + nlo - 1
+                             // lie before the window and are masked; with several query positions
+                             // position i sees tokens up to qlim + i
 };
 
 template <int D>
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   extern __shared__ uint8_t smem_raw[];
   TcSmem<D>& sm = *reinterpret_cast<TcSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = p.G;
+  const int G = p.G, GV = p.GV;  // GV: virtual heads (query heads x positions) of a kv head
 
   // Synchronisation.  kv_full: TMA -> score warp.  s_full: QK(j) committed -> softmax.
   // p_full: the four softmax warps -> PV warp (P(j) written) and score warp; each warp
@@ -152,11 +153,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       const int t0 = t_begin & ~(kT - 1);  // the first tile (t_begin is aligned but for a window)
       const int qb = local_item & 1;
       if (!mbar_wait(&sm.q_empty[qb], ((local_item >> 1) & 1) ^ 1u, p.status)) { ok = false; break; }
+      int qlim = 1 << 30;  // the last token position 0 sees (several query positions only)
+      if (p.qs > 1) qlim = (p.fused_plan ? sm.plan.end[b] : clamp_len(p, b, false)) - p.qs;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&sm.q_full[qb], C::kQBytes);
-        const int32_t row = b * p.Nq + hkv * G;
-        for (int bx = 0; bx < C::kNumBoxes; ++bx)
-          tma_load_2d(sm.q[qb] + bx * (kNP * 128), &tmQ, bx * 64, row, &sm.q_full[qb]);
+        if (p.qs == 1) {  // the group's 16 query rows (rows past G belong to other heads: unused)
+          mbar_arrive_expect_tx(&sm.q_full[qb], C::kQBytes);
+          const int32_t row = b * p.Nq + hkv * G;
+          for (int bx = 0; bx < C::kNumBoxes; ++bx)
+            tma_load_2d(sm.q[qb] + bx * (kNP * 128), &tmQ, bx * 64, row, &sm.q_full[qb]);
+        } else {  // (64 channels, G heads, qs positions) boxes: rows v = i * G + g
+          mbar_arrive_expect_tx(&sm.q_full[qb], (uint32_t)(C::kNumBoxes * GV * 128));
+          for (int bx = 0; bx < C::kNumBoxes; ++bx)
+            tma_load_3d(sm.q[qb] + bx * (kNP * 128), &tmQ, bx * 64, hkv * G, b * p.qs, &sm.q_full[qb]);
+        }
       }
       const int32_t* bt_row = p.block_table + (int64_t)b * p.bt_stride;
       for (int tok0 = t0; tok0 < t_end; tok0 += kT, ++j) {
@@ -178,7 +187,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           TileMeta& m = sm.meta[st];
           m.b = b; m.hkv = hkv; m.tok0 = tok0; m.n = n;
           m.item = item; m.first = (tok0 == t0); m.last = (tok0 + kT >= t_end); m.qbuf = qb;
-          m.nch = it.nch; m.nlo = max(t_begin - tok0, 0);
+          m.nch = it.nch; m.nlo = max(t_begin - tok0, 0); m.qlim = qlim;
           if (bytes) mbar_arrive_expect_tx(&sm.kv_full[st], bytes);
           else mbar_arrive(&sm.kv_full[st]);
         }
@@ -288,9 +297,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     const int r = quad * 32 + lane;            // TMEM lane: token of S, channel of O
     const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);
     float m_run[GH], l_part[GH], alpha_prev[GH], acc[GH], m_fin[GH], l_fin[GH];
+    int vpos[GH];  // query position of each of this group's virtual heads
 #pragma unroll
     for (int g = 0; g < GH; ++g) {
       m_run[g] = -INFINITY; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_fin[g] = -INFINITY; l_fin[g] = 0.f;
+      vpos[g] = (h0 + g) / G;
     }
     int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
     bool prev_first = false, prev_last = false;
@@ -335,41 +346,40 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         if (prev_nch == 1 && !p.partials_only) {
           // the segment is this one item: write the final output directly
           if (!C::kStacked || r < 64) {
-            const int64_t orow = ((int64_t)prev_b * p.Nq + prev_hkv * G) * D + r;
 #pragma unroll
             for (int g = 0; g < GH; ++g) {
               const int hg = h0 + g;
-              if (hg < G) {
+              if (hg < GV) {
                 const float a = C::kStacked ? acc[g] + sm.accx[r][hg] : acc[g];
-                const int h = prev_hkv * G + hg;
+                const int64_t row = q_row(p, prev_b, prev_hkv, hg);
                 float M, W;
-                const float v = single_item_output(a, mm[g], lt[g], p.sink, h, &M, &W);
-                store_out<DT>(p.out, orow + (int64_t)hg * D, v);
+                const float v = single_item_output(a, mm[g], lt[g], p.sink, q_head(p, prev_hkv, hg), &M, &W);
+                store_out<DT>(p.out, row * D + r, v);
                 if (r == hg) {
-                  if (p.softmax_max) p.softmax_max[(int64_t)prev_b * p.Nq + h] = (M == -INFINITY) ? -INFINITY : M * kLn2;
-                  if (p.softmax_sum) p.softmax_sum[(int64_t)prev_b * p.Nq + h] = W;
+                  if (p.softmax_max) p.softmax_max[row] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+                  if (p.softmax_sum) p.softmax_sum[row] = W;
                 }
               }
             }
           }
         } else {
           if (!C::kStacked || r < 64) {
-            float* po = p.ws.part_o + (int64_t)prev_item * G * D;
+            float* po = p.ws.part_o + (int64_t)prev_item * GV * D;
 #pragma unroll
             for (int g = 0; g < GH; ++g) {
               const int hg = h0 + g;
-              if (hg < G) {
+              if (hg < GV) {
                 const float a = C::kStacked ? acc[g] + sm.accx[r][hg] : acc[g];
                 po[hg * D + r] = lt[g] > 0.f ? a / lt[g] : 0.f;
               }
             }
           }
-          if (r >= h0 && r < h0 + GH && r < G) {
+          if (r >= h0 && r < h0 + GH && r < GV) {
             float mv = mm[0], lw = lt[0];
 #pragma unroll
             for (int g = 1; g < GH; ++g)
               if (r == h0 + g) { mv = mm[g]; lw = lt[g]; }
-            p.ws.part_ml[(int64_t)prev_item * G + r] = make_float2(mv, lw);
+            p.ws.part_ml[(int64_t)prev_item * GV + r] = make_float2(mv, lw);
           }
         }
         named_bar_sync(bar_group, 128);
@@ -410,7 +420,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
       for (int g = 0; g < GH; ++g) {
         const float sg = upper ? s[GH + g] : s[g];  // compile-time indices
-        x[g] = valid ? sg * p.scale_log2 : -INFINITY;
+        // (several query positions: position i sees tokens up to qlim + i)
+        const bool vis = valid && (!kKeyMask || meta.tok0 + r <= meta.qlim + vpos[g]);
+        x[g] = vis ? sg * p.scale_log2 : -INFINITY;
         mx[g] = warp_max(x[g]);
       }
       if (lane == 0) {
@@ -435,7 +447,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       uint8_t* pbuf = sm.p[sb];
 #pragma unroll
       for (int g = 0; g < GH; ++g) {
-        if (h0 + g < G) {
+        if (h0 + g < GV) {
           uint16_t h;
           if (DT == kBF16) h = __bfloat16_as_ushort(__float2bfloat16_rn(pr[g]));
           else h = __half_as_ushort(__float2half_rn(pr[g]));
@@ -485,7 +497,8 @@ template <int D, int DT, int GP>
 cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
                       int box_rows, int grid, cudaStream_t stream) {
   const size_t smem = sizeof(TcSmem<D>) + 1024;
-  auto kern = (p.atten_mask || p.windowed) ? decode_tc_kernel<D, DT, GP, true> : decode_tc_kernel<D, DT, GP, false>;
+  auto kern = (p.atten_mask || p.windowed || p.qs > 1) ? decode_tc_kernel<D, DT, GP, true>
+                                                       : decode_tc_kernel<D, DT, GP, false>;
   cudaError_t e = ensure_smem(kern, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);
@@ -499,9 +512,9 @@ cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& tmK, const CUten
 template <int D, int DT>
 cudaError_t launch_tc_g(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
                         int box_rows, int grid, cudaStream_t stream) {
-  if (p.G <= 2) return launch_tc<D, DT, 2>(p, tmK, tmV, tmQ, box_rows, grid, stream);
-  if (p.G <= 4) return launch_tc<D, DT, 4>(p, tmK, tmV, tmQ, box_rows, grid, stream);
-  if (p.G <= 8) return launch_tc<D, DT, 8>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+  if (p.GV <= 2) return launch_tc<D, DT, 2>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+  if (p.GV <= 4) return launch_tc<D, DT, 4>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+  if (p.GV <= 8) return launch_tc<D, DT, 8>(p, tmK, tmV, tmQ, box_rows, grid, stream);
   return launch_tc<D, DT, 16>(p, tmK, tmV, tmQ, box_rows, grid, stream);
 }
 

@@ -112,6 +112,11 @@ struct DecodeParams {
   // nonzero: the tensor-core attention kernel schedules its own work items (no plan launch;
   // B <= kFusedPlanMaxB)
   int fused_plan;
+  // query positions per batch (FusedInferAttentionScore, Q_S > 1 over the paged cache): q and
+  // out are (B, qs, Nq, D), position i of batch b (at key L_b - qs + i) sees keys
+  // t <= L_b - qs + i.  The kernels treat the qs positions of a kv head's G query heads as
+  // GV = G * qs virtual heads v = i * G + g; qs = 1 is plain decode
+  int qs, GV;
   DecodeWorkspace ws;
   unsigned int* status;  // device status word
 };

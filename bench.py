@@ -85,50 +85,64 @@ def max_over_ranks(x: float, dist, device) -> float:
 
 def e2e_pipeline(torch, stream, call, dev_in, pin_in, outs, warmup, steps, barrier):
     """Times `steps` end-to-end steps: step i copies its inputs host -> device (pin_in[j] ->
-    dev_in[j], j = i mod len(dev_in)) on a copy stream, runs call(i, j, o) on `stream`, and
-    copies its results device -> host (outs[o], o = i mod 2) on a second copy stream.  Events
-    keep every buffer's copy and use in order, so the copies of one step overlap the compute
-    of its neighbours.  Returns the milliseconds from the first copy to the last result on
-    the host side of the copy (CUDA events)."""
-    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    dev_in[j], j = i mod len(dev_in)) on a copy stream, runs call(i, j, o) on the compute
+    stream, and copies its results device -> host (outs[o], o = i mod 2) on a second copy
+    stream; events keep every buffer's copies and use in order, so one step's copies overlap
+    its neighbours' compute.  Groups of len(dev_in) steps are captured once in a CUDA graph
+    and replayed (issuing a step's copies, events and launches from Python costs about as
+    much host time as the GPU spends on it); leftover steps run uncaptured.  Returns the
+    milliseconds from the first copy to the last result in host memory (CUDA events on the
+    compute stream)."""
     nin = len(dev_in)
-    in_ready = [torch.cuda.Event() for _ in range(nin)]
-    in_free = [None] * nin
-    out_ready = [torch.cuda.Event() for _ in range(2)]
-    out_free = [None, None]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def one(i):
-        j, o = i % nin, i % 2
-        with torch.cuda.stream(h2d):
-            if in_free[j] is not None:
-                h2d.wait_event(in_free[j])
-            dev_in[j].copy_(pin_in[j], non_blocking=True)
-            in_ready[j].record(h2d)
-        stream.wait_event(in_ready[j])
-        if out_free[o] is not None:
-            stream.wait_event(out_free[o])
-        call(i, j, o)
-        ev = torch.cuda.Event()
-        ev.record(stream)
-        in_free[j] = ev
-        out_ready[o].record(stream)
-        with torch.cuda.stream(d2h):
-            d2h.wait_event(out_ready[o])
-            outs[o][1].copy_(outs[o][0], non_blocking=True)
-            ev2 = torch.cuda.Event()
-            ev2.record(d2h)
-            out_free[o] = ev2
+    def steps_on(comp, first, n):
+        """Issues steps first .. first + n - 1 with `comp` as the compute stream (the copy
+        streams wait for comp before, and comp for them after)."""
+        in_free, out_free = [None] * nin, [None, None]
+        h2d.wait_stream(comp)
+        d2h.wait_stream(comp)
+        for i in range(first, first + n):
+            j, o = i % nin, i % 2
+            with torch.cuda.stream(h2d):
+                if in_free[j] is not None:
+                    h2d.wait_event(in_free[j])
+                dev_in[j].copy_(pin_in[j], non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(h2d)
+            comp.wait_event(ready)
+            if out_free[o] is not None:
+                comp.wait_event(out_free[o])
+            with torch.cuda.stream(comp):
+                call(i, j, o)
+            done = torch.cuda.Event()
+            done.record(comp)
+            in_free[j] = done
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(done)
+                outs[o][1].copy_(outs[o][0], non_blocking=True)
+                freed = torch.cuda.Event()
+                freed.record(d2h)
+                out_free[o] = freed
+        comp.wait_stream(h2d)
+        comp.wait_stream(d2h)
 
-    for k in range(min(warmup, 20)):
-        one(k)
+    steps_on(stream, 0, min(warmup, 2 * nin))  # uncaptured warm-up (the library's set-up happens here)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    with torch.cuda.graph(graph, stream=cap):
+        steps_on(cap, 0, nin)
+    for _ in range(max(1, warmup // nin)):
+        graph.replay()
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    h2d.wait_event(e0)
-    for k in range(steps):
-        one(k)
-    stream.wait_stream(d2h)
+    for _ in range(steps // nin):
+        graph.replay()
+    if steps % nin:
+        steps_on(stream, 0, steps % nin)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -395,7 +409,8 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "per step: q, block table and lengths host->device in one copy; out, max and sum "
                         "device->host in one copy; copies on their own streams, overlapping neighbouring "
-                        "steps' compute (inputs over 4 buffers, results over 2); KV cache resident"},
+                        "steps' compute (inputs over 4 buffers, results over 2); each group of 4 steps one "
+                        "CUDA graph launch; KV cache resident"},
         "gpu_launches": sum(v[1] for v in kern.values()),
         "host_us_per_step": round(host_s / steps * 1e6, 2),
         "device_status": status,
@@ -523,7 +538,8 @@ def run_prefill_bench(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "per step: q, k, v and cumulative lengths host->device in one copy; out, max and sum "
                         "device->host in one copy; copies on their own streams, overlapping neighbouring "
-                        "steps' compute (inputs over 4 buffers, results over 2)"},
+                        "steps' compute (inputs over 4 buffers, results over 2); each group of 4 steps one "
+                        "CUDA graph launch"},
         "gpu_launches": 2 * pf_n, "device_status": status, "clocks": sampler.summary(h0, h1),
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -174,6 +174,17 @@ int fia_decode(const void* q, fia_dtype q_dtype, const void* k_cache, const void
  *                           the window's tiles are read.  Values beyond +-2^30 are clamped;
  *                           pre_tokens + next_tokens < 0 is FIA_ERR_PARAM_INVALID.  A batch
  *                           with no key in the window gets the empty-row outputs.
+ * options->q_len            s > 1: s query positions per batch (FusedInferAttentionScore runs
+ *                           Q_S > 1 against a paged cache with blockTable / actualSeqLengths,
+ *                           e.g. draft tokens of speculative decoding).  q and out are
+ *                           (B, s, Nq, D) row-major (BSND), softmax max / sum / lse (B, s, Nq);
+ *                           position i of batch b sits at key L_b - s + i and sees keys
+ *                           t <= L_b - s + i (rightDownCausal; a position before the first key
+ *                           gets the empty-row outputs).  The cache is read once for all s
+ *                           positions.  In this build (Nq / Nkv) * s <= 16 (<= 8 with int8
+ *                           KV), Nq * s <= 256, and neither atten_mask nor band with s > 1.
+ *                           The workspace is fia_decode_workspace_size() with Nq * s in place
+ *                           of Nq.
  * options == NULL behaves as fia_decode.  The workspace is fia_decode_workspace_size()
  * bytes, as for fia_decode.  Errors: an unknown layout or mode, the per-tensor mode
  * without int8 KV, a mask row shorter than max_kv_len, quant_offset2 without
@@ -192,6 +203,7 @@ typedef struct {
   int band;                    /* nonzero: keys L-1-pre_tokens .. L-1+next_tokens only */
   int64_t pre_tokens;
   int64_t next_tokens;
+  int q_len;                   /* 0 or 1: one query per batch; s > 1: q and out (B, s, Nq, D) */
 } fia_decode_options;
 
 int fia_decode_ex(const void* q, fia_dtype q_dtype, const void* k_cache, const void* v_cache, fia_dtype kv_dtype,

@@ -147,6 +147,12 @@ def _decode_ex(lib, B_, opts, **kw):
     (dict(quant_offset2=P), {}, INVALID),                              # offset without scale
     (dict(quant_scale2=P, quant2_per_channel=2), {}, INVALID),
     (dict(band=1, pre_tokens=3, next_tokens=-4), {}, INVALID),         # a band holding no key
+    (dict(q_len=17), {}, INVALID),                                     # more query positions than built
+    (dict(q_len=-1), {}, INVALID),
+    (dict(q_len=9), {}, INVALID),                                      # G 2 x 9 positions > 16
+    (dict(q_len=5), dict(kv_dtype=3, aqs=P, bs=32), INVALID),          # int8: G 2 x 5 > 8
+    (dict(q_len=2, band=1, pre_tokens=10, next_tokens=0), {}, INVALID),  # positions with a band
+    (dict(q_len=2, atten_mask=P, atten_mask_stride=64), {}, INVALID),  # positions with attenMask
 ])
 def test_decode_ex_rejects(F, fields, kw, code):
     from attention_ifa_fia_gb300 import _binding as B

@@ -47,8 +47,9 @@ def _bnbsh(cache: torch.Tensor) -> torch.Tensor:
 
 def _run(F, dd, ns=0, **kw):
     c = dd.case
-    mx = torch.full((c.B, c.Nq), float("nan"), dtype=torch.float32, device=dd.q.device)
-    sm = torch.full((c.B, c.Nq), float("nan"), dtype=torch.float32, device=dd.q.device)
+    rows = (c.B, c.Nq) if kw.get("q_len", 1) <= 1 else (c.B, kw["q_len"], c.Nq)
+    mx = torch.full(rows, float("nan"), dtype=torch.float32, device=dd.q.device)
+    sm = torch.full(rows, float("nan"), dtype=torch.float32, device=dd.q.device)
     k, v = kw.pop("k", dd.k), kw.pop("v", dd.v)
     out, mx, sm = F.fia_decode_ex(dd.q, k, v, dd.bt, dd.lens, max_kv_len=c.max_len, num_heads=c.Nq,
                                   num_kv_heads=c.Nkv, scale=c.scale, antiquant_scale=kw.pop("aq_scale", dd.aq_scale),
@@ -377,3 +378,91 @@ def test_decode_band_rejects_empty_band(F, cuda):
     dd = DeviceDecode(case)
     with pytest.raises(F.FiaError):
         _run(F, dd, pre_tokens=2, next_tokens=-3)
+
+
+# ------------------------------------------------------------------ several query positions (Q_S > 1)
+QLEN_CASES = {
+    # name: (make_decode_case kwargs with Nq = query heads, q_len); the 16-bit tensor-core kernel
+    # (D 128 and stacked D 64), the int8 tensor-core kernel (D 128) and the CUDA-core int8 kernel
+    "bf16_d128_g4_s4": (dict(B=3, Nq=8, Nkv=2, D=128, block_size=128, lengths=[300, 3, 1000]), 4),
+    "fp16_d64_g2_s8_sink_bs16": (dict(B=2, Nq=4, Nkv=2, D=64, block_size=16, dtype=W.FP16, lengths=[77, 250],
+                                      sink=True), 8),
+    "bf16_d128_mqa_s16": (dict(B=2, Nq=1, Nkv=1, D=128, block_size=64, lengths=[129, 15]), 16),
+    "int8_d128_g2_s4": (dict(B=2, Nq=4, Nkv=2, D=128, block_size=128, kv_dtype=W.INT8, lengths=[700, 130]), 4),
+    "int8_d64_g2_s3": (dict(B=2, Nq=4, Nkv=2, D=64, block_size=64, kv_dtype=W.INT8, lengths=[300, 2]), 3),
+}
+
+
+def _qlen_case(name, kw, s):
+    """A decode case with s query positions: q drawn as (B, s * Nq, D) and viewed as (B, s, Nq, D)."""
+    kw = dict(kw)
+    nq = kw.pop("Nq")
+    case = _case("qlen_" + name, Nq=nq * s, **kw)
+    case.Nq = nq
+    case.q = case.q.reshape(case.B, s, nq, case.D)
+    if case.sink is not None:
+        case.sink = np.ascontiguousarray(case.sink[:nq])
+    return case
+
+
+@pytest.mark.parametrize("num_splits", [0, 3])
+@pytest.mark.parametrize("name", sorted(QLEN_CASES))
+def test_decode_several_query_positions(F, cuda, name, num_splits):
+    """Q_S > 1 over the paged cache (FusedInferAttentionScore): the s positions of a batch are
+    its last s, each seeing the keys up to its own position (a position before the first key
+    gets the empty-row outputs); the oracle's q_len reading, every row."""
+    kw, s = QLEN_CASES[name]
+    case = _qlen_case(name, kw, s)
+    dd = DeviceDecode(case)
+    out, mx, sm = _run(F, dd, num_splits, q_len=s)
+    assert out.shape == (case.B, s, case.Nq, case.D) and mx.shape == (case.B, s, case.Nq)
+    code = {W.BF16: OR.BF16, W.FP16: OR.F16}
+    kvc = OR.I8 if case.kv_dtype == W.INT8 else code[case.kv_dtype]
+    o_ref, m_ref, s_ref = OR.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=case.Nq, Nkv=case.Nkv,
+                                    D=case.D, scale=case.scale, q_dtype=code[case.dtype], kv_dtype=kvc,
+                                    block_table=case.block_table, block_size=case.block_size, aq_scale=case.aq_scale,
+                                    aq_offset=case.aq_offset, sink=case.sink, q_len=s)
+    assert_close("out", out.double().cpu().numpy().reshape(-1, case.D), o_ref, *OUT_TOL[case.dtype])
+    assert_close_max("softmax_max", mx.double().cpu().numpy().reshape(-1), m_ref)
+    assert_close("softmax_sum", sm.double().cpu().numpy().reshape(-1), s_ref, *SUM_TOL)
+    assert F.fia_device_status() == 0
+
+
+def test_decode_several_query_positions_lse_and_int8_out(F, cuda):
+    """Q_S > 1 composed with the log-sum-exp and int8 outputs (every segment through the merge)."""
+    case = _qlen_case("lse_q8", dict(B=2, Nq=8, Nkv=2, D=128, block_size=128, lengths=[500, 60]), 4)
+    dd = DeviceDecode(case)
+    lse = torch.empty((case.B, 4, case.Nq), dtype=torch.float32, device="cuda")
+    out, mx, sm = _run(F, dd, 0, q_len=4, softmax_lse=lse)
+    o_ref, m_ref, s_ref = OR.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=case.Nq, Nkv=case.Nkv,
+                                    D=case.D, scale=case.scale, q_dtype=OR.BF16, kv_dtype=OR.BF16,
+                                    block_table=case.block_table, block_size=case.block_size, q_len=4)
+    fin = s_ref > 0
+    assert_close_max("softmax_lse", lse.double().cpu().numpy().reshape(-1)[fin], (m_ref + np.log(s_ref))[fin])
+    C = case.Nq * case.D
+    s2 = np.array([50.0], np.float32)
+    code, _, _ = _run(F, dd, 3, q_len=4, quant_scale2=torch.from_numpy(s2).cuda())
+    assert code.dtype == torch.int8 and tuple(code.shape) == (case.B, 4, case.Nq, case.D)
+    y, _ = OR.post_quant(o_ref.reshape(-1, C), s2)
+    _check_codes(code.cpu().numpy().reshape(-1, C), y.reshape(-1, C), o_ref.reshape(-1, C),
+                 np.broadcast_to(s2.astype(np.float64), (C,)), *OUT_TOL[case.dtype])
+    assert F.fia_device_status() == 0
+
+
+def test_decode_several_query_positions_full_size(F, cuda):
+    """The bf16 GQA decode workload with 4 query positions per batch (16 virtual heads per kv
+    head), sampled rows: the cache is read once for the 4 positions."""
+    base = W.bf16_gqa_decode()
+    case = _qlen_case("full", dict(B=base.B, Nq=base.Nq, Nkv=base.Nkv, D=base.D, block_size=base.block_size,
+                                   lengths=base.lengths), 4)
+    dd = DeviceDecode(case)
+    out, mx, sm = _run(F, dd, 0, q_len=4)
+    rng = np.random.default_rng(12)
+    rows = np.sort(rng.choice(case.B * 4 * case.Nq, size=512, replace=False)).astype(np.int64)
+    o_ref, m_ref, s_ref = OR.decode(case.q, case.k_cache, case.v_cache, case.lengths, Nq=case.Nq, Nkv=case.Nkv,
+                                    D=case.D, scale=case.scale, q_dtype=OR.BF16, kv_dtype=OR.BF16,
+                                    block_table=case.block_table, block_size=case.block_size, q_len=4, rows=rows)
+    assert_close("out", out.double().cpu().numpy().reshape(-1, case.D)[rows], o_ref, *OUT_TOL[case.dtype])
+    assert_close_max("softmax_max", mx.double().cpu().numpy().reshape(-1)[rows], m_ref)
+    assert_close("softmax_sum", sm.double().cpu().numpy().reshape(-1)[rows], s_ref, *SUM_TOL)
+    assert F.fia_device_status() == 0
