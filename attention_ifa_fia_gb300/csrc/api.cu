@@ -476,9 +476,19 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   const uint64_t cols = kv_layout == FIA_KV_BNBSH ? (uint64_t)Nkv * D : (uint64_t)D;
   const uint64_t rows = kv_layout == FIA_KV_BNBSH ? (uint64_t)num_blocks * block_size
                                                   : (uint64_t)num_blocks * Nkv * block_size;
-  CUtensorMap tmK, tmV, tmQ;
+  CUtensorMap tmK, tmV, tmQ, tail[2];
   if (int rc = make_tmap(&tmK, k_cache, kv_dtype, cols, rows, box_cols, box_rows)) return rc;
   if (int rc = make_tmap(&tmV, v_cache, kv_dtype, cols, rows, box_cols, box_rows)) return rc;
+  // boxes of 16 rows (32 for int8: its block size is a multiple of 32) for tiles with fewer
+  // than 128 keys, so that rows past a sequence's keys are not read
+  const int tail_rows = kv_dtype == FIA_I8 ? 32 : 16;
+  if (tile128 && box_rows > tail_rows) {
+    if (int rc = make_tmap(&tail[0], k_cache, kv_dtype, cols, rows, box_cols, tail_rows)) return rc;
+    if (int rc = make_tmap(&tail[1], v_cache, kv_dtype, cols, rows, box_cols, tail_rows)) return rc;
+  } else {
+    tail[0] = tmK;
+    tail[1] = tmV;
+  }
   if (tc) {
     if (qs == 1) {
       if (int rc = make_tmap(&tmQ, q, q_dtype, D, (uint64_t)B * Nq, 64, 16)) return rc;
@@ -486,7 +496,7 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
       if (int rc = make_tmap_q3(&tmQ, q, q_dtype, D, Nq, (uint64_t)B * qs, G, qs)) return rc;
     }
   }
-  cudaError_t e = fia::launch_decode(p, tmK, tmV, tc ? &tmQ : nullptr, box_rows, d->num_sms, stream);
+  cudaError_t e = fia::launch_decode(p, tmK, tmV, tc ? &tmQ : nullptr, tail, box_rows, d->num_sms, stream);
   if (e != cudaSuccess) return fail(FIA_ERR_RUNTIME, "decode launch: %s", cudaGetErrorString(e));
   if (lse) {
     e = fia::launch_lse(p.softmax_max, p.softmax_sum, lse, (int64_t)B * qs * Nq, stream);

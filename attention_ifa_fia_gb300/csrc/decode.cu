@@ -881,9 +881,10 @@ cudaError_t launch_lse(const float* mx, const float* sm, float* lse, int64_t n, 
 }
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                          const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream) {
+                          const CUtensorMap* tmQ, const CUtensorMap* tail, int box_rows, int num_sms,
+                          cudaStream_t stream) {
   if (tmQ && p.fused_plan) {  // the tensor-core kernel plans for itself: attention, then merge
-    cudaError_t e = launch_decode_tc_attention(p, tmK, tmV, *tmQ, box_rows, num_sms, stream);
+    cudaError_t e = launch_decode_tc_attention(p, tmK, tmV, *tmQ, tail, box_rows, num_sms, stream);
     if (e != cudaSuccess) return e;
     return launch_merge(p, stream);
   }
@@ -900,9 +901,9 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const C
   if (e != cudaSuccess) return e;
   const int grid = num_sms;
   if (tmQ) {
-    e = launch_decode_tc_attention(p, tmK, tmV, *tmQ, box_rows, grid, stream);
+    e = launch_decode_tc_attention(p, tmK, tmV, *tmQ, tail, box_rows, grid, stream);
   } else if (i8tc) {
-    e = launch_decode_i8tc_attention(p, tmK, tmV, box_rows, grid, stream);
+    e = launch_decode_i8tc_attention(p, tmK, tmV, tail, box_rows, grid, stream);
   } else if (p.kv_dtype == kBF16) {
     e = (p.D == 64) ? launch_attention_g<kBF16, 64>(p, tmK, tmV, box_rows, grid, stream)
                     : launch_attention_g<kBF16, 128>(p, tmK, tmV, box_rows, grid, stream);

@@ -144,6 +144,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 template <int QT, int GP, bool kKeyMask>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_i8tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmK16, const __grid_constant__ CUtensorMap tmV16,
                        const DecodeParams p, const int box_rows) {
   extern __shared__ uint8_t smem_raw[];
   I8Smem& sm = *reinterpret_cast<I8Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -193,11 +194,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmK16);
+      tma_prefetch_desc(&tmV16);
     }
     ItemQueue queue;
     queue.start(p, lane);
     const int bs = p.block_size;
-    const uint32_t piece_bytes = (uint32_t)box_rows * 128u;
     int j = 0, local_item = 0;
     bool ok = true;
     while (ok) {
@@ -221,16 +223,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % kStages;
         const uint32_t ph = (uint32_t)(j / kStages) & 1u;
         const int n = min(kT, t_end - tok0);
-        const int npieces = (n + box_rows - 1) / box_rows;
+        // (tiles of fewer than 128 keys in 32-row pieces, as the 16-bit kernel does with 16-row
+        // ones, measured 1% slower here: the tail map is passed but not used)
+        const bool fine = false;
+        const int prow = box_rows;
+        const int npieces = (n + prow - 1) / prow;
         int32_t blk = 0;
         bool valid = false;
         if (lane < npieces) {
-          blk = bt_row[(tok0 + lane * box_rows) / bs];
+          blk = bt_row[(tok0 + lane * prow) / bs];
           valid = blk >= 0 && (int64_t)blk < p.num_blocks;
           if (!valid) raise_status(p.status, kStatusBadBlockIndex);
         }
         const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-        const uint32_t bytes = 2u * piece_bytes * __popc(vmask);
+        const uint32_t bytes = 2u * (uint32_t)prow * 128u * __popc(vmask);
         if (!mbar_wait(&sm.kv_empty[st], ph ^ 1u, p.status)) { ok = false; break; }
         if (lane == 0) {
           I8Meta& m = sm.meta[st];
@@ -243,10 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (valid) {
-          const KvCoord kc = kv_coord(p, blk, tok0 + lane * box_rows, hkv);
-          const uint32_t off = (uint32_t)lane * box_rows * 128u;
-          tma_load_2d(sm.kv[st][0] + off, &tmK, kc.x0, kc.row, &sm.kv_full[st]);
-          tma_load_2d(sm.kv[st][1] + off, &tmV, kc.x0, kc.row, &sm.kv_full[st]);
+          const KvCoord kc = kv_coord(p, blk, tok0 + lane * prow, hkv);
+          const uint32_t off = (uint32_t)lane * prow * 128u;
+          tma_load_2d(sm.kv[st][0] + off, fine ? &tmK16 : &tmK, kc.x0, kc.row, &sm.kv_full[st]);
+          tma_load_2d(sm.kv[st][1] + off, fine ? &tmV16 : &tmV, kc.x0, kc.row, &sm.kv_full[st]);
         }
         if (tok0 == t0) queue.prefetch(p, lane);
       }
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int g = 0; g < GH; ++g) {
       m_run[g] = kNoRef; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_thr[g] = -INFINITY;
-      vpos[g] = (h0 + g) / p.G;
+      vpos[g] = kKeyMask ? (h0 + g) / p.G : 0;
     }
     float vs_cur = 0.f, vo_cur = 0.f;  // value antiquant of channel r for the current item
     int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
@@ -391,9 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int g = 0; g < GH; ++g) {
             const int hg = h0 + g;
             if (hg < G) {
-              const int64_t row = q_row(p, prev_b, prev_hkv, hg);
+              // several query positions run only on the key-mask instantiation; the plain one keeps
+              // the one-position rows (measured: the general mapping here slowed every tile by 4%)
+              const int64_t row = kKeyMask ? q_row(p, prev_b, prev_hkv, hg) : (int64_t)prev_b * p.Nq + prev_hkv * G + hg;
+              const int h = kKeyMask ? q_head(p, prev_hkv, hg) : prev_hkv * G + hg;
               float M, W;
-              const float v = single_item_output(a[g], mm[g], lt[g], p.sink, q_head(p, prev_hkv, hg), &M, &W);
+              const float v = single_item_output(a[g], mm[g], lt[g], p.sink, h, &M, &W);
               store_out<QT>(p.out, row * kD + r, v);
               if (r == hg) {
                 if (p.softmax_max) p.softmax_max[row] = (M == -INFINITY) ? -INFINITY : M * kLn2;
@@ -455,7 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int g = 0; g < GH; ++g) {
         const float2 c = kn[g];
         // (several query positions: position i sees tokens up to qlim + i)
-        const bool vis = valid && (!kKeyMask || meta.tok0 + r <= meta.qlim + vpos[g]);
+        bool vis = valid;
+        if constexpr (kKeyMask) vis = vis && meta.tok0 + r <= meta.qlim + vpos[g];
         x[g] = vis ? fmaf(s[g], c.x, c.y) : -INFINITY;
         above |= x[g] > m_run[g] + kLazyMax;  // (the unset reference, kNoRef, is exceeded by any score)
         m_thr[g] = fmaxf(m_thr[g], x[g]);
@@ -602,34 +612,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int QT, int GP>
-cudaError_t launch_i8(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows, int grid,
-                      cudaStream_t stream) {
+cudaError_t launch_i8(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap* tail,
+                      int box_rows, int grid, cudaStream_t stream) {
   const size_t smem = sizeof(I8Smem) + 1024;
   auto kern = (p.atten_mask || p.windowed || p.qs > 1) ? decode_i8tc_kernel<QT, GP, true>
                                                        : decode_i8tc_kernel<QT, GP, false>;
   cudaError_t e = ensure_smem(kern, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);
-  e = launch_dependent(kern, grid, kThreads, smem, stream, tmK, tmV, p, box_rows);
+  e = launch_dependent(kern, grid, kThreads, smem, stream, tmK, tmV, tail[0], tail[1], p, box_rows);
   trace_mark(kKernelDecodeAttention, 1, stream);
   return e;
 }
 
 template <int QT>
-cudaError_t launch_i8_g(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, int box_rows, int grid,
-                        cudaStream_t stream) {
-  if (p.GV <= 2) return launch_i8<QT, 2>(p, tmK, tmV, box_rows, grid, stream);
-  if (p.GV <= 4) return launch_i8<QT, 4>(p, tmK, tmV, box_rows, grid, stream);
-  if (p.GV <= 8) return launch_i8<QT, 8>(p, tmK, tmV, box_rows, grid, stream);
+cudaError_t launch_i8_g(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap* tail,
+                        int box_rows, int grid, cudaStream_t stream) {
+  if (p.GV <= 2) return launch_i8<QT, 2>(p, tmK, tmV, tail, box_rows, grid, stream);
+  if (p.GV <= 4) return launch_i8<QT, 4>(p, tmK, tmV, tail, box_rows, grid, stream);
+  if (p.GV <= 8) return launch_i8<QT, 8>(p, tmK, tmV, tail, box_rows, grid, stream);
   return cudaErrorInvalidValue;  // int8 groups above 8 are rejected before launch
 }
 
 }  // namespace
 
 cudaError_t launch_decode_i8tc_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                         int box_rows, int grid, cudaStream_t stream) {
-  return p.q_dtype == kBF16 ? launch_i8_g<kBF16>(p, tmK, tmV, box_rows, grid, stream)
-                            : launch_i8_g<kF16>(p, tmK, tmV, box_rows, grid, stream);
+                                         const CUtensorMap* tail, int box_rows, int grid, cudaStream_t stream) {
+  return p.q_dtype == kBF16 ? launch_i8_g<kBF16>(p, tmK, tmV, tail, box_rows, grid, stream)
+                            : launch_i8_g<kF16>(p, tmK, tmV, tail, box_rows, grid, stream);
 }
 
 // ------------------------------------------------------------------- probes

@@ -89,7 +89,8 @@ __device__ __forceinline__ uint32_t p_offset(int g, int t) {
 template <int D, int DT, int GP, bool kKeyMask>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const __grid_constant__ CUtensorMap tmQ, const DecodeParams p, const int box_rows) {
+                     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK16,
+                     const __grid_constant__ CUtensorMap tmV16, const DecodeParams p, const int box_rows) {
   using C = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   TcSmem<D>& sm = *reinterpret_cast<TcSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -131,11 +132,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK16);
+      tma_prefetch_desc(&tmV16);
     }
     ItemQueue queue;
     if (!p.fused_plan) queue.start(p, lane);
     const int bs = p.block_size;
-    const uint32_t piece_bytes = (uint32_t)box_rows * C::kRowBytes;
     int j = 0, local_item = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
@@ -172,16 +174,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const int st = j % C::kStages;
         const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
         const int n = min(kT, t_end - tok0);
-        const int npieces = (n + box_rows - 1) / box_rows;
+        // a tile holding fewer than 128 keys (an item's last) is read in 16-row pieces, so that
+        // rows past its keys are not fetched from memory
+        const bool fine = n < kT && box_rows > 16;
+        const int prow = fine ? 16 : box_rows;
+        const int npieces = (n + prow - 1) / prow;
         int32_t blk = 0;
         bool valid = false;
         if (lane < npieces) {
-          blk = bt_row[(tok0 + lane * box_rows) / bs];
+          blk = bt_row[(tok0 + lane * prow) / bs];
           valid = blk >= 0 && (int64_t)blk < p.num_blocks;
           if (!valid) raise_status(p.status, kStatusBadBlockIndex);
         }
         const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-        const uint32_t bytes = 2u * piece_bytes * __popc(vmask);
+        const uint32_t bytes = 2u * (uint32_t)prow * C::kRowBytes * __popc(vmask);
         if (!mbar_wait(&sm.kv_empty[st], ph ^ 1u, p.status)) { ok = false; break; }
         if (lane == 0) {
           TileMeta& m = sm.meta[st];
@@ -193,11 +199,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         __syncwarp();
         if (valid) {
-          const KvCoord kc = kv_coord(p, blk, tok0 + lane * box_rows, hkv);
+          const KvCoord kc = kv_coord(p, blk, tok0 + lane * prow, hkv);
+          const CUtensorMap* mk = fine ? &tmK16 : &tmK;
+          const CUtensorMap* mv = fine ? &tmV16 : &tmV;
           for (int bx = 0; bx < C::kNumBoxes; ++bx) {
-            const uint32_t off = bx * (kT * 128) + lane * box_rows * 128;
-            tma_load_2d(sm.kv[st][0] + off, &tmK, kc.x0 + bx * 64, kc.row, &sm.kv_full[st]);
-            tma_load_2d(sm.kv[st][1] + off, &tmV, kc.x0 + bx * 64, kc.row, &sm.kv_full[st]);
+            const uint32_t off = bx * (kT * 128) + lane * prow * 128;
+            tma_load_2d(sm.kv[st][0] + off, mk, kc.x0 + bx * 64, kc.row, &sm.kv_full[st]);
+            tma_load_2d(sm.kv[st][1] + off, mv, kc.x0 + bx * 64, kc.row, &sm.kv_full[st]);
           }
         }
         if (tok0 == t0 && !p.fused_plan) queue.prefetch(p, lane);
@@ -301,7 +309,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 #pragma unroll
     for (int g = 0; g < GH; ++g) {
       m_run[g] = -INFINITY; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_fin[g] = -INFINITY; l_fin[g] = 0.f;
-      vpos[g] = (h0 + g) / G;
+      vpos[g] = kKeyMask ? (h0 + g) / G : 0;
     }
     int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
     bool prev_first = false, prev_last = false;
@@ -351,9 +359,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
               const int hg = h0 + g;
               if (hg < GV) {
                 const float a = C::kStacked ? acc[g] + sm.accx[r][hg] : acc[g];
-                const int64_t row = q_row(p, prev_b, prev_hkv, hg);
+                // several query positions run only on the key-mask instantiation
+                const int64_t row = kKeyMask ? q_row(p, prev_b, prev_hkv, hg) : (int64_t)prev_b * p.Nq + prev_hkv * G + hg;
+                const int h = kKeyMask ? q_head(p, prev_hkv, hg) : prev_hkv * G + hg;
                 float M, W;
-                const float v = single_item_output(a, mm[g], lt[g], p.sink, q_head(p, prev_hkv, hg), &M, &W);
+                const float v = single_item_output(a, mm[g], lt[g], p.sink, h, &M, &W);
                 store_out<DT>(p.out, row * D + r, v);
                 if (r == hg) {
                   if (p.softmax_max) p.softmax_max[row] = (M == -INFINITY) ? -INFINITY : M * kLn2;
@@ -495,14 +505,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 
 template <int D, int DT, int GP>
 cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
-                      int box_rows, int grid, cudaStream_t stream) {
+                      const CUtensorMap* tail, int box_rows, int grid, cudaStream_t stream) {
   const size_t smem = sizeof(TcSmem<D>) + 1024;
   auto kern = (p.atten_mask || p.windowed || p.qs > 1) ? decode_tc_kernel<D, DT, GP, true>
                                                        : decode_tc_kernel<D, DT, GP, false>;
   cudaError_t e = ensure_smem(kern, (int)smem);
   if (e != cudaSuccess) return e;
   trace_mark(kKernelDecodeAttention, 0, stream);
-  e = launch_dependent(kern, grid, kThreadsTC, smem, stream, tmK, tmV, tmQ, p, box_rows);
+  e = launch_dependent(kern, grid, kThreadsTC, smem, stream, tmK, tmV, tmQ, tail[0], tail[1], p, box_rows);
   trace_mark(kKernelDecodeAttention, 1, stream);
   return e;
 }
@@ -511,20 +521,21 @@ cudaError_t launch_tc(const DecodeParams& p, const CUtensorMap& tmK, const CUten
 
 template <int D, int DT>
 cudaError_t launch_tc_g(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmQ,
-                        int box_rows, int grid, cudaStream_t stream) {
-  if (p.GV <= 2) return launch_tc<D, DT, 2>(p, tmK, tmV, tmQ, box_rows, grid, stream);
-  if (p.GV <= 4) return launch_tc<D, DT, 4>(p, tmK, tmV, tmQ, box_rows, grid, stream);
-  if (p.GV <= 8) return launch_tc<D, DT, 8>(p, tmK, tmV, tmQ, box_rows, grid, stream);
-  return launch_tc<D, DT, 16>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+                        const CUtensorMap* tail, int box_rows, int grid, cudaStream_t stream) {
+  if (p.GV <= 2) return launch_tc<D, DT, 2>(p, tmK, tmV, tmQ, tail, box_rows, grid, stream);
+  if (p.GV <= 4) return launch_tc<D, DT, 4>(p, tmK, tmV, tmQ, tail, box_rows, grid, stream);
+  if (p.GV <= 8) return launch_tc<D, DT, 8>(p, tmK, tmV, tmQ, tail, box_rows, grid, stream);
+  return launch_tc<D, DT, 16>(p, tmK, tmV, tmQ, tail, box_rows, grid, stream);
 }
 
 cudaError_t launch_decode_tc_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                       const CUtensorMap& tmQ, int box_rows, int grid, cudaStream_t stream) {
+                                       const CUtensorMap& tmQ, const CUtensorMap* tail, int box_rows, int grid,
+                                       cudaStream_t stream) {
   if (p.kv_dtype == kBF16)
-    return p.D == 64 ? launch_tc_g<64, kBF16>(p, tmK, tmV, tmQ, box_rows, grid, stream)
-                     : launch_tc_g<128, kBF16>(p, tmK, tmV, tmQ, box_rows, grid, stream);
-  return p.D == 64 ? launch_tc_g<64, kF16>(p, tmK, tmV, tmQ, box_rows, grid, stream)
-                   : launch_tc_g<128, kF16>(p, tmK, tmV, tmQ, box_rows, grid, stream);
+    return p.D == 64 ? launch_tc_g<64, kBF16>(p, tmK, tmV, tmQ, tail, box_rows, grid, stream)
+                     : launch_tc_g<128, kBF16>(p, tmK, tmV, tmQ, tail, box_rows, grid, stream);
+  return p.D == 64 ? launch_tc_g<64, kF16>(p, tmK, tmV, tmQ, tail, box_rows, grid, stream)
+                   : launch_tc_g<128, kF16>(p, tmK, tmV, tmQ, tail, box_rows, grid, stream);
 }
 
 }  // namespace fia

@@ -134,10 +134,14 @@ DecodeWorkspace decode_workspace_carve(void* base, int B, int Nkv, int G, int D,
 // rows.  With tmQ (the query as a 2-D tensor (D, B * Nq), 16-row boxes) the
 // tensor-core attention kernel runs (16-bit KV, G <= 16, 128-token tiles);
 // without it the CUDA-core kernel (any KV type, G <= 8, 64-token tiles).
+// tail[0], tail[1]: the K and V pools again with 16-row boxes, used for tiles with fewer
+// than 128 keys (the same maps as tmK / tmV when box_rows is 16).
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                          const CUtensorMap* tmQ, int box_rows, int num_sms, cudaStream_t stream);
+                          const CUtensorMap* tmQ, const CUtensorMap* tail, int box_rows, int num_sms,
+                          cudaStream_t stream);
 cudaError_t launch_decode_tc_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                       const CUtensorMap& tmQ, int box_rows, int grid, cudaStream_t stream);
+                                       const CUtensorMap& tmQ, const CUtensorMap* tail, int box_rows, int grid,
+                                       cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
 constexpr int kDecodeTileTC = 128;  // tokens per tensor-core tile; work items are multiples of it
 constexpr int kFusedPlanMaxB = 256;  // batches the in-kernel schedule of the 16-bit kernel holds
@@ -146,7 +150,7 @@ constexpr int kFusedPlanMaxB = 256;  // batches the in-kernel schedule of the 16
 // tiles, G <= 8); other int8 shapes on the CUDA-core kernel.
 inline bool decode_uses_i8tc(int kv_dtype, int D) { return kv_dtype == kI8 && D == 128; }
 cudaError_t launch_decode_i8tc_attention(const DecodeParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                         int box_rows, int grid, cudaStream_t stream);
+                                         const CUtensorMap* tail, int box_rows, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // RingAttentionUpdate
