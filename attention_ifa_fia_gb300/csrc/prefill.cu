@@ -640,18 +640,36 @@ __global__ void __launch_bounds__(kPThreads, 1)
 // 2hp and 2hp + 1), and both heads share the kv head, so each K and V tile is loaded
 // once for two heads.  Tensor memory holds S and O of both heads (4 x 128 columns);
 // P of a head is written over the first 64 columns of its own S once they have been
-// read.  The MMA warp alternates between the heads:
+// read.  The products are issued in the strict order
 //
 //   QK_A(0) QK_B(0) | PV_A(0) QK_A(1) PV_B(0) QK_B(1) | PV_A(1) QK_A(2) ...
 //
-// so that the softmax of one head overlaps the products of the other.  The MMAs of one
-// thread execute in issue order, so QK_X(j+1) may overwrite P_X(j) as soon as PV_X(j)
-// is issued.  Warp roles (320 threads): warp 0 TMA, warp 1 MMA, warps 2-5 head A and
-// warps 6-9 head B: one query row per thread with the whole S row in registers, the
-// softmax of every tile and, after a unit's last tile, its epilogue (normalise O, write
-// out, max and sum), during which the other head keeps the tensor cores busy.
-constexpr int kP2Threads = 320;
-constexpr int kP2TmaWarp = 0, kP2MmaWarp = 1;
+// so that the softmax of one head overlaps the products of the other (the strict order
+// keeps the two heads half a period apart; issued independently they fall into step and
+// their softmaxes contend for the same units).  The MMAs of one thread execute in issue
+// order, so QK_X(j+1) may overwrite P_X(j) as soon as PV_X(j) is issued.  Each head has its
+// own issuing warp, and the two pass a baton: a head's block (PV_X(j), QK_X(j+1)) is issued
+// back to back, the baton passed, and only then committed (a commit holds the issuing
+// thread until the products before it are under way; with one issuer, the other head's P
+// would wait behind it).  PV_X(j) takes keys 0-63 as soon as the softmax has released that
+// half of P.  Warp roles (352 threads): warp 0 TMA, warps 1 and 10 MMA of heads A and B,
+// warps 2-5 head A and warps 6-9 head B: one query row per thread with the whole S row in
+// registers, the softmax of every tile and, after a unit's last tile, its epilogue
+// (normalise O, write out, max and sum), during which the other head keeps the tensor
+// cores busy.
+constexpr int kP2Threads = 352;
+constexpr int kP2TmaWarp = 0, kP2MmaWarpA = 1, kP2MmaWarpB = 10;
+
+// d = a * b + c for two lanes at once (one packed fp32 instruction, each lane rounded as fmaf).
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  uint64_t d;
+  asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %3};\n\tmov.b64 c, {%4, %4};\n\t"
+      "fma.rn.f32x2 %0, a, b, c;\n\t}"
+      : "=l"(d)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+  d0 = __uint_as_float((uint32_t)d);
+  d1 = __uint_as_float((uint32_t)(d >> 32));
+}
 
 // 64 consecutive 32-bit TMEM columns of this thread's lane, load and wait in one statement.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -675,6 +693,68 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 128 consecutive 32-bit TMEM columns of this thread's lane: two loads, one wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,"
+      "%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,"
+      "%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63"
+      "}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+      "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,"
+      "%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,"
+      "%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127"
+      "}, [%129];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]),
+        "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]),
+        "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+        "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]),
+        "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]),
+        "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]),
+        "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]),
+        "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]),
+        "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]),
+        "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
+        "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]),
+        "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]),
+        "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr), "r"(taddr + 64u)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// P = 2^(s mul - m) of keys [64 h, 64 h + 64) of one S row in 16-bit pairs, stored at
+// columns [32 h, 32 h + 32) from taddr; returns their sum of P.
+template <int DT, int h>
+__device__ __forceinline__ float p_pass(const float (&s)[kKT], float mul, float m, uint32_t taddr) {
+  float a[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
+  const float neg_m = -m;
+#pragma unroll
+  for (int c = 64 * h; c < 64 * h + 64; c += 32) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float t0, t1;
+      ffma2(t0, t1, s[c + i], s[c + i + 1], mul, neg_m);
+      const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+      const int k = (i >> 1) & 1;  // (a packed add here would pin register pairs and spill)
+      a[2 * k] += p0;
+      a[2 * k + 1] += p1;
+      pk[i >> 1] = (DT == kBF16) ? pack_bf16(p0, p1) : pack_f16(p0, p1);
+    }
+    tmem_st16u(taddr + (c >> 1), pk);
+  }
+  return (a[0] + a[1]) + (a[2] + a[3]);
+}
+
 template <int kD>
 struct P2Smem {
   static constexpr int kTileB = tile_bytes<kD>();
@@ -686,9 +766,10 @@ struct P2Smem {
   uint64_t q_full, q_empty;
   uint64_t k_full[kPStages], k_empty[kPStages];
   uint64_t v_full[kPStages], v_empty[kPStages];
-  uint64_t s_full[2], p_full[2], pv_done[2];  // per head, one phase per key tile
+  uint64_t s_full[2], p_lo[2], p_full[2], pv_done[2];  // per head, one phase per key tile
   uint64_t o_ready[2], o_free[2];             // per head, one phase per unit
-  int stop;                                   // set by the MMA warp after the last tile
+  uint64_t turn[2];                           // the issue baton: head x's MMA warp may issue its next block
+  int stop[2];                                // set by head x's MMA warp after the last tile
   uint32_t tmem_base;
 };
 static_assert(sizeof(P2Smem<128>) <= 232448, "prefill shared memory exceeds the per-CTA limit");
@@ -708,24 +789,26 @@ __global__ void __launch_bounds__(kP2Threads, 1)
   }
   if (tid == 0) {
     mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.q_empty, 2);  // q_empty, k_empty, v_empty: one commit per head's MMA warp
     for (int st = 0; st < kPStages; ++st) {
       mbar_init(&sm.k_full[st], 1);
-      mbar_init(&sm.k_empty[st], 1);
+      mbar_init(&sm.k_empty[st], 2);
       mbar_init(&sm.v_full[st], 1);
-      mbar_init(&sm.v_empty[st], 1);
+      mbar_init(&sm.v_empty[st], 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sm.s_full[x], 1);
+      mbar_init(&sm.p_lo[x], 4);
       mbar_init(&sm.p_full[x], 4);
       mbar_init(&sm.pv_done[x], 1);
       mbar_init(&sm.o_ready[x], 1);
       mbar_init(&sm.o_free[x], 4);
+      mbar_init(&sm.turn[x], 1);
+      sm.stop[x] = 0;
     }
-    sm.stop = 0;
     fence_mbar_init();
   }
-  if (warp == kP2MmaWarp) tmem_alloc(&sm.tmem_base, 512);
+  if (warp == kP2MmaWarpA) tmem_alloc(&sm.tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -805,83 +888,129 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         }
       }
     }
-  } else if (warp == kP2MmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer (whole warp)
-    {
-      constexpr uint32_t idesc_qk = umma_idesc_f16(DT == kBF16, 0, 0, kQT, kKT);
-      constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 0, 1, kQT, kD);
-      const uint64_t qdesc[2] = {umma_desc(smem_u32(sm.q[0]), 16, 1024), umma_desc(smem_u32(sm.q[1]), 16, 1024)};
-      int o_units0 = 0, o_units1 = 0;  // units whose first PV into O_A / O_B has been issued
-      int u_local = 0;
-      auto qk = [&](int x, int jj) {
-        const uint64_t b0 = umma_desc(smem_u32(sm.k[jj % kPStages]), 16, 1024);
+  } else if (warp == kP2MmaWarpA || warp == kP2MmaWarpB) {
+    // ------------------------------------------------------------------ MMA issuer of head x (whole warp)
+    const int x = warp == kP2MmaWarpA ? 0 : 1;
+    constexpr uint32_t idesc_qk = umma_idesc_f16(DT == kBF16, 0, 0, kQT, kKT);
+    constexpr uint32_t idesc_pv = umma_idesc_f16(DT == kBF16, 0, 1, kQT, kD);
+    const uint64_t qdesc = umma_desc(smem_u32(sm.q[x]), 16, 1024);
+    const uint32_t col_s = tmem + kColS[x], col_o = tmem + kColO[x];
+    int o_units = 0;  // units whose first PV into O_x has been issued
+    int u_local = 0;
+    // S_x = Q_x K(jj)^T (8 MMAs, no commit)
+    auto qk = [&](int jj) {
+      const uint64_t b0 = umma_desc(smem_u32(sm.k[jj % kPStages]), 16, 1024);
 #pragma unroll
-        for (int s = 0; s < kD / 16; ++s) {
-          const uint32_t off = (uint32_t)(((s >> 2) * (kQT * 128) + (s & 3) * 32) >> 4);
-          umma_f16_w(tmem + kColS[x], qdesc[x] + off, b0 + off, idesc_qk, s > 0);
-        }
-        umma_commit_w(&sm.s_full[x]);
-      };
-      // flags of a tile: bit 0 first, bit 1 last; vrows: rows of its V tile to keep (head A
-      // zeroes the rest, once, before its product)
-      auto pv = [&](int x, int jj, int flags, int vrows) -> bool {
-        if (!mbar_wait_warp(&sm.p_full[x], (uint32_t)jj & 1u, p.status)) return false;
-        if (!mbar_wait_warp(&sm.v_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return false;
-        int& ou = x ? o_units1 : o_units0;
-        if ((flags & 1) && ou > 0 && !mbar_wait_warp(&sm.o_free[x], (uint32_t)(ou - 1) & 1u, p.status)) return false;
-        if (x == 0 && vrows < kKT) zero_v_rows<kD>(sm.v[jj % kPStages], vrows, lane);
+      for (int s = 0; s < kD / 16; ++s) {
+        const uint32_t off = (uint32_t)(((s >> 2) * (kQT * 128) + (s & 3) * 32) >> 4);
+        umma_f16_w(col_s, qdesc + off, b0 + off, idesc_qk, s > 0);
+      }
+    };
+    // O_x (+)= P_x(jj) V(jj) (8 MMAs, no commit): keys 0-63 once the softmax has released
+    // that half of P, keys 64-127 once it has released all of it.  flags of a tile: bit 0
+    // first, bit 1 last; vrows: rows of its V tile to keep (head A zeroes the rest, once,
+    // before its product; head B issues after head A's block)
+    auto pv = [&](int jj, int flags, int vrows) -> bool {
+      if ((flags & 1) && o_units > 0 && !mbar_wait_warp(&sm.o_free[x], (uint32_t)(o_units - 1) & 1u, p.status))
+        return false;
+      if (x == 0 && vrows < kKT) zero_v_rows<kD>(sm.v[jj % kPStages], vrows, lane);
+      const uint64_t b0 = umma_desc(smem_u32(sm.v[jj % kPStages]), kKT * 128, 1024);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        if (!mbar_wait_warp(hf ? &sm.p_full[x] : &sm.p_lo[x], (uint32_t)jj & 1u, p.status)) return false;
         tc_fence_after();
-        const uint64_t b0 = umma_desc(smem_u32(sm.v[jj % kPStages]), kKT * 128, 1024);
 #pragma unroll
-        for (int s = 0; s < kKT / 16; ++s)
-          umma_f16_ta_w(tmem + kColO[x], tmem + kColS[x] + s * 8, b0 + (uint64_t)((s * 16 * 128) >> 4), idesc_pv,
+        for (int s = 4 * hf; s < 4 * hf + 4; ++s)
+          umma_f16_ta_w(col_o, col_s + s * 8, b0 + (uint64_t)((s * 16 * 128) >> 4), idesc_pv,
                         ((flags & 1) && s == 0) ? 0u : 1u);
-        umma_commit_w(&sm.pv_done[x]);
-        if (flags & 2) umma_commit_w(&sm.o_ready[x]);
-        if (x == 1) umma_commit_w(&sm.v_empty[jj % kPStages]);
-        if (flags & 1) ++ou;
-        return true;
-      };
-      // waits for K of tile jj; returns its flags, -1 at the sentinel, -2 on error; *vrows
-      // receives the rows of its V tile to keep
-      auto load_tile = [&](int jj, int* vrows) -> int {
-        if (!mbar_wait_warp(&sm.k_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return -2;
-        const PTileMeta& m = sm.meta[jj % kMetaRing];
-        if (m.unit < 0) return -1;
-        const int flags = (m.first ? 1 : 0) | (m.last ? 2 : 0);
-        *vrows = m.vrows;
-        if ((flags & 1) && !mbar_wait_warp(&sm.q_full, (uint32_t)u_local & 1u, p.status)) return -2;
-        tc_fence_after();
-        return flags;
-      };
-      int vr_cur = kKT, vr_nxt = kKT;
-      int cur = load_tile(0, &vr_cur);
-      if (cur >= 0) {
-        qk(0, 0);
-        qk(1, 0);
-        umma_commit_w(&sm.k_empty[0]);
-        if (cur & 2) { umma_commit_w(&sm.q_empty); ++u_local; }
       }
-      for (int j = 0; cur >= 0; ++j) {
-        if (!pv(0, j, cur, vr_cur)) break;
-        const int nxt = load_tile(j + 1, &vr_nxt);
+      if (flags & 1) ++o_units;
+      return true;
+    };
+    // waits for K of tile jj; returns its flags, -1 at the sentinel, -2 on error; *vrows
+    // receives the rows of its V tile to keep
+    auto load_tile = [&](int jj, int* vrows) -> int {
+      if (!mbar_wait_warp(&sm.k_full[jj % kPStages], (uint32_t)(jj / kPStages) & 1u, p.status)) return -2;
+      const PTileMeta& m = sm.meta[jj % kMetaRing];
+      if (m.unit < 0) return -1;
+      *vrows = m.vrows;
+      return (m.first ? 1 : 0) | (m.last ? 2 : 0);
+    };
+    // the unit's Q before the QK products of its first tile
+    auto wait_q = [&](int flags) -> bool {
+      if ((flags & 1) && !mbar_wait_warp(&sm.q_full, (uint32_t)u_local & 1u, p.status)) return false;
+      tc_fence_after();
+      return true;
+    };
+    // the baton: head A's block b follows head B's block b - 1, head B's block b follows
+    // head A's block b
+    int block = 0;
+    auto take_turn = [&]() -> bool {
+      if (x == 0 && block == 0) return true;
+      return mbar_wait_warp(&sm.turn[x], (uint32_t)(x == 0 ? block - 1 : block) & 1u, p.status);
+    };
+    auto pass_turn = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.turn[x ^ 1]);
+      ++block;
+    };
+    int vr_cur = kKT, vr_nxt = kKT;
+    int cur = load_tile(0, &vr_cur);
+    if (cur >= 0 && !wait_q(cur)) cur = -2;
+    if (cur >= 0 && take_turn()) {  // block 0: QK_x(0)
+      qk(0);
+      pass_turn();
+      umma_commit_w(&sm.s_full[x]);
+      umma_commit_w(&sm.k_empty[0]);
+      if (cur & 2) {
+        umma_commit_w(&sm.q_empty);
+        ++u_local;
+      }
+    } else {
+      cur = -2;
+    }
+    // Block j + 1: PV_x(j), then QK_x(j + 1), then (after the baton) the commits: S_x(j + 1)
+    // is complete when s_full fires; pv_done fires once PV_x(j) (and QK_x(j + 1)) are, which
+    // the rescale of O in the softmax of tile j + 1 needs and has by then.
+    for (int j = 0; cur >= 0; ++j) {
+      const int vs = j % kPStages;
+      if (!mbar_wait_warp(&sm.v_full[vs], (uint32_t)(j / kPStages) & 1u, p.status)) break;
+      // within a unit, the next K tile (loaded long before) is checked before PV_x(j), so that
+      // QK_x(j + 1) follows PV_x(j) without a gap; the next unit's first K tile is requested
+      // only as this unit's last QK completes and is waited for after PV_x(j)
+      int nxt = -3;
+      if (!(cur & 2)) {
+        nxt = load_tile(j + 1, &vr_nxt);
         if (nxt == -2) break;
-        if (nxt >= 0) qk(0, j + 1);
-        if (!pv(1, j, cur, vr_cur)) break;
-        if (nxt >= 0) {
-          qk(1, j + 1);
-          umma_commit_w(&sm.k_empty[(j + 1) % kPStages]);
-          if (nxt & 2) { umma_commit_w(&sm.q_empty); ++u_local; }
+      }
+      if (!take_turn()) break;
+      if (!pv(j, cur, vr_cur)) break;
+      if (cur & 2) umma_commit_w(&sm.o_ready[x]);  // the epilogue need not wait for QK_x(j + 1)
+      if (nxt == -3) {
+        nxt = load_tile(j + 1, &vr_nxt);
+        if (nxt == -2) break;
+      }
+      if (nxt >= 0 && !wait_q(nxt)) break;
+      if (nxt >= 0) qk(j + 1);
+      pass_turn();
+      if (nxt >= 0) umma_commit_w(&sm.s_full[x]);
+      umma_commit_w(&sm.pv_done[x]);
+      umma_commit_w(&sm.v_empty[vs]);
+      if (nxt >= 0) {
+        umma_commit_w(&sm.k_empty[(j + 1) % kPStages]);
+        if (nxt & 2) {
+          umma_commit_w(&sm.q_empty);
+          ++u_local;
         }
-        cur = nxt;
-        vr_cur = vr_nxt;
       }
-      // No more tiles.  The softmax warps have consumed every S phase (PV of the last tile
-      // waited for their P), so a plain arrival completes the next one and they see the flag.
-      if (lane == 0) {
-        sm.stop = 1;
-        for (int x = 0; x < 2; ++x) mbar_arrive(&sm.s_full[x]);
-      }
+      cur = nxt;
+      vr_cur = vr_nxt;
+    }
+    // No more tiles.  The softmax warps of head x have consumed every S phase (PV of the last
+    // tile waited for their P), so a plain arrival completes the next one and they see the flag.
+    if (lane == 0) {
+      sm.stop[x] = 1;
+      mbar_arrive(&sm.s_full[x]);
     }
   } else {
     // ------------------------------------------------------------------ softmax and epilogue of head x
@@ -893,93 +1022,107 @@ __global__ void __launch_bounds__(kP2Threads, 1)
     int units = 0;  // units finished by this warp group
     for (int j = 0;; ++j) {
       if (!mbar_wait(&sm.s_full[x], (uint32_t)j & 1u, p.status)) break;
-      if (sm.stop) break;
-      const PTileMeta meta = sm.meta[j % kMetaRing];
+      if (sm.stop[x]) break;
+      // this tile's descriptor: its slot is rewritten only after QK(j + 2), which waits for
+      // this warp group's P(j + 1), so fields are read where they are needed (fewer live
+      // registers across the softmax)
+      const PTileMeta& meta = sm.meta[j % kMetaRing];
       tc_fence_after();
-      if (meta.first) {
+      const bool first = meta.first;
+      if (first) {
         m_run = -INFINITY;
         m_true = -INFINITY;
         l_run = 0.f;
       }
-      const int qi = meta.q0 + r;
-      const bool row_ok = qi < meta.Lq;
-      const int k0 = meta.kvt * kKT;
-      const int dq = qi + (meta.Lkv - meta.Lq);
-      const int k_hi = min(meta.Lkv, dq + p.next + 1);
-      const int nvis = row_ok ? max(0, min(k_hi - k0, kKT)) : 0;  // visible: [k0 + nlo, k0 + nvis)
-      const int nlo = kBand ? min(max(dq - p.pre - k0, 0), kKT) : 0;
-      // the S row in registers, in log2 units, keys past the visible range at -inf.  When
-      // every row of the warp sees all 128 keys and the scale is positive, the row max is
-      // taken on the raw scores (three-input max) and the scale applied once.
+      int nvis, nlo;  // visible keys of the row in this tile: [k0 + nlo, k0 + nvis)
+      bool all_keys;  // the row sees every key of the tile, or is past the sequence's queries
+      {
+        const int qi = meta.q0 + r, Lq = meta.Lq, Lkv = meta.Lkv;
+        const int k0 = meta.kvt * kKT;
+        const int dq = qi + (Lkv - Lq);
+        const int k_hi = min(Lkv, dq + p.next + 1);
+        nvis = qi < Lq ? max(0, min(k_hi - k0, kKT)) : 0;
+        nlo = kBand ? min(max(dq - p.pre - k0, 0), kKT) : 0;
+        all_keys = qi >= Lq || (nvis == kKT && nlo == 0);
+      }
+      // the S row in registers (raw scores)
       float s[kKT];
-      tmem_ld64(tl + kColS[x], *reinterpret_cast<float(*)[64]>(&s[0]));
-      tmem_ld64(tl + kColS[x] + 64, *reinterpret_cast<float(*)[64]>(&s[64]));
+      tmem_ld128(tl + kColS[x], s);
       const float sc = p.scale_log2;
-      const bool full = __all_sync(0xffffffffu, nvis == kKT && nlo == 0) && sc > 0.f;
-      float mt = -INFINITY;
-      if (full) {  // four independent chains
-        float e[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-        for (int i = 4; i < kKT; i += 8)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) e[k] = fmax3(e[k], s[i + 2 * k], s[i + 2 * k + 1]);
-        mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]) * sc;
-      } else if (kBand && __any_sync(0xffffffffu, nlo > 0)) {  // a band's lower edge crosses the tile
-        float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int i = 0; i < kKT; i += 8)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int i0 = i + 2 * k, i1 = i0 + 1;
-            s[i0] = (i0 >= nlo && i0 < nvis) ? s[i0] * sc : -INFINITY;
-            s[i1] = (i1 >= nlo && i1 < nvis) ? s[i1] * sc : -INFINITY;
-            e[k] = fmax3(e[k], s[i0], s[i1]);
-          }
-        mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]);
-      } else {  // scaled scores, keys past the visible range at -inf; four independent chains
-        float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int i = 0; i < kKT; i += 8)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int i0 = i + 2 * k, i1 = i0 + 1;
-            s[i0] = (i0 < nvis) ? s[i0] * sc : -INFINITY;
-            s[i1] = (i1 < nvis) ? s[i1] * sc : -INFINITY;
-            e[k] = fmax3(e[k], s[i0], s[i1]);
-          }
-        mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]);
-      }
-      const float m_old = m_run;
-      m_true = fmaxf(m_true, mt);
-      bool rescale = false;
+      // every row of the warp sees all 128 keys (rows past the sequence's queries are never
+      // written out: any finite values do) and the scale is positive: the row max may be
+      // taken on the raw scores and the scale applied once
+      const bool full = __all_sync(0xffffffffu, all_keys) && sc > 0.f;
+      const uint32_t col_p = tl + kColS[x];  // P (16-bit pairs) over the first 64 columns of S
       float alpha = 1.f;
-      if (mt > m_run + (float)kRescaleThreshold || (m_run == -INFINITY && mt != -INFINITY)) {
-        m_run = mt;
-        if (m_old != -INFINITY) {
-          rescale = true;
-          alpha = fast_exp2(m_old - m_run);
+      bool rescale = false;
+      float lsum;
+      {
+        // the tile max; scores scaled in place unless full, keys outside the visible range at
+        // -inf; four independent chains
+        float mt = -INFINITY;
+        if (full) {
+          float e[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+          for (int i = 4; i < kKT; i += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) e[k] = fmax3(e[k], s[i + 2 * k], s[i + 2 * k + 1]);
+          mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]) * sc;
+        } else if (kBand && __any_sync(0xffffffffu, nlo > 0)) {  // a band's lower edge crosses the tile
+          float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int i = 0; i < kKT; i += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int i0 = i + 2 * k, i1 = i0 + 1;
+              s[i0] = (i0 >= nlo && i0 < nvis) ? s[i0] * sc : -INFINITY;
+              s[i1] = (i1 >= nlo && i1 < nvis) ? s[i1] * sc : -INFINITY;
+              e[k] = fmax3(e[k], s[i0], s[i1]);
+            }
+          mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]);
+        } else {
+          float e[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int i = 0; i < kKT; i += 8)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int i0 = i + 2 * k, i1 = i0 + 1;
+              s[i0] = (i0 < nvis) ? s[i0] * sc : -INFINITY;
+              s[i1] = (i1 < nvis) ? s[i1] * sc : -INFINITY;
+              e[k] = fmax3(e[k], s[i0], s[i1]);
+            }
+          mt = fmax3(fmaxf(e[0], e[1]), e[2], e[3]);
+        }
+        const float m_old = m_run;
+        m_true = fmaxf(m_true, mt);
+        if (mt > m_run + (float)kRescaleThreshold || (m_run == -INFINITY && mt != -INFINITY)) {
+          m_run = mt;
+          if (m_old != -INFINITY) {
+            rescale = true;
+            alpha = fast_exp2(m_old - m_run);
+          }
         }
       }
-      // P = 2^(s - m) in 16-bit pairs, written over the first 64 columns of S
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      const float mul = full ? sc : 1.f;  // raw scores on the fast path, scaled ones otherwise
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
-#pragma unroll
-      for (int c = 0; c < kKT; c += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float e0 = fast_exp2(fmaf(s[c + i], mul, -m_use)), e1 = fast_exp2(fmaf(s[c + i + 1], mul, -m_use));
-          ls[(i >> 1) & 3] += e0 + e1;
-          pk[i >> 1] = (DT == kBF16) ? pack_bf16(e0, e1) : pack_f16(e0, e1);
+      // P = 2^(s - m) in 16-bit pairs (raw scores times the scale when full), released in
+      // two halves: the PV product of keys 0-63 starts while keys 64-127 are exponentiated.
+      // A tile that rescales O (rare) releases both halves after the rescale, which needs
+      // PV(j - 1) complete (pv_done fires with QK(j), before S(j)) and PV(j) not begun.
+      const bool rescale_o = __any_sync(0xffffffffu, rescale && !first);
+      {
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        const float mul = full ? sc : 1.f;
+        lsum = p_pass<DT, 0>(s, mul, m_use, col_p);
+        if (!rescale_o) {
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.p_lo[x]);
         }
-        tmem_st16u(tl + kColS[x] + (c >> 1), pk);
+        lsum += p_pass<DT, 1>(s, mul, m_use, col_p);
       }
-      const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // O rescale (rare): PV(j - 1) complete, PV(j) not begun (it waits for this warp's P)
-      if (__any_sync(0xffffffffu, rescale && !meta.first)) {
+      if (rescale_o) {
         if (!mbar_wait(&sm.pv_done[x], (uint32_t)(j - 1) & 1u, p.status)) break;
-        const float f = (rescale && !meta.first) ? alpha : 1.f;
+        const float f = (rescale && !first) ? alpha : 1.f;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < kD; c += 32) {
@@ -989,6 +1132,10 @@ __global__ void __launch_bounds__(kP2Threads, 1)
           for (int i = 0; i < 32; ++i) o[i] *= f;
           tmem_st32(tl + kColO[x] + c, o);
         }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_lo[x]);
       }
       l_run = fmaf(l_run, alpha, lsum);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -1005,6 +1152,8 @@ __global__ void __launch_bounds__(kP2Threads, 1)
         float denom = l_run;
         if (p.sink && m_run != -INFINITY) denom += fast_exp2(sink2 - m_run);
         const float inv = denom > 0.f ? 1.f / denom : 0.f;
+        const int qi = meta.q0 + r;
+        const bool row_ok = qi < meta.Lq;
         const int64_t tok = (int64_t)meta.tq + qi;
         // out, 64 channels at a time: normalise and pack the warp's 32 rows into its staging
         // slot (16-byte chunk c of row l at position c ^ (l & 7): no bank conflicts either
@@ -1060,7 +1209,7 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kP2MmaWarp) {
+  if (warp == kP2MmaWarpA) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
