@@ -140,15 +140,19 @@ struct DecodePlan {
 // Work items are (b, kv head, chunk) triples of `chunk_tokens` tokens.  With
 // num_splits = n > 0 each sequence splits into at most n chunks; with 0 the
 // chunk is sized so that the upper bound of the work (every sequence at
-// max_kv_len) gives about 12 items per SM, between one tile and 8192 tokens.
-int plan_decode(int B, int Nkv, int max_kv_len, int num_splits, int num_sms, DecodePlan* plan) {
+// max_kv_len) gives about `items_per_sm` items per SM, between one tile and 8192
+// tokens.  Fewer items per SM mean fewer, larger chunks (a smaller workspace).
+constexpr int kItemsPerSm = 12;      // 16-bit caches
+constexpr int kItemsPerSmInt8 = 6;   // int8 caches: an item boundary costs the int8 kernel more
+int plan_decode(int B, int Nkv, int max_kv_len, int num_splits, int num_sms, DecodePlan* plan,
+                int items_per_sm = kItemsPerSm) {
   const int64_t T = fia::kDecodeTileTC;  // items are whole tiles of either attention kernel
   int64_t c;
   if (num_splits > 0) {
     c = ((int64_t)max_kv_len + num_splits - 1) / num_splits;
   } else {
     const int64_t upper = (int64_t)B * Nkv * max_kv_len;
-    c = upper / (12LL * std::max(num_sms, 1));
+    c = upper / ((int64_t)items_per_sm * std::max(num_sms, 1));
     c = std::min<int64_t>(std::max<int64_t>(c, T), 8192);
   }
   c = (c + T - 1) / T * T;
@@ -398,7 +402,9 @@ static int decode_impl(const void* q, fia_dtype q_dtype, const void* k_cache, co
   DeviceInfo* d;
   if (int rc = device_info(&d)) return rc;
   DecodePlan plan;
-  if (int rc = plan_decode(B, Nkv, max_kv_len, num_splits, d->num_sms, &plan)) return rc;
+  if (int rc = plan_decode(B, Nkv, max_kv_len, num_splits, d->num_sms, &plan,
+                           kv_dtype == FIA_I8 ? kItemsPerSmInt8 : kItemsPerSm))
+    return rc;
   const int G = Nq / Nkv;
   const size_t need = fia::decode_workspace_bytes(B, Nkv, G * qs, D, plan.max_items);
   if (check_only) return ok();

@@ -19,18 +19,20 @@
 // Warp roles (608 threads):
 //   warp 0      TMA producer: the item's q' block (one bulk copy from the workspace),
 //               int8 K and V tiles (128 rows x 128 bytes, 128-byte swizzle) into a
-//               4-stage ring.
+//               6-stage ring; a slot is released by the commit of its tile's PV.
 //   warp 1      TMEM allocation; one thread issues the score MMAs.
 //   warp 14     one thread issues the PV MMAs (a second issue stream on another SM
 //               sub-partition: an MMA blocks its issuing thread for about 50 cycles).
-//   warps 2-5   online softmax of tile j (one token per TMEM lane) and the
-//   and 15-18   rescale-and-accumulate of the PV result of tile j-1 (one channel
-//               per lane), final output or split partial; each group takes half of
-//               the heads.
+//   warps 2-5   online softmax of tile j (one token per TMEM lane); the PV products
+//   and 15-18   of an item accumulate in TMEM (items alternate between two O buffers),
+//               rescaled there in the rare tile that raises a head's reference; at the
+//               item's end the final output or split partial (one channel per lane);
+//               each group takes half of the heads.
 //   warps 6-9   K codes -> fp16 pairs in TMEM (one token row per lane): the A
 //               operand of the score MMA, double buffered.
-//   warps 10-13 V codes -> fp16 in shared memory, in the MN-major layout of the A
-//               operand of the PV MMA, double buffered.
+//   warps 10-13 V codes -> fp16 in the tile's own ring slot (over the K codes already
+//               read and the V codes as they are read), in the MN-major layout of the
+//               A operand of the PV MMA.
 // Each code takes one integer and one half-precision operation: the byte (plus
 // 128) is placed under the exponent of 1024 and 1152 is subtracted.
 #include <algorithm>
@@ -44,7 +46,7 @@ namespace {
 constexpr int kT = 128;     // tokens per tile: the M of the score MMA
 constexpr int kNP = 16;     // query heads per group, padded: the N of both MMAs
 constexpr int kD = 128;     // head dim (the M of the PV MMA)
-constexpr int kStages = 4;  // int8 ring
+constexpr int kStages = 6;  // int8 ring (a slot also holds its tile's fp16 V until PV)
 constexpr int kThreads = 608;
 constexpr int kPvWarp = 14;     // issues the PV MMAs (warp 1 the score MMAs)
 constexpr int kSm2Warp0 = 15;   // warps 15-18: the second softmax warp group
@@ -62,7 +64,6 @@ constexpr uint32_t kColO = 64;   // O: 2 buffers x 16 columns
 constexpr uint32_t kColK = 128;  // K codes: 2 buffers x 64 columns
 constexpr uint32_t kTmemCols = 256;
 constexpr int kI8Tile = kT * kD;      // bytes of one int8 K or V tile
-constexpr int kVTile = kT * kD * 2;   // fp16 V codes of one tile
 constexpr int kPBytes = kNP * kT * 2;
 
 struct __align__(16) I8Meta {
@@ -73,21 +74,26 @@ struct __align__(16) I8Meta {
 };
 
 constexpr int kMetaRing = 4;  // tile descriptors in flight between the K converters, MMA and softmax warps
+constexpr int kQBufs = 2;     // q' blocks (the producer may run one item ahead of the one in the softmax)
 
 struct I8Smem {
+  // int8 K and V codes of a tile; after the K converters have read the K half, the V
+  // converters write the tile's fp16 V over both halves (the PV MMA's A operand)
   alignas(1024) uint8_t kv[kStages][2][kI8Tile];
-  alignas(1024) uint8_t v16[2][kVTile];
-  alignas(1024) uint8_t q[2][kI8QBytes];
+  alignas(1024) uint8_t q[kQBufs][kI8QBytes];
   alignas(1024) uint8_t p[2][kPBytes];
-  alignas(16) float2 kn[2][kNP];
+  alignas(16) float2 kn[kQBufs][kNP];
   alignas(16) float red[2][kNP][4];  // [S buffer][head][warp]: per-warp maxima
   float lsum[4][kNP];
   float lmax[4][kNP];  // [warp][head]: per-warp true maxima at an item's end
   I8Meta meta[kStages];    // per int8 stage (producer)
   I8Meta tmeta[kMetaRing];  // per tile j at j % kMetaRing (K converters)
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t k_full[2], v_full[2], q_full[2], q_empty[2];
+  uint64_t kconv[kStages];  // K converters -> V converters: the slot's K codes have been read
+  uint64_t k_full[2], q_full[kQBufs], q_empty[kQBufs];
+  uint64_t v_full[kStages];  // per ring slot: the V converters may run ahead of PV by several tiles
   uint64_t s_full[2], p_full[2], pv_done[2];
+  int pflag[2];  // per P buffer: bit 0 the tile starts its item, bit 1 the item's O buffer
   int pv_stop;  // index of the sentinel tile, set by the softmax warps when they reach it
   uint32_t tmem_base;
 };
@@ -110,6 +116,27 @@ __device__ __forceinline__ void tmem_st32w(uint32_t taddr, const uint32_t (&v)[3
       "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
+}
+
+// N consecutive 32-bit TMEM columns of this thread's lane (32x32b shape, N = 1, 2 or 4).
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_st_n<1>(uint32_t taddr, const float (&v)[1]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(__float_as_uint(v[0])) : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_n<2>(uint32_t taddr, const float (&v)[2]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(__float_as_uint(v[0])),
+               "r"(__float_as_uint(v[1]))
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st_n<4>(uint32_t taddr, const float (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3]))
+               : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T (A: rows on lanes, 16-bit pairs per column).
@@ -154,26 +181,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Synchronisation.  Buffers indexed by tile j use slot j & 1 (j % kStages for the
   // int8 ring); a slot is reused two tiles later, and most "free" signals follow
   // from program order:
+  //   kv_full  TMA -> converters: codes of tile j in ring slot j % kStages
+  //   kconv    K converters -> V converters: the slot's K codes have been read
   //   k_full   K converters -> MMA: codes of tile j in TMEM, descriptor in tmeta
   //   s_full   MMA commit of QK(j) -> softmax (scores ready) and K converters of
   //            tile j + 2 (the K buffer may be overwritten)
   //   p_full   softmax -> MMA: P(j) written.  Each softmax warp arrives after reading
-  //            S(j) and, earlier in its program, O(j - 2): the MMA warp may then also
-  //            overwrite the S and O buffers of those tiles
-  //   v_full   V converters -> MMA: fp16 V codes of tile j
-  //   pv_done  MMA commit of PV(j) -> softmax (O ready; P buffer free) and V
-  //            converters of tile j + 2 (the V buffer may be overwritten)
+  //            S(j) (and, when it rescaled it, O): the MMA warp may then overwrite
+  //            the S buffer and accumulate into O
+  //   v_full   V converters -> MMA: fp16 V of tile j in its ring slot (one barrier per
+  //            slot: nothing else keeps the converters within a phase of the PV warp)
+  //   pv_done  MMA commit of PV(j) -> softmax (O ready; P buffer free)
+  //   kv_empty MMA commit of PV(j) -> TMA: ring slot j % kStages free
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 8);  // the four K and four V converter warps
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.k_full[i], 4);
-      mbar_init(&sm.v_full[i], 4);
+    for (int i = 0; i < kQBufs; ++i) {
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 9);  // MMA commit after the item's last QK + the 8 softmax warps
                                      // after reading the item's constants at its last tile
+    }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);  // the commit of the tile's PV product
+      mbar_init(&sm.kconv[s], 4);     // the four K converter warps
+      mbar_init(&sm.v_full[s], 4);    // the four V converter warps
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.k_full[i], 4);
+
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.p_full[i], 8);
       mbar_init(&sm.pv_done[i], 1);
@@ -209,9 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const DecodeItem it = decode_item(desc);
       const int b = it.b, hkv = it.hkv, t_begin = it.t_begin, t_end = it.t_end;
       const int t0 = t_begin & ~(kT - 1);  // the first tile (t_begin is aligned but for a window)
-      const int qb = local_item & 1;
+      const int qb = local_item % kQBufs;
       const int qlim = p.qs > 1 ? clamp_len(p, b, false) - p.qs : (1 << 30);  // position 0's last key
-      if (!mbar_wait(&sm.q_empty[qb], ((local_item >> 1) & 1) ^ 1u, p.status)) { ok = false; break; }
+      if (!mbar_wait(&sm.q_empty[qb], ((uint32_t)(local_item / kQBufs) & 1u) ^ 1u, p.status)) { ok = false; break; }
       if (lane == 0) {
         const uint8_t* src = p.ws.qprep + ((int64_t)b * p.Nkv + hkv) * kI8QBlockBytes;
         mbar_arrive_expect_tx(&sm.q_full[qb], kI8QBlockBytes);
@@ -281,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const int qb = meta.qbuf;
-        if (meta.first && !mbar_wait(&sm.q_full[qb], (uint32_t)(local_item >> 1) & 1u, p.status)) break;
+        if (meta.first && !mbar_wait(&sm.q_full[qb], (uint32_t)(local_item / kQBufs) & 1u, p.status)) break;
         tc_fence_after();
         const uint32_t tk = tmem + kColK + kb * 64;
         const uint32_t ts = tmem + kColS + kb * kNS;
@@ -307,16 +341,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (uint32_t)(j >> 1) & 1u;
         if (!mbar_wait(&sm.p_full[pb], ph, p.status)) break;
         if (j >= *static_cast<volatile int*>(&sm.pv_stop)) break;  // tile j is the sentinel
-        if (!mbar_wait(&sm.v_full[pb], ph, p.status)) break;
+        if (!mbar_wait(&sm.v_full[j % kStages], (uint32_t)(j / kStages) & 1u, p.status)) break;
         tc_fence_after();
-        const uint32_t ocol = tmem + kColO + pb * kNP;
-        const uint64_t a0 = umma_desc(smem_u32(sm.v16[pb]), kT * 128, 1024);
+        // O of the tile's item accumulates over its tiles; its first tile overwrites it
+        const int fl = *static_cast<volatile int*>(&sm.pflag[pb]);
+        const uint32_t ocol = tmem + kColO + (uint32_t)(fl >> 1) * kNP;
+        const uint64_t a0 = umma_desc(smem_u32(sm.kv[j % kStages][0]), kT * 128, 1024);
         const uint64_t b0 = umma_desc(smem_u32(sm.p[pb]), 16, 1024);
 #pragma unroll
         for (int s = 0; s < kT / 16; ++s)  // 16 tokens per step
           umma_f16(ocol, a0 + ((s * 16 * 128) >> 4), b0 + ((((s >> 2) * (kNP * 128)) + (s & 3) * 32) >> 4),
-                   idesc_pv, s > 0);
+                   idesc_pv, (s > 0 || !(fl & 1)) ? 1u : 0u);
         umma_commit(&sm.pv_done[pb]);
+        umma_commit(&sm.kv_empty[j % kStages]);  // the tile's codes and fp16 V are no longer needed
       }
     }
   } else if (warp < 6 || warp >= kSm2Warp0) {
@@ -338,30 +375,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier-reduction tells) keeps the reference, with no exchange of maxima; otherwise
     // the tile's exact maximum is exchanged and the reference raised.  m_thr is each
     // thread's true maximum, combined at the item's end for the max and sum outputs.
-    float m_run[GH], l_part[GH], alpha_prev[GH], acc[GH], m_thr[GH];
+    float m_run[GH], l_part[GH], acc[GH], m_thr[GH];
     int vpos[GH];  // query position of each of this group's virtual heads
 #pragma unroll
     for (int g = 0; g < GH; ++g) {
-      m_run[g] = kNoRef; l_part[g] = 0.f; alpha_prev[g] = 0.f; acc[g] = 0.f; m_thr[g] = -INFINITY;
+      m_run[g] = kNoRef; l_part[g] = 0.f; acc[g] = 0.f; m_thr[g] = -INFINITY;
       vpos[g] = kKeyMask ? (h0 + g) / p.G : 0;
     }
     float vs_cur = 0.f, vo_cur = 0.f;  // value antiquant of channel r for the current item
     int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
-    bool prev_first = false, prev_last = false;
+    int ob = 1;  // O buffer of the current item (items alternate between the two)
 
-    // Folds in the PV result of tile jj; finishes the item if jj was its last tile.  Called
-    // after the softmax of tile jj + 1, or before it when that tile starts a new item (the
-    // item's state is then still in m_run, l_part and m_thr).
-    auto correct = [&](int jj) -> bool {
-      const int ob = jj & 1;
-      if (!mbar_wait(&sm.pv_done[ob], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
+    // Finishes the item whose last tile is jj (its state is still in m_run, l_part and
+    // m_thr, its PV products accumulated in O buffer ob): called before the softmax of the
+    // next item's first tile, or after the sentinel.
+    auto finish = [&](int jj) -> bool {
+      if (!mbar_wait(&sm.pv_done[jj & 1], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
       tc_fence_after();
       float o[GH];  // this group's heads only; read before this warp's next p_full arrival
       tmem_ld_n<GH>(tq + kColO + ob * kNP + h0, o);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-      for (int g = 0; g < GH; ++g) acc[g] = prev_first ? o[g] : fmaf(acc[g], alpha_prev[g], o[g]);
-      if (prev_last) {
+      for (int g = 0; g < GH; ++g) acc[g] = o[g];
+      {
         float lv[GH], mt[GH];
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
@@ -442,16 +478,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (meta.first) {  // finish the previous item first, then start this one
-        if (j > 0 && !correct(j - 1)) { ok = false; break; }
+        // this item's value scale/offset of channel r: index 1 of (2, Nkv, D); loaded before the
+        // previous item's epilogue so that their latency overlaps it
+        const int64_t vi = ((int64_t)p.Nkv + meta.hkv) * kD + r;
+        const float vs_nxt = p.aq_scale[vi];
+        const float vo_nxt = p.aq_offset ? p.aq_offset[vi] : 0.f;
+        if (j > 0 && !finish(j - 1)) { ok = false; break; }
+        vs_cur = vs_nxt;
+        vo_cur = vo_nxt;
+        ob ^= 1;
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
           m_run[g] = kNoRef;
           l_part[g] = 0.f;
           m_thr[g] = -INFINITY;
         }
-        const int64_t vi = ((int64_t)p.Nkv + meta.hkv) * kD + r;  // value scale/offset: index 1 of (2, Nkv, D)
-        vs_cur = p.aq_scale[vi];
-        vo_cur = p.aq_offset ? p.aq_offset[vi] : 0.f;
       }
       tc_fence_after();
       float s[GH];  // scores of this group's heads
@@ -495,6 +536,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_part[g] = fmaf(l_part[g], alpha[g], pr[g]);
           m_run[g] = m_new;
         }
+        if (!meta.first) {  // O holds the item's earlier tiles relative to the old reference
+          if (!mbar_wait(&sm.pv_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, p.status)) { ok = false; break; }
+          tc_fence_after();
+          float o[GH];
+          tmem_ld_n<GH>(tq + kColO + ob * kNP + h0, o);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int g = 0; g < GH; ++g) o[g] *= alpha[g];
+          tmem_st_n<GH>(tq + kColO + ob * kNP + h0, o);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
       } else {  // every score within 2^kLazyMax of the reference: keep it
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
@@ -503,27 +555,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_part[g] += pr[g];
         }
       }
-      uint8_t* pbuf = sm.p[sb];  // free: PV(j - 2) was waited for in correct(j - 2)
+      uint8_t* pbuf = sm.p[sb];
+      // the P buffer is free once PV(j - 2) has completed
+      if (j >= 2 && !mbar_wait(&sm.pv_done[sb], sph ^ 1u, p.status)) { ok = false; break; }
 #pragma unroll
       for (int g = 0; g < GH; ++g)
         if (h0 + g < G)
           *reinterpret_cast<uint16_t*>(pbuf + i8_p_offset(h0 + g, r)) = __half_as_ushort(__float2half_rn(pr[g]));
+      if (warp == 2 && lane == 0) sm.pflag[sb] = (meta.first ? 1 : 0) | (ob << 1);
       fence_proxy_async_smem();
-      tc_fence_before();  // the tensor-memory reads of S(j) and O(j - 2) precede the arrival
+      tc_fence_before();  // the tensor-memory accesses of S(j) (and O) precede the arrival
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[sb]);
-      if (j > 0 && !meta.first && !correct(j - 1)) { ok = false; break; }
-#pragma unroll
-      for (int g = 0; g < GH; ++g) alpha_prev[g] = alpha[g];
-      prev_first = meta.first;
-      prev_last = meta.last;
       prev_item = meta.item;
       prev_b = meta.b;
       prev_hkv = meta.hkv;
       prev_nch = meta.nch;
       ++j;
     }
-    if (ok && j > 0) correct(j - 1);
+    if (ok && j > 0) finish(j - 1);
   } else if (warp < 10) {
     // ------------------------------------------------------------------ K codes -> TMEM
     const int quad = warp & 3;
@@ -562,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&sm.kv_empty[st]);
+        mbar_arrive(&sm.kconv[st]);
         mbar_arrive(&sm.k_full[kb]);
       }
     }
@@ -573,11 +623,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = j % kStages;
       if (!mbar_wait(&sm.kv_full[st], (uint32_t)(j / kStages) & 1u, p.status)) break;
       if (sm.meta[st].item < 0) break;
-      const int vb = j & 1;
-      // PV(j - 2) has completed: the fp16 V buffer is free
-      if (!mbar_wait(&sm.pv_done[vb], ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status)) break;
+      // fp16 channels 0-63 of row r go over K row r: the K converters must have read it.
+      // Channels 64-127 go over this row's own codes, each 16-byte chunk after the codes
+      // it overwrites have been read (chunk c of codes feeds fp16 chunks 2c and 2c + 1).
+      if (!mbar_wait(&sm.kconv[st], (uint32_t)(j / kStages) & 1u, p.status)) break;
       const uint32_t row = smem_u32(sm.kv[st][1]) + r * 128;
-      const uint32_t dst = smem_u32(sm.v16[vb]) + r * 128;
+      const uint32_t dst = smem_u32(sm.kv[st][0]) + r * 128;
 #pragma unroll
       for (int chunk = 0; chunk < 8; ++chunk) {
         const uint4 w = lds128(row + ((chunk ^ (r & 7)) << 4));
@@ -596,10 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sm.kv_empty[st]);
-        mbar_arrive(&sm.v_full[vb]);
-      }
+      if (lane == 0) mbar_arrive(&sm.v_full[st]);
     }
   }
 
