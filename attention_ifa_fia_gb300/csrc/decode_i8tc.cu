@@ -86,6 +86,7 @@ struct I8Smem {
   alignas(16) float red[2][kNP][4];  // [S buffer][head][warp]: per-warp maxima
   float lsum[4][kNP];
   float lmax[4][kNP];  // [warp][head]: per-warp true maxima at an item's end
+  float lref[kNP];     // [head]: the item's final reference (m_run) at its end
   I8Meta meta[kStages];    // per int8 stage (producer)
   I8Meta tmeta[kMetaRing];  // per tile j at j % kMetaRing (K converters)
   uint64_t kv_full[kStages], kv_empty[kStages];
@@ -375,92 +376,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier-reduction tells) keeps the reference, with no exchange of maxima; otherwise
     // the tile's exact maximum is exchanged and the reference raised.  m_thr is each
     // thread's true maximum, combined at the item's end for the max and sum outputs.
-    float m_run[GH], l_part[GH], acc[GH], m_thr[GH];
+    float m_run[GH], l_part[GH], m_thr[GH];
     int vpos[GH];  // query position of each of this group's virtual heads
 #pragma unroll
     for (int g = 0; g < GH; ++g) {
-      m_run[g] = kNoRef; l_part[g] = 0.f; acc[g] = 0.f; m_thr[g] = -INFINITY;
+      m_run[g] = kNoRef; l_part[g] = 0.f; m_thr[g] = -INFINITY;
       vpos[g] = kKeyMask ? (h0 + g) / p.G : 0;
     }
     float vs_cur = 0.f, vo_cur = 0.f;  // value antiquant of channel r for the current item
     int prev_item = -1, prev_b = 0, prev_hkv = 0, prev_nch = 1;
     int ob = 1;  // O buffer of the current item (items alternate between the two)
+    // The epilogue of a finished item waits until the softmax of the next item's first tile
+    // has released its P, so that the products of the new item run meanwhile.  Its row
+    // partials (sums and maxima reduced over each warp, and the final reference) were left
+    // in shared memory at its last tile; these hold the rest.
+    bool pending = false;
+    int pend_item = 0, pend_b = 0, pend_hkv = 0, pend_nch = 1;
+    float pend_vs = 0.f, pend_vo = 0.f;
 
-    // Finishes the item whose last tile is jj (its state is still in m_run, l_part and
-    // m_thr, its PV products accumulated in O buffer ob): called before the softmax of the
-    // next item's first tile, or after the sentinel.
-    auto finish = [&](int jj) -> bool {
+    // At an item's last tile: this warp's partial sums and maxima, and the reference.
+    auto park = [&]() {
+      float lv[GH], mt[GH];
+#pragma unroll
+      for (int g = 0; g < GH; ++g) {
+        lv[g] = l_part[g];
+        mt[g] = m_thr[g];
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1)
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+          lv[g] += __shfl_xor_sync(0xffffffffu, lv[g], off);
+          mt[g] = fmaxf(mt[g], __shfl_xor_sync(0xffffffffu, mt[g], off));
+        }
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+          sm.lsum[quad][h0 + g] = lv[g];
+          sm.lmax[quad][h0 + g] = mt[g];
+          if (quad == 0) sm.lref[h0 + g] = m_run[g];
+        }
+      }
+    };
+
+    // The epilogue of the pending item (last tile jj, O buffer obuf): final output, or split
+    // partial.
+    auto finish = [&](int jj, int obuf) -> bool {
+      named_bar_sync(bar_group, 128);  // every warp of the group has parked its partials
       if (!mbar_wait(&sm.pv_done[jj & 1], (uint32_t)(jj >> 1) & 1u, p.status)) return false;
       tc_fence_after();
-      float o[GH];  // this group's heads only; read before this warp's next p_full arrival
-      tmem_ld_n<GH>(tq + kColO + ob * kNP + h0, o);
+      float o[GH];  // this group's heads only
+      tmem_ld_n<GH>(tq + kColO + obuf * kNP + h0, o);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      // (mm, lt): the head's true maximum and the sum relative to it; a relative to it too
+      float mm[GH], lt[GH], a[GH];
 #pragma unroll
-      for (int g = 0; g < GH; ++g) acc[g] = o[g];
-      {
-        float lv[GH], mt[GH];
-#pragma unroll
-        for (int g = 0; g < GH; ++g) {
-          lv[g] = l_part[g];
-          mt[g] = m_thr[g];
-        }
-#pragma unroll
-        for (int off = 16; off; off >>= 1)
-#pragma unroll
-          for (int g = 0; g < GH; ++g) {
-            lv[g] += __shfl_xor_sync(0xffffffffu, lv[g], off);
-            mt[g] = fmaxf(mt[g], __shfl_xor_sync(0xffffffffu, mt[g], off));
-          }
-        if (lane == 0) {
-#pragma unroll
-          for (int g = 0; g < GH; ++g) {
-            sm.lsum[quad][h0 + g] = lv[g];
-            sm.lmax[quad][h0 + g] = mt[g];
-          }
-        }
-        named_bar_sync(bar_group, 128);
-        // (mm, lt): the head's true maximum and the sum relative to it; a relative to it too
-        float mm[GH], lt[GH], a[GH];
+      for (int g = 0; g < GH; ++g) {
+        mm[g] = fmax3(fmaxf(sm.lmax[0][h0 + g], sm.lmax[1][h0 + g]), sm.lmax[2][h0 + g], sm.lmax[3][h0 + g]);
+        const float sc = (mm[g] == -INFINITY) ? 0.f : exp2f(sm.lref[h0 + g] - mm[g]);
+        lt[g] = (sm.lsum[0][h0 + g] + sm.lsum[1][h0 + g] + sm.lsum[2][h0 + g] + sm.lsum[3][h0 + g]) * sc;
+        a[g] = pend_vs * fmaf(-pend_vo, lt[g], o[g] * sc);  // sum_t 2^(s_t - mm) v^_t, unnormalised
+      }
+      if (pend_nch == 1 && !p.partials_only) {
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
-          mm[g] = fmax3(fmaxf(sm.lmax[0][h0 + g], sm.lmax[1][h0 + g]), sm.lmax[2][h0 + g], sm.lmax[3][h0 + g]);
-          const float sc = (mm[g] == -INFINITY) ? 0.f : exp2f(m_run[g] - mm[g]);
-          lt[g] = (sm.lsum[0][h0 + g] + sm.lsum[1][h0 + g] + sm.lsum[2][h0 + g] + sm.lsum[3][h0 + g]) * sc;
-          a[g] = vs_cur * fmaf(-vo_cur, lt[g], acc[g] * sc);  // sum_t 2^(s_t - mm) v^_t, unnormalised
-        }
-        if (prev_nch == 1 && !p.partials_only) {
-#pragma unroll
-          for (int g = 0; g < GH; ++g) {
-            const int hg = h0 + g;
-            if (hg < G) {
-              // several query positions run only on the key-mask instantiation; the plain one keeps
-              // the one-position rows (measured: the general mapping here slowed every tile by 4%)
-              const int64_t row = kKeyMask ? q_row(p, prev_b, prev_hkv, hg) : (int64_t)prev_b * p.Nq + prev_hkv * G + hg;
-              const int h = kKeyMask ? q_head(p, prev_hkv, hg) : prev_hkv * G + hg;
-              float M, W;
-              const float v = single_item_output(a[g], mm[g], lt[g], p.sink, h, &M, &W);
-              store_out<QT>(p.out, row * kD + r, v);
-              if (r == hg) {
-                if (p.softmax_max) p.softmax_max[row] = (M == -INFINITY) ? -INFINITY : M * kLn2;
-                if (p.softmax_sum) p.softmax_sum[row] = W;
-              }
+          const int hg = h0 + g;
+          if (hg < G) {
+            // several query positions run only on the key-mask instantiation; the plain one keeps
+            // the one-position rows (measured: the general mapping here slowed every tile by 4%)
+            const int64_t row = kKeyMask ? q_row(p, pend_b, pend_hkv, hg) : (int64_t)pend_b * p.Nq + pend_hkv * G + hg;
+            const int h = kKeyMask ? q_head(p, pend_hkv, hg) : pend_hkv * G + hg;
+            float M, W;
+            const float v = single_item_output(a[g], mm[g], lt[g], p.sink, h, &M, &W);
+            store_out<QT>(p.out, row * kD + r, v);
+            if (r == hg) {
+              if (p.softmax_max) p.softmax_max[row] = (M == -INFINITY) ? -INFINITY : M * kLn2;
+              if (p.softmax_sum) p.softmax_sum[row] = W;
             }
           }
-        } else {
-          float* po = p.ws.part_o + (int64_t)prev_item * G * kD;
-#pragma unroll
-          for (int g = 0; g < GH; ++g)
-            if (h0 + g < G) po[(h0 + g) * kD + r] = lt[g] > 0.f ? a[g] / lt[g] : 0.f;
-          if (r >= h0 && r < h0 + GH && r < G) {
-            float mv = mm[0], lw = lt[0];
-#pragma unroll
-            for (int g = 1; g < GH; ++g)
-              if (r == h0 + g) { mv = mm[g]; lw = lt[g]; }
-            p.ws.part_ml[(int64_t)prev_item * G + r] = make_float2(mv, lw);
-          }
         }
-        named_bar_sync(bar_group, 128);
+      } else {
+        float* po = p.ws.part_o + (int64_t)pend_item * G * kD;
+#pragma unroll
+        for (int g = 0; g < GH; ++g)
+          if (h0 + g < G) po[(h0 + g) * kD + r] = lt[g] > 0.f ? a[g] / lt[g] : 0.f;
+        if (r >= h0 && r < h0 + GH && r < G) {
+          float mv = mm[0], lw = lt[0];
+#pragma unroll
+          for (int g = 1; g < GH; ++g)
+            if (r == h0 + g) { mv = mm[g]; lw = lt[g]; }
+          p.ws.part_ml[(int64_t)pend_item * G + r] = make_float2(mv, lw);
+        }
       }
+      named_bar_sync(bar_group, 128);  // the parked partials may be overwritten
+      pending = false;
       return true;
     };
 
@@ -477,15 +486,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&sm.p_full[sb]);
         break;
       }
-      if (meta.first) {  // finish the previous item first, then start this one
-        // this item's value scale/offset of channel r: index 1 of (2, Nkv, D); loaded before the
-        // previous item's epilogue so that their latency overlaps it
-        const int64_t vi = ((int64_t)p.Nkv + meta.hkv) * kD + r;
-        const float vs_nxt = p.aq_scale[vi];
-        const float vo_nxt = p.aq_offset ? p.aq_offset[vi] : 0.f;
-        if (j > 0 && !finish(j - 1)) { ok = false; break; }
-        vs_cur = vs_nxt;
-        vo_cur = vo_nxt;
+      if (meta.first) {  // the previous item's epilogue waits (see finish); start this one
+        if (j > 0) {
+          pending = true;
+          pend_item = prev_item; pend_b = prev_b; pend_hkv = prev_hkv; pend_nch = prev_nch;
+          pend_vs = vs_cur; pend_vo = vo_cur;
+        }
+        const int64_t vi = ((int64_t)p.Nkv + meta.hkv) * kD + r;  // value scale/offset: index 1 of (2, Nkv, D)
+        vs_cur = p.aq_scale[vi];
+        vo_cur = p.aq_offset ? p.aq_offset[vi] : 0.f;
         ob ^= 1;
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
@@ -567,13 +576,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();  // the tensor-memory accesses of S(j) (and O) precede the arrival
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+      if (pending && !finish(j - 1, ob ^ 1)) { ok = false; break; }  // (this tile starts an item)
+      if (meta.last) park();
       prev_item = meta.item;
       prev_b = meta.b;
       prev_hkv = meta.hkv;
       prev_nch = meta.nch;
       ++j;
     }
-    if (ok && j > 0) finish(j - 1);
+    if (ok && j > 0) {  // the last item: its partials were parked at its last tile
+      pend_item = prev_item; pend_b = prev_b; pend_hkv = prev_hkv; pend_nch = prev_nch;
+      pend_vs = vs_cur; pend_vo = vo_cur;
+      finish(j - 1, ob);
+    }
   } else if (warp < 10) {
     // ------------------------------------------------------------------ K codes -> TMEM
     const int quad = warp & 3;
