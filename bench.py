@@ -88,12 +88,14 @@ def e2e_pipeline(torch, stream, call, dev_in, pin_in, outs, warmup, steps, barri
     dev_in[j], j = i mod len(dev_in)) on a copy stream, runs call(i, j, o) on the compute
     stream, and copies its results device -> host (outs[o], o = i mod 2) on a second copy
     stream; events keep every buffer's copies and use in order, so one step's copies overlap
-    its neighbours' compute.  Groups of len(dev_in) steps are captured once in a CUDA graph
+    its neighbours' compute.  Groups of 8 len(dev_in) steps are captured once in a CUDA graph
     and replayed (issuing a step's copies, events and launches from Python costs about as
-    much host time as the GPU spends on it); leftover steps run uncaptured.  Returns the
-    milliseconds from the first copy to the last result in host memory (CUDA events on the
-    compute stream)."""
+    much host time as the GPU spends on it; a replay starts by joining the copy streams, so
+    one input copy per replay is not overlapped, hence long groups); the remaining steps are a
+    second graph.  Returns the milliseconds from the first copy to the last result in host
+    memory (CUDA events on the compute stream)."""
     nin = len(dev_in)
+    group = 8 * nin
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
     def steps_on(comp, first, n):
@@ -129,20 +131,26 @@ def e2e_pipeline(torch, stream, call, dev_in, pin_in, outs, warmup, steps, barri
 
     steps_on(stream, 0, min(warmup, 2 * nin))  # uncaptured warm-up (the library's set-up happens here)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=cap):
-        steps_on(cap, 0, nin)
-    for _ in range(max(1, warmup // nin)):
-        graph.replay()
+        steps_on(cap, 0, group)
+    rest = None
+    if steps % group:
+        rest = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(rest, stream=cap):
+            steps_on(cap, 0, steps % group)
+    graph.replay()
+    if rest is not None:
+        rest.replay()
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps // nin):
+    for _ in range(steps // group):
         graph.replay()
-    if steps % nin:
-        steps_on(stream, 0, steps % nin)
+    if rest is not None:
+        rest.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
