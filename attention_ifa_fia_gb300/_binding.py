@@ -38,7 +38,8 @@ class PrefillOptions(ctypes.Structure):
     """fia_prefill_options of include/fia.h."""
     _fields_ = [("pre_tokens", ctypes.c_int64), ("next_tokens", ctypes.c_int64), ("block_table", ctypes.c_void_p),
                 ("bt_stride", ctypes.c_int64), ("seq_lens_kv", ctypes.c_void_p), ("block_size", ctypes.c_int),
-                ("num_blocks", ctypes.c_int64), ("kv_layout", ctypes.c_int)]
+                ("num_blocks", ctypes.c_int64), ("kv_layout", ctypes.c_int), ("quant_scale2", ctypes.c_void_p),
+                ("quant_offset2", ctypes.c_void_p), ("quant2_per_channel", ctypes.c_int)]
 
 
 class DecodeOptions(ctypes.Structure):
@@ -276,13 +277,15 @@ def fia_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q:
                 out: Optional[torch.Tensor] = None, softmax_max=None, softmax_sum=None,
                 workspace: Optional[torch.Tensor] = None, stream=None, pre_tokens: Optional[int] = None,
                 next_tokens: Optional[int] = None, block_table: Optional[torch.Tensor] = None,
-                seq_lens_kv: Optional[torch.Tensor] = None, kv_layout: int = KV_BNNBSD):
+                seq_lens_kv: Optional[torch.Tensor] = None, kv_layout: int = KV_BNNBSD,
+                quant_scale2: Optional[torch.Tensor] = None, quant_offset2: Optional[torch.Tensor] = None):
     """Prefill attention, TND.  q: (T, Nq, D); k, v: (Tkv, Nkv, D); cu_seqlens int64 (B + 1,)
     on the device.  mask 3 = rightDownCausal, 0 = none, 4 = band (pre_tokens, next_tokens
     around the rightDownCausal diagonal, through fia_prefill_ex).  With block_table (int32
     (B, width)) and seq_lens_kv (int64 (B,)), k and v are paged pools (num_blocks, Nkv,
     block_size, D), or with kv_layout=KV_BNBSH (num_blocks, block_size, Nkv * D), and
-    cu_seqlens_kv may be None.  Returns (out, softmax_max, softmax_sum)."""
+    cu_seqlens_kv may be None.  quant_scale2 (and quant_offset2): fp32 of 1 or Nq * D values;
+    out is then int8.  Returns (out, softmax_max, softmax_sum)."""
     T, D = int(q.shape[0]), int(q.shape[-1])
     paged = block_table is not None
     Tkv = 0 if paged else int(k.shape[0])
@@ -291,7 +294,16 @@ def fia_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q:
     if scale is None:
         scale = D ** -0.5
     if out is None:
-        out = torch.empty((T, num_heads, D), dtype=q.dtype, device=q.device)
+        out = torch.empty((T, num_heads, D), dtype=torch.int8 if quant_scale2 is not None else q.dtype,
+                          device=q.device)
+    q2_per_channel = 0
+    if quant_scale2 is not None:
+        n2 = quant_scale2.numel()
+        if n2 not in (1, num_heads * D) or quant_scale2.dtype != torch.float32:
+            raise ValueError("quant_scale2 must be fp32 with 1 or Nq * D values")
+        if quant_offset2 is not None and (quant_offset2.numel() != n2 or quant_offset2.dtype != torch.float32):
+            raise ValueError("quant_offset2 must match quant_scale2")
+        q2_per_channel = int(n2 != 1)
     if workspace is None:
         nbytes = fia_prefill_workspace_size(B, num_heads, nkv, D, max_seqlen_q)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
@@ -299,14 +311,15 @@ def fia_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q:
             int(max_seqlen_q), int(max_seqlen_kv), num_heads, nkv, D, float(scale), int(mask), _ptr(sink), _ptr(out),
             _ptr(softmax_max), _ptr(softmax_sum), _ptr(workspace), workspace.numel() * workspace.element_size(),
             _stream(stream))
-    if pre_tokens is None and next_tokens is None and not paged:
+    if pre_tokens is None and next_tokens is None and not paged and quant_scale2 is None and quant_offset2 is None:
         _check(_lib.fia_prefill(*args), "fia_prefill")
     else:
         bs = (int(k.shape[1]) if kv_layout == KV_BNBSH else int(k.shape[2])) if paged else 0
         opts = PrefillOptions(int(pre_tokens if pre_tokens is not None else 1 << 40),
                               int(next_tokens if next_tokens is not None else 1 << 40),
                               _ptr(block_table), int(block_table.shape[1]) if paged else 0, _ptr(seq_lens_kv), bs,
-                              int(k.shape[0]) if paged else 0, int(kv_layout))
+                              int(k.shape[0]) if paged else 0, int(kv_layout), _ptr(quant_scale2),
+                              _ptr(quant_offset2), q2_per_channel)
         _check(_lib.fia_prefill_ex(*args, ctypes.byref(opts)), "fia_prefill_ex")
     return out, softmax_max, softmax_sum
 

@@ -765,6 +765,12 @@ static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype d
       return fail(FIA_ERR_PARAM_INVALID, "block table too narrow: max_seqlen_kv %d > bt_stride %lld * block_size %d",
                   max_seqlen_kv, (long long)opt->bt_stride, bs);
   }
+  const float* qs2 = opt ? opt->quant_scale2 : nullptr;
+  const float* qo2 = opt ? opt->quant_offset2 : nullptr;
+  const int q2_per_channel = opt ? opt->quant2_per_channel : 0;
+  if (qo2 && !qs2) return fail(FIA_ERR_PARAM_INVALID, "quant_offset2 without quant_scale2");
+  if (q2_per_channel != 0 && q2_per_channel != 1)
+    return fail(FIA_ERR_PARAM_INVALID, "quant2_per_channel must be 0 or 1 (got %d)", q2_per_channel);
   if (!std::isfinite(scale)) return fail(FIA_ERR_PARAM_INVALID, "scale is not finite");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(FIA_ERR_PARAM_INVALID, "q, k, v and out must be 16-byte aligned");
@@ -813,6 +819,9 @@ static int prefill_impl(const void* q, const void* k, const void* v, fia_dtype d
   }
   p.dtype = dtype;
   p.scale_log2 = (float)(scale * 1.4426950408889634);
+  p.pq_scale = qs2;
+  p.pq_offset = qo2;
+  p.pq_stride = q2_per_channel;
   p.tile_counter = static_cast<int*>(workspace);
   p.tile_list = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + 256);
   p.max_tiles = (int)((need - 256) / sizeof(int));

@@ -194,6 +194,11 @@ struct PrefillParams {
   int kv_x_h, kv_z_blk, kv_z_h;
   int dtype;          // kBF16 or kF16
   float scale_log2;
+  // int8 output (pq_scale non-null): code = saturate(rne(o * pq_scale[c] + pq_offset[c])),
+  // c = (h * D + d) * pq_stride (pq_stride 0: one value for every channel)
+  const float* pq_scale;
+  const float* pq_offset;
+  int pq_stride;
   int* tile_list;     // workspace: (sequence << 16 | query tile) pairs, longest first
   int* tile_counter;  // workspace: [0] unit counter, [1] number of units
   int max_tiles;

@@ -242,6 +242,21 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// int8 output (quantScale2 / quantOffset2): the codes of channels c0 .. c0 + 3 of a row, each
+// the fp32 output v * inv scaled and offset by its channel's values, rounded to the nearest
+// integer (ties to even) and saturated to [-128, 127]; packed low byte first
+__device__ __forceinline__ uint32_t quant4(const float* v, float inv, const PrefillParams& p, int c0) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int pc = (c0 + i) * p.pq_stride;
+    const float y = fmaf(v[i] * inv, p.pq_scale[pc], p.pq_offset ? p.pq_offset[pc] : 0.f);
+    const int q = min(max(__float2int_rn(y), -128), 127);
+    w |= (uint32_t)(q & 0xff) << (8 * i);
+  }
+  return w;
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
@@ -297,7 +312,7 @@ __device__ __forceinline__ void umma_f16_ta_w(uint32_t d_tmem, uint32_t a_tmem, 
 // kBand: a band's lower edge may fall inside a key tile (pre_tokens below the longest key
 // sequence); without it the lower edge is never inside a tile and the softmax masks the
 // upper edge only.
-template <int kD, int DT, bool kBand>
+template <int kD, int DT, bool kBand, bool kQuant>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -592,11 +607,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int64_t tok = (int64_t)meta.tq + qi;
         // every lane takes part in the (warp-collective) TMEM loads; only valid rows store
         uint8_t* orow = static_cast<uint8_t*>(p.out) + ((tok * p.Nq + meta.h) * (int64_t)kD + o_base) * 2;
+        uint8_t* qrow = static_cast<uint8_t*>(p.out) + (tok * p.Nq + meta.h) * (int64_t)kD + o_base;  // int8
 #pragma unroll
         for (int c = 0; c < kOH; c += 32) {
           float o[32];
           tmem_ld32(tq_lane + kColO + o_base + c, o);
-          if (row_ok) {
+          if constexpr (kQuant) {
+            if (row_ok) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 16) {
+                const int ch = meta.h * kD + o_base + c + i;
+                const uint4 w = make_uint4(quant4(o + i, inv, p, ch), quant4(o + i + 4, inv, p, ch + 4),
+                                           quant4(o + i + 8, inv, p, ch + 8), quant4(o + i + 12, inv, p, ch + 12));
+                *reinterpret_cast<uint4*>(qrow + c + i) = w;
+              }
+            }
+          } else if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
               uint4 w;
@@ -774,7 +800,7 @@ struct P2Smem {
 };
 static_assert(sizeof(P2Smem<128>) <= 232448, "prefill shared memory exceeds the per-CTA limit");
 
-template <int kD, int DT, bool kBand>
+template <int kD, int DT, bool kBand, bool kQuant>
 __global__ void __launch_bounds__(kP2Threads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -1172,6 +1198,17 @@ __global__ void __launch_bounds__(kP2Threads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.o_free[x]);
           }
+          if constexpr (kQuant) {  // int8: the half's 64 codes are chunks 4 half .. 4 half + 3 of the row
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const float* v = o + 16 * c;
+              const int ch = h * kD + half * 64 + 16 * c;
+              const uint4 w = make_uint4(quant4(v, inv, p, ch), quant4(v + 4, inv, p, ch + 4),
+                                         quant4(v + 8, inv, p, ch + 8), quant4(v + 12, inv, p, ch + 12));
+              *reinterpret_cast<uint4*>(stg + lane * 128 + (((4 * half + c) ^ (lane & 7)) << 4)) = w;
+            }
+            continue;  // the rows go out once both halves are staged
+          }
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const float* v = o + 8 * c;
@@ -1190,6 +1227,19 @@ __global__ void __launch_bounds__(kP2Threads, 1)
             const int rr = 4 * k + (lane >> 3), c = lane & 7;
             const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
             if (rr < rows_ok) *reinterpret_cast<uint4*>(obase + rr * orow_stride + half * 128 + c * 16) = w;
+          }
+          __syncwarp();
+        }
+        if constexpr (kQuant) {  // int8 rows of kD bytes: kD / 16 chunks, 32 / (kD / 16) rows per store
+          constexpr int kChunks = kD / 16, kRowsPer = 32 / kChunks;
+          uint8_t* qbase = static_cast<uint8_t*>(p.out) + (((int64_t)meta.tq + row0) * p.Nq + h) * (int64_t)kD;
+          const int64_t qrow_stride = (int64_t)p.Nq * kD;
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < kChunks; ++k) {
+            const int rr = kRowsPer * k + lane / kChunks, c = lane % kChunks;
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((c ^ (rr & 7)) << 4));
+            if (rr < rows_ok) *reinterpret_cast<uint4*>(qbase + rr * qrow_stride + c * 16) = w;
           }
           __syncwarp();
         }
@@ -1233,13 +1283,15 @@ cudaError_t launch_prefill_attention(const PrefillParams& p, const CUtensorMap& 
   const bool band = p.pre < p.max_seqlen_kv;
   if (p.G % 2 == 0) {  // heads 2hp and 2hp + 1 share a kv head
     const size_t smem = sizeof(P2Smem<kD>);
-    auto kern = band ? prefill_pair_kernel<kD, DT, true> : prefill_pair_kernel<kD, DT, false>;
+    auto kern = p.pq_scale ? (band ? prefill_pair_kernel<kD, DT, true, true> : prefill_pair_kernel<kD, DT, false, true>)
+                           : (band ? prefill_pair_kernel<kD, DT, true, false> : prefill_pair_kernel<kD, DT, false, false>);
     cudaError_t e = ensure_smem(kern, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_dependent(kern, num_sms, kP2Threads, smem, stream, tmQ, tmK, tmV, p);
   }
   const size_t smem = sizeof(PSmem<kD>);
-  auto kern = band ? prefill_tc_kernel<kD, DT, true> : prefill_tc_kernel<kD, DT, false>;
+  auto kern = p.pq_scale ? (band ? prefill_tc_kernel<kD, DT, true, true> : prefill_tc_kernel<kD, DT, false, true>)
+                         : (band ? prefill_tc_kernel<kD, DT, true, false> : prefill_tc_kernel<kD, DT, false, false>);
   cudaError_t e = ensure_smem(kern, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms, kPThreads, smem, stream>>>(tmQ, tmK, tmV, p);

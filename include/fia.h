@@ -289,8 +289,17 @@ int fia_prefill(const void* q, const void* k, const void* v, fia_dtype dtype, co
  *   of a sequence's last block past its length, and blocks past it, may hold anything
  *   (NaN included): they are masked in the scores and zeroed in the values.
  *
- * options may be NULL for masks 0 and 3 without paging (NULL with mask 4 is
- * FIA_ERR_PARAM_NULLPTR). */
+ * options->quant_scale2 non-NULL: out is an int8 (T, Nq, D) tensor, the output quantised
+ *   as fia_decode_ex quantises it (aclnnIncreFlashAttentionV3 quantScale2 / quantOffset2;
+ *   FusedInferAttentionScore takes the same pair in both of its modes):
+ *   out = saturate(round-half-even(o * quant_scale2[c] + quant_offset2[c])) to [-128, 127],
+ *   o the fp32 attention output, c = h * D + d with quant2_per_channel = 1 (Nq * D values),
+ *   c = 0 with quant2_per_channel = 0 (one value); quant_offset2 NULL is zero.
+ *   quant_offset2 without quant_scale2, or quant2_per_channel outside {0, 1}, is
+ *   FIA_ERR_PARAM_INVALID.
+ *
+ * options may be NULL for masks 0 and 3 without paging or quantised output (NULL with
+ * mask 4 is FIA_ERR_PARAM_NULLPTR). */
 typedef struct {
   int64_t pre_tokens;           /* mask 4 only */
   int64_t next_tokens;          /* mask 4 only */
@@ -300,6 +309,9 @@ typedef struct {
   int block_size;
   int64_t num_blocks;
   int kv_layout;                /* fia_kv_layout */
+  const float* quant_scale2;    /* device fp32, 1 or Nq * D values, or NULL (16-bit out) */
+  const float* quant_offset2;   /* device fp32, as quant_scale2, or NULL */
+  int quant2_per_channel;       /* 1: Nq * D values, 0: one value */
 } fia_prefill_options;
 
 int fia_prefill_ex(const void* q, const void* k, const void* v, fia_dtype dtype, const int64_t* cu_seqlens_q,

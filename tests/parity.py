@@ -84,6 +84,18 @@ def assert_close_max(name, got, ref, rtol=MAX_RTOL):
 
 
 # ----------------------------------------------------------------------------- decode
+def check_codes(code, y, out_ref, s_c, atol, rtol):
+    """code (rows, C) int8 against the oracle's unrounded y = out_ref * s + o: the kernel
+    quantises its own fp32 output, which is within (atol + rtol |out|) of out_ref, so its
+    code lies within 0.5 + s (atol + rtol |out_ref|) of y after saturation."""
+    c = code.astype(np.float64)
+    margin = np.abs(s_c) * (atol + rtol * np.abs(out_ref))
+    lo = np.clip(np.rint(y - margin), -128, 127)
+    hi = np.clip(np.rint(y + margin), -128, 127)
+    bad = (c < lo) | (c > hi)
+    assert not bad.any(), f"{bad.sum()} codes outside the tolerance band, e.g. {np.argwhere(bad)[:4].tolist()}"
+
+
 def run_decode(F, dd: DeviceDecode, num_splits=0, sink="case", max_kv_len=None, lens=None, bt=None):
     c = dd.case
     B, Nq = c.B, c.Nq

@@ -178,6 +178,8 @@ def _prefill_ex(lib, opts, **kw):
     (None, dict(mask=4), NULLPTR),                                                   # band without options
     (dict(pre_tokens=2, next_tokens=-3), dict(mask=4), INVALID),                     # empty band
     ({}, dict(mask=2), INVALID),                                                     # leftUpCausal: not built
+    (dict(quant_offset2=P), {}, INVALID),                                            # offset without scale
+    (dict(quant_scale2=P, quant2_per_channel=2), {}, INVALID),                       # per channel not 0 / 1
     (dict(block_table=P, bt_stride=1, block_size=128, num_blocks=4), dict(cu_kv=None), NULLPTR),  # no seq_lens_kv
     (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=24, num_blocks=4), {}, INVALID),  # not % 16
     (dict(block_table=P, bt_stride=1, seq_lens_kv=P, block_size=8, num_blocks=4), {}, INVALID),

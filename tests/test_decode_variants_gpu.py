@@ -20,7 +20,8 @@ import torch
 
 import fia_workloads as W
 import oracle as OR
-from parity import OUT_TOL, SUM_TOL, DeviceDecode, assert_close, assert_close_max, compare_decode, oracle_decode, run_decode
+from parity import (OUT_TOL, SUM_TOL, DeviceDecode, assert_close, assert_close_max, check_codes, compare_decode,
+                    oracle_decode, run_decode)
 
 pytestmark = pytest.mark.gpu
 
@@ -225,18 +226,6 @@ def test_atten_mask_rows_too_short(F, cuda):
 
 
 # ------------------------------------------------------------------ int8 post-quant output
-def _check_codes(code, y, out_ref, s_c, atol, rtol):
-    """code (rows, C) int8 against the oracle's unrounded y = out_ref * s + o: the kernel
-    quantises its own fp32 output, which is within (atol + rtol |out|) of out_ref, so its
-    code lies within 0.5 + s (atol + rtol |out_ref|) of y after saturation."""
-    c = code.astype(np.float64)
-    margin = np.abs(s_c) * (atol + rtol * np.abs(out_ref))
-    lo = np.clip(np.rint(y - margin), -128, 127)
-    hi = np.clip(np.rint(y + margin), -128, 127)
-    bad = (c < lo) | (c > hi)
-    assert not bad.any(), f"{bad.sum()} codes outside the tolerance band, e.g. {np.argwhere(bad)[:4].tolist()}"
-
-
 PQ_CASES = {
     "bf16_d128_g4_empty": dict(B=4, Nq=8, Nkv=2, D=128, block_size=128, lengths=[700, 0, 1000, 129]),
     "fp16_d64_g8_sink": dict(B=3, Nq=8, Nkv=1, D=64, block_size=64, dtype=W.FP16, lengths=[450, 0, 260],
@@ -271,7 +260,7 @@ def test_post_quant_int8_output(F, cuda, name, num_splits):
                            quant_offset2=None if o2 is None else torch.from_numpy(o2).cuda())
         assert out.dtype == torch.int8 and tuple(out.shape) == (case.B, case.Nq, case.D)
         s_c = np.broadcast_to(s2.astype(np.float64), (C,))
-        _check_codes(out.cpu().numpy().reshape(-1, C), y.reshape(-1, C), o_ref.reshape(-1, C), s_c, atol, rtol)
+        check_codes(out.cpu().numpy().reshape(-1, C), y.reshape(-1, C), o_ref.reshape(-1, C), s_c, atol, rtol)
         assert_close_max("softmax_max", mx.double().cpu().numpy().reshape(-1), m_ref)
         assert_close("softmax_sum", sm.double().cpu().numpy().reshape(-1), s_ref, *SUM_TOL)
     assert F.fia_device_status() == 0
@@ -358,7 +347,7 @@ def test_decode_band_window_with_mask_and_int8_out(F, cuda):
     y, _ = OR.post_quant(ref[0].reshape(case.B, -1), s2, None)
     code, _, _ = _run(F, dd, 2, pre_tokens=300, next_tokens=0, atten_mask=mask, quant_scale2=torch.from_numpy(s2).cuda())
     C = case.Nq * case.D
-    _check_codes(code.cpu().numpy().reshape(-1, C), y.reshape(-1, C), ref[0].reshape(-1, C),
+    check_codes(code.cpu().numpy().reshape(-1, C), y.reshape(-1, C), ref[0].reshape(-1, C),
                  np.broadcast_to(s2.astype(np.float64), (C,)), *OUT_TOL[case.dtype])
     assert F.fia_device_status() == 0
 
@@ -444,7 +433,7 @@ def test_decode_several_query_positions_lse_and_int8_out(F, cuda):
     code, _, _ = _run(F, dd, 3, q_len=4, quant_scale2=torch.from_numpy(s2).cuda())
     assert code.dtype == torch.int8 and tuple(code.shape) == (case.B, 4, case.Nq, case.D)
     y, _ = OR.post_quant(o_ref.reshape(-1, C), s2)
-    _check_codes(code.cpu().numpy().reshape(-1, C), y.reshape(-1, C), o_ref.reshape(-1, C),
+    check_codes(code.cpu().numpy().reshape(-1, C), y.reshape(-1, C), o_ref.reshape(-1, C),
                  np.broadcast_to(s2.astype(np.float64), (C,)), *OUT_TOL[case.dtype])
     assert F.fia_device_status() == 0
 

@@ -7,7 +7,9 @@ import pytest
 import torch
 
 import fia_workloads as W
-from parity import DevicePrefill, compare_prefill, oracle_prefill, run_prefill, sample_prefill_rows
+import oracle as OR
+from parity import (OUT_TOL, SUM_TOL, DevicePrefill, assert_close, assert_close_max, check_codes, compare_prefill,
+                    oracle_prefill, run_prefill, sample_prefill_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -254,3 +256,84 @@ def test_prefill_paged_rejects_block_sizes(F, cuda, bs):
         F.fia_prefill(dp.q, kp, kp, dp.cu_q, None, max_seqlen_q=5, max_seqlen_kv=100, num_heads=4, num_kv_heads=2,
                       block_table=bt, seq_lens_kv=lens)
     assert ei.value.code == 161002
+
+
+# ------------------------------------------------------------------ int8 post-quant output
+# quantScale2 / quantOffset2 (aclnnIncreFlashAttentionV3 parameter table; FusedInferAttentionScore
+# takes the pair in both modes) on the prefill output: both kernels, D 64 and 128, band, sink
+PQ_CASES = {
+    "pair_bf16_d128": (dict(Nq=8, Nkv=2, D=128, lengths=[300, 0, 129, 700]), None),
+    "odd_g_fp16_d128_sink": (dict(Nq=3, Nkv=1, D=128, lengths=[260, 77], dtype=W.FP16, sink=True), None),
+    "pair_bf16_d64_band": (dict(Nq=4, Nkv=2, D=64, lengths=[400, 130]), (100, 0)),
+    "odd_g_bf16_d64": (dict(Nq=3, Nkv=3, D=64, lengths=[333, 1]), None),
+}
+
+
+def _run_pq(F, dp, band, s2, o2):
+    c = dp.case
+    mx = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device="cuda")
+    sm = torch.full((c.T, c.Nq), float("nan"), dtype=torch.float32, device="cuda")
+    return F.fia_prefill(dp.q, dp.k, dp.v, dp.cu_q, dp.cu_kv, max_seqlen_q=int(c.lengths_q.max(initial=0)),
+                         max_seqlen_kv=int(c.lengths_kv.max(initial=0)), num_heads=c.Nq, num_kv_heads=c.Nkv,
+                         scale=c.scale, mask=3 if band is None else 4, sink=dp.sink, softmax_max=mx,
+                         softmax_sum=sm, pre_tokens=None if band is None else band[0],
+                         next_tokens=None if band is None else band[1], quant_scale2=torch.from_numpy(s2).cuda(),
+                         quant_offset2=None if o2 is None else torch.from_numpy(o2).cuda())
+
+
+@pytest.mark.parametrize("name", sorted(PQ_CASES))
+def test_prefill_post_quant_int8_output(F, cuda, name):
+    kw, band = PQ_CASES[name]
+    case = W.make_prefill_case(seed=zlib.crc32(("pq_" + name).encode()) % (1 << 30), **kw)
+    dp = DevicePrefill(case)
+    o_ref, m_ref, s_ref = oracle_prefill(case, band=band)
+    C = case.Nq * case.D
+    rng = np.random.default_rng(zlib.crc32(name.encode()) & 0xffff)
+    amax = max(float(np.abs(o_ref).max()), 1e-3)
+    atol, rtol = OUT_TOL[case.dtype]
+    per_channel = (rng.uniform(0.5, 1.5, C) * 60.0 / amax).astype(np.float32)
+    offsets = rng.uniform(-20, 20, C).astype(np.float32)
+    variants = [  # (scale2, offset2): per tensor / per channel, symmetric / asymmetric, saturating
+        (np.array([60.0 / amax], np.float32), None),
+        (np.array([60.0 / amax], np.float32), np.array([-7.5], np.float32)),
+        (per_channel, None),
+        (per_channel, offsets),
+        (np.array([1000.0 / amax], np.float32), np.array([3.0], np.float32)),
+    ]
+    for s2, o2 in variants:
+        y, _ = OR.post_quant(o_ref.reshape(case.T, C), s2, o2)   # channels h * D + d of a token row
+        out, mx, sm = _run_pq(F, dp, band, s2, o2)
+        assert out.dtype == torch.int8 and tuple(out.shape) == (case.T, case.Nq, case.D)
+        s_c = np.broadcast_to(s2.astype(np.float64), (C,))
+        check_codes(out.cpu().numpy().reshape(-1, C), y.reshape(-1, C), o_ref.reshape(-1, C), s_c, atol, rtol)
+        assert_close_max("softmax_max", mx.double().cpu().numpy().reshape(-1), m_ref)
+        assert_close("softmax_sum", sm.double().cpu().numpy().reshape(-1), s_ref, *SUM_TOL)
+    assert F.fia_device_status() == 0
+
+
+@pytest.mark.parametrize("Nq,D", [(4, 128), (3, 128), (4, 64), (1, 64)])
+def test_prefill_post_quant_ties_and_saturation_exact(F, cuda, Nq, D):
+    """Sequences of one query and one key: each output row is that key's value row, exactly
+    in fp32.  Values are multiples of 0.25 (exact in bf16), so with scale2 = 2 half of
+    y = 2v + o fall on ties (rounded to even) and with scale2 = 4 the large ones saturate:
+    the int8 output equals the oracle's codes bit for bit, on the head-pair kernel (even G)
+    and the single-head one (odd G)."""
+    case = W.make_prefill_case(Nq=Nq, Nkv=1, D=D, lengths=[1] * 40 + [0, 1], seed=D + Nq)
+    rng = np.random.default_rng(D * 7 + Nq)
+    vals = rng.integers(-255, 256, case.v.shape).astype(np.float32) * 0.25   # |v| <= 63.75
+    case.v = W.to_bits(vals, case.dtype)
+    assert np.array_equal(W.bits_to_f32(case.v, case.dtype), vals)
+    dp = DevicePrefill(case)
+    o_ref, _, _ = oracle_prefill(case)
+    C = Nq * D
+    for s2, o2 in [(2.0, 0.0), (2.0, 0.5), (4.0, -1.0), (0.5, 0.25)]:
+        y, code_ref = OR.post_quant(o_ref.reshape(case.T, C), [s2], [o2])
+        out, _, _ = _run_pq(F, dp, None, np.array([s2], np.float32), np.array([o2], np.float32))
+        got = out.cpu().numpy().reshape(code_ref.shape)
+        assert np.array_equal(got, code_ref), np.argwhere(got != code_ref)[:4].tolist()
+        if s2 == 4.0:
+            assert not np.any(y == np.floor(y) + 0.5)
+            assert np.any(code_ref == 127) and np.any(code_ref == -128)
+        else:
+            assert np.any(y == np.floor(y) + 0.5)      # ties present
+    assert F.fia_device_status() == 0
