@@ -196,13 +196,15 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p, int
   for (int pass = 0; pass < 2; ++pass) {  // pass 0: histogram of key-tile counts; pass 1: scatter
     for (int b0 = 0; b0 < p.B; b0 += kPlanChunk) {
       const int nb = min(kPlanChunk, p.B - b0);
-      __syncthreads();  // the previous chunk's bounds are no longer read
-      for (int i = tid; i < nb; i += blockDim.x) {
-        int tq, Lq, tk, Lkv;
-        seq_bounds(p, b0 + i, tq, Lq, tk, Lkv);
-        bounds[i] = make_int4(tq, Lq, tk, Lkv);
+      __syncthreads();  // the previous chunk's bounds are no longer read (pass 1: the offsets are set)
+      if (pass == 0 || p.B > kPlanChunk) {  // one chunk: pass 1 reads the bounds pass 0 staged
+        for (int i = tid; i < nb; i += blockDim.x) {
+          int tq, Lq, tk, Lkv;
+          seq_bounds(p, b0 + i, tq, Lq, tk, Lkv);
+          bounds[i] = make_int4(tq, Lq, tk, Lkv);
+        }
+        __syncthreads();
       }
-      __syncthreads();
       for (int i = warp; i < nb; i += nwarps) {
         const int4 bd = bounds[i];
         for (int qt = lane; qt * kQT < bd.y; qt += 32) {
@@ -1311,7 +1313,9 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmQ, const
     e = ensure_smem(prefill_plan_kernel, (int)plan_smem);
     if (e != cudaSuccess) return e;
   }
-  e = launch_dependent(prefill_plan_kernel, 1, 1024, plan_smem, stream, p, max_key_tiles, pairs ? 2 : 1);
+  // a warp per sequence of a chunk: a short batch needs few warps (fewer to synchronise)
+  const int plan_threads = std::min(1024, std::max(128, (std::min(p.B, kPlanChunk) * 32 + 127) / 128 * 128));
+  e = launch_dependent(prefill_plan_kernel, 1, plan_threads, plan_smem, stream, p, max_key_tiles, pairs ? 2 : 1);
   if (e != cudaSuccess) return e;
   if (p.D == 64)
     e = p.dtype == kBF16 ? launch_prefill_attention<64, kBF16>(p, tmQ, tmK, tmV, num_sms, stream)
