@@ -417,7 +417,7 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "per step: q, block table and lengths host->device in one copy; out, max and sum "
                         "device->host in one copy; copies on their own streams, overlapping neighbouring "
-                        "steps' compute (inputs over 4 buffers, results over 2); each group of 4 steps one "
+                        "steps' compute (inputs over 4 buffers, results over 2); each group of 32 steps one "
                         "CUDA graph launch; KV cache resident"},
         "gpu_launches": sum(v[1] for v in kern.values()),
         "host_us_per_step": round(host_s / steps * 1e6, 2),
@@ -556,7 +556,7 @@ def run_prefill_bench(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "per step: q, k, v and cumulative lengths host->device in one copy; out, max and sum "
                         "device->host in one copy; copies on their own streams, overlapping neighbouring "
-                        "steps' compute (inputs over 4 buffers, results over 2); each group of 4 steps one "
+                        "steps' compute (inputs over 4 buffers, results over 2); each group of 32 steps one "
                         "CUDA graph launch"},
         "gpu_launches": 2 * pf_n, "device_status": status, "clocks": sampler.summary(h0, h1),
     }
