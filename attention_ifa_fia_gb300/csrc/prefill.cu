@@ -30,6 +30,9 @@
 // gcd(blockSize, 128) rows, each from its own block; rows of a key tile past the
 // sequence's keys are masked in S, and in V they are zeroed before the PV product (a
 // cache may hold anything there, NaN included, and P = 0 would not cancel a NaN).
+// The output is 16-bit, or int8 with quantScale2 / quantOffset2 (aclnnIncreFlashAttentionV3
+// parameter table): each normalised fp32 output is scaled, offset, rounded to the nearest
+// integer and saturated in the epilogue (template parameter kQuant).
 #include "decode_common.cuh"
 
 namespace fia {
@@ -313,7 +316,7 @@ __device__ __forceinline__ void umma_f16_ta_w(uint32_t d_tmem, uint32_t a_tmem, 
 // ------------------------------------------------------------------ attention
 // kBand: a band's lower edge may fall inside a key tile (pre_tokens below the longest key
 // sequence); without it the lower edge is never inside a tile and the softmax masks the
-// upper edge only.
+// upper edge only.  kQuant: int8 output.
 template <int kD, int DT, bool kBand, bool kQuant>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
