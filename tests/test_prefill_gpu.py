@@ -366,3 +366,37 @@ def test_small_cases_after_full_size_launches(F, cuda):
             out, mx, sm = run_prefill(F, dp, causal=causal, band=band)
             compare_prefill(case, out, mx, sm, ref=ref, causal=causal, band=band)
     assert F.fia_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["chunk_after_context_pair", "chunk_odd_g_bs256", "bs16_pair", "bs48_band"])
+def test_prefill_paged_keys_int8_output(F, cuda, name):
+    """The int8 output over paged keys (NaN in every pool row that holds no key): codes within
+    the tolerance band of the oracle's, and bit for bit those of the TND run on the same data."""
+    kw, bs, layout, band = PAGED_CASES[name]
+    case = W.make_prefill_case(seed=zlib.crc32(("paged_pq_" + name).encode()) % (1 << 30), **kw)
+    dp = DevicePrefill(case)
+    kp, vp, bt, lens = _paged_pool(case, bs, layout, seed=zlib.crc32(name.encode()) & 0xffff, poison=True)
+    o_ref, m_ref, s_ref = oracle_prefill(case, band=band)
+    C = case.Nq * case.D
+    rng = np.random.default_rng(zlib.crc32(("pq" + name).encode()) & 0xffff)
+    s2 = (rng.uniform(0.5, 1.5, C) * 60.0 / max(float(np.abs(o_ref).max()), 1e-3)).astype(np.float32)
+    o2 = rng.uniform(-20, 20, C).astype(np.float32)
+    c = case
+    qs, qo = torch.from_numpy(s2).cuda(), torch.from_numpy(o2).cuda()
+    out, mx, sm = F.fia_prefill(dp.q, kp, vp, dp.cu_q, None, max_seqlen_q=int(c.lengths_q.max()),
+                                max_seqlen_kv=int(c.lengths_kv.max()), num_heads=c.Nq, num_kv_heads=c.Nkv,
+                                scale=c.scale, mask=4 if band else 3, sink=dp.sink,
+                                softmax_max=torch.empty((c.T, c.Nq), dtype=torch.float32, device="cuda"),
+                                softmax_sum=torch.empty((c.T, c.Nq), dtype=torch.float32, device="cuda"),
+                                pre_tokens=band[0] if band else None, next_tokens=band[1] if band else None,
+                                block_table=bt, seq_lens_kv=lens, kv_layout=F.KV_BNBSH if layout == "bsh" else 0,
+                                quant_scale2=qs, quant_offset2=qo)
+    assert out.dtype == torch.int8
+    y, _ = OR.post_quant(o_ref.reshape(c.T, C), s2, o2)
+    check_codes(out.cpu().numpy().reshape(-1, C), y.reshape(-1, C), o_ref.reshape(-1, C), s2.astype(np.float64),
+                *OUT_TOL[c.dtype])
+    assert_close_max("softmax_max", mx.double().cpu().numpy().reshape(-1), m_ref)
+    assert_close("softmax_sum", sm.double().cpu().numpy().reshape(-1), s_ref, *SUM_TOL)
+    tnd = _run_pq(F, dp, band, s2, o2)
+    assert torch.equal(out, tnd[0])
+    assert F.fia_device_status() == 0
