@@ -184,9 +184,12 @@ def fia_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     nkv = num_kv_heads if num_kv_heads else num_heads
     if scale is None:
         scale = D ** -0.5
+    out_dtype = torch.int8 if quant_scale2 is not None else q.dtype
     if out is None:
         shape = (B, num_heads, D) if q_len <= 1 else (B, q_len, num_heads, D)
-        out = torch.empty(shape, dtype=torch.int8 if quant_scale2 is not None else q.dtype, device=q.device)
+        out = torch.empty(shape, dtype=out_dtype, device=q.device)
+    elif out.dtype != out_dtype and quant_offset2 is None:  # (an offset alone is the library's error)
+        raise ValueError(f"out must be {out_dtype} (got {out.dtype})")
     mask_stride = 0
     if atten_mask is not None:
         if atten_mask.dtype not in (torch.bool, torch.int8, torch.uint8) or not atten_mask.is_contiguous():
@@ -293,9 +296,11 @@ def fia_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q:
     nkv = num_kv_heads if num_kv_heads else num_heads
     if scale is None:
         scale = D ** -0.5
+    out_dtype = torch.int8 if quant_scale2 is not None else q.dtype
     if out is None:
-        out = torch.empty((T, num_heads, D), dtype=torch.int8 if quant_scale2 is not None else q.dtype,
-                          device=q.device)
+        out = torch.empty((T, num_heads, D), dtype=out_dtype, device=q.device)
+    elif out.dtype != out_dtype and quant_offset2 is None:  # (an offset alone is the library's error)
+        raise ValueError(f"out must be {out_dtype} (got {out.dtype})")
     q2_per_channel = 0
     if quant_scale2 is not None:
         n2 = quant_scale2.numel()

@@ -199,3 +199,25 @@ def test_prefill_ex_rejects(F, fields, kw, code):
             setattr(opts, k, v)
     assert _prefill_ex(lib, opts, **kw) == code
     assert lib.fia_last_error()
+
+
+def test_binding_checks_the_out_dtype(F):
+    """The binding refuses an out tensor whose dtype is not the one the call writes: int8 with
+    quant_scale2, the query's dtype without (checked before any pointer is passed on)."""
+    import torch
+    q = torch.zeros((3, 2, 64), dtype=torch.bfloat16)
+    cu = torch.tensor([0, 3], dtype=torch.int64)
+    with pytest.raises(ValueError):
+        F.fia_prefill(q, q, q, cu, cu, max_seqlen_q=3, max_seqlen_kv=3, num_heads=2,
+                      out=torch.empty((3, 2, 64), dtype=torch.bfloat16), quant_scale2=torch.ones(1))
+    with pytest.raises(ValueError):
+        F.fia_prefill(q, q, q, cu, cu, max_seqlen_q=3, max_seqlen_kv=3, num_heads=2,
+                      out=torch.empty((3, 2, 64), dtype=torch.int8))
+    kc = torch.zeros((2, 2, 16, 64), dtype=torch.bfloat16)
+    bt = torch.zeros((3, 1), dtype=torch.int32)
+    lens = torch.ones(3, dtype=torch.int64)
+    with pytest.raises(ValueError):
+        F.fia_decode(q, kc, kc, bt, lens, max_kv_len=16, num_heads=2,
+                     out=torch.empty((3, 2, 64), dtype=torch.bfloat16), quant_scale2=torch.ones(1))
+    with pytest.raises(ValueError):
+        F.fia_decode(q, kc, kc, bt, lens, max_kv_len=16, num_heads=2, out=torch.empty((3, 2, 64), dtype=torch.float16))
