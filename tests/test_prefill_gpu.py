@@ -1,6 +1,5 @@
 """GPU parity of fia_prefill (TND, causal varlen, tcgen05) against the oracle, and of the
 band mask of fia_prefill_ex (FusedInferAttentionScore sparseMode 4, preTokens/nextTokens)."""
-import time
 import zlib
 
 import numpy as np
@@ -341,30 +340,31 @@ def test_prefill_post_quant_ties_and_saturation_exact(F, cuda, Nq, D):
 
 
 def test_small_cases_after_full_size_launches(F, cuda):
-    """Small launches right after full-size ones, with host work in between (as a test
-    sequence has it): a full-size launch leaves every SM's tensor and shared memory holding
-    its data, and a small one that follows must read none of it (each case is checked on its
-    own against the oracle, and every row of its output is compared)."""
-    big = W.causal_prefill_tnd()
-    dpb = DevicePrefill(big)
+    """Small launches after full-size ones whose buffers were freed, with host work in between
+    (as a test sequence has it): the small case's inputs, outputs and workspace reuse the large
+    one's memory, and every SM's tensor and shared memory still holds the large launch's data;
+    the small case must read none of it (each one checked on every row against the oracle)."""
     small = [("no_mask", dict(Nq=4, Nkv=2, D=128, lengths=[77, 260]), False, None),
              ("sliding_256_pair", dict(Nq=8, Nkv=2, D=128, lengths=[700, 300, 129]), True, (255, 0)),
              ("one_tile_each", dict(Nq=4, Nkv=2, D=128, lengths=[1, 127, 128, 129]), True, None)]
+    big = W.causal_prefill_tnd()
+    rows = sample_prefill_rows(big, 256, seed=9)
     refs = {}
     for _round in range(2):
         for name, kw, causal, band in small:
-            for _ in range(3):
-                run_prefill(F, dpb)
-            torch.cuda.synchronize()
-            if name not in refs:  # host work between the large launches and the small one
+            dpb = DevicePrefill(big)
+            for _ in range(2):
+                res = run_prefill(F, dpb)
+            compare_prefill(big, *res, rows=rows)  # host work between the launches
+            del dpb, res                            # the small case may reuse this memory
+            if name not in refs:
                 case = W.make_prefill_case(seed=zlib.crc32(("after_" + name).encode()) % (1 << 30), **kw)
                 refs[name] = (case, oracle_prefill(case, causal=causal, band=band))
-            else:
-                time.sleep(0.3)
             case, ref = refs[name]
             dp = DevicePrefill(case)
             out, mx, sm = run_prefill(F, dp, causal=causal, band=band)
             compare_prefill(case, out, mx, sm, ref=ref, causal=causal, band=band)
+            del dp, out, mx, sm
     assert F.fia_device_status() == 0
 
 
